@@ -1,0 +1,588 @@
+/*
+ * Gated DeltaNet slot-pool oracle: a plain, slow, double-precision CPU
+ * restatement of the per-layer GDN step over a slot-indexed state pool.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
+ * call this file: only the tests, the smoke check and the CPU-baseline leg of
+ * the benchmark do.  It shares no code, header, table or constant with the
+ * CUDA library; the two meet only through seeded inputs generated elsewhere.
+ *
+ * Sources it follows (page title, section):
+ *  - "TokenSpeed alcanza 580 tps con Qwen3.5-397B-A17B en GPU"
+ *      §"Ciclo de vida de slots": working slot (mutable, updated in place every
+ *        decode step) and checkpoint slot (snapshot target);
+ *      §"Riesgo de correctitud: estado obsoleto": a reused slot is made safe
+ *        only by copy-on-write from a clean checkpoint or by explicit zeroing;
+ *      §"Scheduler dual": per-request mamba_pool_indices, state filled during
+ *        prefill and updated in place during decode, spec_cache of per-step
+ *        conv/SSM snapshots for speculative rollback.
+ *  - "构建面向 Agentic 推理的下一代 LLM 推理引擎" (TokenSpeed talk)
+ *      §"为什么 Agentic 推理需要新推理引擎": linear-attention state is an SSM
+ *        state plus a convolution state.
+ *  - The per-token recurrence is not written on the pages.  It follows the
+ *    published Gated DeltaNet formulation (Yang, Kautz, Hatamizadeh, "Gated
+ *    Delta Networks", ICLR 2025):  S_t = a_t (I - b_t k_t k_t^T) S_{t-1}
+ *    + b_t k_t v_t^T,  o_t = S_t^T q_t, with the gate g = -exp(A_log) *
+ *    softplus(a + dt_bias), a_t = exp(g), b_t = sigmoid(b), a width-W causal
+ *    conv1d + SiLU over the q|k|v channels and an L2 normalisation of q and
+ *    k (q additionally scaled by dk^-1/2).  The chunkwise form used only as a
+ *    cross-check follows the WY/UT representation of Yang et al.,
+ *    "Parallelizing Linear Transformers with the Delta Rule over Sequence
+ *    Length", NeurIPS 2024.
+ *
+ * Conventions (the readings taken where the pages are silent):
+ *  - state per V head is stored transposed, St[dv][dk] (row j = column j of
+ *    S), so o = St q and the update of row j uses only (k, v_j, q);
+ *  - channels are q | k | v, head-major; V head h reads QK head h / (HV/HK);
+ *  - conv state holds the last W-1 raw (pre-conv) inputs, oldest first; the
+ *    weight index W-1 multiplies the newest input; no bias;
+ *  - q_hat = q / sqrt(|q|^2 + 1e-6) / sqrt(dk), k_hat = k / sqrt(|k|^2 + 1e-6);
+ *  - slot id -1 is padding: the row is skipped and its outputs are zero; any
+ *    other id outside [0, num_slots) is skipped the same way and sets bit 1
+ *    of the error word.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_ERR_SLOT_OOB 1u
+
+typedef struct {
+  int32_t hk, hv, dk, dv, w;
+} orc_dims;
+
+typedef struct {
+  double* ssm;  /* [num_slots][hv][dv][dk] */
+  double* conv; /* [num_slots][w-1][C]     */
+  int32_t num_slots;
+} orc_pool;
+
+typedef struct {
+  const double* conv_w;  /* [C][w] */
+  const double* A_log;   /* [hv]   */
+  const double* dt_bias; /* [hv]   */
+} orc_params;
+
+static const double ORC_EPS = 1e-6;
+
+static int64_t n_chan(const orc_dims* d) {
+  return 2 * (int64_t)d->hk * d->dk + (int64_t)d->hv * d->dv;
+}
+static int64_t ssm_elems(const orc_dims* d) {
+  return (int64_t)d->hv * d->dv * d->dk;
+}
+static int64_t conv_elems(const orc_dims* d) {
+  return (int64_t)(d->w - 1) * n_chan(d);
+}
+
+/* 0 = usable slot, 1 = padding (-1), 2 = out of range */
+static int slot_class(int32_t id, int32_t num_slots) {
+  if (id == -1) return 1;
+  if (id < 0 || id >= num_slots) return 2;
+  return 0;
+}
+
+/* ---- the per-token pieces ------------------------------------------------ */
+
+double orc_silu(double y) { return y / (1.0 + exp(-y)); }
+double orc_softplus(double x) { return log1p(exp(x)); }
+double orc_sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+/* g = -exp(A_log) * softplus(a + dt_bias) */
+double orc_gate_g(double A_log, double dt_bias, double a) {
+  return -exp(A_log) * orc_softplus(a + dt_bias);
+}
+
+/* out = x / sqrt(sum x^2 + eps) * scale */
+void orc_l2norm(int32_t n, const double* x, double scale, double* out) {
+  double ss = 0.0;
+  for (int32_t i = 0; i < n; ++i) ss += x[i] * x[i];
+  double r = 1.0 / sqrt(ss + ORC_EPS);
+  for (int32_t i = 0; i < n; ++i) out[i] = x[i] * r * scale;
+}
+
+/* Causal conv1d over the window [hist[0..w-2], x] for every channel, then
+ * SiLU.  hist is [w-1][C], oldest row first. */
+void orc_conv_silu(const orc_dims* d, const double* hist, const double* x,
+                   const double* conv_w, double* y) {
+  int64_t C = n_chan(d);
+  int W = d->w;
+  for (int64_t c = 0; c < C; ++c) {
+    double acc = 0.0;
+    for (int i = 0; i < W - 1; ++i) acc += conv_w[c * W + i] * hist[i * C + c];
+    acc += conv_w[c * W + (W - 1)] * x[c];
+    y[c] = orc_silu(acc);
+  }
+}
+
+/* Shift the conv history by one token: drop the oldest, append x. */
+static void conv_shift(const orc_dims* d, double* hist, const double* x) {
+  int64_t C = n_chan(d);
+  for (int i = 0; i + 1 < d->w - 1; ++i)
+    memcpy(hist + i * C, hist + (i + 1) * C, sizeof(double) * C);
+  if (d->w > 1) memcpy(hist + (int64_t)(d->w - 2) * C, x, sizeof(double) * C);
+}
+
+/* Gated delta rule on one head, state stored transposed St[dv][dk]:
+ *   u = v - alpha * St k
+ *   St <- alpha * St + beta * u k^T
+ *   o = St q          (read out from the updated state)
+ * Equivalent to S <- alpha (I - beta k k^T) S + beta k v^T, o = S^T q. */
+void orc_delta_core(int32_t dk, int32_t dv, double* St, const double* k,
+                    const double* v, const double* q, double alpha,
+                    double beta, double* o) {
+  for (int32_t j = 0; j < dv; ++j) {
+    double* row = St + (int64_t)j * dk;
+    double sk = 0.0;
+    for (int32_t i = 0; i < dk; ++i) sk += row[i] * k[i];
+    double u = v[j] - alpha * sk;
+    for (int32_t i = 0; i < dk; ++i) row[i] = alpha * row[i] + beta * u * k[i];
+    double oj = 0.0;
+    for (int32_t i = 0; i < dk; ++i) oj += row[i] * q[i];
+    o[j] = oj;
+  }
+}
+
+/* Features of one token for every head: q_hat, k_hat per QK head, v per V
+ * head, and (alpha, beta) per V head.  y is [C] (conv + SiLU output). */
+typedef struct {
+  double* qh;    /* [hk][dk] */
+  double* kh;    /* [hk][dk] */
+  double* v;     /* [hv][dv] (points into y) */
+  double* g;     /* [hv] */
+  double* alpha; /* [hv] */
+  double* beta;  /* [hv] */
+} orc_feat;
+
+static void token_features(const orc_dims* d, const orc_params* p,
+                           const double* y, const double* a_t,
+                           const double* b_t, orc_feat* f) {
+  double qscale = 1.0 / sqrt((double)d->dk);
+  for (int h = 0; h < d->hk; ++h) {
+    orc_l2norm(d->dk, y + (int64_t)h * d->dk, qscale, f->qh + (int64_t)h * d->dk);
+    orc_l2norm(d->dk, y + (int64_t)(d->hk + h) * d->dk, 1.0,
+               f->kh + (int64_t)h * d->dk);
+  }
+  for (int h = 0; h < d->hv; ++h) {
+    f->g[h] = orc_gate_g(p->A_log[h], p->dt_bias[h], a_t[h]);
+    f->alpha[h] = exp(f->g[h]);
+    f->beta[h] = orc_sigmoid(b_t[h]);
+  }
+}
+
+/* One token on one slot (conv state and SSM state updated in place).
+ * Heads outside [h_lo, h_hi) keep their state and leave o untouched; the
+ * conv history always advances for every channel. */
+static void token_step(const orc_dims* d, const orc_params* p, double* ssm,
+                       double* conv, const double* x, const double* a_t,
+                       const double* b_t, double* o, int h_lo, int h_hi,
+                       double* work) {
+  int64_t C = n_chan(d);
+  double* y = work;
+  double* qh = y + C;
+  double* kh = qh + (int64_t)d->hk * d->dk;
+  double* g = kh + (int64_t)d->hk * d->dk;
+  double* al = g + d->hv;
+  double* be = al + d->hv;
+  orc_conv_silu(d, conv, x, p->conv_w, y);
+  conv_shift(d, conv, x);
+  orc_feat f = {qh, kh, y + 2 * (int64_t)d->hk * d->dk, g, al, be};
+  token_features(d, p, y, a_t, b_t, &f);
+  int G = d->hv / d->hk;
+  for (int h = h_lo; h < h_hi; ++h) {
+    int hq = h / G;
+    orc_delta_core(d->dk, d->dv, ssm + (int64_t)h * d->dv * d->dk,
+                   kh + (int64_t)hq * d->dk, f.v + (int64_t)h * d->dv,
+                   qh + (int64_t)hq * d->dk, al[h], be[h],
+                   o + (int64_t)h * d->dv);
+  }
+}
+
+static int64_t work_elems(const orc_dims* d) {
+  return n_chan(d) + 2 * (int64_t)d->hk * d->dk + 3 * (int64_t)d->hv;
+}
+
+static int check_dims(const orc_dims* d) {
+  if (!d || d->hk <= 0 || d->hv <= 0 || d->dk <= 0 || d->dv <= 0 || d->w < 1)
+    return 1;
+  if (d->hv % d->hk) return 1;
+  return 0;
+}
+
+static void clamp_heads(const orc_dims* d, int* h_lo, int* h_hi) {
+  if (*h_lo < 0) *h_lo = 0;
+  if (*h_hi > d->hv || *h_hi < 0) *h_hi = d->hv;
+}
+
+/* ---- a0..a6: one decode step over a batch ------------------------------- */
+/* qkv [B][C], a,b [B][hv], out [B][hv][dv].  Heads outside [h_lo,h_hi) are
+ * not advanced (sampling); pass h_lo=0, h_hi=-1 for all heads. */
+int orc_decode_step(const orc_dims* d, orc_pool pool, const orc_params* p,
+                    const int32_t* slot_ids, int32_t B, const double* qkv,
+                    const double* a, const double* b, double* out,
+                    uint32_t* err, int32_t h_lo, int32_t h_hi) {
+  if (check_dims(d)) return 1;
+  clamp_heads(d, &h_lo, &h_hi);
+  int64_t C = n_chan(d), HVDV = (int64_t)d->hv * d->dv;
+  int64_t fail = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : fail)
+  for (int32_t r = 0; r < B; ++r) {
+    int32_t s = slot_ids[r];
+    int cls = slot_class(s, pool.num_slots);
+    double* o = out + r * HVDV;
+    if (cls) {
+      if (cls == 2) fail |= ORC_ERR_SLOT_OOB;
+      for (int64_t i = 0; i < HVDV; ++i) o[i] = 0.0;
+      continue;
+    }
+    double* work = (double*)malloc(sizeof(double) * work_elems(d));
+    token_step(d, p, pool.ssm + s * ssm_elems(d), pool.conv + s * conv_elems(d),
+               qkv + r * C, a + (int64_t)r * d->hv, b + (int64_t)r * d->hv, o,
+               h_lo, h_hi, work);
+    free(work);
+  }
+  if (err) *err |= (uint32_t)fail;
+  return 0;
+}
+
+/* ---- a9 / a10: slot copy and zero ---------------------------------------- */
+int orc_slot_copy(const orc_dims* d, orc_pool src, orc_pool dst,
+                  const int32_t* src_ids, const int32_t* dst_ids, int32_t n,
+                  uint32_t* err) {
+  if (check_dims(d)) return 1;
+  int64_t ns = ssm_elems(d), nc = conv_elems(d);
+  for (int32_t i = 0; i < n; ++i) {
+    int cs = slot_class(src_ids[i], src.num_slots);
+    int cd = slot_class(dst_ids[i], dst.num_slots);
+    if (cs == 2 || cd == 2) {
+      if (err) *err |= ORC_ERR_SLOT_OOB;
+      continue;
+    }
+    if (cs || cd) continue;
+    memmove(dst.ssm + dst_ids[i] * ns, src.ssm + src_ids[i] * ns, sizeof(double) * ns);
+    memmove(dst.conv + dst_ids[i] * nc, src.conv + src_ids[i] * nc, sizeof(double) * nc);
+  }
+  return 0;
+}
+
+int orc_slot_zero(const orc_dims* d, orc_pool pool, const int32_t* ids,
+                  int32_t n, uint32_t* err) {
+  if (check_dims(d)) return 1;
+  int64_t ns = ssm_elems(d), nc = conv_elems(d);
+  for (int32_t i = 0; i < n; ++i) {
+    int c = slot_class(ids[i], pool.num_slots);
+    if (c == 2 && err) *err |= ORC_ERR_SLOT_OOB;
+    if (c) continue;
+    for (int64_t e = 0; e < ns; ++e) pool.ssm[ids[i] * ns + e] = 0.0;
+    for (int64_t e = 0; e < nc; ++e) pool.conv[ids[i] * nc + e] = 0.0;
+  }
+  return 0;
+}
+
+/* ---- a7: speculative verify ---------------------------------------------
+ * For request r, run T draft tokens from its working slot without touching
+ * the working slot; after token t the state (SSM and conv history) is written
+ * into spec slot spec_ids[r][t] (-1: not written).  qkv [B][T][C], a,b
+ * [B][T][hv], out [B][T][hv][dv]. */
+int orc_spec_verify(const orc_dims* d, orc_pool work, orc_pool spec,
+                    const orc_params* p, const int32_t* slot_ids,
+                    const int32_t* spec_ids, int32_t B, int32_t T,
+                    const double* qkv, const double* a, const double* b,
+                    double* out, uint32_t* err) {
+  if (check_dims(d)) return 1;
+  int64_t C = n_chan(d), HVDV = (int64_t)d->hv * d->dv;
+  int64_t ns = ssm_elems(d), nc = conv_elems(d);
+  int64_t fail = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : fail)
+  for (int32_t r = 0; r < B; ++r) {
+    int32_t s = slot_ids[r];
+    int cls = slot_class(s, work.num_slots);
+    if (cls) {
+      if (cls == 2) fail |= ORC_ERR_SLOT_OOB;
+      for (int64_t i = 0; i < (int64_t)T * HVDV; ++i) out[(int64_t)r * T * HVDV + i] = 0.0;
+      continue;
+    }
+    double* st = (double*)malloc(sizeof(double) * (ns + nc + work_elems(d)));
+    double* cv = st + ns;
+    double* wk = cv + nc;
+    memcpy(st, work.ssm + s * ns, sizeof(double) * ns);
+    memcpy(cv, work.conv + s * nc, sizeof(double) * nc);
+    for (int32_t t = 0; t < T; ++t) {
+      int64_t rt = (int64_t)r * T + t;
+      token_step(d, p, st, cv, qkv + rt * C, a + rt * d->hv, b + rt * d->hv,
+                 out + rt * HVDV, 0, d->hv, wk);
+      int32_t sid = spec_ids[rt];
+      int sc = slot_class(sid, spec.num_slots);
+      if (sc == 2) fail |= ORC_ERR_SLOT_OOB;
+      if (sc) continue;
+      memcpy(spec.ssm + sid * ns, st, sizeof(double) * ns);
+      memcpy(spec.conv + sid * nc, cv, sizeof(double) * nc);
+    }
+    free(st);
+  }
+  if (err) *err |= (uint32_t)fail;
+  return 0;
+}
+
+/* ---- a7': commit the accepted snapshot ----------------------------------
+ * accept_len[r] = L in 0..T.  L >= 1 copies spec slot spec_ids[r][L-1] into
+ * the working slot slot_ids[r]; L = 0 keeps the working slot (it already is
+ * the rollback state).  L outside 0..T is out of range (error bit, skip). */
+int orc_spec_commit(const orc_dims* d, orc_pool spec, orc_pool work,
+                    const int32_t* spec_ids, const int32_t* accept_len,
+                    const int32_t* slot_ids, int32_t B, int32_t T,
+                    uint32_t* err) {
+  if (check_dims(d)) return 1;
+  for (int32_t r = 0; r < B; ++r) {
+    int32_t L = accept_len[r];
+    if (L < 0 || L > T) {
+      if (err) *err |= ORC_ERR_SLOT_OOB;
+      continue;
+    }
+    if (L == 0) continue;
+    int32_t src = spec_ids[(int64_t)r * T + (L - 1)];
+    int32_t dst = slot_ids[r];
+    orc_slot_copy(d, spec, work, &src, &dst, 1, err);
+  }
+  return 0;
+}
+
+/* ---- a8: prefill, token by token (the plain definition) -----------------
+ * Sequence n owns tokens [cu_seqlens[n], cu_seqlens[n+1]) of qkv [Ttot][C]
+ * (a,b [Ttot][hv], out [Ttot][hv][dv]); its first token sits at absolute
+ * position start_pos[n] and its state lives in slot slot_ids[n].  After the
+ * token at absolute position P-1, for every P with P % ckpt_block == 0 and
+ * start_pos < P <= end, the slot's state (SSM + conv history) is copied to
+ * checkpoint slot ckpt_ids[n][P/ckpt_block - floor(start_pos/ckpt_block) - 1]
+ * (entry -1: skipped; index beyond max_ckpt: skipped).  Heads outside
+ * [h_lo,h_hi) are not advanced (sampling). */
+int orc_prefill(const orc_dims* d, orc_pool pool, orc_pool ckpt,
+                const orc_params* p, const int32_t* slot_ids,
+                const int32_t* cu_seqlens, const int64_t* start_pos,
+                int32_t n_seq, const int32_t* ckpt_ids, int32_t max_ckpt,
+                int32_t ckpt_block, const double* qkv, const double* a,
+                const double* b, double* out, uint32_t* err, int32_t h_lo,
+                int32_t h_hi) {
+  if (check_dims(d) || ckpt_block <= 0) return 1;
+  clamp_heads(d, &h_lo, &h_hi);
+  int64_t C = n_chan(d), HVDV = (int64_t)d->hv * d->dv;
+  int64_t ns = ssm_elems(d), nc = conv_elems(d);
+  int64_t fail = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : fail)
+  for (int32_t n = 0; n < n_seq; ++n) {
+    int32_t s = slot_ids[n];
+    int64_t t0 = cu_seqlens[n], t1 = cu_seqlens[n + 1];
+    int cls = slot_class(s, pool.num_slots);
+    if (cls) {
+      if (cls == 2) fail |= ORC_ERR_SLOT_OOB;
+      for (int64_t i = t0 * HVDV; i < t1 * HVDV; ++i) out[i] = 0.0;
+      continue;
+    }
+    double* ssm = pool.ssm + s * ns;
+    double* conv = pool.conv + s * nc;
+    double* wk = (double*)malloc(sizeof(double) * work_elems(d));
+    int64_t p0 = start_pos[n];
+    int64_t blk0 = p0 / ckpt_block;
+    for (int64_t i = t0; i < t1; ++i) {
+      int64_t pos = p0 + (i - t0);
+      token_step(d, p, ssm, conv, qkv + i * C, a + i * d->hv, b + i * d->hv,
+                 out + i * HVDV, h_lo, h_hi, wk);
+      int64_t P = pos + 1;
+      if (P % ckpt_block) continue;
+      int64_t idx = P / ckpt_block - blk0 - 1;
+      if (idx < 0 || idx >= max_ckpt) continue;
+      int32_t cid = ckpt_ids[(int64_t)n * max_ckpt + idx];
+      int cc = slot_class(cid, ckpt.num_slots);
+      if (cc == 2) fail |= ORC_ERR_SLOT_OOB;
+      if (cc) continue;
+      memcpy(ckpt.ssm + cid * ns, ssm, sizeof(double) * ns);
+      memcpy(ckpt.conv + cid * nc, conv, sizeof(double) * nc);
+    }
+    free(wk);
+  }
+  if (err) *err |= (uint32_t)fail;
+  return 0;
+}
+
+/* ---- a8 cross-check: the chunkwise WY/UT form (double) -------------------
+ * Same contract as orc_prefill, but the state recurrence is evaluated one
+ * chunk of `chunk` tokens at a time, chunks aligned to absolute positions
+ * (multiples of `chunk`).  For a chunk with rows i (tokens), local cumulative
+ * log-decay b_i = sum_{j<=i} g_j and Gamma_ij = exp(b_i - b_j) (i >= j):
+ *   A = strict_lower(diag(beta) (K K^T (.) Gamma))
+ *   T = (I + A)^{-1} diag(beta)          (forward substitution)
+ *   W = T diag(e^b) K,   U = T V,   Delta = U - W S0
+ *   O = diag(e^b) Q S0 + (Q K^T (.) Gamma (.) lower_incl_diag) Delta
+ *   S_end = e^{b_last} S0 + (diag(e^{b_last - b}) K)^T Delta
+ * with S = dk x dv.  ckpt_block must be a multiple of chunk. */
+int orc_prefill_chunked(const orc_dims* d, orc_pool pool, orc_pool ckpt,
+                        const orc_params* p, const int32_t* slot_ids,
+                        const int32_t* cu_seqlens, const int64_t* start_pos,
+                        int32_t n_seq, const int32_t* ckpt_ids,
+                        int32_t max_ckpt, int32_t ckpt_block, int32_t chunk,
+                        const double* qkv, const double* a, const double* b,
+                        double* out, uint32_t* err) {
+  if (check_dims(d) || ckpt_block <= 0 || chunk <= 0 || ckpt_block % chunk) return 1;
+  int64_t C = n_chan(d), HVDV = (int64_t)d->hv * d->dv;
+  int64_t ns = ssm_elems(d), nc = conv_elems(d);
+  int dk = d->dk, dv = d->dv, G = d->hv / d->hk;
+  int64_t fail = 0;
+  for (int32_t n = 0; n < n_seq; ++n) {
+    int32_t s = slot_ids[n];
+    int64_t t0 = cu_seqlens[n], t1 = cu_seqlens[n + 1], L = t1 - t0;
+    int cls = slot_class(s, pool.num_slots);
+    if (cls) {
+      if (cls == 2) fail |= ORC_ERR_SLOT_OOB;
+      for (int64_t i = t0 * HVDV; i < t1 * HVDV; ++i) out[i] = 0.0;
+      continue;
+    }
+    int64_t p0 = start_pos[n], blk0 = p0 / ckpt_block;
+    /* per-token features, and the conv history at every chunk boundary */
+    double* feat_q = (double*)malloc(sizeof(double) * (L + 1) * d->hk * dk);
+    double* feat_k = (double*)malloc(sizeof(double) * (L + 1) * d->hk * dk);
+    double* feat_v = (double*)malloc(sizeof(double) * (L + 1) * d->hv * dv);
+    double* feat_g = (double*)malloc(sizeof(double) * (L + 1) * d->hv);
+    double* feat_b = (double*)malloc(sizeof(double) * (L + 1) * d->hv);
+    double* hist_at = (double*)malloc(sizeof(double) * (L + 1) * nc); /* history before token i */
+    double* conv = pool.conv + s * nc;
+    double* y = (double*)malloc(sizeof(double) * C);
+    double* alpha_tmp = (double*)malloc(sizeof(double) * d->hv);
+    for (int64_t i = 0; i < L; ++i) {
+      memcpy(hist_at + i * nc, conv, sizeof(double) * nc);
+      const double* x = qkv + (t0 + i) * C;
+      orc_conv_silu(d, conv, x, p->conv_w, y);
+      conv_shift(d, conv, x);
+      orc_feat f = {feat_q + i * d->hk * dk, feat_k + i * d->hk * dk, NULL,
+                    feat_g + i * d->hv, alpha_tmp, feat_b + i * d->hv};
+      token_features(d, p, y, a + (t0 + i) * d->hv, b + (t0 + i) * d->hv, &f);
+      memcpy(feat_v + i * d->hv * dv, y + 2 * (int64_t)d->hk * dk, sizeof(double) * d->hv * dv);
+    }
+    memcpy(hist_at + L * nc, conv, sizeof(double) * nc);
+
+    int64_t maxc = chunk;
+    double* S = (double*)malloc(sizeof(double) * dk * dv);     /* S[m][j] */
+    double* bcum = (double*)malloc(sizeof(double) * maxc);
+    double* A = (double*)malloc(sizeof(double) * maxc * maxc);
+    double* Tm = (double*)malloc(sizeof(double) * maxc * maxc);
+    double* Wm = (double*)malloc(sizeof(double) * maxc * dk);
+    double* Um = (double*)malloc(sizeof(double) * maxc * dv);
+    double* Dm = (double*)malloc(sizeof(double) * maxc * dv);
+    double* Snew = (double*)malloc(sizeof(double) * dk * dv);
+
+    for (int h = 0; h < d->hv; ++h) {
+      int hq = h / G;
+      double* St = pool.ssm + s * ns + (int64_t)h * dv * dk;
+      for (int m = 0; m < dk; ++m)
+        for (int j = 0; j < dv; ++j) S[m * dv + j] = St[(int64_t)j * dk + m];
+      int64_t i = 0;
+      while (i < L) {
+        int64_t pos = p0 + i;
+        int64_t cend = (pos / chunk + 1) * chunk; /* absolute end of this chunk */
+        int64_t n_r = cend - pos;
+        if (n_r > L - i) n_r = L - i;
+#define KR(r) (feat_k + (i + (r)) * d->hk * dk + (int64_t)hq * dk)
+#define QR(r) (feat_q + (i + (r)) * d->hk * dk + (int64_t)hq * dk)
+#define VR(r) (feat_v + (i + (r)) * d->hv * dv + (int64_t)h * dv)
+        double acc = 0.0;
+        for (int64_t r = 0; r < n_r; ++r) {
+          acc += feat_g[(i + r) * d->hv + h];
+          bcum[r] = acc;
+        }
+        for (int64_t r = 0; r < n_r; ++r)
+          for (int64_t c = 0; c < n_r; ++c) {
+            double v = 0.0;
+            if (c < r) {
+              double kk = 0.0;
+              for (int m = 0; m < dk; ++m) kk += KR(r)[m] * KR(c)[m];
+              v = feat_b[(i + r) * d->hv + h] * kk * exp(bcum[r] - bcum[c]);
+            }
+            A[r * n_r + c] = v;
+          }
+        /* (I + A) T = diag(beta), row by row */
+        for (int64_t r = 0; r < n_r; ++r)
+          for (int64_t c = 0; c < n_r; ++c) {
+            double v = (r == c) ? feat_b[(i + r) * d->hv + h] : 0.0;
+            for (int64_t m = 0; m < r; ++m) v -= A[r * n_r + m] * Tm[m * n_r + c];
+            Tm[r * n_r + c] = v;
+          }
+        for (int64_t r = 0; r < n_r; ++r) {
+          for (int m = 0; m < dk; ++m) {
+            double v = 0.0;
+            for (int64_t c = 0; c < n_r; ++c) v += Tm[r * n_r + c] * exp(bcum[c]) * KR(c)[m];
+            Wm[r * dk + m] = v;
+          }
+          for (int j = 0; j < dv; ++j) {
+            double v = 0.0;
+            for (int64_t c = 0; c < n_r; ++c) v += Tm[r * n_r + c] * VR(c)[j];
+            Um[r * dv + j] = v;
+          }
+        }
+        for (int64_t r = 0; r < n_r; ++r)
+          for (int j = 0; j < dv; ++j) {
+            double ws = 0.0;
+            for (int m = 0; m < dk; ++m) ws += Wm[r * dk + m] * S[m * dv + j];
+            Dm[r * dv + j] = Um[r * dv + j] - ws;
+          }
+        for (int64_t r = 0; r < n_r; ++r) {
+          double* o = out + (t0 + i + r) * HVDV + (int64_t)h * dv;
+          for (int j = 0; j < dv; ++j) {
+            double qs = 0.0;
+            for (int m = 0; m < dk; ++m) qs += QR(r)[m] * S[m * dv + j];
+            double v = exp(bcum[r]) * qs;
+            for (int64_t c = 0; c <= r; ++c) {
+              double qk = 0.0;
+              for (int m = 0; m < dk; ++m) qk += QR(r)[m] * KR(c)[m];
+              v += qk * exp(bcum[r] - bcum[c]) * Dm[c * dv + j];
+            }
+            o[j] = v;
+          }
+        }
+        double blast = bcum[n_r - 1];
+        for (int m = 0; m < dk; ++m)
+          for (int j = 0; j < dv; ++j) {
+            double v = exp(blast) * S[m * dv + j];
+            for (int64_t c = 0; c < n_r; ++c)
+              v += exp(blast - bcum[c]) * KR(c)[m] * Dm[c * dv + j];
+            Snew[m * dv + j] = v;
+          }
+        memcpy(S, Snew, sizeof(double) * dk * dv);
+#undef KR
+#undef QR
+#undef VR
+        i += n_r;
+        int64_t P = p0 + i;
+        if (P % ckpt_block == 0) {
+          int64_t idx = P / ckpt_block - blk0 - 1;
+          if (idx >= 0 && idx < max_ckpt) {
+            int32_t cid = ckpt_ids[(int64_t)n * max_ckpt + idx];
+            int cc = slot_class(cid, ckpt.num_slots);
+            if (cc == 2) fail |= ORC_ERR_SLOT_OOB;
+            if (!cc) {
+              double* Ct = ckpt.ssm + cid * ns + (int64_t)h * dv * dk;
+              for (int m = 0; m < dk; ++m)
+                for (int j = 0; j < dv; ++j) Ct[(int64_t)j * dk + m] = S[m * dv + j];
+              if (h == 0) memcpy(ckpt.conv + cid * nc, hist_at + i * nc, sizeof(double) * nc);
+            }
+          }
+        }
+      }
+      for (int m = 0; m < dk; ++m)
+        for (int j = 0; j < dv; ++j) St[(int64_t)j * dk + m] = S[m * dv + j];
+    }
+    free(S); free(bcum); free(A); free(Tm); free(Wm); free(Um); free(Dm); free(Snew);
+    free(feat_q); free(feat_k); free(feat_v); free(feat_g); free(feat_b);
+    free(hist_at); free(y); free(alpha_tmp);
+  }
+  if (err) *err |= (uint32_t)fail;
+  return 0;
+}
+
+int orc_num_threads(void) {
+#ifdef _OPENMP
+  extern int omp_get_max_threads(void);
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
