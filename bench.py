@@ -1,0 +1,471 @@
+#!/usr/bin/env python3
+"""Benchmark: GDN decode tokens/s per layer and achieved HBM GB/s on one GB300.
+
+Headline workload: the Qwen3.5-shaped GDN layer (16 QK heads, 32 V heads,
+dk = dv = 128, conv width 4 over 8192 channels, bf16 activations and conv
+history, fp32 state), batch 64, over a 512-slot pool.  One step = one
+gdn_decode_step launch (conv1d update + SiLU + L2 norm + gates + gated delta
+rule + readout for 64 requests).  Consecutive steps rotate over 8 disjoint
+64-slot sets of the pool, so the state touched between two visits of a slot
+(1.1 GB) is far larger than the 129 MB L2: every step streams its state from
+HBM.
+
+The other hot-path rows (batch sweep, speculative verify + commit, chunked
+prefill, slot copy / zero) are timed after the headline and reported under
+"rows"; they are not part of the headline number.
+
+`--impl reference` times the CPU oracle (the reference arm of this build).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN decode tokens/s per layer & achieved HBM GB/s (% of roofline), 1×GB300"
+UNIT = "tokens/s"
+B_HEAD = 64
+SETS = 8
+POOL = 512
+
+# bytes per decode token, Qwen3.5-shaped layer (bf16 activations / history):
+#   state 2 x 32 x 128 x 128 x 4, conv history 2 x 3 x 8192 x 2, qkv 8192 x 2,
+#   a and b 2 x 32 x 2, out 32 x 128 x 2, slot id 4
+DECODE_TOKEN_BYTES = 2 * 2097152 + 2 * 49152 + 16384 + 128 + 8192 + 4
+DECODE_STEP_PARAM_BYTES = 8192 * 4 * 4 + 2 * 32 * 4
+
+# ncu DRAM traffic (read + write bytes per launch) of the decode kernel, with
+# the sha256 of the kernel source it was captured on; reported only while the
+# source is unchanged.
+DECODE_TRAFFIC = {"bytes_per_launch": None, "source_sha256": None, "case": None}
+
+
+def _sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), d.get(
+            "bf16_tflops_sustained", 1700.0), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled in the background."""
+
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self, t_lo: float, t_hi: float):
+        """Summary of the samples taken between wall times t_lo and t_hi."""
+        import datetime
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        lines = self.file.read().splitlines()
+        os.unlink(self.file.name)
+        win = []
+        for ln in lines:
+            r = [x.strip() for x in ln.split(",")]
+            if len(r) < 10:
+                continue
+            try:
+                ts = datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                sm, mx = float(r[2]), float(r[3])
+            except ValueError:
+                continue
+            if t_lo - 0.15 <= ts <= t_hi + 0.15:
+                win.append((sm, mx, r[6:10]))
+        reasons = sorted({n for _, _, rs in win for n, v in zip(self.REASONS, rs)
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(w[0] for w in win) if win else None,
+                "sm_max_mhz": max(w[1] for w in win) if win else None,
+                "reasons": reasons, "samples": len(win)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# --------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The oracle on the host cores, same metric and workload, bounded sample."""
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from hybrid_linear_attention_gdn_gb300 import synth
+    shape = synth.QWEN
+    g = synth.generator(1)
+    conv_w, A_log, dt_bias = synth.params(shape, g)
+    sample_b = 8  # requests per reference step (a bounded sample of the 64)
+    ssm, conv = synth.pool(shape, g, sample_b)
+    od = oracle.Dims(shape.hk, shape.hv, shape.dk, shape.dv, shape.w)
+    op = oracle.Params(conv_w.double().numpy(), A_log.double().numpy(), dt_bias.double().numpy())
+    pool = oracle.Pool(ssm.double().numpy(), conv.double().numpy())
+    ids = np.arange(sample_b, dtype=np.int32)
+    qkv, a, b = synth.tokens(shape, g, (sample_b,))
+    qkv, a, b = (t.double().numpy() for t in (qkv, a, b))
+    for _ in range(args.warmup):
+        oracle.decode_step(od, pool, op, ids, qkv, a, b)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.decode_step(od, pool, op, ids, qkv, a, b)
+    dt = time.perf_counter() - t0
+    value = sample_b * args.steps / dt
+    cores = oracle.num_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "qwen35_gdn_decode_h16x32_d128", "batch": sample_b,
+                   "note": "CPU oracle (double precision); each step a bounded sample of "
+                           "8 of the 64 requests"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{sample_b} requests x {args.steps} decode steps"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------- our arm
+
+def _events_time(fn, reps, stream):
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(reps):
+        fn(i)
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / reps  # ms
+
+
+def _cpu_baseline(budget_s=12.0):
+    """The oracle as it stands, on the host cores, on a bounded sample."""
+    import numpy as np
+    import oracle
+    from hybrid_linear_attention_gdn_gb300 import synth
+    shape = synth.QWEN
+    g = synth.generator(7)
+    conv_w, A_log, dt_bias = synth.params(shape, g)
+    B = B_HEAD
+    ssm, conv = synth.pool(shape, g, B)
+    od = oracle.Dims(shape.hk, shape.hv, shape.dk, shape.dv, shape.w)
+    op = oracle.Params(conv_w.double().numpy(), A_log.double().numpy(), dt_bias.double().numpy())
+    pool = oracle.Pool(ssm.double().numpy(), conv.double().numpy())
+    ids = np.arange(B, dtype=np.int32)
+    qkv, a, b = (t.double().numpy() for t in synth.tokens(shape, g, (B,)))
+    oracle.decode_step(od, pool, op, ids, qkv, a, b)  # warm
+    steps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.decode_step(od, pool, op, ids, qkv, a, b)
+        steps += 1
+        dt = time.perf_counter() - t0
+        if dt > budget_s or steps >= 200:
+            break
+    return {"value": B * steps / dt, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{steps} decode steps of the batch-64 workload ({B * steps} tokens), "
+                      f"{dt:.1f} s"}
+
+
+def run_ours(args):
+    import torch
+    import hybrid_linear_attention_gdn_gb300 as gdn
+    from hybrid_linear_attention_gdn_gb300 import synth
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    gdn.load()
+    hbm_peak, bf16_peak, bf16_sust, peak_src = _peaks()
+    shape = synth.QWEN
+    dims = gdn.Dims.of(shape)
+    g = synth.generator(1000 + rank)
+    conv_w, A_log, dt_bias = synth.params(shape, g)
+    params = gdn.LayerParams(conv_w.to(dev), A_log.to(dev), dt_bias.to(dev))
+    ssm, conv = synth.pool(shape, g, POOL)
+    pool = gdn.StatePool(ssm.to(dev), conv.to(dev))
+    del ssm, conv
+    perm = torch.randperm(POOL, generator=g).to(torch.int32)
+    id_sets = [perm[k * B_HEAD:(k + 1) * B_HEAD].to(dev) for k in range(SETS)]
+    inputs = [tuple(t.to(dev) for t in synth.tokens(shape, g, (B_HEAD,))) for _ in range(SETS)]
+    out = torch.empty((B_HEAD, shape.hv, shape.dv), dtype=shape.act_dtype, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        q, a, b = inputs[i % SETS]
+        gdn.decode_step(dims, pool, params, id_sets[i % SETS], q, a, b, out)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    # make sure the clock sampler sees a loaded window even for short runs
+    t_soak = time.time()
+    while time.time() - t_soak < 1.0:
+        for i in range(200):
+            step(i)
+        torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    n0 = sum(gdn.launch_counts())
+    t_lo = time.time()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    t_hi = time.time()
+    launches = sum(gdn.launch_counts()) - n0
+    ms = e0.elapsed_time(e1)
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    clocks = sampler.stop(min(t_soak, t_lo), t_hi)
+    ms_step = ms / args.steps
+    tok_s = ws * B_HEAD * args.steps / (ms * 1e-3)
+    step_bytes = B_HEAD * DECODE_TOKEN_BYTES + DECODE_STEP_PARAM_BYTES
+    achieved = step_bytes / (ms_step * 1e-3) / 1e9
+    src = os.path.join(ROOT, "hybrid_linear_attention_gdn_gb300", "csrc", "decode.cu")
+    traffic = DECODE_TRAFFIC["bytes_per_launch"] if DECODE_TRAFFIC["source_sha256"] == _sha(src) else None
+
+    # ---- end to end through the public API with host buffers
+    pin = [tuple(t.cpu().pin_memory() for t in inp) for inp in inputs]
+    pin_ids = [ids.cpu().pin_memory() for ids in id_sets]
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    d_q = torch.empty_like(inputs[0][0])
+    d_a = torch.empty_like(inputs[0][1])
+    d_b = torch.empty_like(inputs[0][2])
+    d_ids = torch.empty_like(id_sets[0])
+    h2d = sum(t.numel() * t.element_size() for t in pin[0]) + pin_ids[0].numel() * 4
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step(i):
+        q, a, b = pin[i % SETS]
+        d_q.copy_(q, non_blocking=True)
+        d_a.copy_(a, non_blocking=True)
+        d_b.copy_(b, non_blocking=True)
+        d_ids.copy_(pin_ids[i % SETS], non_blocking=True)
+        gdn.decode_step(dims, pool, params, d_ids, d_q, d_a, d_b, out)
+        out_host.copy_(out, non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    if ws > 1:
+        torch.distributed.barrier()
+    e2e_ms = _events_time(e2e_step, args.steps, stream)
+    if ws > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": ws * B_HEAD / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h}
+
+    rows = {} if args.no_rows else measure_rows(gdn, synth, dev, stream, hbm_peak, bf16_peak)
+
+    if rank != 0:
+        return
+    cpu = None if (ws > 1 or args.no_cpu) else _cpu_baseline()
+    line = {
+        "metric": METRIC, "value": tok_s, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "qwen35_gdn_decode_b64_h16x32_d128_pool512",
+                   "batch": B_HEAD, "pool_slots": POOL,
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "l2": "inputs larger than L2: steps rotate over 8 disjoint 64-slot sets "
+                         "(1.1 GB of state between visits of a slot)",
+                   "activations": "bf16", "state": "fp32"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": traffic,
+                     "kernel": "decode_kernel<128,4,bf16,bf16>",
+                     "algorithmic_bytes_per_launch": step_bytes, "peak_source": peak_src},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
+        "rows": rows,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def measure_rows(gdn, synth, dev, stream, hbm_peak, bf16_peak):
+    """Every other row of the hot path, timed with CUDA events (not headline)."""
+    import torch
+    shape = synth.QWEN
+    dims = gdn.Dims.of(shape)
+    g = synth.generator(77)
+    conv_w, A_log, dt_bias = synth.params(shape, g)
+    params = gdn.LayerParams(conv_w.to(dev), A_log.to(dev), dt_bias.to(dev))
+    ssm, conv = synth.pool(shape, g, POOL)
+    pool = gdn.StatePool(ssm.to(dev), conv.to(dev))
+    del ssm, conv
+    rows = {}
+    reps = 50
+
+    def frac(nbytes, ms):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        return {"ms": ms, "algorithmic_GBps": gbs, "frac_hbm": gbs / hbm_peak}
+
+    # batch sweep (state rotates over POOL // B disjoint sets where possible)
+    sweep = {}
+    for B in [1, 2, 4, 8, 16, 32, 64, 128, 256]:
+        nsets = max(1, min(8, POOL // B))
+        perm = torch.randperm(POOL, generator=g).to(torch.int32)
+        sets = [perm[k * B:(k + 1) * B].to(dev) for k in range(nsets)]
+        inp = [tuple(t.to(dev) for t in synth.tokens(shape, g, (B,))) for _ in range(nsets)]
+        out = torch.empty((B, 32, 128), dtype=torch.bfloat16, device=dev)
+
+        def f(i, sets=sets, inp=inp, out=out):
+            q, a, b = inp[i % len(sets)]
+            gdn.decode_step(dims, pool, params, sets[i % len(sets)], q, a, b, out)
+        for i in range(10):
+            f(i)
+        ms = _events_time(f, reps, stream)
+        r = frac(B * DECODE_TOKEN_BYTES + DECODE_STEP_PARAM_BYTES, ms)
+        r["tokens_per_s"] = B / (ms * 1e-3)
+        sweep[str(B)] = r
+    rows["decode_sweep"] = sweep
+
+    slot_bytes = 2097152 + 49152
+    perm = torch.randperm(POOL, generator=g).to(torch.int32)
+    pair_sets = [(perm[k * 128:k * 128 + 64].to(dev), perm[k * 128 + 64:(k + 1) * 128].to(dev))
+                 for k in range(4)]
+
+    def fc(i):
+        s, d = pair_sets[i % 4]
+        gdn.slot_copy(dims, pool, pool, s, d)
+    fc(0)
+    rows["slot_copy_64"] = frac(64 * 2 * slot_bytes, _events_time(fc, reps, stream))
+
+    def fz(i):
+        gdn.slot_zero(dims, pool, pair_sets[i % 4][1])
+    fz(0)
+    rows["slot_zero_64"] = frac(64 * slot_bytes, _events_time(fz, reps, stream))
+
+    # speculative verify, batch 16, T = 8, spec cache of 16 x 8 slots, then commit
+    B, T = 16, 8
+    spec = gdn.StatePool.empty(dims, 4 * B * T, dev)
+    spec_sets = [torch.arange(k * B * T, (k + 1) * B * T, dtype=torch.int32, device=dev).reshape(B, T)
+                 for k in range(4)]
+    work_sets = [perm[k * B:(k + 1) * B].to(dev) for k in range(4)]
+    vin = [tuple(t.to(dev) for t in synth.tokens(shape, g, (B, T))) for _ in range(4)]
+    vout = torch.empty((B, T, 32, 128), dtype=torch.bfloat16, device=dev)
+    L = synth.accept_lengths(B, T, g).to(dev)
+
+    def fv(i):
+        q, a, b = vin[i % 4]
+        gdn.spec_verify(dims, pool, spec, params, work_sets[i % 4], spec_sets[i % 4], q, a, b, vout)
+    fv(0)
+    vbytes = B * (slot_bytes + T * (16384 + 128) + T * slot_bytes + T * 8192)
+    r = frac(vbytes, _events_time(fv, reps, stream))
+    r["draft_tokens_per_s"] = B * T / (r["ms"] * 1e-3)
+    rows["spec_verify_b16_t8"] = r
+
+    def fm(i):
+        gdn.spec_commit(dims, spec, pool, spec_sets[i % 4], L, work_sets[i % 4])
+    fm(0)
+    rows["spec_commit_b16"] = frac(B * 2 * slot_bytes, _events_time(fm, reps, stream))
+
+    # chunked prefill: 4 sequences x 8192 tokens, checkpoints every 256
+    n_seq, S = 4, 8192
+    total = n_seq * S
+    qkv, a, b = (t.to(dev) for t in synth.tokens(shape, g, (total,)))
+    cu = torch.arange(0, total + 1, S, dtype=torch.int32, device=dev)
+    sp = torch.zeros(n_seq, dtype=torch.int64, device=dev)
+    ck = gdn.StatePool.empty(dims, 128, dev)
+    ck_ids = torch.arange(128, dtype=torch.int32, device=dev).reshape(4, 32)
+    pout = torch.empty((total, 32, 128), dtype=torch.bfloat16, device=dev)
+    wsb = gdn.chunk_prefill_workspace_size(dims, n_seq, total)
+    wsp = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    pids = [perm[k * 4:(k + 1) * 4].to(dev) for k in range(4)]
+
+    def fp(i):
+        gdn.chunk_prefill(dims, pool, ck, params, pids[i % 4], cu, sp, total, ck_ids, 256, qkv, a,
+                          b, pout, wsp)
+    fp(0)
+    pms = _events_time(fp, 5, stream)
+    pbytes = total * (16384 + 128 + 8192) + (128 + 8) * slot_bytes
+    pflop = 1.92e11
+    rows["chunk_prefill_4x8192"] = {
+        "ms": pms, "tokens_per_s": total / (pms * 1e-3),
+        "algorithmic_GBps": pbytes / (pms * 1e-3) / 1e9,
+        "frac_hbm": pbytes / (pms * 1e-3) / 1e9 / hbm_peak,
+        "TFLOPs": pflop / (pms * 1e-3) / 1e12,
+        "frac_bf16_peak": pflop / (pms * 1e-3) / 1e12 / bf16_peak,
+        "workspace_bytes": wsb}
+    del qkv, a, b, pout, wsp
+    torch.cuda.synchronize()
+    return rows
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-rows", action="store_true", help="headline only")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

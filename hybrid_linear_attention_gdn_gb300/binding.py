@@ -1,0 +1,261 @@
+"""Thin ctypes binding over libgdn.so (argument marshalling only).
+
+Each function has the name of the C entry point it wraps, minus the ``gdn_``
+prefix, takes torch tensors, passes their ``data_ptr()`` and the current CUDA
+stream, and raises :class:`GdnError` on a non-OK status.  All arithmetic runs
+in the library's kernels; there is no fallback: if the library is missing the
+first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+
+import torch
+
+from . import _build
+
+F32, BF16 = 0, 1
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA = 0, 1, 2, 3
+DEV_ERR_SLOT_OOB, DEV_ERR_TIMEOUT, DEV_ERR_SEQLENS = 1, 2, 4
+K_DECODE, K_SPEC_VERIFY, K_SLOT_COPY, K_SLOT_ZERO, K_SPEC_COMMIT, K_PREFILL = range(6)
+K_COUNT = 8
+
+_DT_CODE = {torch.float32: F32, torch.bfloat16: BF16}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class GdnError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn} failed: {msg} ({status})")
+        self.status = status
+
+
+class CDims(ctypes.Structure):
+    _fields_ = [("hk", ctypes.c_int32), ("hv", ctypes.c_int32), ("dk", ctypes.c_int32),
+                ("dv", ctypes.c_int32), ("conv_width", ctypes.c_int32),
+                ("act_dtype", ctypes.c_int32), ("conv_dtype", ctypes.c_int32)]
+
+
+class CPool(ctypes.Structure):
+    _fields_ = [("ssm", ctypes.c_void_p), ("conv", ctypes.c_void_p),
+                ("num_slots", ctypes.c_int32)]
+
+
+class CParams(ctypes.Structure):
+    _fields_ = [("conv_w", ctypes.c_void_p), ("A_log", ctypes.c_void_p),
+                ("dt_bias", ctypes.c_void_p)]
+
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_PD = ctypes.POINTER(CDims)
+_PP = ctypes.POINTER(CParams)
+
+EXPORTS = {
+    "gdn_decode_step": ([_PD, CPool, _PP, _P, _I32, _P, _P, _P, _P, _P, _P], _I32),
+    "gdn_spec_verify": ([_PD, CPool, CPool, _PP, _P, _P, _I32, _I32, _P, _P, _P, _P, _P, _P], _I32),
+    "gdn_spec_commit": ([_PD, CPool, CPool, _P, _P, _P, _I32, _I32, _P, _P], _I32),
+    "gdn_chunk_prefill_workspace_size": ([_PD, _I32, _I64], ctypes.c_size_t),
+    "gdn_chunk_prefill": ([_PD, CPool, CPool, _PP, _P, _P, _P, _I32, _I64, _P, _I32, _I32,
+                           _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P], _I32),
+    "gdn_slot_copy": ([_PD, CPool, CPool, _P, _P, _I32, _P, _P], _I32),
+    "gdn_slot_zero": ([_PD, CPool, _P, _I32, _P, _P], _I32),
+    "gdn_status_string": ([_I32], ctypes.c_char_p),
+    "gdn_launch_count": ([_I32], ctypes.c_uint64),
+    "gdn_launch_count_reset": ([], None),
+}
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load libgdn.so (optionally building it first).  Raises if absent."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if build_if_missing:
+                _build.build()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"libgdn.so not found at {path}: build it with "
+                    "`python -c 'import __graft_entry__ as g; g.build()'`")
+            lib = ctypes.CDLL(path)
+            for name, (argtypes, restype) in EXPORTS.items():
+                fn = getattr(lib, name)
+                fn.argtypes = argtypes
+                fn.restype = restype
+            _lib = lib
+    return _lib
+
+
+def _check(fn: str, status: int):
+    if status != OK:
+        msg = load().gdn_status_string(status).decode()
+        raise GdnError(fn, status, msg)
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+# ---------------------------------------------------------------- structures
+
+@dataclass(frozen=True)
+class Dims:
+    hk: int
+    hv: int
+    dk: int
+    dv: int
+    conv_width: int
+    act_dtype: torch.dtype
+    conv_dtype: torch.dtype
+
+    @staticmethod
+    def of(shape) -> "Dims":
+        """From any object with hk, hv, dk, dv, w, act_dtype, conv_dtype."""
+        return Dims(shape.hk, shape.hv, shape.dk, shape.dv, shape.w, shape.act_dtype,
+                    shape.conv_dtype)
+
+    @property
+    def channels(self) -> int:
+        return 2 * self.hk * self.dk + self.hv * self.dv
+
+    def c(self) -> CDims:
+        return CDims(self.hk, self.hv, self.dk, self.dv, self.conv_width,
+                     _DT_CODE[self.act_dtype], _DT_CODE[self.conv_dtype])
+
+
+@dataclass
+class StatePool:
+    """Device pool: ssm [N][HV][DV][DK] fp32, conv [N][W-1][C]."""
+
+    ssm: torch.Tensor
+    conv: torch.Tensor
+
+    @property
+    def num_slots(self) -> int:
+        return self.ssm.shape[0]
+
+    def c(self) -> CPool:
+        return CPool(self.ssm.data_ptr(), self.conv.data_ptr(), self.num_slots)
+
+    @staticmethod
+    def empty(dims: Dims, num_slots: int, device="cuda") -> "StatePool":
+        ssm = torch.empty((num_slots, dims.hv, dims.dv, dims.dk), dtype=torch.float32, device=device)
+        conv = torch.empty((num_slots, dims.conv_width - 1, dims.channels), dtype=dims.conv_dtype,
+                           device=device)
+        return StatePool(ssm, conv)
+
+
+@dataclass
+class LayerParams:
+    conv_w: torch.Tensor   # [C][W] fp32
+    A_log: torch.Tensor    # [HV] fp32
+    dt_bias: torch.Tensor  # [HV] fp32
+
+    def c(self) -> CParams:
+        return CParams(self.conv_w.data_ptr(), self.A_log.data_ptr(), self.dt_bias.data_ptr())
+
+
+# ---------------------------------------------------------------- entry points
+
+def decode_step(dims: Dims, pool: StatePool, params: LayerParams, slot_ids, qkv, a, b, out,
+                dev_err=None, stream=None):
+    L = load()
+    cd, cp = dims.c(), params.c()
+    st = L.gdn_decode_step(ctypes.byref(cd), pool.c(), ctypes.byref(cp), _ptr(slot_ids),
+                           int(slot_ids.shape[0]), _ptr(qkv), _ptr(a), _ptr(b), _ptr(out),
+                           _ptr(dev_err), _stream(stream))
+    _check("gdn_decode_step", st)
+
+
+def spec_verify(dims: Dims, work: StatePool, spec: StatePool, params: LayerParams, slot_ids,
+                spec_ids, qkv, a, b, out, dev_err=None, stream=None):
+    L = load()
+    B, T = spec_ids.shape
+    cd, cp = dims.c(), params.c()
+    st = L.gdn_spec_verify(ctypes.byref(cd), work.c(), spec.c(), ctypes.byref(cp),
+                           _ptr(slot_ids), _ptr(spec_ids), int(B), int(T), _ptr(qkv), _ptr(a),
+                           _ptr(b), _ptr(out), _ptr(dev_err), _stream(stream))
+    _check("gdn_spec_verify", st)
+
+
+def spec_commit(dims: Dims, spec: StatePool, work: StatePool, spec_ids, accept_len, slot_ids,
+                dev_err=None, stream=None):
+    L = load()
+    B, T = spec_ids.shape
+    cd = dims.c()
+    st = L.gdn_spec_commit(ctypes.byref(cd), spec.c(), work.c(), _ptr(spec_ids),
+                           _ptr(accept_len), _ptr(slot_ids), int(B), int(T), _ptr(dev_err),
+                           _stream(stream))
+    _check("gdn_spec_commit", st)
+
+
+def chunk_prefill_workspace_size(dims: Dims, n_seq: int, total_tokens: int) -> int:
+    cd = dims.c()
+    return int(load().gdn_chunk_prefill_workspace_size(ctypes.byref(cd), int(n_seq),
+                                                        int(total_tokens)))
+
+
+def chunk_prefill(dims: Dims, pool: StatePool, ckpt: StatePool, params: LayerParams, slot_ids,
+                  cu_seqlens, start_pos, total_tokens: int, ckpt_ids, ckpt_block: int, qkv, a, b,
+                  out, workspace, dev_err=None, stream=None):
+    L = load()
+    n_seq = int(slot_ids.shape[0])
+    max_ckpt = int(ckpt_ids.shape[1]) if ckpt_ids is not None and ckpt_ids.dim() == 2 else 0
+    cd, cp = dims.c(), params.c()
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = L.gdn_chunk_prefill(ctypes.byref(cd), pool.c(), ckpt.c(), ctypes.byref(cp),
+                             _ptr(slot_ids), _ptr(cu_seqlens), _ptr(start_pos), n_seq,
+                             int(total_tokens), _ptr(ckpt_ids), max_ckpt, int(ckpt_block),
+                             _ptr(qkv), _ptr(a), _ptr(b), _ptr(out), _ptr(workspace), ws_bytes,
+                             _ptr(dev_err), _stream(stream))
+    _check("gdn_chunk_prefill", st)
+
+
+def slot_copy(dims: Dims, src: StatePool, dst: StatePool, src_ids, dst_ids, dev_err=None,
+              stream=None):
+    L = load()
+    cd = dims.c()
+    st = L.gdn_slot_copy(ctypes.byref(cd), src.c(), dst.c(), _ptr(src_ids), _ptr(dst_ids),
+                         int(src_ids.shape[0]), _ptr(dev_err), _stream(stream))
+    _check("gdn_slot_copy", st)
+
+
+def slot_zero(dims: Dims, pool: StatePool, ids, dev_err=None, stream=None):
+    L = load()
+    cd = dims.c()
+    st = L.gdn_slot_zero(ctypes.byref(cd), pool.c(), _ptr(ids), int(ids.shape[0]), _ptr(dev_err),
+                         _stream(stream))
+    _check("gdn_slot_zero", st)
+
+
+def launch_count(kernel: int) -> int:
+    return int(load().gdn_launch_count(int(kernel)))
+
+
+def launch_counts() -> list[int]:
+    return [launch_count(k) for k in range(K_COUNT)]
+
+
+def launch_count_reset():
+    load().gdn_launch_count_reset()

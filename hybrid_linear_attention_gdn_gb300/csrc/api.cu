@@ -1,0 +1,55 @@
+// Host-side pieces shared by all entry points: argument checks, status
+// strings and launch counters.
+#include "gdn_common.cuh"
+
+namespace gdn {
+
+std::atomic<uint64_t> g_launches[GDN_K_COUNT];
+
+gdn_status check_dims(const gdn_dims* d) {
+  if (!d) return GDN_ERR_INVALID_ARG;
+  if (d->hk <= 0 || d->hv <= 0 || d->dk <= 0 || d->dv <= 0 || d->conv_width <= 0)
+    return GDN_ERR_INVALID_ARG;
+  if (d->hv % d->hk) return GDN_ERR_INVALID_ARG;
+  if (d->act_dtype != GDN_F32 && d->act_dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
+  if (d->conv_dtype != GDN_F32 && d->conv_dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
+  if (d->dk != 16 && d->dk != 64 && d->dk != 128) return GDN_ERR_UNSUPPORTED;
+  if (d->dv > 256) return GDN_ERR_UNSUPPORTED;
+  if (d->conv_width < 2 || d->conv_width > 8) return GDN_ERR_UNSUPPORTED;
+  if (d->act_dtype == GDN_F32 && d->conv_dtype == GDN_BF16) return GDN_ERR_UNSUPPORTED;
+  return GDN_OK;
+}
+
+gdn_status check_pool(const gdn_dims& d, const gdn_pool& p) {
+  if (p.num_slots < 0) return GDN_ERR_INVALID_ARG;
+  if (p.num_slots == 0) return GDN_OK;
+  if (!p.ssm || !p.conv) return GDN_ERR_INVALID_ARG;
+  if (!aligned(p.ssm, 16) || !aligned(p.conv, 16)) return GDN_ERR_INVALID_ARG;
+  return GDN_OK;
+}
+
+gdn_status launch_status() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+}  // namespace gdn
+
+extern "C" const char* gdn_status_string(int32_t s) {
+  switch (s) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG";
+    case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
+    default: return "GDN_UNKNOWN_STATUS";
+  }
+}
+
+extern "C" uint64_t gdn_launch_count(int32_t k) {
+  if (k < 0 || k >= GDN_K_COUNT) return 0;
+  return gdn::g_launches[k].load(std::memory_order_relaxed);
+}
+
+extern "C" void gdn_launch_count_reset(void) {
+  for (int k = 0; k < GDN_K_COUNT; ++k) gdn::g_launches[k].store(0);
+}

@@ -1,0 +1,590 @@
+// Fused GDN decode step and speculative verify over the slot pool.
+//
+// One CTA owns R rows (dv indices) of one V head of one request.  The fp32
+// state of that head is stored transposed, St[dv][dk], so row j of St is an
+// independent dk-vector: its update needs only (k^, v_j, q^), and the two dot
+// products per row reduce over dk with warp shuffles - no cross-warp traffic.
+//
+//   lanes per row  LPR = dk/16      (each lane holds 16 consecutive-in-phase
+//                                    floats of the row as 4 float4)
+//   rows per warp  RW  = 32/LPR
+//   rows per CTA   R   = NIT * 8 warps * RW
+//
+// The state rows are loaded with 128-bit streaming loads at kernel entry,
+// before the slot's conv history, the activations and the gates are even
+// read, so the HBM latency of the 64 KiB-per-head state overlaps the whole
+// prologue (conv1d + SiLU + L2 norm + gates).  Each state element is read
+// once and written once.
+//
+// Conv history ownership: the v channels of rows [row0, row0+R) of head h are
+// read and rewritten by this CTA alone.  The q/k channels of QK head hq are
+// shared by the G V heads that read hq and by all P row-parts of each, so
+// those G*P CTAs form one thread-block cluster: each arrives on the cluster
+// barrier once its history reads are done, and cluster rank 0 rewrites the
+// q/k history after waiting - after its own state work, when the others
+// have long arrived.  No distributed shared memory and no multicast is used.
+#include "gdn_common.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxW = 8;
+constexpr int kMaxT = 16;
+
+struct StepArgs {
+  float* ssm;
+  void* conv;
+  int32_t num_slots;
+  float* spec_ssm;
+  void* spec_conv;
+  int32_t spec_num_slots;
+  const int32_t* spec_ids;  // [B][T]
+  int32_t T;
+  const float* conv_w;
+  const float* A_log;
+  const float* dt_bias;
+  const int32_t* slot_ids;
+  int32_t B;
+  const void* qkv;
+  const void* a;
+  const void* b;
+  void* out;
+  uint32_t* err;
+  int32_t hk, hv, dv, W, C, G, P;
+};
+
+template <int DK>
+struct RowMap {
+  static constexpr int LPR = DK / 16;
+  static constexpr int RW = 32 / LPR;
+  static constexpr int RI = kWarps * RW;
+  // column of float4 number c (0..3) held by lane segment `seg`
+  static __device__ __forceinline__ int col(int c, int seg) { return c * 4 * LPR + seg * 4; }
+};
+
+__device__ __forceinline__ float dot4(float4 a, float4 b) {
+  return a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
+}
+
+template <int DK>
+__device__ __forceinline__ int channel_of(int i, int hq, int h, int hk, int dv, int row0) {
+  if (i < DK) return hq * DK + i;
+  if (i < 2 * DK) return hk * DK + hq * DK + (i - DK);
+  return 2 * hk * DK + h * dv + row0 + (i - 2 * DK);
+}
+
+template <int DK, int NIT>
+__device__ __forceinline__ void load_rows(float4 (&s)[NIT][4], const float* base, int nrows,
+                                          int rloc, int seg) {
+  using M = RowMap<DK>;
+#pragma unroll
+  for (int it = 0; it < NIT; ++it) {
+    const int row = it * M::RI + rloc;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      s[it][c] = row < nrows
+                     ? ld_stream(reinterpret_cast<const float4*>(base + (size_t)row * DK + M::col(c, seg)))
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+// Reduce (q.q, k.k, q.k) over the dk channels of one QK head held in smem,
+// with all warps; result in red_out[0..2] (shared).
+template <int DK>
+__device__ __forceinline__ void block_norms(const float* sq, const float* sk, float (*sred)[kWarps],
+                                            float* red_out) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float pq = 0.f, pk = 0.f, pqk = 0.f;
+  for (int i = tid; i < DK; i += kThreads) {
+    pq = fmaf(sq[i], sq[i], pq);
+    pk = fmaf(sk[i], sk[i], pk);
+    pqk = fmaf(sq[i], sk[i], pqk);
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    pq += __shfl_xor_sync(0xffffffffu, pq, o);
+    pk += __shfl_xor_sync(0xffffffffu, pk, o);
+    pqk += __shfl_xor_sync(0xffffffffu, pqk, o);
+  }
+  if (lane == 0) {
+    sred[0][warp] = pq;
+    sred[1][warp] = pk;
+    sred[2][warp] = pqk;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float a = 0.f, b = 0.f, c = 0.f;
+    for (int w = 0; w < kWarps; ++w) {
+      a += sred[0][w];
+      b += sred[1][w];
+      c += sred[2][w];
+    }
+    red_out[0] = a;
+    red_out[1] = b;
+    red_out[2] = c;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Decode: one token per request.
+// ---------------------------------------------------------------------------
+template <int DK, int NIT, typename Tact, typename Tconv>
+__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const StepArgs a) {
+  using M = RowMap<DK>;
+  constexpr int R = NIT * M::RI;
+  __shared__ float sq[DK], sk[DK], sv[R], so[R];
+  __shared__ float sraw[kMaxW][2 * DK];
+  __shared__ float sred[3][kWarps];
+  __shared__ float sscal[8];
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int r = blockIdx.y;
+  const int h = blockIdx.x / a.P, p = blockIdx.x % a.P;
+  const int hq = h / a.G;
+  const int row0 = p * R;
+  const int nrows = min(R, a.dv - row0);
+  const int csize = a.G * a.P;
+  const int32_t slot = a.slot_ids[r];
+  const int cls = slot_class(slot, a.num_slots);
+  Tact* out = reinterpret_cast<Tact*>(a.out) + ((size_t)r * a.hv + h) * a.dv + row0;
+  if (cls) {  // the whole cluster shares r, so it skips together
+    if (cls == 2 && blockIdx.x == 0 && tid == 0) report(a.err, GDN_DEV_ERR_SLOT_OOB);
+    for (int i = tid; i < nrows; i += kThreads) out[i] = from_f32<Tact>(0.f);
+    return;
+  }
+
+  // 1. state rows in flight first
+  const int seg = lane % M::LPR;
+  const int rloc = warp * M::RW + lane / M::LPR;
+  float* St = a.ssm + (((size_t)slot * a.hv + h) * a.dv + row0) * DK;
+  float4 s[NIT][4];
+  load_rows<DK, NIT>(s, St, nrows, rloc, seg);
+
+  // 2. conv1d + SiLU on the q/k channels of hq and the v channels of our rows
+  const bool qk_writer = csize == 1 || cluster_ctarank() == 0;
+  Tconv* conv = reinterpret_cast<Tconv*>(a.conv) + (size_t)slot * (a.W - 1) * a.C;
+  const Tact* x = reinterpret_cast<const Tact*>(a.qkv) + (size_t)r * a.C;
+  for (int i = tid; i < 2 * DK + nrows; i += kThreads) {
+    const int c = channel_of<DK>(i, hq, h, a.hk, a.dv, row0);
+    const float* w = a.conv_w + (size_t)c * a.W;
+    float hist[kMaxW];
+    float acc = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxW - 1; ++j)
+      if (j < a.W - 1) {
+        hist[j] = to_f32(conv[(size_t)j * a.C + c]);
+        acc = fmaf(w[j], hist[j], acc);
+      }
+    const float xv = to_f32(x[c]);
+    acc = fmaf(w[a.W - 1], xv, acc);
+    const float y = silu_f(acc);
+    if (i < DK) {
+      sq[i] = y;
+    } else if (i < 2 * DK) {
+      sk[i - DK] = y;
+    } else {
+      sv[i - 2 * DK] = y;
+      // this CTA alone owns these channels: shift the history now
+#pragma unroll
+      for (int j = 0; j < kMaxW - 2; ++j)
+        if (j < a.W - 2) conv[(size_t)j * a.C + c] = from_f32<Tconv>(hist[j + 1]);
+      conv[(size_t)(a.W - 2) * a.C + c] = from_f32<Tconv>(xv);
+    }
+    if (i < 2 * DK && qk_writer) {
+#pragma unroll
+      for (int j = 0; j < kMaxW - 1; ++j)
+        if (j < a.W - 1) sraw[j][i] = hist[j];
+      sraw[a.W - 1][i] = xv;
+    }
+  }
+  if (csize > 1) cluster_arrive_release();  // our reads of the shared history are done
+  __syncthreads();
+
+  // 3. L2 norms and gates
+  block_norms<DK>(sq, sk, sred, sscal);
+  if (tid == 0) {
+    const Tact* av = reinterpret_cast<const Tact*>(a.a) + (size_t)r * a.hv;
+    const Tact* bv = reinterpret_cast<const Tact*>(a.b) + (size_t)r * a.hv;
+    const float rq = rsqrtf(sscal[0] + kNormEps) * rsqrtf((float)DK);
+    const float rk = rsqrtf(sscal[1] + kNormEps);
+    sscal[3] = rq;
+    sscal[4] = rk;
+    sscal[5] = sscal[2] * rq * rk;  // k^ . q^
+    sscal[6] = gate_alpha(a.A_log[h], a.dt_bias[h], to_f32(av[h]));
+    sscal[7] = sigmoid_f(to_f32(bv[h]));
+  }
+  __syncthreads();
+  const float rq = sscal[3], rk = sscal[4], kq = sscal[5], alpha = sscal[6], beta = sscal[7];
+  float4 kk[4], qq[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int col = M::col(c, seg);
+    kk[c] = make_float4(sk[col] * rk, sk[col + 1] * rk, sk[col + 2] * rk, sk[col + 3] * rk);
+    qq[c] = make_float4(sq[col] * rq, sq[col + 1] * rq, sq[col + 2] * rq, sq[col + 3] * rq);
+  }
+
+  // 4. gated delta rule + readout, row by row
+  //    u = v - alpha St k^ ; St' = alpha St + beta u k^T ; o = St' q^
+  //      = alpha (St q^) + beta u (k^ . q^)
+#pragma unroll
+  for (int it = 0; it < NIT; ++it) {
+    const int row = it * M::RI + rloc;
+    float dk_ = 0.f, dq_ = 0.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      dk_ += dot4(s[it][c], kk[c]);
+      dq_ += dot4(s[it][c], qq[c]);
+    }
+#pragma unroll
+    for (int o = M::LPR / 2; o; o >>= 1) {
+      dk_ += __shfl_xor_sync(0xffffffffu, dk_, o);
+      dq_ += __shfl_xor_sync(0xffffffffu, dq_, o);
+    }
+    if (row < nrows) {
+      const float bu = beta * (sv[row] - alpha * dk_);
+      float4* dst = reinterpret_cast<float4*>(St + (size_t)row * DK);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float4 v = s[it][c];
+        v.x = fmaf(bu, kk[c].x, alpha * v.x);
+        v.y = fmaf(bu, kk[c].y, alpha * v.y);
+        v.z = fmaf(bu, kk[c].z, alpha * v.z);
+        v.w = fmaf(bu, kk[c].w, alpha * v.w);
+        st_stream(dst + M::col(c, seg) / 4, v);
+      }
+      if (seg == 0) so[row] = fmaf(bu, kq, alpha * dq_);
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < nrows; i += kThreads) out[i] = from_f32<Tact>(so[i]);
+
+  // 5. q/k history: one writer per cluster, after every reader arrived
+  if (csize > 1) cluster_wait_acquire();
+  if (qk_writer) {
+    for (int i = tid; i < 2 * DK; i += kThreads) {
+      const int c = channel_of<DK>(i, hq, h, a.hk, a.dv, row0);
+#pragma unroll
+      for (int j = 0; j < kMaxW - 1; ++j)
+        if (j < a.W - 1) conv[(size_t)j * a.C + c] = from_f32<Tconv>(sraw[j + 1][i]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Speculative verify: T draft tokens per request from the working slot, which
+// is only read; the state after draft t goes to spec slot spec_ids[r][t].
+// The state rows stay in registers across the T steps.
+// ---------------------------------------------------------------------------
+template <int DK, int NIT, typename Tact, typename Tconv>
+__global__ void __launch_bounds__(kThreads, 2) verify_kernel(const StepArgs a) {
+  using M = RowMap<DK>;
+  constexpr int R = NIT * M::RI;
+  constexpr int NCH = 2 * DK + R;  // channels handled: q, k, our v rows
+  extern __shared__ __align__(16) float smem[];
+  float* sy = smem;                     // [T][NCH]  conv+SiLU outputs
+  float* so = sy + (size_t)a.T * NCH;   // [T][R]    outputs
+  float* sscal = so + (size_t)a.T * R;  // [T][5]    rq, rk, kq, alpha, beta
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int r = blockIdx.y;
+  const int h = blockIdx.x / a.P, p = blockIdx.x % a.P;
+  const int hq = h / a.G;
+  const int row0 = p * R;
+  const int nrows = min(R, a.dv - row0);
+  const int T = a.T;
+  const int32_t slot = a.slot_ids[r];
+  const int cls = slot_class(slot, a.num_slots);
+  if (cls) {
+    if (cls == 2 && blockIdx.x == 0 && tid == 0) report(a.err, GDN_DEV_ERR_SLOT_OOB);
+    for (int t = 0; t < T; ++t) {
+      Tact* out = reinterpret_cast<Tact*>(a.out) + ((((size_t)r * T + t) * a.hv) + h) * a.dv + row0;
+      for (int i = tid; i < nrows; i += kThreads) out[i] = from_f32<Tact>(0.f);
+    }
+    return;
+  }
+
+  const int seg = lane % M::LPR;
+  const int rloc = warp * M::RW + lane / M::LPR;
+  const float* St = a.ssm + (((size_t)slot * a.hv + h) * a.dv + row0) * DK;
+  float4 s[NIT][4];
+  load_rows<DK, NIT>(s, St, nrows, rloc, seg);
+
+  // conv over the draft sequence; snapshot histories go straight to the spec
+  // slots (v rows: this CTA; q/k channels: the first V head of the group)
+  const bool qk_writer = (h % a.G) == 0 && p == 0;
+  const Tconv* conv = reinterpret_cast<const Tconv*>(a.conv) + (size_t)slot * (a.W - 1) * a.C;
+  const int32_t* sids = a.spec_ids + (size_t)r * T;
+  for (int i = tid; i < NCH; i += kThreads) {
+    if (i >= 2 * DK + nrows) continue;
+    const int c = channel_of<DK>(i, hq, h, a.hk, a.dv, row0);
+    const float* w = a.conv_w + (size_t)c * a.W;
+    float win[kMaxW];  // win[0..W-2] = history, oldest first
+#pragma unroll
+    for (int j = 0; j < kMaxW - 1; ++j)
+      if (j < a.W - 1) win[j] = to_f32(conv[(size_t)j * a.C + c]);
+    const bool writes = i >= 2 * DK || qk_writer;
+    for (int t = 0; t < T; ++t) {
+      const float xv = to_f32(reinterpret_cast<const Tact*>(a.qkv)[((size_t)r * T + t) * a.C + c]);
+      float acc = 0.f;
+#pragma unroll
+      for (int j = 0; j < kMaxW - 1; ++j)
+        if (j < a.W - 1) acc = fmaf(w[j], win[j], acc);
+      acc = fmaf(w[a.W - 1], xv, acc);
+      sy[(size_t)t * NCH + i] = silu_f(acc);
+      // advance the window
+#pragma unroll
+      for (int j = 0; j < kMaxW - 2; ++j)
+        if (j < a.W - 2) win[j] = win[j + 1];
+      win[a.W - 2] = xv;
+      if (writes) {
+        const int32_t sid = sids[t];
+        if (slot_class(sid, a.spec_num_slots) == 0) {
+          Tconv* sc = reinterpret_cast<Tconv*>(a.spec_conv) + (size_t)sid * (a.W - 1) * a.C;
+#pragma unroll
+          for (int j = 0; j < kMaxW - 1; ++j)
+            if (j < a.W - 1) sc[(size_t)j * a.C + c] = from_f32<Tconv>(win[j]);
+        }
+      }
+    }
+  }
+  if (tid < T && blockIdx.x == 0 && slot_class(sids[tid], a.spec_num_slots) == 2)
+    report(a.err, GDN_DEV_ERR_SLOT_OOB);
+  __syncthreads();
+
+  // per-token norms and gates: warp w handles tokens w, w+8, ...
+  for (int t = warp; t < T; t += kWarps) {
+    const float* yq = sy + (size_t)t * NCH;
+    const float* yk = yq + DK;
+    float pq = 0.f, pk = 0.f, pqk = 0.f;
+    for (int i = lane; i < DK; i += 32) {
+      pq = fmaf(yq[i], yq[i], pq);
+      pk = fmaf(yk[i], yk[i], pk);
+      pqk = fmaf(yq[i], yk[i], pqk);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      pq += __shfl_xor_sync(0xffffffffu, pq, o);
+      pk += __shfl_xor_sync(0xffffffffu, pk, o);
+      pqk += __shfl_xor_sync(0xffffffffu, pqk, o);
+    }
+    if (lane == 0) {
+      const size_t rt = (size_t)r * T + t;
+      const float rq = rsqrtf(pq + kNormEps) * rsqrtf((float)DK);
+      const float rk = rsqrtf(pk + kNormEps);
+      sscal[t * 5 + 0] = rq;
+      sscal[t * 5 + 1] = rk;
+      sscal[t * 5 + 2] = pqk * rq * rk;
+      sscal[t * 5 + 3] = gate_alpha(a.A_log[h], a.dt_bias[h],
+                                    to_f32(reinterpret_cast<const Tact*>(a.a)[rt * a.hv + h]));
+      sscal[t * 5 + 4] = sigmoid_f(to_f32(reinterpret_cast<const Tact*>(a.b)[rt * a.hv + h]));
+    }
+  }
+  __syncthreads();
+
+  for (int t = 0; t < T; ++t) {
+    const float* yq = sy + (size_t)t * NCH;
+    const float* yk = yq + DK;
+    const float* yv = yk + DK;
+    const float rq = sscal[t * 5 + 0], rk = sscal[t * 5 + 1], kq = sscal[t * 5 + 2];
+    const float alpha = sscal[t * 5 + 3], beta = sscal[t * 5 + 4];
+    float4 kk[4], qq[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const float4 k4 = *reinterpret_cast<const float4*>(yk + M::col(c, seg));
+      const float4 q4 = *reinterpret_cast<const float4*>(yq + M::col(c, seg));
+      kk[c] = make_float4(k4.x * rk, k4.y * rk, k4.z * rk, k4.w * rk);
+      qq[c] = make_float4(q4.x * rq, q4.y * rq, q4.z * rq, q4.w * rq);
+    }
+    const int32_t sid = sids[t];
+    float* Sp = slot_class(sid, a.spec_num_slots) == 0
+                    ? a.spec_ssm + (((size_t)sid * a.hv + h) * a.dv + row0) * DK
+                    : nullptr;
+#pragma unroll
+    for (int it = 0; it < NIT; ++it) {
+      const int row = it * M::RI + rloc;
+      float dk_ = 0.f, dq_ = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        dk_ += dot4(s[it][c], kk[c]);
+        dq_ += dot4(s[it][c], qq[c]);
+      }
+#pragma unroll
+      for (int o = M::LPR / 2; o; o >>= 1) {
+        dk_ += __shfl_xor_sync(0xffffffffu, dk_, o);
+        dq_ += __shfl_xor_sync(0xffffffffu, dq_, o);
+      }
+      const float bu = row < nrows ? beta * (yv[row] - alpha * dk_) : 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float4& v = s[it][c];
+        v.x = fmaf(bu, kk[c].x, alpha * v.x);
+        v.y = fmaf(bu, kk[c].y, alpha * v.y);
+        v.z = fmaf(bu, kk[c].z, alpha * v.z);
+        v.w = fmaf(bu, kk[c].w, alpha * v.w);
+      }
+      if (row < nrows) {
+        if (Sp) {
+          float4* dst = reinterpret_cast<float4*>(Sp + (size_t)row * DK);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) st_stream(dst + M::col(c, seg) / 4, s[it][c]);
+        }
+        if (seg == 0) so[(size_t)t * R + row] = fmaf(bu, kq, alpha * dq_);
+      }
+    }
+  }
+  __syncthreads();
+  for (int t = 0; t < T; ++t) {
+    Tact* out = reinterpret_cast<Tact*>(a.out) + ((((size_t)r * T + t) * a.hv) + h) * a.dv + row0;
+    for (int i = tid; i < nrows; i += kThreads) out[i] = from_f32<Tact>(so[(size_t)t * R + i]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+template <int DK, int NIT, typename Tact, typename Tconv>
+cudaError_t launch_decode_t(const StepArgs& a, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(a.hv * a.P), (unsigned)a.B);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  cfg.attrs = attr;
+  cfg.numAttrs = 0;
+  if (a.G * a.P > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)(a.G * a.P);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, decode_kernel<DK, NIT, Tact, Tconv>, a);
+}
+
+template <int DK, int NIT, typename Tact, typename Tconv>
+cudaError_t launch_verify_t(const StepArgs& a, cudaStream_t s) {
+  constexpr int R = NIT * RowMap<DK>::RI;
+  const size_t smem = sizeof(float) * ((size_t)a.T * (2 * DK + R) + (size_t)a.T * R + (size_t)a.T * 5);
+  auto k = verify_kernel<DK, NIT, Tact, Tconv>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  k<<<dim3((unsigned)(a.hv * a.P), (unsigned)a.B), kThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int DK, int NIT>
+cudaError_t dispatch_dtype(bool verify, const StepArgs& a, int act, int cv, cudaStream_t s) {
+  if (act == GDN_F32 && cv == GDN_F32)
+    return verify ? launch_verify_t<DK, NIT, float, float>(a, s)
+                  : launch_decode_t<DK, NIT, float, float>(a, s);
+  if (act == GDN_BF16 && cv == GDN_BF16)
+    return verify ? launch_verify_t<DK, NIT, __nv_bfloat16, __nv_bfloat16>(a, s)
+                  : launch_decode_t<DK, NIT, __nv_bfloat16, __nv_bfloat16>(a, s);
+  return verify ? launch_verify_t<DK, NIT, __nv_bfloat16, float>(a, s)
+                : launch_decode_t<DK, NIT, __nv_bfloat16, float>(a, s);
+}
+
+// rows-per-CTA choice: fewer rows (more CTAs, smaller clusters of work) when
+// the batch is small, so that enough bytes are in flight to cover HBM latency.
+int choose_nit(int dk, int dv, int units, int G, bool verify) {
+  if (dk == 16) return 1;
+  const int ri = kWarps * (32 / (dk / 16));
+  int nit = dk == 64 ? 2 : 4;
+  const int target = verify ? 512 : 1024;  // CTAs wanted before the largest tile is used
+  while (nit > 1 && (long)units * ((dv + nit * ri - 1) / (nit * ri)) < target) nit >>= 1;
+  // a cluster spans G V heads x P row-parts; keep it within the portable 8
+  while (!verify && nit < (dk == 64 ? 2 : 4) && G * ((dv + nit * ri - 1) / (nit * ri)) > 8) nit <<= 1;
+  return nit;
+}
+
+gdn_status run_step(bool verify, const gdn_dims* dims, const gdn_pool& work, const gdn_pool* spec,
+                    const gdn_params* params, const int32_t* slot_ids, const int32_t* spec_ids,
+                    int32_t B, int32_t T, const void* qkv, const void* a, const void* b, void* out,
+                    uint32_t* dev_err, void* stream) {
+  gdn_status st = check_dims(dims);
+  if (st != GDN_OK) return st;
+  if (B < 0 || (verify && (T < 1))) return GDN_ERR_INVALID_ARG;
+  if (verify && T > kMaxT) return GDN_ERR_UNSUPPORTED;
+  if (B == 0) return GDN_OK;
+  if (B > 65535) return GDN_ERR_UNSUPPORTED;
+  if ((st = check_pool(*dims, work)) != GDN_OK) return st;
+  if (verify && (st = check_pool(*dims, *spec)) != GDN_OK) return st;
+  if (!params || !params->conv_w || !params->A_log || !params->dt_bias) return GDN_ERR_INVALID_ARG;
+  if (!slot_ids || !qkv || !a || !b || !out || (verify && !spec_ids)) return GDN_ERR_INVALID_ARG;
+  const int G = dims->hv / dims->hk;
+  if (G > 8) return GDN_ERR_UNSUPPORTED;
+  StepArgs s = {};
+  s.ssm = work.ssm;
+  s.conv = work.conv;
+  s.num_slots = work.num_slots;
+  if (verify) {
+    s.spec_ssm = spec->ssm;
+    s.spec_conv = spec->conv;
+    s.spec_num_slots = spec->num_slots;
+    s.spec_ids = spec_ids;
+    s.T = T;
+  }
+  s.conv_w = params->conv_w;
+  s.A_log = params->A_log;
+  s.dt_bias = params->dt_bias;
+  s.slot_ids = slot_ids;
+  s.B = B;
+  s.qkv = qkv;
+  s.a = a;
+  s.b = b;
+  s.out = out;
+  s.err = dev_err;
+  s.hk = dims->hk;
+  s.hv = dims->hv;
+  s.dv = dims->dv;
+  s.W = dims->conv_width;
+  s.C = (int32_t)channels(*dims);
+  s.G = G;
+  const int nit = choose_nit(dims->dk, dims->dv, B * dims->hv, G, verify);
+  const int ri = kWarps * (32 / (dims->dk / 16));
+  s.P = (dims->dv + nit * ri - 1) / (nit * ri);
+  if (!verify && G * s.P > 8) return GDN_ERR_UNSUPPORTED;
+  if ((long)dims->hv * s.P > 2147483647L) return GDN_ERR_UNSUPPORTED;
+  const int act = dims->act_dtype, cv = dims->conv_dtype;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaErrorInvalidValue;
+  switch (dims->dk) {
+    case 16: e = dispatch_dtype<16, 1>(verify, s, act, cv, cs); break;
+    case 64:
+      e = nit == 1 ? dispatch_dtype<64, 1>(verify, s, act, cv, cs)
+                   : dispatch_dtype<64, 2>(verify, s, act, cv, cs);
+      break;
+    case 128:
+      e = nit == 1   ? dispatch_dtype<128, 1>(verify, s, act, cv, cs)
+          : nit == 2 ? dispatch_dtype<128, 2>(verify, s, act, cv, cs)
+                     : dispatch_dtype<128, 4>(verify, s, act, cv, cs);
+      break;
+  }
+  count_launch(verify ? GDN_K_SPEC_VERIFY : GDN_K_DECODE);
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace gdn
+
+extern "C" gdn_status gdn_decode_step(const gdn_dims* dims, gdn_pool pool, const gdn_params* params,
+                                      const int32_t* slot_ids, int32_t B, const void* qkv,
+                                      const void* a, const void* b, void* out, uint32_t* dev_err,
+                                      void* stream) {
+  return gdn::run_step(false, dims, pool, nullptr, params, slot_ids, nullptr, B, 1, qkv, a, b, out,
+                       dev_err, stream);
+}
+
+extern "C" gdn_status gdn_spec_verify(const gdn_dims* dims, gdn_pool work, gdn_pool spec,
+                                      const gdn_params* params, const int32_t* slot_ids,
+                                      const int32_t* spec_ids, int32_t B, int32_t T,
+                                      const void* qkv, const void* a, const void* b, void* out,
+                                      uint32_t* dev_err, void* stream) {
+  return gdn::run_step(true, dims, work, &spec, params, slot_ids, spec_ids, B, T, qkv, a, b, out,
+                       dev_err, stream);
+}

@@ -1,0 +1,86 @@
+// Shared helpers for the libgdn kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "gdn.h"
+
+namespace gdn {
+
+// ---- element conversion ---------------------------------------------------
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// ---- streaming 128-bit global access (data touched once per launch) --------
+__device__ __forceinline__ float4 ld_stream(const float4* p) { return __ldcs(p); }
+__device__ __forceinline__ void st_stream(float4* p, float4 v) { __stcs(p, v); }
+
+// ---- device error word ----------------------------------------------------
+__device__ __forceinline__ void report(uint32_t* err, uint32_t bits) {
+  if (err) atomicOr(err, bits);
+}
+
+// 0 = usable, 1 = padding (-1), 2 = out of range
+__device__ __forceinline__ int slot_class(int32_t id, int32_t n) {
+  if (id == -1) return 1;
+  return (id < 0 || id >= n) ? 2 : 0;
+}
+
+// ---- thread-block cluster barrier (split arrive / wait) --------------------
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+  return r;
+}
+
+// ---- math (CUDA library functions; fp32) -----------------------------------
+__device__ __forceinline__ float silu_f(float y) { return y / (1.0f + expf(-y)); }
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
+__device__ __forceinline__ float softplus_f(float x) {
+  return x > 20.0f ? x : log1pf(expf(x));
+}
+// alpha = exp(-exp(A_log) * softplus(a + dt_bias))
+__device__ __forceinline__ float gate_alpha(float A_log, float dt_bias, float a) {
+  return expf(-expf(A_log) * softplus_f(a + dt_bias));
+}
+
+constexpr float kNormEps = 1e-6f;
+
+// ---- host side ------------------------------------------------------------
+extern std::atomic<uint64_t> g_launches[GDN_K_COUNT];
+inline void count_launch(int k) { g_launches[k].fetch_add(1, std::memory_order_relaxed); }
+
+inline int64_t channels(const gdn_dims& d) {
+  return 2 * (int64_t)d.hk * d.dk + (int64_t)d.hv * d.dv;
+}
+inline size_t dtype_size(int32_t t) { return t == GDN_BF16 ? 2 : 4; }
+inline size_t ssm_slot_bytes(const gdn_dims& d) {
+  return (size_t)d.hv * d.dv * d.dk * sizeof(float);
+}
+inline size_t conv_slot_bytes(const gdn_dims& d) {
+  return (size_t)(d.conv_width - 1) * channels(d) * dtype_size(d.conv_dtype);
+}
+
+// Host-side validation shared by every entry point.
+gdn_status check_dims(const gdn_dims* d);
+gdn_status check_pool(const gdn_dims& d, const gdn_pool& p);
+inline bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+gdn_status launch_status();
+
+}  // namespace gdn

@@ -1,0 +1,539 @@
+// Chunked GDN prefill with block-aligned checkpoints.
+//
+// TokenSpeed Qwen3.5 page, "Ciclo de vida de slots": prefill fills the
+// working slot, and checkpoint slots receive clean snapshots that become
+// reusable at block-aligned prefix boundaries.  The state recurrence is
+// evaluated in the chunkwise WY/UT form of the delta rule (Yang et al.,
+// "Parallelizing Linear Transformers with the Delta Rule over Sequence
+// Length", NeurIPS 2024, with the Gated DeltaNet decay): for a chunk of n
+// tokens with local cumulative log-decay b_i = sum_{j<=i} g_j,
+//   A = strict_lower(diag(beta) (K K^T (.) Gamma)),  Gamma_ij = e^{b_i - b_j}
+//   T = (I + A)^{-1} diag(beta)
+//   W = T diag(e^b) K,  U = T V,  Delta = U - W S
+//   O = diag(e^b) Q S + (Q K^T (.) Gamma (.) lower-incl-diag) Delta
+//   S' = e^{b_n} S + (diag(e^{b_n - b}) K)^T Delta
+// Chunks are 64 tokens aligned to absolute positions, so every checkpoint
+// boundary (a multiple of the checkpoint block, itself a multiple of 64) is
+// a chunk boundary.
+//
+// Three kernels, in stream order:
+//   features: conv1d + SiLU + L2 norm + gates per (token, QK head) -> workspace
+//   chunks:   one CTA per (sequence, V head, dv tile) walks the chunks in
+//             order, keeping its slice of S in shared memory
+//   history:  one thread per (sequence, channel) writes the conv history of
+//             every checkpoint and the final one (it reads the old history
+//             before overwriting it, and runs after `features` read it)
+#include "gdn_common.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kChunk = 64;
+constexpr int kMaxW = 8;
+
+struct PrefillArgs {
+  float* ssm;
+  void* conv;
+  int32_t num_slots;
+  float* ck_ssm;
+  void* ck_conv;
+  int32_t ck_num_slots;
+  const float* conv_w;
+  const float* A_log;
+  const float* dt_bias;
+  const int32_t* slot_ids;
+  const int32_t* cu_seqlens;
+  const int64_t* start_pos;
+  int32_t n_seq;
+  int64_t total;
+  const int32_t* ckpt_ids;
+  int32_t max_ckpt;
+  int32_t ckpt_block;
+  const void* qkv;
+  const void* a;
+  const void* b;
+  void* out;
+  uint32_t* err;
+  // workspace (fp32)
+  float* ws_q;     // [total][hk][dk]  q^ (scaled by dk^-1/2)
+  float* ws_k;     // [total][hk][dk]  k^
+  float* ws_v;     // [total][hv][dv]
+  float* ws_g;     // [total][hv]      log decay g
+  float* ws_beta;  // [total][hv]
+  int32_t hk, hv, dk, dv, W, C, G;
+};
+
+__device__ __forceinline__ int seq_of_token(const int32_t* cu, int n_seq, int64_t t) {
+  int lo = 0, hi = n_seq - 1;  // last n with cu[n] <= t
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((int64_t)cu[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// ---------------------------------------------------------------------------
+// features: grid (total tokens, hk)
+// ---------------------------------------------------------------------------
+template <int DK, typename Tact, typename Tconv>
+__global__ void __launch_bounds__(kThreads) features_kernel(const PrefillArgs a) {
+  __shared__ float sq[DK], sk[DK];
+  __shared__ float sred[2][kWarps];
+  __shared__ float sr[2];
+  const int64_t t = blockIdx.x;
+  const int hq = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n = seq_of_token(a.cu_seqlens, a.n_seq, t);
+  const int32_t slot = a.slot_ids[n];
+  if (slot_class(slot, a.num_slots)) return;  // the chunk kernel zeroes its outputs
+  const int64_t t0 = a.cu_seqlens[n];
+  const int64_t i = t - t0;  // index within the sequence
+  if (i < 0) return;         // inconsistent cu_seqlens: reported by the chunk kernel
+  const Tact* qkv = reinterpret_cast<const Tact*>(a.qkv);
+  const Tconv* hist = reinterpret_cast<const Tconv*>(a.conv) + (size_t)slot * (a.W - 1) * a.C;
+  const int nch = 2 * DK + a.G * a.dv;
+  for (int idx = tid; idx < nch; idx += kThreads) {
+    int c;
+    if (idx < DK) c = hq * DK + idx;
+    else if (idx < 2 * DK) c = a.hk * DK + hq * DK + (idx - DK);
+    else c = 2 * a.hk * DK + hq * a.G * a.dv + (idx - 2 * DK);
+    const float* w = a.conv_w + (size_t)c * a.W;
+    float acc = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxW; ++j) {
+      if (j < a.W) {
+        const int64_t m = i - (a.W - 1) + j;  // window element j, sequence-relative
+        const float xv = m >= 0 ? to_f32(qkv[(t0 + m) * a.C + c])
+                                : to_f32(hist[(size_t)(a.W - 1 + m) * a.C + c]);
+        acc = fmaf(w[j], xv, acc);
+      }
+    }
+    const float y = silu_f(acc);
+    if (idx < DK) sq[idx] = y;
+    else if (idx < 2 * DK) sk[idx - DK] = y;
+    else a.ws_v[(size_t)t * a.hv * a.dv + (size_t)hq * a.G * a.dv + (idx - 2 * DK)] = y;
+  }
+  __syncthreads();
+  float pq = 0.f, pk = 0.f;
+  for (int m = tid; m < DK; m += kThreads) {
+    pq = fmaf(sq[m], sq[m], pq);
+    pk = fmaf(sk[m], sk[m], pk);
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    pq += __shfl_xor_sync(0xffffffffu, pq, o);
+    pk += __shfl_xor_sync(0xffffffffu, pk, o);
+  }
+  if (lane == 0) {
+    sred[0][warp] = pq;
+    sred[1][warp] = pk;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float x = 0.f, y = 0.f;
+    for (int w = 0; w < kWarps; ++w) {
+      x += sred[0][w];
+      y += sred[1][w];
+    }
+    sr[0] = rsqrtf(x + kNormEps) * rsqrtf((float)DK);
+    sr[1] = rsqrtf(y + kNormEps);
+  }
+  __syncthreads();
+  float* oq = a.ws_q + ((size_t)t * a.hk + hq) * DK;
+  float* ok = a.ws_k + ((size_t)t * a.hk + hq) * DK;
+  for (int m = tid; m < DK; m += kThreads) {
+    oq[m] = sq[m] * sr[0];
+    ok[m] = sk[m] * sr[1];
+  }
+  if (tid < a.G) {
+    const int h = hq * a.G + tid;
+    const float av = to_f32(reinterpret_cast<const Tact*>(a.a)[(size_t)t * a.hv + h]);
+    const float bv = to_f32(reinterpret_cast<const Tact*>(a.b)[(size_t)t * a.hv + h]);
+    a.ws_g[(size_t)t * a.hv + h] = -expf(a.A_log[h]) * softplus_f(av + a.dt_bias[h]);
+    a.ws_beta[(size_t)t * a.hv + h] = sigmoid_f(bv);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// chunks: grid (hv * n_tiles, n_seq); S slice St[DVT][DK] lives in smem
+// ---------------------------------------------------------------------------
+template <int DK, int DVT>
+struct ChunkSmem {
+  static constexpr int LK = DK + 1;   // padded row strides (column walks
+  static constexpr int LV = DVT + 1;  // across rows stay conflict-free)
+  static constexpr int LC = kChunk + 1;
+  static constexpr size_t floats =
+      (size_t)DVT * LK            // St
+      + 3 * (size_t)kChunk * LK   // K, Q, W
+      + 2 * (size_t)kChunk * LV   // V, U (then Delta)
+      + 2 * (size_t)kChunk * LC   // A (then QK), T
+      + 3 * kChunk;               // b, beta, e^b
+  static constexpr size_t bytes = floats * sizeof(float);
+};
+
+template <int DK, int DVT, typename Tact>
+__global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const PrefillArgs a) {
+  using L = ChunkSmem<DK, DVT>;
+  extern __shared__ float sm[];
+  float* St = sm;
+  float* K = St + DVT * L::LK;
+  float* Q = K + kChunk * L::LK;
+  float* Wm = Q + kChunk * L::LK;
+  float* V = Wm + kChunk * L::LK;
+  float* U = V + kChunk * L::LV;
+  float* A = U + kChunk * L::LV;
+  float* Tm = A + kChunk * L::LC;
+  float* sb = Tm + kChunk * L::LC;
+  float* sbeta = sb + kChunk;
+  float* seb = sbeta + kChunk;
+
+  const int tid = threadIdx.x;
+  const int n_tiles = (a.dv + DVT - 1) / DVT;
+  const int n = blockIdx.y;
+  const int h = blockIdx.x / n_tiles;
+  const int j0 = (blockIdx.x % n_tiles) * DVT;
+  const int ncols = min(DVT, a.dv - j0);
+  const int hq = h / a.G;
+  const int64_t t0 = a.cu_seqlens[n], len = (int64_t)a.cu_seqlens[n + 1] - t0;
+  const int64_t p0 = a.start_pos[n];
+  const int32_t slot = a.slot_ids[n];
+  Tact* out = reinterpret_cast<Tact*>(a.out);
+  if (t0 < 0 || len < 0 || t0 + len > a.total || p0 < 0) {
+    if (blockIdx.x == 0 && tid == 0) report(a.err, GDN_DEV_ERR_SEQLENS);
+    return;
+  }
+  const int cls = slot_class(slot, a.num_slots);
+  if (cls) {
+    if (cls == 2 && blockIdx.x == 0 && tid == 0) report(a.err, GDN_DEV_ERR_SLOT_OOB);
+    for (int64_t e = tid; e < len * ncols; e += kThreads) {
+      const int64_t r = e / ncols;
+      out[((t0 + r) * a.hv + h) * a.dv + j0 + (e % ncols)] = from_f32<Tact>(0.f);
+    }
+    return;
+  }
+  float* gS = a.ssm + (((size_t)slot * a.hv + h) * a.dv + j0) * DK;
+  for (int e = tid; e < DVT * DK; e += kThreads) {
+    const int j = e / DK, m = e % DK;
+    St[j * L::LK + m] = j < ncols ? gS[(size_t)j * DK + m] : 0.f;
+  }
+
+  int64_t pos = p0;
+  const int64_t p1 = p0 + len;
+  while (pos < p1) {
+    const int64_t cend = min(p1, (pos / kChunk + 1) * kChunk);
+    const int nr = (int)(cend - pos);
+    const int64_t tb = t0 + (pos - p0);  // packed index of row 0
+    __syncthreads();  // previous chunk done with K, Q, V, St
+    for (int e = tid; e < kChunk * DK; e += kThreads) {
+      const int r = e / DK, m = e % DK;
+      const bool ok = r < nr;
+      K[r * L::LK + m] = ok ? a.ws_k[((tb + r) * a.hk + hq) * DK + m] : 0.f;
+      Q[r * L::LK + m] = ok ? a.ws_q[((tb + r) * a.hk + hq) * DK + m] : 0.f;
+    }
+    for (int e = tid; e < kChunk * DVT; e += kThreads) {
+      const int r = e / DVT, j = e % DVT;
+      V[r * L::LV + j] = (r < nr && j < ncols) ? a.ws_v[((tb + r) * a.hv + h) * a.dv + j0 + j] : 0.f;
+    }
+    if (tid < 32) {  // inclusive prefix sum of g (warp 0, two 32-wide halves)
+      float carry = 0.f;
+      for (int half = 0; half < 2; ++half) {
+        const int r = half * 32 + tid;
+        float v = r < nr ? a.ws_g[(tb + r) * a.hv + h] : 0.f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float u = __shfl_up_sync(0xffffffffu, v, o);
+          if (tid >= o) v += u;
+        }
+        v += carry;
+        sb[r] = v;
+        carry = __shfl_sync(0xffffffffu, v, 31);
+      }
+    }
+    if (tid >= 64 && tid < 128) {
+      const int r = tid - 64;
+      sbeta[r] = r < nr ? a.ws_beta[(tb + r) * a.hv + h] : 0.f;
+    }
+    __syncthreads();
+    if (tid < kChunk) seb[tid] = expf(sb[tid]);
+    // A = strict_lower(diag(beta) (K K^T (.) Gamma))
+    for (int e = tid; e < kChunk * kChunk; e += kThreads) {
+      const int r = e / kChunk, c = e % kChunk;
+      float v = 0.f;
+      if (c < r && r < nr) {
+        float d = 0.f;
+        for (int m = 0; m < DK; ++m) d = fmaf(K[r * L::LK + m], K[c * L::LK + m], d);
+        v = sbeta[r] * d * expf(sb[r] - sb[c]);
+      }
+      A[r * L::LC + c] = v;
+    }
+    __syncthreads();
+    // T = (I + A)^{-1} diag(beta): forward substitution, one row at a time
+    for (int r = 0; r < nr; ++r) {
+      if (tid < kChunk) {
+        const int c = tid;
+        float v = 0.f;
+        if (c <= r) {
+          v = (c == r) ? sbeta[r] : 0.f;
+          for (int m = c; m < r; ++m) v = fmaf(-A[r * L::LC + m], Tm[m * L::LC + c], v);
+        }
+        Tm[r * L::LC + c] = v;
+      }
+      __syncthreads();
+    }
+    // A <- Q K^T (.) Gamma (.) lower-incl-diag ;  W = T diag(e^b) K ;  U = T V
+    for (int e = tid; e < kChunk * kChunk; e += kThreads) {
+      const int r = e / kChunk, c = e % kChunk;
+      float v = 0.f;
+      if (c <= r && r < nr) {
+        float d = 0.f;
+        for (int m = 0; m < DK; ++m) d = fmaf(Q[r * L::LK + m], K[c * L::LK + m], d);
+        v = d * expf(sb[r] - sb[c]);
+      }
+      A[r * L::LC + c] = v;
+    }
+    for (int e = tid; e < kChunk * DK; e += kThreads) {
+      const int r = e / DK, m = e % DK;
+      float v = 0.f;
+      if (r < nr)
+        for (int c = 0; c <= r; ++c) v = fmaf(Tm[r * L::LC + c] * seb[c], K[c * L::LK + m], v);
+      Wm[r * L::LK + m] = v;
+    }
+    for (int e = tid; e < kChunk * DVT; e += kThreads) {
+      const int r = e / DVT, j = e % DVT;
+      float v = 0.f;
+      if (r < nr)
+        for (int c = 0; c <= r; ++c) v = fmaf(Tm[r * L::LC + c], V[c * L::LV + j], v);
+      U[r * L::LV + j] = v;
+    }
+    __syncthreads();
+    // Delta = U - W S   (in place)
+    for (int e = tid; e < kChunk * DVT; e += kThreads) {
+      const int r = e / DVT, j = e % DVT;
+      if (r < nr) {
+        float v = U[r * L::LV + j];
+        for (int m = 0; m < DK; ++m) v = fmaf(-Wm[r * L::LK + m], St[j * L::LK + m], v);
+        U[r * L::LV + j] = v;
+      }
+    }
+    __syncthreads();
+    // O = diag(e^b) Q S + (QK^T (.) Gamma) Delta
+    for (int e = tid; e < kChunk * DVT; e += kThreads) {
+      const int r = e / DVT, j = e % DVT;
+      if (r < nr && j < ncols) {
+        float qs = 0.f;
+        for (int m = 0; m < DK; ++m) qs = fmaf(Q[r * L::LK + m], St[j * L::LK + m], qs);
+        float v = seb[r] * qs;
+        for (int c = 0; c <= r; ++c) v = fmaf(A[r * L::LC + c], U[c * L::LV + j], v);
+        out[((tb + r) * a.hv + h) * a.dv + j0 + j] = from_f32<Tact>(v);
+      }
+    }
+    __syncthreads();
+    // S' = e^{b_n} S + (diag(e^{b_n - b}) K)^T Delta
+    const float blast = sb[nr - 1];
+    for (int e = tid; e < DVT * DK; e += kThreads) {
+      const int j = e / DK, m = e % DK;
+      float v = expf(blast) * St[j * L::LK + m];
+      for (int c = 0; c < nr; ++c)
+        v = fmaf(expf(blast - sb[c]) * K[c * L::LK + m], U[c * L::LV + j], v);
+      St[j * L::LK + m] = v;
+    }
+    pos = cend;
+    if (pos % a.ckpt_block == 0) {
+      const int64_t idx = pos / a.ckpt_block - p0 / a.ckpt_block - 1;
+      if (idx >= 0 && idx < a.max_ckpt) {
+        const int32_t cid = a.ckpt_ids[(size_t)n * a.max_ckpt + idx];
+        if (slot_class(cid, a.ck_num_slots) == 0) {
+          __syncthreads();
+          float* cS = a.ck_ssm + (((size_t)cid * a.hv + h) * a.dv + j0) * DK;
+          for (int e = tid; e < ncols * DK; e += kThreads)
+            cS[(size_t)(e / DK) * DK + (e % DK)] = St[(e / DK) * L::LK + (e % DK)];
+        }
+      }
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < ncols * DK; e += kThreads)
+    gS[(size_t)(e / DK) * DK + (e % DK)] = St[(e / DK) * L::LK + (e % DK)];
+}
+
+// ---------------------------------------------------------------------------
+// history: grid (ceil(C / 256), n_seq); one thread per channel
+// ---------------------------------------------------------------------------
+template <typename Tact, typename Tconv>
+__global__ void __launch_bounds__(kThreads) history_kernel(const PrefillArgs a) {
+  const int n = blockIdx.y;
+  const int c = blockIdx.x * kThreads + threadIdx.x;
+  if (c >= a.C) return;
+  const int32_t slot = a.slot_ids[n];
+  if (slot_class(slot, a.num_slots)) return;
+  const int64_t t0 = a.cu_seqlens[n], len = (int64_t)a.cu_seqlens[n + 1] - t0;
+  const int64_t p0 = a.start_pos[n], p1 = p0 + len;
+  if (t0 < 0 || len < 0 || t0 + len > a.total || p0 < 0) return;
+  Tconv* hist = reinterpret_cast<Tconv*>(a.conv) + (size_t)slot * (a.W - 1) * a.C;
+  const Tact* qkv = reinterpret_cast<const Tact*>(a.qkv);
+  float old[kMaxW];
+#pragma unroll
+  for (int j = 0; j < kMaxW - 1; ++j)
+    if (j < a.W - 1) old[j] = to_f32(hist[(size_t)j * a.C + c]);
+  // raw input at sequence-relative index m (negative: the old history)
+  auto raw = [&](int64_t m) -> float {
+    if (m >= 0) return to_f32(qkv[(t0 + m) * a.C + c]);
+    float v = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxW - 1; ++j)
+      if (j == a.W - 1 + m) v = old[j];
+    return v;
+  };
+  const int64_t blk = a.ckpt_block;
+  for (int64_t P = (p0 / blk + 1) * blk; P <= p1; P += blk) {
+    const int64_t idx = P / blk - p0 / blk - 1;
+    if (idx >= a.max_ckpt) break;
+    const int32_t cid = a.ckpt_ids[(size_t)n * a.max_ckpt + idx];
+    const int cc = slot_class(cid, a.ck_num_slots);
+    if (cc == 2 && c == 0) report(a.err, GDN_DEV_ERR_SLOT_OOB);
+    if (cc) continue;
+    Tconv* ch = reinterpret_cast<Tconv*>(a.ck_conv) + (size_t)cid * (a.W - 1) * a.C;
+    for (int j = 0; j < a.W - 1; ++j)
+      ch[(size_t)j * a.C + c] = from_f32<Tconv>(raw(P - p0 - (a.W - 1) + j));
+  }
+  float nw[kMaxW];
+#pragma unroll
+  for (int j = 0; j < kMaxW - 1; ++j)
+    if (j < a.W - 1) nw[j] = raw(len - (a.W - 1) + j);
+#pragma unroll
+  for (int j = 0; j < kMaxW - 1; ++j)
+    if (j < a.W - 1) hist[(size_t)j * a.C + c] = from_f32<Tconv>(nw[j]);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct WsLayout {
+  size_t q, k, v, g, beta, total;
+};
+
+WsLayout ws_layout(const gdn_dims& d, int64_t total) {
+  WsLayout w;
+  size_t off = 0;
+  w.q = off; off += align256(sizeof(float) * (size_t)total * d.hk * d.dk);
+  w.k = off; off += align256(sizeof(float) * (size_t)total * d.hk * d.dk);
+  w.v = off; off += align256(sizeof(float) * (size_t)total * d.hv * d.dv);
+  w.g = off; off += align256(sizeof(float) * (size_t)total * d.hv);
+  w.beta = off; off += align256(sizeof(float) * (size_t)total * d.hv);
+  w.total = off;
+  return w;
+}
+
+template <int DK, int DVT, typename Tact, typename Tconv>
+cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t s) {
+  if (a.total > 0) {
+    features_kernel<DK, Tact, Tconv><<<dim3((unsigned)a.total, (unsigned)a.hk), kThreads, 0, s>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  using L = ChunkSmem<DK, DVT>;
+  auto ck = chunk_kernel<DK, DVT, Tact>;
+  cudaError_t e = cudaFuncSetAttribute(ck, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::bytes);
+  if (e != cudaSuccess) return e;
+  const int n_tiles = (a.dv + DVT - 1) / DVT;
+  ck<<<dim3((unsigned)(a.hv * n_tiles), (unsigned)a.n_seq), kThreads, L::bytes, s>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  history_kernel<Tact, Tconv><<<dim3((unsigned)((a.C + kThreads - 1) / kThreads), (unsigned)a.n_seq),
+                                kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int DK, int DVT>
+cudaError_t dispatch_prefill(const PrefillArgs& a, int act, int cv, cudaStream_t s) {
+  if (act == GDN_F32 && cv == GDN_F32) return launch_prefill_t<DK, DVT, float, float>(a, s);
+  if (act == GDN_BF16 && cv == GDN_BF16)
+    return launch_prefill_t<DK, DVT, __nv_bfloat16, __nv_bfloat16>(a, s);
+  return launch_prefill_t<DK, DVT, __nv_bfloat16, float>(a, s);
+}
+
+}  // namespace
+}  // namespace gdn
+
+extern "C" size_t gdn_chunk_prefill_workspace_size(const gdn_dims* dims, int32_t n_seq,
+                                                   int64_t total_tokens) {
+  (void)n_seq;
+  if (gdn::check_dims(dims) != GDN_OK || total_tokens < 0) return 0;
+  return gdn::ws_layout(*dims, total_tokens).total;
+}
+
+extern "C" gdn_status gdn_chunk_prefill(const gdn_dims* dims, gdn_pool pool, gdn_pool ckpt,
+                                        const gdn_params* params, const int32_t* slot_ids,
+                                        const int32_t* cu_seqlens, const int64_t* start_pos,
+                                        int32_t n_seq, int64_t total_tokens,
+                                        const int32_t* ckpt_ids, int32_t max_ckpt,
+                                        int32_t ckpt_block, const void* qkv, const void* a,
+                                        const void* b, void* out, void* workspace,
+                                        size_t workspace_bytes, uint32_t* dev_err, void* stream) {
+  using namespace gdn;
+  gdn_status st = check_dims(dims);
+  if (st != GDN_OK) return st;
+  if (n_seq < 0 || total_tokens < 0 || max_ckpt < 0) return GDN_ERR_INVALID_ARG;
+  if (ckpt_block <= 0 || ckpt_block % kChunk) return GDN_ERR_INVALID_ARG;
+  if (n_seq == 0) return GDN_OK;
+  if (n_seq > 65535 || total_tokens > 2147483647LL) return GDN_ERR_UNSUPPORTED;
+  if ((st = check_pool(*dims, pool)) != GDN_OK) return st;
+  if (max_ckpt > 0 && (st = check_pool(*dims, ckpt)) != GDN_OK) return st;
+  if (!params || !params->conv_w || !params->A_log || !params->dt_bias) return GDN_ERR_INVALID_ARG;
+  if (!slot_ids || !cu_seqlens || !start_pos || (max_ckpt > 0 && !ckpt_ids))
+    return GDN_ERR_INVALID_ARG;
+  if (total_tokens > 0 && (!qkv || !a || !b || !out)) return GDN_ERR_INVALID_ARG;
+  const WsLayout wl = ws_layout(*dims, total_tokens);
+  if (total_tokens > 0 && (!workspace || workspace_bytes < wl.total || !aligned(workspace, 256)))
+    return GDN_ERR_INVALID_ARG;
+  if (dims->hv / dims->hk * dims->dv + 2 * dims->dk > 4096) return GDN_ERR_UNSUPPORTED;
+  PrefillArgs p = {};
+  p.ssm = pool.ssm;
+  p.conv = pool.conv;
+  p.num_slots = pool.num_slots;
+  p.ck_ssm = ckpt.ssm;
+  p.ck_conv = ckpt.conv;
+  p.ck_num_slots = max_ckpt > 0 ? ckpt.num_slots : 0;
+  p.conv_w = params->conv_w;
+  p.A_log = params->A_log;
+  p.dt_bias = params->dt_bias;
+  p.slot_ids = slot_ids;
+  p.cu_seqlens = cu_seqlens;
+  p.start_pos = start_pos;
+  p.n_seq = n_seq;
+  p.total = total_tokens;
+  p.ckpt_ids = ckpt_ids;
+  p.max_ckpt = max_ckpt;
+  p.ckpt_block = ckpt_block;
+  p.qkv = qkv;
+  p.a = a;
+  p.b = b;
+  p.out = out;
+  p.err = dev_err;
+  char* ws = reinterpret_cast<char*>(workspace);
+  p.ws_q = reinterpret_cast<float*>(ws + wl.q);
+  p.ws_k = reinterpret_cast<float*>(ws + wl.k);
+  p.ws_v = reinterpret_cast<float*>(ws + wl.v);
+  p.ws_g = reinterpret_cast<float*>(ws + wl.g);
+  p.ws_beta = reinterpret_cast<float*>(ws + wl.beta);
+  p.hk = dims->hk;
+  p.hv = dims->hv;
+  p.dk = dims->dk;
+  p.dv = dims->dv;
+  p.W = dims->conv_width;
+  p.C = (int32_t)channels(*dims);
+  p.G = dims->hv / dims->hk;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaErrorInvalidValue;
+  const int act = dims->act_dtype, cv = dims->conv_dtype;
+  switch (dims->dk) {
+    case 16: e = dispatch_prefill<16, 16>(p, act, cv, s); break;
+    case 64: e = dispatch_prefill<64, 64>(p, act, cv, s); break;
+    case 128: e = dispatch_prefill<128, 64>(p, act, cv, s); break;
+  }
+  count_launch(GDN_K_PREFILL);
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}

@@ -1,0 +1,157 @@
+// Slot copy-on-write, slot zeroing and speculative commit.
+//
+// TokenSpeed Qwen3.5 page, "Riesgo de correctitud: estado obsoleto": the
+// allocator hands out slot ids without clearing GPU memory, so a new working
+// slot is safe only after a copy from a clean checkpoint or an explicit zero.
+// "Scheduler dual": the spec_cache snapshot of the accepted draft step becomes
+// the working state (rollback = keep the working slot).
+//
+// All three are pure HBM streams: each CTA moves one 32 KiB piece of one slot
+// (SSM bytes followed by the conv history, viewed as one byte range) with
+// 128-bit accesses, 8 in flight per thread before the first store.
+#include "gdn_common.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kVec = 8;                              // uint4 per thread
+constexpr size_t kPiece = (size_t)kThreads * kVec * 16;  // bytes per CTA
+
+enum { MODE_COPY = 0, MODE_ZERO = 1, MODE_COMMIT = 2 };
+
+struct SlotOpArgs {
+  const char* src_ssm;
+  const char* src_conv;
+  int32_t src_n;
+  char* dst_ssm;
+  char* dst_conv;
+  int32_t dst_n;
+  size_t ssm_bytes;   // per slot
+  size_t conv_bytes;  // per slot
+  const int32_t* src_ids;     // copy: [n]; commit: spec ids [n][T]
+  const int32_t* dst_ids;     // [n]
+  const int32_t* accept_len;  // commit: [n]
+  int32_t T;
+  int32_t n;
+  uint32_t* err;
+};
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads) slot_op_kernel(SlotOpArgs a) {
+  const bool leader = blockIdx.x == 0 && threadIdx.x == 0;
+  const size_t total = a.ssm_bytes + a.conv_bytes;
+  for (int32_t r = blockIdx.y; r < a.n; r += gridDim.y) {
+    int32_t src = 0, dst;
+    if (MODE == MODE_COMMIT) {
+      const int32_t L = a.accept_len[r];
+      if (L < 0 || L > a.T) {
+        if (leader) report(a.err, GDN_DEV_ERR_SLOT_OOB);
+        continue;
+      }
+      if (L == 0) continue;
+      src = a.src_ids[(size_t)r * a.T + (L - 1)];
+    } else if (MODE == MODE_COPY) {
+      src = a.src_ids[r];
+    }
+    dst = a.dst_ids[r];
+    const int cd = slot_class(dst, a.dst_n);
+    const int cs = MODE == MODE_ZERO ? 0 : slot_class(src, a.src_n);
+    if (cd | cs) {
+      if ((cd == 2 || cs == 2) && leader) report(a.err, GDN_DEV_ERR_SLOT_OOB);
+      continue;
+    }
+    const size_t begin = (size_t)blockIdx.x * kPiece;
+    if (begin >= total) continue;
+    char* dssm = a.dst_ssm + (size_t)dst * a.ssm_bytes;
+    char* dconv = a.dst_conv + (size_t)dst * a.conv_bytes;
+    const char* sssm = a.src_ssm + (size_t)src * a.ssm_bytes;
+    const char* sconv = a.src_conv + (size_t)src * a.conv_bytes;
+    uint4 v[kVec];
+#pragma unroll
+    for (int i = 0; i < kVec; ++i) {
+      const size_t off = begin + ((size_t)i * kThreads + threadIdx.x) * 16;
+      v[i] = make_uint4(0, 0, 0, 0);
+      if (MODE != MODE_ZERO && off < total) {
+        const char* p = off < a.ssm_bytes ? sssm + off : sconv + (off - a.ssm_bytes);
+        v[i] = *reinterpret_cast<const uint4*>(p);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kVec; ++i) {
+      const size_t off = begin + ((size_t)i * kThreads + threadIdx.x) * 16;
+      if (off < total) {
+        char* p = off < a.ssm_bytes ? dssm + off : dconv + (off - a.ssm_bytes);
+        __stcs(reinterpret_cast<uint4*>(p), v[i]);
+      }
+    }
+  }
+}
+
+gdn_status launch_slot_op(int mode, const gdn_dims* dims, const gdn_pool* src,
+                          const gdn_pool& dst, const int32_t* src_ids,
+                          const int32_t* dst_ids, const int32_t* accept_len,
+                          int32_t T, int32_t n, uint32_t* dev_err, void* stream) {
+  gdn_status st = check_dims(dims);
+  if (st != GDN_OK) return st;
+  if (n < 0) return GDN_ERR_INVALID_ARG;
+  if (n == 0) return GDN_OK;
+  if ((st = check_pool(*dims, dst)) != GDN_OK) return st;
+  if (src && (st = check_pool(*dims, *src)) != GDN_OK) return st;
+  if (!dst_ids || (mode != MODE_ZERO && !src_ids)) return GDN_ERR_INVALID_ARG;
+  if (mode == MODE_COMMIT && (!accept_len || T <= 0)) return GDN_ERR_INVALID_ARG;
+  SlotOpArgs a;
+  a.ssm_bytes = ssm_slot_bytes(*dims);
+  a.conv_bytes = conv_slot_bytes(*dims);
+  if (a.ssm_bytes % 16 || a.conv_bytes % 16) return GDN_ERR_UNSUPPORTED;
+  a.src_ssm = src ? reinterpret_cast<const char*>(src->ssm) : nullptr;
+  a.src_conv = src ? reinterpret_cast<const char*>(src->conv) : nullptr;
+  a.src_n = src ? src->num_slots : 0;
+  a.dst_ssm = reinterpret_cast<char*>(dst.ssm);
+  a.dst_conv = reinterpret_cast<char*>(dst.conv);
+  a.dst_n = dst.num_slots;
+  a.src_ids = src_ids;
+  a.dst_ids = dst_ids;
+  a.accept_len = accept_len;
+  a.T = T;
+  a.n = n;
+  a.err = dev_err;
+  const size_t pieces = (a.ssm_bytes + a.conv_bytes + kPiece - 1) / kPiece;
+  dim3 grid((unsigned)pieces, (unsigned)(n < 65535 ? n : 65535));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (mode == MODE_COPY) {
+    slot_op_kernel<MODE_COPY><<<grid, kThreads, 0, s>>>(a);
+    count_launch(GDN_K_SLOT_COPY);
+  } else if (mode == MODE_ZERO) {
+    slot_op_kernel<MODE_ZERO><<<grid, kThreads, 0, s>>>(a);
+    count_launch(GDN_K_SLOT_ZERO);
+  } else {
+    slot_op_kernel<MODE_COMMIT><<<grid, kThreads, 0, s>>>(a);
+    count_launch(GDN_K_SPEC_COMMIT);
+  }
+  return launch_status();
+}
+
+}  // namespace
+}  // namespace gdn
+
+extern "C" gdn_status gdn_slot_copy(const gdn_dims* dims, gdn_pool src, gdn_pool dst,
+                                    const int32_t* src_ids, const int32_t* dst_ids,
+                                    int32_t n, uint32_t* dev_err, void* stream) {
+  return gdn::launch_slot_op(gdn::MODE_COPY, dims, &src, dst, src_ids, dst_ids,
+                             nullptr, 0, n, dev_err, stream);
+}
+
+extern "C" gdn_status gdn_slot_zero(const gdn_dims* dims, gdn_pool pool, const int32_t* ids,
+                                    int32_t n, uint32_t* dev_err, void* stream) {
+  return gdn::launch_slot_op(gdn::MODE_ZERO, dims, nullptr, pool, nullptr, ids, nullptr,
+                             0, n, dev_err, stream);
+}
+
+extern "C" gdn_status gdn_spec_commit(const gdn_dims* dims, gdn_pool spec, gdn_pool work,
+                                      const int32_t* spec_ids, const int32_t* accept_len,
+                                      const int32_t* slot_ids, int32_t B, int32_t T,
+                                      uint32_t* dev_err, void* stream) {
+  return gdn::launch_slot_op(gdn::MODE_COMMIT, dims, &spec, work, spec_ids, slot_ids,
+                             accept_len, T, B, dev_err, stream);
+}

@@ -1,0 +1,206 @@
+/*
+ * gdn.h - C ABI of libgdn, the GB300 (sm_103a) Gated DeltaNet slot-pool step.
+ *
+ * The library runs the per-layer linear-attention step of a hybrid-attention
+ * serving engine over a pool of recurrent-state slots.  Each slot holds one
+ * request's GDN state: an fp32 SSM state per V head and a short convolution
+ * history ("TokenSpeed" talk, section "为什么 Agentic 推理需要新推理引擎":
+ * linear-attention state = SSM state + conv state).  Slots are working slots
+ * (updated in place every decode step) or checkpoint slots (snapshot targets)
+ * ("TokenSpeed alcanza 580 tps con Qwen3.5-397B-A17B en GPU", section "Ciclo
+ * de vida de slots"); requests address them through integer slot ids (the
+ * same page, section "Scheduler dual": mamba_pool_indices).
+ *
+ * Conventions for every call:
+ *  - All pointers are DEVICE pointers owned by the caller.  The library keeps
+ *    no state besides launch counters, allocates nothing and is thread-safe.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are
+ *    asynchronous on it and never synchronise the host.
+ *  - The returned gdn_status covers host-side argument checks and the launch
+ *    itself.  Data-dependent problems (bad slot ids) are reported by OR-ing
+ *    GDN_DEV_ERR_* bits into *dev_err (device memory, may be NULL); read it
+ *    after synchronising the stream.  Kernels never trap.
+ *  - Pools are updated in place; inputs are never written; outputs must not
+ *    alias inputs.
+ *  - Slot id -1 is padding: the row is skipped and its outputs are written as
+ *    zeros.  Any other id outside [0, num_slots) is skipped the same way and
+ *    sets GDN_DEV_ERR_SLOT_OOB.
+ *
+ * Layouts (row-major, C order):
+ *   channels   C = 2*hk*dk + hv*dv, ordered q | k | v, each head-major
+ *   pool.ssm   float [num_slots][hv][dv][dk]   (S transposed: dk contiguous)
+ *   pool.conv  conv_dtype [num_slots][conv_width-1][C], oldest input first
+ *   params.conv_w  float [C][conv_width]  (index conv_width-1 = newest input)
+ *   params.A_log, params.dt_bias  float [hv]
+ *   V head h reads QK head h / (hv/hk).
+ *
+ * The per-token arithmetic is the Gated DeltaNet step (Yang, Kautz &
+ * Hatamizadeh, "Gated Delta Networks", ICLR 2025), which the pages name but
+ * do not write out:
+ *   y = SiLU(conv1d(history, x));  q,k,v = split(y)
+ *   q^ = q / sqrt(|q|^2 + 1e-6) / sqrt(dk);  k^ = k / sqrt(|k|^2 + 1e-6)
+ *   g = -exp(A_log) * softplus(a + dt_bias);  alpha = exp(g);  beta = sigmoid(b)
+ *   S <- alpha (I - beta k^ k^T) S + beta k^ v^T;  o = S^T q^  (updated S)
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* element types */
+#define GDN_F32 0
+#define GDN_BF16 1
+
+typedef enum {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad alignment, ... */
+  GDN_ERR_UNSUPPORTED = 2, /* shape / dtype combination not compiled in      */
+  GDN_ERR_CUDA = 3         /* the launch failed (cudaGetLastError)            */
+} gdn_status;
+
+/* bits OR-ed into *dev_err by the kernels */
+#define GDN_DEV_ERR_SLOT_OOB 1u /* a slot id (or accept length) out of range   */
+#define GDN_DEV_ERR_TIMEOUT 2u  /* a bounded inter-CTA wait gave up            */
+#define GDN_DEV_ERR_SEQLENS 4u  /* prefill: cu_seqlens / start_pos inconsistent */
+
+typedef struct {
+  int32_t hk;         /* QK heads                                   */
+  int32_t hv;         /* V heads, a multiple of hk                  */
+  int32_t dk;         /* key/query head dim: 16, 64 or 128          */
+  int32_t dv;         /* value head dim: 1..256                     */
+  int32_t conv_width; /* conv1d width W: 2..8                       */
+  int32_t act_dtype;  /* GDN_F32 or GDN_BF16: qkv, a, b and outputs */
+  int32_t conv_dtype; /* GDN_F32 or GDN_BF16: the conv history      */
+} gdn_dims;
+
+typedef struct {
+  float* ssm;        /* [num_slots][hv][dv][dk], 16-byte aligned */
+  void* conv;        /* [num_slots][conv_width-1][C]             */
+  int32_t num_slots;
+} gdn_pool;
+
+typedef struct {
+  const float* conv_w;  /* [C][conv_width] */
+  const float* A_log;   /* [hv]            */
+  const float* dt_bias; /* [hv]            */
+} gdn_params;
+
+/*
+ * Decode: one token per request, state updated in place in its working slot
+ * (TokenSpeed Qwen3.5 page, "Scheduler dual": the state is updated in place at
+ * every decode step).  For each request r with slot s = slot_ids[r]:
+ * causal conv1d update of the history, SiLU, q/k L2 norm, gates, gated delta
+ * rule on every V head, readout from the updated state.
+ *   slot_ids [B] int32, distinct (precondition)
+ *   qkv [B][C], a [B][hv], b [B][hv]  (act_dtype)
+ *   out [B][hv][dv] (act_dtype; bf16 is rounded to nearest even)
+ * B = 0 is a no-op.
+ */
+gdn_status gdn_decode_step(const gdn_dims* dims, gdn_pool pool,
+                           const gdn_params* params, const int32_t* slot_ids,
+                           int32_t B, const void* qkv, const void* a,
+                           const void* b, void* out, uint32_t* dev_err,
+                           void* stream);
+
+/*
+ * Speculative verify (TokenSpeed Qwen3.5 page, "Scheduler dual": spec_cache
+ * of per-step conv/SSM snapshots for rollback).  Request r runs its T draft
+ * tokens starting from working slot slot_ids[r], which is NOT modified; after
+ * draft t the full slot state (SSM + conv history) is written into spec slot
+ * spec_ids[r][t] of pool `spec` (-1: not written).
+ *   spec_ids [B][T] int32, distinct, disjoint from the working slots if the
+ *   two pools are the same memory (precondition); 1 <= T <= 16
+ *   qkv [B][T][C], a,b [B][T][hv], out [B][T][hv][dv]
+ */
+gdn_status gdn_spec_verify(const gdn_dims* dims, gdn_pool work, gdn_pool spec,
+                           const gdn_params* params, const int32_t* slot_ids,
+                           const int32_t* spec_ids, int32_t B, int32_t T,
+                           const void* qkv, const void* a, const void* b,
+                           void* out, uint32_t* dev_err, void* stream);
+
+/*
+ * Commit after verification (same section: rollback when verification
+ * rejects drafts).  accept_len[r] = L in 0..T: L >= 1 copies spec slot
+ * spec_ids[r][L-1] into working slot slot_ids[r]; L = 0 leaves the working
+ * slot as is (it already holds the pre-draft state).  L outside 0..T sets
+ * GDN_DEV_ERR_SLOT_OOB and skips the request.
+ */
+gdn_status gdn_spec_commit(const gdn_dims* dims, gdn_pool spec, gdn_pool work,
+                           const int32_t* spec_ids, const int32_t* accept_len,
+                           const int32_t* slot_ids, int32_t B, int32_t T,
+                           uint32_t* dev_err, void* stream);
+
+/*
+ * Chunked prefill with block-aligned checkpoints (TokenSpeed Qwen3.5 page,
+ * "Ciclo de vida de slots": a checkpoint becomes reusable once filled with
+ * clean state and attached to a block-aligned prefix node).  Sequence n owns
+ * tokens [cu_seqlens[n], cu_seqlens[n+1]) of the packed inputs; its first
+ * token sits at absolute position start_pos[n] and its state (read, then
+ * replaced by the final state) is slot slot_ids[n] of `pool`.  For every
+ * absolute position P with P % ckpt_block == 0 and
+ * start_pos[n] < P <= start_pos[n] + len, the state after token P-1 (SSM and
+ * the last W-1 raw inputs) is written to checkpoint slot
+ * ckpt_ids[n][P/ckpt_block - floor(start_pos[n]/ckpt_block) - 1] of `ckpt`
+ * (-1 or an index >= max_ckpt: skipped).  The intra-chunk work uses chunks
+ * of 64 tokens aligned to absolute positions.
+ *   cu_seqlens [n_seq+1] int32 (device): cu_seqlens[0] = 0, non-decreasing,
+ *     cu_seqlens[n_seq] = total_tokens; a sequence violating this (or with
+ *     start_pos < 0) is skipped and sets GDN_DEV_ERR_SEQLENS
+ *   start_pos [n_seq] int64 (device)
+ *   ckpt_ids [n_seq][max_ckpt] int32; ckpt_block a positive multiple of 64
+ *   qkv [total_tokens][C], a,b [total_tokens][hv], out [total_tokens][hv][dv]
+ *   workspace: >= gdn_chunk_prefill_workspace_size(...) bytes, 256-aligned
+ */
+size_t gdn_chunk_prefill_workspace_size(const gdn_dims* dims, int32_t n_seq,
+                                        int64_t total_tokens);
+gdn_status gdn_chunk_prefill(const gdn_dims* dims, gdn_pool pool, gdn_pool ckpt,
+                             const gdn_params* params, const int32_t* slot_ids,
+                             const int32_t* cu_seqlens, const int64_t* start_pos,
+                             int32_t n_seq, int64_t total_tokens,
+                             const int32_t* ckpt_ids, int32_t max_ckpt,
+                             int32_t ckpt_block, const void* qkv, const void* a,
+                             const void* b, void* out, void* workspace,
+                             size_t workspace_bytes, uint32_t* dev_err,
+                             void* stream);
+
+/*
+ * Copy-on-write from a clean slot (TokenSpeed Qwen3.5 page, "Riesgo de
+ * correctitud: estado obsoleto": a reused working slot is made safe by a copy
+ * from a checkpoint known to be clean, or by explicit zeroing).
+ * dst slot dst_ids[i] of `dst` <- src slot src_ids[i] of `src`, SSM and conv
+ * history, bit for bit.  The pools must have the same dims.  dst_ids must be
+ * distinct and, when src and dst are the same pool, disjoint from src_ids
+ * (precondition).
+ */
+gdn_status gdn_slot_copy(const gdn_dims* dims, gdn_pool src, gdn_pool dst,
+                         const int32_t* src_ids, const int32_t* dst_ids,
+                         int32_t n, uint32_t* dev_err, void* stream);
+
+/* Explicit zeroing of slots ids[0..n) (same section): SSM and conv <- +0. */
+gdn_status gdn_slot_zero(const gdn_dims* dims, gdn_pool pool,
+                         const int32_t* ids, int32_t n, uint32_t* dev_err,
+                         void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* gdn_status_string(int32_t status);
+
+/* Launch counters: how many kernels of each kind this process launched. */
+#define GDN_K_DECODE 0
+#define GDN_K_SPEC_VERIFY 1
+#define GDN_K_SLOT_COPY 2
+#define GDN_K_SLOT_ZERO 3
+#define GDN_K_SPEC_COMMIT 4
+#define GDN_K_PREFILL 5
+#define GDN_K_COUNT 8
+uint64_t gdn_launch_count(int32_t kernel);
+void gdn_launch_count_reset(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GDN_H */

@@ -1,0 +1,97 @@
+"""Shared test helpers: seeded set-ups for both sides and the comparisons.
+
+Tolerances (stated by the workload definition): bf16 outputs max relative-L2
+2e-3; fp32 state 1e-4 after one step and 5e-4 after 64 steps; fp32 outputs
+1e-4; slot gather/scatter, copy, zero and snapshot indexing bit-exact.
+Relative-L2 is taken per row (one request and V head) and the maximum over
+rows is compared.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from hybrid_linear_attention_gdn_gb300 import synth
+
+OUT_TOL_BF16 = 2e-3
+OUT_TOL_F32 = 1e-4
+STATE_TOL_1 = 1e-4
+STATE_TOL_64 = 5e-4
+PREFILL_TOL = 2e-3
+
+
+def out_tol(shape) -> float:
+    return OUT_TOL_BF16 if shape.act == "bf16" else OUT_TOL_F32
+
+
+def odims(shape) -> oracle.Dims:
+    return oracle.Dims(shape.hk, shape.hv, shape.dk, shape.dv, shape.w)
+
+
+def max_rel_l2(x, ref, axis_rows) -> float:
+    """max over rows of |x - ref| / |ref|; rows whose reference is 0 must match 0."""
+    x = np.asarray(x, np.float64)
+    ref = np.asarray(ref, np.float64)
+    x = x.reshape(-1, axis_rows)
+    ref = ref.reshape(-1, axis_rows)
+    num = np.linalg.norm(x - ref, axis=1)
+    den = np.linalg.norm(ref, axis=1)
+    zero = den == 0
+    assert np.all(num[zero] == 0), "rows that must be zero are not"
+    if np.all(zero):
+        return 0.0
+    return float((num[~zero] / den[~zero]).max())
+
+
+def to_np(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+class Setup:
+    """One layer: params, a device pool and its oracle twin (float64)."""
+
+    def __init__(self, shape, seed, num_slots=None, device="cuda"):
+        from hybrid_linear_attention_gdn_gb300 import Dims, LayerParams, StatePool
+        self.shape = shape
+        self.gen = synth.generator(seed)
+        conv_w, A_log, dt_bias = synth.params(shape, self.gen)
+        ssm, conv = synth.pool(shape, self.gen, num_slots)
+        self.dims = Dims.of(shape)
+        self.params = LayerParams(conv_w.to(device), A_log.to(device), dt_bias.to(device))
+        self.pool = StatePool(ssm.to(device), conv.to(device))
+        self.oparams = oracle.Params(conv_w.double().numpy(), A_log.double().numpy(),
+                                     dt_bias.double().numpy())
+        self.opool = oracle.Pool(ssm.double().numpy(), conv.double().numpy())
+        self.od = odims(shape)
+        self.device = device
+
+    def tokens(self, lead):
+        qkv, a, b = synth.tokens(self.shape, self.gen, lead)
+        return qkv, a, b
+
+
+def oracle_pool_of(pool) -> oracle.Pool:
+    return oracle.Pool(to_np(pool.ssm), to_np(pool.conv))
+
+
+def assert_pool_bits_equal(gpu_pool, opool: oracle.Pool, slots=None):
+    """Bit-exact comparison of a device pool against an oracle pool (the oracle
+    holds exact copies of the fp32/bf16 values)."""
+    ssm = gpu_pool.ssm.cpu()
+    conv = gpu_pool.conv.cpu()
+    ref_ssm = torch.from_numpy(opool.ssm).to(ssm.dtype)
+    ref_conv = torch.from_numpy(opool.conv).to(conv.dtype)
+    if slots is not None:
+        idx = torch.as_tensor(slots, dtype=torch.long)
+        ssm, conv, ref_ssm, ref_conv = ssm[idx], conv[idx], ref_ssm[idx], ref_conv[idx]
+    assert torch.equal(ssm.view(torch.int32), ref_ssm.view(torch.int32))
+    conv_iv = torch.int16 if conv.dtype == torch.bfloat16 else torch.int32
+    assert torch.equal(conv.view(conv_iv), ref_conv.view(conv_iv))
+
+
+def conv_bits_equal(gpu_conv: torch.Tensor, ref: np.ndarray) -> bool:
+    c = gpu_conv.cpu()
+    r = torch.from_numpy(np.ascontiguousarray(ref)).to(c.dtype)
+    iv = torch.int16 if c.dtype == torch.bfloat16 else torch.int32
+    return torch.equal(c.view(iv), r.view(iv))

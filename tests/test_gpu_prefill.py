@@ -1,0 +1,144 @@
+"""GPU chunked prefill with block-aligned checkpoints against the oracle's
+token-by-token recurrence."""
+import numpy as np
+import pytest
+import torch
+
+import hybrid_linear_attention_gdn_gb300 as gdn
+import oracle
+from hybrid_linear_attention_gdn_gb300 import StatePool, synth
+from helpers import PREFILL_TOL, Setup, conv_bits_equal, max_rel_l2, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _workspace(dims, n_seq, total):
+    nbytes = gdn.chunk_prefill_workspace_size(dims, n_seq, total)
+    return torch.empty(max(nbytes, 1), dtype=torch.uint8, device="cuda")
+
+
+def _run(st: Setup, ck: StatePool, ids, lens, starts, ck_ids, blk, qkv, a, b, err=None):
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32)
+    sp = torch.tensor(starts, dtype=torch.int64)
+    total = int(cu[-1])
+    out = torch.full((total, st.shape.hv, st.shape.dv), 3.0, dtype=st.shape.act_dtype, device="cuda")
+    ws = _workspace(st.dims, len(lens), total)
+    gdn.chunk_prefill(st.dims, st.pool, ck, st.params, ids.cuda(), cu.cuda(), sp.cuda(), total,
+                      ck_ids.cuda(), blk, qkv.cuda(), a.cuda(), b.cuda(), out, ws, err)
+    return out, cu, sp
+
+
+def _ck_pool(st, n):
+    p = StatePool.empty(st.dims, n, "cuda")
+    p.ssm.fill_(-5.0)
+    p.conv.fill_(9.0)
+    return p
+
+
+@pytest.mark.parametrize("shape,lens,starts,blk", [
+    (synth.TINY, [1, 37, 130, 300, 0], [0, 64, 100, 256, 5], 64),
+    (synth.QWEN, [70, 200, 513], [0, 128, 0], 256),
+    (synth.QWEN.replace(hk=2, hv=8, dk=64, dv=64), [129, 64, 3], [0, 192, 61], 64),
+], ids=["tiny", "qwen", "dk64_g4"])
+def test_prefill_vs_token_recurrence(cuda, shape, lens, starts, blk):
+    n = len(lens)
+    n_slots = 8 if shape.dk == 16 else 12
+    st = Setup(shape, seed=40, num_slots=n_slots)
+    ids = synth.slot_ids(n_slots, n, st.gen)
+    max_ck = max(1, max((s + L) // blk - s // blk for s, L in zip(starts, lens)))
+    n_ck = n * max_ck + 2
+    ck_ids = synth.slot_ids(n_ck, n * max_ck, st.gen).reshape(n, max_ck)
+    ck = _ck_pool(st, n_ck)
+    qkv, a, b = st.tokens((int(sum(lens)),))
+    out, cu, sp = _run(st, ck, ids, lens, starts, ck_ids, blk, qkv, a, b)
+    ock = oracle.Pool(np.full((n_ck, shape.hv, shape.dv, shape.dk), -5.0),
+                      np.full((n_ck, shape.w - 1, shape.channels), 9.0))
+    o_ref, err = oracle.prefill(st.od, st.opool, ock, st.oparams, ids.numpy(), cu.numpy(),
+                                sp.numpy(), ck_ids.numpy(), blk, to_np(qkv), to_np(a), to_np(b))
+    torch.cuda.synchronize()
+    assert err == 0
+    assert max_rel_l2(to_np(out), o_ref, shape.dv) <= PREFILL_TOL
+    used = ids.tolist()
+    assert max_rel_l2(to_np(st.pool.ssm[used]), st.opool.ssm[used], shape.dk) <= PREFILL_TOL
+    assert conv_bits_equal(st.pool.conv[used], st.opool.conv[used])
+    written = [i for i in range(n_ck) if not np.all(ock.ssm[i] == -5.0)]
+    assert len(written) == sum((s + L) // blk - s // blk for s, L in zip(starts, lens))
+    assert max_rel_l2(to_np(ck.ssm[written]), ock.ssm[written], shape.dk) <= PREFILL_TOL
+    assert conv_bits_equal(ck.conv, ock.conv)
+    assert torch.all(ck.ssm[[i for i in range(n_ck) if i not in written]] == -5.0)
+
+
+def test_prefill_four_by_8192_sampled_heads(cuda):
+    """The full 4 x 8192-token workload (chunk 64, checkpoints every 256) in
+    the launch shape the benchmark times; the oracle recomputes two sampled V
+    heads of two sequences token by token, with all their checkpoints."""
+    shape = synth.QWEN
+    st = Setup(shape, seed=41, num_slots=8)
+    lens, starts, blk = [8192] * 4, [0] * 4, 256
+    ids = torch.tensor([5, 1, 6, 2], dtype=torch.int32)
+    ck_ids = torch.arange(128, dtype=torch.int32).reshape(4, 32)
+    ck = _ck_pool(st, 128)
+    qkv, a, b = st.tokens((32768,))
+    ssm0, conv0 = st.opool.ssm.copy(), st.opool.conv.copy()
+    out, cu, sp = _run(st, ck, ids, lens, starts, ck_ids, blk, qkv, a, b)
+    torch.cuda.synchronize()
+    for n, heads in [(0, (16, 18)), (3, (30, 32))]:
+        t0, t1 = 8192 * n, 8192 * (n + 1)
+        opool = oracle.Pool(ssm0[[int(ids[n])]].copy(), conv0[[int(ids[n])]].copy())
+        ock = oracle.Pool(np.zeros((32, shape.hv, shape.dv, shape.dk)),
+                          np.zeros((32, shape.w - 1, shape.channels)))
+        o_ref, _ = oracle.prefill(st.od, opool, ock, st.oparams, [0], [0, 8192], [0],
+                                  np.arange(32, dtype=np.int32).reshape(1, 32), blk,
+                                  to_np(qkv[t0:t1]), to_np(a[t0:t1]), to_np(b[t0:t1]), heads=heads)
+        h0, h1 = heads
+        assert max_rel_l2(to_np(out[t0:t1, h0:h1]), o_ref[:, h0:h1], 128) <= PREFILL_TOL
+        assert max_rel_l2(to_np(st.pool.ssm[int(ids[n]), h0:h1]), opool.ssm[0, h0:h1], 128) <= PREFILL_TOL
+        cks = ck_ids[n].tolist()
+        assert max_rel_l2(to_np(ck.ssm[cks, h0:h1]), ock.ssm[:, h0:h1], 128) <= PREFILL_TOL
+        assert conv_bits_equal(ck.conv[cks], ock.conv)
+        assert conv_bits_equal(st.pool.conv[int(ids[n])], opool.conv[0])
+
+
+def test_prefill_resume_from_checkpoint_bit_exact(cuda):
+    """A sequence resumed at token 4096 from a copied checkpoint reaches the
+    from-scratch state bit for bit (same absolute chunk grid)."""
+    shape = synth.QWEN
+    st = Setup(shape, seed=42, num_slots=4)
+    ck = _ck_pool(st, 64)
+    qkv, a, b = st.tokens((8192,))
+    ck_ids = torch.arange(32, dtype=torch.int32).reshape(1, 32)
+    out_full, _, _ = _run(st, ck, torch.tensor([0], dtype=torch.int32), [8192], [0], ck_ids, 256,
+                          qkv, a, b)
+    # copy-on-write of the 4096 checkpoint (index 15) into slot 2, then resume
+    gdn.slot_copy(st.dims, ck, st.pool, torch.tensor([15], dtype=torch.int32, device="cuda"),
+                  torch.tensor([2], dtype=torch.int32, device="cuda"))
+    ck_ids2 = torch.arange(32, 48, dtype=torch.int32).reshape(1, 16)
+    out_res, _, _ = _run(st, ck, torch.tensor([2], dtype=torch.int32), [4096], [4096], ck_ids2, 256,
+                         qkv[4096:], a[4096:], b[4096:])
+    torch.cuda.synchronize()
+    assert torch.equal(out_res, out_full[4096:])
+    assert torch.equal(st.pool.ssm[2].view(torch.int32), st.pool.ssm[0].view(torch.int32))
+    assert torch.equal(st.pool.conv[2], st.pool.conv[0])
+    assert torch.equal(ck.ssm[32:48].view(torch.int32), ck.ssm[16:32].view(torch.int32))
+    assert torch.equal(ck.conv[32:48], ck.conv[16:32])
+
+
+def test_prefill_bad_ids_and_empty(cuda):
+    shape = synth.QWEN
+    st = Setup(shape, seed=43, num_slots=6)
+    ck = _ck_pool(st, 2)
+    lens, starts = [100, 300, 0, 64], [0, 0, 0, 0]
+    ids = torch.tensor([-1, 3, 4, 9], dtype=torch.int32)
+    ck_ids = torch.tensor([[0], [7], [1], [1]], dtype=torch.int32)
+    qkv, a, b = st.tokens((464,))
+    before = st.pool.ssm.clone(), st.pool.conv.clone()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, cu, sp = _run(st, ck, ids, lens, starts, ck_ids, 256, qkv, a, b, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == gdn.DEV_ERR_SLOT_OOB
+    assert torch.all(out[:100] == 0) and torch.all(out[400:] == 0)
+    assert not torch.all(out[100:400] == 0)
+    for s in [0, 1, 2, 4, 5]:  # the empty sequence leaves slot 4 unchanged
+        assert torch.equal(st.pool.ssm[s], before[0][s])
+        assert torch.equal(st.pool.conv[s], before[1][s])
+    assert torch.all(ck.ssm == -5.0)  # id 7 is out of range; nothing else was due

@@ -1,0 +1,101 @@
+"""GPU speculative verify (per-draft-step snapshots into the spec cache) and
+commit of the accepted snapshot, against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import hybrid_linear_attention_gdn_gb300 as gdn
+import oracle
+from hybrid_linear_attention_gdn_gb300 import StatePool, synth
+from helpers import (STATE_TOL_1, Setup, assert_pool_bits_equal, conv_bits_equal, max_rel_l2,
+                     out_tol, to_np)
+
+pytestmark = pytest.mark.gpu
+
+
+def _spec_pool(st: Setup, n):
+    """A spec cache filled with a sentinel pattern (stale data)."""
+    s = StatePool.empty(st.dims, n, "cuda")
+    s.ssm.fill_(12345.5)
+    s.conv.fill_(-77.0)
+    return s
+
+
+@pytest.mark.parametrize("shape,B,T", [(synth.TINY, 2, 5), (synth.QWEN, 16, 8), (synth.QWEN, 3, 4)],
+                         ids=["tiny", "qwen_b16_t8", "qwen_b3_t4"])
+def test_verify_then_commit(cuda, shape, B, T):
+    n_work = 8 if shape is synth.TINY else 40
+    st = Setup(shape, seed=30, num_slots=n_work)
+    ids = synth.slot_ids(n_work, B, st.gen)
+    spec = _spec_pool(st, B * T + 3)
+    spec_ids = synth.slot_ids(B * T + 3, B * T, st.gen).reshape(B, T)
+    qkv, a, b = st.tokens((B, T))
+    work_before = st.pool.ssm.clone(), st.pool.conv.clone()
+    out = torch.empty((B, T, shape.hv, shape.dv), dtype=shape.act_dtype, device="cuda")
+    gdn.spec_verify(st.dims, st.pool, spec, st.params, ids.cuda(), spec_ids.cuda(), qkv.cuda(),
+                    a.cuda(), b.cuda(), out)
+    ospec = oracle.Pool(np.full((B * T + 3, shape.hv, shape.dv, shape.dk), 12345.5),
+                        np.full((B * T + 3, shape.w - 1, shape.channels), -77.0))
+    o_ref, err = oracle.spec_verify(st.od, st.opool, ospec, st.oparams, ids.numpy(),
+                                    spec_ids.numpy(), to_np(qkv), to_np(a), to_np(b))
+    torch.cuda.synchronize()
+    assert err == 0
+    # the working slots are only read
+    assert torch.equal(st.pool.ssm, work_before[0]) and torch.equal(st.pool.conv, work_before[1])
+    assert max_rel_l2(to_np(out), o_ref, shape.dv) <= out_tol(shape)
+    sids = spec_ids.flatten().tolist()
+    assert max_rel_l2(to_np(spec.ssm[sids]), ospec.ssm[sids], shape.dv * shape.dk) <= STATE_TOL_1 * 5
+    assert conv_bits_equal(spec.conv[sids], ospec.conv[sids])
+    # unused spec slots keep their sentinel bytes
+    unused = [s for s in range(B * T + 3) if s not in sids]
+    assert torch.all(spec.ssm[unused] == 12345.5) and torch.all(spec.conv[unused] == -77.0)
+
+    # commit: accepted length uniform in 1..T (plus one explicit 0)
+    L = synth.accept_lengths(B, T, st.gen)
+    L[0] = 0
+    spec_snapshot = StatePool(spec.ssm.clone(), spec.conv.clone())
+    gdn.spec_commit(st.dims, spec, st.pool, spec_ids.cuda(), L.cuda(), ids.cuda())
+    # the oracle commit is a bit copy; apply it to the GPU's own snapshots
+    exp = oracle.Pool(to_np(work_before[0]), to_np(work_before[1]))
+    oracle.spec_commit(st.od, oracle.Pool(to_np(spec_snapshot.ssm), to_np(spec_snapshot.conv)),
+                       exp, spec_ids.numpy(), L.numpy(), ids.numpy())
+    torch.cuda.synchronize()
+    assert_pool_bits_equal(st.pool, exp)
+    # and against the oracle's own L decode steps (state within tolerance)
+    ref = oracle.Pool(to_np(work_before[0]), to_np(work_before[1]))
+    for r in range(B):
+        for t in range(int(L[r])):
+            oracle.decode_step(st.od, ref, st.oparams, ids[r:r + 1].numpy(), to_np(qkv[r:r + 1, t]),
+                               to_np(a[r:r + 1, t]), to_np(b[r:r + 1, t]))
+    used = ids.tolist()
+    assert max_rel_l2(to_np(st.pool.ssm[used]), ref.ssm[used], shape.dv * shape.dk) <= STATE_TOL_1 * 5
+    assert conv_bits_equal(st.pool.conv[used], ref.conv[used])
+
+
+def test_verify_bad_ids(cuda):
+    shape = synth.QWEN
+    st = Setup(shape, seed=31, num_slots=10)
+    B, T = 3, 2
+    ids = torch.tensor([4, -1, 10], dtype=torch.int32)
+    spec = _spec_pool(st, 6)
+    spec_ids = torch.tensor([[0, -1], [1, 2], [3, 9]], dtype=torch.int32)
+    qkv, a, b = st.tokens((B, T))
+    out = torch.empty((B, T, 32, 128), dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gdn.spec_verify(st.dims, st.pool, spec, st.params, ids.cuda(), spec_ids.cuda(), qkv.cuda(),
+                    a.cuda(), b.cuda(), out, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == gdn.DEV_ERR_SLOT_OOB
+    assert torch.all(out[1:] == 0)
+    # request 0 wrote snapshot 0 only; slots 1..5 untouched
+    assert not torch.all(spec.ssm[0] == 12345.5)
+    assert torch.all(spec.ssm[1:] == 12345.5)
+    L = torch.tensor([2, 1, 1], dtype=torch.int32)  # L=2 for request 0 reads spec_ids[0][1] = -1
+    gdn.spec_commit(st.dims, spec, st.pool, spec_ids.cuda(), L.cuda(), ids.cuda(), err)
+    L_bad = torch.tensor([5, 0, 0], dtype=torch.int32)
+    err2 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    before = st.pool.ssm.clone()
+    gdn.spec_commit(st.dims, spec, st.pool, spec_ids.cuda(), L_bad.cuda(), ids.cuda(), err2)
+    torch.cuda.synchronize()
+    assert int(err2.item()) == gdn.DEV_ERR_SLOT_OOB
+    assert torch.equal(st.pool.ssm, before)
