@@ -7,7 +7,7 @@ import torch
 import hybrid_linear_attention_gdn_gb300 as gdn
 import oracle
 from hybrid_linear_attention_gdn_gb300 import StatePool, synth
-from helpers import PREFILL_TOL, Setup, conv_bits_equal, max_rel_l2, to_np
+from helpers import PREFILL_TOL, assert_out_close, Setup, conv_bits_equal, max_rel_l2, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -57,7 +57,7 @@ def test_prefill_vs_token_recurrence(cuda, shape, lens, starts, blk):
                                 sp.numpy(), ck_ids.numpy(), blk, to_np(qkv), to_np(a), to_np(b))
     torch.cuda.synchronize()
     assert err == 0
-    assert max_rel_l2(to_np(out), o_ref, shape.dv) <= PREFILL_TOL
+    assert_out_close(out, o_ref, shape.dv, PREFILL_TOL)
     used = ids.tolist()
     assert max_rel_l2(to_np(st.pool.ssm[used]), st.opool.ssm[used], shape.dk) <= PREFILL_TOL
     assert conv_bits_equal(st.pool.conv[used], st.opool.conv[used])
@@ -91,7 +91,7 @@ def test_prefill_four_by_8192_sampled_heads(cuda):
                                   np.arange(32, dtype=np.int32).reshape(1, 32), blk,
                                   to_np(qkv[t0:t1]), to_np(a[t0:t1]), to_np(b[t0:t1]), heads=heads)
         h0, h1 = heads
-        assert max_rel_l2(to_np(out[t0:t1, h0:h1]), o_ref[:, h0:h1], 128) <= PREFILL_TOL
+        assert_out_close(out[t0:t1, h0:h1], o_ref[:, h0:h1], 128, PREFILL_TOL)
         assert max_rel_l2(to_np(st.pool.ssm[int(ids[n]), h0:h1]), opool.ssm[0, h0:h1], 128) <= PREFILL_TOL
         cks = ck_ids[n].tolist()
         assert max_rel_l2(to_np(ck.ssm[cks, h0:h1]), ock.ssm[:, h0:h1], 128) <= PREFILL_TOL
