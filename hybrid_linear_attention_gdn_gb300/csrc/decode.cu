@@ -24,6 +24,10 @@
 // q/k history after waiting - after its own state work, when the others
 // have long arrived.  No distributed shared memory and no multicast is used.
 #include "gdn_common.cuh"
+#include "decode_tma.cuh"
+
+#include <cstdlib>
+#include <cstring>
 
 namespace gdn {
 namespace {
@@ -502,6 +506,23 @@ int choose_nit(int dk, int dv, int units, int G, bool verify) {
   return nit;
 }
 
+// Decode kernel choice.  The persistent TMA-fed kernel needs at least one work
+// item (request x QK head) per SM; below that, the per-head kernel with row
+// parts spread over a cluster keeps more bytes in flight.  GDN_DECODE_PATH
+// ("tma" / "rows") overrides the choice, for measurement.
+bool use_tma_decode(const gdn_dims& d, int32_t B, const void* qkv, const gdn_params& p) {
+  static int forced = [] {
+    const char* e = std::getenv("GDN_DECODE_PATH");
+    if (!e) return 0;
+    if (!std::strcmp(e, "tma")) return 1;
+    if (!std::strcmp(e, "rows")) return 2;
+    return 0;
+  }();
+  if (!decode_tma_supported(d, qkv, p)) return false;
+  if (forced) return forced == 1;
+  return (long)B * d.hk >= sm_count();
+}
+
 gdn_status run_step(bool verify, const gdn_dims* dims, const gdn_pool& work, const gdn_pool* spec,
                     const gdn_params* params, const int32_t* slot_ids, const int32_t* spec_ids,
                     int32_t B, int32_t T, const void* qkv, const void* a, const void* b, void* out,
@@ -518,6 +539,12 @@ gdn_status run_step(bool verify, const gdn_dims* dims, const gdn_pool& work, con
   if (!slot_ids || !qkv || !a || !b || !out || (verify && !spec_ids)) return GDN_ERR_INVALID_ARG;
   const int G = dims->hv / dims->hk;
   if (G > 8) return GDN_ERR_UNSUPPORTED;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (!verify && use_tma_decode(*dims, B, qkv, *params)) {
+    cudaError_t e = decode_tma_launch(*dims, work, *params, slot_ids, B, qkv, a, b, out, dev_err, cs);
+    if (e == cudaSuccess) count_launch(GDN_K_DECODE);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+  }
   StepArgs s = {};
   s.ssm = work.ssm;
   s.conv = work.conv;
@@ -551,7 +578,6 @@ gdn_status run_step(bool verify, const gdn_dims* dims, const gdn_pool& work, con
   if (!verify && G * s.P > 8) return GDN_ERR_UNSUPPORTED;
   if ((long)dims->hv * s.P > 2147483647L) return GDN_ERR_UNSUPPORTED;
   const int act = dims->act_dtype, cv = dims->conv_dtype;
-  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaErrorInvalidValue;
   switch (dims->dk) {
     case 16: e = dispatch_dtype<16, 1>(verify, s, act, cv, cs); break;
@@ -565,7 +591,7 @@ gdn_status run_step(bool verify, const gdn_dims* dims, const gdn_pool& work, con
                      : dispatch_dtype<128, 4>(verify, s, act, cv, cs);
       break;
   }
-  count_launch(verify ? GDN_K_SPEC_VERIFY : GDN_K_DECODE);
+  if (e == cudaSuccess) count_launch(verify ? GDN_K_SPEC_VERIFY : GDN_K_DECODE);
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

@@ -1,0 +1,371 @@
+// Persistent, TMA-fed GDN decode step (dk = 128, conv width 4).
+//
+// One CTA per SM walks a static list of work items.  An item is one request
+// and one QK head hq together with the G V heads that read it: G*dv state rows
+// of 512 bytes, contiguous in the pool ([slot][hv][dv][dk]), plus the q/k
+// channels of hq and the v channels of its V heads.  Owning the whole group
+// means the CTA alone reads and rewrites that slice of the conv history, so no
+// other CTA ever touches it: no cluster, no cross-CTA ordering.
+//
+// Warp roles:
+//   warp 8 (producer, one lane): streams each item's "bundle" (conv history,
+//     activations, conv weights; 15 bulk copies) and then its state rows in
+//     16 KiB chunks (32 rows) through a ring of STAGES shared-memory buffers
+//     with cp.async.bulk, completion tracked by mbarriers (full/empty).
+//   warps 0-7 (consumers): conv1d + SiLU, L2 norms and gates from the bundle,
+//     then, chunk by chunk, the gated delta rule on 32 rows (4 rows per warp,
+//     8 lanes per row, 3-level shuffle reductions), streaming the updated rows
+//     straight to HBM with 128-bit stores.
+// The producer runs up to STAGES chunks (and the next bundle) ahead, so HBM
+// reads continue while the consumers are in an item's prologue.
+//
+// Every mbarrier wait is bounded (1 s); on a timeout the CTA sets
+// GDN_DEV_ERR_TIMEOUT, stops issuing, waits (bounded) for the copies it has in
+// flight and returns.
+#include "gdn_common.cuh"
+#include "decode_tma.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kCW = 8;             // consumer warps
+constexpr int kCons = kCW * 32;    // consumer threads
+constexpr int kThr = kCons + 32;   // + producer warp
+constexpr int kDK = 128;
+constexpr int kLPR = kDK / 16;     // lanes per state row
+constexpr int kRows = 32;          // state rows per ring stage
+constexpr int kStageFloats = kRows * kDK;
+constexpr uint32_t kStageBytes = kStageFloats * sizeof(float);
+constexpr int kW = 4;              // conv width
+constexpr int kMaxGR = 256;        // G * dv rows per item, at most
+constexpr int kMaxCh = 2 * kDK + kMaxGR;
+constexpr int kBarCons = 1;        // named barrier of the consumer warps
+
+template <typename Tact, typename Tconv, int STAGES>
+struct __align__(128) TmaSmem {
+  float ring[STAGES][kStageFloats];
+  struct Bundle {
+    Tconv hist[kW - 1][kMaxCh];  // [q | k | v of the group] per history row
+    Tact x[kMaxCh];
+    float w[kMaxCh * kW];
+  } bundle[2];
+  float sy[kMaxCh];    // conv + SiLU output: q, k, v of the group
+  float so[kMaxGR];    // readout of the group's rows
+  float sred[3][kCW];
+  float sgate[2][8];   // alpha, beta per V head of the group
+  float snorm[4];      // rq, rk, k^.q^
+  uint64_t full[STAGES], empty[STAGES], bfull[2], bempty[2];
+  int abort;
+};
+
+struct TmaArgs {
+  float* ssm;
+  void* conv;
+  int32_t num_slots;
+  const float* conv_w;
+  const float* A_log;
+  const float* dt_bias;
+  const int32_t* slot_ids;
+  const void* qkv;
+  const void* a;
+  const void* b;
+  void* out;
+  uint32_t* err;
+  int32_t hk, hv, dv, C, G, n_items;
+};
+
+template <typename Tact, typename Tconv, int STAGES>
+__global__ void __launch_bounds__(kThr, 1) decode_tma_kernel(const TmaArgs a) {
+  using SM = TmaSmem<Tact, Tconv, STAGES>;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  SM& S = *reinterpret_cast<SM*>(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int GR = a.G * a.dv;           // rows per item
+  const int nchunks = GR / kRows;
+  const int nch = 2 * kDK + GR;        // conv channels per item
+  volatile int* abort_flag = &S.abort;
+
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], kCW);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&S.bfull[s], 1);
+      mbar_init(&S.bempty[s], kCons);
+    }
+    S.abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kCW) {
+    // ------------------------------------------------------------ producer
+    if (lane != 0) return;
+    const uint32_t esz_c = sizeof(Tconv), esz_a = sizeof(Tact);
+    const uint32_t bundle_bytes = (kW - 1) * nch * esz_c + nch * esz_a + nch * kW * 4;
+    uint32_t n = 0, vk = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
+      const int r = item / a.hk, hq = item % a.hk;
+      const int32_t slot = a.slot_ids[r];
+      if (slot_class(slot, a.num_slots)) continue;
+      if (*abort_flag) break;
+      const int bb = vk & 1;
+      if (!mbar_wait(&S.bempty[bb], ((vk >> 1) & 1) ^ 1)) { ok = false; break; }
+      mbar_arrive_expect_tx(&S.bfull[bb], bundle_bytes);
+      typename SM::Bundle& B = S.bundle[bb];
+      const size_t cq = (size_t)hq * kDK, ck = (size_t)a.hk * kDK + cq,
+                   cv = 2 * (size_t)a.hk * kDK + (size_t)hq * GR;
+      const Tconv* hist = reinterpret_cast<const Tconv*>(a.conv) + (size_t)slot * (kW - 1) * a.C;
+      for (int j = 0; j < kW - 1; ++j) {
+        bulk_g2s(&B.hist[j][0], hist + (size_t)j * a.C + cq, kDK * esz_c, &S.bfull[bb]);
+        bulk_g2s(&B.hist[j][kDK], hist + (size_t)j * a.C + ck, kDK * esz_c, &S.bfull[bb]);
+        bulk_g2s(&B.hist[j][2 * kDK], hist + (size_t)j * a.C + cv, GR * esz_c, &S.bfull[bb]);
+      }
+      const Tact* x = reinterpret_cast<const Tact*>(a.qkv) + (size_t)r * a.C;
+      bulk_g2s(&B.x[0], x + cq, kDK * esz_a, &S.bfull[bb]);
+      bulk_g2s(&B.x[kDK], x + ck, kDK * esz_a, &S.bfull[bb]);
+      bulk_g2s(&B.x[2 * kDK], x + cv, GR * esz_a, &S.bfull[bb]);
+      bulk_g2s(&B.w[0], a.conv_w + cq * kW, kDK * kW * 4, &S.bfull[bb]);
+      bulk_g2s(&B.w[kDK * kW], a.conv_w + ck * kW, kDK * kW * 4, &S.bfull[bb]);
+      bulk_g2s(&B.w[2 * kDK * kW], a.conv_w + cv * kW, GR * kW * 4, &S.bfull[bb]);
+      ++vk;
+      const float* src = a.ssm + ((size_t)slot * a.hv + (size_t)hq * a.G) * a.dv * kDK;
+      for (int c = 0; c < nchunks; ++c, ++n) {
+        const int st = n % STAGES;
+        if (*abort_flag || !mbar_wait(&S.empty[st], ((n / STAGES) & 1) ^ 1)) { ok = false; break; }
+        mbar_arrive_expect_tx(&S.full[st], kStageBytes);
+        bulk_g2s(S.ring[st], src + (size_t)c * kStageFloats, kStageBytes, &S.full[st]);
+      }
+    }
+    if (!ok || *abort_flag) {
+      *abort_flag = 1;
+      report(a.err, GDN_DEV_ERR_TIMEOUT);
+      // let the copies already issued land before the CTA's memory goes away
+      const uint32_t first = n > (uint32_t)STAGES ? n - STAGES : 0;
+      for (uint32_t m = first; m < n; ++m) mbar_wait(&S.full[m % STAGES], (m / STAGES) & 1);
+      for (uint32_t m = vk > 2 ? vk - 2 : 0; m < vk; ++m) mbar_wait(&S.bfull[m & 1], (m >> 1) & 1);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int seg = lane % kLPR;
+  const int rloc = warp * (32 / kLPR) + lane / kLPR;  // row within a chunk
+  uint32_t n = 0, vk = 0;
+  int item = blockIdx.x;
+  int32_t slot_next = item < a.n_items ? a.slot_ids[item / a.hk] : -1;
+  for (; item < a.n_items; item += gridDim.x) {
+    const int r = item / a.hk, hq = item % a.hk;
+    const int32_t slot = slot_next;
+    const int nitem = item + gridDim.x;
+    if (nitem < a.n_items) slot_next = a.slot_ids[nitem / a.hk];
+    Tact* out = reinterpret_cast<Tact*>(a.out) + ((size_t)r * a.hv + (size_t)hq * a.G) * a.dv;
+    const int cls = slot_class(slot, a.num_slots);
+    if (cls) {
+      if (cls == 2 && hq == 0 && tid == 0) report(a.err, GDN_DEV_ERR_SLOT_OOB);
+      for (int i = tid; i < GR; i += kCons) out[i] = from_f32<Tact>(0.f);
+      continue;
+    }
+    const int bb = vk & 1;
+    if (!*abort_flag && !mbar_wait(&S.bfull[bb], (vk >> 1) & 1)) *abort_flag = 1;
+    named_sync(kBarCons, kCons);
+    if (*abort_flag) break;
+    const typename SM::Bundle& B = S.bundle[bb];
+    // conv1d + SiLU; the old history is in the bundle, so the new one can be
+    // written at once (this CTA is the only one touching these channels)
+    Tconv* hist = reinterpret_cast<Tconv*>(a.conv) + (size_t)slot * (kW - 1) * a.C;
+    for (int i = tid; i < nch; i += kCons) {
+      const float h0 = to_f32(B.hist[0][i]), h1 = to_f32(B.hist[1][i]), h2 = to_f32(B.hist[2][i]);
+      const float xv = to_f32(B.x[i]);
+      const float4 w = *reinterpret_cast<const float4*>(&B.w[i * kW]);
+      float acc = w.x * h0;
+      acc = fmaf(w.y, h1, acc);
+      acc = fmaf(w.z, h2, acc);
+      acc = fmaf(w.w, xv, acc);
+      S.sy[i] = silu_f(acc);
+      const size_t c = i < kDK ? (size_t)hq * kDK + i
+                     : i < 2 * kDK ? (size_t)a.hk * kDK + (size_t)hq * kDK + (i - kDK)
+                                   : 2 * (size_t)a.hk * kDK + (size_t)hq * GR + (i - 2 * kDK);
+      hist[c] = B.hist[1][i];
+      hist[a.C + c] = B.hist[2][i];
+      hist[2 * (size_t)a.C + c] = from_f32<Tconv>(xv);
+    }
+    if (tid < a.G) {
+      const int h = hq * a.G + tid;
+      const float av = to_f32(reinterpret_cast<const Tact*>(a.a)[(size_t)r * a.hv + h]);
+      const float bv = to_f32(reinterpret_cast<const Tact*>(a.b)[(size_t)r * a.hv + h]);
+      S.sgate[0][tid] = gate_alpha(a.A_log[h], a.dt_bias[h], av);
+      S.sgate[1][tid] = sigmoid_f(bv);
+    }
+    named_sync(kBarCons, kCons);
+    mbar_arrive(&S.bempty[bb]);
+    ++vk;
+    // L2 norms of q and k, and k^.q^
+    {
+      float pq = 0.f, pk = 0.f, pqk = 0.f;
+      if (tid < kDK) {
+        const float q = S.sy[tid], k = S.sy[kDK + tid];
+        pq = q * q;
+        pk = k * k;
+        pqk = q * k;
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        pq += __shfl_xor_sync(0xffffffffu, pq, o);
+        pk += __shfl_xor_sync(0xffffffffu, pk, o);
+        pqk += __shfl_xor_sync(0xffffffffu, pqk, o);
+      }
+      if (lane == 0) {
+        S.sred[0][warp] = pq;
+        S.sred[1][warp] = pk;
+        S.sred[2][warp] = pqk;
+      }
+      named_sync(kBarCons, kCons);
+      if (tid == 0) {
+        float x = 0.f, y = 0.f, z = 0.f;
+        for (int w = 0; w < kCW; ++w) {
+          x += S.sred[0][w];
+          y += S.sred[1][w];
+          z += S.sred[2][w];
+        }
+        const float rq = rsqrtf(x + kNormEps) * rsqrtf((float)kDK);
+        const float rk = rsqrtf(y + kNormEps);
+        S.snorm[0] = rq;
+        S.snorm[1] = rk;
+        S.snorm[2] = z * rq * rk;
+      }
+      named_sync(kBarCons, kCons);
+    }
+    const float rq = S.snorm[0], rk = S.snorm[1], kq = S.snorm[2];
+    float4 kk[4], qq[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int col = c * 4 * kLPR + seg * 4;
+      const float4 k4 = *reinterpret_cast<const float4*>(&S.sy[kDK + col]);
+      const float4 q4 = *reinterpret_cast<const float4*>(&S.sy[col]);
+      kk[c] = make_float4(k4.x * rk, k4.y * rk, k4.z * rk, k4.w * rk);
+      qq[c] = make_float4(q4.x * rq, q4.y * rq, q4.z * rq, q4.w * rq);
+    }
+    float* dst_base = a.ssm + ((size_t)slot * a.hv + (size_t)hq * a.G) * a.dv * kDK;
+    for (int c = 0; c < nchunks; ++c, ++n) {
+      const int st = n % STAGES;
+      if (!*abort_flag && !mbar_wait(&S.full[st], (n / STAGES) & 1)) *abort_flag = 1;
+      if (*abort_flag) continue;
+      const int grow = c * kRows + rloc;  // row within the group
+      const int g = grow / a.dv;
+      const float alpha = S.sgate[0][g], beta = S.sgate[1][g];
+      const float* srow = S.ring[st] + rloc * kDK;
+      float4 s4[4];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc)
+        s4[cc] = *reinterpret_cast<const float4*>(srow + cc * 4 * kLPR + seg * 4);
+      float dk_ = 0.f, dq_ = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        dk_ += s4[cc].x * kk[cc].x + s4[cc].y * kk[cc].y + s4[cc].z * kk[cc].z + s4[cc].w * kk[cc].w;
+        dq_ += s4[cc].x * qq[cc].x + s4[cc].y * qq[cc].y + s4[cc].z * qq[cc].z + s4[cc].w * qq[cc].w;
+      }
+      __syncwarp();  // every lane has consumed its part of the stage
+      if (lane == 0) mbar_arrive(&S.empty[st]);  // the producer may refill it
+#pragma unroll
+      for (int o = kLPR / 2; o; o >>= 1) {
+        dk_ += __shfl_xor_sync(0xffffffffu, dk_, o);
+        dq_ += __shfl_xor_sync(0xffffffffu, dq_, o);
+      }
+      const float bu = beta * (S.sy[2 * kDK + grow] - alpha * dk_);
+      float4* drow = reinterpret_cast<float4*>(dst_base + (size_t)grow * kDK);
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        float4 v = s4[cc];
+        v.x = fmaf(bu, kk[cc].x, alpha * v.x);
+        v.y = fmaf(bu, kk[cc].y, alpha * v.y);
+        v.z = fmaf(bu, kk[cc].z, alpha * v.z);
+        v.w = fmaf(bu, kk[cc].w, alpha * v.w);
+        st_stream(drow + (cc * 4 * kLPR + seg * 4) / 4, v);
+      }
+      if (seg == 0) S.so[grow] = fmaf(bu, kq, alpha * dq_);
+    }
+    named_sync(kBarCons, kCons);
+    if (*abort_flag) break;
+    for (int i = tid; i < GR; i += kCons) out[i] = from_f32<Tact>(S.so[i]);
+  }
+  if (*abort_flag && tid == 0) report(a.err, GDN_DEV_ERR_TIMEOUT);
+}
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!cached[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 1;
+  }
+  return cached[dev];
+}
+
+template <typename Tact, typename Tconv, int STAGES>
+cudaError_t launch_tma(const TmaArgs& a, cudaStream_t s) {
+  using SM = TmaSmem<Tact, Tconv, STAGES>;
+  auto k = decode_tma_kernel<Tact, Tconv, STAGES>;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(SM));
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const int grid = a.n_items < sm_count() ? a.n_items : sm_count();
+  k<<<grid, kThr, sizeof(SM), s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool decode_tma_supported(const gdn_dims& d, const void* qkv, const gdn_params& p) {
+  const size_t ea = dtype_size(d.act_dtype), ec = dtype_size(d.conv_dtype);
+  const int64_t C = channels(d);
+  const int G = d.hv / d.hk;
+  if (d.dk != kDK || d.conv_width != kW) return false;
+  if (d.dv % kRows || G * d.dv > kMaxGR) return false;
+  if ((C * ea) % 16 || (C * ec) % 16) return false;
+  if ((kDK * ea) % 16 || (kDK * ec) % 16 || ((size_t)G * d.dv * ea) % 16 || ((size_t)G * d.dv * ec) % 16)
+    return false;
+  if (!aligned(qkv, 16) || !aligned(p.conv_w, 16)) return false;
+  return true;
+}
+
+cudaError_t decode_tma_launch(const gdn_dims& d, const gdn_pool& pool, const gdn_params& p,
+                              const int32_t* slot_ids, int32_t B, const void* qkv, const void* av,
+                              const void* bv, void* out, uint32_t* dev_err, cudaStream_t s) {
+  TmaArgs a;
+  a.ssm = pool.ssm;
+  a.conv = pool.conv;
+  a.num_slots = pool.num_slots;
+  a.conv_w = p.conv_w;
+  a.A_log = p.A_log;
+  a.dt_bias = p.dt_bias;
+  a.slot_ids = slot_ids;
+  a.qkv = qkv;
+  a.a = av;
+  a.b = bv;
+  a.out = out;
+  a.err = dev_err;
+  a.hk = d.hk;
+  a.hv = d.hv;
+  a.dv = d.dv;
+  a.C = (int32_t)channels(d);
+  a.G = d.hv / d.hk;
+  a.n_items = B * d.hk;
+  constexpr int ST = 10;
+  if (d.act_dtype == GDN_BF16 && d.conv_dtype == GDN_BF16)
+    return launch_tma<__nv_bfloat16, __nv_bfloat16, ST>(a, s);
+  if (d.act_dtype == GDN_BF16) return launch_tma<__nv_bfloat16, float, ST>(a, s);
+  return launch_tma<float, float, ST>(a, s);
+}
+
+}  // namespace gdn

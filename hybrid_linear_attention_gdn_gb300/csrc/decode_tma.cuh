@@ -1,0 +1,12 @@
+// Persistent TMA-fed decode path (dk = 128, conv width 4); see decode_tma.cu.
+#pragma once
+#include "gdn_common.cuh"
+
+namespace gdn {
+// True when the shape, dtypes and pointer alignment fit the TMA-fed kernel.
+bool decode_tma_supported(const gdn_dims& d, const void* qkv, const gdn_params& p);
+cudaError_t decode_tma_launch(const gdn_dims& d, const gdn_pool& pool, const gdn_params& p,
+                              const int32_t* slot_ids, int32_t B, const void* qkv, const void* a,
+                              const void* b, void* out, uint32_t* dev_err, cudaStream_t s);
+int sm_count();
+}  // namespace gdn

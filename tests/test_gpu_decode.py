@@ -95,6 +95,35 @@ def test_padding_and_out_of_range_ids(cuda):
     _check_state(st, [5, 3], STATE_TOL_1)
 
 
+@pytest.mark.parametrize("shape,B", [
+    (synth.QWEN, 20),
+    (synth.QWEN.replace(act="f32", conv="f32", hk=4, hv=8), 40),
+    (synth.QWEN.replace(conv="f32", hk=4, hv=16, dv=64), 40),
+], ids=["qwen_b20", "f32_g2", "bf16_f32hist_g4_dv64"])
+def test_persistent_path_with_padding(cuda, shape, B):
+    """Batches with at least one (request, QK head) item per SM run the
+    persistent TMA-fed kernel; padding and out-of-range ids inside it."""
+    n_slots = B + 6
+    st = Setup(shape, seed=10, num_slots=n_slots)
+    ids = synth.slot_ids(n_slots, B, st.gen)
+    ids[3] = -1
+    ids[B - 2] = n_slots + 3
+    err_dev = torch.zeros(1, dtype=torch.int32, device="cuda")
+    before = st.pool.ssm.clone(), st.pool.conv.clone()
+    for step in range(3):
+        qkv, a, b = st.tokens((B,))
+        out, o_ref, err = _step(st, ids, qkv, a, b, dev_err=err_dev)
+        assert err == oracle.ERR_SLOT_OOB
+        assert int(err_dev.item()) == gdn.DEV_ERR_SLOT_OOB
+        assert torch.all(out[3] == 0) and torch.all(out[B - 2] == 0)
+        assert_out_close(out, o_ref, shape.dv, out_tol(shape))
+    valid = [int(s) for s in ids.tolist() if 0 <= s < n_slots]
+    others = [s for s in range(n_slots) if s not in valid]
+    assert torch.equal(st.pool.ssm[others], before[0][others])
+    assert torch.equal(st.pool.conv[others], before[1][others])
+    _check_state(st, valid, STATE_TOL_64)
+
+
 def test_batch_zero_is_noop(cuda):
     st = Setup(synth.TINY, seed=4)
     before = st.pool.ssm.clone()
