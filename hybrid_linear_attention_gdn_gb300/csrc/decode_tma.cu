@@ -294,19 +294,6 @@ __global__ void __launch_bounds__(kThr, 1) decode_tma_kernel(const TmaArgs a) {
   if (*abort_flag && tid == 0) report(a.err, GDN_DEV_ERR_TIMEOUT);
 }
 
-int sm_count() {
-  static int cached[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) dev = 0;
-  if (!cached[dev]) {
-    int n = 0;
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    cached[dev] = n > 0 ? n : 1;
-  }
-  return cached[dev];
-}
-
 template <typename Tact, typename Tconv, int STAGES>
 cudaError_t launch_tma(const TmaArgs& a, cudaStream_t s) {
   using SM = TmaSmem<Tact, Tconv, STAGES>;
@@ -325,6 +312,19 @@ cudaError_t launch_tma(const TmaArgs& a, cudaStream_t s) {
 }
 
 }  // namespace
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!cached[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 1;
+  }
+  return cached[dev];
+}
 
 bool decode_tma_supported(const gdn_dims& d, const void* qkv, const gdn_params& p) {
   const size_t ea = dtype_size(d.act_dtype), ec = dtype_size(d.conv_dtype);
