@@ -506,10 +506,10 @@ int choose_nit(int dk, int dv, int units, int G, bool verify) {
   return nit;
 }
 
-// Decode kernel choice.  The persistent TMA-fed kernel needs at least one work
-// item (request x QK head) per SM; below that, the per-head kernel with row
-// parts spread over a cluster keeps more bytes in flight.  GDN_DECODE_PATH
-// ("tma" / "rows") overrides the choice, for measurement.
+// Decode kernel choice.  The persistent TMA-fed kernel is at least as fast as
+// the per-head kernel at every batch measured (1..256) on the Qwen3.5-shaped
+// layer, so it takes every shape it supports (dk 128, width 4, G*dv <= 256).
+// GDN_DECODE_PATH ("tma" / "rows") overrides the choice, for measurement.
 bool use_tma_decode(const gdn_dims& d, int32_t B, const void* qkv, const gdn_params& p) {
   static int forced = [] {
     const char* e = std::getenv("GDN_DECODE_PATH");
@@ -519,8 +519,9 @@ bool use_tma_decode(const gdn_dims& d, int32_t B, const void* qkv, const gdn_par
     return 0;
   }();
   if (!decode_tma_supported(d, qkv, p)) return false;
+  (void)B;
   if (forced) return forced == 1;
-  return (long)B * d.hk >= sm_count();
+  return true;
 }
 
 gdn_status run_step(bool verify, const gdn_dims* dims, const gdn_pool& work, const gdn_pool* spec,
