@@ -51,8 +51,8 @@ def test_tiny_eight_steps(cuda):
 
 @pytest.mark.parametrize("B", [1, 3, 8, 16, 64])
 def test_qwen_one_step(cuda, B):
-    """Qwen3.5-shaped layer (16 QK / 32 V heads, dk=dv=128, bf16): every launch
-    shape the batch heuristic picks (4, 2 or 1 row-parts per head)."""
+    """Qwen3.5-shaped layer (16 QK / 32 V heads, dk=dv=128, bf16), batches from
+    far below one work item per SM to several per SM."""
     st = Setup(synth.QWEN, seed=1, num_slots=80)
     ids = synth.slot_ids(80, B, st.gen)
     untouched = [s for s in range(80) if s not in ids.tolist()][:8]
@@ -191,6 +191,21 @@ def test_f32_activations_with_f32_history(cuda):
         qkv, a, b = st.tokens((5,))
         out, o_ref, err = _step(st, ids, qkv, a, b)
         assert_out_close(out, o_ref, 128, 1e-4)
+    _check_state(st, ids.tolist(), STATE_TOL_64)
+
+
+@pytest.mark.parametrize("B", [1, 5, 24])
+def test_per_head_kernel_for_wide_groups(cuda, B):
+    """G * dv = 512 rows per QK head is beyond the TMA-fed kernel's item size,
+    so these shapes run the per-head kernel (row parts in one cluster)."""
+    shape = synth.QWEN.replace(hk=2, hv=8)
+    st = Setup(shape, seed=11, num_slots=B + 4)
+    ids = synth.slot_ids(B + 4, B, st.gen)
+    for _ in range(3):
+        qkv, a, b = st.tokens((B,))
+        out, o_ref, err = _step(st, ids, qkv, a, b)
+        assert err == 0
+        assert_out_close(out, o_ref, 128, out_tol(shape))
     _check_state(st, ids.tolist(), STATE_TOL_64)
 
 
