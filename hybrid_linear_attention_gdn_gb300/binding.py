@@ -18,7 +18,7 @@ import torch
 from . import _build
 
 F32, BF16 = 0, 1
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA = 0, 1, 2, 3
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_SCRATCH_LIMIT = 0, 1, 2, 3, 4
 DEV_ERR_SLOT_OOB, DEV_ERR_TIMEOUT, DEV_ERR_SEQLENS = 1, 2, 4
 K_DECODE, K_SPEC_VERIFY, K_SLOT_COPY, K_SLOT_ZERO, K_SPEC_COMMIT, K_PREFILL = range(6)
 K_COUNT = 8
@@ -64,6 +64,8 @@ EXPORTS = {
     "gdn_chunk_prefill_workspace_size": ([_PD, _I32, _I64], ctypes.c_size_t),
     "gdn_chunk_prefill": ([_PD, CPool, CPool, _PP, _P, _P, _P, _I32, _I64, _P, _I32, _I32,
                            _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P], _I32),
+    "gdn_chunk_prefill_noalloc": ([_PD, CPool, CPool, _PP, _P, _P, _P, _I32, _I64, _P, _I32,
+                                   _I32, _P, _P, _P, _P, _P, _P], _I32),
     "gdn_slot_copy": ([_PD, CPool, CPool, _P, _P, _I32, _P, _P], _I32),
     "gdn_slot_zero": ([_PD, CPool, _P, _I32, _P, _P], _I32),
     "gdn_status_string": ([_I32], ctypes.c_char_p),
@@ -230,6 +232,29 @@ def chunk_prefill(dims: Dims, pool: StatePool, ckpt: StatePool, params: LayerPar
                              _ptr(qkv), _ptr(a), _ptr(b), _ptr(out), _ptr(workspace), ws_bytes,
                              _ptr(dev_err), _stream(stream))
     _check("gdn_chunk_prefill", st)
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def chunk_prefill_noalloc(dims: Dims, pool: StatePool, ckpt: StatePool, params: LayerParams,
+                          slot_ids, cu_seqlens, start_pos, total_tokens: int, ckpt_ids,
+                          ckpt_block: int, qkv, a, b, out, dev_err=None, stream=None):
+    """The same prefill as chunk_prefill, for callers that cannot allocate a
+    device workspace (a host framework that owns all device memory and passes
+    only input/output pointers, or a runtime that reserved its whole budget at
+    start-up): it works in the library's built-in 64 MiB scratch buffer.
+    Raises GdnError (ERR_SCRATCH_LIMIT) when a call needs more than that."""
+    L = load()
+    n_seq = int(slot_ids.shape[0])
+    max_ckpt = int(ckpt_ids.shape[1]) if ckpt_ids is not None and ckpt_ids.dim() == 2 else 0
+    cd, cp = dims.c(), params.c()
+    st = L.gdn_chunk_prefill_noalloc(ctypes.byref(cd), pool.c(), ckpt.c(), ctypes.byref(cp),
+                                     _ptr(slot_ids), _ptr(cu_seqlens), _ptr(start_pos), n_seq,
+                                     int(total_tokens), _ptr(ckpt_ids), max_ckpt, int(ckpt_block),
+                                     _ptr(qkv), _ptr(a), _ptr(b), _ptr(out), _ptr(dev_err),
+                                     _stream(stream))
+    _check("gdn_chunk_prefill_noalloc", st)
 
 
 def slot_copy(dims: Dims, src: StatePool, dst: StatePool, src_ids, dst_ids, dev_err=None,

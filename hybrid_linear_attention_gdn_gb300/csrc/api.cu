@@ -41,6 +41,7 @@ extern "C" const char* gdn_status_string(int32_t s) {
     case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG";
     case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED";
     case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
+    case GDN_ERR_SCRATCH_LIMIT: return "GDN_ERR_SCRATCH_LIMIT";
     default: return "GDN_UNKNOWN_STATUS";
   }
 }

@@ -25,6 +25,8 @@
 //             before overwriting it, and runs after `features` read it)
 #include "gdn_common.cuh"
 
+#include <mutex>
+
 namespace gdn {
 namespace {
 
@@ -536,4 +538,59 @@ extern "C" gdn_status gdn_chunk_prefill(const gdn_dims* dims, gdn_pool pool, gdn
   }
   count_launch(GDN_K_PREFILL);
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// No-allocation variant: the same prefill, working in a scratch array that
+// is part of the library image instead of a caller-provided workspace.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_noalloc_scratch[GDN_NOALLOC_SCRATCH_BYTES];
+
+namespace gdn {
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  In host code
+// the array's name only stands for the symbol; the address is looked up once
+// per device, with that device current.
+gdn_status noalloc_scratch(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return GDN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return GDN_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return GDN_OK;
+}
+
+}  // namespace
+}  // namespace gdn
+
+extern "C" gdn_status gdn_chunk_prefill_noalloc(const gdn_dims* dims, gdn_pool pool, gdn_pool ckpt,
+                                                const gdn_params* params, const int32_t* slot_ids,
+                                                const int32_t* cu_seqlens, const int64_t* start_pos,
+                                                int32_t n_seq, int64_t total_tokens,
+                                                const int32_t* ckpt_ids, int32_t max_ckpt,
+                                                int32_t ckpt_block, const void* qkv, const void* a,
+                                                const void* b, void* out, uint32_t* dev_err,
+                                                void* stream) {
+  const size_t need = gdn_chunk_prefill_workspace_size(dims, n_seq, total_tokens);
+  if (need > (size_t)GDN_NOALLOC_SCRATCH_BYTES) return GDN_ERR_SCRATCH_LIMIT;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  if (need > 0) {
+    const gdn_status st = gdn::noalloc_scratch(&ws);
+    if (st != GDN_OK) return st;
+    ws_bytes = GDN_NOALLOC_SCRATCH_BYTES;
+  }
+  return gdn_chunk_prefill(dims, pool, ckpt, params, slot_ids, cu_seqlens, start_pos, n_seq,
+                           total_tokens, ckpt_ids, max_ckpt, ckpt_block, qkv, a, b, out, ws,
+                           ws_bytes, dev_err, stream);
 }

@@ -60,7 +60,8 @@ typedef enum {
   GDN_OK = 0,
   GDN_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad alignment, ... */
   GDN_ERR_UNSUPPORTED = 2, /* shape / dtype combination not compiled in      */
-  GDN_ERR_CUDA = 3         /* the launch failed (cudaGetLastError)            */
+  GDN_ERR_CUDA = 3,        /* the launch failed (cudaGetLastError)            */
+  GDN_ERR_SCRATCH_LIMIT = 4 /* needs more than the built-in static scratch   */
 } gdn_status;
 
 /* bits OR-ed into *dev_err by the kernels */
@@ -167,6 +168,44 @@ gdn_status gdn_chunk_prefill(const gdn_dims* dims, gdn_pool pool, gdn_pool ckpt,
                              const void* b, void* out, void* workspace,
                              size_t workspace_bytes, uint32_t* dev_err,
                              void* stream);
+
+/*
+ * Chunked prefill that allocates nothing.  The pages have no counterpart to
+ * this call; it is a convenience of this library.
+ *
+ * gdn_chunk_prefill needs a device workspace from its caller.  Some callers
+ * cannot allocate device memory at the point where they run a prefill: code
+ * hosted by a framework that owns all device memory and hands its plugins
+ * only input and output pointers, or a runtime that reserves its whole memory
+ * budget at start-up and allows no later cudaMalloc (which can synchronise
+ * the device and would eat into that budget).  This variant takes the same
+ * arguments as gdn_chunk_prefill minus the workspace, and works in a scratch
+ * buffer built into the library: a static device array of
+ * GDN_NOALLOC_SCRATCH_BYTES (64 MiB) that every GPU which loads the library
+ * holds until the process exits.  That covers about 2,000 tokens per call of
+ * a 16 QK / 32 V head, dk = dv = 128 layer (33,024 bytes per token); split a
+ * longer prefill into several calls - the state carries over in the slot.
+ *  - A call whose gdn_chunk_prefill_workspace_size(...) exceeds the scratch
+ *    returns GDN_ERR_SCRATCH_LIMIT and launches nothing.
+ *  - The first call on a device looks up the scratch's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ *  - Every call on a device shares the one buffer and finds the previous
+ *    call's contents in it.  Nothing in it needs to start at zero: each call
+ *    writes what it later reads.  Calls that can overlap on the GPU (streams
+ *    with no ordering between them) race on the buffer; order them.
+ */
+#define GDN_NOALLOC_SCRATCH_BYTES (64u << 20)
+gdn_status gdn_chunk_prefill_noalloc(const gdn_dims* dims, gdn_pool pool,
+                                     gdn_pool ckpt, const gdn_params* params,
+                                     const int32_t* slot_ids,
+                                     const int32_t* cu_seqlens,
+                                     const int64_t* start_pos, int32_t n_seq,
+                                     int64_t total_tokens,
+                                     const int32_t* ckpt_ids, int32_t max_ckpt,
+                                     int32_t ckpt_block, const void* qkv,
+                                     const void* a, const void* b, void* out,
+                                     uint32_t* dev_err, void* stream);
 
 /*
  * Copy-on-write from a clean slot (TokenSpeed Qwen3.5 page, "Riesgo de
