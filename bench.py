@@ -128,6 +128,32 @@ def _dist():
     return ws, rank, local
 
 
+def reduce_max(value: float, device=None) -> float:
+    """Maximum of `value` over the ranks of the default process group (the
+    value itself when there is no group or one rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, ms_max: float) -> float:
+    """Units processed by all ranks per second, timed by the slowest rank."""
+    return world * units_per_rank / (ms_max * 1e-3)
+
+
+def headline_config(n_slots: int, n_sets: int, ws: int) -> dict:
+    return {"workload": f"qwen35_gdn_decode_b64_h16x32_d128_pool{n_slots}",
+            "batch": B_HEAD, "pool_slots": n_slots,
+            "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+            "l2": f"inputs larger than L2: steps rotate over {n_sets} disjoint 64-slot "
+                  f"sets ({n_sets * 0.137:.2f} GB of state between visits of a slot)",
+            "activations": "bf16", "state": "fp32"}
+
+
 # --------------------------------------------------------------- reference arm
 
 def run_reference(args):
@@ -162,11 +188,10 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": "qwen35_gdn_decode_h16x32_d128", "batch": sample_b,
-                   "note": "CPU oracle (double precision); each step a bounded sample of "
-                           "8 of the 64 requests"},
+        "config": headline_config(POOL, SETS, ws),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": f"{sample_b} requests x {args.steps} decode steps"},
+                         "sample": f"each step a bounded sample: {sample_b} of the {B_HEAD} "
+                                   f"requests, double precision; {args.steps} steps"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -207,7 +232,7 @@ def _cpu_baseline(budget_s=12.0):
         oracle.decode_step(od, pool, op, ids, qkv, a, b)
         steps += 1
         dt = time.perf_counter() - t0
-        if dt > budget_s or steps >= 200:
+        if dt > budget_s:
             break
     return {"value": B * steps / dt, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"{steps} decode steps of the batch-64 workload ({B * steps} tokens), "
@@ -273,17 +298,13 @@ def run_ours(args):
     torch.cuda.synchronize()
     t_hi = time.time()
     launches = sum(gdn.launch_counts()) - n0
-    ms = e0.elapsed_time(e1)
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max(e0.elapsed_time(e1), dev)
     clocks = sampler.stop(min(t_soak, t_lo), t_hi)
     ms_step = ms / args.steps
-    tok_s = ws * B_HEAD * args.steps / (ms * 1e-3)
+    tok_s = whole_job_rate(B_HEAD * args.steps, ws, ms)
     step_bytes = B_HEAD * DECODE_TOKEN_BYTES + DECODE_STEP_PARAM_BYTES
     achieved = step_bytes / (ms_step * 1e-3) / 1e9
-    src = os.path.join(ROOT, "hybrid_linear_attention_gdn_gb300", "csrc", "decode.cu")
+    src = os.path.join(ROOT, "hybrid_linear_attention_gdn_gb300", "csrc", "decode_tma.cu")
     traffic = DECODE_TRAFFIC["bytes_per_launch"] if DECODE_TRAFFIC["source_sha256"] == _sha(src) else None
 
     # ---- end to end through the public API with host buffers
@@ -310,12 +331,8 @@ def run_ours(args):
         e2e_step(i)
     if ws > 1:
         torch.distributed.barrier()
-    e2e_ms = _events_time(e2e_step, args.steps, stream)
-    if ws > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": ws * B_HEAD / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+    e2e_ms = reduce_max(_events_time(e2e_step, args.steps, stream), dev)
+    e2e = {"value": whole_job_rate(B_HEAD, ws, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h}
 
     rows = {} if args.no_rows else measure_rows(gdn, synth, dev, stream, hbm_peak, bf16_peak)
@@ -327,15 +344,10 @@ def run_ours(args):
         "metric": METRIC, "value": tok_s, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"qwen35_gdn_decode_b64_h16x32_d128_pool{n_slots}",
-                   "batch": B_HEAD, "pool_slots": n_slots,
-                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-                   "l2": f"inputs larger than L2: steps rotate over {n_sets} disjoint 64-slot "
-                         f"sets ({n_sets * 0.137:.2f} GB of state between visits of a slot)",
-                   "activations": "bf16", "state": "fp32"},
+        "config": headline_config(n_slots, n_sets, ws),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": traffic,
-                     "kernel": "decode_kernel<128,4,bf16,bf16>",
+                     "kernel": "decode_tma_kernel<bf16,bf16,10>",
                      "algorithmic_bytes_per_launch": step_bytes, "peak_source": peak_src},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
         "rows": rows,

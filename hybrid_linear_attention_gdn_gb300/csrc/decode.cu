@@ -506,11 +506,12 @@ int choose_nit(int dk, int dv, int units, int G, bool verify) {
   return nit;
 }
 
-// Decode kernel choice.  The persistent TMA-fed kernel is at least as fast as
-// the per-head kernel at every batch measured (1..256) on the Qwen3.5-shaped
-// layer, so it takes every shape it supports (dk 128, width 4, G*dv <= 256).
-// GDN_DECODE_PATH ("tma" / "rows") overrides the choice, for measurement.
-bool use_tma_decode(const gdn_dims& d, int32_t B, const void* qkv, const gdn_params& p) {
+// Kernel choice.  The persistent TMA-fed kernels are at least as fast as the
+// per-head kernels at every batch measured (1..256) on the Qwen3.5-shaped
+// layer, so they take every shape they support (dk 128, width 4; decode also
+// G*dv <= 256).  GDN_DECODE_PATH ("tma" / "rows") overrides the choice for
+// both decode and verify, for measurement.
+int forced_path() {
   static int forced = [] {
     const char* e = std::getenv("GDN_DECODE_PATH");
     if (!e) return 0;
@@ -518,10 +519,18 @@ bool use_tma_decode(const gdn_dims& d, int32_t B, const void* qkv, const gdn_par
     if (!std::strcmp(e, "rows")) return 2;
     return 0;
   }();
-  if (!decode_tma_supported(d, qkv, p)) return false;
+  return forced;
+}
+
+bool use_tma_decode(const gdn_dims& d, int32_t B, const void* qkv, const gdn_params& p) {
   (void)B;
-  if (forced) return forced == 1;
-  return true;
+  if (!decode_tma_supported(d, qkv, p)) return false;
+  return forced_path() != 2;
+}
+
+bool use_tma_verify(const gdn_dims& d, int32_t T, const void* qkv, const gdn_params& p) {
+  if (!verify_tma_supported(d, T, qkv, p)) return false;
+  return forced_path() != 2;
 }
 
 gdn_status run_step(bool verify, const gdn_dims* dims, const gdn_pool& work, const gdn_pool* spec,
@@ -544,6 +553,12 @@ gdn_status run_step(bool verify, const gdn_dims* dims, const gdn_pool& work, con
   if (!verify && use_tma_decode(*dims, B, qkv, *params)) {
     cudaError_t e = decode_tma_launch(*dims, work, *params, slot_ids, B, qkv, a, b, out, dev_err, cs);
     if (e == cudaSuccess) count_launch(GDN_K_DECODE);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+  }
+  if (verify && use_tma_verify(*dims, T, qkv, *params)) {
+    cudaError_t e = verify_tma_launch(*dims, work, *spec, *params, slot_ids, spec_ids, B, T, qkv, a,
+                                      b, out, dev_err, cs);
+    if (e == cudaSuccess) count_launch(GDN_K_SPEC_VERIFY);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
   }
   StepArgs s = {};

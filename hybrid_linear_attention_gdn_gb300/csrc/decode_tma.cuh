@@ -9,4 +9,11 @@ cudaError_t decode_tma_launch(const gdn_dims& d, const gdn_pool& pool, const gdn
                               const int32_t* slot_ids, int32_t B, const void* qkv, const void* a,
                               const void* b, void* out, uint32_t* dev_err, cudaStream_t s);
 int sm_count();
+
+// Persistent TMA-fed speculative verify (dk = 128, conv width 4, T <= 16).
+bool verify_tma_supported(const gdn_dims& d, int32_t T, const void* qkv, const gdn_params& p);
+cudaError_t verify_tma_launch(const gdn_dims& d, const gdn_pool& work, const gdn_pool& spec,
+                              const gdn_params& p, const int32_t* slot_ids, const int32_t* spec_ids,
+                              int32_t B, int32_t T, const void* qkv, const void* a, const void* b,
+                              void* out, uint32_t* dev_err, cudaStream_t s);
 }  // namespace gdn

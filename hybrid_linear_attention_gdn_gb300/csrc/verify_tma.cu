@@ -1,0 +1,385 @@
+// Persistent, TMA-fed speculative verify (dk = 128, conv width 4).
+//
+// TokenSpeed Qwen3.5 page, "Scheduler dual": the spec_cache keeps per-draft-
+// step conv/SSM snapshots so that the state can roll back when verification
+// rejects drafts.  Verify runs the T draft tokens of each request from its
+// working slot and writes the state after every draft into a spec slot; the
+// working slot is only read.
+//
+// Because nothing here is written in place, work splits freely: an item is one
+// request, one V head h and one block of R = dv/P rows (P chosen so that there
+// are several items per SM).  One CTA per SM walks a static item list:
+//   warp 8 (producer, one lane): per item, a bundle of bulk copies (the conv
+//     history rows and the T draft activations of the q/k channels of h's QK
+//     head and of the item's v channels, plus their conv weights), then the
+//     item's state rows in 16 KiB chunks through a ring of mbarrier-tracked
+//     shared-memory stages;
+//   warps 0-7: conv + SiLU over the draft sequence (and the snapshot conv
+//     histories, written straight to the spec slots), per-draft L2 norms and
+//     gates; then per chunk, 4 rows per warp are held in registers through all
+//     T drafts, each draft's rows streamed to its spec slot with 128-bit stores.
+// Snapshot writes are T times the state reads, so HBM time is mostly stores.
+// All waits are bounded (GDN_DEV_ERR_TIMEOUT).
+#include "gdn_common.cuh"
+#include "decode_tma.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kCW = 8;
+constexpr int kCons = kCW * 32;
+constexpr int kThr = kCons + 32;
+constexpr int kDK = 128;
+constexpr int kLPR = kDK / 16;
+constexpr int kRows = 32;
+constexpr int kStageFloats = kRows * kDK;
+constexpr uint32_t kStageBytes = kStageFloats * sizeof(float);
+constexpr int kW = 4;
+constexpr int kMaxT = 16;
+constexpr int kMaxR = 128;
+constexpr int kMaxCh = 2 * kDK + kMaxR;
+constexpr int kBarCons = 1;
+
+template <typename Tact, typename Tconv, int STAGES>
+struct __align__(128) VSmem {
+  float ring[STAGES][kStageFloats];
+  struct Bundle {
+    Tconv hist[kW - 1][kMaxCh];
+    Tact x[kMaxT][kMaxCh];
+    float w[kMaxCh * kW];
+  } bundle[2];
+  float sy[kMaxT][kMaxCh];   // conv + SiLU per draft: q | k | v rows
+  float so[kMaxT][kMaxR];    // readout per draft
+  float snorm[kMaxT][3];     // rq, rk, k^.q^ per draft
+  float sgate[kMaxT][2];     // alpha, beta per draft
+  uint64_t full[STAGES], empty[STAGES], bfull[2], bempty[2];
+  int abort;
+};
+
+struct VArgs {
+  const float* ssm;
+  const void* conv;
+  int32_t num_slots;
+  float* spec_ssm;
+  void* spec_conv;
+  int32_t spec_num_slots;
+  const int32_t* spec_ids;
+  const float* conv_w;
+  const float* A_log;
+  const float* dt_bias;
+  const int32_t* slot_ids;
+  const void* qkv;
+  const void* a;
+  const void* b;
+  void* out;
+  uint32_t* err;
+  int32_t hk, hv, dv, C, G, P, T, n_items;
+};
+
+template <typename Tact, typename Tconv, int STAGES>
+__global__ void __launch_bounds__(kThr, 1) verify_tma_kernel(const VArgs a) {
+  using SM = VSmem<Tact, Tconv, STAGES>;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  SM& S = *reinterpret_cast<SM*>(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int R = a.dv / a.P;
+  const int nchunks = R / kRows;
+  const int nch = 2 * kDK + R;
+  const int T = a.T;
+  const int per_req = a.hv * a.P;  // items per request
+  volatile int* abort_flag = &S.abort;
+
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], kCW);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&S.bfull[s], 1);
+      mbar_init(&S.bempty[s], kCons);
+    }
+    S.abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kCW) {
+    // ------------------------------------------------------------ producer
+    if (lane != 0) return;
+    const uint32_t ec = sizeof(Tconv), ea = sizeof(Tact);
+    const uint32_t bundle_bytes = (kW - 1) * nch * ec + T * nch * ea + nch * kW * 4;
+    uint32_t n = 0, vk = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
+      const int r = item / per_req, h = (item % per_req) / a.P, p = item % a.P;
+      const int32_t slot = a.slot_ids[r];
+      if (slot_class(slot, a.num_slots)) continue;
+      if (*abort_flag) break;
+      const int hq = h / a.G;
+      const int bb = vk & 1;
+      if (!mbar_wait(&S.bempty[bb], ((vk >> 1) & 1) ^ 1)) { ok = false; break; }
+      mbar_arrive_expect_tx(&S.bfull[bb], bundle_bytes);
+      typename SM::Bundle& Bd = S.bundle[bb];
+      const size_t cq = (size_t)hq * kDK, ck = (size_t)a.hk * kDK + cq,
+                   cv = 2 * (size_t)a.hk * kDK + (size_t)h * a.dv + (size_t)p * R;
+      const Tconv* hist = reinterpret_cast<const Tconv*>(a.conv) + (size_t)slot * (kW - 1) * a.C;
+      for (int j = 0; j < kW - 1; ++j) {
+        bulk_g2s(&Bd.hist[j][0], hist + (size_t)j * a.C + cq, kDK * ec, &S.bfull[bb]);
+        bulk_g2s(&Bd.hist[j][kDK], hist + (size_t)j * a.C + ck, kDK * ec, &S.bfull[bb]);
+        bulk_g2s(&Bd.hist[j][2 * kDK], hist + (size_t)j * a.C + cv, R * ec, &S.bfull[bb]);
+      }
+      for (int t = 0; t < T; ++t) {
+        const Tact* x = reinterpret_cast<const Tact*>(a.qkv) + ((size_t)r * T + t) * a.C;
+        bulk_g2s(&Bd.x[t][0], x + cq, kDK * ea, &S.bfull[bb]);
+        bulk_g2s(&Bd.x[t][kDK], x + ck, kDK * ea, &S.bfull[bb]);
+        bulk_g2s(&Bd.x[t][2 * kDK], x + cv, R * ea, &S.bfull[bb]);
+      }
+      bulk_g2s(&Bd.w[0], a.conv_w + cq * kW, kDK * kW * 4, &S.bfull[bb]);
+      bulk_g2s(&Bd.w[kDK * kW], a.conv_w + ck * kW, kDK * kW * 4, &S.bfull[bb]);
+      bulk_g2s(&Bd.w[2 * kDK * kW], a.conv_w + cv * kW, R * kW * 4, &S.bfull[bb]);
+      ++vk;
+      const float* src = a.ssm + (((size_t)slot * a.hv + h) * a.dv + (size_t)p * R) * kDK;
+      for (int c = 0; c < nchunks; ++c, ++n) {
+        const int st = n % STAGES;
+        if (*abort_flag || !mbar_wait(&S.empty[st], ((n / STAGES) & 1) ^ 1)) { ok = false; break; }
+        mbar_arrive_expect_tx(&S.full[st], kStageBytes);
+        bulk_g2s(S.ring[st], src + (size_t)c * kStageFloats, kStageBytes, &S.full[st]);
+      }
+    }
+    if (!ok || *abort_flag) {
+      *abort_flag = 1;
+      report(a.err, GDN_DEV_ERR_TIMEOUT);
+      const uint32_t first = n > (uint32_t)STAGES ? n - STAGES : 0;
+      for (uint32_t m = first; m < n; ++m) mbar_wait(&S.full[m % STAGES], (m / STAGES) & 1);
+      for (uint32_t m = vk > 2 ? vk - 2 : 0; m < vk; ++m) mbar_wait(&S.bfull[m & 1], (m >> 1) & 1);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int seg = lane % kLPR;
+  const int rloc = warp * (32 / kLPR) + lane / kLPR;
+  uint32_t n = 0, vk = 0;
+  for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
+    const int r = item / per_req, h = (item % per_req) / a.P, p = item % a.P;
+    const int hq = h / a.G;
+    const int32_t slot = a.slot_ids[r];
+    const int32_t* sids = a.spec_ids + (size_t)r * T;
+    const int cls = slot_class(slot, a.num_slots);
+    if (cls) {
+      if (cls == 2 && h == 0 && p == 0 && tid == 0) report(a.err, GDN_DEV_ERR_SLOT_OOB);
+      for (int e = tid; e < T * R; e += kCons) {
+        const int t = e / R, i = e % R;
+        reinterpret_cast<Tact*>(a.out)[(((size_t)r * T + t) * a.hv + h) * a.dv + p * R + i] =
+            from_f32<Tact>(0.f);
+      }
+      continue;
+    }
+    if (h == 0 && p == 0 && tid < T && slot_class(sids[tid], a.spec_num_slots) == 2)
+      report(a.err, GDN_DEV_ERR_SLOT_OOB);
+    const int bb = vk & 1;
+    if (!*abort_flag && !mbar_wait(&S.bfull[bb], (vk >> 1) & 1)) *abort_flag = 1;
+    named_sync(kBarCons, kCons);
+    if (*abort_flag) break;
+    const typename SM::Bundle& Bd = S.bundle[bb];
+    // conv over the drafts; the snapshot history after draft t is
+    // [win1, win2, x_t].  q/k channels are written by the (p = 0) item of the
+    // first V head of the QK group, v channels by their own item.
+    const bool qk_writer = (h % a.G) == 0 && p == 0;
+    for (int i = tid; i < nch; i += kCons) {
+      const float4 w = *reinterpret_cast<const float4*>(&Bd.w[i * kW]);
+      float w0 = to_f32(Bd.hist[0][i]), w1 = to_f32(Bd.hist[1][i]), w2 = to_f32(Bd.hist[2][i]);
+      const size_t c = i < kDK ? (size_t)hq * kDK + i
+                     : i < 2 * kDK ? (size_t)a.hk * kDK + (size_t)hq * kDK + (i - kDK)
+                                   : 2 * (size_t)a.hk * kDK + (size_t)h * a.dv + (size_t)p * R + (i - 2 * kDK);
+      const bool writes = i >= 2 * kDK || qk_writer;
+      for (int t = 0; t < T; ++t) {
+        const float xv = to_f32(Bd.x[t][i]);
+        float acc = w.x * w0;
+        acc = fmaf(w.y, w1, acc);
+        acc = fmaf(w.z, w2, acc);
+        acc = fmaf(w.w, xv, acc);
+        S.sy[t][i] = silu_f(acc);
+        w0 = w1;
+        w1 = w2;
+        w2 = xv;
+        const int32_t sid = sids[t];
+        if (writes && slot_class(sid, a.spec_num_slots) == 0) {
+          Tconv* sc = reinterpret_cast<Tconv*>(a.spec_conv) + (size_t)sid * (kW - 1) * a.C + c;
+          sc[0] = from_f32<Tconv>(w0);
+          sc[a.C] = from_f32<Tconv>(w1);
+          sc[2 * (size_t)a.C] = from_f32<Tconv>(w2);
+        }
+      }
+    }
+    if (tid < T) {
+      const size_t rt = (size_t)r * T + tid;
+      S.sgate[tid][0] = gate_alpha(a.A_log[h], a.dt_bias[h],
+                                   to_f32(reinterpret_cast<const Tact*>(a.a)[rt * a.hv + h]));
+      S.sgate[tid][1] = sigmoid_f(to_f32(reinterpret_cast<const Tact*>(a.b)[rt * a.hv + h]));
+    }
+    named_sync(kBarCons, kCons);
+    mbar_arrive(&S.bempty[bb]);
+    ++vk;
+    for (int t = warp; t < T; t += kCW) {
+      float pq = 0.f, pk = 0.f, pqk = 0.f;
+      for (int i = lane; i < kDK; i += 32) {
+        const float q = S.sy[t][i], k = S.sy[t][kDK + i];
+        pq = fmaf(q, q, pq);
+        pk = fmaf(k, k, pk);
+        pqk = fmaf(q, k, pqk);
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        pq += __shfl_xor_sync(0xffffffffu, pq, o);
+        pk += __shfl_xor_sync(0xffffffffu, pk, o);
+        pqk += __shfl_xor_sync(0xffffffffu, pqk, o);
+      }
+      if (lane == 0) {
+        const float rq = rsqrtf(pq + kNormEps) * rsqrtf((float)kDK);
+        const float rk = rsqrtf(pk + kNormEps);
+        S.snorm[t][0] = rq;
+        S.snorm[t][1] = rk;
+        S.snorm[t][2] = pqk * rq * rk;
+      }
+    }
+    named_sync(kBarCons, kCons);
+
+    for (int c = 0; c < nchunks; ++c, ++n) {
+      const int st = n % STAGES;
+      if (!*abort_flag && !mbar_wait(&S.full[st], (n / STAGES) & 1)) *abort_flag = 1;
+      if (*abort_flag) continue;
+      const int row = c * kRows + rloc;  // row within the item
+      float4 s4[4];
+      const float* srow = S.ring[st] + rloc * kDK;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc)
+        s4[cc] = *reinterpret_cast<const float4*>(srow + cc * 4 * kLPR + seg * 4);
+      for (int t = 0; t < T; ++t) {
+        const float rq = S.snorm[t][0], rk = S.snorm[t][1], kq = S.snorm[t][2];
+        const float alpha = S.sgate[t][0], beta = S.sgate[t][1];
+        float4 kk[4], qq[4];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          const int col = cc * 4 * kLPR + seg * 4;
+          const float4 k4 = *reinterpret_cast<const float4*>(&S.sy[t][kDK + col]);
+          const float4 q4 = *reinterpret_cast<const float4*>(&S.sy[t][col]);
+          kk[cc] = make_float4(k4.x * rk, k4.y * rk, k4.z * rk, k4.w * rk);
+          qq[cc] = make_float4(q4.x * rq, q4.y * rq, q4.z * rq, q4.w * rq);
+        }
+        float dk_ = 0.f, dq_ = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          dk_ += s4[cc].x * kk[cc].x + s4[cc].y * kk[cc].y + s4[cc].z * kk[cc].z + s4[cc].w * kk[cc].w;
+          dq_ += s4[cc].x * qq[cc].x + s4[cc].y * qq[cc].y + s4[cc].z * qq[cc].z + s4[cc].w * qq[cc].w;
+        }
+#pragma unroll
+        for (int o = kLPR / 2; o; o >>= 1) {
+          dk_ += __shfl_xor_sync(0xffffffffu, dk_, o);
+          dq_ += __shfl_xor_sync(0xffffffffu, dq_, o);
+        }
+        const float bu = beta * (S.sy[t][2 * kDK + row] - alpha * dk_);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          s4[cc].x = fmaf(bu, kk[cc].x, alpha * s4[cc].x);
+          s4[cc].y = fmaf(bu, kk[cc].y, alpha * s4[cc].y);
+          s4[cc].z = fmaf(bu, kk[cc].z, alpha * s4[cc].z);
+          s4[cc].w = fmaf(bu, kk[cc].w, alpha * s4[cc].w);
+        }
+        const int32_t sid = sids[t];
+        if (slot_class(sid, a.spec_num_slots) == 0) {
+          float4* drow = reinterpret_cast<float4*>(
+              a.spec_ssm + (((size_t)sid * a.hv + h) * a.dv + (size_t)p * R + row) * kDK);
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) st_stream(drow + (cc * 4 * kLPR + seg * 4) / 4, s4[cc]);
+        }
+        if (seg == 0) S.so[t][row] = fmaf(bu, kq, alpha * dq_);
+      }
+      __syncwarp();  // the whole warp is done with its rows of the stage
+      if (lane == 0) mbar_arrive(&S.empty[st]);
+    }
+    named_sync(kBarCons, kCons);
+    if (*abort_flag) break;
+    for (int e = tid; e < T * R; e += kCons) {
+      const int t = e / R, i = e % R;
+      reinterpret_cast<Tact*>(a.out)[(((size_t)r * T + t) * a.hv + h) * a.dv + p * R + i] =
+          from_f32<Tact>(S.so[t][i]);
+    }
+  }
+  if (*abort_flag && tid == 0) report(a.err, GDN_DEV_ERR_TIMEOUT);
+}
+
+template <typename Tact, typename Tconv, int STAGES>
+cudaError_t launch_v(const VArgs& a, cudaStream_t s) {
+  using SM = VSmem<Tact, Tconv, STAGES>;
+  auto k = verify_tma_kernel<Tact, Tconv, STAGES>;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(SM));
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const int grid = a.n_items < sm_count() ? a.n_items : sm_count();
+  k<<<grid, kThr, sizeof(SM), s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool verify_tma_supported(const gdn_dims& d, int32_t T, const void* qkv, const gdn_params& p) {
+  const size_t ea = dtype_size(d.act_dtype), ec = dtype_size(d.conv_dtype);
+  const int64_t C = channels(d);
+  if (d.dk != kDK || d.conv_width != kW || T < 1 || T > kMaxT) return false;
+  if (d.dv % kRows) return false;
+  if ((C * ea) % 16 || (C * ec) % 16 || (kDK * ea) % 16 || (kDK * ec) % 16) return false;
+  if ((kRows * ea) % 16 || (kRows * ec) % 16) return false;
+  if (!aligned(qkv, 16) || !aligned(p.conv_w, 16)) return false;
+  return true;
+}
+
+cudaError_t verify_tma_launch(const gdn_dims& d, const gdn_pool& work, const gdn_pool& spec,
+                              const gdn_params& p, const int32_t* slot_ids, const int32_t* spec_ids,
+                              int32_t B, int32_t T, const void* qkv, const void* av, const void* bv,
+                              void* out, uint32_t* dev_err, cudaStream_t s) {
+  VArgs a;
+  a.ssm = work.ssm;
+  a.conv = work.conv;
+  a.num_slots = work.num_slots;
+  a.spec_ssm = spec.ssm;
+  a.spec_conv = spec.conv;
+  a.spec_num_slots = spec.num_slots;
+  a.spec_ids = spec_ids;
+  a.conv_w = p.conv_w;
+  a.A_log = p.A_log;
+  a.dt_bias = p.dt_bias;
+  a.slot_ids = slot_ids;
+  a.qkv = qkv;
+  a.a = av;
+  a.b = bv;
+  a.out = out;
+  a.err = dev_err;
+  a.hk = d.hk;
+  a.hv = d.hv;
+  a.dv = d.dv;
+  a.C = (int32_t)channels(d);
+  a.G = d.hv / d.hk;
+  a.T = T;
+  // row blocks per head: smallest P (R = dv/P a multiple of 32, R <= 128)
+  // that gives at least four items per SM
+  int P = 1;
+  while ((d.dv / P > kMaxR) ||
+         ((long)B * d.hv * P < 4L * sm_count() && (d.dv / (2 * P)) % kRows == 0 && d.dv / (2 * P) >= kRows))
+    P *= 2;
+  if (d.dv % P || (d.dv / P) % kRows || d.dv / P > kMaxR) return cudaErrorInvalidValue;
+  a.P = P;
+  a.n_items = B * d.hv * P;
+  constexpr int ST = 6;
+  if (d.act_dtype == GDN_BF16 && d.conv_dtype == GDN_BF16)
+    return launch_v<__nv_bfloat16, __nv_bfloat16, ST>(a, s);
+  if (d.act_dtype == GDN_BF16) return launch_v<__nv_bfloat16, float, ST>(a, s);
+  return launch_v<float, float, ST>(a, s);
+}
+
+}  // namespace gdn
