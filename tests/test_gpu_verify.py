@@ -25,10 +25,10 @@ def _spec_pool(st: Setup, n):
     (synth.TINY, 2, 5),
     (synth.QWEN, 16, 8),
     (synth.QWEN, 3, 4),
-    (synth.QWEN, 40, 16),
+    (synth.QWEN, 24, 16),
     (synth.QWEN.replace(act="f32", conv="f32", hk=4, hv=8), 5, 6),
     (synth.QWEN.replace(hk=2, hv=8, dk=64, dv=64), 3, 3),
-], ids=["tiny", "qwen_b16_t8", "qwen_b3_t4", "qwen_b40_t16", "f32_b5_t6", "dk64_g4"])
+], ids=["tiny", "qwen_b16_t8", "qwen_b3_t4", "qwen_b24_t16", "f32_b5_t6", "dk64_g4"])
 def test_verify_then_commit(cuda, shape, B, T):
     n_work = 8 if shape is synth.TINY else 40
     st = Setup(shape, seed=30, num_slots=n_work)
