@@ -25,6 +25,8 @@
 #include "gdn_common.cuh"
 #include "decode_tma.cuh"
 
+#include <cstdlib>
+
 namespace gdn {
 namespace {
 
@@ -74,8 +76,8 @@ struct TmaArgs {
   int32_t hk, hv, dv, C, G, n_items;
 };
 
-template <typename Tact, typename Tconv, int STAGES>
-__global__ void __launch_bounds__(kThr, 1) decode_tma_kernel(const TmaArgs a) {
+template <typename Tact, typename Tconv, int STAGES, int MINB>
+__global__ void __launch_bounds__(kThr, MINB) decode_tma_kernel(const TmaArgs a) {
   using SM = TmaSmem<Tact, Tconv, STAGES>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   SM& S = *reinterpret_cast<SM*>(smem_raw);
@@ -294,10 +296,10 @@ __global__ void __launch_bounds__(kThr, 1) decode_tma_kernel(const TmaArgs a) {
   if (*abort_flag && tid == 0) report(a.err, GDN_DEV_ERR_TIMEOUT);
 }
 
-template <typename Tact, typename Tconv, int STAGES>
+template <typename Tact, typename Tconv, int STAGES, int MINB>
 cudaError_t launch_tma(const TmaArgs& a, cudaStream_t s) {
   using SM = TmaSmem<Tact, Tconv, STAGES>;
-  auto k = decode_tma_kernel<Tact, Tconv, STAGES>;
+  auto k = decode_tma_kernel<Tact, Tconv, STAGES, MINB>;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -306,12 +308,29 @@ cudaError_t launch_tma(const TmaArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  const int grid = a.n_items < sm_count() ? a.n_items : sm_count();
+  const int slots = sm_count() * MINB;
+  const int grid = a.n_items < slots ? a.n_items : slots;
   k<<<grid, kThr, sizeof(SM), s>>>(a);
   return cudaGetLastError();
 }
 
+// One CTA per SM with a 10-stage ring, or two per SM with 4 stages each (one
+// CTA's item prologue then overlaps the other's state stream).
+template <typename Tact, typename Tconv>
+cudaError_t launch_tma_dt(const TmaArgs& a, cudaStream_t s) {
+  if (tma_ctas_per_sm() == 2) return launch_tma<Tact, Tconv, 4, 2>(a, s);
+  return launch_tma<Tact, Tconv, 10, 1>(a, s);
+}
+
 }  // namespace
+
+int tma_ctas_per_sm() {
+  static int v = [] {
+    const char* e = std::getenv("GDN_TMA_CTAS");
+    return (e && e[0] == '2') ? 2 : (e && e[0] == '1') ? 1 : 0;
+  }();
+  return v;
+}
 
 int sm_count() {
   static int cached[64] = {0};
@@ -361,11 +380,10 @@ cudaError_t decode_tma_launch(const gdn_dims& d, const gdn_pool& pool, const gdn
   a.C = (int32_t)channels(d);
   a.G = d.hv / d.hk;
   a.n_items = B * d.hk;
-  constexpr int ST = 10;
   if (d.act_dtype == GDN_BF16 && d.conv_dtype == GDN_BF16)
-    return launch_tma<__nv_bfloat16, __nv_bfloat16, ST>(a, s);
-  if (d.act_dtype == GDN_BF16) return launch_tma<__nv_bfloat16, float, ST>(a, s);
-  return launch_tma<float, float, ST>(a, s);
+    return launch_tma_dt<__nv_bfloat16, __nv_bfloat16>(a, s);
+  if (d.act_dtype == GDN_BF16) return launch_tma_dt<__nv_bfloat16, float>(a, s);
+  return launch_tma_dt<float, float>(a, s);
 }
 
 }  // namespace gdn

@@ -9,6 +9,9 @@ cudaError_t decode_tma_launch(const gdn_dims& d, const gdn_pool& pool, const gdn
                               const int32_t* slot_ids, int32_t B, const void* qkv, const void* a,
                               const void* b, void* out, uint32_t* dev_err, cudaStream_t s);
 int sm_count();
+// CTAs per SM for the persistent kernels: 0 = the default choice of each
+// kernel, 1 or 2 forced by GDN_TMA_CTAS (for measurement).
+int tma_ctas_per_sm();
 
 // Persistent TMA-fed speculative verify (dk = 128, conv width 4, T <= 16).
 bool verify_tma_supported(const gdn_dims& d, int32_t T, const void* qkv, const gdn_params& p);

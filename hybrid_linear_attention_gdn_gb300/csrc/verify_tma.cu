@@ -40,18 +40,21 @@ constexpr int kMaxR = 128;
 constexpr int kMaxCh = 2 * kDK + kMaxR;
 constexpr int kBarCons = 1;
 
-template <typename Tact, typename Tconv, int STAGES>
+// MT: drafts the shared-memory layout holds (T <= MT).  The T <= 8 layout is
+// small enough for two CTAs per SM, so one CTA's prologue overlaps the other's
+// stream of snapshot stores.
+template <typename Tact, typename Tconv, int STAGES, int MT>
 struct __align__(128) VSmem {
   float ring[STAGES][kStageFloats];
   struct Bundle {
     Tconv hist[kW - 1][kMaxCh];
-    Tact x[kMaxT][kMaxCh];
+    Tact x[MT][kMaxCh];
     float w[kMaxCh * kW];
   } bundle[2];
-  float sy[kMaxT][kMaxCh];   // conv + SiLU per draft: q | k | v rows
-  float so[kMaxT][kMaxR];    // readout per draft
-  float snorm[kMaxT][3];     // rq, rk, k^.q^ per draft
-  float sgate[kMaxT][2];     // alpha, beta per draft
+  float sy[MT][kMaxCh];   // conv + SiLU per draft: q | k | v rows
+  float so[MT][kMaxR];    // readout per draft
+  float snorm[MT][3];     // rq, rk, k^.q^ per draft
+  float sgate[MT][2];     // alpha, beta per draft
   uint64_t full[STAGES], empty[STAGES], bfull[2], bempty[2];
   int abort;
 };
@@ -76,9 +79,9 @@ struct VArgs {
   int32_t hk, hv, dv, C, G, P, T, n_items;
 };
 
-template <typename Tact, typename Tconv, int STAGES>
-__global__ void __launch_bounds__(kThr, 1) verify_tma_kernel(const VArgs a) {
-  using SM = VSmem<Tact, Tconv, STAGES>;
+template <typename Tact, typename Tconv, int STAGES, int MT, int MINB>
+__global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
+  using SM = VSmem<Tact, Tconv, STAGES, MT>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   SM& S = *reinterpret_cast<SM*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -309,10 +312,10 @@ __global__ void __launch_bounds__(kThr, 1) verify_tma_kernel(const VArgs a) {
   if (*abort_flag && tid == 0) report(a.err, GDN_DEV_ERR_TIMEOUT);
 }
 
-template <typename Tact, typename Tconv, int STAGES>
+template <typename Tact, typename Tconv, int STAGES, int MT, int MINB>
 cudaError_t launch_v(const VArgs& a, cudaStream_t s) {
-  using SM = VSmem<Tact, Tconv, STAGES>;
-  auto k = verify_tma_kernel<Tact, Tconv, STAGES>;
+  using SM = VSmem<Tact, Tconv, STAGES, MT>;
+  auto k = verify_tma_kernel<Tact, Tconv, STAGES, MT, MINB>;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -321,9 +324,16 @@ cudaError_t launch_v(const VArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  const int grid = a.n_items < sm_count() ? a.n_items : sm_count();
+  const int slots = sm_count() * MINB;
+  const int grid = a.n_items < slots ? a.n_items : slots;
   k<<<grid, kThr, sizeof(SM), s>>>(a);
   return cudaGetLastError();
+}
+
+template <typename Tact, typename Tconv>
+cudaError_t launch_v_dt(const VArgs& a, cudaStream_t s) {
+  if (a.T <= 8 && tma_ctas_per_sm() != 1) return launch_v<Tact, Tconv, 3, 8, 2>(a, s);
+  return launch_v<Tact, Tconv, 4, kMaxT, 1>(a, s);
 }
 
 }  // namespace
@@ -367,19 +377,19 @@ cudaError_t verify_tma_launch(const gdn_dims& d, const gdn_pool& work, const gdn
   a.G = d.hv / d.hk;
   a.T = T;
   // row blocks per head: smallest P (R = dv/P a multiple of 32, R <= 128)
-  // that gives at least four items per SM
+  // that gives at least six items per resident CTA
+  const long slots = (long)sm_count() * (T <= 8 && tma_ctas_per_sm() != 1 ? 2 : 1);
   int P = 1;
   while ((d.dv / P > kMaxR) ||
-         ((long)B * d.hv * P < 4L * sm_count() && (d.dv / (2 * P)) % kRows == 0 && d.dv / (2 * P) >= kRows))
+         ((long)B * d.hv * P < 6L * slots && (d.dv / (2 * P)) % kRows == 0 && d.dv / (2 * P) >= kRows))
     P *= 2;
   if (d.dv % P || (d.dv / P) % kRows || d.dv / P > kMaxR) return cudaErrorInvalidValue;
   a.P = P;
   a.n_items = B * d.hv * P;
-  constexpr int ST = 6;
   if (d.act_dtype == GDN_BF16 && d.conv_dtype == GDN_BF16)
-    return launch_v<__nv_bfloat16, __nv_bfloat16, ST>(a, s);
-  if (d.act_dtype == GDN_BF16) return launch_v<__nv_bfloat16, float, ST>(a, s);
-  return launch_v<float, float, ST>(a, s);
+    return launch_v_dt<__nv_bfloat16, __nv_bfloat16>(a, s);
+  if (d.act_dtype == GDN_BF16) return launch_v_dt<__nv_bfloat16, float>(a, s);
+  return launch_v_dt<float, float>(a, s);
 }
 
 }  // namespace gdn
