@@ -24,7 +24,10 @@
 //             every checkpoint and the final one (it reads the old history
 //             before overwriting it, and runs after `features` read it)
 #include "gdn_common.cuh"
+#include "prefill_tc.cuh"
 
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 namespace gdn {
@@ -457,14 +460,37 @@ cudaError_t dispatch_prefill(const PrefillArgs& a, int act, int cv, cudaStream_t
   return launch_prefill_t<DK, DVT, __nv_bfloat16, float>(a, s);
 }
 
+cudaError_t launch_history(const PrefillArgs& a, int act, int cv, cudaStream_t s) {
+  const dim3 grid((unsigned)((a.C + kThreads - 1) / kThreads), (unsigned)a.n_seq);
+  if (act == GDN_F32 && cv == GDN_F32)
+    history_kernel<float, float><<<grid, kThreads, 0, s>>>(a);
+  else if (act == GDN_BF16 && cv == GDN_BF16)
+    history_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, kThreads, 0, s>>>(a);
+  else
+    history_kernel<__nv_bfloat16, float><<<grid, kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+// The tensor-core path takes dk = dv = 128, width 4 (GDN_PREFILL_PATH=cuda
+// forces the CUDA-core path, for measurement).
+bool use_tc_prefill(const gdn_dims& d, const void* qkv, const gdn_params& p) {
+  static const bool forced_cuda = [] {
+    const char* e = std::getenv("GDN_PREFILL_PATH");
+    return e && !std::strcmp(e, "cuda");
+  }();
+  return !forced_cuda && prefill_tc_supported(d, qkv, p);
+}
+
 }  // namespace
 }  // namespace gdn
 
+// Sized for either path (the tensor-core path needs about half of it).
 extern "C" size_t gdn_chunk_prefill_workspace_size(const gdn_dims* dims, int32_t n_seq,
                                                    int64_t total_tokens) {
-  (void)n_seq;
-  if (gdn::check_dims(dims) != GDN_OK || total_tokens < 0) return 0;
-  return gdn::ws_layout(*dims, total_tokens).total;
+  if (gdn::check_dims(dims) != GDN_OK || total_tokens < 0 || n_seq < 0) return 0;
+  const size_t v1 = gdn::ws_layout(*dims, total_tokens).total;
+  const size_t tc = gdn::prefill_tc_workspace(*dims, n_seq, total_tokens);
+  return total_tokens == 0 ? 0 : (v1 > tc ? v1 : tc);
 }
 
 extern "C" gdn_status gdn_chunk_prefill(const gdn_dims* dims, gdn_pool pool, gdn_pool ckpt,
@@ -489,7 +515,9 @@ extern "C" gdn_status gdn_chunk_prefill(const gdn_dims* dims, gdn_pool pool, gdn
     return GDN_ERR_INVALID_ARG;
   if (total_tokens > 0 && (!qkv || !a || !b || !out)) return GDN_ERR_INVALID_ARG;
   const WsLayout wl = ws_layout(*dims, total_tokens);
-  if (total_tokens > 0 && (!workspace || workspace_bytes < wl.total || !aligned(workspace, 256)))
+  const bool tc = use_tc_prefill(*dims, qkv, *params);
+  const size_t need = tc ? prefill_tc_workspace(*dims, n_seq, total_tokens) : wl.total;
+  if (total_tokens > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
     return GDN_ERR_INVALID_ARG;
   if (dims->hv / dims->hk * dims->dv + 2 * dims->dk > 4096) return GDN_ERR_UNSUPPORTED;
   PrefillArgs p = {};
@@ -531,12 +559,19 @@ extern "C" gdn_status gdn_chunk_prefill(const gdn_dims* dims, gdn_pool pool, gdn
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaErrorInvalidValue;
   const int act = dims->act_dtype, cv = dims->conv_dtype;
-  switch (dims->dk) {
-    case 16: e = dispatch_prefill<16, 16>(p, act, cv, s); break;
-    case 64: e = dispatch_prefill<64, 64>(p, act, cv, s); break;
-    case 128: e = dispatch_prefill<128, 64>(p, act, cv, s); break;
+  if (tc) {
+    e = prefill_tc_launch(*dims, pool, ckpt, *params, slot_ids, cu_seqlens, start_pos, n_seq,
+                          total_tokens, ckpt_ids, max_ckpt, ckpt_block, qkv, a, b, out, workspace,
+                          dev_err, s);
+    if (e == cudaSuccess) e = launch_history(p, act, cv, s);
+  } else {
+    switch (dims->dk) {
+      case 16: e = dispatch_prefill<16, 16>(p, act, cv, s); break;
+      case 64: e = dispatch_prefill<64, 64>(p, act, cv, s); break;
+      case 128: e = dispatch_prefill<128, 64>(p, act, cv, s); break;
+    }
   }
-  count_launch(GDN_K_PREFILL);
+  if (e == cudaSuccess) count_launch(GDN_K_PREFILL);
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

@@ -1,0 +1,759 @@
+// Chunked GDN prefill on the 5th-generation tensor cores (tcgen05 / TMEM).
+//
+// Same contract and chunk form as prefill.cu (TokenSpeed Qwen3.5 page, "Ciclo
+// de vida de slots": block-aligned checkpoints; chunkwise WY/UT form of the
+// gated delta rule), specialised for dk = dv = 128, conv width 4.
+//
+//   plan:     per-sequence offsets of its 64-token chunks (absolute-aligned).
+//   features: one CTA per (chunk, QK head): conv1d + SiLU + L2 norm + gates
+//             for the chunk's 64 tokens, written as bf16 operand images in the
+//             tensor core's 128B-swizzled shared-memory layout, so the chain
+//             kernel fetches each with a single bulk copy:
+//               KQ image [K^ rows 0..63 ; Q^ rows 64..127] x dk (K-major),
+//               V image per V head (read as the MN-major A operand of V^T),
+//               g and beta per V head (fp32; rows outside the sequence get
+//               zero features and g = beta = 0, which makes every chunk a
+//               full 64-row chunk without changing the result).
+//   chain:    one CTA per (sequence, V head) walks its chunks in order.  The
+//             fp32 state S^T (dv x dk) lives in registers (one dv row per TMEM
+//             lane, 64 columns per thread); a bf16 copy in shared memory is the
+//             MMA operand.  Per chunk (transposed so that M = 128 throughout):
+//               [K;Q] K^T             -> K K^T (A), Q K^T (masked, decayed)
+//               T = (I + A)^-1 diag(beta)   (fp32, CUDA cores, blocked)
+//               U^T = V^T T^T,  W^T = K^T (T diag(e^b))^T
+//               P = S^T W^T,  O1 = S^T Q^T
+//               Delta^T = U^T - P
+//               D2 = (Delta^T diag(e^{b_last - b})) K,  O2 = Delta^T (QK^T (.) Gamma)^T
+//               S^T <- e^{b_last} S^T + D2,  O = O1 diag(e^b) + O2
+//             Every product is one tcgen05.mma chain (bf16 in, fp32 TMEM
+//             accumulators; 7 groups, 40 MMA instructions per chunk), issued
+//             by one thread and completed through tcgen05.commit -> mbarrier.
+//   The conv histories of checkpoints and of the final state come from the
+//   history kernel of prefill.cu.
+#include "gdn_common.cuh"
+#include "umma.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kC = 64;        // chunk
+constexpr int kD = 128;       // dk = dv
+constexpr int kTh = 256;      // chain / features CTA size
+constexpr uint32_t kKQBytes = 2 * 128 * 128;  // [K;Q] image: 2 blocks x 128 rows x 128 B
+constexpr uint32_t kVBytes = 2 * 64 * 128;    // V image: 2 atoms x 64 rows x 128 B
+constexpr uint32_t kGateBytes = 2 * kC * 4;   // g[64], beta[64]
+
+// TMEM columns
+constexpr uint32_t TM_KQ = 0, TM_U = 64, TM_W = 128, TM_P = 192, TM_O1 = 256, TM_O2 = 320,
+                   TM_D2 = 384, TM_COLS = 512;
+
+struct TcArgs {
+  float* ssm;
+  int32_t num_slots;
+  float* ck_ssm;
+  int32_t ck_num_slots;
+  const void* conv;
+  const float* conv_w;
+  const float* A_log;
+  const float* dt_bias;
+  const int32_t* slot_ids;
+  const int32_t* cu_seqlens;
+  const int64_t* start_pos;
+  int32_t n_seq;
+  int64_t total;
+  const int32_t* ckpt_ids;
+  int32_t max_ckpt;
+  int32_t ckpt_block;
+  const void* qkv;
+  const void* a;
+  const void* b;
+  void* out;
+  uint32_t* err;
+  int32_t* chunk_base;  // [n_seq + 1]
+  uint8_t* ws_kq;       // [n_chunks][hk][kKQBytes]
+  uint8_t* ws_v;        // [n_chunks][hv][kVBytes]
+  float* ws_gate;       // [n_chunks][hv][2][64]
+  int32_t n_chunks_max;
+  int32_t hk, hv, C, G;
+};
+
+__device__ __forceinline__ bool seq_ok(const TcArgs& a, int n, int64_t& t0, int64_t& len, int64_t& p0) {
+  t0 = a.cu_seqlens[n];
+  len = (int64_t)a.cu_seqlens[n + 1] - t0;
+  p0 = a.start_pos[n];
+  return !(t0 < 0 || len < 0 || t0 + len > a.total || p0 < 0);
+}
+
+__device__ __forceinline__ int n_chunks_of(int64_t p0, int64_t len) {
+  if (len <= 0) return 0;
+  return (int)((p0 + len + kC - 1) / kC - p0 / kC);
+}
+
+// ---------------------------------------------------------------------------
+// plan: chunk_base[n] = chunks of sequences 0..n-1 (one CTA, 1024 threads)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) plan_kernel(const TcArgs a) {
+  __shared__ int warp_sums[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (a.n_seq + 1023) / 1024;
+  const int lo = tid * per, hi = min(a.n_seq, lo + per);
+  int sum = 0;
+  for (int n = lo; n < hi; ++n) {
+    int64_t t0, len, p0;
+    if (seq_ok(a, n, t0, len, p0)) sum += n_chunks_of(p0, len);
+  }
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += v;
+    }
+    warp_sums[lane] = w;
+  }
+  __syncthreads();
+  int run = (warp ? warp_sums[warp - 1] : 0) + incl - sum;  // exclusive prefix of this thread
+  for (int n = lo; n < hi; ++n) {
+    a.chunk_base[n] = run;
+    int64_t t0, len, p0;
+    if (seq_ok(a, n, t0, len, p0)) run += n_chunks_of(p0, len);
+  }
+  if (tid == 1023) a.chunk_base[a.n_seq] = warp_sums[31];
+}
+
+__device__ __forceinline__ int seq_of_chunk(const int32_t* base, int n_seq, int gc) {
+  int lo = 0, hi = n_seq - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (base[mid] <= gc) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// ---------------------------------------------------------------------------
+// features: grid (n_chunks_max, hk), 256 threads
+// ---------------------------------------------------------------------------
+template <typename Tact, typename Tconv>
+__global__ void __launch_bounds__(kTh) tc_features_kernel(const TcArgs a) {
+  extern __shared__ __align__(16) float ys[];  // [64][256]: q | k conv+SiLU outputs
+  __shared__ float snorm[kC][2];
+  const int gc = blockIdx.x, hq = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (gc >= a.chunk_base[a.n_seq]) return;
+  const int n = seq_of_chunk(a.chunk_base, a.n_seq, gc);
+  int64_t t0, len, p0;
+  if (!seq_ok(a, n, t0, len, p0)) return;
+  const int32_t slot = a.slot_ids[n];
+  if (slot_class(slot, a.num_slots)) return;
+  const int64_t P = (p0 / kC + (gc - a.chunk_base[n])) * kC;  // absolute position of row 0
+  const int64_t p1 = p0 + len;
+  const Tact* qkv = reinterpret_cast<const Tact*>(a.qkv);
+  const Tconv* hist = reinterpret_cast<const Tconv*>(a.conv) + (size_t)slot * 3 * a.C;
+  const int GD = a.G * kD;
+  const int npairs = (2 * kD + GD) / 2;
+  uint8_t* kq = a.ws_kq + ((size_t)gc * a.hk + hq) * kKQBytes;
+
+  for (int cp = tid; cp < npairs; cp += kTh) {
+    const int lc = 2 * cp;  // local channel (even)
+    const size_t c = lc < kD ? (size_t)hq * kD + lc
+                   : lc < 2 * kD ? (size_t)a.hk * kD + (size_t)hq * kD + (lc - kD)
+                                 : 2 * (size_t)a.hk * kD + (size_t)hq * GD + (lc - 2 * kD);
+    const float4 w0 = *reinterpret_cast<const float4*>(a.conv_w + c * 4);
+    const float4 w1 = *reinterpret_cast<const float4*>(a.conv_w + (c + 1) * 4);
+    auto raw = [&](int64_t pos, float& x0, float& x1) {
+      x0 = 0.f;
+      x1 = 0.f;
+      if (pos >= p0 && pos < p1) {
+        const Tact* s = qkv + (size_t)(t0 + pos - p0) * a.C + c;
+        x0 = to_f32(s[0]);
+        x1 = to_f32(s[1]);
+      } else if (pos < p0 && pos >= p0 - 3) {
+        const Tconv* s = hist + (size_t)(3 - (p0 - pos)) * a.C + c;
+        x0 = to_f32(s[0]);
+        x1 = to_f32(s[1]);
+      }
+    };
+    float a0, a1, b0, b1, c0_, c1_;
+    raw(P - 3, a0, a1);
+    raw(P - 2, b0, b1);
+    raw(P - 1, c0_, c1_);
+    for (int r = 0; r < kC; ++r) {
+      float x0, x1;
+      raw(P + r, x0, x1);
+      const bool valid = P + r >= p0 && P + r < p1;
+      float y0 = w0.x * a0;
+      y0 = fmaf(w0.y, b0, y0);
+      y0 = fmaf(w0.z, c0_, y0);
+      y0 = fmaf(w0.w, x0, y0);
+      float y1 = w1.x * a1;
+      y1 = fmaf(w1.y, b1, y1);
+      y1 = fmaf(w1.z, c1_, y1);
+      y1 = fmaf(w1.w, x1, y1);
+      y0 = valid ? silu_f(y0) : 0.f;
+      y1 = valid ? silu_f(y1) : 0.f;
+      a0 = b0; a1 = b1;
+      b0 = c0_; b1 = c1_;
+      c0_ = x0; c1_ = x1;
+      if (lc < 2 * kD) {
+        ys[r * (2 * kD) + lc] = y0;
+        ys[r * (2 * kD) + lc + 1] = y1;
+      } else {
+        const int vl = lc - 2 * kD;  // channel within the group's v channels
+        const int h = hq * a.G + vl / kD, d = vl % kD;
+        uint8_t* vimg = a.ws_v + ((size_t)gc * a.hv + h) * kVBytes;
+        __nv_bfloat162 p = __floats2bfloat162_rn(y0, y1);
+        *reinterpret_cast<__nv_bfloat162*>(vimg + umma::sw128_off(r, d, 64 * 128)) = p;
+      }
+    }
+  }
+  // gates (rows outside the sequence: g = beta = 0)
+  for (int e = tid; e < kC * a.G; e += kTh) {
+    const int r = e % kC, gi = e / kC;
+    const int h = hq * a.G + gi;
+    const int64_t pos = P + r;
+    float gv = 0.f, bv = 0.f;
+    if (pos >= p0 && pos < p1) {
+      const size_t tok = (size_t)(t0 + pos - p0);
+      const float av = to_f32(reinterpret_cast<const Tact*>(a.a)[tok * a.hv + h]);
+      const float bb = to_f32(reinterpret_cast<const Tact*>(a.b)[tok * a.hv + h]);
+      gv = -expf(a.A_log[h]) * softplus_f(av + a.dt_bias[h]);
+      bv = sigmoid_f(bb);
+    }
+    float* gt = a.ws_gate + ((size_t)gc * a.hv + h) * (2 * kC);
+    gt[r] = gv;
+    gt[kC + r] = bv;
+  }
+  __syncthreads();
+  // per-row L2 norms of q and k
+  for (int r = warp; r < kC; r += kTh / 32) {
+    float sq = 0.f, sk = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float q = ys[r * (2 * kD) + lane + 32 * i];
+      const float k = ys[r * (2 * kD) + kD + lane + 32 * i];
+      sq = fmaf(q, q, sq);
+      sk = fmaf(k, k, sk);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      sq += __shfl_xor_sync(0xffffffffu, sq, o);
+      sk += __shfl_xor_sync(0xffffffffu, sk, o);
+    }
+    if (lane == 0) {
+      snorm[r][0] = rsqrtf(sq + kNormEps) * rsqrtf((float)kD);
+      snorm[r][1] = rsqrtf(sk + kNormEps);
+    }
+  }
+  __syncthreads();
+  // KQ image: rows 0..63 = k^, rows 64..127 = q^; 16-byte chunks of 8 values
+  for (int e = tid; e < 2 * kC * (kD / 8); e += kTh) {
+    const int R = e / (kD / 8), ch = e % (kD / 8);
+    const bool isq = R >= kC;
+    const int r = isq ? R - kC : R;
+    const float s = snorm[r][isq ? 0 : 1];
+    const float* src = ys + r * (2 * kD) + (isq ? 0 : kD) + ch * 8;
+    float v8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v8[i] = src[i] * s;
+    *reinterpret_cast<uint4*>(kq + umma::sw128_off(R, ch * 8, 128 * 128)) = umma::pack8_bf16(v8);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// chain: grid (hv, n_seq), 256 threads, one CTA per SM
+// ---------------------------------------------------------------------------
+struct __align__(1024) ChainSmem {
+  uint8_t kq[2][kKQBytes];
+  uint8_t v[2][kVBytes];
+  uint8_t st[2 * 128 * 128];  // S^T bf16 operand (K-major, 2 blocks of 64 dk)
+  uint8_t wt[128 * 128];      // W^T (MN-major B: 128 dk rows x 64 tokens); solve scratch
+  uint8_t dt[128 * 128];      // Delta^T (K-major A: 128 dv rows x 64 tokens); A (fp32) in the solve
+  uint8_t dtt[128 * 128];     // Delta^T diag(e^{b_last - b}); X (fp32) in the solve
+  uint8_t tm[64 * 128];       // T (K-major B: 64 rows x 64)
+  uint8_t tp[64 * 128];       // T diag(e^b)
+  uint8_t qk[64 * 128];       // QK^T (.) Gamma (.) lower-incl
+  float gates[2][2][kC];
+  float b[kC], eb[kC], ebl[kC];
+  uint64_t ld_full[2], mma_bar;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// all threads wait (bounded) on a barrier phase; uniform result
+__device__ __forceinline__ bool cta_wait(ChainSmem& S, uint64_t* bar, uint32_t parity) {
+  if (!mbar_wait(bar, parity)) S.abort = 1;
+  __syncthreads();
+  return !S.abort;
+}
+
+// X = (I + A)^-1 for the 64 x 64 strictly lower A (fp32, row stride 64):
+// 16 x 16 diagonal blocks by substitution, then merged 16 -> 32 -> 64 with
+// X_ba = -X_b A_ba X_a.  Y is 32 x 32 scratch.  256 threads.
+__device__ void unit_lower_inverse(const float* A, float* X, float* Y) {
+  const int tid = threadIdx.x;
+  if (tid < 64) {
+    const int i = tid >> 4, c = tid & 15, o = 16 * i;
+    float x[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      float s = (r == c) ? 1.f : 0.f;
+#pragma unroll
+      for (int m = 0; m < r; ++m) s = fmaf(-A[(o + r) * 64 + o + m], x[m], s);
+      x[r] = s;
+    }
+#pragma unroll
+    for (int r = 0; r < 16; ++r) X[(o + r) * 64 + o + c] = x[r];
+  }
+  __syncthreads();
+  // 16 -> 32: for both 32-blocks, Y = A10 X00 then X10 = -X11 Y
+  for (int e = tid; e < 512; e += kTh) {
+    const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15, o = 32 * blk;
+    float s = 0.f;
+    for (int m = c; m < 16; ++m) s = fmaf(A[(o + 16 + r) * 64 + o + m], X[(o + m) * 64 + o + c], s);
+    Y[blk * 256 + r * 16 + c] = s;
+  }
+  __syncthreads();
+  for (int e = tid; e < 512; e += kTh) {
+    const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15, o = 32 * blk;
+    float s = 0.f;
+    for (int m = 0; m <= r; ++m) s = fmaf(X[(o + 16 + r) * 64 + o + 16 + m], Y[blk * 256 + m * 16 + c], s);
+    X[(o + 16 + r) * 64 + o + c] = -s;
+  }
+  __syncthreads();
+  // 32 -> 64: Y = A_ba X_a, X_ba = -X_b Y
+  for (int e = tid; e < 1024; e += kTh) {
+    const int r = e >> 5, c = e & 31;
+    float s = 0.f;
+    for (int m = c; m < 32; ++m) s = fmaf(A[(32 + r) * 64 + m], X[m * 64 + c], s);
+    Y[r * 32 + c] = s;
+  }
+  __syncthreads();
+  for (int e = tid; e < 1024; e += kTh) {
+    const int r = e >> 5, c = e & 31;
+    float s = 0.f;
+    for (int m = 0; m <= r; ++m) s = fmaf(X[(32 + r) * 64 + 32 + m], Y[m * 32 + c], s);
+    X[(32 + r) * 64 + c] = -s;
+  }
+  __syncthreads();
+}
+
+template <typename Tact>
+__global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // the swizzled operand tiles need 1024-byte aligned bases
+  ChainSmem& S = *reinterpret_cast<ChainSmem*>(
+      smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023));
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int h = blockIdx.x, n = blockIdx.y, hq = h / a.G;
+  int64_t t0, len, p0;
+  if (!seq_ok(a, n, t0, len, p0)) {
+    if (h == 0 && tid == 0) report(a.err, GDN_DEV_ERR_SEQLENS);
+    return;
+  }
+  const int32_t slot = a.slot_ids[n];
+  Tact* out = reinterpret_cast<Tact*>(a.out);
+  const int cls = slot_class(slot, a.num_slots);
+  if (cls) {
+    if (cls == 2 && h == 0 && tid == 0) report(a.err, GDN_DEV_ERR_SLOT_OOB);
+    for (int64_t e = tid; e < len * kD; e += kTh)
+      out[((t0 + e / kD) * a.hv + h) * kD + (e % kD)] = from_f32<Tact>(0.f);
+    return;
+  }
+  const int nch = n_chunks_of(p0, len);
+  const int gc0 = a.chunk_base[n];
+  const int64_t p1 = p0 + len;
+
+  if (tid == 0) {
+    mbar_init(&S.ld_full[0], 1);
+    mbar_init(&S.ld_full[1], 1);
+    mbar_init(&S.mma_bar, 1);
+    S.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) umma::tmem_alloc(&S.tmem_base, TM_COLS);
+  umma::fence_before();
+  __syncthreads();
+  umma::fence_after();
+  const uint32_t tmem = S.tmem_base;
+  const int lrow = 32 * (warp & 3) + lane;  // TMEM lane = dv (or dk / token) row
+  const int half = warp >> 2;               // which 64-column half this warp handles
+  const uint32_t tlane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+
+  // state rows: S^T[lrow][64*half .. +64) in registers, bf16 copy as operand
+  float* gS = a.ssm + (((size_t)slot * a.hv + h) * kD + lrow) * kD + 64 * half;
+  float sreg[64];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float4 v = *reinterpret_cast<const float4*>(gS + 4 * i);
+    sreg[4 * i] = v.x;
+    sreg[4 * i + 1] = v.y;
+    sreg[4 * i + 2] = v.z;
+    sreg[4 * i + 3] = v.w;
+  }
+  umma::store_row64(S.st + half * (128 * 128), lrow, sreg);
+
+  auto issue_load = [&](int c) {
+    const int gc = gc0 + c, buf = c & 1;
+    mbar_arrive_expect_tx(&S.ld_full[buf], kKQBytes + kVBytes + kGateBytes);
+    bulk_g2s(S.kq[buf], a.ws_kq + ((size_t)gc * a.hk + hq) * kKQBytes, kKQBytes, &S.ld_full[buf]);
+    bulk_g2s(S.v[buf], a.ws_v + ((size_t)gc * a.hv + h) * kVBytes, kVBytes, &S.ld_full[buf]);
+    bulk_g2s(S.gates[buf], a.ws_gate + ((size_t)gc * a.hv + h) * (2 * kC), kGateBytes, &S.ld_full[buf]);
+  };
+  if (tid == 0 && nch > 0) issue_load(0);
+  umma::fence_proxy_async();
+  __syncthreads();
+
+  constexpr uint32_t ID_64_KK = umma::idesc_bf16(128, 64, false, false);
+  constexpr uint32_t ID_64_MK = umma::idesc_bf16(128, 64, true, false);
+  constexpr uint32_t ID_64_KM = umma::idesc_bf16(128, 64, false, true);
+  constexpr uint32_t ID_128_KM = umma::idesc_bf16(128, 128, false, true);
+  uint32_t mph = 0;
+  int issued = nch > 0 ? 1 : 0;
+  float* Af = reinterpret_cast<float*>(S.dt);
+  float* Xf = reinterpret_cast<float*>(S.dtt);
+  float* Yf = reinterpret_cast<float*>(S.wt);
+
+  for (int c = 0; c < nch; ++c) {
+    const int buf = c & 1;
+    const int64_t P = (p0 / kC + c) * kC;
+    if (tid == 0 && c + 1 < nch) {
+      issue_load(c + 1);
+      issued = c + 2;
+    }
+    if (!cta_wait(S, &S.ld_full[buf], (c >> 1) & 1)) break;
+    const uint32_t kq = smem_addr(S.kq[buf]), vv = smem_addr(S.v[buf]);
+    const uint32_t st = smem_addr(S.st);
+    // cumulative log-decay of the chunk
+    if (warp == 0) {
+      float carry = 0.f;
+      for (int hh = 0; hh < 2; ++hh) {
+        float v = S.gates[buf][0][32 * hh + lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float u = __shfl_up_sync(0xffffffffu, v, o);
+          if (lane >= o) v += u;
+        }
+        v += carry;
+        S.b[32 * hh + lane] = v;
+        carry = __shfl_sync(0xffffffffu, v, 31);
+      }
+    }
+    __syncthreads();
+    if (tid < kC) {
+      S.eb[tid] = expf(S.b[tid]);
+      S.ebl[tid] = expf(S.b[kC - 1] - S.b[tid]);
+    }
+    // [K;Q] K^T and S^T Q^T
+    if (tid == 0) {
+      umma::fence_after();
+      for (int s = 0; s < 8; ++s) {
+        const uint32_t ko = (s >> 2) * 16384 + (s & 3) * 32;
+        umma::mma_bf16(tmem + TM_KQ, umma::desc(kq + ko, 16, 1024), umma::desc(kq + ko, 16, 1024),
+                       ID_64_KK, s > 0);
+      }
+      for (int s = 0; s < 8; ++s) {
+        const uint32_t ko = (s >> 2) * 16384 + (s & 3) * 32;
+        umma::mma_bf16(tmem + TM_O1, umma::desc(st + ko, 16, 1024),
+                       umma::desc(kq + 8192 + ko, 16, 1024), ID_64_KK, s > 0);
+      }
+      umma::commit(&S.mma_bar);
+    }
+    if (!cta_wait(S, &S.mma_bar, mph)) break;
+    mph ^= 1;
+    umma::fence_after();
+    // A = strict_lower(beta (.) K K^T (.) Gamma) (fp32) and the decayed,
+    // masked Q K^T operand; lanes 0-63 hold K K^T rows, 64-127 Q K^T rows
+    {
+      float v[32];
+      umma::tmem_ld32(tlane + TM_KQ + 32 * half, v);
+      const int c0 = 32 * half;
+      if (lrow < kC) {
+        const int r = lrow;
+        const float br = S.b[r], betar = S.gates[buf][1][r];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int cc = c0 + i;
+          Af[r * 64 + cc] = cc < r ? betar * v[i] * expf(br - S.b[cc]) : 0.f;
+        }
+      } else {
+        const int t = lrow - kC;
+        const float bt = S.b[t];
+        float m[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int cc = c0 + i;
+          m[i] = cc <= t ? v[i] * expf(bt - S.b[cc]) : 0.f;
+        }
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          const int cch = 4 * half + ch;
+          *reinterpret_cast<uint4*>(S.qk + (t >> 3) * 1024 + (t & 7) * 128 + ((cch ^ (t & 7)) << 4)) =
+              umma::pack8_bf16(m + 8 * ch);
+        }
+      }
+    }
+    umma::fence_before();
+    __syncthreads();
+    unit_lower_inverse(Af, Xf, Yf);
+    // T = X diag(beta) and T' = X diag(beta e^b) as bf16 K-major tiles
+    for (int e = tid; e < kC * 8; e += kTh) {
+      const int r = e >> 3, ch = e & 7;
+      float t8[8], tp8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int cc = ch * 8 + i;
+        const float x = cc <= r ? Xf[r * 64 + cc] * S.gates[buf][1][cc] : 0.f;
+        t8[i] = x;
+        tp8[i] = x * S.eb[cc];
+      }
+      const uint32_t off = (r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4);
+      *reinterpret_cast<uint4*>(S.tm + off) = umma::pack8_bf16(t8);
+      *reinterpret_cast<uint4*>(S.tp + off) = umma::pack8_bf16(tp8);
+    }
+    umma::fence_proxy_async();
+    __syncthreads();
+    // U^T = V^T T^T ; W^T = K^T T'^T
+    if (tid == 0) {
+      umma::fence_after();
+      const uint32_t tm = smem_addr(S.tm), tp = smem_addr(S.tp);
+      for (int s = 0; s < 4; ++s)
+        umma::mma_bf16(tmem + TM_U, umma::desc(vv + s * 2048, 64 * 128, 1024),
+                       umma::desc(tm + s * 32, 16, 1024), ID_64_MK, s > 0);
+      for (int s = 0; s < 4; ++s)
+        umma::mma_bf16(tmem + TM_W, umma::desc(kq + s * 2048, 16384, 1024),
+                       umma::desc(tp + s * 32, 16, 1024), ID_64_MK, s > 0);
+      umma::commit(&S.mma_bar);
+    }
+    if (!cta_wait(S, &S.mma_bar, mph)) break;
+    mph ^= 1;
+    umma::fence_after();
+    // W^T -> bf16 MN-major B tile (row = dk, 64 tokens)
+    {
+      float v[32];
+      umma::tmem_ld32(tlane + TM_W + 32 * half, v);
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        const int cch = 4 * half + ch;
+        *reinterpret_cast<uint4*>(S.wt + (lrow >> 3) * 1024 + (lrow & 7) * 128 +
+                                  ((cch ^ (lrow & 7)) << 4)) = umma::pack8_bf16(v + 8 * ch);
+      }
+    }
+    umma::fence_proxy_async();
+    umma::fence_before();
+    __syncthreads();
+    // P = S^T W^T
+    if (tid == 0) {
+      umma::fence_after();
+      const uint32_t wt = smem_addr(S.wt);
+      for (int s = 0; s < 8; ++s) {
+        const uint32_t ko = (s >> 2) * 16384 + (s & 3) * 32;
+        umma::mma_bf16(tmem + TM_P, umma::desc(st + ko, 16, 1024), umma::desc(wt + s * 2048, 0, 1024),
+                       ID_64_KM, s > 0);
+      }
+      umma::commit(&S.mma_bar);
+    }
+    if (!cta_wait(S, &S.mma_bar, mph)) break;
+    mph ^= 1;
+    umma::fence_after();
+    // Delta^T = U^T - P, and its columns scaled by e^{b_last - b}
+    {
+      float u[32], p[32], d[32], dd[32];
+      umma::tmem_ld32(tlane + TM_U + 32 * half, u);
+      umma::tmem_ld32(tlane + TM_P + 32 * half, p);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        d[i] = u[i] - p[i];
+        dd[i] = d[i] * S.ebl[32 * half + i];
+      }
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        const int cch = 4 * half + ch;
+        const uint32_t off = (lrow >> 3) * 1024 + (lrow & 7) * 128 + ((cch ^ (lrow & 7)) << 4);
+        *reinterpret_cast<uint4*>(S.dt + off) = umma::pack8_bf16(d + 8 * ch);
+        *reinterpret_cast<uint4*>(S.dtt + off) = umma::pack8_bf16(dd + 8 * ch);
+      }
+    }
+    umma::fence_proxy_async();
+    umma::fence_before();
+    __syncthreads();
+    // D2 = Delta~^T K ; O2 = Delta^T (QK^T Gamma)^T
+    if (tid == 0) {
+      umma::fence_after();
+      const uint32_t dt = smem_addr(S.dt), dtt = smem_addr(S.dtt), qk = smem_addr(S.qk);
+      for (int s = 0; s < 4; ++s)
+        umma::mma_bf16(tmem + TM_D2, umma::desc(dtt + s * 32, 16, 1024),
+                       umma::desc(kq + s * 2048, 16384, 1024), ID_128_KM, s > 0);
+      for (int s = 0; s < 4; ++s)
+        umma::mma_bf16(tmem + TM_O2, umma::desc(dt + s * 32, 16, 1024), umma::desc(qk + s * 32, 16, 1024),
+                       ID_64_KK, s > 0);
+      umma::commit(&S.mma_bar);
+    }
+    if (!cta_wait(S, &S.mma_bar, mph)) break;
+    mph ^= 1;
+    umma::fence_after();
+    // S^T <- e^{b_last} S^T + D2 ; O = O1 diag(e^b) + O2
+    {
+      const float dec = S.eb[kC - 1];
+      float d2[32];
+      umma::tmem_ld32(tlane + TM_D2 + 64 * half, d2);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) sreg[i] = fmaf(dec, sreg[i], d2[i]);
+      umma::tmem_ld32(tlane + TM_D2 + 64 * half + 32, d2);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) sreg[32 + i] = fmaf(dec, sreg[32 + i], d2[i]);
+      float o1[32], o2[32];
+      umma::tmem_ld32(tlane + TM_O1 + 32 * half, o1);
+      umma::tmem_ld32(tlane + TM_O2 + 32 * half, o2);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int r = 32 * half + i;
+        const int64_t pos = P + r;
+        if (pos >= p0 && pos < p1)
+          out[((t0 + pos - p0) * a.hv + h) * kD + lrow] = from_f32<Tact>(fmaf(o1[i], S.eb[r], o2[i]));
+      }
+    }
+    umma::store_row64(S.st + half * (128 * 128), lrow, sreg);
+    // checkpoint at a block boundary
+    const int64_t pend = P + kC < p1 ? P + kC : p1;
+    if (pend % a.ckpt_block == 0) {
+      const int64_t idx = pend / a.ckpt_block - p0 / a.ckpt_block - 1;
+      if (idx >= 0 && idx < a.max_ckpt) {
+        const int32_t cid = a.ckpt_ids[(size_t)n * a.max_ckpt + idx];
+        if (slot_class(cid, a.ck_num_slots) == 0) {
+          float* cS = a.ck_ssm + (((size_t)cid * a.hv + h) * kD + lrow) * kD + 64 * half;
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            *reinterpret_cast<float4*>(cS + 4 * i) =
+                make_float4(sreg[4 * i], sreg[4 * i + 1], sreg[4 * i + 2], sreg[4 * i + 3]);
+        }
+      }
+    }
+    umma::fence_proxy_async();
+    umma::fence_before();
+    __syncthreads();
+  }
+  if (S.abort) {
+    if (tid == 0) {
+      report(a.err, GDN_DEV_ERR_TIMEOUT);
+      // let issued loads land before the shared memory goes away
+      for (int c = (issued > 2 ? issued - 2 : 0); c < issued; ++c) mbar_wait(&S.ld_full[c & 1], (c >> 1) & 1);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      *reinterpret_cast<float4*>(gS + 4 * i) =
+          make_float4(sreg[4 * i], sreg[4 * i + 1], sreg[4 * i + 2], sreg[4 * i + 3]);
+  }
+  umma::fence_before();
+  __syncthreads();
+  if (warp == 0) umma::tmem_dealloc(tmem, TM_COLS);
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// host side (declared in prefill_tc.cuh)
+// ---------------------------------------------------------------------------
+struct TcLayout {
+  size_t base, kq, v, gate, total;
+  int32_t n_chunks_max;
+};
+
+static TcLayout tc_layout(const gdn_dims& d, int32_t n_seq, int64_t total) {
+  TcLayout L;
+  L.n_chunks_max = (int32_t)(total / kC + 2 * (int64_t)n_seq);
+  size_t off = 0;
+  L.base = off; off += align256(sizeof(int32_t) * ((size_t)n_seq + 1));
+  L.kq = off; off += align256((size_t)L.n_chunks_max * d.hk * kKQBytes);
+  L.v = off; off += align256((size_t)L.n_chunks_max * d.hv * kVBytes);
+  L.gate = off; off += align256((size_t)L.n_chunks_max * d.hv * kGateBytes);
+  L.total = off;
+  return L;
+}
+
+bool prefill_tc_supported(const gdn_dims& d, const void* qkv, const gdn_params& p) {
+  if (d.dk != kD || d.dv != kD || d.conv_width != 4) return false;
+  if (d.hv / d.hk > 8) return false;
+  if (!aligned(qkv, 4) || !aligned(p.conv_w, 16)) return false;
+  return true;
+}
+
+size_t prefill_tc_workspace(const gdn_dims& d, int32_t n_seq, int64_t total) {
+  return tc_layout(d, n_seq, total).total;
+}
+
+template <typename Tact, typename Tconv>
+static cudaError_t launch_tc_t(const TcArgs& a, cudaStream_t s) {
+  plan_kernel<<<1, 1024, 0, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const size_t fsm = sizeof(float) * kC * 2 * kD;
+  auto fk = tc_features_kernel<Tact, Tconv>;
+  if ((e = cudaFuncSetAttribute(fk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsm)) != cudaSuccess)
+    return e;
+  fk<<<dim3((unsigned)a.n_chunks_max, (unsigned)a.hk), kTh, fsm, s>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  auto ck = tc_chain_kernel<Tact>;
+  const size_t csm = sizeof(ChainSmem) + 1024;
+  if ((e = cudaFuncSetAttribute(ck, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csm)) != cudaSuccess)
+    return e;
+  ck<<<dim3((unsigned)a.hv, (unsigned)a.n_seq), kTh, csm, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t prefill_tc_launch(const gdn_dims& d, const gdn_pool& pool, const gdn_pool& ckpt,
+                              const gdn_params& p, const int32_t* slot_ids, const int32_t* cu_seqlens,
+                              const int64_t* start_pos, int32_t n_seq, int64_t total,
+                              const int32_t* ckpt_ids, int32_t max_ckpt, int32_t ckpt_block,
+                              const void* qkv, const void* av, const void* bv, void* out,
+                              void* workspace, uint32_t* dev_err, cudaStream_t s) {
+  const TcLayout L = tc_layout(d, n_seq, total);
+  TcArgs a;
+  a.ssm = pool.ssm;
+  a.num_slots = pool.num_slots;
+  a.ck_ssm = ckpt.ssm;
+  a.ck_num_slots = max_ckpt > 0 ? ckpt.num_slots : 0;
+  a.conv = pool.conv;
+  a.conv_w = p.conv_w;
+  a.A_log = p.A_log;
+  a.dt_bias = p.dt_bias;
+  a.slot_ids = slot_ids;
+  a.cu_seqlens = cu_seqlens;
+  a.start_pos = start_pos;
+  a.n_seq = n_seq;
+  a.total = total;
+  a.ckpt_ids = ckpt_ids;
+  a.max_ckpt = max_ckpt;
+  a.ckpt_block = ckpt_block;
+  a.qkv = qkv;
+  a.a = av;
+  a.b = bv;
+  a.out = out;
+  a.err = dev_err;
+  uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+  a.chunk_base = reinterpret_cast<int32_t*>(ws + L.base);
+  a.ws_kq = ws + L.kq;
+  a.ws_v = ws + L.v;
+  a.ws_gate = reinterpret_cast<float*>(ws + L.gate);
+  a.n_chunks_max = L.n_chunks_max;
+  a.hk = d.hk;
+  a.hv = d.hv;
+  a.C = (int32_t)channels(d);
+  a.G = d.hv / d.hk;
+  if (d.act_dtype == GDN_BF16 && d.conv_dtype == GDN_BF16)
+    return launch_tc_t<__nv_bfloat16, __nv_bfloat16>(a, s);
+  if (d.act_dtype == GDN_BF16) return launch_tc_t<__nv_bfloat16, float>(a, s);
+  return launch_tc_t<float, float>(a, s);
+}
+
+}  // namespace gdn

@@ -1,0 +1,14 @@
+// Tensor-core (tcgen05) chunked prefill for dk = dv = 128; see prefill_tc.cu.
+#pragma once
+#include "gdn_common.cuh"
+
+namespace gdn {
+bool prefill_tc_supported(const gdn_dims& d, const void* qkv, const gdn_params& p);
+size_t prefill_tc_workspace(const gdn_dims& d, int32_t n_seq, int64_t total);
+cudaError_t prefill_tc_launch(const gdn_dims& d, const gdn_pool& pool, const gdn_pool& ckpt,
+                              const gdn_params& p, const int32_t* slot_ids, const int32_t* cu_seqlens,
+                              const int64_t* start_pos, int32_t n_seq, int64_t total,
+                              const int32_t* ckpt_ids, int32_t max_ckpt, int32_t ckpt_block,
+                              const void* qkv, const void* a, const void* b, void* out,
+                              void* workspace, uint32_t* dev_err, cudaStream_t s);
+}  // namespace gdn

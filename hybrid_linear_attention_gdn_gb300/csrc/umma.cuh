@@ -1,0 +1,130 @@
+// tcgen05 (5th-generation tensor core) helpers: shared-memory matrix
+// descriptors, the kind::f16 instruction descriptor, MMA issue/commit, TMEM
+// allocation and loads.  Inline PTX only.
+//
+// Shared-memory operand layouts used here (bf16, 128-byte swizzle):
+//  * K-major tile, R rows x 64 K: row r at (r/8)*1024 + (r%8)*128 bytes, its
+//    16-byte chunk k/8 stored at chunk (k/8) ^ (r%8); a wider K is stored as
+//    consecutive such 64-wide blocks.  One MMA k-step (16 elements) advances
+//    the descriptor start by 32 bytes inside a block.
+//  * MN-major tile, K rows x MN: the same 128-byte rows, each holding 64 MN
+//    elements of one k; wider MN uses further 64-wide atoms at the descriptor's
+//    leading byte offset.  One MMA k-step (16 rows) advances the start by 2048.
+// Both forms (and M = 128, N = 64..256) were checked against a CPU GEMM.
+#pragma once
+#include <stdint.h>
+
+#include "gdn_common.cuh"
+
+namespace gdn {
+namespace umma {
+
+constexpr uint32_t kSwizzle128 = 2;
+
+__device__ __forceinline__ uint64_t desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version
+  d |= (uint64_t)kSwizzle128 << 61;
+  return d;
+}
+
+// kind::f16 instruction descriptor: bf16 A and B, fp32 D.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
+                                         bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every MMA issued so far by this thread has completed.
+__device__ __forceinline__ void commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
+                   smem_addr(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+}
+__device__ __forceinline__ void fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+}
+// generic-proxy shared-memory writes -> visible to the tensor core / TMA
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
+// whole warp: allocate ncols TMEM columns, address written to *slot
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
+                   smem_addr(slot)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane (warp w reads lanes
+// 32*(w%4) .. +31; taddr already carries the lane base in bits 16..31).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// byte offset of element (row, col) in a K-major / MN-major 128B-swizzled tile
+// whose 64-wide column blocks are `block_bytes` apart
+__device__ __forceinline__ uint32_t sw128_off(int row, int col, uint32_t block_bytes) {
+  return (uint32_t)(col >> 6) * block_bytes + (uint32_t)(row >> 3) * 1024u + (uint32_t)(row & 7) * 128u +
+         (uint32_t)((((col & 63) >> 3) ^ (row & 7)) << 4) + (uint32_t)(col & 7) * 2u;
+}
+
+// pack 8 floats to 8 bf16 (round to nearest even) in one 16-byte value
+__device__ __forceinline__ uint4 pack8_bf16(const float* f) {
+  uint4 u;
+  __nv_bfloat162 p0 = __floats2bfloat162_rn(f[0], f[1]);
+  __nv_bfloat162 p1 = __floats2bfloat162_rn(f[2], f[3]);
+  __nv_bfloat162 p2 = __floats2bfloat162_rn(f[4], f[5]);
+  __nv_bfloat162 p3 = __floats2bfloat162_rn(f[6], f[7]);
+  u.x = *reinterpret_cast<uint32_t*>(&p0);
+  u.y = *reinterpret_cast<uint32_t*>(&p1);
+  u.z = *reinterpret_cast<uint32_t*>(&p2);
+  u.w = *reinterpret_cast<uint32_t*>(&p3);
+  return u;
+}
+
+// store one 64-element row (8 x 16-byte chunks) of a swizzled tile
+__device__ __forceinline__ void store_row64(uint8_t* tile, int row, const float* v64) {
+#pragma unroll
+  for (int ch = 0; ch < 8; ++ch) {
+    const uint32_t off = (uint32_t)(row >> 3) * 1024u + (uint32_t)(row & 7) * 128u +
+                         (uint32_t)((ch ^ (row & 7)) << 4);
+    *reinterpret_cast<uint4*>(tile + off) = pack8_bf16(v64 + ch * 8);
+  }
+}
+
+}  // namespace umma
+}  // namespace gdn
