@@ -335,7 +335,8 @@ def run_ours(args):
     e2e = {"value": whole_job_rate(B_HEAD, ws, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h}
 
-    rows = {} if args.no_rows else measure_rows(gdn, synth, dev, stream, hbm_peak, bf16_peak)
+    rows = {} if args.no_rows else measure_rows(gdn, synth, dev, stream, hbm_peak, bf16_peak,
+                                                args.rows, args.prefill_len)
 
     if rank != 0:
         return
@@ -355,8 +356,9 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
 
 
-def measure_rows(gdn, synth, dev, stream, hbm_peak, bf16_peak):
-    """Every other row of the hot path, timed with CUDA events (not headline)."""
+def measure_rows(gdn, synth, dev, stream, hbm_peak, bf16_peak, which="all", prefill_len=8192):
+    """Every other row of the hot path, timed with CUDA events (not headline).
+    which = "prefill" times only the chunked prefill (for profiling)."""
     import torch
     shape = synth.QWEN
     dims = gdn.Dims.of(shape)
@@ -374,8 +376,9 @@ def measure_rows(gdn, synth, dev, stream, hbm_peak, bf16_peak):
         return {"ms": ms, "algorithmic_GBps": gbs, "frac_hbm": gbs / hbm_peak}
 
     # batch sweep (state rotates over POOL // B disjoint sets where possible)
+    full = which == "all"
     sweep = {}
-    for B in [1, 2, 4, 8, 16, 32, 64, 128, 256]:
+    for B in ([1, 2, 4, 8, 16, 32, 64, 128, 256] if full else []):
         nsets = max(1, min(8, POOL // B))
         perm = torch.randperm(POOL, generator=g).to(torch.int32)
         sets = [perm[k * B:(k + 1) * B].to(dev) for k in range(nsets)]
@@ -398,49 +401,55 @@ def measure_rows(gdn, synth, dev, stream, hbm_peak, bf16_peak):
     pair_sets = [(perm[k * 128:k * 128 + 64].to(dev), perm[k * 128 + 64:(k + 1) * 128].to(dev))
                  for k in range(4)]
 
-    def fc(i):
-        s, d = pair_sets[i % 4]
-        gdn.slot_copy(dims, pool, pool, s, d)
-    fc(0)
-    rows["slot_copy_64"] = frac(64 * 2 * slot_bytes, _events_time(fc, reps, stream))
+    def slot_and_spec_rows():
+        def fc(i):
+            s, d = pair_sets[i % 4]
+            gdn.slot_copy(dims, pool, pool, s, d)
+        fc(0)
+        rows["slot_copy_64"] = frac(64 * 2 * slot_bytes, _events_time(fc, reps, stream))
 
-    def fz(i):
-        gdn.slot_zero(dims, pool, pair_sets[i % 4][1])
-    fz(0)
-    rows["slot_zero_64"] = frac(64 * slot_bytes, _events_time(fz, reps, stream))
+        def fz(i):
+            gdn.slot_zero(dims, pool, pair_sets[i % 4][1])
+        fz(0)
+        rows["slot_zero_64"] = frac(64 * slot_bytes, _events_time(fz, reps, stream))
 
-    # speculative verify, batch 16, T = 8, spec cache of 16 x 8 slots, then commit
-    B, T = 16, 8
-    spec = gdn.StatePool.empty(dims, 4 * B * T, dev)
-    spec_sets = [torch.arange(k * B * T, (k + 1) * B * T, dtype=torch.int32, device=dev).reshape(B, T)
-                 for k in range(4)]
-    work_sets = [perm[k * B:(k + 1) * B].to(dev) for k in range(4)]
-    vin = [tuple(t.to(dev) for t in synth.tokens(shape, g, (B, T))) for _ in range(4)]
-    vout = torch.empty((B, T, 32, 128), dtype=torch.bfloat16, device=dev)
-    L = synth.accept_lengths(B, T, g).to(dev)
+        # speculative verify, batch 16, T = 8, spec cache of 16 x 8 slots, then commit
+        B, T = 16, 8
+        spec = gdn.StatePool.empty(dims, 4 * B * T, dev)
+        spec_sets = [torch.arange(k * B * T, (k + 1) * B * T, dtype=torch.int32,
+                                  device=dev).reshape(B, T) for k in range(4)]
+        work_sets = [perm[k * B:(k + 1) * B].to(dev) for k in range(4)]
+        vin = [tuple(t.to(dev) for t in synth.tokens(shape, g, (B, T))) for _ in range(4)]
+        vout = torch.empty((B, T, 32, 128), dtype=torch.bfloat16, device=dev)
+        L = synth.accept_lengths(B, T, g).to(dev)
 
-    def fv(i):
-        q, a, b = vin[i % 4]
-        gdn.spec_verify(dims, pool, spec, params, work_sets[i % 4], spec_sets[i % 4], q, a, b, vout)
-    fv(0)
-    vbytes = B * (slot_bytes + T * (16384 + 128) + T * slot_bytes + T * 8192)
-    r = frac(vbytes, _events_time(fv, reps, stream))
-    r["draft_tokens_per_s"] = B * T / (r["ms"] * 1e-3)
-    rows["spec_verify_b16_t8"] = r
+        def fv(i):
+            q, a, b = vin[i % 4]
+            gdn.spec_verify(dims, pool, spec, params, work_sets[i % 4], spec_sets[i % 4], q, a, b,
+                            vout)
+        fv(0)
+        vbytes = B * (slot_bytes + T * (16384 + 128) + T * slot_bytes + T * 8192)
+        r = frac(vbytes, _events_time(fv, reps, stream))
+        r["draft_tokens_per_s"] = B * T / (r["ms"] * 1e-3)
+        rows["spec_verify_b16_t8"] = r
 
-    def fm(i):
-        gdn.spec_commit(dims, spec, pool, spec_sets[i % 4], L, work_sets[i % 4])
-    fm(0)
-    rows["spec_commit_b16"] = frac(B * 2 * slot_bytes, _events_time(fm, reps, stream))
+        def fm(i):
+            gdn.spec_commit(dims, spec, pool, spec_sets[i % 4], L, work_sets[i % 4])
+        fm(0)
+        rows["spec_commit_b16"] = frac(B * 2 * slot_bytes, _events_time(fm, reps, stream))
 
-    # chunked prefill: 4 sequences x 8192 tokens, checkpoints every 256
-    n_seq, S = 4, 8192
+    if full:
+        slot_and_spec_rows()
+
+    # chunked prefill: 4 sequences x prefill_len tokens, checkpoints every 256
+    n_seq, S = 4, prefill_len
     total = n_seq * S
     qkv, a, b = (t.to(dev) for t in synth.tokens(shape, g, (total,)))
     cu = torch.arange(0, total + 1, S, dtype=torch.int32, device=dev)
     sp = torch.zeros(n_seq, dtype=torch.int64, device=dev)
-    ck = gdn.StatePool.empty(dims, 128, dev)
-    ck_ids = torch.arange(128, dtype=torch.int32, device=dev).reshape(4, 32)
+    n_ck = S // 256
+    ck = gdn.StatePool.empty(dims, 4 * n_ck, dev)
+    ck_ids = torch.arange(4 * n_ck, dtype=torch.int32, device=dev).reshape(4, n_ck)
     pout = torch.empty((total, 32, 128), dtype=torch.bfloat16, device=dev)
     wsb = gdn.chunk_prefill_workspace_size(dims, n_seq, total)
     wsp = torch.empty(wsb, dtype=torch.uint8, device=dev)
@@ -451,9 +460,11 @@ def measure_rows(gdn, synth, dev, stream, hbm_peak, bf16_peak):
                           b, pout, wsp)
     fp(0)
     pms = _events_time(fp, 5, stream)
-    pbytes = total * (16384 + 128 + 8192) + (128 + 8) * slot_bytes
-    pflop = 1.92e11
-    rows["chunk_prefill_4x8192"] = {
+    # qkv, a, b and out per token; checkpoints plus each sequence's state read and written
+    pbytes = total * (16384 + 128 + 8192) + (4 * n_ck + 8) * slot_bytes
+    # ~11.7 MFLOP per (64-token chunk, V head) for the chunk form
+    pflop = total / 64 * 32 * 11.7e6
+    rows[f"chunk_prefill_4x{S}"] = {
         "ms": pms, "tokens_per_s": total / (pms * 1e-3),
         "algorithmic_GBps": pbytes / (pms * 1e-3) / 1e9,
         "frac_hbm": pbytes / (pms * 1e-3) / 1e9 / hbm_peak,
@@ -472,6 +483,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-rows", action="store_true", help="headline only")
+    ap.add_argument("--rows", default="all", choices=["all", "prefill"],
+                    help="which secondary rows to time (prefill: the chunked prefill alone)")
+    ap.add_argument("--prefill-len", type=int, default=8192,
+                    help="tokens per sequence of the 4-sequence prefill row (multiple of 256)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-soak", action="store_true",
                     help="skip the untimed 1 s warm loop that gives the clock sampler a window")

@@ -26,6 +26,21 @@ OUT_TOL_F32 = 1e-4
 STATE_TOL_1 = 1e-4
 STATE_TOL_64 = 5e-4
 PREFILL_TOL = 2e-3
+# Tensor-core prefill (dk = dv = 128): the workload fixes its intra-chunk
+# WY/UT contractions as bf16 with fp32 accumulation.  Rounding an operand to
+# bf16 perturbs it by a relative RMS of ~1.65e-3 (measured on the workload's
+# distributions); an output's dependency chain passes through four such
+# roundings (q^ and k^ into QK^T, the decayed/masked QK^T operand, Delta) plus
+# the bf16 output rounding: sqrt(5) * 1.65e-3 = 3.7e-3.  Bound: 5e-3 (about 35%
+# above the model) for outputs, final states and checkpoints.
+PREFILL_TC_TOL = 5e-3
+
+
+def prefill_tol(shape) -> float:
+    """The tensor-core path runs dk = dv = 128, width 4; other shapes run the
+    fp32 CUDA-core prefill."""
+    tc = shape.dk == 128 and shape.dv == 128 and shape.w == 4
+    return PREFILL_TC_TOL if tc else PREFILL_TOL
 
 
 def out_tol(shape) -> float:
