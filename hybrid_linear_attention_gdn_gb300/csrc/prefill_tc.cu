@@ -139,11 +139,22 @@ __device__ __forceinline__ int seq_of_chunk(const int32_t* base, int n_seq, int 
 }
 
 // ---------------------------------------------------------------------------
-// features: grid (n_chunks_max, hk), 256 threads
+// features: grid (n_chunks_max, hk), 256 threads; two launches:
+//   part 0: q and k of QK head hq (256 channels) -> L2 norms -> KQ image
+//   part 1: v of the G V heads reading hq (G*128 channels) -> V images, gates
+// Each CTA first stages its input tile (3 history rows + 64 token rows of its
+// channels) in shared memory with cp.async, so all loads are in flight at once.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
+}
+
 template <typename Tact, typename Tconv>
-__global__ void __launch_bounds__(kTh) tc_features_kernel(const TcArgs a) {
-  extern __shared__ __align__(16) float ys[];  // [64][256]: q | k conv+SiLU outputs
+__global__ void __launch_bounds__(kTh) tc_features_kernel(const TcArgs a, int part) {
+  extern __shared__ __align__(16) unsigned char fsm[];
   __shared__ float snorm[kC][2];
   const int gc = blockIdx.x, hq = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -155,81 +166,95 @@ __global__ void __launch_bounds__(kTh) tc_features_kernel(const TcArgs a) {
   if (slot_class(slot, a.num_slots)) return;
   const int64_t P = (p0 / kC + (gc - a.chunk_base[n])) * kC;  // absolute position of row 0
   const int64_t p1 = p0 + len;
+  const int GD = a.G * kD;
+  const int nch = part == 0 ? 2 * kD : GD;   // channels of this CTA
+  constexpr int EPC = 16 / sizeof(Tact);     // elements per 16-byte chunk
+  const int cpr = nch / EPC;                 // chunks per tile row
+  Tact* xs = reinterpret_cast<Tact*>(fsm);   // [kC + 3][nch], row i = position P - 3 + i
+  float* ys = reinterpret_cast<float*>(fsm + (size_t)(kC + 3) * nch * sizeof(Tact));  // part 0: [kC][256]
   const Tact* qkv = reinterpret_cast<const Tact*>(a.qkv);
   const Tconv* hist = reinterpret_cast<const Tconv*>(a.conv) + (size_t)slot * 3 * a.C;
-  const int GD = a.G * kD;
-  const int npairs = (2 * kD + GD) / 2;
-  uint8_t* kq = a.ws_kq + ((size_t)gc * a.hk + hq) * kKQBytes;
+  auto gchan = [&](int lc) -> size_t {  // global channel of local channel lc
+    if (part == 1) return 2 * (size_t)a.hk * kD + (size_t)hq * GD + lc;
+    return lc < kD ? (size_t)hq * kD + lc : (size_t)a.hk * kD + (size_t)hq * kD + (lc - kD);
+  };
+  for (int e = tid; e < (kC + 3) * cpr; e += kTh) {
+    const int i = e / cpr, ch = e % cpr;
+    const int64_t pos = P - 3 + i;
+    Tact* dst = xs + (size_t)i * nch + ch * EPC;
+    const size_t c = gchan(ch * EPC);
+    if (pos >= p0 && pos < p1) {
+      cp_async16(dst, qkv + (size_t)(t0 + pos - p0) * a.C + c);
+    } else if (pos < p0 && pos >= p0 - 3) {
+      const Tconv* src = hist + (size_t)(3 - (p0 - pos)) * a.C + c;
+#pragma unroll
+      for (int k = 0; k < EPC; ++k) dst[k] = from_f32<Tact>(to_f32(src[k]));
+    } else {
+#pragma unroll
+      for (int k = 0; k < EPC; ++k) dst[k] = from_f32<Tact>(0.f);
+    }
+  }
+  cp_async_wait_all();
+  __syncthreads();
 
-  for (int cp = tid; cp < npairs; cp += kTh) {
-    const int lc = 2 * cp;  // local channel (even)
-    const size_t c = lc < kD ? (size_t)hq * kD + lc
-                   : lc < 2 * kD ? (size_t)a.hk * kD + (size_t)hq * kD + (lc - kD)
-                                 : 2 * (size_t)a.hk * kD + (size_t)hq * GD + (lc - 2 * kD);
+  // conv1d + SiLU, one channel pair per thread walking the 64 rows
+  for (int cp = tid; cp < nch / 2; cp += kTh) {
+    const int lc = 2 * cp;
+    const size_t c = gchan(lc);
     const float4 w0 = *reinterpret_cast<const float4*>(a.conv_w + c * 4);
     const float4 w1 = *reinterpret_cast<const float4*>(a.conv_w + (c + 1) * 4);
-    auto raw = [&](int64_t pos, float& x0, float& x1) {
-      x0 = 0.f;
-      x1 = 0.f;
-      if (pos >= p0 && pos < p1) {
-        const Tact* s = qkv + (size_t)(t0 + pos - p0) * a.C + c;
-        x0 = to_f32(s[0]);
-        x1 = to_f32(s[1]);
-      } else if (pos < p0 && pos >= p0 - 3) {
-        const Tconv* s = hist + (size_t)(3 - (p0 - pos)) * a.C + c;
-        x0 = to_f32(s[0]);
-        x1 = to_f32(s[1]);
-      }
-    };
-    float a0, a1, b0, b1, c0_, c1_;
-    raw(P - 3, a0, a1);
-    raw(P - 2, b0, b1);
-    raw(P - 1, c0_, c1_);
+    float h0[3], h1[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      h0[k] = to_f32(xs[(size_t)k * nch + lc]);
+      h1[k] = to_f32(xs[(size_t)k * nch + lc + 1]);
+    }
     for (int r = 0; r < kC; ++r) {
-      float x0, x1;
-      raw(P + r, x0, x1);
+      const float x0 = to_f32(xs[(size_t)(r + 3) * nch + lc]);
+      const float x1 = to_f32(xs[(size_t)(r + 3) * nch + lc + 1]);
       const bool valid = P + r >= p0 && P + r < p1;
-      float y0 = w0.x * a0;
-      y0 = fmaf(w0.y, b0, y0);
-      y0 = fmaf(w0.z, c0_, y0);
+      float y0 = w0.x * h0[0];
+      y0 = fmaf(w0.y, h0[1], y0);
+      y0 = fmaf(w0.z, h0[2], y0);
       y0 = fmaf(w0.w, x0, y0);
-      float y1 = w1.x * a1;
-      y1 = fmaf(w1.y, b1, y1);
-      y1 = fmaf(w1.z, c1_, y1);
+      float y1 = w1.x * h1[0];
+      y1 = fmaf(w1.y, h1[1], y1);
+      y1 = fmaf(w1.z, h1[2], y1);
       y1 = fmaf(w1.w, x1, y1);
       y0 = valid ? silu_f(y0) : 0.f;
       y1 = valid ? silu_f(y1) : 0.f;
-      a0 = b0; a1 = b1;
-      b0 = c0_; b1 = c1_;
-      c0_ = x0; c1_ = x1;
-      if (lc < 2 * kD) {
+      h0[0] = h0[1]; h0[1] = h0[2]; h0[2] = x0;
+      h1[0] = h1[1]; h1[1] = h1[2]; h1[2] = x1;
+      if (part == 0) {
         ys[r * (2 * kD) + lc] = y0;
         ys[r * (2 * kD) + lc + 1] = y1;
       } else {
-        const int vl = lc - 2 * kD;  // channel within the group's v channels
-        const int h = hq * a.G + vl / kD, d = vl % kD;
+        const int h = hq * a.G + lc / kD, d = lc % kD;
         uint8_t* vimg = a.ws_v + ((size_t)gc * a.hv + h) * kVBytes;
-        __nv_bfloat162 p = __floats2bfloat162_rn(y0, y1);
-        *reinterpret_cast<__nv_bfloat162*>(vimg + umma::sw128_off(r, d, 64 * 128)) = p;
+        *reinterpret_cast<__nv_bfloat162*>(vimg + umma::sw128_off(r, d, 64 * 128)) =
+            __floats2bfloat162_rn(y0, y1);
       }
     }
   }
-  // gates (rows outside the sequence: g = beta = 0)
-  for (int e = tid; e < kC * a.G; e += kTh) {
-    const int r = e % kC, gi = e / kC;
-    const int h = hq * a.G + gi;
-    const int64_t pos = P + r;
-    float gv = 0.f, bv = 0.f;
-    if (pos >= p0 && pos < p1) {
-      const size_t tok = (size_t)(t0 + pos - p0);
-      const float av = to_f32(reinterpret_cast<const Tact*>(a.a)[tok * a.hv + h]);
-      const float bb = to_f32(reinterpret_cast<const Tact*>(a.b)[tok * a.hv + h]);
-      gv = -expf(a.A_log[h]) * softplus_f(av + a.dt_bias[h]);
-      bv = sigmoid_f(bb);
+  if (part == 1) {
+    // gates (rows outside the sequence: g = beta = 0)
+    for (int e = tid; e < kC * a.G; e += kTh) {
+      const int r = e % kC, gi = e / kC;
+      const int h = hq * a.G + gi;
+      const int64_t pos = P + r;
+      float gv = 0.f, bv = 0.f;
+      if (pos >= p0 && pos < p1) {
+        const size_t tok = (size_t)(t0 + pos - p0);
+        const float av = to_f32(reinterpret_cast<const Tact*>(a.a)[tok * a.hv + h]);
+        const float bb = to_f32(reinterpret_cast<const Tact*>(a.b)[tok * a.hv + h]);
+        gv = -expf(a.A_log[h]) * softplus_f(av + a.dt_bias[h]);
+        bv = sigmoid_f(bb);
+      }
+      float* gt = a.ws_gate + ((size_t)gc * a.hv + h) * (2 * kC);
+      gt[r] = gv;
+      gt[kC + r] = bv;
     }
-    float* gt = a.ws_gate + ((size_t)gc * a.hv + h) * (2 * kC);
-    gt[r] = gv;
-    gt[kC + r] = bv;
+    return;
   }
   __syncthreads();
   // per-row L2 norms of q and k
@@ -254,15 +279,16 @@ __global__ void __launch_bounds__(kTh) tc_features_kernel(const TcArgs a) {
   }
   __syncthreads();
   // KQ image: rows 0..63 = k^, rows 64..127 = q^; 16-byte chunks of 8 values
+  uint8_t* kq = a.ws_kq + ((size_t)gc * a.hk + hq) * kKQBytes;
   for (int e = tid; e < 2 * kC * (kD / 8); e += kTh) {
     const int R = e / (kD / 8), ch = e % (kD / 8);
     const bool isq = R >= kC;
     const int r = isq ? R - kC : R;
-    const float s = snorm[r][isq ? 0 : 1];
+    const float sc = snorm[r][isq ? 0 : 1];
     const float* src = ys + r * (2 * kD) + (isq ? 0 : kD) + ch * 8;
     float v8[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v8[i] = src[i] * s;
+    for (int i = 0; i < 8; ++i) v8[i] = src[i] * sc;
     *reinterpret_cast<uint4*>(kq + umma::sw128_off(R, ch * 8, 128 * 128)) = umma::pack8_bf16(v8);
   }
 }
@@ -294,9 +320,15 @@ __device__ __forceinline__ bool cta_wait(ChainSmem& S, uint64_t* bar, uint32_t p
   return !S.abort;
 }
 
-// X = (I + A)^-1 for the 64 x 64 strictly lower A (fp32, row stride 64):
-// 16 x 16 diagonal blocks by substitution, then merged 16 -> 32 -> 64 with
-// X_ba = -X_b A_ba X_a.  Y is 32 x 32 scratch.  256 threads.
+// Element (r, c) of the 64 x 64 fp32 matrices A and X: rows of 64 with the
+// column rotated by the row, so that a warp walking a column (one row per
+// lane) hits 32 different banks.
+__device__ __forceinline__ int ix(int r, int c) { return r * 64 + ((c + r) & 63); }
+
+// X = (I + A)^-1 for the 64 x 64 strictly lower A (fp32): 16 x 16 diagonal
+// blocks by substitution, then merged 16 -> 32 -> 64 with X_ba = -X_b A_ba X_a.
+// Inner loops have fixed trip counts (masked terms) so they unroll.  Y is
+// 32 x 32 scratch.  256 threads.
 __device__ void unit_lower_inverse(const float* A, float* X, float* Y) {
   const int tid = threadIdx.x;
   if (tid < 64) {
@@ -306,41 +338,65 @@ __device__ void unit_lower_inverse(const float* A, float* X, float* Y) {
     for (int r = 0; r < 16; ++r) {
       float s = (r == c) ? 1.f : 0.f;
 #pragma unroll
-      for (int m = 0; m < r; ++m) s = fmaf(-A[(o + r) * 64 + o + m], x[m], s);
+      for (int m = 0; m < r; ++m) s = fmaf(-A[ix(o + r, o + m)], x[m], s);
       x[r] = s;
     }
 #pragma unroll
-    for (int r = 0; r < 16; ++r) X[(o + r) * 64 + o + c] = x[r];
+    for (int r = 0; r < 16; ++r) X[ix(o + r, o + c)] = x[r];
   }
   __syncthreads();
   // 16 -> 32: for both 32-blocks, Y = A10 X00 then X10 = -X11 Y
-  for (int e = tid; e < 512; e += kTh) {
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int e = tid + k * kTh;
     const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15, o = 32 * blk;
     float s = 0.f;
-    for (int m = c; m < 16; ++m) s = fmaf(A[(o + 16 + r) * 64 + o + m], X[(o + m) * 64 + o + c], s);
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+      const float t = A[ix(o + 16 + r, o + m)] * X[ix(o + m, o + c)];
+      s += m >= c ? t : 0.f;
+    }
     Y[blk * 256 + r * 16 + c] = s;
   }
   __syncthreads();
-  for (int e = tid; e < 512; e += kTh) {
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int e = tid + k * kTh;
     const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15, o = 32 * blk;
     float s = 0.f;
-    for (int m = 0; m <= r; ++m) s = fmaf(X[(o + 16 + r) * 64 + o + 16 + m], Y[blk * 256 + m * 16 + c], s);
-    X[(o + 16 + r) * 64 + o + c] = -s;
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+      const float t = X[ix(o + 16 + r, o + 16 + m)] * Y[blk * 256 + m * 16 + c];
+      s += m <= r ? t : 0.f;
+    }
+    X[ix(o + 16 + r, o + c)] = -s;
   }
   __syncthreads();
   // 32 -> 64: Y = A_ba X_a, X_ba = -X_b Y
-  for (int e = tid; e < 1024; e += kTh) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int e = tid + k * kTh;
     const int r = e >> 5, c = e & 31;
     float s = 0.f;
-    for (int m = c; m < 32; ++m) s = fmaf(A[(32 + r) * 64 + m], X[m * 64 + c], s);
+#pragma unroll
+    for (int m = 0; m < 32; ++m) {
+      const float t = A[ix(32 + r, m)] * X[ix(m, c)];
+      s += m >= c ? t : 0.f;
+    }
     Y[r * 32 + c] = s;
   }
   __syncthreads();
-  for (int e = tid; e < 1024; e += kTh) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int e = tid + k * kTh;
     const int r = e >> 5, c = e & 31;
     float s = 0.f;
-    for (int m = 0; m <= r; ++m) s = fmaf(X[(32 + r) * 64 + 32 + m], Y[m * 32 + c], s);
-    X[(32 + r) * 64 + c] = -s;
+#pragma unroll
+    for (int m = 0; m < 32; ++m) {
+      const float t = X[ix(32 + r, 32 + m)] * Y[m * 32 + c];
+      s += m <= r ? t : 0.f;
+    }
+    X[ix(32 + r, c)] = -s;
   }
   __syncthreads();
 }
@@ -481,7 +537,7 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int cc = c0 + i;
-          Af[r * 64 + cc] = cc < r ? betar * v[i] * expf(br - S.b[cc]) : 0.f;
+          Af[ix(r, cc)] = cc < r ? betar * v[i] * __expf(br - S.b[cc]) : 0.f;
         }
       } else {
         const int t = lrow - kC;
@@ -490,7 +546,7 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int cc = c0 + i;
-          m[i] = cc <= t ? v[i] * expf(bt - S.b[cc]) : 0.f;
+          m[i] = cc <= t ? v[i] * __expf(bt - S.b[cc]) : 0.f;
         }
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
@@ -510,7 +566,7 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int cc = ch * 8 + i;
-        const float x = cc <= r ? Xf[r * 64 + cc] * S.gates[buf][1][cc] : 0.f;
+        const float x = cc <= r ? Xf[ix(r, cc)] * S.gates[buf][1][cc] : 0.f;
         t8[i] = x;
         tp8[i] = x * S.eb[cc];
       }
@@ -684,7 +740,7 @@ static TcLayout tc_layout(const gdn_dims& d, int32_t n_seq, int64_t total) {
 bool prefill_tc_supported(const gdn_dims& d, const void* qkv, const gdn_params& p) {
   if (d.dk != kD || d.dv != kD || d.conv_width != 4) return false;
   if (d.hv / d.hk > 8) return false;
-  if (!aligned(qkv, 4) || !aligned(p.conv_w, 16)) return false;
+  if (!aligned(qkv, 16) || !aligned(p.conv_w, 16)) return false;
   return true;
 }
 
@@ -697,12 +753,15 @@ static cudaError_t launch_tc_t(const TcArgs& a, cudaStream_t s) {
   plan_kernel<<<1, 1024, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const size_t fsm = sizeof(float) * kC * 2 * kD;
   auto fk = tc_features_kernel<Tact, Tconv>;
-  if ((e = cudaFuncSetAttribute(fk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsm)) != cudaSuccess)
-    return e;
-  fk<<<dim3((unsigned)a.n_chunks_max, (unsigned)a.hk), kTh, fsm, s>>>(a);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  for (int part = 0; part < 2; ++part) {
+    const int nch = part == 0 ? 2 * kD : a.G * kD;
+    const size_t fsm = (size_t)(kC + 3) * nch * sizeof(Tact) + (part == 0 ? sizeof(float) * kC * 2 * kD : 0);
+    if ((e = cudaFuncSetAttribute(fk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsm)) != cudaSuccess)
+      return e;
+    fk<<<dim3((unsigned)a.n_chunks_max, (unsigned)a.hk), kTh, fsm, s>>>(a, part);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   auto ck = tc_chain_kernel<Tact>;
   const size_t csm = sizeof(ChainSmem) + 1024;
   if ((e = cudaFuncSetAttribute(ck, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csm)) != cudaSuccess)

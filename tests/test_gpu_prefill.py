@@ -58,7 +58,7 @@ def test_prefill_vs_token_recurrence(cuda, shape, lens, starts, blk):
     torch.cuda.synchronize()
     assert err == 0
     tol = prefill_tol(shape)
-    assert_out_close(out, o_ref, shape.dv, tol)
+    assert_out_close(out, o_ref, shape.dv, tol, row_floor_rms=True)
     used = ids.tolist()
     assert max_rel_l2(to_np(st.pool.ssm[used]), st.opool.ssm[used], shape.dv * shape.dk) <= tol
     assert conv_bits_equal(st.pool.conv[used], st.opool.conv[used])
@@ -93,7 +93,7 @@ def test_prefill_four_by_8192_sampled_heads(cuda):
                                   to_np(qkv[t0:t1]), to_np(a[t0:t1]), to_np(b[t0:t1]), heads=heads)
         h0, h1 = heads
         tol = prefill_tol(shape)
-        assert_out_close(out[t0:t1, h0:h1], o_ref[:, h0:h1], 128, tol)
+        assert_out_close(out[t0:t1, h0:h1], o_ref[:, h0:h1], 128, tol, row_floor_rms=True)
         assert max_rel_l2(to_np(st.pool.ssm[int(ids[n]), h0:h1]), opool.ssm[0, h0:h1], 128 * 128) <= tol
         cks = ck_ids[n].tolist()
         assert max_rel_l2(to_np(ck.ssm[cks, h0:h1]), ock.ssm[:, h0:h1], 128 * 128) <= tol
