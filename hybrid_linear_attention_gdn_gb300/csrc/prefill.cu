@@ -473,12 +473,12 @@ cudaError_t launch_history(const PrefillArgs& a, int act, int cv, cudaStream_t s
 
 // The tensor-core path takes dk = dv = 128, width 4 (GDN_PREFILL_PATH=cuda
 // forces the CUDA-core path, for measurement).
-bool use_tc_prefill(const gdn_dims& d, const void* qkv, const gdn_params& p) {
+bool use_tc_prefill(const gdn_dims& d, const void* qkv, const void* out, const gdn_params& p) {
   static const bool forced_cuda = [] {
     const char* e = std::getenv("GDN_PREFILL_PATH");
     return e && !std::strcmp(e, "cuda");
   }();
-  return !forced_cuda && prefill_tc_supported(d, qkv, p);
+  return !forced_cuda && prefill_tc_supported(d, qkv, out, p);
 }
 
 }  // namespace
@@ -515,7 +515,7 @@ extern "C" gdn_status gdn_chunk_prefill(const gdn_dims* dims, gdn_pool pool, gdn
     return GDN_ERR_INVALID_ARG;
   if (total_tokens > 0 && (!qkv || !a || !b || !out)) return GDN_ERR_INVALID_ARG;
   const WsLayout wl = ws_layout(*dims, total_tokens);
-  const bool tc = use_tc_prefill(*dims, qkv, *params);
+  const bool tc = use_tc_prefill(*dims, qkv, out, *params);
   const size_t need = tc ? prefill_tc_workspace(*dims, n_seq, total_tokens) : wl.total;
   if (total_tokens > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
     return GDN_ERR_INVALID_ARG;

@@ -221,8 +221,10 @@ __global__ void __launch_bounds__(kTh) tc_features_kernel(const TcArgs a, int pa
       y1 = fmaf(w1.y, h1[1], y1);
       y1 = fmaf(w1.z, h1[2], y1);
       y1 = fmaf(w1.w, x1, y1);
-      y0 = valid ? silu_f(y0) : 0.f;
-      y1 = valid ? silu_f(y1) : 0.f;
+      // SiLU with the fast exponential and division: these values become
+      // bf16 operands, far coarser than either approximation
+      y0 = valid ? __fdividef(y0, 1.f + __expf(-y0)) : 0.f;
+      y1 = valid ? __fdividef(y1, 1.f + __expf(-y1)) : 0.f;
       h0[0] = h0[1]; h0[1] = h0[2]; h0[2] = x0;
       h1[0] = h1[1]; h1[1] = h1[2]; h1[2] = x1;
       if (part == 0) {
@@ -320,6 +322,39 @@ __device__ __forceinline__ bool cta_wait(ChainSmem& S, uint64_t* bar, uint32_t p
   return !S.abort;
 }
 
+// Warp-level tf32 MMA (m16n8k8, fp32 accumulate).  Fragment layout: lane =
+// 4 * g + t; A holds (g, t), (g + 8, t), (g, t + 4), (g + 8, t + 4); B holds
+// (t, g), (t + 4, g); D holds (g, 2t), (g, 2t + 1), (g + 8, 2t), (g + 8, 2t + 1).
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;\n" : "=r"(r) : "f"(x));
+  return r;
+}
+// d = L[r0 .. r0+16) x R[.., c0 .. c0+8) over k in [0, K); L(r, k), R(k, c)
+template <class LF, class RF>
+__device__ __forceinline__ void warp_tile_mm(float (&d)[4], int K, LF L, RF R, int r0, int c0) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  d[0] = d[1] = d[2] = d[3] = 0.f;
+  for (int k = 0; k < K; k += 8) {
+    const uint32_t a0 = to_tf32(L(r0 + g, k + t)), a1 = to_tf32(L(r0 + g + 8, k + t));
+    const uint32_t a2 = to_tf32(L(r0 + g, k + t + 4)), a3 = to_tf32(L(r0 + g + 8, k + t + 4));
+    const uint32_t b0 = to_tf32(R(k + t, c0 + g)), b1 = to_tf32(R(k + t + 4, c0 + g));
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+}
+template <class SF>
+__device__ __forceinline__ void warp_tile_store(const float (&d)[4], int r0, int c0, SF S) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  S(r0 + g, c0 + 2 * t, d[0]);
+  S(r0 + g, c0 + 2 * t + 1, d[1]);
+  S(r0 + g + 8, c0 + 2 * t, d[2]);
+  S(r0 + g + 8, c0 + 2 * t + 1, d[3]);
+}
+
 // Element (r, c) of the 64 x 64 fp32 matrices A and X: rows of 64 with the
 // column rotated by the row, so that a warp walking a column (one row per
 // lane) hits 32 different banks.
@@ -345,58 +380,43 @@ __device__ void unit_lower_inverse(const float* A, float* X, float* Y) {
     for (int r = 0; r < 16; ++r) X[ix(o + r, o + c)] = x[r];
   }
   __syncthreads();
-  // 16 -> 32: for both 32-blocks, Y = A10 X00 then X10 = -X11 Y
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const int e = tid + k * kTh;
-    const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15, o = 32 * blk;
-    float s = 0.f;
-#pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      const float t = A[ix(o + 16 + r, o + m)] * X[ix(o + m, o + c)];
-      s += m >= c ? t : 0.f;
-    }
-    Y[blk * 256 + r * 16 + c] = s;
+  // The merges are small dense products; each warp computes 16 x 8 output
+  // tiles with warp-level tf32 MMAs (T is rounded to bf16 afterwards, far
+  // coarser than tf32).  Entries above the diagonal of X are not stored and
+  // read as zero.
+  const int warp = tid >> 5;
+  // 16 -> 32, both 32-blocks: Y = A10 X00 (warps 0-3), then X10 = -X11 Y
+  if (warp < 4) {
+    const int o = 32 * (warp >> 1), c0 = 8 * (warp & 1);
+    float d[4];
+    warp_tile_mm(d, 16, [&](int r, int k) { return A[ix(o + 16 + r, o + k)]; },
+                 [&](int k, int c) { return k >= c ? X[ix(o + k, o + c)] : 0.f; }, 0, c0);
+    warp_tile_store(d, 0, c0, [&](int r, int c, float v) { Y[(o >> 5) * 256 + r * 16 + c] = v; });
   }
   __syncthreads();
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const int e = tid + k * kTh;
-    const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15, o = 32 * blk;
-    float s = 0.f;
-#pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      const float t = X[ix(o + 16 + r, o + 16 + m)] * Y[blk * 256 + m * 16 + c];
-      s += m <= r ? t : 0.f;
-    }
-    X[ix(o + 16 + r, o + c)] = -s;
+  if (warp < 4) {
+    const int o = 32 * (warp >> 1), c0 = 8 * (warp & 1);
+    float d[4];
+    warp_tile_mm(d, 16, [&](int r, int k) { return k <= r ? X[ix(o + 16 + r, o + 16 + k)] : 0.f; },
+                 [&](int k, int c) { return Y[(o >> 5) * 256 + k * 16 + c]; }, 0, c0);
+    warp_tile_store(d, 0, c0, [&](int r, int c, float v) { X[ix(o + 16 + r, o + c)] = -v; });
   }
   __syncthreads();
-  // 32 -> 64: Y = A_ba X_a, X_ba = -X_b Y
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int e = tid + k * kTh;
-    const int r = e >> 5, c = e & 31;
-    float s = 0.f;
-#pragma unroll
-    for (int m = 0; m < 32; ++m) {
-      const float t = A[ix(32 + r, m)] * X[ix(m, c)];
-      s += m >= c ? t : 0.f;
-    }
-    Y[r * 32 + c] = s;
+  // 32 -> 64: Y = A_ba X_a, then X_ba = -X_b Y (8 warps: 2 row tiles x 4 column tiles)
+  {
+    const int r0 = 16 * (warp >> 2), c0 = 8 * (warp & 3);
+    float d[4];
+    warp_tile_mm(d, 32, [&](int r, int k) { return A[ix(32 + r, k)]; },
+                 [&](int k, int c) { return k >= c ? X[ix(k, c)] : 0.f; }, r0, c0);
+    warp_tile_store(d, r0, c0, [&](int r, int c, float v) { Y[r * 32 + c] = v; });
   }
   __syncthreads();
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int e = tid + k * kTh;
-    const int r = e >> 5, c = e & 31;
-    float s = 0.f;
-#pragma unroll
-    for (int m = 0; m < 32; ++m) {
-      const float t = X[ix(32 + r, 32 + m)] * Y[m * 32 + c];
-      s += m <= r ? t : 0.f;
-    }
-    X[ix(32 + r, c)] = -s;
+  {
+    const int r0 = 16 * (warp >> 2), c0 = 8 * (warp & 3);
+    float d[4];
+    warp_tile_mm(d, 32, [&](int r, int k) { return k <= r ? X[ix(32 + r, 32 + k)] : 0.f; },
+                 [&](int k, int c) { return Y[k * 32 + c]; }, r0, c0);
+    warp_tile_store(d, r0, c0, [&](int r, int c, float v) { X[ix(32 + r, c)] = -v; });
   }
   __syncthreads();
 }
@@ -668,12 +688,12 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
       float o1[32], o2[32];
       umma::tmem_ld32(tlane + TM_O1 + 32 * half, o1);
       umma::tmem_ld32(tlane + TM_O2 + 32 * half, o2);
+      // stage O as [token][dv] in the (now free) W^T / Delta^T tiles
+      Tact* ot = reinterpret_cast<Tact*>(S.wt);
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const int r = 32 * half + i;
-        const int64_t pos = P + r;
-        if (pos >= p0 && pos < p1)
-          out[((t0 + pos - p0) * a.hv + h) * kD + lrow] = from_f32<Tact>(fmaf(o1[i], S.eb[r], o2[i]));
+        ot[r * kD + lrow] = from_f32<Tact>(fmaf(o1[i], S.eb[r], o2[i]));
       }
     }
     umma::store_row64(S.st + half * (128 * 128), lrow, sreg);
@@ -694,6 +714,19 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
     }
     umma::fence_proxy_async();
     umma::fence_before();
+    __syncthreads();
+    // output rows of the chunk's tokens: 16-byte stores of whole rows
+    {
+      constexpr int EPC = 16 / sizeof(Tact), CPR = kD / EPC;
+      const Tact* ot = reinterpret_cast<const Tact*>(S.wt);
+      for (int e = tid; e < kC * CPR; e += kTh) {
+        const int r = e / CPR, ch = e % CPR;
+        const int64_t pos = P + r;
+        if (pos >= p0 && pos < p1)
+          *reinterpret_cast<uint4*>(out + ((t0 + pos - p0) * a.hv + h) * kD + ch * EPC) =
+              *reinterpret_cast<const uint4*>(ot + r * kD + ch * EPC);
+      }
+    }
     __syncthreads();
   }
   if (S.abort) {
@@ -737,10 +770,10 @@ static TcLayout tc_layout(const gdn_dims& d, int32_t n_seq, int64_t total) {
   return L;
 }
 
-bool prefill_tc_supported(const gdn_dims& d, const void* qkv, const gdn_params& p) {
+bool prefill_tc_supported(const gdn_dims& d, const void* qkv, const void* out, const gdn_params& p) {
   if (d.dk != kD || d.dv != kD || d.conv_width != 4) return false;
   if (d.hv / d.hk > 8) return false;
-  if (!aligned(qkv, 16) || !aligned(p.conv_w, 16)) return false;
+  if (!aligned(qkv, 16) || !aligned(out, 16) || !aligned(p.conv_w, 16)) return false;
   return true;
 }
 

@@ -3,7 +3,7 @@
 #include "gdn_common.cuh"
 
 namespace gdn {
-bool prefill_tc_supported(const gdn_dims& d, const void* qkv, const gdn_params& p);
+bool prefill_tc_supported(const gdn_dims& d, const void* qkv, const void* out, const gdn_params& p);
 size_t prefill_tc_workspace(const gdn_dims& d, int32_t n_seq, int64_t total);
 cudaError_t prefill_tc_launch(const gdn_dims& d, const gdn_pool& pool, const gdn_pool& ckpt,
                               const gdn_params& p, const int32_t* slot_ids, const int32_t* cu_seqlens,
