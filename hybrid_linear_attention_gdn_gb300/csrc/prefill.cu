@@ -471,13 +471,12 @@ cudaError_t launch_history(const PrefillArgs& a, int act, int cv, cudaStream_t s
   return cudaGetLastError();
 }
 
-// The tensor-core path takes dk = dv = 128, width 4 (GDN_PREFILL_PATH=cuda
-// forces the CUDA-core path, for measurement).
+// The tensor-core path takes dk = dv = 128, width 4; GDN_PREFILL_PATH=cuda
+// forces the fp32 CUDA-core path (read on every call, so a process can time
+// or test both).
 bool use_tc_prefill(const gdn_dims& d, const void* qkv, const void* out, const gdn_params& p) {
-  static const bool forced_cuda = [] {
-    const char* e = std::getenv("GDN_PREFILL_PATH");
-    return e && !std::strcmp(e, "cuda");
-  }();
+  const char* e = std::getenv("GDN_PREFILL_PATH");
+  const bool forced_cuda = e && !std::strcmp(e, "cuda");
   return !forced_cuda && prefill_tc_supported(d, qkv, out, p);
 }
 

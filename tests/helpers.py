@@ -34,13 +34,29 @@ PREFILL_TOL = 2e-3
 # the bf16 output rounding: sqrt(5) * 1.65e-3 = 3.7e-3.  Bound: 5e-3 (about 35%
 # above the model) for outputs, final states and checkpoints.
 PREFILL_TC_TOL = 5e-3
+# Rows of the tensor-core prefill: the rounding of q^ to bf16 moves a whole
+# output row coherently (the row is S q^, so its error is S dq^), and rows
+# whose q^ meets S's small directions get a larger share.  An fp64 emulation
+# of the chunk form with the same bf16 operand roundings, on the workload's
+# distributions (6 V heads x 1024 tokens), puts the worst RMS-floored row at
+# 1.0e-2 (2.5x the tensor's 4.05e-3; q^/k^ rounding alone: 8.6e-3 worst row
+# for 1.6e-3 overall).  Bound: 3x the tensor tolerance.
+PREFILL_TC_ROW_TOL = 3 * PREFILL_TC_TOL
 
 
-def prefill_tol(shape) -> float:
-    """The tensor-core path runs dk = dv = 128, width 4; other shapes run the
-    fp32 CUDA-core prefill."""
-    tc = shape.dk == 128 and shape.dv == 128 and shape.w == 4
-    return PREFILL_TC_TOL if tc else PREFILL_TOL
+def uses_tc_prefill(shape, path="tc") -> bool:
+    """The tensor-core path runs dk = dv = 128, width 4 unless the fp32
+    CUDA-core path is forced; other shapes always run the CUDA-core path."""
+    return path == "tc" and shape.dk == 128 and shape.dv == 128 and shape.w == 4
+
+
+def prefill_tol(shape, path="tc") -> float:
+    return PREFILL_TC_TOL if uses_tc_prefill(shape, path) else PREFILL_TOL
+
+
+def prefill_row_tol(shape, path="tc"):
+    """Per-row bound for assert_out_close (None: the default reading)."""
+    return PREFILL_TC_ROW_TOL if uses_tc_prefill(shape, path) else None
 
 
 def out_tol(shape) -> float:
@@ -69,18 +85,21 @@ def max_rel_l2(x, ref, axis_rows) -> float:
 UNIT_ROUNDOFF = {torch.bfloat16: 2.0 ** -8, torch.float32: 2.0 ** -24}
 
 
-def assert_out_close(out: torch.Tensor, ref, row: int, tol: float, row_floor_rms: bool = False):
+def assert_out_close(out: torch.Tensor, ref, row: int, tol: float, row_floor_rms: bool = False,
+                     row_tol: float | None = None):
     """Output check described in the module docstring.  row_floor_rms: a row's
     error is measured against max(its own norm, the RMS row norm of the
     tensor) - for bf16-operand arithmetic, whose error is absolute in scale
     (a row whose exact value is thousands of times below the typical row gets
-    the typical absolute error, not a proportionally smaller one)."""
+    the typical absolute error, not a proportionally smaller one).  row_tol
+    replaces the default per-row bound (tol + unit roundoff)."""
     x = to_np(out)
     ref = np.asarray(ref, np.float64)
     den = np.linalg.norm(ref)
     whole = np.linalg.norm(x - ref) / den if den > 0 else np.linalg.norm(x)
     assert whole <= tol, f"relative L2 of the output tensor {whole:.3e} > {tol:.1e}"
-    row_tol = tol + UNIT_ROUNDOFF[out.dtype]
+    if row_tol is None:
+        row_tol = tol + UNIT_ROUNDOFF[out.dtype]
     if row_floor_rms:
         xr, rr = x.reshape(-1, row), ref.reshape(-1, row)
         num = np.linalg.norm(xr - rr, axis=1)

@@ -7,7 +7,8 @@ import torch
 import hybrid_linear_attention_gdn_gb300 as gdn
 import oracle
 from hybrid_linear_attention_gdn_gb300 import StatePool, synth
-from helpers import assert_out_close, Setup, conv_bits_equal, max_rel_l2, prefill_tol, to_np
+from helpers import (assert_out_close, Setup, conv_bits_equal, max_rel_l2, prefill_row_tol, prefill_tol,
+                     to_np)
 
 pytestmark = pytest.mark.gpu
 
@@ -35,12 +36,17 @@ def _ck_pool(st, n):
     return p
 
 
-@pytest.mark.parametrize("shape,lens,starts,blk", [
-    (synth.TINY, [1, 37, 130, 300, 0], [0, 64, 100, 256, 5], 64),
-    (synth.QWEN, [70, 200, 513], [0, 128, 0], 256),
-    (synth.QWEN.replace(hk=2, hv=8, dk=64, dv=64), [129, 64, 3], [0, 192, 61], 64),
-], ids=["tiny", "qwen", "dk64_g4"])
-def test_prefill_vs_token_recurrence(cuda, shape, lens, starts, blk):
+@pytest.mark.parametrize("shape,lens,starts,blk,path", [
+    (synth.TINY, [1, 37, 130, 300, 0], [0, 64, 100, 256, 5], 64, "tc"),
+    (synth.QWEN, [70, 200, 513], [0, 128, 0], 256, "tc"),
+    (synth.QWEN, [70, 200, 513], [0, 128, 0], 256, "cuda"),
+    (synth.QWEN.replace(hk=2, hv=8, dk=64, dv=64), [129, 64, 3], [0, 192, 61], 64, "tc"),
+], ids=["tiny", "qwen", "qwen_fp32_path", "dk64_g4"])
+def test_prefill_vs_token_recurrence(cuda, monkeypatch, shape, lens, starts, blk, path):
+    """path "cuda" forces the fp32 CUDA-core prefill (the library reads
+    GDN_PREFILL_PATH on every call); it meets the stated 2e-3."""
+    if path == "cuda":
+        monkeypatch.setenv("GDN_PREFILL_PATH", "cuda")
     n = len(lens)
     n_slots = 8 if shape.dk == 16 else 12
     st = Setup(shape, seed=40, num_slots=n_slots)
@@ -57,8 +63,8 @@ def test_prefill_vs_token_recurrence(cuda, shape, lens, starts, blk):
                                 sp.numpy(), ck_ids.numpy(), blk, to_np(qkv), to_np(a), to_np(b))
     torch.cuda.synchronize()
     assert err == 0
-    tol = prefill_tol(shape)
-    assert_out_close(out, o_ref, shape.dv, tol, row_floor_rms=True)
+    tol = prefill_tol(shape, path)
+    assert_out_close(out, o_ref, shape.dv, tol, row_floor_rms=True, row_tol=prefill_row_tol(shape, path))
     used = ids.tolist()
     assert max_rel_l2(to_np(st.pool.ssm[used]), st.opool.ssm[used], shape.dv * shape.dk) <= tol
     assert conv_bits_equal(st.pool.conv[used], st.opool.conv[used])
@@ -93,7 +99,8 @@ def test_prefill_four_by_8192_sampled_heads(cuda):
                                   to_np(qkv[t0:t1]), to_np(a[t0:t1]), to_np(b[t0:t1]), heads=heads)
         h0, h1 = heads
         tol = prefill_tol(shape)
-        assert_out_close(out[t0:t1, h0:h1], o_ref[:, h0:h1], 128, tol, row_floor_rms=True)
+        assert_out_close(out[t0:t1, h0:h1], o_ref[:, h0:h1], 128, tol, row_floor_rms=True,
+                         row_tol=prefill_row_tol(shape))
         assert max_rel_l2(to_np(st.pool.ssm[int(ids[n]), h0:h1]), opool.ssm[0, h0:h1], 128 * 128) <= tol
         cks = ck_ids[n].tolist()
         assert max_rel_l2(to_np(ck.ssm[cks, h0:h1]), ock.ssm[:, h0:h1], 128 * 128) <= tol
