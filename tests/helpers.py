@@ -27,21 +27,22 @@ STATE_TOL_1 = 1e-4
 STATE_TOL_64 = 5e-4
 PREFILL_TOL = 2e-3
 # Tensor-core prefill (dk = dv = 128): the workload fixes its intra-chunk
-# WY/UT contractions as bf16 with fp32 accumulation.  Rounding an operand to
-# bf16 perturbs it by a relative RMS of ~1.65e-3 (measured on the workload's
-# distributions); an output's dependency chain passes through four such
-# roundings (q^ and k^ into QK^T, the decayed/masked QK^T operand, Delta) plus
-# the bf16 output rounding: sqrt(5) * 1.65e-3 = 3.7e-3.  Bound: 5e-3 (about 35%
-# above the model) for outputs, final states and checkpoints.
+# WY/UT contractions as bf16 products with fp32 accumulation, which puts the
+# error of exact bf16-operand arithmetic above the 2e-3 stated for bf16
+# outputs.  The bounds come from a float64 model of the chunk form with the
+# same operand roundings (tests/test_prefill_tolerance_model.py; 12 V heads x
+# 4096 tokens on the workload's distributions):
+#   output tensor relative L2: model 4.0e-3 -> 5e-3.  Five roundings of ~1.6e-3
+#     each (q^/k^, v, T, the masked Q K^T, Delta) plus the output's own.
+#   worst output row (RMS-floored): model 1.1e-2 -> 1.5e-2.  The rounding of q^
+#     moves a whole row coherently (the row is S q^, its error S dq^), so rows
+#     have a heavier tail than the output rounding alone gives.
+#   worst state / checkpoint matrix: model 5.8e-3 over 192 matrices -> 1e-2.
+#     The state is dominated by the last few tokens' rank-one terms, so it
+#     averages the roundings over few terms.
 PREFILL_TC_TOL = 5e-3
-# Rows of the tensor-core prefill: the rounding of q^ to bf16 moves a whole
-# output row coherently (the row is S q^, so its error is S dq^), and rows
-# whose q^ meets S's small directions get a larger share.  An fp64 emulation
-# of the chunk form with the same bf16 operand roundings, on the workload's
-# distributions (6 V heads x 1024 tokens), puts the worst RMS-floored row at
-# 1.0e-2 (2.5x the tensor's 4.05e-3; q^/k^ rounding alone: 8.6e-3 worst row
-# for 1.6e-3 overall).  Bound: 3x the tensor tolerance.
-PREFILL_TC_ROW_TOL = 3 * PREFILL_TC_TOL
+PREFILL_TC_ROW_TOL = 1.5e-2
+PREFILL_TC_STATE_TOL = 1e-2
 
 
 def uses_tc_prefill(shape, path="tc") -> bool:
@@ -52,6 +53,10 @@ def uses_tc_prefill(shape, path="tc") -> bool:
 
 def prefill_tol(shape, path="tc") -> float:
     return PREFILL_TC_TOL if uses_tc_prefill(shape, path) else PREFILL_TOL
+
+
+def prefill_state_tol(shape, path="tc") -> float:
+    return PREFILL_TC_STATE_TOL if uses_tc_prefill(shape, path) else PREFILL_TOL
 
 
 def prefill_row_tol(shape, path="tc"):

@@ -7,8 +7,8 @@ import torch
 import hybrid_linear_attention_gdn_gb300 as gdn
 import oracle
 from hybrid_linear_attention_gdn_gb300 import StatePool, synth
-from helpers import (assert_out_close, Setup, conv_bits_equal, max_rel_l2, prefill_row_tol, prefill_tol,
-                     to_np)
+from helpers import (assert_out_close, Setup, conv_bits_equal, max_rel_l2, prefill_row_tol, prefill_state_tol,
+                     prefill_tol, to_np)
 
 pytestmark = pytest.mark.gpu
 
@@ -66,11 +66,12 @@ def test_prefill_vs_token_recurrence(cuda, monkeypatch, shape, lens, starts, blk
     tol = prefill_tol(shape, path)
     assert_out_close(out, o_ref, shape.dv, tol, row_floor_rms=True, row_tol=prefill_row_tol(shape, path))
     used = ids.tolist()
-    assert max_rel_l2(to_np(st.pool.ssm[used]), st.opool.ssm[used], shape.dv * shape.dk) <= tol
+    stol = prefill_state_tol(shape, path)
+    assert max_rel_l2(to_np(st.pool.ssm[used]), st.opool.ssm[used], shape.dv * shape.dk) <= stol
     assert conv_bits_equal(st.pool.conv[used], st.opool.conv[used])
     written = [i for i in range(n_ck) if not np.all(ock.ssm[i] == -5.0)]
     assert len(written) == sum((s + L) // blk - s // blk for s, L in zip(starts, lens))
-    assert max_rel_l2(to_np(ck.ssm[written]), ock.ssm[written], shape.dv * shape.dk) <= tol
+    assert max_rel_l2(to_np(ck.ssm[written]), ock.ssm[written], shape.dv * shape.dk) <= stol
     assert conv_bits_equal(ck.conv, ock.conv)
     assert torch.all(ck.ssm[[i for i in range(n_ck) if i not in written]] == -5.0)
 
@@ -101,9 +102,10 @@ def test_prefill_four_by_8192_sampled_heads(cuda):
         tol = prefill_tol(shape)
         assert_out_close(out[t0:t1, h0:h1], o_ref[:, h0:h1], 128, tol, row_floor_rms=True,
                          row_tol=prefill_row_tol(shape))
-        assert max_rel_l2(to_np(st.pool.ssm[int(ids[n]), h0:h1]), opool.ssm[0, h0:h1], 128 * 128) <= tol
+        stol = prefill_state_tol(shape)
+        assert max_rel_l2(to_np(st.pool.ssm[int(ids[n]), h0:h1]), opool.ssm[0, h0:h1], 128 * 128) <= stol
         cks = ck_ids[n].tolist()
-        assert max_rel_l2(to_np(ck.ssm[cks, h0:h1]), ock.ssm[:, h0:h1], 128 * 128) <= tol
+        assert max_rel_l2(to_np(ck.ssm[cks, h0:h1]), ock.ssm[:, h0:h1], 128 * 128) <= stol
         assert conv_bits_equal(ck.conv[cks], ock.conv)
         assert conv_bits_equal(st.pool.conv[int(ids[n])], opool.conv[0])
 
