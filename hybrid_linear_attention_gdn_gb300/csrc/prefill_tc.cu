@@ -197,19 +197,22 @@ __global__ void __launch_bounds__(kTh) tc_features_kernel(const TcArgs a, int pa
   cp_async_wait_all();
   __syncthreads();
 
-  // conv1d + SiLU, one channel pair per thread walking the 64 rows
-  for (int cp = tid; cp < nch / 2; cp += kTh) {
-    const int lc = 2 * cp;
+  // conv1d + SiLU: a thread walks one channel pair through one 32-row half
+  // of the chunk (tile rows r0 .. r0 + 2 are the inputs before row r0)
+  const int npairs = nch / 2;
+  for (int job = tid; job < 2 * npairs; job += kTh) {
+    const int lc = 2 * (job % npairs), r0 = 32 * (job / npairs);
     const size_t c = gchan(lc);
     const float4 w0 = *reinterpret_cast<const float4*>(a.conv_w + c * 4);
     const float4 w1 = *reinterpret_cast<const float4*>(a.conv_w + (c + 1) * 4);
     float h0[3], h1[3];
 #pragma unroll
     for (int k = 0; k < 3; ++k) {
-      h0[k] = to_f32(xs[(size_t)k * nch + lc]);
-      h1[k] = to_f32(xs[(size_t)k * nch + lc + 1]);
+      h0[k] = to_f32(xs[(size_t)(r0 + k) * nch + lc]);
+      h1[k] = to_f32(xs[(size_t)(r0 + k) * nch + lc + 1]);
     }
-    for (int r = 0; r < kC; ++r) {
+#pragma unroll 4
+    for (int r = r0; r < r0 + 32; ++r) {
       const float x0 = to_f32(xs[(size_t)(r + 3) * nch + lc]);
       const float x1 = to_f32(xs[(size_t)(r + 3) * nch + lc + 1]);
       const bool valid = P + r >= p0 && P + r < p1;
@@ -330,15 +333,16 @@ __device__ __forceinline__ uint32_t to_tf32(float x) {
   asm("cvt.rna.tf32.f32 %0, %1;\n" : "=r"(r) : "f"(x));
   return r;
 }
-// d = L[r0 .. r0+16) x R[.., c0 .. c0+8) over k in [0, K); L(r, k), R(k, c)
+// d = L[0 .. 16) x R[.., 0 .. 8) over k in [k0, K); L(r, k), R(k, c)
 template <class LF, class RF>
-__device__ __forceinline__ void warp_tile_mm(float (&d)[4], int K, LF L, RF R, int r0, int c0) {
+__device__ __forceinline__ void warp_tile_mm(float (&d)[4], int k0, int K, LF L, RF R) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   d[0] = d[1] = d[2] = d[3] = 0.f;
-  for (int k = 0; k < K; k += 8) {
-    const uint32_t a0 = to_tf32(L(r0 + g, k + t)), a1 = to_tf32(L(r0 + g + 8, k + t));
-    const uint32_t a2 = to_tf32(L(r0 + g, k + t + 4)), a3 = to_tf32(L(r0 + g + 8, k + t + 4));
-    const uint32_t b0 = to_tf32(R(k + t, c0 + g)), b1 = to_tf32(R(k + t + 4, c0 + g));
+#pragma unroll
+  for (int k = k0; k < K; k += 8) {
+    const uint32_t a0 = to_tf32(L(g, k + t)), a1 = to_tf32(L(g + 8, k + t));
+    const uint32_t a2 = to_tf32(L(g, k + t + 4)), a3 = to_tf32(L(g + 8, k + t + 4));
+    const uint32_t b0 = to_tf32(R(k + t, g)), b1 = to_tf32(R(k + t + 4, g));
     asm volatile(
         "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};\n"
@@ -346,79 +350,138 @@ __device__ __forceinline__ void warp_tile_mm(float (&d)[4], int K, LF L, RF R, i
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
   }
 }
-template <class SF>
-__device__ __forceinline__ void warp_tile_store(const float (&d)[4], int r0, int c0, SF S) {
-  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  S(r0 + g, c0 + 2 * t, d[0]);
-  S(r0 + g, c0 + 2 * t + 1, d[1]);
-  S(r0 + g + 8, c0 + 2 * t, d[2]);
-  S(r0 + g + 8, c0 + 2 * t + 1, d[3]);
-}
 
 // Element (r, c) of the 64 x 64 fp32 matrices A and X: rows of 64 with the
 // column rotated by the row, so that a warp walking a column (one row per
 // lane) hits 32 different banks.
 __device__ __forceinline__ int ix(int r, int c) { return r * 64 + ((c + r) & 63); }
 
-// X = (I + A)^-1 for the 64 x 64 strictly lower A (fp32): 16 x 16 diagonal
-// blocks by substitution, then merged 16 -> 32 -> 64 with X_ba = -X_b A_ba X_a.
-// Inner loops have fixed trip counts (masked terms) so they unroll.  Y is
-// 32 x 32 scratch.  256 threads.
-__device__ void unit_lower_inverse(const float* A, float* X, float* Y) {
-  const int tid = threadIdx.x;
-  if (tid < 64) {
-    const int i = tid >> 4, c = tid & 15, o = 16 * i;
-    float x[16];
+// Byte offset of element (r, c) in a 64 x 64 bf16 K-major 128B-swizzled tile.
+__device__ __forceinline__ uint32_t t_off(int r, int c) {
+  return (uint32_t)(r >> 3) * 1024u + (uint32_t)(r & 7) * 128u + (uint32_t)((((c >> 3) ^ (r & 7))) << 4) +
+         (uint32_t)(c & 7) * 2u;
+}
+
+struct TOut {
+  uint8_t* tm;        // T = X diag(beta)
+  uint8_t* tp;        // T' = X diag(beta e^b)
+  const float* beta;  // [64]
+  const float* eb;    // [64]
+};
+
+// T and T' entries (r, c), (r, c + 1) (c even) as bf16 pairs
+__device__ __forceinline__ void put_t_pair(const TOut& o, int r, int c, float x0, float x1) {
+  const float t0 = x0 * o.beta[c], t1 = x1 * o.beta[c + 1];
+  const __nv_bfloat162 p = __floats2bfloat162_rn(t0, t1);
+  const __nv_bfloat162 q = __floats2bfloat162_rn(t0 * o.eb[c], t1 * o.eb[c + 1]);
+  const uint32_t off = t_off(r, c);
+  *reinterpret_cast<__nv_bfloat162*>(o.tm + off) = p;
+  *reinterpret_cast<__nv_bfloat162*>(o.tp + off) = q;
+}
+__device__ __forceinline__ void put_t(const TOut& o, int r, int c, float x) {
+  const float t = x * o.beta[c];
+  const uint32_t off = t_off(r, c);
+  *reinterpret_cast<__nv_bfloat16*>(o.tm + off) = __float2bfloat16_rn(t);
+  *reinterpret_cast<__nv_bfloat16*>(o.tp + off) = __float2bfloat16_rn(t * o.eb[c]);
+}
+
+// X = (I + A)^-1 for the 64 x 64 strictly lower A (fp32), written out as the
+// lower triangles of T = X diag(beta) and T' = X diag(beta e^b) (their upper
+// triangles stay zero).  8 x 8 diagonal blocks by substitution, then merged
+// 8 -> 16 -> 32 -> 64 with X_ba = -X_b (A_ba X_a), the products on warp-level
+// tf32 MMAs (T is rounded to bf16 afterwards, far coarser than tf32).  Each
+// output column tile j of X_ba needs only column tile j of A_ba X_a, so a warp
+// carries its tile through both products.  Entries above the diagonal of X are
+// never stored; reads mask them to zero.  Y: 2048 floats of scratch.  256
+// threads; the caller synchronises before (A complete) and after.
+__device__ void solve_T(const float* A, float* X, float* Y, const TOut& to) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+  // 8 x 8 diagonal blocks: warp w, lanes 0..7 = columns of block w
+  if (lane < 8) {
+    const int o = 8 * warp, c = lane;
+    float a[28];
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      float s = (r == c) ? 1.f : 0.f;
+    for (int r = 1, i = 0; r < 8; ++r)
 #pragma unroll
-      for (int m = 0; m < r; ++m) s = fmaf(-A[ix(o + r, o + m)], x[m], s);
-      x[r] = s;
+      for (int m = 0; m < r; ++m, ++i) a[i] = A[ix(o + r, o + m)];
+    float x[8];
+#pragma unroll
+    for (int r = 0, i = 0; r < 8; ++r) {
+      float sum = (r == c) ? 1.f : 0.f;
+#pragma unroll
+      for (int m = 0; m < r; ++m, ++i) sum = fmaf(-a[i], x[m], sum);
+      x[r] = sum;
     }
 #pragma unroll
-    for (int r = 0; r < 16; ++r) X[ix(o + r, o + c)] = x[r];
+    for (int r = 0; r < 8; ++r)
+      if (r >= c) {
+        X[ix(o + r, o + c)] = x[r];
+        put_t(to, o + r, o + c, x[r]);
+      }
   }
   __syncthreads();
-  // The merges are small dense products; each warp computes 16 x 8 output
-  // tiles with warp-level tf32 MMAs (T is rounded to bf16 afterwards, far
-  // coarser than tf32).  Entries above the diagonal of X are not stored and
-  // read as zero.
-  const int warp = tid >> 5;
-  // 16 -> 32, both 32-blocks: Y = A10 X00 (warps 0-3), then X10 = -X11 Y
+  // 8 -> 16: warps 0..3, block pair p (rows/cols 16p ..); M padded to 16
   if (warp < 4) {
-    const int o = 32 * (warp >> 1), c0 = 8 * (warp & 1);
+    const int o = 16 * warp;
+    float* Ys = Y + warp * 128;
     float d[4];
-    warp_tile_mm(d, 16, [&](int r, int k) { return A[ix(o + 16 + r, o + k)]; },
-                 [&](int k, int c) { return k >= c ? X[ix(o + k, o + c)] : 0.f; }, 0, c0);
-    warp_tile_store(d, 0, c0, [&](int r, int c, float v) { Y[(o >> 5) * 256 + r * 16 + c] = v; });
+    warp_tile_mm(d, 0, 8, [&](int r, int k) { return r < 8 ? A[ix(o + 8 + r, o + k)] : 0.f; },
+                 [&](int k, int c) { return k >= c ? X[ix(o + k, o + c)] : 0.f; });
+    Ys[g * 8 + 2 * t] = d[0];
+    Ys[g * 8 + 2 * t + 1] = d[1];
+    __syncwarp();
+    warp_tile_mm(d, 0, 8, [&](int r, int k) { return (r < 8 && k <= r) ? X[ix(o + 8 + r, o + 8 + k)] : 0.f; },
+                 [&](int k, int c) { return Ys[k * 8 + c]; });
+    X[ix(o + 8 + g, o + 2 * t)] = -d[0];
+    X[ix(o + 8 + g, o + 2 * t + 1)] = -d[1];
+    put_t_pair(to, o + 8 + g, o + 2 * t, -d[0], -d[1]);
   }
   __syncthreads();
+  // 16 -> 32: warps 0..3 = (pair q, column tile j)
   if (warp < 4) {
-    const int o = 32 * (warp >> 1), c0 = 8 * (warp & 1);
+    const int o = 32 * (warp >> 1), j = warp & 1;
+    float* Ys = Y + 512 + warp * 128;
     float d[4];
-    warp_tile_mm(d, 16, [&](int r, int k) { return k <= r ? X[ix(o + 16 + r, o + 16 + k)] : 0.f; },
-                 [&](int k, int c) { return Y[(o >> 5) * 256 + k * 16 + c]; }, 0, c0);
-    warp_tile_store(d, 0, c0, [&](int r, int c, float v) { X[ix(o + 16 + r, o + c)] = -v; });
+    warp_tile_mm(d, 0, 16, [&](int r, int k) { return A[ix(o + 16 + r, o + k)]; },
+                 [&](int k, int c) { return k >= 8 * j + c ? X[ix(o + k, o + 8 * j + c)] : 0.f; });
+    Ys[g * 8 + 2 * t] = d[0];
+    Ys[g * 8 + 2 * t + 1] = d[1];
+    Ys[(g + 8) * 8 + 2 * t] = d[2];
+    Ys[(g + 8) * 8 + 2 * t + 1] = d[3];
+    __syncwarp();
+    warp_tile_mm(d, 0, 16, [&](int r, int k) { return k <= r ? X[ix(o + 16 + r, o + 16 + k)] : 0.f; },
+                 [&](int k, int c) { return Ys[k * 8 + c]; });
+    const int cc = o + 8 * j + 2 * t;
+    X[ix(o + 16 + g, cc)] = -d[0];
+    X[ix(o + 16 + g, cc + 1)] = -d[1];
+    X[ix(o + 24 + g, cc)] = -d[2];
+    X[ix(o + 24 + g, cc + 1)] = -d[3];
+    put_t_pair(to, o + 16 + g, cc, -d[0], -d[1]);
+    put_t_pair(to, o + 24 + g, cc, -d[2], -d[3]);
   }
   __syncthreads();
-  // 32 -> 64: Y = A_ba X_a, then X_ba = -X_b Y (8 warps: 2 row tiles x 4 column tiles)
+  // 32 -> 64: warps = (column tile j, row half mh); the two warps of a column
+  // tile exchange their halves of Y_j = A_ba X_a[:, j] through a named barrier
   {
-    const int r0 = 16 * (warp >> 2), c0 = 8 * (warp & 3);
+    const int j = warp & 3, mh = warp >> 2;
+    float* Ys = Y + 1024 + j * 256;  // 32 x 8
     float d[4];
-    warp_tile_mm(d, 32, [&](int r, int k) { return A[ix(32 + r, k)]; },
-                 [&](int k, int c) { return k >= c ? X[ix(k, c)] : 0.f; }, r0, c0);
-    warp_tile_store(d, r0, c0, [&](int r, int c, float v) { Y[r * 32 + c] = v; });
+    warp_tile_mm(d, 8 * j, 32, [&](int r, int k) { return A[ix(32 + 16 * mh + r, k)]; },
+                 [&](int k, int c) { return k >= 8 * j + c ? X[ix(k, 8 * j + c)] : 0.f; });
+    const int yr = 16 * mh + g;
+    Ys[yr * 8 + 2 * t] = d[0];
+    Ys[yr * 8 + 2 * t + 1] = d[1];
+    Ys[(yr + 8) * 8 + 2 * t] = d[2];
+    Ys[(yr + 8) * 8 + 2 * t + 1] = d[3];
+    named_sync(1 + j, 64);
+    warp_tile_mm(d, 0, 16 + 16 * mh,
+                 [&](int r, int k) { return k <= 16 * mh + r ? X[ix(32 + 16 * mh + r, 32 + k)] : 0.f; },
+                 [&](int k, int c) { return Ys[k * 8 + c]; });
+    const int cc = 8 * j + 2 * t;
+    put_t_pair(to, 32 + yr, cc, -d[0], -d[1]);
+    put_t_pair(to, 40 + yr, cc, -d[2], -d[3]);
   }
-  __syncthreads();
-  {
-    const int r0 = 16 * (warp >> 2), c0 = 8 * (warp & 3);
-    float d[4];
-    warp_tile_mm(d, 32, [&](int r, int k) { return k <= r ? X[ix(32 + r, 32 + k)] : 0.f; },
-                 [&](int k, int c) { return Y[k * 32 + c]; }, r0, c0);
-    warp_tile_store(d, r0, c0, [&](int r, int c, float v) { X[ix(32 + r, c)] = -v; });
-  }
-  __syncthreads();
 }
 
 template <typename Tact>
@@ -475,6 +538,9 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
     sreg[4 * i + 3] = v.w;
   }
   umma::store_row64(S.st + half * (128 * 128), lrow, sreg);
+  // T and T' are lower triangular: their upper triangles are written only here
+  for (int e = tid; e < 2 * 64 * 128 / 16; e += kTh)
+    reinterpret_cast<uint4*>(e < 512 ? S.tm : S.tp)[e & 511] = make_uint4(0u, 0u, 0u, 0u);
 
   auto issue_load = [&](int c) {
     const int gc = gc0 + c, buf = c & 1;
@@ -548,16 +614,25 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
     // A = strict_lower(beta (.) K K^T (.) Gamma) (fp32) and the decayed,
     // masked Q K^T operand; lanes 0-63 hold K K^T rows, 64-127 Q K^T rows
     {
-      float v[32];
-      umma::tmem_ld32(tlane + TM_KQ + 32 * half, v);
+      float v[32], bc[32];
       const int c0 = 32 * half;
+      // the column decays, loaded before any store so none waits on one
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 b4 = *reinterpret_cast<const float4*>(S.b + c0 + 4 * i);
+        bc[4 * i] = b4.x;
+        bc[4 * i + 1] = b4.y;
+        bc[4 * i + 2] = b4.z;
+        bc[4 * i + 3] = b4.w;
+      }
+      umma::tmem_ld32(tlane + TM_KQ + 32 * half, v);
       if (lrow < kC) {
         const int r = lrow;
         const float br = S.b[r], betar = S.gates[buf][1][r];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int cc = c0 + i;
-          Af[ix(r, cc)] = cc < r ? betar * v[i] * __expf(br - S.b[cc]) : 0.f;
+          Af[ix(r, cc)] = cc < r ? betar * v[i] * __expf(br - bc[i]) : 0.f;
         }
       } else {
         const int t = lrow - kC;
@@ -566,7 +641,7 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int cc = c0 + i;
-          m[i] = cc <= t ? v[i] * __expf(bt - S.b[cc]) : 0.f;
+          m[i] = cc <= t ? v[i] * __expf(bt - bc[i]) : 0.f;
         }
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
@@ -578,22 +653,8 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
     }
     umma::fence_before();
     __syncthreads();
-    unit_lower_inverse(Af, Xf, Yf);
     // T = X diag(beta) and T' = X diag(beta e^b) as bf16 K-major tiles
-    for (int e = tid; e < kC * 8; e += kTh) {
-      const int r = e >> 3, ch = e & 7;
-      float t8[8], tp8[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int cc = ch * 8 + i;
-        const float x = cc <= r ? Xf[ix(r, cc)] * S.gates[buf][1][cc] : 0.f;
-        t8[i] = x;
-        tp8[i] = x * S.eb[cc];
-      }
-      const uint32_t off = (r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4);
-      *reinterpret_cast<uint4*>(S.tm + off) = umma::pack8_bf16(t8);
-      *reinterpret_cast<uint4*>(S.tp + off) = umma::pack8_bf16(tp8);
-    }
+    solve_T(Af, Xf, Yf, TOut{S.tm, S.tp, S.gates[buf][1], S.eb});
     umma::fence_proxy_async();
     __syncthreads();
     // U^T = V^T T^T ; W^T = K^T T'^T
@@ -688,13 +749,19 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
       float o1[32], o2[32];
       umma::tmem_ld32(tlane + TM_O1 + 32 * half, o1);
       umma::tmem_ld32(tlane + TM_O2 + 32 * half, o2);
+      float ebr[32];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 e4 = *reinterpret_cast<const float4*>(S.eb + 32 * half + 4 * i);
+        ebr[4 * i] = e4.x;
+        ebr[4 * i + 1] = e4.y;
+        ebr[4 * i + 2] = e4.z;
+        ebr[4 * i + 3] = e4.w;
+      }
       // stage O as [token][dv] in the (now free) W^T / Delta^T tiles
       Tact* ot = reinterpret_cast<Tact*>(S.wt);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int r = 32 * half + i;
-        ot[r * kD + lrow] = from_f32<Tact>(fmaf(o1[i], S.eb[r], o2[i]));
-      }
+      for (int i = 0; i < 32; ++i) ot[(32 * half + i) * kD + lrow] = from_f32<Tact>(fmaf(o1[i], ebr[i], o2[i]));
     }
     umma::store_row64(S.st + half * (128 * 128), lrow, sreg);
     // checkpoint at a block boundary
