@@ -226,8 +226,8 @@ __global__ void __launch_bounds__(kTh) tc_features_kernel(const TcArgs a, int pa
       y1 = fmaf(w1.w, x1, y1);
       // SiLU with the fast exponential and division: these values become
       // bf16 operands, far coarser than either approximation
-      y0 = valid ? __fdividef(y0, 1.f + __expf(-y0)) : 0.f;
-      y1 = valid ? __fdividef(y1, 1.f + __expf(-y1)) : 0.f;
+      y0 = valid ? __fdividef(y0, 1.f + exp_ftz(-y0)) : 0.f;
+      y1 = valid ? __fdividef(y1, 1.f + exp_ftz(-y1)) : 0.f;
       h0[0] = h0[1]; h0[1] = h0[2]; h0[2] = x0;
       h1[0] = h1[1]; h1[1] = h1[2]; h1[2] = x1;
       if (part == 0) {
@@ -333,22 +333,34 @@ __device__ __forceinline__ uint32_t to_tf32(float x) {
   asm("cvt.rna.tf32.f32 %0, %1;\n" : "=r"(r) : "f"(x));
   return r;
 }
-// d = L[0 .. 16) x R[.., 0 .. 8) over k in [k0, K); L(r, k), R(k, c)
-template <class LF, class RF>
-__device__ __forceinline__ void warp_tile_mm(float (&d)[4], int k0, int K, LF L, RF R) {
+// Fragments of one m16n8k8 step: A = L[0..16)[k..k+8), B = R[k..k+8)[0..8).
+template <class LF>
+__device__ __forceinline__ void frag_a(uint32_t (&a)[4], int k, LF L) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  a[0] = to_tf32(L(g, k + t));
+  a[1] = to_tf32(L(g + 8, k + t));
+  a[2] = to_tf32(L(g, k + t + 4));
+  a[3] = to_tf32(L(g + 8, k + t + 4));
+}
+template <class RF>
+__device__ __forceinline__ void frag_b(uint32_t (&b)[2], int k, RF R) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  b[0] = to_tf32(R(k + t, g));
+  b[1] = to_tf32(R(k + t + 4, g));
+}
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+// A 16 x 8 tile product over NK k-steps of 8 from preloaded fragments.
+template <int NK>
+__device__ __forceinline__ void tile_mm(float (&d)[4], const uint32_t (&a)[NK][4], const uint32_t (&b)[NK][2]) {
   d[0] = d[1] = d[2] = d[3] = 0.f;
 #pragma unroll
-  for (int k = k0; k < K; k += 8) {
-    const uint32_t a0 = to_tf32(L(g, k + t)), a1 = to_tf32(L(g + 8, k + t));
-    const uint32_t a2 = to_tf32(L(g, k + t + 4)), a3 = to_tf32(L(g + 8, k + t + 4));
-    const uint32_t b0 = to_tf32(R(k + t, g)), b1 = to_tf32(R(k + t + 4, g));
-    asm volatile(
-        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};\n"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-  }
+  for (int s = 0; s < NK; ++s) mma_tf32(d, a[s], b[s]);
 }
 
 // Element (r, c) of the 64 x 64 fp32 matrices A and X: rows of 64 with the
@@ -369,20 +381,14 @@ struct TOut {
   const float* eb;    // [64]
 };
 
-// T and T' entries (r, c), (r, c + 1) (c even) as bf16 pairs
-__device__ __forceinline__ void put_t_pair(const TOut& o, int r, int c, float x0, float x1) {
-  const float t0 = x0 * o.beta[c], t1 = x1 * o.beta[c + 1];
-  const __nv_bfloat162 p = __floats2bfloat162_rn(t0, t1);
-  const __nv_bfloat162 q = __floats2bfloat162_rn(t0 * o.eb[c], t1 * o.eb[c + 1]);
+// T and T' entries (r, c), (r, c + 1) (c even) as bf16 pairs; bc/ec are
+// beta and e^b of the two columns (loaded once per lane by the caller)
+__device__ __forceinline__ void put_t_pair(const TOut& o, int r, int c, float x0, float x1, const float2& bc,
+                                           const float2& ec) {
+  const float t0 = x0 * bc.x, t1 = x1 * bc.y;
   const uint32_t off = t_off(r, c);
-  *reinterpret_cast<__nv_bfloat162*>(o.tm + off) = p;
-  *reinterpret_cast<__nv_bfloat162*>(o.tp + off) = q;
-}
-__device__ __forceinline__ void put_t(const TOut& o, int r, int c, float x) {
-  const float t = x * o.beta[c];
-  const uint32_t off = t_off(r, c);
-  *reinterpret_cast<__nv_bfloat16*>(o.tm + off) = __float2bfloat16_rn(t);
-  *reinterpret_cast<__nv_bfloat16*>(o.tp + off) = __float2bfloat16_rn(t * o.eb[c]);
+  *reinterpret_cast<__nv_bfloat162*>(o.tm + off) = __floats2bfloat162_rn(t0, t1);
+  *reinterpret_cast<__nv_bfloat162*>(o.tp + off) = __floats2bfloat162_rn(t0 * ec.x, t1 * ec.y);
 }
 
 // X = (I + A)^-1 for the 64 x 64 strictly lower A (fp32), written out as the
@@ -391,20 +397,25 @@ __device__ __forceinline__ void put_t(const TOut& o, int r, int c, float x) {
 // 8 -> 16 -> 32 -> 64 with X_ba = -X_b (A_ba X_a), the products on warp-level
 // tf32 MMAs (T is rounded to bf16 afterwards, far coarser than tf32).  Each
 // output column tile j of X_ba needs only column tile j of A_ba X_a, so a warp
-// carries its tile through both products.  Entries above the diagonal of X are
-// never stored; reads mask them to zero.  Y: 2048 floats of scratch.  256
-// threads; the caller synchronises before (A complete) and after.
-__device__ void solve_T(const float* A, float* X, float* Y, const TOut& to) {
+// carries its tile through both products; every operand fragment is loaded
+// before the warp's first product, so a phase waits on one load latency.
+// Entries above the diagonal of X are never stored; reads mask them to zero.
+// Y: 2048 floats of scratch.  256 threads; the caller synchronises before (A
+// complete) and after.
+__device__ __forceinline__ void solve_T(const float* A, float* X, float* Y, const TOut& to) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
-  // 8 x 8 diagonal blocks: warp w, lanes 0..7 = columns of block w
-  if (lane < 8) {
-    const int o = 8 * warp, c = lane;
+  // 8 x 8 diagonal blocks: warp w, lanes 0..7 = columns of block w; the
+  // column pairs (2l, 2l+1) of lanes 0..3 are written as bf16 pairs
+  {
+    const int o = 8 * warp, c = lane & 7;
     float a[28];
 #pragma unroll
     for (int r = 1, i = 0; r < 8; ++r)
 #pragma unroll
       for (int m = 0; m < r; ++m, ++i) a[i] = A[ix(o + r, o + m)];
+    const float2 bc = make_float2(to.beta[o + 2 * (lane & 3)], to.beta[o + 2 * (lane & 3) + 1]);
+    const float2 ec = make_float2(to.eb[o + 2 * (lane & 3)], to.eb[o + 2 * (lane & 3) + 1]);
     float x[8];
 #pragma unroll
     for (int r = 0, i = 0; r < 8; ++r) {
@@ -413,74 +424,109 @@ __device__ void solve_T(const float* A, float* X, float* Y, const TOut& to) {
       for (int m = 0; m < r; ++m, ++i) sum = fmaf(-a[i], x[m], sum);
       x[r] = sum;
     }
+    if (lane < 8) {
 #pragma unroll
-    for (int r = 0; r < 8; ++r)
-      if (r >= c) {
-        X[ix(o + r, o + c)] = x[r];
-        put_t(to, o + r, o + c, x[r]);
-      }
+      for (int r = 0; r < 8; ++r)
+        if (r >= c) X[ix(o + r, o + c)] = x[r];
+    }
+    // lane l < 4 writes columns 2l, 2l+1 of every row: fetch the odd column
+    // from lane 2l+1 (entries above the diagonal are zero)
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const float x0 = __shfl_sync(0xffffffffu, x[r], 2 * (lane & 3));
+      const float x1 = __shfl_sync(0xffffffffu, x[r], 2 * (lane & 3) + 1);
+      if (lane < 4 && 2 * lane <= r) put_t_pair(to, o + r, o + 2 * lane, x0, r >= 2 * lane + 1 ? x1 : 0.f, bc, ec);
+    }
   }
   __syncthreads();
   // 8 -> 16: warps 0..3, block pair p (rows/cols 16p ..); M padded to 16
   if (warp < 4) {
     const int o = 16 * warp;
     float* Ys = Y + warp * 128;
+    uint32_t fa[1][4], fb[1][2], fx[1][4], fy[1][2];
+    frag_a(fa[0], 0, [&](int r, int k) { return r < 8 ? A[ix(o + 8 + r, o + k)] : 0.f; });
+    frag_b(fb[0], 0, [&](int k, int c) { return k >= c ? X[ix(o + k, o + c)] : 0.f; });
+    frag_a(fx[0], 0, [&](int r, int k) { return (r < 8 && k <= r) ? X[ix(o + 8 + r, o + 8 + k)] : 0.f; });
+    const float2 bc = make_float2(to.beta[o + 2 * t], to.beta[o + 2 * t + 1]);
+    const float2 ec = make_float2(to.eb[o + 2 * t], to.eb[o + 2 * t + 1]);
     float d[4];
-    warp_tile_mm(d, 0, 8, [&](int r, int k) { return r < 8 ? A[ix(o + 8 + r, o + k)] : 0.f; },
-                 [&](int k, int c) { return k >= c ? X[ix(o + k, o + c)] : 0.f; });
+    tile_mm<1>(d, fa, fb);
     Ys[g * 8 + 2 * t] = d[0];
     Ys[g * 8 + 2 * t + 1] = d[1];
     __syncwarp();
-    warp_tile_mm(d, 0, 8, [&](int r, int k) { return (r < 8 && k <= r) ? X[ix(o + 8 + r, o + 8 + k)] : 0.f; },
-                 [&](int k, int c) { return Ys[k * 8 + c]; });
+    frag_b(fy[0], 0, [&](int k, int c) { return Ys[k * 8 + c]; });
+    tile_mm<1>(d, fx, fy);
     X[ix(o + 8 + g, o + 2 * t)] = -d[0];
     X[ix(o + 8 + g, o + 2 * t + 1)] = -d[1];
-    put_t_pair(to, o + 8 + g, o + 2 * t, -d[0], -d[1]);
+    put_t_pair(to, o + 8 + g, o + 2 * t, -d[0], -d[1], bc, ec);
   }
   __syncthreads();
   // 16 -> 32: warps 0..3 = (pair q, column tile j)
   if (warp < 4) {
     const int o = 32 * (warp >> 1), j = warp & 1;
     float* Ys = Y + 512 + warp * 128;
+    uint32_t fa[2][4], fb[2][2], fx[2][4], fy[2][2];
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      frag_a(fa[s], 8 * s, [&](int r, int k) { return A[ix(o + 16 + r, o + k)]; });
+      frag_b(fb[s], 8 * s, [&](int k, int c) { return k >= 8 * j + c ? X[ix(o + k, o + 8 * j + c)] : 0.f; });
+      frag_a(fx[s], 8 * s, [&](int r, int k) { return k <= r ? X[ix(o + 16 + r, o + 16 + k)] : 0.f; });
+    }
+    const int cc = o + 8 * j + 2 * t;
+    const float2 bc = make_float2(to.beta[cc], to.beta[cc + 1]);
+    const float2 ec = make_float2(to.eb[cc], to.eb[cc + 1]);
     float d[4];
-    warp_tile_mm(d, 0, 16, [&](int r, int k) { return A[ix(o + 16 + r, o + k)]; },
-                 [&](int k, int c) { return k >= 8 * j + c ? X[ix(o + k, o + 8 * j + c)] : 0.f; });
+    tile_mm<2>(d, fa, fb);
     Ys[g * 8 + 2 * t] = d[0];
     Ys[g * 8 + 2 * t + 1] = d[1];
     Ys[(g + 8) * 8 + 2 * t] = d[2];
     Ys[(g + 8) * 8 + 2 * t + 1] = d[3];
     __syncwarp();
-    warp_tile_mm(d, 0, 16, [&](int r, int k) { return k <= r ? X[ix(o + 16 + r, o + 16 + k)] : 0.f; },
-                 [&](int k, int c) { return Ys[k * 8 + c]; });
-    const int cc = o + 8 * j + 2 * t;
+#pragma unroll
+    for (int s = 0; s < 2; ++s) frag_b(fy[s], 8 * s, [&](int k, int c) { return Ys[k * 8 + c]; });
+    tile_mm<2>(d, fx, fy);
     X[ix(o + 16 + g, cc)] = -d[0];
     X[ix(o + 16 + g, cc + 1)] = -d[1];
     X[ix(o + 24 + g, cc)] = -d[2];
     X[ix(o + 24 + g, cc + 1)] = -d[3];
-    put_t_pair(to, o + 16 + g, cc, -d[0], -d[1]);
-    put_t_pair(to, o + 24 + g, cc, -d[2], -d[3]);
+    put_t_pair(to, o + 16 + g, cc, -d[0], -d[1], bc, ec);
+    put_t_pair(to, o + 24 + g, cc, -d[2], -d[3], bc, ec);
   }
   __syncthreads();
   // 32 -> 64: warps = (column tile j, row half mh); the two warps of a column
-  // tile exchange their halves of Y_j = A_ba X_a[:, j] through a named barrier
+  // tile exchange their halves of Y_j = A_ba X_a[:, j] through a named
+  // barrier.  Rows of X_a above 8j of column tile j are zero (k-steps skipped).
   {
     const int j = warp & 3, mh = warp >> 2;
     float* Ys = Y + 1024 + j * 256;  // 32 x 8
+    uint32_t fa[4][4], fb[4][2], fx[4][4], fy[4][2];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      if (s >= j) {
+        frag_a(fa[s], 8 * s, [&](int r, int k) { return A[ix(32 + 16 * mh + r, k)]; });
+        frag_b(fb[s], 8 * s, [&](int k, int c) { return k >= 8 * j + c ? X[ix(k, 8 * j + c)] : 0.f; });
+      } else {
+        fa[s][0] = fa[s][1] = fa[s][2] = fa[s][3] = 0u;
+        fb[s][0] = fb[s][1] = 0u;
+      }
+      frag_a(fx[s], 8 * s, [&](int r, int k) { return k <= 16 * mh + r ? X[ix(32 + 16 * mh + r, 32 + k)] : 0.f; });
+    }
+    const int cc = 8 * j + 2 * t;
+    const float2 bc = make_float2(to.beta[cc], to.beta[cc + 1]);
+    const float2 ec = make_float2(to.eb[cc], to.eb[cc + 1]);
     float d[4];
-    warp_tile_mm(d, 8 * j, 32, [&](int r, int k) { return A[ix(32 + 16 * mh + r, k)]; },
-                 [&](int k, int c) { return k >= 8 * j + c ? X[ix(k, 8 * j + c)] : 0.f; });
+    tile_mm<4>(d, fa, fb);
     const int yr = 16 * mh + g;
     Ys[yr * 8 + 2 * t] = d[0];
     Ys[yr * 8 + 2 * t + 1] = d[1];
     Ys[(yr + 8) * 8 + 2 * t] = d[2];
     Ys[(yr + 8) * 8 + 2 * t + 1] = d[3];
     named_sync(1 + j, 64);
-    warp_tile_mm(d, 0, 16 + 16 * mh,
-                 [&](int r, int k) { return k <= 16 * mh + r ? X[ix(32 + 16 * mh + r, 32 + k)] : 0.f; },
-                 [&](int k, int c) { return Ys[k * 8 + c]; });
-    const int cc = 8 * j + 2 * t;
-    put_t_pair(to, 32 + yr, cc, -d[0], -d[1]);
-    put_t_pair(to, 40 + yr, cc, -d[2], -d[3]);
+#pragma unroll
+    for (int s = 0; s < 4; ++s) frag_b(fy[s], 8 * s, [&](int k, int c) { return Ys[k * 8 + c]; });
+    tile_mm<4>(d, fx, fy);
+    put_t_pair(to, 32 + yr, cc, -d[0], -d[1], bc, ec);
+    put_t_pair(to, 40 + yr, cc, -d[2], -d[3], bc, ec);
   }
 }
 
@@ -632,7 +678,7 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int cc = c0 + i;
-          Af[ix(r, cc)] = cc < r ? betar * v[i] * __expf(br - bc[i]) : 0.f;
+          Af[ix(r, cc)] = cc < r ? betar * v[i] * exp_ftz(br - bc[i]) : 0.f;
         }
       } else {
         const int t = lrow - kC;
@@ -641,7 +687,7 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int cc = c0 + i;
-          m[i] = cc <= t ? v[i] * __expf(bt - bc[i]) : 0.f;
+          m[i] = cc <= t ? v[i] * exp_ftz(bt - bc[i]) : 0.f;
         }
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
