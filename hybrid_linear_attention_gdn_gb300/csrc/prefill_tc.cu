@@ -139,11 +139,14 @@ __device__ __forceinline__ int seq_of_chunk(const int32_t* base, int n_seq, int 
 }
 
 // ---------------------------------------------------------------------------
-// features: grid (n_chunks_max, hk), 256 threads; two launches:
-//   part 0: q and k of QK head hq (256 channels) -> L2 norms -> KQ image
-//   part 1: v of the G V heads reading hq (G*128 channels) -> V images, gates
-// Each CTA first stages its input tile (3 history rows + 64 token rows of its
-// channels) in shared memory with cp.async, so all loads are in flight at once.
+// features: grid (n_chunks_max, hk), 256 threads, one CTA per (chunk, QK head):
+// q and k of QK head hq and v of the G V heads reading it.  The CTA stages its
+// input tile (3 rows before the chunk + its 64 rows, all 256 + G*128 channels)
+// in shared memory with cp.async; then each thread takes one 8-channel group
+// of a row at a time: conv1d over the 4 staged rows, SiLU, and for q/k the
+// row's L2 norm from a 16-lane shuffle reduction (a warp holds one row's 16 q
+// groups and 16 k groups), and writes the 8 results as one 16-byte piece of
+// the swizzled operand image.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_addr(dst)), "l"(src) : "memory");
@@ -151,11 +154,44 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
 }
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(h[i]);
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
+  }
+}
+__device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+// conv1d (width 4, tile rows r .. r+3 = positions P+r-3 .. P+r) + SiLU for the
+// 8 channels at local channel lc; zero outside the sequence.  The fast
+// exponential and division are far finer than the bf16 operands they feed.
+template <typename Tact>
+__device__ __forceinline__ void conv8(const Tact* xs, int nch, int r, int lc, const float (&w)[8][4], bool valid,
+                                      float (&y)[8]) {
+  float x[4][8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) load8(xs + (size_t)(r + j) * nch + lc, x[j]);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    float acc = w[c][0] * x[0][c];
+    acc = fmaf(w[c][1], x[1][c], acc);
+    acc = fmaf(w[c][2], x[2][c], acc);
+    acc = fmaf(w[c][3], x[3][c], acc);
+    y[c] = valid ? __fdividef(acc, 1.f + exp_ftz(-acc)) : 0.f;
+  }
+}
 
 template <typename Tact, typename Tconv>
-__global__ void __launch_bounds__(kTh) tc_features_kernel(const TcArgs a, int part) {
+__global__ void __launch_bounds__(kTh) tc_features_kernel(const TcArgs a) {
   extern __shared__ __align__(16) unsigned char fsm[];
-  __shared__ float snorm[kC][2];
   const int gc = blockIdx.x, hq = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (gc >= a.chunk_base[a.n_seq]) return;
@@ -167,16 +203,16 @@ __global__ void __launch_bounds__(kTh) tc_features_kernel(const TcArgs a, int pa
   const int64_t P = (p0 / kC + (gc - a.chunk_base[n])) * kC;  // absolute position of row 0
   const int64_t p1 = p0 + len;
   const int GD = a.G * kD;
-  const int nch = part == 0 ? 2 * kD : GD;   // channels of this CTA
-  constexpr int EPC = 16 / sizeof(Tact);     // elements per 16-byte chunk
-  const int cpr = nch / EPC;                 // chunks per tile row
+  const int nch = 2 * kD + GD;               // local channels: q | k | v of the G heads
+  constexpr int EPC = 16 / sizeof(Tact);     // elements per 16-byte piece
+  const int cpr = nch / EPC;                 // pieces per tile row
   Tact* xs = reinterpret_cast<Tact*>(fsm);   // [kC + 3][nch], row i = position P - 3 + i
-  float* ys = reinterpret_cast<float*>(fsm + (size_t)(kC + 3) * nch * sizeof(Tact));  // part 0: [kC][256]
   const Tact* qkv = reinterpret_cast<const Tact*>(a.qkv);
   const Tconv* hist = reinterpret_cast<const Tconv*>(a.conv) + (size_t)slot * 3 * a.C;
   auto gchan = [&](int lc) -> size_t {  // global channel of local channel lc
-    if (part == 1) return 2 * (size_t)a.hk * kD + (size_t)hq * GD + lc;
-    return lc < kD ? (size_t)hq * kD + lc : (size_t)a.hk * kD + (size_t)hq * kD + (lc - kD);
+    if (lc < kD) return (size_t)hq * kD + lc;
+    if (lc < 2 * kD) return (size_t)a.hk * kD + (size_t)hq * kD + (lc - kD);
+    return 2 * (size_t)a.hk * kD + (size_t)hq * GD + (lc - 2 * kD);
   };
   for (int e = tid; e < (kC + 3) * cpr; e += kTh) {
     const int i = e / cpr, ch = e % cpr;
@@ -194,107 +230,76 @@ __global__ void __launch_bounds__(kTh) tc_features_kernel(const TcArgs a, int pa
       for (int k = 0; k < EPC; ++k) dst[k] = from_f32<Tact>(0.f);
     }
   }
+  // gates (rows outside the sequence: g = beta = 0)
+  for (int e = tid; e < kC * a.G; e += kTh) {
+    const int r = e % kC, gi = e / kC;
+    const int h = hq * a.G + gi;
+    const int64_t pos = P + r;
+    float gv = 0.f, bv = 0.f;
+    if (pos >= p0 && pos < p1) {
+      const size_t tok = (size_t)(t0 + pos - p0);
+      const float av = to_f32(reinterpret_cast<const Tact*>(a.a)[tok * a.hv + h]);
+      const float bb = to_f32(reinterpret_cast<const Tact*>(a.b)[tok * a.hv + h]);
+      gv = -expf(a.A_log[h]) * softplus_f(av + a.dt_bias[h]);
+      bv = sigmoid_f(bb);
+    }
+    float* gt = a.ws_gate + ((size_t)gc * a.hv + h) * (2 * kC);
+    gt[r] = gv;
+    gt[kC + r] = bv;
+  }
   cp_async_wait_all();
   __syncthreads();
 
-  // conv1d + SiLU: a thread walks one channel pair through one 32-row half
-  // of the chunk (tile rows r0 .. r0 + 2 are the inputs before row r0)
-  const int npairs = nch / 2;
-  for (int job = tid; job < 2 * npairs; job += kTh) {
-    const int lc = 2 * (job % npairs), r0 = 32 * (job / npairs);
-    const size_t c = gchan(lc);
-    const float4 w0 = *reinterpret_cast<const float4*>(a.conv_w + c * 4);
-    const float4 w1 = *reinterpret_cast<const float4*>(a.conv_w + (c + 1) * 4);
-    float h0[3], h1[3];
+  // q and k: warp w takes rows w, w + 8, ...; lane l < 16 is q channels
+  // 8l .. 8l+7, lane 16 + l the same k channels
+  {
+    const int lc = 8 * lane;  // local channel (q: 0..127, k: 128..255)
+    float w[8][4];
 #pragma unroll
-    for (int k = 0; k < 3; ++k) {
-      h0[k] = to_f32(xs[(size_t)(r0 + k) * nch + lc]);
-      h1[k] = to_f32(xs[(size_t)(r0 + k) * nch + lc + 1]);
+    for (int c = 0; c < 8; ++c) {
+      const float4 w4 = *reinterpret_cast<const float4*>(a.conv_w + gchan(lc + c) * 4);
+      w[c][0] = w4.x; w[c][1] = w4.y; w[c][2] = w4.z; w[c][3] = w4.w;
     }
-#pragma unroll 4
-    for (int r = r0; r < r0 + 32; ++r) {
-      const float x0 = to_f32(xs[(size_t)(r + 3) * nch + lc]);
-      const float x1 = to_f32(xs[(size_t)(r + 3) * nch + lc + 1]);
-      const bool valid = P + r >= p0 && P + r < p1;
-      float y0 = w0.x * h0[0];
-      y0 = fmaf(w0.y, h0[1], y0);
-      y0 = fmaf(w0.z, h0[2], y0);
-      y0 = fmaf(w0.w, x0, y0);
-      float y1 = w1.x * h1[0];
-      y1 = fmaf(w1.y, h1[1], y1);
-      y1 = fmaf(w1.z, h1[2], y1);
-      y1 = fmaf(w1.w, x1, y1);
-      // SiLU with the fast exponential and division: these values become
-      // bf16 operands, far coarser than either approximation
-      y0 = valid ? __fdividef(y0, 1.f + exp_ftz(-y0)) : 0.f;
-      y1 = valid ? __fdividef(y1, 1.f + exp_ftz(-y1)) : 0.f;
-      h0[0] = h0[1]; h0[1] = h0[2]; h0[2] = x0;
-      h1[0] = h1[1]; h1[1] = h1[2]; h1[2] = x1;
-      if (part == 0) {
-        ys[r * (2 * kD) + lc] = y0;
-        ys[r * (2 * kD) + lc + 1] = y1;
-      } else {
-        const int h = hq * a.G + lc / kD, d = lc % kD;
-        uint8_t* vimg = a.ws_v + ((size_t)gc * a.hv + h) * kVBytes;
-        *reinterpret_cast<__nv_bfloat162*>(vimg + umma::sw128_off(r, d, 64 * 128)) =
-            __floats2bfloat162_rn(y0, y1);
+    const bool isq = lane < 16;
+    const float qscale = isq ? rsqrtf((float)kD) : 1.f;
+    uint8_t* kq = a.ws_kq + ((size_t)gc * a.hk + hq) * kKQBytes;
+    for (int r = warp; r < kC; r += kTh / 32) {
+      float y[8];
+      conv8(xs, nch, r, lc, w, P + r >= p0 && P + r < p1, y);
+      float ss = 0.f;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) ss = fmaf(y[c], y[c], ss);
+#pragma unroll
+      for (int o = 8; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      const float sc = rsqrtf(ss + kNormEps) * qscale;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) y[c] *= sc;
+      const int R = isq ? kC + r : r;  // image rows: k^ 0..63, q^ 64..127
+      *reinterpret_cast<uint4*>(kq + umma::sw128_off(R, 8 * (lane & 15), 128 * 128)) = umma::pack8_bf16(y);
+    }
+  }
+  // v: 8-channel groups of the G heads, G*16 groups per row
+  {
+    const int gpr = a.G * (kD / 8);
+    int wch = -1;
+    float w[8][4];
+    for (int e = tid; e < kC * gpr; e += kTh) {
+      const int r = e / gpr, ch = e % gpr;
+      const int lc = 2 * kD + 8 * ch;
+      if (ch != wch) {
+        wch = ch;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const float4 w4 = *reinterpret_cast<const float4*>(a.conv_w + gchan(lc + c) * 4);
+          w[c][0] = w4.x; w[c][1] = w4.y; w[c][2] = w4.z; w[c][3] = w4.w;
+        }
       }
+      float y[8];
+      conv8(xs, nch, r, lc, w, P + r >= p0 && P + r < p1, y);
+      const int h = hq * a.G + ch / (kD / 8), d = 8 * (ch % (kD / 8));
+      uint8_t* vimg = a.ws_v + ((size_t)gc * a.hv + h) * kVBytes;
+      *reinterpret_cast<uint4*>(vimg + umma::sw128_off(r, d, 64 * 128)) = umma::pack8_bf16(y);
     }
-  }
-  if (part == 1) {
-    // gates (rows outside the sequence: g = beta = 0)
-    for (int e = tid; e < kC * a.G; e += kTh) {
-      const int r = e % kC, gi = e / kC;
-      const int h = hq * a.G + gi;
-      const int64_t pos = P + r;
-      float gv = 0.f, bv = 0.f;
-      if (pos >= p0 && pos < p1) {
-        const size_t tok = (size_t)(t0 + pos - p0);
-        const float av = to_f32(reinterpret_cast<const Tact*>(a.a)[tok * a.hv + h]);
-        const float bb = to_f32(reinterpret_cast<const Tact*>(a.b)[tok * a.hv + h]);
-        gv = -expf(a.A_log[h]) * softplus_f(av + a.dt_bias[h]);
-        bv = sigmoid_f(bb);
-      }
-      float* gt = a.ws_gate + ((size_t)gc * a.hv + h) * (2 * kC);
-      gt[r] = gv;
-      gt[kC + r] = bv;
-    }
-    return;
-  }
-  __syncthreads();
-  // per-row L2 norms of q and k
-  for (int r = warp; r < kC; r += kTh / 32) {
-    float sq = 0.f, sk = 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float q = ys[r * (2 * kD) + lane + 32 * i];
-      const float k = ys[r * (2 * kD) + kD + lane + 32 * i];
-      sq = fmaf(q, q, sq);
-      sk = fmaf(k, k, sk);
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      sq += __shfl_xor_sync(0xffffffffu, sq, o);
-      sk += __shfl_xor_sync(0xffffffffu, sk, o);
-    }
-    if (lane == 0) {
-      snorm[r][0] = rsqrtf(sq + kNormEps) * rsqrtf((float)kD);
-      snorm[r][1] = rsqrtf(sk + kNormEps);
-    }
-  }
-  __syncthreads();
-  // KQ image: rows 0..63 = k^, rows 64..127 = q^; 16-byte chunks of 8 values
-  uint8_t* kq = a.ws_kq + ((size_t)gc * a.hk + hq) * kKQBytes;
-  for (int e = tid; e < 2 * kC * (kD / 8); e += kTh) {
-    const int R = e / (kD / 8), ch = e % (kD / 8);
-    const bool isq = R >= kC;
-    const int r = isq ? R - kC : R;
-    const float sc = snorm[r][isq ? 0 : 1];
-    const float* src = ys + r * (2 * kD) + (isq ? 0 : kD) + ch * 8;
-    float v8[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v8[i] = src[i] * sc;
-    *reinterpret_cast<uint4*>(kq + umma::sw128_off(R, ch * 8, 128 * 128)) = umma::pack8_bf16(v8);
   }
 }
 
@@ -886,6 +891,9 @@ static TcLayout tc_layout(const gdn_dims& d, int32_t n_seq, int64_t total) {
 bool prefill_tc_supported(const gdn_dims& d, const void* qkv, const void* out, const gdn_params& p) {
   if (d.dk != kD || d.dv != kD || d.conv_width != 4) return false;
   if (d.hv / d.hk > 8) return false;
+  // the features kernel stages (64 + 3) rows of the CTA's 256 + G*128 channels
+  if ((size_t)(kC + 3) * (2 * kD + (size_t)(d.hv / d.hk) * kD) * dtype_size(d.act_dtype) > 227u * 1024u)
+    return false;
   if (!aligned(qkv, 16) || !aligned(out, 16) || !aligned(p.conv_w, 16)) return false;
   return true;
 }
@@ -900,14 +908,11 @@ static cudaError_t launch_tc_t(const TcArgs& a, cudaStream_t s) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   auto fk = tc_features_kernel<Tact, Tconv>;
-  for (int part = 0; part < 2; ++part) {
-    const int nch = part == 0 ? 2 * kD : a.G * kD;
-    const size_t fsm = (size_t)(kC + 3) * nch * sizeof(Tact) + (part == 0 ? sizeof(float) * kC * 2 * kD : 0);
-    if ((e = cudaFuncSetAttribute(fk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsm)) != cudaSuccess)
-      return e;
-    fk<<<dim3((unsigned)a.n_chunks_max, (unsigned)a.hk), kTh, fsm, s>>>(a, part);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
+  const size_t fsm = (size_t)(kC + 3) * (2 * kD + a.G * kD) * sizeof(Tact);
+  if ((e = cudaFuncSetAttribute(fk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsm)) != cudaSuccess)
+    return e;
+  fk<<<dim3((unsigned)a.n_chunks_max, (unsigned)a.hk), kTh, fsm, s>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   auto ck = tc_chain_kernel<Tact>;
   const size_t csm = sizeof(ChainSmem) + 1024;
   if ((e = cudaFuncSetAttribute(ck, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csm)) != cudaSuccess)
