@@ -306,19 +306,25 @@ __global__ void __launch_bounds__(kTh) tc_features_kernel(const TcArgs a) {
 // ---------------------------------------------------------------------------
 // chain: grid (hv, n_seq), 256 threads, one CTA per SM
 // ---------------------------------------------------------------------------
+constexpr int kAXStride = 68;  // row stride (floats) of the solve's A and X
 struct __align__(1024) ChainSmem {
   uint8_t kq[2][kKQBytes];
   uint8_t v[2][kVBytes];
   uint8_t st[2 * 128 * 128];  // S^T bf16 operand (K-major, 2 blocks of 64 dk)
   uint8_t wt[128 * 128];      // W^T (MN-major B: 128 dk rows x 64 tokens); solve scratch
-  uint8_t dt[128 * 128];      // Delta^T (K-major A: 128 dv rows x 64 tokens); A (fp32) in the solve
-  uint8_t dtt[128 * 128];     // Delta^T diag(e^{b_last - b}); X (fp32) in the solve
+  union {
+    struct {
+      uint8_t dt[128 * 128];   // Delta^T (K-major A: 128 dv rows x 64 tokens)
+      uint8_t dtt[128 * 128];  // Delta^T diag(e^{b_last - b})
+    };
+    float ax[2][64 * kAXStride];  // A and X (fp32) in the solve
+  };
   uint8_t tm[64 * 128];       // T (K-major B: 64 rows x 64)
   uint8_t tp[64 * 128];       // T diag(e^b)
   uint8_t qk[64 * 128];       // QK^T (.) Gamma (.) lower-incl
   float gates[2][2][kC];
-  float b[kC], eb[kC], ebl[kC];
-  uint64_t ld_full[2], mma_bar;
+  float b[2][kC], eb[2][kC], ebl[2][kC];  // by chunk parity
+  uint64_t ld_full[2], mma_bar, kq_bar;
   uint32_t tmem_base;
   int abort;
 };
@@ -333,11 +339,9 @@ __device__ __forceinline__ bool cta_wait(ChainSmem& S, uint64_t* bar, uint32_t p
 // Warp-level tf32 MMA (m16n8k8, fp32 accumulate).  Fragment layout: lane =
 // 4 * g + t; A holds (g, t), (g + 8, t), (g, t + 4), (g + 8, t + 4); B holds
 // (t, g), (t + 4, g); D holds (g, 2t), (g, 2t + 1), (g + 8, 2t), (g + 8, 2t + 1).
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;\n" : "=r"(r) : "f"(x));
-  return r;
-}
+// tf32 operands are the fp32 bit patterns: the MMA reads the top 19 bits
+// (truncation, relative error below 2^-10, far under T's bf16 rounding).
+__device__ __forceinline__ uint32_t to_tf32(float x) { return __float_as_uint(x); }
 // Fragments of one m16n8k8 step: A = L[0..16)[k..k+8), B = R[k..k+8)[0..8).
 template <class LF>
 __device__ __forceinline__ void frag_a(uint32_t (&a)[4], int k, LF L) {
@@ -368,10 +372,10 @@ __device__ __forceinline__ void tile_mm(float (&d)[4], const uint32_t (&a)[NK][4
   for (int s = 0; s < NK; ++s) mma_tf32(d, a[s], b[s]);
 }
 
-// Element (r, c) of the 64 x 64 fp32 matrices A and X: rows of 64 with the
-// column rotated by the row, so that a warp walking a column (one row per
-// lane) hits 32 different banks.
-__device__ __forceinline__ int ix(int r, int c) { return r * 64 + ((c + r) & 63); }
+// Element (r, c) of the 64 x 64 fp32 matrices A and X: rows 68 floats apart,
+// so the m16n8k8 fragment loads (lanes (g, t) at rows g, columns t, or the
+// transpose) and 16-byte row stores by consecutive rows are conflict-free.
+__device__ __forceinline__ int ix(int r, int c) { return r * kAXStride + c; }
 
 // Byte offset of element (r, c) in a 64 x 64 bf16 K-major 128B-swizzled tile.
 __device__ __forceinline__ uint32_t t_off(int r, int c) {
@@ -565,6 +569,7 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
     mbar_init(&S.ld_full[0], 1);
     mbar_init(&S.ld_full[1], 1);
     mbar_init(&S.mma_bar, 1);
+    mbar_init(&S.kq_bar, 1);
     S.abort = 0;
     fence_mbar_init();
   }
@@ -609,68 +614,80 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
   constexpr uint32_t ID_64_KM = umma::idesc_bf16(128, 64, false, true);
   constexpr uint32_t ID_128_KM = umma::idesc_bf16(128, 128, false, true);
   uint32_t mph = 0;
-  int issued = nch > 0 ? 1 : 0;
-  float* Af = reinterpret_cast<float*>(S.dt);
-  float* Xf = reinterpret_cast<float*>(S.dtt);
+  int issued = nch > 0 ? 1 : 0;  // chunks whose loads were issued
+  int kq_issued = 0;             // chunks whose [K;Q] K^T was issued
+  float* Af = S.ax[0];
+  float* Xf = S.ax[1];
   float* Yf = reinterpret_cast<float*>(S.wt);
 
-  for (int c = 0; c < nch; ++c) {
+  // warp 0, gates of chunk c resident: cumulative log-decay b, e^b, e^{b_last - b}
+  auto chunk_decays = [&](int c) {
+    const int buf = c & 1;
+    float bv[2], carry = 0.f;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      float v = S.gates[buf][0][32 * hh + lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+      }
+      bv[hh] = v + carry;
+      carry = __shfl_sync(0xffffffffu, bv[hh], 31);
+    }
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      S.b[buf][32 * hh + lane] = bv[hh];
+      S.eb[buf][32 * hh + lane] = expf(bv[hh]);
+      S.ebl[buf][32 * hh + lane] = expf(carry - bv[hh]);
+    }
+  };
+  // thread 0: [K;Q] K^T of chunk c into TM_KQ, completed on kq_bar
+  auto issue_kq = [&](int c) {
+    const uint32_t kq = smem_addr(S.kq[c & 1]);
+    for (int s = 0; s < 8; ++s) {
+      const uint32_t ko = (s >> 2) * 16384 + (s & 3) * 32;
+      umma::mma_bf16(tmem + TM_KQ, umma::desc(kq + ko, 16, 1024), umma::desc(kq + ko, 16, 1024), ID_64_KK,
+                     s > 0);
+    }
+    umma::commit(&S.kq_bar);
+  };
+  if (nch > 0 && cta_wait(S, &S.ld_full[0], 0)) {
+    if (warp == 0) chunk_decays(0);
+    if (tid == 0) {
+      umma::fence_after();
+      issue_kq(0);
+      kq_issued = 1;
+    }
+  }
+
+  // Per chunk c: the state-independent products of chunk c + 1 ([K;Q] K^T
+  // and its decays) are started while chunk c's state update finishes.
+  for (int c = 0; c < nch && !S.abort; ++c) {
     const int buf = c & 1;
     const int64_t P = (p0 / kC + c) * kC;
+    const float* eb = S.eb[buf];
     if (tid == 0 && c + 1 < nch) {
       issue_load(c + 1);
       issued = c + 2;
     }
-    if (!cta_wait(S, &S.ld_full[buf], (c >> 1) & 1)) break;
+    // chunk c's operands landed (warp 0 saw it already; each thread observes
+    // the copy's completion itself before reading the gates)
+    if (!mbar_wait(&S.ld_full[buf], (c >> 1) & 1)) S.abort = 1;
+    if (!cta_wait(S, &S.kq_bar, c & 1)) break;
+    umma::fence_after();
     const uint32_t kq = smem_addr(S.kq[buf]), vv = smem_addr(S.v[buf]);
     const uint32_t st = smem_addr(S.st);
-    // cumulative log-decay of the chunk
-    if (warp == 0) {
-      float carry = 0.f;
-      for (int hh = 0; hh < 2; ++hh) {
-        float v = S.gates[buf][0][32 * hh + lane];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float u = __shfl_up_sync(0xffffffffu, v, o);
-          if (lane >= o) v += u;
-        }
-        v += carry;
-        S.b[32 * hh + lane] = v;
-        carry = __shfl_sync(0xffffffffu, v, 31);
-      }
-    }
-    __syncthreads();
-    if (tid < kC) {
-      S.eb[tid] = expf(S.b[tid]);
-      S.ebl[tid] = expf(S.b[kC - 1] - S.b[tid]);
-    }
-    // [K;Q] K^T and S^T Q^T
-    if (tid == 0) {
-      umma::fence_after();
-      for (int s = 0; s < 8; ++s) {
-        const uint32_t ko = (s >> 2) * 16384 + (s & 3) * 32;
-        umma::mma_bf16(tmem + TM_KQ, umma::desc(kq + ko, 16, 1024), umma::desc(kq + ko, 16, 1024),
-                       ID_64_KK, s > 0);
-      }
-      for (int s = 0; s < 8; ++s) {
-        const uint32_t ko = (s >> 2) * 16384 + (s & 3) * 32;
-        umma::mma_bf16(tmem + TM_O1, umma::desc(st + ko, 16, 1024),
-                       umma::desc(kq + 8192 + ko, 16, 1024), ID_64_KK, s > 0);
-      }
-      umma::commit(&S.mma_bar);
-    }
-    if (!cta_wait(S, &S.mma_bar, mph)) break;
-    mph ^= 1;
-    umma::fence_after();
     // A = strict_lower(beta (.) K K^T (.) Gamma) (fp32) and the decayed,
     // masked Q K^T operand; lanes 0-63 hold K K^T rows, 64-127 Q K^T rows
     {
+      const float* b = S.b[buf];
       float v[32], bc[32];
       const int c0 = 32 * half;
       // the column decays, loaded before any store so none waits on one
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const float4 b4 = *reinterpret_cast<const float4*>(S.b + c0 + 4 * i);
+        const float4 b4 = *reinterpret_cast<const float4*>(b + c0 + 4 * i);
         bc[4 * i] = b4.x;
         bc[4 * i + 1] = b4.y;
         bc[4 * i + 2] = b4.z;
@@ -679,15 +696,20 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
       umma::tmem_ld32(tlane + TM_KQ + 32 * half, v);
       if (lrow < kC) {
         const int r = lrow;
-        const float br = S.b[r], betar = S.gates[buf][1][r];
+        const float br = b[r], betar = S.gates[buf][1][r];
+        float av[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int cc = c0 + i;
-          Af[ix(r, cc)] = cc < r ? betar * v[i] * exp_ftz(br - bc[i]) : 0.f;
+          av[i] = cc < r ? betar * v[i] * exp_ftz(br - bc[i]) : 0.f;
         }
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<float4*>(Af + ix(r, c0 + 4 * q)) =
+              make_float4(av[4 * q], av[4 * q + 1], av[4 * q + 2], av[4 * q + 3]);
       } else {
         const int t = lrow - kC;
-        const float bt = S.b[t];
+        const float bt = b[t];
         float m[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -705,10 +727,10 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
     umma::fence_before();
     __syncthreads();
     // T = X diag(beta) and T' = X diag(beta e^b) as bf16 K-major tiles
-    solve_T(Af, Xf, Yf, TOut{S.tm, S.tp, S.gates[buf][1], S.eb});
+    solve_T(Af, Xf, Yf, TOut{S.tm, S.tp, S.gates[buf][1], eb});
     umma::fence_proxy_async();
     __syncthreads();
-    // U^T = V^T T^T ; W^T = K^T T'^T
+    // U^T = V^T T^T ; W^T = K^T T'^T ; O1 = S^T Q^T
     if (tid == 0) {
       umma::fence_after();
       const uint32_t tm = smem_addr(S.tm), tp = smem_addr(S.tp);
@@ -718,6 +740,11 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
       for (int s = 0; s < 4; ++s)
         umma::mma_bf16(tmem + TM_W, umma::desc(kq + s * 2048, 16384, 1024),
                        umma::desc(tp + s * 32, 16, 1024), ID_64_MK, s > 0);
+      for (int s = 0; s < 8; ++s) {
+        const uint32_t ko = (s >> 2) * 16384 + (s & 3) * 32;
+        umma::mma_bf16(tmem + TM_O1, umma::desc(st + ko, 16, 1024),
+                       umma::desc(kq + 8192 + ko, 16, 1024), ID_64_KK, s > 0);
+      }
       umma::commit(&S.mma_bar);
     }
     if (!cta_wait(S, &S.mma_bar, mph)) break;
@@ -753,13 +780,14 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
     umma::fence_after();
     // Delta^T = U^T - P, and its columns scaled by e^{b_last - b}
     {
+      const float* ebl = S.ebl[buf];
       float u[32], p[32], d[32], dd[32];
       umma::tmem_ld32(tlane + TM_U + 32 * half, u);
       umma::tmem_ld32(tlane + TM_P + 32 * half, p);
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         d[i] = u[i] - p[i];
-        dd[i] = d[i] * S.ebl[32 * half + i];
+        dd[i] = d[i] * ebl[32 * half + i];
       }
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
@@ -772,24 +800,40 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
     umma::fence_proxy_async();
     umma::fence_before();
     __syncthreads();
-    // D2 = Delta~^T K ; O2 = Delta^T (QK^T Gamma)^T
-    if (tid == 0) {
-      umma::fence_after();
-      const uint32_t dt = smem_addr(S.dt), dtt = smem_addr(S.dtt), qk = smem_addr(S.qk);
-      for (int s = 0; s < 4; ++s)
-        umma::mma_bf16(tmem + TM_D2, umma::desc(dtt + s * 32, 16, 1024),
-                       umma::desc(kq + s * 2048, 16384, 1024), ID_128_KM, s > 0);
-      for (int s = 0; s < 4; ++s)
-        umma::mma_bf16(tmem + TM_O2, umma::desc(dt + s * 32, 16, 1024), umma::desc(qk + s * 32, 16, 1024),
-                       ID_64_KK, s > 0);
-      umma::commit(&S.mma_bar);
+    // D2 = Delta~^T K ; O2 = Delta^T (QK^T Gamma)^T ; then, with chunk c + 1
+    // resident, its decays and its [K;Q] K^T
+    if (warp == 0) {
+      if (lane == 0) {
+        umma::fence_after();
+        const uint32_t dt = smem_addr(S.dt), dtt = smem_addr(S.dtt), qk = smem_addr(S.qk);
+        for (int s = 0; s < 4; ++s)
+          umma::mma_bf16(tmem + TM_D2, umma::desc(dtt + s * 32, 16, 1024),
+                         umma::desc(kq + s * 2048, 16384, 1024), ID_128_KM, s > 0);
+        for (int s = 0; s < 4; ++s)
+          umma::mma_bf16(tmem + TM_O2, umma::desc(dt + s * 32, 16, 1024), umma::desc(qk + s * 32, 16, 1024),
+                         ID_64_KK, s > 0);
+        umma::commit(&S.mma_bar);
+      }
+      __syncwarp();
+      if (c + 1 < nch) {
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(&S.ld_full[(c + 1) & 1], ((c + 1) >> 1) & 1));
+        if (ok) {
+          chunk_decays(c + 1);
+          if (lane == 0) {
+            issue_kq(c + 1);
+            kq_issued = c + 2;
+          }
+        } else if (lane == 0) {
+          S.abort = 1;
+        }
+      }
     }
     if (!cta_wait(S, &S.mma_bar, mph)) break;
     mph ^= 1;
     umma::fence_after();
     // S^T <- e^{b_last} S^T + D2 ; O = O1 diag(e^b) + O2
     {
-      const float dec = S.eb[kC - 1];
+      const float dec = eb[kC - 1];
       float d2[32];
       umma::tmem_ld32(tlane + TM_D2 + 64 * half, d2);
 #pragma unroll
@@ -803,13 +847,13 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
       float ebr[32];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const float4 e4 = *reinterpret_cast<const float4*>(S.eb + 32 * half + 4 * i);
+        const float4 e4 = *reinterpret_cast<const float4*>(eb + 32 * half + 4 * i);
         ebr[4 * i] = e4.x;
         ebr[4 * i + 1] = e4.y;
         ebr[4 * i + 2] = e4.z;
         ebr[4 * i + 3] = e4.w;
       }
-      // stage O as [token][dv] in the (now free) W^T / Delta^T tiles
+      // stage O as [token][dv] in the (now free) W^T tile
       Tact* ot = reinterpret_cast<Tact*>(S.wt);
 #pragma unroll
       for (int i = 0; i < 32; ++i) ot[(32 * half + i) * kD + lrow] = from_f32<Tact>(fmaf(o1[i], ebr[i], o2[i]));
@@ -850,8 +894,10 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
   if (S.abort) {
     if (tid == 0) {
       report(a.err, GDN_DEV_ERR_TIMEOUT);
-      // let issued loads land before the shared memory goes away
+      // let issued loads and the last [K;Q] K^T land before the shared memory
+      // and TMEM go away
       for (int c = (issued > 2 ? issued - 2 : 0); c < issued; ++c) mbar_wait(&S.ld_full[c & 1], (c >> 1) & 1);
+      if (kq_issued > 0) mbar_wait(&S.kq_bar, (kq_issued - 1) & 1);
     }
   } else {
 #pragma unroll
