@@ -414,38 +414,36 @@ __device__ __forceinline__ void put_t_pair(const TOut& o, int r, int c, float x0
 __device__ __forceinline__ void solve_T(const float* A, float* X, float* Y, const TOut& to) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
-  // 8 x 8 diagonal blocks: warp w, lanes 0..7 = columns of block w; the
-  // column pairs (2l, 2l+1) of lanes 0..3 are written as bf16 pairs
-  {
-    const int o = 8 * warp, c = lane & 7;
+  // 8 x 8 diagonal blocks: warp w, lane l < 4 = columns 2l and 2l+1 of block
+  // w (two independent substitutions), written as fp32 pairs to X and bf16
+  // pairs to T and T'
+  if (lane < 4) {
+    const int o = 8 * warp, c0 = 2 * lane;
     float a[28];
 #pragma unroll
     for (int r = 1, i = 0; r < 8; ++r)
 #pragma unroll
       for (int m = 0; m < r; ++m, ++i) a[i] = A[ix(o + r, o + m)];
-    const float2 bc = make_float2(to.beta[o + 2 * (lane & 3)], to.beta[o + 2 * (lane & 3) + 1]);
-    const float2 ec = make_float2(to.eb[o + 2 * (lane & 3)], to.eb[o + 2 * (lane & 3) + 1]);
-    float x[8];
+    const float2 bc = make_float2(to.beta[o + c0], to.beta[o + c0 + 1]);
+    const float2 ec = make_float2(to.eb[o + c0], to.eb[o + c0 + 1]);
+    float x0[8], x1[8];
 #pragma unroll
     for (int r = 0, i = 0; r < 8; ++r) {
-      float sum = (r == c) ? 1.f : 0.f;
+      float s0 = (r == c0) ? 1.f : 0.f, s1 = (r == c0 + 1) ? 1.f : 0.f;
 #pragma unroll
-      for (int m = 0; m < r; ++m, ++i) sum = fmaf(-a[i], x[m], sum);
-      x[r] = sum;
+      for (int m = 0; m < r; ++m, ++i) {
+        s0 = fmaf(-a[i], x0[m], s0);
+        s1 = fmaf(-a[i], x1[m], s1);
+      }
+      x0[r] = s0;
+      x1[r] = s1;
     }
-    if (lane < 8) {
 #pragma unroll
-      for (int r = 0; r < 8; ++r)
-        if (r >= c) X[ix(o + r, o + c)] = x[r];
-    }
-    // lane l < 4 writes columns 2l, 2l+1 of every row: fetch the odd column
-    // from lane 2l+1 (entries above the diagonal are zero)
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      const float x0 = __shfl_sync(0xffffffffu, x[r], 2 * (lane & 3));
-      const float x1 = __shfl_sync(0xffffffffu, x[r], 2 * (lane & 3) + 1);
-      if (lane < 4 && 2 * lane <= r) put_t_pair(to, o + r, o + 2 * lane, x0, r >= 2 * lane + 1 ? x1 : 0.f, bc, ec);
-    }
+    for (int r = 0; r < 8; ++r)
+      if (r >= c0) {
+        *reinterpret_cast<float2*>(X + ix(o + r, o + c0)) = make_float2(x0[r], x1[r]);
+        put_t_pair(to, o + r, o + c0, x0[r], x1[r], bc, ec);
+      }
   }
   __syncthreads();
   // 8 -> 16: warps 0..3, block pair p (rows/cols 16p ..); M padded to 16
@@ -620,7 +618,7 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
   float* Xf = S.ax[1];
   float* Yf = reinterpret_cast<float*>(S.wt);
 
-  // warp 0, gates of chunk c resident: cumulative log-decay b, e^b, e^{b_last - b}
+  // one warp, gates of chunk c resident: cumulative log-decay b, e^b, e^{b_last - b}
   auto chunk_decays = [&](int c) {
     const int buf = c & 1;
     float bv[2], carry = 0.f;
@@ -724,6 +722,7 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
         }
       }
     }
+    if (warp == 7) bulk_wait_read();  // the previous chunk's output rows left S.wt
     umma::fence_before();
     __syncthreads();
     // T = X diag(beta) and T' = X diag(beta e^b) as bf16 K-major tiles
@@ -801,32 +800,30 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
     umma::fence_before();
     __syncthreads();
     // D2 = Delta~^T K ; O2 = Delta^T (QK^T Gamma)^T ; then, with chunk c + 1
-    // resident, its decays and its [K;Q] K^T
-    if (warp == 0) {
-      if (lane == 0) {
-        umma::fence_after();
-        const uint32_t dt = smem_addr(S.dt), dtt = smem_addr(S.dtt), qk = smem_addr(S.qk);
-        for (int s = 0; s < 4; ++s)
-          umma::mma_bf16(tmem + TM_D2, umma::desc(dtt + s * 32, 16, 1024),
-                         umma::desc(kq + s * 2048, 16384, 1024), ID_128_KM, s > 0);
-        for (int s = 0; s < 4; ++s)
-          umma::mma_bf16(tmem + TM_O2, umma::desc(dt + s * 32, 16, 1024), umma::desc(qk + s * 32, 16, 1024),
-                         ID_64_KK, s > 0);
-        umma::commit(&S.mma_bar);
-      }
-      __syncwarp();
+    // resident, its [K;Q] K^T (thread 0) and its decays (warp 4)
+    if (tid == 0) {
+      umma::fence_after();
+      const uint32_t dt = smem_addr(S.dt), dtt = smem_addr(S.dtt), qk = smem_addr(S.qk);
+      for (int s = 0; s < 4; ++s)
+        umma::mma_bf16(tmem + TM_D2, umma::desc(dtt + s * 32, 16, 1024),
+                       umma::desc(kq + s * 2048, 16384, 1024), ID_128_KM, s > 0);
+      for (int s = 0; s < 4; ++s)
+        umma::mma_bf16(tmem + TM_O2, umma::desc(dt + s * 32, 16, 1024), umma::desc(qk + s * 32, 16, 1024),
+                       ID_64_KK, s > 0);
+      umma::commit(&S.mma_bar);
       if (c + 1 < nch) {
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(&S.ld_full[(c + 1) & 1], ((c + 1) >> 1) & 1));
-        if (ok) {
-          chunk_decays(c + 1);
-          if (lane == 0) {
-            issue_kq(c + 1);
-            kq_issued = c + 2;
-          }
-        } else if (lane == 0) {
+        if (mbar_wait(&S.ld_full[(c + 1) & 1], ((c + 1) >> 1) & 1)) {
+          issue_kq(c + 1);
+          kq_issued = c + 2;
+        } else {
           S.abort = 1;
         }
       }
+    } else if (warp == 4 && c + 1 < nch) {
+      if (__all_sync(0xffffffffu, mbar_wait(&S.ld_full[(c + 1) & 1], ((c + 1) >> 1) & 1)))
+        chunk_decays(c + 1);
+      else if (lane == 0)
+        S.abort = 1;
     }
     if (!cta_wait(S, &S.mma_bar, mph)) break;
     mph ^= 1;
@@ -877,20 +874,22 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
     umma::fence_proxy_async();
     umma::fence_before();
     __syncthreads();
-    // output rows of the chunk's tokens: 16-byte stores of whole rows
-    {
-      constexpr int EPC = 16 / sizeof(Tact), CPR = kD / EPC;
+    // output rows of the chunk's tokens: one bulk shared -> global copy per
+    // row by warp 7 (two rows per lane); the staging tile is next written by
+    // the following chunk's solve, after warp 7 waited for these reads
+    if (warp == 7) {
       const Tact* ot = reinterpret_cast<const Tact*>(S.wt);
-      for (int e = tid; e < kC * CPR; e += kTh) {
-        const int r = e / CPR, ch = e % CPR;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int r = lane + 32 * k;
         const int64_t pos = P + r;
         if (pos >= p0 && pos < p1)
-          *reinterpret_cast<uint4*>(out + ((t0 + pos - p0) * a.hv + h) * kD + ch * EPC) =
-              *reinterpret_cast<const uint4*>(ot + r * kD + ch * EPC);
+          bulk_s2g(out + ((t0 + pos - p0) * a.hv + h) * kD, ot + r * kD, kD * sizeof(Tact));
       }
+      bulk_commit();
     }
-    __syncthreads();
   }
+  if (warp == 7) bulk_wait_all();  // output rows written before the CTA exits
   if (S.abort) {
     if (tid == 0) {
       report(a.err, GDN_DEV_ERR_TIMEOUT);
