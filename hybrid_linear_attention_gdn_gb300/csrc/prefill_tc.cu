@@ -722,7 +722,6 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
         }
       }
     }
-    if (warp == 7) bulk_wait_read();  // the previous chunk's output rows left S.wt
     umma::fence_before();
     __syncthreads();
     // T = X diag(beta) and T' = X diag(beta e^b) as bf16 K-major tiles
@@ -874,22 +873,20 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
     umma::fence_proxy_async();
     umma::fence_before();
     __syncthreads();
-    // output rows of the chunk's tokens: one bulk shared -> global copy per
-    // row by warp 7 (two rows per lane); the staging tile is next written by
-    // the following chunk's solve, after warp 7 waited for these reads
-    if (warp == 7) {
+    // output rows of the chunk's tokens: 16-byte stores of whole rows (the
+    // staging tile is next written after the following chunk's first barrier)
+    {
+      constexpr int EPC = 16 / sizeof(Tact), CPR = kD / EPC;
       const Tact* ot = reinterpret_cast<const Tact*>(S.wt);
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int r = lane + 32 * k;
+      for (int e = tid; e < kC * CPR; e += kTh) {
+        const int r = e / CPR, ch = e % CPR;
         const int64_t pos = P + r;
         if (pos >= p0 && pos < p1)
-          bulk_s2g(out + ((t0 + pos - p0) * a.hv + h) * kD, ot + r * kD, kD * sizeof(Tact));
+          *reinterpret_cast<uint4*>(out + ((t0 + pos - p0) * a.hv + h) * kD + ch * EPC) =
+              *reinterpret_cast<const uint4*>(ot + r * kD + ch * EPC);
       }
-      bulk_commit();
     }
   }
-  if (warp == 7) bulk_wait_all();  // output rows written before the CTA exits
   if (S.abort) {
     if (tid == 0) {
       report(a.err, GDN_DEV_ERR_TIMEOUT);
