@@ -640,13 +640,23 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
       S.ebl[buf][32 * hh + lane] = expf(carry - bv[hh]);
     }
   };
-  // thread 0: [K;Q] K^T of chunk c into TM_KQ, completed on kq_bar
+  // thread 0: [K;Q] K^T of chunk c into TM_KQ
   auto issue_kq = [&](int c) {
     const uint32_t kq = smem_addr(S.kq[c & 1]);
     for (int s = 0; s < 8; ++s) {
       const uint32_t ko = (s >> 2) * 16384 + (s & 3) * 32;
       umma::mma_bf16(tmem + TM_KQ, umma::desc(kq + ko, 16, 1024), umma::desc(kq + ko, 16, 1024), ID_64_KK,
                      s > 0);
+    }
+  };
+  // thread 0: O1 = S^T Q^T of chunk c (S as it enters the chunk) into TM_O1;
+  // kq_bar then completes with both of chunk c's state-entry products
+  auto issue_o1_commit = [&](int c) {
+    const uint32_t kq = smem_addr(S.kq[c & 1]), st = smem_addr(S.st);
+    for (int s = 0; s < 8; ++s) {
+      const uint32_t ko = (s >> 2) * 16384 + (s & 3) * 32;
+      umma::mma_bf16(tmem + TM_O1, umma::desc(st + ko, 16, 1024), umma::desc(kq + 8192 + ko, 16, 1024),
+                     ID_64_KK, s > 0);
     }
     umma::commit(&S.kq_bar);
   };
@@ -655,12 +665,14 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
     if (tid == 0) {
       umma::fence_after();
       issue_kq(0);
+      issue_o1_commit(0);
       kq_issued = 1;
     }
   }
 
   // Per chunk c: the state-independent products of chunk c + 1 ([K;Q] K^T
-  // and its decays) are started while chunk c's state update finishes.
+  // and its decays) start while chunk c's state update runs, and chunk c + 1's
+  // O1 as soon as the state has left chunk c.
   for (int c = 0; c < nch && !S.abort; ++c) {
     const int buf = c & 1;
     const int64_t P = (p0 / kC + c) * kC;
@@ -728,7 +740,7 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
     solve_T(Af, Xf, Yf, TOut{S.tm, S.tp, S.gates[buf][1], eb});
     umma::fence_proxy_async();
     __syncthreads();
-    // U^T = V^T T^T ; W^T = K^T T'^T ; O1 = S^T Q^T
+    // U^T = V^T T^T ; W^T = K^T T'^T
     if (tid == 0) {
       umma::fence_after();
       const uint32_t tm = smem_addr(S.tm), tp = smem_addr(S.tp);
@@ -738,11 +750,6 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
       for (int s = 0; s < 4; ++s)
         umma::mma_bf16(tmem + TM_W, umma::desc(kq + s * 2048, 16384, 1024),
                        umma::desc(tp + s * 32, 16, 1024), ID_64_MK, s > 0);
-      for (int s = 0; s < 8; ++s) {
-        const uint32_t ko = (s >> 2) * 16384 + (s & 3) * 32;
-        umma::mma_bf16(tmem + TM_O1, umma::desc(st + ko, 16, 1024),
-                       umma::desc(kq + 8192 + ko, 16, 1024), ID_64_KK, s > 0);
-      }
       umma::commit(&S.mma_bar);
     }
     if (!cta_wait(S, &S.mma_bar, mph)) break;
@@ -772,6 +779,15 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
                        ID_64_KM, s > 0);
       }
       umma::commit(&S.mma_bar);
+      // chunk c + 1's [K;Q] K^T runs on the tensor core during Delta below
+      if (c + 1 < nch) {
+        if (mbar_wait(&S.ld_full[(c + 1) & 1], ((c + 1) >> 1) & 1)) {
+          issue_kq(c + 1);
+          kq_issued = c + 2;
+        } else {
+          S.abort = 1;
+        }
+      }
     }
     if (!cta_wait(S, &S.mma_bar, mph)) break;
     mph ^= 1;
@@ -798,8 +814,8 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
     umma::fence_proxy_async();
     umma::fence_before();
     __syncthreads();
-    // D2 = Delta~^T K ; O2 = Delta^T (QK^T Gamma)^T ; then, with chunk c + 1
-    // resident, its [K;Q] K^T (thread 0) and its decays (warp 4)
+    // D2 = Delta~^T K ; O2 = Delta^T (QK^T Gamma)^T ; chunk c + 1's decays
+    // (warp 4) meanwhile
     if (tid == 0) {
       umma::fence_after();
       const uint32_t dt = smem_addr(S.dt), dtt = smem_addr(S.dtt), qk = smem_addr(S.qk);
@@ -810,14 +826,6 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
         umma::mma_bf16(tmem + TM_O2, umma::desc(dt + s * 32, 16, 1024), umma::desc(qk + s * 32, 16, 1024),
                        ID_64_KK, s > 0);
       umma::commit(&S.mma_bar);
-      if (c + 1 < nch) {
-        if (mbar_wait(&S.ld_full[(c + 1) & 1], ((c + 1) >> 1) & 1)) {
-          issue_kq(c + 1);
-          kq_issued = c + 2;
-        } else {
-          S.abort = 1;
-        }
-      }
     } else if (warp == 4 && c + 1 < nch) {
       if (__all_sync(0xffffffffu, mbar_wait(&S.ld_full[(c + 1) & 1], ((c + 1) >> 1) & 1)))
         chunk_decays(c + 1);
@@ -873,6 +881,10 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
     umma::fence_proxy_async();
     umma::fence_before();
     __syncthreads();
+    if (tid == 0 && c + 1 < nch && kq_issued == c + 2) {
+      umma::fence_after();
+      issue_o1_commit(c + 1);
+    }
     // output rows of the chunk's tokens: 16-byte stores of whole rows (the
     // staging tile is next written after the following chunk's first barrier)
     {
