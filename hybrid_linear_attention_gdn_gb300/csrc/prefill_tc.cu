@@ -642,21 +642,22 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
   };
   // thread 0: [K;Q] K^T of chunk c into TM_KQ
   auto issue_kq = [&](int c) {
-    const uint32_t kq = smem_addr(S.kq[c & 1]);
+    const uint64_t dkq = umma::desc(smem_addr(S.kq[c & 1]), 16, 1024);
+#pragma unroll
     for (int s = 0; s < 8; ++s) {
       const uint32_t ko = (s >> 2) * 16384 + (s & 3) * 32;
-      umma::mma_bf16(tmem + TM_KQ, umma::desc(kq + ko, 16, 1024), umma::desc(kq + ko, 16, 1024), ID_64_KK,
-                     s > 0);
+      umma::mma_bf16(tmem + TM_KQ, umma::adv(dkq, ko), umma::adv(dkq, ko), ID_64_KK, s > 0);
     }
   };
   // thread 0: O1 = S^T Q^T of chunk c (S as it enters the chunk) into TM_O1;
   // kq_bar then completes with both of chunk c's state-entry products
   auto issue_o1_commit = [&](int c) {
-    const uint32_t kq = smem_addr(S.kq[c & 1]), st = smem_addr(S.st);
+    const uint64_t dq = umma::desc(smem_addr(S.kq[c & 1]) + 8192, 16, 1024);
+    const uint64_t dst = umma::desc(smem_addr(S.st), 16, 1024);
+#pragma unroll
     for (int s = 0; s < 8; ++s) {
       const uint32_t ko = (s >> 2) * 16384 + (s & 3) * 32;
-      umma::mma_bf16(tmem + TM_O1, umma::desc(st + ko, 16, 1024), umma::desc(kq + 8192 + ko, 16, 1024),
-                     ID_64_KK, s > 0);
+      umma::mma_bf16(tmem + TM_O1, umma::adv(dst, ko), umma::adv(dq, ko), ID_64_KK, s > 0);
     }
     umma::commit(&S.kq_bar);
   };
@@ -743,13 +744,14 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
     // U^T = V^T T^T ; W^T = K^T T'^T
     if (tid == 0) {
       umma::fence_after();
-      const uint32_t tm = smem_addr(S.tm), tp = smem_addr(S.tp);
+      const uint64_t dv = umma::desc(vv, 64 * 128, 1024), dkm = umma::desc(kq, 16384, 1024);
+      const uint64_t dtm = umma::desc(smem_addr(S.tm), 16, 1024), dtp = umma::desc(smem_addr(S.tp), 16, 1024);
+#pragma unroll
       for (int s = 0; s < 4; ++s)
-        umma::mma_bf16(tmem + TM_U, umma::desc(vv + s * 2048, 64 * 128, 1024),
-                       umma::desc(tm + s * 32, 16, 1024), ID_64_MK, s > 0);
+        umma::mma_bf16(tmem + TM_U, umma::adv(dv, s * 2048), umma::adv(dtm, s * 32), ID_64_MK, s > 0);
+#pragma unroll
       for (int s = 0; s < 4; ++s)
-        umma::mma_bf16(tmem + TM_W, umma::desc(kq + s * 2048, 16384, 1024),
-                       umma::desc(tp + s * 32, 16, 1024), ID_64_MK, s > 0);
+        umma::mma_bf16(tmem + TM_W, umma::adv(dkm, s * 2048), umma::adv(dtp, s * 32), ID_64_MK, s > 0);
       umma::commit(&S.mma_bar);
     }
     if (!cta_wait(S, &S.mma_bar, mph)) break;
@@ -772,11 +774,11 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
     // P = S^T W^T
     if (tid == 0) {
       umma::fence_after();
-      const uint32_t wt = smem_addr(S.wt);
+      const uint64_t dst = umma::desc(st, 16, 1024), dwt = umma::desc(smem_addr(S.wt), 0, 1024);
+#pragma unroll
       for (int s = 0; s < 8; ++s) {
         const uint32_t ko = (s >> 2) * 16384 + (s & 3) * 32;
-        umma::mma_bf16(tmem + TM_P, umma::desc(st + ko, 16, 1024), umma::desc(wt + s * 2048, 0, 1024),
-                       ID_64_KM, s > 0);
+        umma::mma_bf16(tmem + TM_P, umma::adv(dst, ko), umma::adv(dwt, s * 2048), ID_64_KM, s > 0);
       }
       umma::commit(&S.mma_bar);
       // chunk c + 1's [K;Q] K^T runs on the tensor core during Delta below
@@ -818,13 +820,14 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
     // (warp 4) meanwhile
     if (tid == 0) {
       umma::fence_after();
-      const uint32_t dt = smem_addr(S.dt), dtt = smem_addr(S.dtt), qk = smem_addr(S.qk);
+      const uint64_t ddt = umma::desc(smem_addr(S.dt), 16, 1024), ddtt = umma::desc(smem_addr(S.dtt), 16, 1024);
+      const uint64_t dqk = umma::desc(smem_addr(S.qk), 16, 1024), dkm = umma::desc(kq, 16384, 1024);
+#pragma unroll
       for (int s = 0; s < 4; ++s)
-        umma::mma_bf16(tmem + TM_D2, umma::desc(dtt + s * 32, 16, 1024),
-                       umma::desc(kq + s * 2048, 16384, 1024), ID_128_KM, s > 0);
+        umma::mma_bf16(tmem + TM_D2, umma::adv(ddtt, s * 32), umma::adv(dkm, s * 2048), ID_128_KM, s > 0);
+#pragma unroll
       for (int s = 0; s < 4; ++s)
-        umma::mma_bf16(tmem + TM_O2, umma::desc(dt + s * 32, 16, 1024), umma::desc(qk + s * 32, 16, 1024),
-                       ID_64_KK, s > 0);
+        umma::mma_bf16(tmem + TM_O2, umma::adv(ddt, s * 32), umma::adv(dqk, s * 32), ID_64_KK, s > 0);
       umma::commit(&S.mma_bar);
     } else if (warp == 4 && c + 1 < nch) {
       if (__all_sync(0xffffffffu, mbar_wait(&S.ld_full[(c + 1) & 1], ((c + 1) >> 1) & 1)))

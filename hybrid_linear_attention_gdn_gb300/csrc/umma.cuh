@@ -31,6 +31,11 @@ __device__ __forceinline__ uint64_t desc(uint32_t saddr, uint32_t lbo, uint32_t 
   return d;
 }
 
+// The descriptor of a tile `bytes` further on (a multiple of 16): only the
+// start-address field changes, and it cannot carry out for shared-memory
+// addresses below 256 KB.
+__device__ __forceinline__ uint64_t adv(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
+
 // kind::f16 instruction descriptor: bf16 A and B, fp32 D.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
