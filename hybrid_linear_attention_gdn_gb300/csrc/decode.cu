@@ -506,11 +506,11 @@ int choose_nit(int dk, int dv, int units, int G, bool verify) {
   return nit;
 }
 
-// Kernel choice.  The persistent TMA-fed kernels are at least as fast as the
-// per-head kernels at every batch measured (1..256) on the Qwen3.5-shaped
-// layer, so they take every shape they support (dk 128, width 4; decode also
-// G*dv <= 256).  GDN_DECODE_PATH ("tma" / "rows") overrides the choice for
-// both decode and verify, for measurement.
+// Kernel choice.  The persistent TMA-fed decode kernel is at least as fast as
+// the per-head kernel at every batch measured (1..256) on the Qwen3.5-shaped
+// layer, so it takes every shape it supports (dk 128, width 4, G*dv <= 256);
+// verify keeps the per-head kernel (below).  GDN_DECODE_PATH=rows forces the
+// per-head decode, GDN_DECODE_PATH=tma the persistent verify, for measurement.
 int forced_path() {
   static int forced = [] {
     const char* e = std::getenv("GDN_DECODE_PATH");

@@ -37,6 +37,7 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kChunk = 64;
 constexpr int kMaxW = 8;
+constexpr int kCkGroup = 4;  // checkpoints per history-kernel thread
 
 struct PrefillArgs {
   float* ssm;
@@ -368,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const PrefillArgs a)
 // ---------------------------------------------------------------------------
 template <typename Tact, typename Tconv>
 __global__ void __launch_bounds__(kThreads) history_kernel(const PrefillArgs a) {
-  const int n = blockIdx.y;
+  const int n = blockIdx.y, grp = blockIdx.z;
   const int c = blockIdx.x * kThreads + threadIdx.x;
   if (c >= a.C) return;
   const int32_t slot = a.slot_ids[n];
@@ -378,10 +379,13 @@ __global__ void __launch_bounds__(kThreads) history_kernel(const PrefillArgs a) 
   if (t0 < 0 || len < 0 || t0 + len > a.total || p0 < 0) return;
   Tconv* hist = reinterpret_cast<Tconv*>(a.conv) + (size_t)slot * (a.W - 1) * a.C;
   const Tact* qkv = reinterpret_cast<const Tact*>(a.qkv);
+  // Group 0 owns the working slot's history: it reads the old rows before
+  // writing the new ones, and only its first checkpoint can reach back into
+  // them (later checkpoints lie at least one 64-token block further on).
   float old[kMaxW];
 #pragma unroll
   for (int j = 0; j < kMaxW - 1; ++j)
-    if (j < a.W - 1) old[j] = to_f32(hist[(size_t)j * a.C + c]);
+    if (j < a.W - 1) old[j] = grp == 0 ? to_f32(hist[(size_t)j * a.C + c]) : 0.f;
   // raw input at sequence-relative index m (negative: the old history)
   auto raw = [&](int64_t m) -> float {
     if (m >= 0) return to_f32(qkv[(t0 + m) * a.C + c]);
@@ -392,9 +396,11 @@ __global__ void __launch_bounds__(kThreads) history_kernel(const PrefillArgs a) 
     return v;
   };
   const int64_t blk = a.ckpt_block;
-  for (int64_t P = (p0 / blk + 1) * blk; P <= p1; P += blk) {
-    const int64_t idx = P / blk - p0 / blk - 1;
-    if (idx >= a.max_ckpt) break;
+#pragma unroll
+  for (int k = 0; k < kCkGroup; ++k) {
+    const int idx = grp * kCkGroup + k;
+    const int64_t P = (p0 / blk + 1 + idx) * blk;
+    if (idx >= a.max_ckpt || P > p1) break;
     const int32_t cid = a.ckpt_ids[(size_t)n * a.max_ckpt + idx];
     const int cc = slot_class(cid, a.ck_num_slots);
     if (cc == 2 && c == 0) report(a.err, GDN_DEV_ERR_SLOT_OOB);
@@ -403,6 +409,7 @@ __global__ void __launch_bounds__(kThreads) history_kernel(const PrefillArgs a) 
     for (int j = 0; j < a.W - 1; ++j)
       ch[(size_t)j * a.C + c] = from_f32<Tconv>(raw(P - p0 - (a.W - 1) + j));
   }
+  if (grp != 0) return;
   float nw[kMaxW];
 #pragma unroll
   for (int j = 0; j < kMaxW - 1; ++j)
@@ -410,6 +417,12 @@ __global__ void __launch_bounds__(kThreads) history_kernel(const PrefillArgs a) 
 #pragma unroll
   for (int j = 0; j < kMaxW - 1; ++j)
     if (j < a.W - 1) hist[(size_t)j * a.C + c] = from_f32<Tconv>(nw[j]);
+}
+
+// channels x sequences x groups of kCkGroup checkpoints
+dim3 history_grid(const PrefillArgs& a) {
+  const int groups = a.max_ckpt > kCkGroup ? (a.max_ckpt + kCkGroup - 1) / kCkGroup : 1;
+  return dim3((unsigned)((a.C + kThreads - 1) / kThreads), (unsigned)a.n_seq, (unsigned)groups);
 }
 
 // ---------------------------------------------------------------------------
@@ -447,8 +460,7 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t s) {
   const int n_tiles = (a.dv + DVT - 1) / DVT;
   ck<<<dim3((unsigned)(a.hv * n_tiles), (unsigned)a.n_seq), kThreads, L::bytes, s>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  history_kernel<Tact, Tconv><<<dim3((unsigned)((a.C + kThreads - 1) / kThreads), (unsigned)a.n_seq),
-                                kThreads, 0, s>>>(a);
+  history_kernel<Tact, Tconv><<<history_grid(a), kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -461,7 +473,7 @@ cudaError_t dispatch_prefill(const PrefillArgs& a, int act, int cv, cudaStream_t
 }
 
 cudaError_t launch_history(const PrefillArgs& a, int act, int cv, cudaStream_t s) {
-  const dim3 grid((unsigned)((a.C + kThreads - 1) / kThreads), (unsigned)a.n_seq);
+  const dim3 grid = history_grid(a);
   if (act == GDN_F32 && cv == GDN_F32)
     history_kernel<float, float><<<grid, kThreads, 0, s>>>(a);
   else if (act == GDN_BF16 && cv == GDN_BF16)
@@ -506,7 +518,8 @@ extern "C" gdn_status gdn_chunk_prefill(const gdn_dims* dims, gdn_pool pool, gdn
   if (n_seq < 0 || total_tokens < 0 || max_ckpt < 0) return GDN_ERR_INVALID_ARG;
   if (ckpt_block <= 0 || ckpt_block % kChunk) return GDN_ERR_INVALID_ARG;
   if (n_seq == 0) return GDN_OK;
-  if (n_seq > 65535 || total_tokens > 2147483647LL) return GDN_ERR_UNSUPPORTED;
+  if (n_seq > 65535 || total_tokens > 2147483647LL || max_ckpt > kCkGroup * 65535)
+    return GDN_ERR_UNSUPPORTED;
   if ((st = check_pool(*dims, pool)) != GDN_OK) return st;
   if (max_ckpt > 0 && (st = check_pool(*dims, ckpt)) != GDN_OK) return st;
   if (!params || !params->conv_w || !params->A_log || !params->dt_bias) return GDN_ERR_INVALID_ARG;

@@ -153,7 +153,8 @@ gdn_status gdn_spec_commit(const gdn_dims* dims, gdn_pool spec, gdn_pool work,
  *     cu_seqlens[n_seq] = total_tokens; a sequence violating this (or with
  *     start_pos < 0) is skipped and sets GDN_DEV_ERR_SEQLENS
  *   start_pos [n_seq] int64 (device)
- *   ckpt_ids [n_seq][max_ckpt] int32; ckpt_block a positive multiple of 64
+ *   ckpt_ids [n_seq][max_ckpt] int32; ckpt_block a positive multiple of 64;
+ *     max_ckpt above 262,140 returns GDN_ERR_UNSUPPORTED
  *   qkv [total_tokens][C], a,b [total_tokens][hv], out [total_tokens][hv][dv]
  *   workspace: >= gdn_chunk_prefill_workspace_size(...) bytes, 256-aligned
  */
