@@ -444,6 +444,29 @@ def measure_rows(gdn, synth, dev, stream, hbm_peak, bf16_peak, which="all", pref
             gdn.spec_commit(dims, spec, pool, spec_sets[i % 4], L, work_sets[i % 4])
         fm(0)
         rows["spec_commit_b16"] = frac(B * 2 * slot_bytes, _events_time(fm, reps, stream))
+        del spec
+
+        # verify at larger batches (T = 8), two alternating request / spec-cache sets
+        vsweep = {}
+        for Bv in (32, 64, 128):
+            spec_v = gdn.StatePool.empty(dims, 2 * Bv * T, dev)
+            ss = [torch.arange(k * Bv * T, (k + 1) * Bv * T, dtype=torch.int32, device=dev).reshape(Bv, T)
+                  for k in range(2)]
+            ws_ = [perm[k * Bv:(k + 1) * Bv].to(dev) for k in range(2)]
+            vi = [tuple(t.to(dev) for t in synth.tokens(shape, g, (Bv, T))) for _ in range(2)]
+            vo = torch.empty((Bv, T, 32, 128), dtype=torch.bfloat16, device=dev)
+
+            def fvb(i, spec_v=spec_v, ss=ss, ws_=ws_, vi=vi, vo=vo):
+                q, a, b = vi[i % 2]
+                gdn.spec_verify(dims, pool, spec_v, params, ws_[i % 2], ss[i % 2], q, a, b, vo)
+            fvb(0)
+            nb = Bv * (slot_bytes + T * (16384 + 128) + T * slot_bytes + T * 8192)
+            rv = frac(nb, _events_time(fvb, reps, stream))
+            rv["draft_tokens_per_s"] = Bv * T / (rv["ms"] * 1e-3)
+            vsweep[str(Bv)] = rv
+            del spec_v
+            torch.cuda.empty_cache()
+        rows["spec_verify_sweep_t8"] = vsweep
 
     if full:
         slot_and_spec_rows()

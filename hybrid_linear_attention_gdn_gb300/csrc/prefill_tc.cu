@@ -142,18 +142,13 @@ __device__ __forceinline__ int seq_of_chunk(const int32_t* base, int n_seq, int 
 // features: grid (n_chunks_max, hk), 256 threads, one CTA per (chunk, QK head):
 // q and k of QK head hq and v of the G V heads reading it.  The CTA stages its
 // input tile (3 rows before the chunk + its 64 rows, all 256 + G*128 channels)
-// in shared memory with cp.async; then each thread takes one 8-channel group
-// of a row at a time: conv1d over the 4 staged rows, SiLU, and for q/k the
-// row's L2 norm from a 16-lane shuffle reduction (a warp holds one row's 16 q
-// groups and 16 k groups), and writes the 8 results as one 16-byte piece of
-// the swizzled operand image.
+// in shared memory: rows inside the sequence by bulk copies (q, k and v
+// segments of each token row), rows before it from the conv history, rows
+// past it as zeros.  Then each lane walks 8 consecutive rows of one 8-channel
+// group (a sliding window of 4 staged rows): conv1d, SiLU, for q/k the row's
+// L2 norm by a 16-lane shuffle reduction (a warp holds one row's 16 q groups
+// and 16 k groups), and one 16-byte store into the swizzled operand image.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_addr(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
-}
 __device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8]) {
   const uint4 u = *reinterpret_cast<const uint4*>(p);
   const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
@@ -170,28 +165,38 @@ __device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
   v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
-// conv1d (width 4, tile rows r .. r+3 = positions P+r-3 .. P+r) + SiLU for the
-// 8 channels at local channel lc; zero outside the sequence.  The fast
+// conv1d (width 4) + SiLU of 8 channels walking 8 rows r0 .. r0+7 (tile rows
+// r .. r+3 = positions P+r-3 .. P+r); zero outside the sequence.  The fast
 // exponential and division are far finer than the bf16 operands they feed.
-template <typename Tact>
-__device__ __forceinline__ void conv8(const Tact* xs, int nch, int r, int lc, const float (&w)[8][4], bool valid,
-                                      float (&y)[8]) {
+// emit(r, y) receives each row's 8 results.
+template <typename Tact, class Emit>
+__device__ __forceinline__ void conv_walk8(const Tact* xs, int nch, int r0, int lc, const float (&w)[8][4],
+                                           int64_t P, int64_t p0, int64_t p1, Emit emit) {
   float x[4][8];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) load8(xs + (size_t)(r + j) * nch + lc, x[j]);
+  for (int j = 0; j < 3; ++j) load8(xs + (size_t)(r0 + j) * nch + lc, x[j]);
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    float acc = w[c][0] * x[0][c];
-    acc = fmaf(w[c][1], x[1][c], acc);
-    acc = fmaf(w[c][2], x[2][c], acc);
-    acc = fmaf(w[c][3], x[3][c], acc);
-    y[c] = valid ? __fdividef(acc, 1.f + exp_ftz(-acc)) : 0.f;
+  for (int k = 0; k < 8; ++k) {
+    const int r = r0 + k;
+    load8(xs + (size_t)(r + 3) * nch + lc, x[(k + 3) & 3]);
+    const bool valid = P + r >= p0 && P + r < p1;
+    float y[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      float acc = w[c][0] * x[k & 3][c];
+      acc = fmaf(w[c][1], x[(k + 1) & 3][c], acc);
+      acc = fmaf(w[c][2], x[(k + 2) & 3][c], acc);
+      acc = fmaf(w[c][3], x[(k + 3) & 3][c], acc);
+      y[c] = valid ? __fdividef(acc, 1.f + exp_ftz(-acc)) : 0.f;
+    }
+    emit(r, y);
   }
 }
 
 template <typename Tact, typename Tconv>
 __global__ void __launch_bounds__(kTh) tc_features_kernel(const TcArgs a) {
   extern __shared__ __align__(16) unsigned char fsm[];
+  __shared__ __align__(8) uint64_t tile_bar;
   const int gc = blockIdx.x, hq = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (gc >= a.chunk_base[a.n_seq]) return;
@@ -204,8 +209,6 @@ __global__ void __launch_bounds__(kTh) tc_features_kernel(const TcArgs a) {
   const int64_t p1 = p0 + len;
   const int GD = a.G * kD;
   const int nch = 2 * kD + GD;               // local channels: q | k | v of the G heads
-  constexpr int EPC = 16 / sizeof(Tact);     // elements per 16-byte piece
-  const int cpr = nch / EPC;                 // pieces per tile row
   Tact* xs = reinterpret_cast<Tact*>(fsm);   // [kC + 3][nch], row i = position P - 3 + i
   const Tact* qkv = reinterpret_cast<const Tact*>(a.qkv);
   const Tconv* hist = reinterpret_cast<const Tconv*>(a.conv) + (size_t)slot * 3 * a.C;
@@ -214,21 +217,36 @@ __global__ void __launch_bounds__(kTh) tc_features_kernel(const TcArgs a) {
     if (lc < 2 * kD) return (size_t)a.hk * kD + (size_t)hq * kD + (lc - kD);
     return 2 * (size_t)a.hk * kD + (size_t)hq * GD + (lc - 2 * kD);
   };
-  for (int e = tid; e < (kC + 3) * cpr; e += kTh) {
-    const int i = e / cpr, ch = e % cpr;
-    const int64_t pos = P - 3 + i;
-    Tact* dst = xs + (size_t)i * nch + ch * EPC;
-    const size_t c = gchan(ch * EPC);
-    if (pos >= p0 && pos < p1) {
-      cp_async16(dst, qkv + (size_t)(t0 + pos - p0) * a.C + c);
-    } else if (pos < p0 && pos >= p0 - 3) {
-      const Tconv* src = hist + (size_t)(3 - (p0 - pos)) * a.C + c;
-#pragma unroll
-      for (int k = 0; k < EPC; ++k) dst[k] = from_f32<Tact>(to_f32(src[k]));
-    } else {
-#pragma unroll
-      for (int k = 0; k < EPC; ++k) dst[k] = from_f32<Tact>(0.f);
+  // tile rows inside the sequence: [i_lo, i_hi)
+  const int64_t lo = p0 - (P - 3), hi = p1 - (P - 3);
+  const int i_lo = lo > 0 ? (int)lo : 0, i_hi = hi < kC + 3 ? (int)hi : kC + 3;
+  const int n_in = max(0, i_hi - i_lo);
+  if (tid == 0) {
+    mbar_init(&tile_bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (warp == 0) {
+    if (lane == 0) mbar_arrive_expect_tx(&tile_bar, (uint32_t)(n_in * nch * sizeof(Tact)));
+    __syncwarp();
+    // three segments per row: q (kD), k (kD), v (G*kD) channels
+    for (int e = lane; e < 3 * n_in; e += 32) {
+      const int i = i_lo + e / 3, sg = e % 3;
+      const int lc = sg == 0 ? 0 : (sg == 1 ? kD : 2 * kD);
+      const uint32_t nb = (uint32_t)((sg == 2 ? GD : kD) * sizeof(Tact));
+      const int64_t pos = P - 3 + i;
+      bulk_g2s(xs + (size_t)i * nch + lc, qkv + (size_t)(t0 + pos - p0) * a.C + gchan(lc), nb, &tile_bar);
     }
+  }
+  // rows before the sequence (conv history) and past it (zeros)
+  const int n_out = (kC + 3) - n_in;
+  for (int e = tid; e < n_out * nch; e += kTh) {
+    const int k = e / nch, lc = e % nch;
+    const int i = k < i_lo ? k : n_in + k;  // rows [0, i_lo) then [i_hi, kC + 3)
+    const int64_t pos = P - 3 + i;
+    float v = 0.f;
+    if (pos < p0 && pos >= p0 - 3) v = to_f32(hist[(size_t)(3 - (p0 - pos)) * a.C + gchan(lc)]);
+    xs[(size_t)i * nch + lc] = from_f32<Tact>(v);
   }
   // gates (rows outside the sequence: g = beta = 0)
   for (int e = tid; e < kC * a.G; e += kTh) {
@@ -247,11 +265,16 @@ __global__ void __launch_bounds__(kTh) tc_features_kernel(const TcArgs a) {
     gt[r] = gv;
     gt[kC + r] = bv;
   }
-  cp_async_wait_all();
+  // every thread observes the copies' completion before reading the tile
+  if (!mbar_wait(&tile_bar, 0)) {
+    report(a.err, GDN_DEV_ERR_TIMEOUT);
+    mbar_wait(&tile_bar, 0);  // one more bounded wait for copies still in flight
+    return;
+  }
   __syncthreads();
 
-  // q and k: warp w takes rows w, w + 8, ...; lane l < 16 is q channels
-  // 8l .. 8l+7, lane 16 + l the same k channels
+  // q and k: warp w walks rows 8w .. 8w+7; lane l < 16 is q channels 8l .. 8l+7,
+  // lane 16 + l the same k channels
   {
     const int lc = 8 * lane;  // local channel (q: 0..127, k: 128..255)
     float w[8][4];
@@ -263,9 +286,7 @@ __global__ void __launch_bounds__(kTh) tc_features_kernel(const TcArgs a) {
     const bool isq = lane < 16;
     const float qscale = isq ? rsqrtf((float)kD) : 1.f;
     uint8_t* kq = a.ws_kq + ((size_t)gc * a.hk + hq) * kKQBytes;
-    for (int r = warp; r < kC; r += kTh / 32) {
-      float y[8];
-      conv8(xs, nch, r, lc, w, P + r >= p0 && P + r < p1, y);
+    conv_walk8(xs, nch, 8 * warp, lc, w, P, p0, p1, [&](int r, float (&y)[8]) {
       float ss = 0.f;
 #pragma unroll
       for (int c = 0; c < 8; ++c) ss = fmaf(y[c], y[c], ss);
@@ -276,29 +297,25 @@ __global__ void __launch_bounds__(kTh) tc_features_kernel(const TcArgs a) {
       for (int c = 0; c < 8; ++c) y[c] *= sc;
       const int R = isq ? kC + r : r;  // image rows: k^ 0..63, q^ 64..127
       *reinterpret_cast<uint4*>(kq + umma::sw128_off(R, 8 * (lane & 15), 128 * 128)) = umma::pack8_bf16(y);
-    }
+    });
   }
-  // v: 8-channel groups of the G heads, G*16 groups per row
+  // v: (8-channel group, 8-row block) items, G*16 groups per row
   {
     const int gpr = a.G * (kD / 8);
-    int wch = -1;
-    float w[8][4];
-    for (int e = tid; e < kC * gpr; e += kTh) {
-      const int r = e / gpr, ch = e % gpr;
+    for (int e = tid; e < 8 * gpr; e += kTh) {
+      const int ch = e % gpr, rb = e / gpr;
       const int lc = 2 * kD + 8 * ch;
-      if (ch != wch) {
-        wch = ch;
+      float w[8][4];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const float4 w4 = *reinterpret_cast<const float4*>(a.conv_w + gchan(lc + c) * 4);
-          w[c][0] = w4.x; w[c][1] = w4.y; w[c][2] = w4.z; w[c][3] = w4.w;
-        }
+      for (int c = 0; c < 8; ++c) {
+        const float4 w4 = *reinterpret_cast<const float4*>(a.conv_w + gchan(lc + c) * 4);
+        w[c][0] = w4.x; w[c][1] = w4.y; w[c][2] = w4.z; w[c][3] = w4.w;
       }
-      float y[8];
-      conv8(xs, nch, r, lc, w, P + r >= p0 && P + r < p1, y);
       const int h = hq * a.G + ch / (kD / 8), d = 8 * (ch % (kD / 8));
       uint8_t* vimg = a.ws_v + ((size_t)gc * a.hv + h) * kVBytes;
-      *reinterpret_cast<uint4*>(vimg + umma::sw128_off(r, d, 64 * 128)) = umma::pack8_bf16(y);
+      conv_walk8(xs, nch, 8 * rb, lc, w, P, p0, p1, [&](int r, float (&y)[8]) {
+        *reinterpret_cast<uint4*>(vimg + umma::sw128_off(r, d, 64 * 128)) = umma::pack8_bf16(y);
+      });
     }
   }
 }
