@@ -142,13 +142,18 @@ __device__ __forceinline__ int seq_of_chunk(const int32_t* base, int n_seq, int 
 // features: grid (n_chunks_max, hk), 256 threads, one CTA per (chunk, QK head):
 // q and k of QK head hq and v of the G V heads reading it.  The CTA stages its
 // input tile (3 rows before the chunk + its 64 rows, all 256 + G*128 channels)
-// in shared memory: rows inside the sequence by bulk copies (q, k and v
-// segments of each token row), rows before it from the conv history, rows
-// past it as zeros.  Then each lane walks 8 consecutive rows of one 8-channel
+// in shared memory with cp.async (rows before the sequence from the conv
+// history, rows past it as zeros).  Then each lane walks 8 consecutive rows of one 8-channel
 // group (a sliding window of 4 staged rows): conv1d, SiLU, for q/k the row's
 // L2 norm by a 16-lane shuffle reduction (a warp holds one row's 16 q groups
 // and 16 k groups), and one 16-byte store into the swizzled operand image.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
+}
 __device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8]) {
   const uint4 u = *reinterpret_cast<const uint4*>(p);
   const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
@@ -196,7 +201,6 @@ __device__ __forceinline__ void conv_walk8(const Tact* xs, int nch, int r0, int 
 template <typename Tact, typename Tconv>
 __global__ void __launch_bounds__(kTh) tc_features_kernel(const TcArgs a) {
   extern __shared__ __align__(16) unsigned char fsm[];
-  __shared__ __align__(8) uint64_t tile_bar;
   const int gc = blockIdx.x, hq = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (gc >= a.chunk_base[a.n_seq]) return;
@@ -217,36 +221,23 @@ __global__ void __launch_bounds__(kTh) tc_features_kernel(const TcArgs a) {
     if (lc < 2 * kD) return (size_t)a.hk * kD + (size_t)hq * kD + (lc - kD);
     return 2 * (size_t)a.hk * kD + (size_t)hq * GD + (lc - 2 * kD);
   };
-  // tile rows inside the sequence: [i_lo, i_hi)
-  const int64_t lo = p0 - (P - 3), hi = p1 - (P - 3);
-  const int i_lo = lo > 0 ? (int)lo : 0, i_hi = hi < kC + 3 ? (int)hi : kC + 3;
-  const int n_in = max(0, i_hi - i_lo);
-  if (tid == 0) {
-    mbar_init(&tile_bar, 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-  if (warp == 0) {
-    if (lane == 0) mbar_arrive_expect_tx(&tile_bar, (uint32_t)(n_in * nch * sizeof(Tact)));
-    __syncwarp();
-    // three segments per row: q (kD), k (kD), v (G*kD) channels
-    for (int e = lane; e < 3 * n_in; e += 32) {
-      const int i = i_lo + e / 3, sg = e % 3;
-      const int lc = sg == 0 ? 0 : (sg == 1 ? kD : 2 * kD);
-      const uint32_t nb = (uint32_t)((sg == 2 ? GD : kD) * sizeof(Tact));
-      const int64_t pos = P - 3 + i;
-      bulk_g2s(xs + (size_t)i * nch + lc, qkv + (size_t)(t0 + pos - p0) * a.C + gchan(lc), nb, &tile_bar);
-    }
-  }
-  // rows before the sequence (conv history) and past it (zeros)
-  const int n_out = (kC + 3) - n_in;
-  for (int e = tid; e < n_out * nch; e += kTh) {
-    const int k = e / nch, lc = e % nch;
-    const int i = k < i_lo ? k : n_in + k;  // rows [0, i_lo) then [i_hi, kC + 3)
+  constexpr int EPC = 16 / sizeof(Tact);     // elements per 16-byte piece
+  const int cpr = nch / EPC;                 // pieces per tile row
+  for (int e = tid; e < (kC + 3) * cpr; e += kTh) {
+    const int i = e / cpr, pc = e % cpr;
     const int64_t pos = P - 3 + i;
-    float v = 0.f;
-    if (pos < p0 && pos >= p0 - 3) v = to_f32(hist[(size_t)(3 - (p0 - pos)) * a.C + gchan(lc)]);
-    xs[(size_t)i * nch + lc] = from_f32<Tact>(v);
+    Tact* dst = xs + (size_t)i * nch + pc * EPC;
+    const size_t c = gchan(pc * EPC);
+    if (pos >= p0 && pos < p1) {
+      cp_async16(dst, qkv + (size_t)(t0 + pos - p0) * a.C + c);
+    } else if (pos < p0 && pos >= p0 - 3) {
+      const Tconv* src = hist + (size_t)(3 - (p0 - pos)) * a.C + c;
+#pragma unroll
+      for (int k = 0; k < EPC; ++k) dst[k] = from_f32<Tact>(to_f32(src[k]));
+    } else {
+#pragma unroll
+      for (int k = 0; k < EPC; ++k) dst[k] = from_f32<Tact>(0.f);
+    }
   }
   // gates (rows outside the sequence: g = beta = 0)
   for (int e = tid; e < kC * a.G; e += kTh) {
@@ -265,12 +256,7 @@ __global__ void __launch_bounds__(kTh) tc_features_kernel(const TcArgs a) {
     gt[r] = gv;
     gt[kC + r] = bv;
   }
-  // every thread observes the copies' completion before reading the tile
-  if (!mbar_wait(&tile_bar, 0)) {
-    report(a.err, GDN_DEV_ERR_TIMEOUT);
-    mbar_wait(&tile_bar, 0);  // one more bounded wait for copies still in flight
-    return;
-  }
+  cp_async_wait_all();
   __syncthreads();
 
   // q and k: warp w walks rows 8w .. 8w+7; lane l < 16 is q channels 8l .. 8l+7,
