@@ -199,7 +199,7 @@ __device__ __forceinline__ void conv_walk8(const Tact* xs, int nch, int r0, int 
 }
 
 template <typename Tact, typename Tconv>
-__global__ void __launch_bounds__(kTh) tc_features_kernel(const TcArgs a) {
+__global__ void __launch_bounds__(kTh, 3) tc_features_kernel(const TcArgs a) {
   extern __shared__ __align__(16) unsigned char fsm[];
   const int gc = blockIdx.x, hq = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
