@@ -328,15 +328,25 @@ struct __align__(1024) ChainSmem {
   float gates[2][2][kC];
   float b[2][kC], eb[2][kC], ebl[2][kC];  // by chunk parity
   uint64_t ld_full[2], mma_bar, kq_bar;
+  uint64_t ext_bar;  // compute warps finished reading [K;Q] K^T (one arrival per warp)
+  uint64_t st_bar;   // compute warps wrote the state image and read O1 (one arrival per warp)
   uint32_t tmem_base;
-  int abort;
 };
 
-// all threads wait (bounded) on a barrier phase; uniform result
-__device__ __forceinline__ bool cta_wait(ChainSmem& S, uint64_t* bar, uint32_t parity) {
-  if (!mbar_wait(bar, parity)) S.abort = 1;
-  __syncthreads();
-  return !S.abort;
+// The chain CTA is 8 compute warps and one issue warp (warp 8: TMA loads and
+// the tensor-core products that do not depend on the running state).  The
+// compute warps synchronise among themselves on named barrier kCompBar.
+constexpr int kIssueWarp = 8;
+constexpr int kChainThreads = kTh + 32;
+constexpr int kCompBar = 5;  // 1..4 are the solve's column-tile barriers
+__device__ __forceinline__ void compute_sync() { named_sync(kCompBar, kTh); }
+
+// compute threads wait (bounded) on a barrier phase, then synchronise; the
+// result (no compute thread has seen a wait expire, now or before) is the
+// same in every compute thread, so they all leave the chunk loop together
+__device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, bool& bad) {
+  if (!mbar_wait(bar, parity)) bad = true;
+  return !named_sync_or(kCompBar, kTh, bad);
 }
 
 // Warp-level tf32 MMA (m16n8k8, fp32 accumulate).  Fragment layout: lane =
@@ -448,7 +458,7 @@ __device__ __forceinline__ void solve_T(const float* A, float* X, float* Y, cons
         put_t_pair(to, o + r, o + c0, x0[r], x1[r], bc, ec);
       }
   }
-  __syncthreads();
+  compute_sync();
   // 8 -> 16: warps 0..3, block pair p (rows/cols 16p ..); M padded to 16
   if (warp < 4) {
     const int o = 16 * warp;
@@ -470,7 +480,7 @@ __device__ __forceinline__ void solve_T(const float* A, float* X, float* Y, cons
     X[ix(o + 8 + g, o + 2 * t + 1)] = -d[1];
     put_t_pair(to, o + 8 + g, o + 2 * t, -d[0], -d[1], bc, ec);
   }
-  __syncthreads();
+  compute_sync();
   // 16 -> 32: warps 0..3 = (pair q, column tile j)
   if (warp < 4) {
     const int o = 32 * (warp >> 1), j = warp & 1;
@@ -502,7 +512,7 @@ __device__ __forceinline__ void solve_T(const float* A, float* X, float* Y, cons
     put_t_pair(to, o + 16 + g, cc, -d[0], -d[1], bc, ec);
     put_t_pair(to, o + 24 + g, cc, -d[2], -d[3], bc, ec);
   }
-  __syncthreads();
+  compute_sync();
   // 32 -> 64: warps = (column tile j, row half mh); the two warps of a column
   // tile exchange their halves of Y_j = A_ba X_a[:, j] through a named
   // barrier.  Rows of X_a above 8j of column tile j are zero (k-steps skipped).
@@ -541,7 +551,7 @@ __device__ __forceinline__ void solve_T(const float* A, float* X, float* Y, cons
 }
 
 template <typename Tact>
-__global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
+__global__ void __launch_bounds__(kChainThreads, 1) tc_chain_kernel(const TcArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // the swizzled operand tiles need 1024-byte aligned bases
   ChainSmem& S = *reinterpret_cast<ChainSmem*>(
@@ -558,7 +568,7 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
   const int cls = slot_class(slot, a.num_slots);
   if (cls) {
     if (cls == 2 && h == 0 && tid == 0) report(a.err, GDN_DEV_ERR_SLOT_OOB);
-    for (int64_t e = tid; e < len * kD; e += kTh)
+    for (int64_t e = tid; e < len * kD; e += kChainThreads)
       out[((t0 + e / kD) * a.hv + h) * kD + (e % kD)] = from_f32<Tact>(0.f);
     return;
   }
@@ -571,7 +581,8 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
     mbar_init(&S.ld_full[1], 1);
     mbar_init(&S.mma_bar, 1);
     mbar_init(&S.kq_bar, 1);
-    S.abort = 0;
+    mbar_init(&S.ext_bar, kTh / 32);
+    mbar_init(&S.st_bar, kTh / 32);
     fence_mbar_init();
   }
   if (warp == 0) umma::tmem_alloc(&S.tmem_base, TM_COLS);
@@ -583,341 +594,344 @@ __global__ void __launch_bounds__(kTh, 1) tc_chain_kernel(const TcArgs a) {
   const int half = warp >> 2;               // which 64-column half this warp handles
   const uint32_t tlane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
 
-  // state rows: S^T[lrow][64*half .. +64) in registers, bf16 copy as operand
-  float* gS = a.ssm + (((size_t)slot * a.hv + h) * kD + lrow) * kD + 64 * half;
-  float sreg[64];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const float4 v = *reinterpret_cast<const float4*>(gS + 4 * i);
-    sreg[4 * i] = v.x;
-    sreg[4 * i + 1] = v.y;
-    sreg[4 * i + 2] = v.z;
-    sreg[4 * i + 3] = v.w;
-  }
-  umma::store_row64(S.st + half * (128 * 128), lrow, sreg);
-  // T and T' are lower triangular: their upper triangles are written only here
-  for (int e = tid; e < 2 * 64 * 128 / 16; e += kTh)
-    reinterpret_cast<uint4*>(e < 512 ? S.tm : S.tp)[e & 511] = make_uint4(0u, 0u, 0u, 0u);
-
-  auto issue_load = [&](int c) {
-    const int gc = gc0 + c, buf = c & 1;
-    mbar_arrive_expect_tx(&S.ld_full[buf], kKQBytes + kVBytes + kGateBytes);
-    bulk_g2s(S.kq[buf], a.ws_kq + ((size_t)gc * a.hk + hq) * kKQBytes, kKQBytes, &S.ld_full[buf]);
-    bulk_g2s(S.v[buf], a.ws_v + ((size_t)gc * a.hv + h) * kVBytes, kVBytes, &S.ld_full[buf]);
-    bulk_g2s(S.gates[buf], a.ws_gate + ((size_t)gc * a.hv + h) * (2 * kC), kGateBytes, &S.ld_full[buf]);
-  };
-  if (tid == 0 && nch > 0) issue_load(0);
-  umma::fence_proxy_async();
-  __syncthreads();
-
   constexpr uint32_t ID_64_KK = umma::idesc_bf16(128, 64, false, false);
   constexpr uint32_t ID_64_MK = umma::idesc_bf16(128, 64, true, false);
   constexpr uint32_t ID_64_KM = umma::idesc_bf16(128, 64, false, true);
   constexpr uint32_t ID_128_KM = umma::idesc_bf16(128, 128, false, true);
-  uint32_t mph = 0;
-  int issued = nch > 0 ? 1 : 0;  // chunks whose loads were issued
-  int kq_issued = 0;             // chunks whose [K;Q] K^T was issued
-  float* Af = S.ax[0];
-  float* Xf = S.ax[1];
-  float* Yf = reinterpret_cast<float*>(S.wt);
 
-  // one warp, gates of chunk c resident: cumulative log-decay b, e^b, e^{b_last - b}
-  auto chunk_decays = [&](int c) {
-    const int buf = c & 1;
-    float bv[2], carry = 0.f;
+  if (warp == kIssueWarp) {
+    // Issue warp, one lane: operand loads one chunk ahead; for chunk c, [K;Q]
+    // K^T as soon as chunk c-1's extraction freed TM_KQ (it runs on the tensor
+    // core during chunk c-1's solve) and O1 = S^T Q^T once the state entering
+    // chunk c is in its image (it runs under chunk c-1's output stores); both
+    // complete on kq_bar.
+    if (lane == 0 && nch > 0) {
+      auto issue_load = [&](int c) {
+        const int gc = gc0 + c, buf = c & 1;
+        mbar_arrive_expect_tx(&S.ld_full[buf], kKQBytes + kVBytes + kGateBytes);
+        bulk_g2s(S.kq[buf], a.ws_kq + ((size_t)gc * a.hk + hq) * kKQBytes, kKQBytes, &S.ld_full[buf]);
+        bulk_g2s(S.v[buf], a.ws_v + ((size_t)gc * a.hv + h) * kVBytes, kVBytes, &S.ld_full[buf]);
+        bulk_g2s(S.gates[buf], a.ws_gate + ((size_t)gc * a.hv + h) * (2 * kC), kGateBytes, &S.ld_full[buf]);
+      };
+      int issued = 1, kq_issued = 0;
+      bool ok = true;
+      issue_load(0);
+      for (int c = 0; c < nch && ok; ++c) {
+        ok = mbar_wait(&S.ld_full[c & 1], (c >> 1) & 1) && (c == 0 || mbar_wait(&S.ext_bar, (c - 1) & 1));
+        if (!ok) break;
+        umma::fence_after();
+        const uint64_t dkq = umma::desc(smem_addr(S.kq[c & 1]), 16, 1024);
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      float v = S.gates[buf][0][32 * hh + lane];
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float u = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += u;
-      }
-      bv[hh] = v + carry;
-      carry = __shfl_sync(0xffffffffu, bv[hh], 31);
-    }
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      S.b[buf][32 * hh + lane] = bv[hh];
-      S.eb[buf][32 * hh + lane] = expf(bv[hh]);
-      S.ebl[buf][32 * hh + lane] = expf(carry - bv[hh]);
-    }
-  };
-  // thread 0: [K;Q] K^T of chunk c into TM_KQ
-  auto issue_kq = [&](int c) {
-    const uint64_t dkq = umma::desc(smem_addr(S.kq[c & 1]), 16, 1024);
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      const uint32_t ko = (s >> 2) * 16384 + (s & 3) * 32;
-      umma::mma_bf16(tmem + TM_KQ, umma::adv(dkq, ko), umma::adv(dkq, ko), ID_64_KK, s > 0);
-    }
-  };
-  // thread 0: O1 = S^T Q^T of chunk c (S as it enters the chunk) into TM_O1;
-  // kq_bar then completes with both of chunk c's state-entry products
-  auto issue_o1_commit = [&](int c) {
-    const uint64_t dq = umma::desc(smem_addr(S.kq[c & 1]) + 8192, 16, 1024);
-    const uint64_t dst = umma::desc(smem_addr(S.st), 16, 1024);
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      const uint32_t ko = (s >> 2) * 16384 + (s & 3) * 32;
-      umma::mma_bf16(tmem + TM_O1, umma::adv(dst, ko), umma::adv(dq, ko), ID_64_KK, s > 0);
-    }
-    umma::commit(&S.kq_bar);
-  };
-  if (nch > 0 && cta_wait(S, &S.ld_full[0], 0)) {
-    if (warp == 0) chunk_decays(0);
-    if (tid == 0) {
-      umma::fence_after();
-      issue_kq(0);
-      issue_o1_commit(0);
-      kq_issued = 1;
-    }
-  }
-
-  // Per chunk c: the state-independent products of chunk c + 1 ([K;Q] K^T
-  // and its decays) start while chunk c's state update runs, and chunk c + 1's
-  // O1 as soon as the state has left chunk c.
-  for (int c = 0; c < nch && !S.abort; ++c) {
-    const int buf = c & 1;
-    const int64_t P = (p0 / kC + c) * kC;
-    const float* eb = S.eb[buf];
-    if (tid == 0 && c + 1 < nch) {
-      issue_load(c + 1);
-      issued = c + 2;
-    }
-    // chunk c's operands landed (warp 0 saw it already; each thread observes
-    // the copy's completion itself before reading the gates)
-    if (!mbar_wait(&S.ld_full[buf], (c >> 1) & 1)) S.abort = 1;
-    if (!cta_wait(S, &S.kq_bar, c & 1)) break;
-    umma::fence_after();
-    const uint32_t kq = smem_addr(S.kq[buf]), vv = smem_addr(S.v[buf]);
-    const uint32_t st = smem_addr(S.st);
-    // A = strict_lower(beta (.) K K^T (.) Gamma) (fp32) and the decayed,
-    // masked Q K^T operand; lanes 0-63 hold K K^T rows, 64-127 Q K^T rows
-    {
-      const float* b = S.b[buf];
-      float v[32], bc[32];
-      const int c0 = 32 * half;
-      // the column decays, loaded before any store so none waits on one
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float4 b4 = *reinterpret_cast<const float4*>(b + c0 + 4 * i);
-        bc[4 * i] = b4.x;
-        bc[4 * i + 1] = b4.y;
-        bc[4 * i + 2] = b4.z;
-        bc[4 * i + 3] = b4.w;
-      }
-      umma::tmem_ld32(tlane + TM_KQ + 32 * half, v);
-      if (lrow < kC) {
-        const int r = lrow;
-        const float br = b[r], betar = S.gates[buf][1][r];
-        float av[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int cc = c0 + i;
-          av[i] = cc < r ? betar * v[i] * exp_ftz(br - bc[i]) : 0.f;
+        for (int s = 0; s < 8; ++s) {
+          const uint32_t ko = (s >> 2) * 16384 + (s & 3) * 32;
+          umma::mma_bf16(tmem + TM_KQ, umma::adv(dkq, ko), umma::adv(dkq, ko), ID_64_KK, s > 0);
         }
+        ok = mbar_wait(&S.st_bar, c & 1);
+        if (!ok) break;
+        umma::fence_after();
+        const uint64_t dq = umma::adv(dkq, 8192), dst = umma::desc(smem_addr(S.st), 16, 1024);
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          *reinterpret_cast<float4*>(Af + ix(r, c0 + 4 * q)) =
-              make_float4(av[4 * q], av[4 * q + 1], av[4 * q + 2], av[4 * q + 3]);
-      } else {
-        const int t = lrow - kC;
-        const float bt = b[t];
-        float m[32];
+        for (int s = 0; s < 8; ++s) {
+          const uint32_t ko = (s >> 2) * 16384 + (s & 3) * 32;
+          umma::mma_bf16(tmem + TM_O1, umma::adv(dst, ko), umma::adv(dq, ko), ID_64_KK, s > 0);
+        }
+        umma::commit(&S.kq_bar);
+        kq_issued = c + 1;
+        // chunk c+1 into the buffer of chunk c-1, whose last reader (its state
+        // update) finished before st_bar completed
+        if (c + 1 < nch) {
+          issue_load(c + 1);
+          issued = c + 2;
+        }
+      }
+      if (!ok) {
+        report(a.err, GDN_DEV_ERR_TIMEOUT);
+        // let issued loads and products land before shared memory and TMEM go away
+        for (int c = (issued > 2 ? issued - 2 : 0); c < issued; ++c) mbar_wait(&S.ld_full[c & 1], (c >> 1) & 1);
+        if (kq_issued > 0) mbar_wait(&S.kq_bar, (kq_issued - 1) & 1);
+      }
+    }
+    __syncwarp();
+  } else {
+    // state rows: S^T[lrow][64*half .. +64) in registers, bf16 copy as operand
+    float* gS = a.ssm + (((size_t)slot * a.hv + h) * kD + lrow) * kD + 64 * half;
+    float sreg[64];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float4 v = *reinterpret_cast<const float4*>(gS + 4 * i);
+      sreg[4 * i] = v.x;
+      sreg[4 * i + 1] = v.y;
+      sreg[4 * i + 2] = v.z;
+      sreg[4 * i + 3] = v.w;
+    }
+    umma::store_row64(S.st + half * (128 * 128), lrow, sreg);
+    // T and T' are lower triangular: their upper triangles are written only here
+    for (int e = tid; e < 2 * 64 * 128 / 16; e += kTh)
+      reinterpret_cast<uint4*>(e < 512 ? S.tm : S.tp)[e & 511] = make_uint4(0u, 0u, 0u, 0u);
+
+    // the state image and the T tiles reach the tensor core's proxy; then
+    // the issue warp may read the image
+    umma::fence_proxy_async();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.st_bar);
+    uint32_t mph = 0;
+    bool bad = false;  // this thread saw a bounded wait expire
+    float* Af = S.ax[0];
+    float* Xf = S.ax[1];
+    float* Yf = reinterpret_cast<float*>(S.wt);
+
+    // one warp, gates of chunk c resident: cumulative log-decay b, e^b, e^{b_last - b}
+    auto chunk_decays = [&](int c) {
+      const int buf = c & 1;
+      float bv[2], carry = 0.f;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float v = S.gates[buf][0][32 * hh + lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float u = __shfl_up_sync(0xffffffffu, v, o);
+          if (lane >= o) v += u;
+        }
+        bv[hh] = v + carry;
+        carry = __shfl_sync(0xffffffffu, bv[hh], 31);
+      }
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        S.b[buf][32 * hh + lane] = bv[hh];
+        S.eb[buf][32 * hh + lane] = expf(bv[hh]);
+        S.ebl[buf][32 * hh + lane] = expf(carry - bv[hh]);
+      }
+    };
+    bool alive = nch == 0 || cta_wait(&S.ld_full[0], 0, bad);
+    if (nch > 0 && alive && warp == 0) chunk_decays(0);
+
+    // Per chunk c (compute warps): the decays of chunk c + 1 are computed while
+    // chunk c's state update runs; [K;Q] K^T and O1 come from the issue warp.
+    for (int c = 0; c < nch && alive; ++c) {
+      const int buf = c & 1;
+      const int64_t P = (p0 / kC + c) * kC;
+      const float* eb = S.eb[buf];
+      // chunk c's operands landed (warp 0 saw it already; each thread observes
+      // the copy's completion itself before reading the gates)
+      if (!mbar_wait(&S.ld_full[buf], (c >> 1) & 1)) bad = true;
+      if (!(alive = cta_wait(&S.kq_bar, c & 1, bad))) break;
+      umma::fence_after();
+      const uint32_t kq = smem_addr(S.kq[buf]), vv = smem_addr(S.v[buf]);
+      const uint32_t st = smem_addr(S.st);
+      // A = strict_lower(beta (.) K K^T (.) Gamma) (fp32) and the decayed,
+      // masked Q K^T operand; lanes 0-63 hold K K^T rows, 64-127 Q K^T rows
+      {
+        const float* b = S.b[buf];
+        float v[32], bc[32];
+        const int c0 = 32 * half;
+        // the column decays, loaded before any store so none waits on one
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 b4 = *reinterpret_cast<const float4*>(b + c0 + 4 * i);
+          bc[4 * i] = b4.x;
+          bc[4 * i + 1] = b4.y;
+          bc[4 * i + 2] = b4.z;
+          bc[4 * i + 3] = b4.w;
+        }
+        umma::tmem_ld32(tlane + TM_KQ + 32 * half, v);
+        if (lrow < kC) {
+          const int r = lrow;
+          const float br = b[r], betar = S.gates[buf][1][r];
+          float av[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int cc = c0 + i;
+            av[i] = cc < r ? betar * v[i] * exp_ftz(br - bc[i]) : 0.f;
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4*>(Af + ix(r, c0 + 4 * q)) =
+                make_float4(av[4 * q], av[4 * q + 1], av[4 * q + 2], av[4 * q + 3]);
+        } else {
+          const int t = lrow - kC;
+          const float bt = b[t];
+          float m[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int cc = c0 + i;
+            m[i] = cc <= t ? v[i] * exp_ftz(bt - bc[i]) : 0.f;
+          }
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            const int cch = 4 * half + ch;
+            *reinterpret_cast<uint4*>(S.qk + (t >> 3) * 1024 + (t & 7) * 128 + ((cch ^ (t & 7)) << 4)) =
+                umma::pack8_bf16(m + 8 * ch);
+          }
+        }
+      }
+      // TM_KQ read: the issue warp may overwrite it with chunk c + 1's product
+      umma::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.ext_bar);
+      compute_sync();
+      // T = X diag(beta) and T' = X diag(beta e^b) as bf16 K-major tiles
+      solve_T(Af, Xf, Yf, TOut{S.tm, S.tp, S.gates[buf][1], eb});
+      umma::fence_proxy_async();
+      compute_sync();
+      // U^T = V^T T^T ; W^T = K^T T'^T
+      if (tid == 0) {
+        umma::fence_after();
+        const uint64_t dv = umma::desc(vv, 64 * 128, 1024), dkm = umma::desc(kq, 16384, 1024);
+        const uint64_t dtm = umma::desc(smem_addr(S.tm), 16, 1024), dtp = umma::desc(smem_addr(S.tp), 16, 1024);
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          umma::mma_bf16(tmem + TM_U, umma::adv(dv, s * 2048), umma::adv(dtm, s * 32), ID_64_MK, s > 0);
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          umma::mma_bf16(tmem + TM_W, umma::adv(dkm, s * 2048), umma::adv(dtp, s * 32), ID_64_MK, s > 0);
+        umma::commit(&S.mma_bar);
+      }
+      if (!(alive = cta_wait(&S.mma_bar, mph, bad))) break;
+      mph ^= 1;
+      umma::fence_after();
+      // W^T -> bf16 MN-major B tile (row = dk, 64 tokens)
+      {
+        float v[32];
+        umma::tmem_ld32(tlane + TM_W + 32 * half, v);
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          const int cch = 4 * half + ch;
+          *reinterpret_cast<uint4*>(S.wt + (lrow >> 3) * 1024 + (lrow & 7) * 128 +
+                                    ((cch ^ (lrow & 7)) << 4)) = umma::pack8_bf16(v + 8 * ch);
+        }
+      }
+      umma::fence_proxy_async();
+      umma::fence_before();
+      compute_sync();
+      // P = S^T W^T
+      if (tid == 0) {
+        umma::fence_after();
+        const uint64_t dst = umma::desc(st, 16, 1024), dwt = umma::desc(smem_addr(S.wt), 0, 1024);
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          const uint32_t ko = (s >> 2) * 16384 + (s & 3) * 32;
+          umma::mma_bf16(tmem + TM_P, umma::adv(dst, ko), umma::adv(dwt, s * 2048), ID_64_KM, s > 0);
+        }
+        umma::commit(&S.mma_bar);
+      }
+      if (!(alive = cta_wait(&S.mma_bar, mph, bad))) break;
+      mph ^= 1;
+      umma::fence_after();
+      // Delta^T = U^T - P, and its columns scaled by e^{b_last - b}
+      {
+        const float* ebl = S.ebl[buf];
+        float u[32], p[32], d[32], dd[32];
+        umma::tmem_ld32(tlane + TM_U + 32 * half, u);
+        umma::tmem_ld32(tlane + TM_P + 32 * half, p);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const int cc = c0 + i;
-          m[i] = cc <= t ? v[i] * exp_ftz(bt - bc[i]) : 0.f;
+          d[i] = u[i] - p[i];
+          dd[i] = d[i] * ebl[32 * half + i];
         }
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
           const int cch = 4 * half + ch;
-          *reinterpret_cast<uint4*>(S.qk + (t >> 3) * 1024 + (t & 7) * 128 + ((cch ^ (t & 7)) << 4)) =
-              umma::pack8_bf16(m + 8 * ch);
+          const uint32_t off = (lrow >> 3) * 1024 + (lrow & 7) * 128 + ((cch ^ (lrow & 7)) << 4);
+          *reinterpret_cast<uint4*>(S.dt + off) = umma::pack8_bf16(d + 8 * ch);
+          *reinterpret_cast<uint4*>(S.dtt + off) = umma::pack8_bf16(dd + 8 * ch);
+        }
+      }
+      umma::fence_proxy_async();
+      umma::fence_before();
+      compute_sync();
+      // D2 = Delta~^T K ; O2 = Delta^T (QK^T Gamma)^T ; chunk c + 1's decays
+      // (warp 4) meanwhile
+      if (tid == 0) {
+        umma::fence_after();
+        const uint64_t ddt = umma::desc(smem_addr(S.dt), 16, 1024), ddtt = umma::desc(smem_addr(S.dtt), 16, 1024);
+        const uint64_t dqk = umma::desc(smem_addr(S.qk), 16, 1024), dkm = umma::desc(kq, 16384, 1024);
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          umma::mma_bf16(tmem + TM_D2, umma::adv(ddtt, s * 32), umma::adv(dkm, s * 2048), ID_128_KM, s > 0);
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          umma::mma_bf16(tmem + TM_O2, umma::adv(ddt, s * 32), umma::adv(dqk, s * 32), ID_64_KK, s > 0);
+        umma::commit(&S.mma_bar);
+      } else if (warp == 4 && c + 1 < nch) {
+        if (__all_sync(0xffffffffu, mbar_wait(&S.ld_full[(c + 1) & 1], ((c + 1) >> 1) & 1)))
+          chunk_decays(c + 1);
+        else
+          bad = true;
+      }
+      if (!(alive = cta_wait(&S.mma_bar, mph, bad))) break;
+      mph ^= 1;
+      umma::fence_after();
+      // S^T <- e^{b_last} S^T + D2 ; O = O1 diag(e^b) + O2
+      {
+        const float dec = eb[kC - 1];
+        float d2[32];
+        umma::tmem_ld32(tlane + TM_D2 + 64 * half, d2);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sreg[i] = fmaf(dec, sreg[i], d2[i]);
+        umma::tmem_ld32(tlane + TM_D2 + 64 * half + 32, d2);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sreg[32 + i] = fmaf(dec, sreg[32 + i], d2[i]);
+        float o1[32], o2[32];
+        umma::tmem_ld32(tlane + TM_O1 + 32 * half, o1);
+        umma::tmem_ld32(tlane + TM_O2 + 32 * half, o2);
+        float ebr[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 e4 = *reinterpret_cast<const float4*>(eb + 32 * half + 4 * i);
+          ebr[4 * i] = e4.x;
+          ebr[4 * i + 1] = e4.y;
+          ebr[4 * i + 2] = e4.z;
+          ebr[4 * i + 3] = e4.w;
+        }
+        // stage O as [token][dv] in the (now free) W^T tile
+        Tact* ot = reinterpret_cast<Tact*>(S.wt);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) ot[(32 * half + i) * kD + lrow] = from_f32<Tact>(fmaf(o1[i], ebr[i], o2[i]));
+      }
+      umma::store_row64(S.st + half * (128 * 128), lrow, sreg);
+      // checkpoint at a block boundary
+      const int64_t pend = P + kC < p1 ? P + kC : p1;
+      if (pend % a.ckpt_block == 0) {
+        const int64_t idx = pend / a.ckpt_block - p0 / a.ckpt_block - 1;
+        if (idx >= 0 && idx < a.max_ckpt) {
+          const int32_t cid = a.ckpt_ids[(size_t)n * a.max_ckpt + idx];
+          if (slot_class(cid, a.ck_num_slots) == 0) {
+            float* cS = a.ck_ssm + (((size_t)cid * a.hv + h) * kD + lrow) * kD + 64 * half;
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              *reinterpret_cast<float4*>(cS + 4 * i) =
+                  make_float4(sreg[4 * i], sreg[4 * i + 1], sreg[4 * i + 2], sreg[4 * i + 3]);
+          }
+        }
+      }
+      // state image written, O1 read: the issue warp may start chunk c + 1's O1
+      umma::fence_proxy_async();
+      umma::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.st_bar);
+      compute_sync();
+      // output rows of the chunk's tokens: 16-byte stores of whole rows (the
+      // staging tile is next written after the following chunk's first barrier)
+      {
+        constexpr int EPC = 16 / sizeof(Tact), CPR = kD / EPC;
+        const Tact* ot = reinterpret_cast<const Tact*>(S.wt);
+        for (int e = tid; e < kC * CPR; e += kTh) {
+          const int r = e / CPR, ch = e % CPR;
+          const int64_t pos = P + r;
+          if (pos >= p0 && pos < p1)
+            *reinterpret_cast<uint4*>(out + ((t0 + pos - p0) * a.hv + h) * kD + ch * EPC) =
+                *reinterpret_cast<const uint4*>(ot + r * kD + ch * EPC);
         }
       }
     }
-    umma::fence_before();
-    __syncthreads();
-    // T = X diag(beta) and T' = X diag(beta e^b) as bf16 K-major tiles
-    solve_T(Af, Xf, Yf, TOut{S.tm, S.tp, S.gates[buf][1], eb});
-    umma::fence_proxy_async();
-    __syncthreads();
-    // U^T = V^T T^T ; W^T = K^T T'^T
-    if (tid == 0) {
-      umma::fence_after();
-      const uint64_t dv = umma::desc(vv, 64 * 128, 1024), dkm = umma::desc(kq, 16384, 1024);
-      const uint64_t dtm = umma::desc(smem_addr(S.tm), 16, 1024), dtp = umma::desc(smem_addr(S.tp), 16, 1024);
+    if (!alive) {
+      if (tid == 0) report(a.err, GDN_DEV_ERR_TIMEOUT);
+    } else {
 #pragma unroll
-      for (int s = 0; s < 4; ++s)
-        umma::mma_bf16(tmem + TM_U, umma::adv(dv, s * 2048), umma::adv(dtm, s * 32), ID_64_MK, s > 0);
-#pragma unroll
-      for (int s = 0; s < 4; ++s)
-        umma::mma_bf16(tmem + TM_W, umma::adv(dkm, s * 2048), umma::adv(dtp, s * 32), ID_64_MK, s > 0);
-      umma::commit(&S.mma_bar);
+      for (int i = 0; i < 16; ++i)
+        *reinterpret_cast<float4*>(gS + 4 * i) =
+            make_float4(sreg[4 * i], sreg[4 * i + 1], sreg[4 * i + 2], sreg[4 * i + 3]);
     }
-    if (!cta_wait(S, &S.mma_bar, mph)) break;
-    mph ^= 1;
-    umma::fence_after();
-    // W^T -> bf16 MN-major B tile (row = dk, 64 tokens)
-    {
-      float v[32];
-      umma::tmem_ld32(tlane + TM_W + 32 * half, v);
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        const int cch = 4 * half + ch;
-        *reinterpret_cast<uint4*>(S.wt + (lrow >> 3) * 1024 + (lrow & 7) * 128 +
-                                  ((cch ^ (lrow & 7)) << 4)) = umma::pack8_bf16(v + 8 * ch);
-      }
-    }
-    umma::fence_proxy_async();
-    umma::fence_before();
-    __syncthreads();
-    // P = S^T W^T
-    if (tid == 0) {
-      umma::fence_after();
-      const uint64_t dst = umma::desc(st, 16, 1024), dwt = umma::desc(smem_addr(S.wt), 0, 1024);
-#pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        const uint32_t ko = (s >> 2) * 16384 + (s & 3) * 32;
-        umma::mma_bf16(tmem + TM_P, umma::adv(dst, ko), umma::adv(dwt, s * 2048), ID_64_KM, s > 0);
-      }
-      umma::commit(&S.mma_bar);
-      // chunk c + 1's [K;Q] K^T runs on the tensor core during Delta below
-      if (c + 1 < nch) {
-        if (mbar_wait(&S.ld_full[(c + 1) & 1], ((c + 1) >> 1) & 1)) {
-          issue_kq(c + 1);
-          kq_issued = c + 2;
-        } else {
-          S.abort = 1;
-        }
-      }
-    }
-    if (!cta_wait(S, &S.mma_bar, mph)) break;
-    mph ^= 1;
-    umma::fence_after();
-    // Delta^T = U^T - P, and its columns scaled by e^{b_last - b}
-    {
-      const float* ebl = S.ebl[buf];
-      float u[32], p[32], d[32], dd[32];
-      umma::tmem_ld32(tlane + TM_U + 32 * half, u);
-      umma::tmem_ld32(tlane + TM_P + 32 * half, p);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        d[i] = u[i] - p[i];
-        dd[i] = d[i] * ebl[32 * half + i];
-      }
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        const int cch = 4 * half + ch;
-        const uint32_t off = (lrow >> 3) * 1024 + (lrow & 7) * 128 + ((cch ^ (lrow & 7)) << 4);
-        *reinterpret_cast<uint4*>(S.dt + off) = umma::pack8_bf16(d + 8 * ch);
-        *reinterpret_cast<uint4*>(S.dtt + off) = umma::pack8_bf16(dd + 8 * ch);
-      }
-    }
-    umma::fence_proxy_async();
-    umma::fence_before();
-    __syncthreads();
-    // D2 = Delta~^T K ; O2 = Delta^T (QK^T Gamma)^T ; chunk c + 1's decays
-    // (warp 4) meanwhile
-    if (tid == 0) {
-      umma::fence_after();
-      const uint64_t ddt = umma::desc(smem_addr(S.dt), 16, 1024), ddtt = umma::desc(smem_addr(S.dtt), 16, 1024);
-      const uint64_t dqk = umma::desc(smem_addr(S.qk), 16, 1024), dkm = umma::desc(kq, 16384, 1024);
-#pragma unroll
-      for (int s = 0; s < 4; ++s)
-        umma::mma_bf16(tmem + TM_D2, umma::adv(ddtt, s * 32), umma::adv(dkm, s * 2048), ID_128_KM, s > 0);
-#pragma unroll
-      for (int s = 0; s < 4; ++s)
-        umma::mma_bf16(tmem + TM_O2, umma::adv(ddt, s * 32), umma::adv(dqk, s * 32), ID_64_KK, s > 0);
-      umma::commit(&S.mma_bar);
-    } else if (warp == 4 && c + 1 < nch) {
-      if (__all_sync(0xffffffffu, mbar_wait(&S.ld_full[(c + 1) & 1], ((c + 1) >> 1) & 1)))
-        chunk_decays(c + 1);
-      else if (lane == 0)
-        S.abort = 1;
-    }
-    if (!cta_wait(S, &S.mma_bar, mph)) break;
-    mph ^= 1;
-    umma::fence_after();
-    // S^T <- e^{b_last} S^T + D2 ; O = O1 diag(e^b) + O2
-    {
-      const float dec = eb[kC - 1];
-      float d2[32];
-      umma::tmem_ld32(tlane + TM_D2 + 64 * half, d2);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) sreg[i] = fmaf(dec, sreg[i], d2[i]);
-      umma::tmem_ld32(tlane + TM_D2 + 64 * half + 32, d2);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) sreg[32 + i] = fmaf(dec, sreg[32 + i], d2[i]);
-      float o1[32], o2[32];
-      umma::tmem_ld32(tlane + TM_O1 + 32 * half, o1);
-      umma::tmem_ld32(tlane + TM_O2 + 32 * half, o2);
-      float ebr[32];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float4 e4 = *reinterpret_cast<const float4*>(eb + 32 * half + 4 * i);
-        ebr[4 * i] = e4.x;
-        ebr[4 * i + 1] = e4.y;
-        ebr[4 * i + 2] = e4.z;
-        ebr[4 * i + 3] = e4.w;
-      }
-      // stage O as [token][dv] in the (now free) W^T tile
-      Tact* ot = reinterpret_cast<Tact*>(S.wt);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) ot[(32 * half + i) * kD + lrow] = from_f32<Tact>(fmaf(o1[i], ebr[i], o2[i]));
-    }
-    umma::store_row64(S.st + half * (128 * 128), lrow, sreg);
-    // checkpoint at a block boundary
-    const int64_t pend = P + kC < p1 ? P + kC : p1;
-    if (pend % a.ckpt_block == 0) {
-      const int64_t idx = pend / a.ckpt_block - p0 / a.ckpt_block - 1;
-      if (idx >= 0 && idx < a.max_ckpt) {
-        const int32_t cid = a.ckpt_ids[(size_t)n * a.max_ckpt + idx];
-        if (slot_class(cid, a.ck_num_slots) == 0) {
-          float* cS = a.ck_ssm + (((size_t)cid * a.hv + h) * kD + lrow) * kD + 64 * half;
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            *reinterpret_cast<float4*>(cS + 4 * i) =
-                make_float4(sreg[4 * i], sreg[4 * i + 1], sreg[4 * i + 2], sreg[4 * i + 3]);
-        }
-      }
-    }
-    umma::fence_proxy_async();
-    umma::fence_before();
-    __syncthreads();
-    if (tid == 0 && c + 1 < nch && kq_issued == c + 2) {
-      umma::fence_after();
-      issue_o1_commit(c + 1);
-    }
-    // output rows of the chunk's tokens: 16-byte stores of whole rows (the
-    // staging tile is next written after the following chunk's first barrier)
-    {
-      constexpr int EPC = 16 / sizeof(Tact), CPR = kD / EPC;
-      const Tact* ot = reinterpret_cast<const Tact*>(S.wt);
-      for (int e = tid; e < kC * CPR; e += kTh) {
-        const int r = e / CPR, ch = e % CPR;
-        const int64_t pos = P + r;
-        if (pos >= p0 && pos < p1)
-          *reinterpret_cast<uint4*>(out + ((t0 + pos - p0) * a.hv + h) * kD + ch * EPC) =
-              *reinterpret_cast<const uint4*>(ot + r * kD + ch * EPC);
-      }
-    }
-  }
-  if (S.abort) {
-    if (tid == 0) {
-      report(a.err, GDN_DEV_ERR_TIMEOUT);
-      // let issued loads and the last [K;Q] K^T land before the shared memory
-      // and TMEM go away
-      for (int c = (issued > 2 ? issued - 2 : 0); c < issued; ++c) mbar_wait(&S.ld_full[c & 1], (c >> 1) & 1);
-      if (kq_issued > 0) mbar_wait(&S.kq_bar, (kq_issued - 1) & 1);
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-      *reinterpret_cast<float4*>(gS + 4 * i) =
-          make_float4(sreg[4 * i], sreg[4 * i + 1], sreg[4 * i + 2], sreg[4 * i + 3]);
   }
   umma::fence_before();
   __syncthreads();
@@ -977,7 +991,7 @@ static cudaError_t launch_tc_t(const TcArgs& a, cudaStream_t s) {
   const size_t csm = sizeof(ChainSmem) + 1024;
   if ((e = cudaFuncSetAttribute(ck, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csm)) != cudaSuccess)
     return e;
-  ck<<<dim3((unsigned)a.hv, (unsigned)a.n_seq), kTh, csm, s>>>(a);
+  ck<<<dim3((unsigned)a.hv, (unsigned)a.n_seq), kChainThreads, csm, s>>>(a);
   return cudaGetLastError();
 }
 
