@@ -43,9 +43,12 @@ constexpr uint32_t kKQBytes = 2 * 128 * 128;  // [K;Q] image: 2 blocks x 128 row
 constexpr uint32_t kVBytes = 2 * 64 * 128;    // V image: 2 atoms x 64 rows x 128 B
 constexpr uint32_t kGateBytes = 2 * kC * 4;   // g[64], beta[64]
 
-// TMEM columns
-constexpr uint32_t TM_KQ = 0, TM_U = 64, TM_W = 128, TM_P = 192, TM_O1 = 256, TM_O2 = 320,
+// TMEM columns.  [K;Q] K^T is double-buffered by chunk parity (TM_KQ + 192
+// for odd chunks, so the next chunk's product can run while this one is
+// read); P reuses W's columns (W is converted to bf16 before P is computed).
+constexpr uint32_t TM_KQ = 0, TM_U = 64, TM_W = 128, TM_P = 128, TM_KQ_ODD = 192, TM_O1 = 256, TM_O2 = 320,
                    TM_D2 = 384, TM_COLS = 512;
+__host__ __device__ constexpr uint32_t tm_kq(int c) { return (c & 1) ? TM_KQ_ODD : TM_KQ; }
 
 struct TcArgs {
   float* ssm;
@@ -328,7 +331,7 @@ struct __align__(1024) ChainSmem {
   float gates[2][2][kC];
   float b[2][kC], eb[2][kC], ebl[2][kC];  // by chunk parity
   uint64_t ld_full[2], mma_bar, kq_bar;
-  uint64_t ext_bar;  // compute warps finished reading [K;Q] K^T (one arrival per warp)
+  uint64_t p_bar;    // P of the current chunk complete (its [K;Q] K^T buffer long read)
   uint64_t st_bar;   // compute warps wrote the state image and read O1 (one arrival per warp)
   uint32_t tmem_base;
 };
@@ -581,7 +584,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) tc_chain_kernel(const TcArgs
     mbar_init(&S.ld_full[1], 1);
     mbar_init(&S.mma_bar, 1);
     mbar_init(&S.kq_bar, 1);
-    mbar_init(&S.ext_bar, kTh / 32);
+    mbar_init(&S.p_bar, 1);
     mbar_init(&S.st_bar, kTh / 32);
     fence_mbar_init();
   }
@@ -600,11 +603,11 @@ __global__ void __launch_bounds__(kChainThreads, 1) tc_chain_kernel(const TcArgs
   constexpr uint32_t ID_128_KM = umma::idesc_bf16(128, 128, false, true);
 
   if (warp == kIssueWarp) {
-    // Issue warp, one lane: operand loads one chunk ahead; for chunk c, [K;Q]
-    // K^T as soon as chunk c-1's extraction freed TM_KQ (it runs on the tensor
-    // core during chunk c-1's solve) and O1 = S^T Q^T once the state entering
-    // chunk c is in its image (it runs under chunk c-1's output stores); both
-    // complete on kq_bar.
+    // Issue warp, one lane: operand loads one chunk ahead; [K;Q] K^T of chunk
+    // c + 1 into its TMEM buffer once chunk c's P is done (it runs on the
+    // tensor core during chunk c's Delta, which uses no tensor core) and O1 =
+    // S^T Q^T of chunk c + 1 once the state leaving chunk c is in its image (it
+    // runs under chunk c's output stores); each chunk's pair completes on kq_bar.
     if (lane == 0 && nch > 0) {
       auto issue_load = [&](int c) {
         const int gc = gc0 + c, buf = c & 1;
@@ -613,23 +616,29 @@ __global__ void __launch_bounds__(kChainThreads, 1) tc_chain_kernel(const TcArgs
         bulk_g2s(S.v[buf], a.ws_v + ((size_t)gc * a.hv + h) * kVBytes, kVBytes, &S.ld_full[buf]);
         bulk_g2s(S.gates[buf], a.ws_gate + ((size_t)gc * a.hv + h) * (2 * kC), kGateBytes, &S.ld_full[buf]);
       };
-      int issued = 1, kq_issued = 0;
-      bool ok = true;
-      issue_load(0);
-      for (int c = 0; c < nch && ok; ++c) {
-        ok = mbar_wait(&S.ld_full[c & 1], (c >> 1) & 1) && (c == 0 || mbar_wait(&S.ext_bar, (c - 1) & 1));
-        if (!ok) break;
-        umma::fence_after();
+      auto issue_kq = [&](int c) {
         const uint64_t dkq = umma::desc(smem_addr(S.kq[c & 1]), 16, 1024);
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
           const uint32_t ko = (s >> 2) * 16384 + (s & 3) * 32;
-          umma::mma_bf16(tmem + TM_KQ, umma::adv(dkq, ko), umma::adv(dkq, ko), ID_64_KK, s > 0);
+          umma::mma_bf16(tmem + tm_kq(c), umma::adv(dkq, ko), umma::adv(dkq, ko), ID_64_KK, s > 0);
         }
+      };
+      int issued = 1, kq_issued = 0;
+      bool ok = true;
+      issue_load(0);
+      ok = mbar_wait(&S.ld_full[0], 0);
+      if (ok) {
+        umma::fence_after();
+        issue_kq(0);
+      }
+      for (int c = 0; c < nch && ok; ++c) {
+        // O1 of chunk c, after the state entering it reached its image
         ok = mbar_wait(&S.st_bar, c & 1);
         if (!ok) break;
         umma::fence_after();
-        const uint64_t dq = umma::adv(dkq, 8192), dst = umma::desc(smem_addr(S.st), 16, 1024);
+        const uint64_t dq = umma::desc(smem_addr(S.kq[c & 1]) + 8192, 16, 1024);
+        const uint64_t dst = umma::desc(smem_addr(S.st), 16, 1024);
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
           const uint32_t ko = (s >> 2) * 16384 + (s & 3) * 32;
@@ -637,18 +646,24 @@ __global__ void __launch_bounds__(kChainThreads, 1) tc_chain_kernel(const TcArgs
         }
         umma::commit(&S.kq_bar);
         kq_issued = c + 1;
+        if (c + 1 >= nch) break;
         // chunk c+1 into the buffer of chunk c-1, whose last reader (its state
         // update) finished before st_bar completed
-        if (c + 1 < nch) {
-          issue_load(c + 1);
-          issued = c + 2;
-        }
+        issue_load(c + 1);
+        issued = c + 2;
+        // [K;Q] K^T of chunk c + 1, after chunk c's P (its TMEM buffer was last
+        // read by chunk c - 1's extraction)
+        ok = mbar_wait(&S.p_bar, c & 1) && mbar_wait(&S.ld_full[(c + 1) & 1], ((c + 1) >> 1) & 1);
+        if (!ok) break;
+        umma::fence_after();
+        issue_kq(c + 1);
       }
       if (!ok) {
         report(a.err, GDN_DEV_ERR_TIMEOUT);
         // let issued loads and products land before shared memory and TMEM go away
         for (int c = (issued > 2 ? issued - 2 : 0); c < issued; ++c) mbar_wait(&S.ld_full[c & 1], (c >> 1) & 1);
-        if (kq_issued > 0) mbar_wait(&S.kq_bar, (kq_issued - 1) & 1);
+        umma::commit(&S.kq_bar);
+        mbar_wait(&S.kq_bar, kq_issued & 1);
       }
     }
     __syncwarp();
@@ -733,7 +748,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) tc_chain_kernel(const TcArgs
           bc[4 * i + 2] = b4.z;
           bc[4 * i + 3] = b4.w;
         }
-        umma::tmem_ld32(tlane + TM_KQ + 32 * half, v);
+        umma::tmem_ld32(tlane + tm_kq(c) + 32 * half, v);
         if (lrow < kC) {
           const int r = lrow;
           const float br = b[r], betar = S.gates[buf][1][r];
@@ -764,10 +779,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) tc_chain_kernel(const TcArgs
           }
         }
       }
-      // TM_KQ read: the issue warp may overwrite it with chunk c + 1's product
       umma::fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.ext_bar);
       compute_sync();
       // T = X diag(beta) and T' = X diag(beta e^b) as bf16 K-major tiles
       solve_T(Af, Xf, Yf, TOut{S.tm, S.tp, S.gates[buf][1], eb});
@@ -813,6 +825,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) tc_chain_kernel(const TcArgs
           umma::mma_bf16(tmem + TM_P, umma::adv(dst, ko), umma::adv(dwt, s * 2048), ID_64_KM, s > 0);
         }
         umma::commit(&S.mma_bar);
+        umma::commit(&S.p_bar);
       }
       if (!(alive = cta_wait(&S.mma_bar, mph, bad))) break;
       mph ^= 1;
