@@ -497,6 +497,11 @@ cudaError_t dispatch_dtype(bool verify, const StepArgs& a, int act, int cv, cuda
 // the batch is small, so that enough bytes are in flight to cover HBM latency.
 int choose_nit(int dk, int dv, int units, int G, bool verify) {
   if (dk == 16) return 1;
+  if (verify) {  // GDN_VERIFY_NIT=1|2|4 fixes the verify tile, for measurement
+    const char* e = std::getenv("GDN_VERIFY_NIT");
+    const int f = e ? std::atoi(e) : 0;
+    if (f == 1 || f == 2 || (f == 4 && dk == 128)) return f;
+  }
   const int ri = kWarps * (32 / (dk / 16));
   int nit = dk == 64 ? 2 : 4;
   const int target = verify ? 512 : 1024;  // CTAs wanted before the largest tile is used
@@ -511,15 +516,12 @@ int choose_nit(int dk, int dv, int units, int G, bool verify) {
 // layer, so it takes every shape it supports (dk 128, width 4, G*dv <= 256);
 // verify keeps the per-head kernel (below).  GDN_DECODE_PATH=rows forces the
 // per-head decode, GDN_DECODE_PATH=tma the persistent verify, for measurement.
-int forced_path() {
-  static int forced = [] {
-    const char* e = std::getenv("GDN_DECODE_PATH");
-    if (!e) return 0;
-    if (!std::strcmp(e, "tma")) return 1;
-    if (!std::strcmp(e, "rows")) return 2;
-    return 0;
-  }();
-  return forced;
+int forced_path() {  // read on every call, so a process can time both paths
+  const char* e = std::getenv("GDN_DECODE_PATH");
+  if (!e) return 0;
+  if (!std::strcmp(e, "tma")) return 1;
+  if (!std::strcmp(e, "rows")) return 2;
+  return 0;
 }
 
 bool use_tma_decode(const gdn_dims& d, int32_t B, const void* qkv, const gdn_params& p) {
@@ -528,12 +530,17 @@ bool use_tma_decode(const gdn_dims& d, int32_t B, const void* qkv, const gdn_par
   return forced_path() != 2;
 }
 
-// The persistent verify kernel is not yet faster than the per-head one (batch
-// 16, T = 8: 0.57 vs 0.67 of HBM peak; its per-item prologue repeats the q/k
-// conv for every row block), so it runs only when asked for.
-bool use_tma_verify(const gdn_dims& d, int32_t T, const void* qkv, const gdn_params& p) {
+// Verify: the persistent TMA-fed kernel from 6 (request, V head) items per
+// SM up (Qwen3.5-shaped layer, T = 8: 0.74 / 0.83 / 0.89 of HBM at batch
+// 32 / 64 / 128 against 0.70 / 0.73 / 0.74 for the per-head kernel); below
+// that its per-item prologue (the q/k conv of every row block) is not hidden
+// and the per-head kernel is faster (batch 16: 0.72 against 0.57).
+// GDN_DECODE_PATH=tma / rows forces either, for measurement.
+bool use_tma_verify(const gdn_dims& d, int32_t B, int32_t T, const void* qkv, const gdn_params& p) {
   if (!verify_tma_supported(d, T, qkv, p)) return false;
-  return forced_path() == 1;
+  const int f = forced_path();
+  if (f) return f == 1;
+  return (long)B * d.hv >= 6L * sm_count();
 }
 
 gdn_status run_step(bool verify, const gdn_dims* dims, const gdn_pool& work, const gdn_pool* spec,
@@ -558,7 +565,7 @@ gdn_status run_step(bool verify, const gdn_dims* dims, const gdn_pool& work, con
     if (e == cudaSuccess) count_launch(GDN_K_DECODE);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
   }
-  if (verify && use_tma_verify(*dims, T, qkv, *params)) {
+  if (verify && use_tma_verify(*dims, B, T, qkv, *params)) {
     cudaError_t e = verify_tma_launch(*dims, work, *spec, *params, slot_ids, spec_ids, B, T, qkv, a,
                                       b, out, dev_err, cs);
     if (e == cudaSuccess) count_launch(GDN_K_SPEC_VERIFY);

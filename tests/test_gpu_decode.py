@@ -65,6 +65,22 @@ def test_qwen_one_step(cuda, B):
     assert torch.equal(st.pool.ssm[untouched], before)
 
 
+@pytest.mark.parametrize("B", [3, 64])
+def test_qwen_one_step_per_head_kernel(cuda, monkeypatch, B):
+    """The per-head decode kernel at the Qwen3.5 shape (the TMA-fed kernel
+    takes this shape by default; GDN_DECODE_PATH=rows selects the other)."""
+    monkeypatch.setenv("GDN_DECODE_PATH", "rows")
+    st = Setup(synth.QWEN, seed=11, num_slots=80)
+    ids = synth.slot_ids(80, B, st.gen)
+    n0 = gdn.launch_count(gdn.K_DECODE)
+    qkv, a, b = st.tokens((B,))
+    out, o_ref, err = _step(st, ids, qkv, a, b)
+    assert err == 0
+    assert gdn.launch_count(gdn.K_DECODE) == n0 + 1
+    assert_out_close(out, o_ref, 128, out_tol(st.shape))
+    _check_state(st, ids.tolist(), STATE_TOL_1)
+
+
 @pytest.mark.parametrize("B", [8, 32])
 def test_qwen_64_steps(cuda, B):
     st = Setup(synth.QWEN, seed=2, num_slots=40)

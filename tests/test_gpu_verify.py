@@ -21,16 +21,26 @@ def _spec_pool(st: Setup, n):
     return s
 
 
-@pytest.mark.parametrize("shape,B,T", [
-    (synth.TINY, 2, 5),
-    (synth.QWEN, 16, 8),
-    (synth.QWEN, 3, 4),
-    (synth.QWEN, 24, 16),
-    (synth.QWEN.replace(act="f32", conv="f32", hk=4, hv=8), 5, 6),
-    (synth.QWEN.replace(hk=2, hv=8, dk=64, dv=64), 3, 3),
-], ids=["tiny", "qwen_b16_t8", "qwen_b3_t4", "qwen_b24_t16", "f32_b5_t6", "dk64_g4"])
-def test_verify_then_commit(cuda, shape, B, T):
-    n_work = 8 if shape is synth.TINY else 40
+@pytest.mark.parametrize("shape,B,T,path", [
+    (synth.TINY, 2, 5, None),
+    (synth.QWEN, 16, 8, None),
+    (synth.QWEN, 16, 8, "tma"),
+    (synth.QWEN, 32, 8, None),
+    (synth.QWEN, 32, 8, "rows"),
+    (synth.QWEN, 3, 4, "tma"),
+    (synth.QWEN, 24, 16, None),
+    (synth.QWEN, 24, 16, "tma"),
+    (synth.QWEN.replace(act="f32", conv="f32", hk=4, hv=8), 5, 6, None),
+    (synth.QWEN.replace(hk=2, hv=8, dk=64, dv=64), 3, 3, None),
+], ids=["tiny", "qwen_b16_t8", "qwen_b16_t8_persistent", "qwen_b32_t8", "qwen_b32_t8_per_head",
+        "qwen_b3_t4_persistent", "qwen_b24_t16", "qwen_b24_t16_persistent", "f32_b5_t6", "dk64_g4"])
+def test_verify_then_commit(cuda, monkeypatch, shape, B, T, path):
+    """path: None = the library's own choice (per-head kernel below six
+    (request, V head) items per SM, the persistent TMA-fed kernel above);
+    "tma" / "rows" force one (GDN_DECODE_PATH, read on every call)."""
+    if path:
+        monkeypatch.setenv("GDN_DECODE_PATH", path)
+    n_work = 8 if shape is synth.TINY else 48
     st = Setup(shape, seed=30, num_slots=n_work)
     ids = synth.slot_ids(n_work, B, st.gen)
     spec = _spec_pool(st, B * T + 3)
