@@ -363,6 +363,27 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
 
 
+def _graph_time(f, n_steps, n_replays, dev):
+    """ms per step of n_steps calls of f captured in one CUDA graph (None if
+    the capture is refused)."""
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n_steps):
+                f(i)
+        g.replay()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n_replays):
+            g.replay()
+        e1.record()
+        e1.synchronize()
+        return e0.elapsed_time(e1) / (n_steps * n_replays)
+    except RuntimeError:
+        return None
+
+
 def measure_rows(gdn, synth, dev, stream, hbm_peak, bf16_peak, which="all", prefill_len=8192):
     """Every other row of the hot path, timed with CUDA events (not headline).
     which = "prefill" times only the chunked prefill (for profiling)."""
@@ -400,6 +421,9 @@ def measure_rows(gdn, synth, dev, stream, hbm_peak, bf16_peak, which="all", pref
         ms = _events_time(f, reps, stream)
         r = frac(B * DECODE_TOKEN_BYTES + DECODE_STEP_PARAM_BYTES, ms)
         r["tokens_per_s"] = B / (ms * 1e-3)
+        # the same steps replayed from a CUDA graph: the GPU-side time per step
+        # without the per-call host cost (what a graph-captured serving loop sees)
+        r["ms_graph"] = _graph_time(f, 20, 10, dev)
         sweep[str(B)] = r
     rows["decode_sweep"] = sweep
 

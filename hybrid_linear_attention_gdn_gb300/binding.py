@@ -142,8 +142,13 @@ class Dims:
         return 2 * self.hk * self.dk + self.hv * self.dv
 
     def c(self) -> CDims:
-        return CDims(self.hk, self.hv, self.dk, self.dv, self.conv_width,
-                     _DT_CODE[self.act_dtype], _DT_CODE[self.conv_dtype])
+        key = (self.hk, self.hv, self.dk, self.dv, self.conv_width, self.act_dtype, self.conv_dtype)
+        cached = self.__dict__.get("_c")
+        if cached is None or cached[0] != key:
+            cached = (key, CDims(self.hk, self.hv, self.dk, self.dv, self.conv_width,
+                                 _DT_CODE[self.act_dtype], _DT_CODE[self.conv_dtype]))
+            self.__dict__["_c"] = cached
+        return cached[1]
 
 
 @dataclass
@@ -158,7 +163,12 @@ class StatePool:
         return self.ssm.shape[0]
 
     def c(self) -> CPool:
-        return CPool(self.ssm.data_ptr(), self.conv.data_ptr(), self.num_slots)
+        key = (self.ssm.data_ptr(), self.conv.data_ptr(), self.ssm.shape[0])
+        cached = self.__dict__.get("_c")
+        if cached is None or cached[0] != key:
+            cached = (key, CPool(*key))
+            self.__dict__["_c"] = cached
+        return cached[1]
 
     @staticmethod
     def empty(dims: Dims, num_slots: int, device="cuda") -> "StatePool":
@@ -175,7 +185,12 @@ class LayerParams:
     dt_bias: torch.Tensor  # [HV] fp32
 
     def c(self) -> CParams:
-        return CParams(self.conv_w.data_ptr(), self.A_log.data_ptr(), self.dt_bias.data_ptr())
+        key = (self.conv_w.data_ptr(), self.A_log.data_ptr(), self.dt_bias.data_ptr())
+        cached = self.__dict__.get("_c")
+        if cached is None or cached[0] != key:
+            cached = (key, CParams(*key))
+            self.__dict__["_c"] = cached
+        return cached[1]
 
 
 # ---------------------------------------------------------------- entry points
