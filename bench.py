@@ -366,6 +366,7 @@ def run_ours(args):
 def _graph_time(f, n_steps, n_replays, dev):
     """ms per step of n_steps calls of f captured in one CUDA graph (None if
     the capture is refused)."""
+    import torch
     try:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):

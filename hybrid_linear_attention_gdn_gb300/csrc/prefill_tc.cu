@@ -31,7 +31,6 @@
 //   The conv histories of checkpoints and of the final state come from the
 //   history kernel of prefill.cu.
 #include "gdn_common.cuh"
-#include "decode_tma.cuh"  // sm_count()
 #include "umma.cuh"
 
 namespace gdn {
@@ -155,11 +154,8 @@ __device__ __forceinline__ int seq_of_chunk(const int32_t* base, int n_seq, int 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-// all but the most recent committed group are complete
-__device__ __forceinline__ void cp_async_wait_one() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all_groups() {
-  asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
 }
 __device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8]) {
   const uint4 u = *reinterpret_cast<const uint4*>(p);
@@ -205,158 +201,112 @@ __device__ __forceinline__ void conv_walk8(const Tact* xs, int nch, int r0, int 
   }
 }
 
-// One work item of the features kernel: (chunk gc, QK head hq).
-struct FeatItem {
-  bool valid;
-  int gc, hq;
-  int64_t t0, p0, p1, P;  // sequence start token, first / end positions, chunk row 0
-  int32_t slot;
-};
-
-__device__ __forceinline__ FeatItem feat_item(const TcArgs& a, int it, int n_items) {
-  FeatItem f;
-  f.valid = false;
-  if (it >= n_items) return f;
-  f.gc = it / a.hk;
-  f.hq = it % a.hk;
-  const int n = seq_of_chunk(a.chunk_base, a.n_seq, f.gc);
-  int64_t len;
-  if (!seq_ok(a, n, f.t0, len, f.p0)) return f;
-  f.slot = a.slot_ids[n];
-  if (slot_class(f.slot, a.num_slots)) return f;
-  f.p1 = f.p0 + len;
-  f.P = (f.p0 / kC + (f.gc - a.chunk_base[n])) * kC;
-  f.valid = true;
-  return f;
-}
-
-// Persistent: CTA b takes items b, b + grid, ...  Its tile is split in a q/k
-// half and a v half; each half is refilled with the next item's rows (one
-// cp.async group) as soon as it has been consumed, so the loads of one half
-// overlap the compute on the other.
 template <typename Tact, typename Tconv>
 __global__ void __launch_bounds__(kTh, 3) tc_features_kernel(const TcArgs a) {
   extern __shared__ __align__(16) unsigned char fsm[];
+  const int gc = blockIdx.x, hq = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n_items = a.chunk_base[a.n_seq] * a.hk;
+  if (gc >= a.chunk_base[a.n_seq]) return;
+  const int n = seq_of_chunk(a.chunk_base, a.n_seq, gc);
+  int64_t t0, len, p0;
+  if (!seq_ok(a, n, t0, len, p0)) return;
+  const int32_t slot = a.slot_ids[n];
+  if (slot_class(slot, a.num_slots)) return;
+  const int64_t P = (p0 / kC + (gc - a.chunk_base[n])) * kC;  // absolute position of row 0
+  const int64_t p1 = p0 + len;
   const int GD = a.G * kD;
-  Tact* xqk = reinterpret_cast<Tact*>(fsm);   // [kC + 3][2 kD], row i = position P - 3 + i
-  Tact* xv = xqk + (size_t)(kC + 3) * 2 * kD;  // [kC + 3][G kD]
+  const int nch = 2 * kD + GD;               // local channels: q | k | v of the G heads
+  Tact* xs = reinterpret_cast<Tact*>(fsm);   // [kC + 3][nch], row i = position P - 3 + i
   const Tact* qkv = reinterpret_cast<const Tact*>(a.qkv);
-  constexpr int EPC = 16 / sizeof(Tact);       // elements per 16-byte piece
-
-  // global channel of q/k-half channel lc (q: 0..kD-1, k: kD..2kD-1) / v-half channel lc
-  auto qk_chan = [&](const FeatItem& f, int lc) -> size_t {
-    return lc < kD ? (size_t)f.hq * kD + lc : (size_t)a.hk * kD + (size_t)f.hq * kD + (lc - kD);
+  const Tconv* hist = reinterpret_cast<const Tconv*>(a.conv) + (size_t)slot * 3 * a.C;
+  auto gchan = [&](int lc) -> size_t {  // global channel of local channel lc
+    if (lc < kD) return (size_t)hq * kD + lc;
+    if (lc < 2 * kD) return (size_t)a.hk * kD + (size_t)hq * kD + (lc - kD);
+    return 2 * (size_t)a.hk * kD + (size_t)hq * GD + (lc - 2 * kD);
   };
-  auto v_chan = [&](const FeatItem& f, int lc) -> size_t {
-    return 2 * (size_t)a.hk * kD + (size_t)f.hq * GD + lc;
-  };
-  // stage one half of item f's tile (rows before the sequence from the conv
-  // history, rows past it zero); always commits one cp.async group
-  auto stage = [&](const FeatItem& f, bool v_half) {
-    if (f.valid) {
-      const int nch = v_half ? GD : 2 * kD, cpr = nch / EPC;
-      Tact* xs = v_half ? xv : xqk;
-      const Tconv* hist = reinterpret_cast<const Tconv*>(a.conv) + (size_t)f.slot * 3 * a.C;
-      for (int e = tid; e < (kC + 3) * cpr; e += kTh) {
-        const int i = e / cpr, pc = e % cpr;
-        const int64_t pos = f.P - 3 + i;
-        Tact* dst = xs + (size_t)i * nch + pc * EPC;
-        const size_t c = v_half ? v_chan(f, pc * EPC) : qk_chan(f, pc * EPC);
-        if (pos >= f.p0 && pos < f.p1) {
-          cp_async16(dst, qkv + (size_t)(f.t0 + pos - f.p0) * a.C + c);
-        } else if (pos < f.p0 && pos >= f.p0 - 3) {
-          const Tconv* src = hist + (size_t)(3 - (f.p0 - pos)) * a.C + c;
+  constexpr int EPC = 16 / sizeof(Tact);     // elements per 16-byte piece
+  const int cpr = nch / EPC;                 // pieces per tile row
+  for (int e = tid; e < (kC + 3) * cpr; e += kTh) {
+    const int i = e / cpr, pc = e % cpr;
+    const int64_t pos = P - 3 + i;
+    Tact* dst = xs + (size_t)i * nch + pc * EPC;
+    const size_t c = gchan(pc * EPC);
+    if (pos >= p0 && pos < p1) {
+      cp_async16(dst, qkv + (size_t)(t0 + pos - p0) * a.C + c);
+    } else if (pos < p0 && pos >= p0 - 3) {
+      const Tconv* src = hist + (size_t)(3 - (p0 - pos)) * a.C + c;
 #pragma unroll
-          for (int k = 0; k < EPC; ++k) dst[k] = from_f32<Tact>(to_f32(src[k]));
-        } else {
+      for (int k = 0; k < EPC; ++k) dst[k] = from_f32<Tact>(to_f32(src[k]));
+    } else {
 #pragma unroll
-          for (int k = 0; k < EPC; ++k) dst[k] = from_f32<Tact>(0.f);
-        }
-      }
+      for (int k = 0; k < EPC; ++k) dst[k] = from_f32<Tact>(0.f);
     }
-    cp_async_commit();
-  };
+  }
+  // gates (rows outside the sequence: g = beta = 0)
+  for (int e = tid; e < kC * a.G; e += kTh) {
+    const int r = e % kC, gi = e / kC;
+    const int h = hq * a.G + gi;
+    const int64_t pos = P + r;
+    float gv = 0.f, bv = 0.f;
+    if (pos >= p0 && pos < p1) {
+      const size_t tok = (size_t)(t0 + pos - p0);
+      const float av = to_f32(reinterpret_cast<const Tact*>(a.a)[tok * a.hv + h]);
+      const float bb = to_f32(reinterpret_cast<const Tact*>(a.b)[tok * a.hv + h]);
+      gv = -expf(a.A_log[h]) * softplus_f(av + a.dt_bias[h]);
+      bv = sigmoid_f(bb);
+    }
+    float* gt = a.ws_gate + ((size_t)gc * a.hv + h) * (2 * kC);
+    gt[r] = gv;
+    gt[kC + r] = bv;
+  }
+  cp_async_wait_all();
+  __syncthreads();
 
-  int it = blockIdx.x;
-  FeatItem cur = feat_item(a, it, n_items);
-  stage(cur, false);
-  stage(cur, true);
-  for (; it < n_items; it += gridDim.x) {
-    const FeatItem nxt = feat_item(a, it + (int)gridDim.x, n_items);
-    // q and k: warp w walks rows 8w .. 8w+7; lane l < 16 is q channels
-    // 8l .. 8l+7, lane 16 + l the same k channels
-    cp_async_wait_one();
-    __syncthreads();
-    if (cur.valid) {
-      const int lc = 8 * lane;
+  // q and k: warp w walks rows 8w .. 8w+7; lane l < 16 is q channels 8l .. 8l+7,
+  // lane 16 + l the same k channels
+  {
+    const int lc = 8 * lane;  // local channel (q: 0..127, k: 128..255)
+    float w[8][4];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const float4 w4 = *reinterpret_cast<const float4*>(a.conv_w + gchan(lc + c) * 4);
+      w[c][0] = w4.x; w[c][1] = w4.y; w[c][2] = w4.z; w[c][3] = w4.w;
+    }
+    const bool isq = lane < 16;
+    const float qscale = isq ? rsqrtf((float)kD) : 1.f;
+    uint8_t* kq = a.ws_kq + ((size_t)gc * a.hk + hq) * kKQBytes;
+    conv_walk8(xs, nch, 8 * warp, lc, w, P, p0, p1, [&](int r, float (&y)[8]) {
+      float ss = 0.f;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) ss = fmaf(y[c], y[c], ss);
+#pragma unroll
+      for (int o = 8; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      const float sc = rsqrtf(ss + kNormEps) * qscale;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) y[c] *= sc;
+      const int R = isq ? kC + r : r;  // image rows: k^ 0..63, q^ 64..127
+      *reinterpret_cast<uint4*>(kq + umma::sw128_off(R, 8 * (lane & 15), 128 * 128)) = umma::pack8_bf16(y);
+    });
+  }
+  // v: (8-channel group, 8-row block) items, G*16 groups per row
+  {
+    const int gpr = a.G * (kD / 8);
+    for (int e = tid; e < 8 * gpr; e += kTh) {
+      const int ch = e % gpr, rb = e / gpr;
+      const int lc = 2 * kD + 8 * ch;
       float w[8][4];
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        const float4 w4 = *reinterpret_cast<const float4*>(a.conv_w + qk_chan(cur, lc + c) * 4);
+        const float4 w4 = *reinterpret_cast<const float4*>(a.conv_w + gchan(lc + c) * 4);
         w[c][0] = w4.x; w[c][1] = w4.y; w[c][2] = w4.z; w[c][3] = w4.w;
       }
-      const bool isq = lane < 16;
-      const float qscale = isq ? rsqrtf((float)kD) : 1.f;
-      uint8_t* kq = a.ws_kq + ((size_t)cur.gc * a.hk + cur.hq) * kKQBytes;
-      conv_walk8(xqk, 2 * kD, 8 * warp, lc, w, cur.P, cur.p0, cur.p1, [&](int r, float (&y)[8]) {
-        float ss = 0.f;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) ss = fmaf(y[c], y[c], ss);
-#pragma unroll
-        for (int o = 8; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        const float sc = rsqrtf(ss + kNormEps) * qscale;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) y[c] *= sc;
-        const int R = isq ? kC + r : r;  // image rows: k^ 0..63, q^ 64..127
-        *reinterpret_cast<uint4*>(kq + umma::sw128_off(R, 8 * (lane & 15), 128 * 128)) = umma::pack8_bf16(y);
+      const int h = hq * a.G + ch / (kD / 8), d = 8 * (ch % (kD / 8));
+      uint8_t* vimg = a.ws_v + ((size_t)gc * a.hv + h) * kVBytes;
+      conv_walk8(xs, nch, 8 * rb, lc, w, P, p0, p1, [&](int r, float (&y)[8]) {
+        *reinterpret_cast<uint4*>(vimg + umma::sw128_off(r, d, 64 * 128)) = umma::pack8_bf16(y);
       });
     }
-    __syncthreads();
-    stage(nxt, false);
-    // v: (8-channel group, 8-row block) items, G*16 groups per row; gates
-    cp_async_wait_one();
-    __syncthreads();
-    if (cur.valid) {
-      const int gpr = a.G * (kD / 8);
-      for (int e = tid; e < 8 * gpr; e += kTh) {
-        const int ch = e % gpr, rb = e / gpr;
-        float w[8][4];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const float4 w4 = *reinterpret_cast<const float4*>(a.conv_w + v_chan(cur, 8 * ch + c) * 4);
-          w[c][0] = w4.x; w[c][1] = w4.y; w[c][2] = w4.z; w[c][3] = w4.w;
-        }
-        const int h = cur.hq * a.G + ch / (kD / 8), d = 8 * (ch % (kD / 8));
-        uint8_t* vimg = a.ws_v + ((size_t)cur.gc * a.hv + h) * kVBytes;
-        conv_walk8(xv, GD, 8 * rb, 8 * ch, w, cur.P, cur.p0, cur.p1, [&](int r, float (&y)[8]) {
-          *reinterpret_cast<uint4*>(vimg + umma::sw128_off(r, d, 64 * 128)) = umma::pack8_bf16(y);
-        });
-      }
-      // gates (rows outside the sequence: g = beta = 0)
-      for (int e = tid; e < kC * a.G; e += kTh) {
-        const int r = e % kC, gi = e / kC;
-        const int h = cur.hq * a.G + gi;
-        const int64_t pos = cur.P + r;
-        float gv = 0.f, bv = 0.f;
-        if (pos >= cur.p0 && pos < cur.p1) {
-          const size_t tok = (size_t)(cur.t0 + pos - cur.p0);
-          const float av = to_f32(reinterpret_cast<const Tact*>(a.a)[tok * a.hv + h]);
-          const float bb = to_f32(reinterpret_cast<const Tact*>(a.b)[tok * a.hv + h]);
-          gv = -expf(a.A_log[h]) * softplus_f(av + a.dt_bias[h]);
-          bv = sigmoid_f(bb);
-        }
-        float* gt = a.ws_gate + ((size_t)cur.gc * a.hv + h) * (2 * kC);
-        gt[r] = gv;
-        gt[kC + r] = bv;
-      }
-    }
-    __syncthreads();
-    stage(nxt, true);
-    cur = nxt;
   }
-  cp_async_wait_all_groups();
 }
 
 // ---------------------------------------------------------------------------
@@ -1048,8 +998,7 @@ static cudaError_t launch_tc_t(const TcArgs& a, cudaStream_t s) {
   const size_t fsm = (size_t)(kC + 3) * (2 * kD + a.G * kD) * sizeof(Tact);
   if ((e = cudaFuncSetAttribute(fk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsm)) != cudaSuccess)
     return e;
-  const long items = (long)a.n_chunks_max * a.hk, slots = 3L * sm_count();
-  fk<<<(unsigned)(items < slots ? items : slots), kTh, fsm, s>>>(a);
+  fk<<<dim3((unsigned)a.n_chunks_max, (unsigned)a.hk), kTh, fsm, s>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   auto ck = tc_chain_kernel<Tact>;
   const size_t csm = sizeof(ChainSmem) + 1024;
