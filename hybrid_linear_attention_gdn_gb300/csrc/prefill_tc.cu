@@ -14,23 +14,20 @@
 //               g and beta per V head (fp32; rows outside the sequence get
 //               zero features and g = beta = 0, which makes every chunk a
 //               full 64-row chunk without changing the result).
-//   chain:    one CTA per (sequence, V head) walks its chunks in order: 8
-//             compute warps and 1 issue warp.  The fp32 state S^T (dv x dk)
-//             lives in registers (one dv row per TMEM lane, 64 columns per
-//             thread); a bf16 copy in shared memory is the MMA operand.  Per
-//             chunk (transposed so that M = 128 throughout):
+//   chain:    one CTA per (sequence, V head) walks its chunks in order.  The
+//             fp32 state S^T (dv x dk) lives in registers (one dv row per TMEM
+//             lane, 64 columns per thread); a bf16 copy in shared memory is the
+//             MMA operand.  Per chunk (transposed so that M = 128 throughout):
 //               [K;Q] K^T             -> K K^T (A), Q K^T (masked, decayed)
-//               T = (I + A)^-1 diag(beta)   (fp32 / tf32, CUDA cores, blocked)
+//               T = (I + A)^-1 diag(beta)   (fp32, CUDA cores, blocked)
 //               U^T = V^T T^T,  W^T = K^T (T diag(e^b))^T
 //               P = S^T W^T,  O1 = S^T Q^T
 //               Delta^T = U^T - P
 //               D2 = (Delta^T diag(e^{b_last - b})) K,  O2 = Delta^T (QK^T (.) Gamma)^T
 //               S^T <- e^{b_last} S^T + D2,  O = O1 diag(e^b) + O2
 //             Every product is one tcgen05.mma chain (bf16 in, fp32 TMEM
-//             accumulators; 40 MMA instructions per chunk) completed through
-//             tcgen05.commit -> mbarrier.  The issue warp loads the operands
-//             and issues the two products that do not depend on the running
-//             state ([K;Q] K^T, O1) a phase ahead; thread 0 issues the rest.
+//             accumulators; 7 groups, 40 MMA instructions per chunk), issued
+//             by one thread and completed through tcgen05.commit -> mbarrier.
 //   The conv histories of checkpoints and of the final state come from the
 //   history kernel of prefill.cu.
 #include "gdn_common.cuh"
@@ -160,57 +157,45 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
 }
-// 8 consecutive channels as 4 fp32 pairs
-__device__ __forceinline__ void load8(const __nv_bfloat16* p, float2 (&v)[4]) {
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8]) {
   const uint4 u = *reinterpret_cast<const uint4*>(p);
   const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) v[i] = __bfloat1622float2(h[i]);
-}
-__device__ __forceinline__ void load8(const float* p, float2 (&v)[4]) {
-  const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
-  v[0] = make_float2(a.x, a.y); v[1] = make_float2(a.z, a.w);
-  v[2] = make_float2(b.x, b.y); v[3] = make_float2(b.z, b.w);
-}
-// conv weights of channels c, c+1 (pair p of an 8-channel group) per tap
-__device__ __forceinline__ void load_w8(const float* conv_w, size_t c0, float2 (&w)[4][4]) {
-#pragma unroll
-  for (int p = 0; p < 4; ++p) {
-    const float4 a = *reinterpret_cast<const float4*>(conv_w + (c0 + 2 * p) * 4);
-    const float4 b = *reinterpret_cast<const float4*>(conv_w + (c0 + 2 * p + 1) * 4);
-    w[p][0] = make_float2(a.x, b.x); w[p][1] = make_float2(a.y, b.y);
-    w[p][2] = make_float2(a.z, b.z); w[p][3] = make_float2(a.w, b.w);
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(h[i]);
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
   }
+}
+__device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
 // conv1d (width 4) + SiLU of 8 channels walking 8 rows r0 .. r0+7 (tile rows
-// r .. r+3 = positions P+r-3 .. P+r); zero outside the sequence.  Channel
-// pairs use the packed fp32 instructions; the SiLU uses the fast exponential
-// and reciprocal, far finer than the bf16 operands they feed.  emit(r, y)
-// receives each row's 8 results as 4 pairs.
+// r .. r+3 = positions P+r-3 .. P+r); zero outside the sequence.  The fast
+// exponential and division are far finer than the bf16 operands they feed.
+// emit(r, y) receives each row's 8 results.
 template <typename Tact, class Emit>
-__device__ __forceinline__ void conv_walk8(const Tact* xs, int nch, int r0, int lc, const float2 (&w)[4][4],
+__device__ __forceinline__ void conv_walk8(const Tact* xs, int nch, int r0, int lc, const float (&w)[8][4],
                                            int64_t P, int64_t p0, int64_t p1, Emit emit) {
-  const float2 nl2e = make_float2(-1.4426950408889634f, -1.4426950408889634f), one = make_float2(1.f, 1.f);
-  float2 x[4][4];
+  float x[4][8];
 #pragma unroll
   for (int j = 0; j < 3; ++j) load8(xs + (size_t)(r0 + j) * nch + lc, x[j]);
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     const int r = r0 + k;
     load8(xs + (size_t)(r + 3) * nch + lc, x[(k + 3) & 3]);
-    const float m = (P + r >= p0 && P + r < p1) ? 1.f : 0.f;
-    float2 y[4];
+    const bool valid = P + r >= p0 && P + r < p1;
+    float y[8];
 #pragma unroll
-    for (int p = 0; p < 4; ++p) {
-      float2 acc = mul2(w[p][0], x[k & 3][p]);
-      acc = fma2(w[p][1], x[(k + 1) & 3][p], acc);
-      acc = fma2(w[p][2], x[(k + 2) & 3][p], acc);
-      acc = fma2(w[p][3], x[(k + 3) & 3][p], acc);
-      const float2 z = mul2(acc, nl2e);
-      const float2 den = add2(make_float2(ex2_ftz(z.x), ex2_ftz(z.y)), one);
-      const float2 inv = make_float2(__fdividef(m, den.x), __fdividef(m, den.y));
-      y[p] = mul2(acc, inv);
+    for (int c = 0; c < 8; ++c) {
+      float acc = w[c][0] * x[k & 3][c];
+      acc = fmaf(w[c][1], x[(k + 1) & 3][c], acc);
+      acc = fmaf(w[c][2], x[(k + 2) & 3][c], acc);
+      acc = fmaf(w[c][3], x[(k + 3) & 3][c], acc);
+      y[c] = valid ? __fdividef(acc, 1.f + exp_ftz(-acc)) : 0.f;
     }
     emit(r, y);
   }
@@ -241,12 +226,8 @@ __global__ void __launch_bounds__(kTh, 3) tc_features_kernel(const TcArgs a) {
   };
   constexpr int EPC = 16 / sizeof(Tact);     // elements per 16-byte piece
   const int cpr = nch / EPC;                 // pieces per tile row
-  // a thread keeps one piece column when the row's pieces divide the CTA
-  const bool fixed_col = kTh % cpr == 0;
-  const int rstep = fixed_col ? kTh / cpr : 0;
   for (int e = tid; e < (kC + 3) * cpr; e += kTh) {
-    const int i = fixed_col ? tid / cpr + (e - tid) / kTh * rstep : e / cpr;
-    const int pc = fixed_col ? tid % cpr : e % cpr;
+    const int i = e / cpr, pc = e % cpr;
     const int64_t pos = P - 3 + i;
     Tact* dst = xs + (size_t)i * nch + pc * EPC;
     const size_t c = gchan(pc * EPC);
@@ -285,24 +266,26 @@ __global__ void __launch_bounds__(kTh, 3) tc_features_kernel(const TcArgs a) {
   // lane 16 + l the same k channels
   {
     const int lc = 8 * lane;  // local channel (q: 0..127, k: 128..255)
-    float2 w[4][4];
-    load_w8(a.conv_w, gchan(lc), w);
+    float w[8][4];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const float4 w4 = *reinterpret_cast<const float4*>(a.conv_w + gchan(lc + c) * 4);
+      w[c][0] = w4.x; w[c][1] = w4.y; w[c][2] = w4.z; w[c][3] = w4.w;
+    }
     const bool isq = lane < 16;
     const float qscale = isq ? rsqrtf((float)kD) : 1.f;
     uint8_t* kq = a.ws_kq + ((size_t)gc * a.hk + hq) * kKQBytes;
-    conv_walk8(xs, nch, 8 * warp, lc, w, P, p0, p1, [&](int r, float2 (&y)[4]) {
-      float2 s2 = mul2(y[0], y[0]);
+    conv_walk8(xs, nch, 8 * warp, lc, w, P, p0, p1, [&](int r, float (&y)[8]) {
+      float ss = 0.f;
 #pragma unroll
-      for (int p = 1; p < 4; ++p) s2 = fma2(y[p], y[p], s2);
-      float ss = s2.x + s2.y;
+      for (int c = 0; c < 8; ++c) ss = fmaf(y[c], y[c], ss);
 #pragma unroll
       for (int o = 8; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
       const float sc = rsqrtf(ss + kNormEps) * qscale;
 #pragma unroll
-      for (int p = 0; p < 4; ++p) y[p] = mul2(y[p], make_float2(sc, sc));
+      for (int c = 0; c < 8; ++c) y[c] *= sc;
       const int R = isq ? kC + r : r;  // image rows: k^ 0..63, q^ 64..127
-      *reinterpret_cast<uint4*>(kq + umma::sw128_off(R, 8 * (lane & 15), 128 * 128)) =
-          umma::pack8_bf16(reinterpret_cast<const float*>(y));
+      *reinterpret_cast<uint4*>(kq + umma::sw128_off(R, 8 * (lane & 15), 128 * 128)) = umma::pack8_bf16(y);
     });
   }
   // v: (8-channel group, 8-row block) items, G*16 groups per row
@@ -311,13 +294,16 @@ __global__ void __launch_bounds__(kTh, 3) tc_features_kernel(const TcArgs a) {
     for (int e = tid; e < 8 * gpr; e += kTh) {
       const int ch = e % gpr, rb = e / gpr;
       const int lc = 2 * kD + 8 * ch;
-      float2 w[4][4];
-      load_w8(a.conv_w, gchan(lc), w);
+      float w[8][4];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const float4 w4 = *reinterpret_cast<const float4*>(a.conv_w + gchan(lc + c) * 4);
+        w[c][0] = w4.x; w[c][1] = w4.y; w[c][2] = w4.z; w[c][3] = w4.w;
+      }
       const int h = hq * a.G + ch / (kD / 8), d = 8 * (ch % (kD / 8));
       uint8_t* vimg = a.ws_v + ((size_t)gc * a.hv + h) * kVBytes;
-      conv_walk8(xs, nch, 8 * rb, lc, w, P, p0, p1, [&](int r, float2 (&y)[4]) {
-        *reinterpret_cast<uint4*>(vimg + umma::sw128_off(r, d, 64 * 128)) =
-            umma::pack8_bf16(reinterpret_cast<const float*>(y));
+      conv_walk8(xs, nch, 8 * rb, lc, w, P, p0, p1, [&](int r, float (&y)[8]) {
+        *reinterpret_cast<uint4*>(vimg + umma::sw128_off(r, d, 64 * 128)) = umma::pack8_bf16(y);
       });
     }
   }
