@@ -226,12 +226,8 @@ __global__ void __launch_bounds__(kTh, 3) tc_features_kernel(const TcArgs a) {
   };
   constexpr int EPC = 16 / sizeof(Tact);     // elements per 16-byte piece
   const int cpr = nch / EPC;                 // pieces per tile row
-  // a thread keeps one piece column when the row's pieces divide the CTA
-  const bool fixed_col = kTh % cpr == 0;
-  const int rstep = fixed_col ? kTh / cpr : 0;
   for (int e = tid; e < (kC + 3) * cpr; e += kTh) {
-    const int i = fixed_col ? tid / cpr + (e - tid) / kTh * rstep : e / cpr;
-    const int pc = fixed_col ? tid % cpr : e % cpr;
+    const int i = e / cpr, pc = e % cpr;
     const int64_t pos = P - 3 + i;
     Tact* dst = xs + (size_t)i * nch + pc * EPC;
     const size_t c = gchan(pc * EPC);
