@@ -316,25 +316,22 @@ cudaError_t launch_tma(const TmaArgs& a, cudaStream_t s) {
 
 // One CTA per SM with a 10-stage ring, or two per SM with 4 stages each (one
 // CTA's item prologue then overlaps the other's state stream).  Measured on
-// the Qwen3.5-shaped layer: two per SM is better below ~4 items per SM (batch
-// 16: 0.63 vs 0.60 of HBM peak; batch 32: 0.73 vs 0.70), one per SM above
-// (batch 64: 0.85 vs 0.80; batch 256: 0.95 vs 0.91).
+// the Qwen3.5-shaped layer: two per SM is better below ~6 items per SM (batch
+// 32: 0.76 vs 0.71 of HBM peak; batch 48: 0.82 vs 0.80), one per SM above
+// (batch 64: 0.88 vs 0.83; batch 128: 0.93 vs 0.89).
 template <typename Tact, typename Tconv>
 cudaError_t launch_tma_dt(const TmaArgs& a, cudaStream_t s) {
   const int forced = tma_ctas_per_sm();
-  const bool two = forced ? forced == 2 : a.n_items < 4 * sm_count();
+  const bool two = forced ? forced == 2 : a.n_items < 6 * sm_count();
   if (two) return launch_tma<Tact, Tconv, 4, 2>(a, s);
   return launch_tma<Tact, Tconv, 10, 1>(a, s);
 }
 
 }  // namespace
 
-int tma_ctas_per_sm() {
-  static int v = [] {
-    const char* e = std::getenv("GDN_TMA_CTAS");
-    return (e && e[0] == '2') ? 2 : (e && e[0] == '1') ? 1 : 0;
-  }();
-  return v;
+int tma_ctas_per_sm() {  // read on every call, so a process can time both
+  const char* e = std::getenv("GDN_TMA_CTAS");
+  return (e && e[0] == '2') ? 2 : (e && e[0] == '1') ? 1 : 0;
 }
 
 int sm_count() {
