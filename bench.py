@@ -48,8 +48,8 @@ DECODE_STEP_PARAM_BYTES = 8192 * 4 * 4 + 2 * 32 * 4
 # the sha256 of the kernel source it was captured on; reported only while the
 # source is unchanged.
 DECODE_TRAFFIC = {
-    "bytes_per_launch": 138588416 + 77827840,
-    "source_sha256": "8e4c63a6274e8f0f529099a64a468eba2bf04cf52ca8a89c0f955e07e7fd031f",
+    "bytes_per_launch": 138589184 + 77341952,
+    "source_sha256": "0c1aaa9438733a9ed461bbc4522ff39328a263560b78c6926f79a5104bd375d6",
     "case": "batch 64 over a 128-slot pool (same requests per launch as the headline), one launch after "
             "5 warm-up launches; written bytes fall short of the 138 MB of state written because part "
             "of it is still dirty in L2 when the kernel ends",
