@@ -328,7 +328,6 @@ struct __align__(1024) ChainSmem {
   uint8_t tm[64 * 128];       // T (K-major B: 64 rows x 64)
   uint8_t tp[64 * 128];       // T diag(e^b)
   uint8_t qk[64 * 128];       // QK^T (.) Gamma (.) lower-incl
-  uint8_t ob[64 * 128 * 2];   // bf16 O of the previous chunk, [token][dv], stored during the next one
   float gates[2][2][kC];
   float b[2][kC], eb[2][kC], ebl[2][kC];  // by chunk parity
   uint64_t ld_full[2], mma_bar, kq_bar;
@@ -695,21 +694,6 @@ __global__ void __launch_bounds__(kChainThreads, 1) tc_chain_kernel(const TcArgs
     float* Af = S.ax[0];
     float* Xf = S.ax[1];
     float* Yf = reinterpret_cast<float*>(S.wt);
-    // bf16 outputs are staged in S.ob and written during the next chunk's U/W
-    // products (the compute warps only wait there); fp32 ones, too large for
-    // the spare shared memory, go out at the end of their own chunk from S.wt
-    constexpr bool kDeferOut = sizeof(Tact) == 2;
-    Tact* const ostage = reinterpret_cast<Tact*>(kDeferOut ? S.ob : S.wt);
-    auto store_rows = [&](int64_t Pc) {  // chunk whose row 0 sits at position Pc
-      constexpr int EPC = 16 / sizeof(Tact), CPR = kD / EPC;
-      for (int e = tid; e < kC * CPR; e += kTh) {
-        const int r = e / CPR, ch = e % CPR;
-        const int64_t pos = Pc + r;
-        if (pos >= p0 && pos < p1)
-          *reinterpret_cast<uint4*>(out + ((t0 + pos - p0) * a.hv + h) * kD + ch * EPC) =
-              *reinterpret_cast<const uint4*>(ostage + r * kD + ch * EPC);
-      }
-    };
 
     // one warp, gates of chunk c resident: cumulative log-decay b, e^b, e^{b_last - b}
     auto chunk_decays = [&](int c) {
@@ -814,8 +798,6 @@ __global__ void __launch_bounds__(kChainThreads, 1) tc_chain_kernel(const TcArgs
           umma::mma_bf16(tmem + TM_W, umma::adv(dkm, s * 2048), umma::adv(dtp, s * 32), ID_64_MK, s > 0);
         umma::commit(&S.mma_bar);
       }
-      // the previous chunk's staged output rows, while the products run
-      if (kDeferOut && c > 0) store_rows(P - kC);
       if (!(alive = cta_wait(&S.mma_bar, mph, bad))) break;
       mph ^= 1;
       umma::fence_after();
@@ -914,10 +896,10 @@ __global__ void __launch_bounds__(kChainThreads, 1) tc_chain_kernel(const TcArgs
           ebr[4 * i + 2] = e4.z;
           ebr[4 * i + 3] = e4.w;
         }
-        // stage O as [token][dv]
+        // stage O as [token][dv] in the (now free) W^T tile
+        Tact* ot = reinterpret_cast<Tact*>(S.wt);
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          ostage[(32 * half + i) * kD + lrow] = from_f32<Tact>(fmaf(o1[i], ebr[i], o2[i]));
+        for (int i = 0; i < 32; ++i) ot[(32 * half + i) * kD + lrow] = from_f32<Tact>(fmaf(o1[i], ebr[i], o2[i]));
       }
       umma::store_row64(S.st + half * (128 * 128), lrow, sreg);
       // checkpoint at a block boundary
@@ -941,14 +923,19 @@ __global__ void __launch_bounds__(kChainThreads, 1) tc_chain_kernel(const TcArgs
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.st_bar);
       compute_sync();
-      // fp32 output rows of the chunk (the staging tile is next written after
-      // the following chunk's first barrier)
-      if (!kDeferOut) store_rows(P);
-    }
-    // the last chunk's staged bf16 rows
-    if (kDeferOut && alive && nch > 0) {
-      compute_sync();
-      store_rows((p0 / kC + nch - 1) * kC);
+      // output rows of the chunk's tokens: 16-byte stores of whole rows (the
+      // staging tile is next written after the following chunk's first barrier)
+      {
+        constexpr int EPC = 16 / sizeof(Tact), CPR = kD / EPC;
+        const Tact* ot = reinterpret_cast<const Tact*>(S.wt);
+        for (int e = tid; e < kC * CPR; e += kTh) {
+          const int r = e / CPR, ch = e % CPR;
+          const int64_t pos = P + r;
+          if (pos >= p0 && pos < p1)
+            *reinterpret_cast<uint4*>(out + ((t0 + pos - p0) * a.hv + h) * kD + ch * EPC) =
+                *reinterpret_cast<const uint4*>(ot + r * kD + ch * EPC);
+        }
+      }
     }
     if (!alive) {
       if (tid == 0) report(a.err, GDN_DEV_ERR_TIMEOUT);
