@@ -511,11 +511,10 @@ int choose_nit(int dk, int dv, int units, int G, bool verify) {
   return nit;
 }
 
-// Kernel choice.  The persistent TMA-fed decode kernel is at least as fast as
-// the per-head kernel at every batch measured (1..256) on the Qwen3.5-shaped
-// layer, so it takes every shape it supports (dk 128, width 4, G*dv <= 256);
-// verify keeps the per-head kernel (below).  GDN_DECODE_PATH=rows forces the
-// per-head decode, GDN_DECODE_PATH=tma the persistent verify, for measurement.
+// Kernel choice between the persistent TMA-fed kernels (dk 128, width 4;
+// decode also G*dv <= 256) and the per-head kernels, by batch (below).
+// GDN_DECODE_PATH=rows / tma forces either for decode and verify, for
+// measurement.
 int forced_path() {  // read on every call, so a process can time both paths
   const char* e = std::getenv("GDN_DECODE_PATH");
   if (!e) return 0;
@@ -524,10 +523,16 @@ int forced_path() {  // read on every call, so a process can time both paths
   return 0;
 }
 
+// Decode: the persistent TMA-fed kernel from a quarter of an item (request x
+// QK head) per SM up; below that its few CTAs each stream a whole 128 KiB
+// group and the per-head kernel, which spreads a request's rows over more
+// CTAs, is faster (GPU time per step, Qwen3.5-shaped layer: batch 1: 4.4 us vs
+// 6.9; batch 2: 4.8 vs 7.0; batch 4: 8.9 vs 7.3).
 bool use_tma_decode(const gdn_dims& d, int32_t B, const void* qkv, const gdn_params& p) {
-  (void)B;
   if (!decode_tma_supported(d, qkv, p)) return false;
-  return forced_path() != 2;
+  const int f = forced_path();
+  if (f) return f != 2;
+  return 4L * B * d.hk > sm_count();
 }
 
 // Verify: the persistent TMA-fed kernel from 6 (request, V head) items per

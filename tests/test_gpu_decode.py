@@ -65,11 +65,11 @@ def test_qwen_one_step(cuda, B):
     assert torch.equal(st.pool.ssm[untouched], before)
 
 
-@pytest.mark.parametrize("B", [3, 64])
-def test_qwen_one_step_per_head_kernel(cuda, monkeypatch, B):
-    """The per-head decode kernel at the Qwen3.5 shape (the TMA-fed kernel
-    takes this shape by default; GDN_DECODE_PATH=rows selects the other)."""
-    monkeypatch.setenv("GDN_DECODE_PATH", "rows")
+@pytest.mark.parametrize("path,B", [("rows", 3), ("rows", 64), ("tma", 1), ("tma", 2)])
+def test_qwen_one_step_forced_kernel(cuda, monkeypatch, path, B):
+    """Each decode kernel at the Qwen3.5 shape where the library would pick
+    the other (per-head below a quarter item per SM, TMA-fed above)."""
+    monkeypatch.setenv("GDN_DECODE_PATH", path)
     st = Setup(synth.QWEN, seed=11, num_slots=80)
     ids = synth.slot_ids(80, B, st.gen)
     n0 = gdn.launch_count(gdn.K_DECODE)
