@@ -28,11 +28,6 @@ gdn_status check_pool(const gdn_dims& d, const gdn_pool& p) {
   return GDN_OK;
 }
 
-gdn_status launch_status() {
-  cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
-}
-
 }  // namespace gdn
 
 extern "C" const char* gdn_status_string(int32_t s) {

@@ -136,6 +136,8 @@ __device__ __forceinline__ void block_norms(const float* sq, const float* sk, fl
 // ---------------------------------------------------------------------------
 template <int DK, int NIT, typename Tact, typename Tconv>
 __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const StepArgs a) {
+  pdl_wait();
+  pdl_trigger();
   using M = RowMap<DK>;
   constexpr int R = NIT * M::RI;
   __shared__ float sq[DK], sk[DK], sv[R], so[R];
@@ -283,6 +285,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const StepArgs a) {
 // ---------------------------------------------------------------------------
 template <int DK, int NIT, typename Tact, typename Tconv>
 __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const StepArgs a) {
+  pdl_wait();
+  pdl_trigger();
   using M = RowMap<DK>;
   constexpr int R = NIT * M::RI;
   constexpr int NCH = 2 * DK + R;  // channels handled: q, k, our v rows
@@ -450,22 +454,10 @@ __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const StepArgs a) {
 // ---------------------------------------------------------------------------
 template <int DK, int NIT, typename Tact, typename Tconv>
 cudaError_t launch_decode_t(const StepArgs& a, cudaStream_t s) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(a.hv * a.P), (unsigned)a.B);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  cfg.attrs = attr;
-  cfg.numAttrs = 0;
-  if (a.G * a.P > 1) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)(a.G * a.P);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.numAttrs = 1;
-  }
-  return cudaLaunchKernelEx(&cfg, decode_kernel<DK, NIT, Tact, Tconv>, a);
+  // the G*P CTAs of a QK head form one cluster (shared q/k history writer)
+  const dim3 cluster(a.G * a.P > 1 ? (unsigned)(a.G * a.P) : 1u);
+  return launch_pdl(decode_kernel<DK, NIT, Tact, Tconv>, dim3((unsigned)(a.hv * a.P), (unsigned)a.B),
+                    dim3(kThreads), 0, s, cluster, a);
 }
 
 template <int DK, int NIT, typename Tact, typename Tconv>
@@ -477,8 +469,7 @@ cudaError_t launch_verify_t(const StepArgs& a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  k<<<dim3((unsigned)(a.hv * a.P), (unsigned)a.B), kThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k, dim3((unsigned)(a.hv * a.P), (unsigned)a.B), dim3(kThreads), smem, s, dim3(1), a);
 }
 
 template <int DK, int NIT>

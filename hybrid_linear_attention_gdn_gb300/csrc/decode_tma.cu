@@ -100,6 +100,10 @@ __global__ void __launch_bounds__(kThr, MINB) decode_tma_kernel(const TmaArgs a)
     fence_mbar_init();
   }
   __syncthreads();
+  // programmatic dependent launch: everything above touches only this CTA's
+  // shared memory
+  pdl_wait();
+  pdl_trigger();
 
   if (warp == kCW) {
     // ------------------------------------------------------------ producer
@@ -310,8 +314,7 @@ cudaError_t launch_tma(const TmaArgs& a, cudaStream_t s) {
   }
   const int slots = sm_count() * MINB;
   const int grid = a.n_items < slots ? a.n_items : slots;
-  k<<<grid, kThr, sizeof(SM), s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k, dim3((unsigned)grid), dim3(kThr), sizeof(SM), s, dim3(1), a);
 }
 
 // One CTA per SM with a 10-stage ring, or two per SM with 4 stages each (one

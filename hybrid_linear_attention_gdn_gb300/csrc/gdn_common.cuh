@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <utility>
 
 #include "gdn.h"
 
@@ -104,6 +105,16 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "l"(src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
 }
+// Programmatic dependent launch.  Every kernel of this library is launched
+// with launch_pdl: it may be scheduled while the previous kernel in the stream
+// finishes, and calls pdl_wait() before its first access to global memory
+// (the wait returns once every earlier grid in the stream has completed and its
+// writes are visible), then pdl_trigger() so that the next kernel can in turn
+// be scheduled early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
 // barrier over a subset of warps that also ORs `v` over its threads: every
 // participant gets the same result
 __device__ __forceinline__ bool named_sync_or(int id, int nthreads, bool v) {
@@ -151,6 +162,31 @@ inline int64_t channels(const gdn_dims& d) {
   return 2 * (int64_t)d.hk * d.dk + (int64_t)d.hv * d.dv;
 }
 inline size_t dtype_size(int32_t t) { return t == GDN_BF16 ? 2 : 4; }
+
+// launch k<<<grid, block, smem, s>>>(args...) as a programmatic dependent of
+// the previous work in the stream (optionally as clusters of `cluster` CTAs)
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       dim3 cluster, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.numAttrs = 1;
+  if (cluster.x * cluster.y * cluster.z > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster.x;
+    attr[1].val.clusterDim.y = cluster.y;
+    attr[1].val.clusterDim.z = cluster.z;
+    cfg.numAttrs = 2;
+  }
+  cfg.attrs = attr;
+  return cudaLaunchKernelEx(&cfg, k, std::forward<Args>(args)...);
+}
 inline size_t ssm_slot_bytes(const gdn_dims& d) {
   return (size_t)d.hv * d.dv * d.dk * sizeof(float);
 }
@@ -162,6 +198,5 @@ inline size_t conv_slot_bytes(const gdn_dims& d) {
 gdn_status check_dims(const gdn_dims* d);
 gdn_status check_pool(const gdn_dims& d, const gdn_pool& p);
 inline bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
-gdn_status launch_status();
 
 }  // namespace gdn

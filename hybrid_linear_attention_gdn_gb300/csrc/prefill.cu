@@ -85,6 +85,8 @@ __device__ __forceinline__ int seq_of_token(const int32_t* cu, int n_seq, int64_
 // ---------------------------------------------------------------------------
 template <int DK, typename Tact, typename Tconv>
 __global__ void __launch_bounds__(kThreads) features_kernel(const PrefillArgs a) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float sq[DK], sk[DK];
   __shared__ float sred[2][kWarps];
   __shared__ float sr[2];
@@ -181,6 +183,8 @@ struct ChunkSmem {
 
 template <int DK, int DVT, typename Tact>
 __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const PrefillArgs a) {
+  pdl_wait();
+  pdl_trigger();
   using L = ChunkSmem<DK, DVT>;
   extern __shared__ float sm[];
   float* St = sm;
@@ -369,6 +373,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const PrefillArgs a)
 // ---------------------------------------------------------------------------
 template <typename Tact, typename Tconv>
 __global__ void __launch_bounds__(kThreads) history_kernel(const PrefillArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int n = blockIdx.y, grp = blockIdx.z;
   const int c = blockIdx.x * kThreads + threadIdx.x;
   if (c >= a.C) return;
@@ -449,8 +455,8 @@ WsLayout ws_layout(const gdn_dims& d, int64_t total) {
 template <int DK, int DVT, typename Tact, typename Tconv>
 cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t s) {
   if (a.total > 0) {
-    features_kernel<DK, Tact, Tconv><<<dim3((unsigned)a.total, (unsigned)a.hk), kThreads, 0, s>>>(a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(features_kernel<DK, Tact, Tconv>, dim3((unsigned)a.total, (unsigned)a.hk),
+                               dim3(kThreads), 0, s, dim3(1), a);
     if (e != cudaSuccess) return e;
   }
   using L = ChunkSmem<DK, DVT>;
@@ -458,10 +464,9 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(ck, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::bytes);
   if (e != cudaSuccess) return e;
   const int n_tiles = (a.dv + DVT - 1) / DVT;
-  ck<<<dim3((unsigned)(a.hv * n_tiles), (unsigned)a.n_seq), kThreads, L::bytes, s>>>(a);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  history_kernel<Tact, Tconv><<<history_grid(a), kThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  e = launch_pdl(ck, dim3((unsigned)(a.hv * n_tiles), (unsigned)a.n_seq), dim3(kThreads), L::bytes, s, dim3(1), a);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(history_kernel<Tact, Tconv>, history_grid(a), dim3(kThreads), 0, s, dim3(1), a);
 }
 
 template <int DK, int DVT>
@@ -475,12 +480,10 @@ cudaError_t dispatch_prefill(const PrefillArgs& a, int act, int cv, cudaStream_t
 cudaError_t launch_history(const PrefillArgs& a, int act, int cv, cudaStream_t s) {
   const dim3 grid = history_grid(a);
   if (act == GDN_F32 && cv == GDN_F32)
-    history_kernel<float, float><<<grid, kThreads, 0, s>>>(a);
-  else if (act == GDN_BF16 && cv == GDN_BF16)
-    history_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, kThreads, 0, s>>>(a);
-  else
-    history_kernel<__nv_bfloat16, float><<<grid, kThreads, 0, s>>>(a);
-  return cudaGetLastError();
+    return launch_pdl(history_kernel<float, float>, grid, dim3(kThreads), 0, s, dim3(1), a);
+  if (act == GDN_BF16 && cv == GDN_BF16)
+    return launch_pdl(history_kernel<__nv_bfloat16, __nv_bfloat16>, grid, dim3(kThreads), 0, s, dim3(1), a);
+  return launch_pdl(history_kernel<__nv_bfloat16, float>, grid, dim3(kThreads), 0, s, dim3(1), a);
 }
 
 // The tensor-core path takes dk = dv = 128, width 4; GDN_PREFILL_PATH=cuda

@@ -96,6 +96,8 @@ __device__ __forceinline__ int n_chunks_of(int64_t p0, int64_t len) {
 // plan: chunk_base[n] = chunks of sequences 0..n-1 (one CTA, 1024 threads)
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) plan_kernel(const TcArgs a) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int warp_sums[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int per = (a.n_seq + 1023) / 1024;
@@ -203,6 +205,8 @@ __device__ __forceinline__ void conv_walk8(const Tact* xs, int nch, int r0, int 
 
 template <typename Tact, typename Tconv>
 __global__ void __launch_bounds__(kTh, 3) tc_features_kernel(const TcArgs a) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(16) unsigned char fsm[];
   const int gc = blockIdx.x, hq = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -555,6 +559,8 @@ __device__ __forceinline__ void solve_T(const float* A, float* X, float* Y, cons
 
 template <typename Tact>
 __global__ void __launch_bounds__(kChainThreads, 1) tc_chain_kernel(const TcArgs a) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // the swizzled operand tiles need 1024-byte aligned bases
   ChainSmem& S = *reinterpret_cast<ChainSmem*>(
@@ -991,21 +997,19 @@ size_t prefill_tc_workspace(const gdn_dims& d, int32_t n_seq, int64_t total) {
 
 template <typename Tact, typename Tconv>
 static cudaError_t launch_tc_t(const TcArgs& a, cudaStream_t s) {
-  plan_kernel<<<1, 1024, 0, s>>>(a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, s, dim3(1), a);
   if (e != cudaSuccess) return e;
   auto fk = tc_features_kernel<Tact, Tconv>;
   const size_t fsm = (size_t)(kC + 3) * (2 * kD + a.G * kD) * sizeof(Tact);
   if ((e = cudaFuncSetAttribute(fk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsm)) != cudaSuccess)
     return e;
-  fk<<<dim3((unsigned)a.n_chunks_max, (unsigned)a.hk), kTh, fsm, s>>>(a);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  e = launch_pdl(fk, dim3((unsigned)a.n_chunks_max, (unsigned)a.hk), dim3(kTh), fsm, s, dim3(1), a);
+  if (e != cudaSuccess) return e;
   auto ck = tc_chain_kernel<Tact>;
   const size_t csm = sizeof(ChainSmem) + 1024;
   if ((e = cudaFuncSetAttribute(ck, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csm)) != cudaSuccess)
     return e;
-  ck<<<dim3((unsigned)a.hv, (unsigned)a.n_seq), kChainThreads, csm, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(ck, dim3((unsigned)a.hv, (unsigned)a.n_seq), dim3(kChainThreads), csm, s, dim3(1), a);
 }
 
 cudaError_t prefill_tc_launch(const gdn_dims& d, const gdn_pool& pool, const gdn_pool& ckpt,

@@ -39,6 +39,8 @@ struct SlotOpArgs {
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads) slot_op_kernel(SlotOpArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const bool leader = blockIdx.x == 0 && threadIdx.x == 0;
   const size_t total = a.ssm_bytes + a.conv_bytes;
   for (int32_t r = blockIdx.y; r < a.n; r += gridDim.y) {
@@ -119,17 +121,18 @@ gdn_status launch_slot_op(int mode, const gdn_dims* dims, const gdn_pool* src,
   const size_t pieces = (a.ssm_bytes + a.conv_bytes + kPiece - 1) / kPiece;
   dim3 grid((unsigned)pieces, (unsigned)(n < 65535 ? n : 65535));
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
   if (mode == MODE_COPY) {
-    slot_op_kernel<MODE_COPY><<<grid, kThreads, 0, s>>>(a);
+    e = launch_pdl(slot_op_kernel<MODE_COPY>, dim3(grid), dim3(kThreads), 0, s, dim3(1), a);
     count_launch(GDN_K_SLOT_COPY);
   } else if (mode == MODE_ZERO) {
-    slot_op_kernel<MODE_ZERO><<<grid, kThreads, 0, s>>>(a);
+    e = launch_pdl(slot_op_kernel<MODE_ZERO>, dim3(grid), dim3(kThreads), 0, s, dim3(1), a);
     count_launch(GDN_K_SLOT_ZERO);
   } else {
-    slot_op_kernel<MODE_COMMIT><<<grid, kThreads, 0, s>>>(a);
+    e = launch_pdl(slot_op_kernel<MODE_COMMIT>, dim3(grid), dim3(kThreads), 0, s, dim3(1), a);
     count_launch(GDN_K_SPEC_COMMIT);
   }
-  return launch_status();
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
 }  // namespace

@@ -83,6 +83,8 @@ struct VArgs {
 
 template <typename Tact, typename Tconv, int STAGES, int MT, int MINB>
 __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
+  pdl_wait();
+  pdl_trigger();
   using SM = VSmem<Tact, Tconv, STAGES, MT>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   SM& S = *reinterpret_cast<SM*>(smem_raw);
@@ -328,8 +330,7 @@ cudaError_t launch_v(const VArgs& a, cudaStream_t s) {
   }
   const int slots = sm_count() * MINB;
   const int grid = a.n_items < slots ? a.n_items : slots;
-  k<<<grid, kThr, sizeof(SM), s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k, dim3((unsigned)grid), dim3(kThr), sizeof(SM), s, dim3(1), a);
 }
 
 template <typename Tact, typename Tconv>
