@@ -48,8 +48,8 @@ DECODE_STEP_PARAM_BYTES = 8192 * 4 * 4 + 2 * 32 * 4
 # the sha256 of the kernel source it was captured on; reported only while the
 # source is unchanged.
 DECODE_TRAFFIC = {
-    "bytes_per_launch": 138589184 + 77341952,
-    "source_sha256": "0c1aaa9438733a9ed461bbc4522ff39328a263560b78c6926f79a5104bd375d6",
+    "bytes_per_launch": 138589952 + 77269760,
+    "source_sha256": "2e9d5e5e7003eb310806993e46828ac6483cb1133ee1968b0190ff19a570d534",
     "case": "batch 64 over a 128-slot pool (same requests per launch as the headline), one launch after "
             "5 warm-up launches; written bytes fall short of the 138 MB of state written because part "
             "of it is still dirty in L2 when the kernel ends",

@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <cstdlib>
 #include <utility>
 
 #include "gdn.h"
@@ -105,12 +106,12 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "l"(src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
 }
-// Programmatic dependent launch.  Every kernel of this library is launched
-// with launch_pdl: it may be scheduled while the previous kernel in the stream
-// finishes, and calls pdl_wait() before its first access to global memory
-// (the wait returns once every earlier grid in the stream has completed and its
-// writes are visible), then pdl_trigger() so that the next kernel can in turn
-// be scheduled early.
+// Programmatic dependent launch.  A kernel launched with launch_pdl may be
+// scheduled while the previous kernel in the stream finishes; every kernel of
+// this library calls pdl_wait() before its first access to global memory (the
+// wait returns once every earlier grid in the stream has completed and its
+// writes are visible; at once for a plain launch), then pdl_trigger() so that
+// the next kernel can in turn be scheduled early.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
@@ -163,29 +164,53 @@ inline int64_t channels(const gdn_dims& d) {
 }
 inline size_t dtype_size(int32_t t) { return t == GDN_BF16 ? 2 : 4; }
 
-// launch k<<<grid, block, smem, s>>>(args...) as a programmatic dependent of
-// the previous work in the stream (optionally as clusters of `cluster` CTAs)
+// launch k<<<grid, block, smem, s>>>(args...), optionally as clusters of
+// `cluster` CTAs and as a programmatic dependent of the previous work in the
+// stream (pdl; GDN_NO_PDL=1 turns that off, for measurement)
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                       dim3 cluster, Args&&... args) {
+cudaError_t launch_ex(bool pdl, void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                      dim3 cluster, Args&&... args) {
+  static const bool no_pdl = [] {
+    const char* e = std::getenv("GDN_NO_PDL");
+    return e && e[0] == '1';
+  }();
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.numAttrs = 1;
+  unsigned n = 0;
+  if (pdl && !no_pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
   if (cluster.x * cluster.y * cluster.z > 1) {
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = cluster.x;
-    attr[1].val.clusterDim.y = cluster.y;
-    attr[1].val.clusterDim.z = cluster.z;
-    cfg.numAttrs = 2;
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster.x;
+    attr[n].val.clusterDim.y = cluster.y;
+    attr[n].val.clusterDim.z = cluster.z;
+    ++n;
   }
   cfg.attrs = attr;
+  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, k, std::forward<Args>(args)...);
+}
+// Programmatic dependent launch pays off for the decode and per-head verify
+// kernels and the slot operations (the next launch overlaps the previous
+// kernel's tail: decode batch 64, 0.85 -> 0.89 of HBM); it measured slower
+// for the persistent verify kernel and the prefill kernels, which launch in
+// plain stream order (their pdl_wait() then returns at once).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, dim3 cluster,
+                       Args&&... args) {
+  return launch_ex(true, k, grid, block, smem, s, cluster, std::forward<Args>(args)...);
+}
+template <typename... KArgs, typename... Args>
+cudaError_t launch_plain(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, dim3 cluster,
+                         Args&&... args) {
+  return launch_ex(false, k, grid, block, smem, s, cluster, std::forward<Args>(args)...);
 }
 inline size_t ssm_slot_bytes(const gdn_dims& d) {
   return (size_t)d.hv * d.dv * d.dk * sizeof(float);

@@ -455,7 +455,7 @@ WsLayout ws_layout(const gdn_dims& d, int64_t total) {
 template <int DK, int DVT, typename Tact, typename Tconv>
 cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t s) {
   if (a.total > 0) {
-    cudaError_t e = launch_pdl(features_kernel<DK, Tact, Tconv>, dim3((unsigned)a.total, (unsigned)a.hk),
+    cudaError_t e = launch_plain(features_kernel<DK, Tact, Tconv>, dim3((unsigned)a.total, (unsigned)a.hk),
                                dim3(kThreads), 0, s, dim3(1), a);
     if (e != cudaSuccess) return e;
   }
@@ -464,9 +464,9 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(ck, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::bytes);
   if (e != cudaSuccess) return e;
   const int n_tiles = (a.dv + DVT - 1) / DVT;
-  e = launch_pdl(ck, dim3((unsigned)(a.hv * n_tiles), (unsigned)a.n_seq), dim3(kThreads), L::bytes, s, dim3(1), a);
+  e = launch_plain(ck, dim3((unsigned)(a.hv * n_tiles), (unsigned)a.n_seq), dim3(kThreads), L::bytes, s, dim3(1), a);
   if (e != cudaSuccess) return e;
-  return launch_pdl(history_kernel<Tact, Tconv>, history_grid(a), dim3(kThreads), 0, s, dim3(1), a);
+  return launch_plain(history_kernel<Tact, Tconv>, history_grid(a), dim3(kThreads), 0, s, dim3(1), a);
 }
 
 template <int DK, int DVT>
@@ -480,10 +480,10 @@ cudaError_t dispatch_prefill(const PrefillArgs& a, int act, int cv, cudaStream_t
 cudaError_t launch_history(const PrefillArgs& a, int act, int cv, cudaStream_t s) {
   const dim3 grid = history_grid(a);
   if (act == GDN_F32 && cv == GDN_F32)
-    return launch_pdl(history_kernel<float, float>, grid, dim3(kThreads), 0, s, dim3(1), a);
+    return launch_plain(history_kernel<float, float>, grid, dim3(kThreads), 0, s, dim3(1), a);
   if (act == GDN_BF16 && cv == GDN_BF16)
-    return launch_pdl(history_kernel<__nv_bfloat16, __nv_bfloat16>, grid, dim3(kThreads), 0, s, dim3(1), a);
-  return launch_pdl(history_kernel<__nv_bfloat16, float>, grid, dim3(kThreads), 0, s, dim3(1), a);
+    return launch_plain(history_kernel<__nv_bfloat16, __nv_bfloat16>, grid, dim3(kThreads), 0, s, dim3(1), a);
+  return launch_plain(history_kernel<__nv_bfloat16, float>, grid, dim3(kThreads), 0, s, dim3(1), a);
 }
 
 // The tensor-core path takes dk = dv = 128, width 4; GDN_PREFILL_PATH=cuda

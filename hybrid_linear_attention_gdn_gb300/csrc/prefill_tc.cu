@@ -997,19 +997,19 @@ size_t prefill_tc_workspace(const gdn_dims& d, int32_t n_seq, int64_t total) {
 
 template <typename Tact, typename Tconv>
 static cudaError_t launch_tc_t(const TcArgs& a, cudaStream_t s) {
-  cudaError_t e = launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, s, dim3(1), a);
+  cudaError_t e = launch_plain(plan_kernel, dim3(1), dim3(1024), 0, s, dim3(1), a);
   if (e != cudaSuccess) return e;
   auto fk = tc_features_kernel<Tact, Tconv>;
   const size_t fsm = (size_t)(kC + 3) * (2 * kD + a.G * kD) * sizeof(Tact);
   if ((e = cudaFuncSetAttribute(fk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsm)) != cudaSuccess)
     return e;
-  e = launch_pdl(fk, dim3((unsigned)a.n_chunks_max, (unsigned)a.hk), dim3(kTh), fsm, s, dim3(1), a);
+  e = launch_plain(fk, dim3((unsigned)a.n_chunks_max, (unsigned)a.hk), dim3(kTh), fsm, s, dim3(1), a);
   if (e != cudaSuccess) return e;
   auto ck = tc_chain_kernel<Tact>;
   const size_t csm = sizeof(ChainSmem) + 1024;
   if ((e = cudaFuncSetAttribute(ck, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csm)) != cudaSuccess)
     return e;
-  return launch_pdl(ck, dim3((unsigned)a.hv, (unsigned)a.n_seq), dim3(kChainThreads), csm, s, dim3(1), a);
+  return launch_plain(ck, dim3((unsigned)a.hv, (unsigned)a.n_seq), dim3(kChainThreads), csm, s, dim3(1), a);
 }
 
 cudaError_t prefill_tc_launch(const gdn_dims& d, const gdn_pool& pool, const gdn_pool& ckpt,

@@ -330,7 +330,7 @@ cudaError_t launch_v(const VArgs& a, cudaStream_t s) {
   }
   const int slots = sm_count() * MINB;
   const int grid = a.n_items < slots ? a.n_items : slots;
-  return launch_pdl(k, dim3((unsigned)grid), dim3(kThr), sizeof(SM), s, dim3(1), a);
+  return launch_plain(k, dim3((unsigned)grid), dim3(kThr), sizeof(SM), s, dim3(1), a);
 }
 
 template <typename Tact, typename Tconv>
