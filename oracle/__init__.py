@@ -234,6 +234,47 @@ def spec_commit(dims: Dims, spec: Pool, work: Pool, spec_ids, accept_len, slot_i
     return err.value
 
 
+def commit_index(spec_ids, accept_len, slot_ids):
+    """Index-update commit; returns (new slot_ids [B], freed [B][T], err)."""
+    L = lib()
+    spec_ids, accept_len = _i32(spec_ids), _i32(accept_len)
+    B, T = spec_ids.shape
+    slots = _i32(slot_ids).copy()
+    freed = np.zeros((B, T), np.int32)
+    err = ctypes.c_uint32(0)
+    rc = L.orc_commit_index(_ptr(spec_ids), _ptr(accept_len), _ptr(slots), _ptr(freed),
+                            ctypes.c_int32(B), ctypes.c_int32(T), ctypes.byref(err))
+    assert rc == 0
+    return slots, freed, err.value
+
+
+def state_pack(dims: Dims, pool: Pool, ids):
+    """Returns (ssm records [n][HV][DV][DK], conv records [n][W-1][C], err)."""
+    L = lib()
+    ids = _i32(ids)
+    n = ids.shape[0]
+    st_ssm = np.zeros((n, dims.hv, dims.dv, dims.dk), np.float64)
+    st_conv = np.zeros((n, dims.w - 1, dims.channels), np.float64)
+    err = ctypes.c_uint32(0)
+    cd = dims.c()
+    rc = L.orc_state_pack(ctypes.byref(cd), pool.c(), _ptr(ids), ctypes.c_int32(n), _ptr(st_ssm),
+                          _ptr(st_conv), ctypes.byref(err))
+    assert rc == 0
+    return st_ssm, st_conv, err.value
+
+
+def state_unpack(dims: Dims, st_ssm, st_conv, pool: Pool, ids):
+    L = lib()
+    ids = _i32(ids)
+    st_ssm, st_conv = _f64(st_ssm), _f64(st_conv)
+    err = ctypes.c_uint32(0)
+    cd = dims.c()
+    rc = L.orc_state_unpack(ctypes.byref(cd), _ptr(st_ssm), _ptr(st_conv), pool.c(), _ptr(ids),
+                            ctypes.c_int32(ids.shape[0]), ctypes.byref(err))
+    assert rc == 0
+    return err.value
+
+
 def _prefill_common(dims, slot_ids, cu_seqlens, start_pos, ckpt_ids, qkv, a, b):
     slot_ids = _i32(slot_ids)
     cu = _i32(cu_seqlens)

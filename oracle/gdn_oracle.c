@@ -348,6 +348,76 @@ int orc_spec_commit(const orc_dims* d, orc_pool spec, orc_pool work,
   return 0;
 }
 
+/* ---- index-update commit ------------------------------------------------
+ * TokenSpeed talk, "Kernel: 让 MLA 真正跑满 GPU": the accepted draft's state is
+ * adopted by updating the request's index rather than by moving data; the
+ * Qwen3.5 page, "Scheduler dual": rollback keeps the pre-draft working slot.
+ * The snapshots live in the working pool.  For request r, L = accept_len[r]:
+ *   L = 0: the working slot stays; freed[r][t] = spec_ids[r][t] for all t.
+ *   1 <= L <= T and spec_ids[r][L-1] >= 0: slot_ids[r] becomes
+ *     spec_ids[r][L-1]; freed[r][0] = the old working slot and
+ *     freed[r][1..T) = the other snapshots in draft order.
+ *   anything else: error bit, slot_ids[r] unchanged, freed[r][*] = -1. */
+int orc_commit_index(const int32_t* spec_ids, const int32_t* accept_len, int32_t* slot_ids,
+                     int32_t* freed, int32_t B, int32_t T, uint32_t* err) {
+  if (B < 0 || T < 1) return 1;
+  for (int32_t r = 0; r < B; ++r) {
+    const int32_t* sp = spec_ids + (int64_t)r * T;
+    int32_t* fr = freed + (int64_t)r * T;
+    int32_t L = accept_len[r];
+    if (L == 0) {
+      for (int32_t t = 0; t < T; ++t) fr[t] = sp[t];
+      continue;
+    }
+    if (L < 0 || L > T || sp[L - 1] < 0) {
+      if (err) *err |= ORC_ERR_SLOT_OOB;
+      for (int32_t t = 0; t < T; ++t) fr[t] = -1;
+      continue;
+    }
+    int32_t k = 0;
+    fr[k++] = slot_ids[r];
+    for (int32_t t = 0; t < T; ++t)
+      if (t != L - 1) fr[k++] = sp[t];
+    slot_ids[r] = sp[L - 1];
+  }
+  return 0;
+}
+
+/* ---- state pack / unpack ---------------------------------------------------
+ * TokenSpeed Qwen3.5 page, "Disaggregacion Prefill-Decode": slot ids become
+ * offsets and the states move as contiguous blocks.  Record i of the staging
+ * area holds slot ids[i]: its SSM [hv][dv][dk] (st_ssm + i * ssm elements)
+ * and its conv history [W-1][C] (st_conv + i * conv elements).
+ * Pack: id -1 gives a zero record; an id outside the pool a zero record and
+ * the error bit.  Unpack: record i -> slot ids[i]; -1 is skipped; an id
+ * outside the pool is skipped with the error bit. */
+int orc_state_pack(const orc_dims* d, orc_pool pool, const int32_t* ids, int32_t n,
+                   double* st_ssm, double* st_conv, uint32_t* err) {
+  if (check_dims(d)) return 1;
+  int64_t ns = ssm_elems(d), nc = conv_elems(d);
+  for (int32_t i = 0; i < n; ++i) {
+    int c = slot_class(ids[i], pool.num_slots);
+    if (c == 2 && err) *err |= ORC_ERR_SLOT_OOB;
+    for (int64_t e = 0; e < ns; ++e) st_ssm[i * ns + e] = c ? 0.0 : pool.ssm[ids[i] * ns + e];
+    for (int64_t e = 0; e < nc; ++e) st_conv[i * nc + e] = c ? 0.0 : pool.conv[ids[i] * nc + e];
+  }
+  return 0;
+}
+
+int orc_state_unpack(const orc_dims* d, const double* st_ssm, const double* st_conv, orc_pool pool,
+                     const int32_t* ids, int32_t n, uint32_t* err) {
+  if (check_dims(d)) return 1;
+  int64_t ns = ssm_elems(d), nc = conv_elems(d);
+  for (int32_t i = 0; i < n; ++i) {
+    int c = slot_class(ids[i], pool.num_slots);
+    if (c == 2 && err) *err |= ORC_ERR_SLOT_OOB;
+    if (c) continue;
+    for (int64_t e = 0; e < ns; ++e) pool.ssm[ids[i] * ns + e] = st_ssm[i * ns + e];
+    for (int64_t e = 0; e < nc; ++e) pool.conv[ids[i] * nc + e] = st_conv[i * nc + e];
+  }
+  return 0;
+}
+
 /* ---- a8: prefill, token by token (the plain definition) -----------------
  * Sequence n owns tokens [cu_seqlens[n], cu_seqlens[n+1]) of qkv [Ttot][C]
  * (a,b [Ttot][hv], out [Ttot][hv][dv]); its first token sits at absolute

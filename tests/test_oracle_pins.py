@@ -340,6 +340,70 @@ def test_verify_then_commit_equals_L_decode_steps():
         np.testing.assert_array_equal(work.conv, ref.conv)
 
 
+def test_commit_index_hand_worked():
+    """Index-update commit, each case worked by hand: rollback (L = 0), a
+    middle draft, the last draft, an accepted snapshot that was never written
+    (-1) and an accept length beyond T."""
+    spec_ids = np.array([[5, 6, 7], [8, 9, 10], [11, 12, 13], [14, -1, 15], [16, 17, 18]], np.int32)
+    L = np.array([0, 2, 3, 2, 4], np.int32)
+    slots, freed, err = oracle.commit_index(spec_ids, L, [1, 2, 3, 4, 0])
+    assert err == oracle.ERR_SLOT_OOB
+    np.testing.assert_array_equal(slots, [1, 9, 13, 4, 0])
+    np.testing.assert_array_equal(freed, [[5, 6, 7], [2, 8, 10], [3, 11, 12], [-1, -1, -1], [-1, -1, -1]])
+
+
+def test_commit_index_equals_copy_commit():
+    """Adopting the accepted snapshot by index leaves the same state under the
+    request's slot as the copying commit, and every slot that held a draft or
+    the old working state is either the new working slot or freed, once."""
+    shape = synth.TINY
+    d = _dims(shape)
+    g, pool, params = _tiny_setup(12)
+    B, T = 2, 3
+    ids = np.array([0, 1], np.int32)
+    spec_ids = np.array([[2, 3, 4], [5, 6, 7]], np.int32)  # snapshots in the working pool
+    qkv, a, b = (t.double().numpy() for t in synth.tokens(shape, g, (B, T)))
+    _, err = oracle.spec_verify(d, pool, pool, params, ids, spec_ids, qkv, a, b)
+    assert err == 0
+    for L in range(T + 1):
+        Ls = np.array([L, T - L], np.int32)
+        copied = pool.copy()
+        assert oracle.spec_commit(d, copied, copied, spec_ids, Ls, ids) == 0
+        slots, freed, err = oracle.commit_index(spec_ids, Ls, ids)
+        assert err == 0
+        for r in range(B):
+            np.testing.assert_array_equal(pool.ssm[slots[r]], copied.ssm[ids[r]])
+            np.testing.assert_array_equal(pool.conv[slots[r]], copied.conv[ids[r]])
+            assert sorted([slots[r], *freed[r]]) == sorted([ids[r], *spec_ids[r]])
+
+
+def test_state_pack_unpack():
+    """Pack gathers slots into records (zero record for -1 and, with the
+    error bit, for an id outside the pool); unpacking the records into other
+    slots is the slot copy."""
+    shape = synth.TINY
+    d = _dims(shape)
+    _, pool, _ = _tiny_setup(13)
+    ids = [3, -1, 6, 9, 0]
+    st_ssm, st_conv, err = oracle.state_pack(d, pool, ids)
+    assert err == oracle.ERR_SLOT_OOB
+    for i, s in enumerate(ids):
+        if 0 <= s < 8:
+            np.testing.assert_array_equal(st_ssm[i], pool.ssm[s])
+            np.testing.assert_array_equal(st_conv[i], pool.conv[s])
+        else:
+            assert np.all(st_ssm[i] == 0) and np.all(st_conv[i] == 0)
+    _, dst, _ = _tiny_setup(14)
+    expect = dst.copy()
+    err = oracle.state_unpack(d, st_ssm, st_conv, dst, [7, 2, 1, -1, 12])
+    assert err == oracle.ERR_SLOT_OOB
+    assert oracle.slot_copy(d, pool, expect, [3, 6], [7, 1]) == 0
+    expect.ssm[2] = 0.0  # record 1 is the zero record of id -1
+    expect.conv[2] = 0.0
+    np.testing.assert_array_equal(dst.ssm, expect.ssm)
+    np.testing.assert_array_equal(dst.conv, expect.conv)
+
+
 # ----------------------------------------------------------------- prefill
 
 def _prefill_inputs(shape, seed, lens, starts):
