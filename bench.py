@@ -517,6 +517,32 @@ def measure_rows(gdn, synth, dev, stream, hbm_peak, bf16_peak, which="all", pref
         rows["spec_commit_b16"] = frac(B * 2 * slot_bytes, _events_time(fm, reps, stream))
         del spec
 
+        # index-update commit of the same batch: only int32 indices move
+        idx_slots = work_sets[0].clone()
+        freed = torch.empty((B, T), dtype=torch.int32, device=dev)
+
+        def fi(i):
+            gdn.spec_commit_index(spec_sets[i % 4], L, idx_slots, freed)
+        fi(0)
+        ms_i = _events_time(fi, reps, stream)
+        rows["spec_commit_index_b16"] = {"ms": ms_i, "ms_graph": _graph_time(fi, 20, 10, dev),
+                                         "bytes_moved": B * (T + 1 + 2 * T + 2) * 4}
+
+        # state pack / unpack of 64 slots through one contiguous staging buffer
+        rec = gdn.state_record_bytes(dims)
+        staging = torch.empty(64 * rec, dtype=torch.uint8, device=dev)
+
+        def fpk(i):
+            gdn.state_pack(dims, pool, pair_sets[i % 4][0], staging)
+        fpk(0)
+        rows["state_pack_64"] = frac(64 * 2 * rec, _events_time(fpk, reps, stream))
+
+        def fup(i):
+            gdn.state_unpack(dims, staging, pool, pair_sets[i % 4][1])
+        fup(0)
+        rows["state_unpack_64"] = frac(64 * 2 * rec, _events_time(fup, reps, stream))
+        del staging
+
         # verify at larger batches (T = 8), two alternating request / spec-cache sets
         vsweep = {}
         for Bv in (32, 64, 128):

@@ -20,7 +20,8 @@ from . import _build
 F32, BF16 = 0, 1
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_SCRATCH_LIMIT = 0, 1, 2, 3, 4
 DEV_ERR_SLOT_OOB, DEV_ERR_TIMEOUT, DEV_ERR_SEQLENS = 1, 2, 4
-K_DECODE, K_SPEC_VERIFY, K_SLOT_COPY, K_SLOT_ZERO, K_SPEC_COMMIT, K_PREFILL = range(6)
+(K_DECODE, K_SPEC_VERIFY, K_SLOT_COPY, K_SLOT_ZERO, K_SPEC_COMMIT, K_PREFILL, K_COMMIT_INDEX,
+ K_STATE_PACK) = range(8)
 K_COUNT = 8
 
 _DT_CODE = {torch.float32: F32, torch.bfloat16: BF16}
@@ -68,6 +69,10 @@ EXPORTS = {
                                    _I32, _P, _P, _P, _P, _P, _P], _I32),
     "gdn_slot_copy": ([_PD, CPool, CPool, _P, _P, _I32, _P, _P], _I32),
     "gdn_slot_zero": ([_PD, CPool, _P, _I32, _P, _P], _I32),
+    "gdn_spec_commit_index": ([_P, _P, _P, _P, _I32, _I32, _P, _P], _I32),
+    "gdn_state_record_bytes": ([_PD], ctypes.c_size_t),
+    "gdn_state_pack": ([_PD, CPool, _P, _I32, _P, ctypes.c_size_t, _P, _P], _I32),
+    "gdn_state_unpack": ([_PD, _P, ctypes.c_size_t, CPool, _P, _I32, _P, _P], _I32),
     "gdn_status_string": ([_I32], ctypes.c_char_p),
     "gdn_launch_count": ([_I32], ctypes.c_uint64),
     "gdn_launch_count_reset": ([], None),
@@ -287,6 +292,44 @@ def slot_zero(dims: Dims, pool: StatePool, ids, dev_err=None, stream=None):
     st = L.gdn_slot_zero(ctypes.byref(cd), pool.c(), _ptr(ids), int(ids.shape[0]), _ptr(dev_err),
                          _stream(stream))
     _check("gdn_slot_zero", st)
+
+
+def spec_commit_index(spec_ids, accept_len, slot_ids, freed_ids, dev_err=None, stream=None):
+    """Adopt the accepted snapshot by index: slot_ids is updated in place and
+    freed_ids [B][T] receives the slots the caller returns to its allocator."""
+    L = load()
+    B, T = spec_ids.shape
+    st = L.gdn_spec_commit_index(_ptr(spec_ids), _ptr(accept_len), _ptr(slot_ids),
+                                 _ptr(freed_ids), int(B), int(T), _ptr(dev_err),
+                                 _stream(stream))
+    _check("gdn_spec_commit_index", st)
+
+
+def state_record_bytes(dims: Dims) -> int:
+    cd = dims.c()
+    return int(load().gdn_state_record_bytes(ctypes.byref(cd)))
+
+
+def _nbytes(t) -> int:
+    return t.numel() * t.element_size()
+
+
+def state_pack(dims: Dims, pool: StatePool, ids, staging, dev_err=None, stream=None):
+    """Records of slots ids[i] into the byte buffer ``staging``."""
+    L = load()
+    cd = dims.c()
+    st = L.gdn_state_pack(ctypes.byref(cd), pool.c(), _ptr(ids), int(ids.shape[0]),
+                          _ptr(staging), _nbytes(staging), _ptr(dev_err), _stream(stream))
+    _check("gdn_state_pack", st)
+
+
+def state_unpack(dims: Dims, staging, pool: StatePool, ids, dev_err=None, stream=None):
+    """Record i of ``staging`` into slot ids[i]."""
+    L = load()
+    cd = dims.c()
+    st = L.gdn_state_unpack(ctypes.byref(cd), _ptr(staging), _nbytes(staging), pool.c(),
+                            _ptr(ids), int(ids.shape[0]), _ptr(dev_err), _stream(stream))
+    _check("gdn_state_unpack", st)
 
 
 def launch_count(kernel: int) -> int:

@@ -226,6 +226,45 @@ gdn_status gdn_slot_zero(const gdn_dims* dims, gdn_pool pool,
                          const int32_t* ids, int32_t n, uint32_t* dev_err,
                          void* stream);
 
+/*
+ * Index-update commit (TokenSpeed talk, "Kernel: 让 MLA 真正跑满 GPU": the
+ * accepted state is adopted by updating an index, not by moving data; Qwen3.5
+ * page, "Scheduler dual": rollback keeps the pre-draft working slot).  For
+ * callers whose spec snapshots live in the working pool (gdn_spec_verify with
+ * spec == work).  Nothing but indices moves.  For request r, L = accept_len[r]:
+ *   L = 0: slot_ids[r] is kept; freed_ids[r][t] = spec_ids[r][t].
+ *   1 <= L <= T with spec_ids[r][L-1] >= 0: slot_ids[r] <- spec_ids[r][L-1];
+ *     freed_ids[r][0] = the previous working slot, freed_ids[r][1..T) = the
+ *     other snapshots in draft order (slots the caller returns to its
+ *     allocator; -1 entries of spec_ids pass through).
+ *   anything else: GDN_DEV_ERR_SLOT_OOB, slot_ids[r] kept, freed_ids[r][*] = -1.
+ *   spec_ids [B][T], accept_len [B], slot_ids [B] (read and written),
+ *   freed_ids [B][T] (written); all int32 device arrays.
+ */
+gdn_status gdn_spec_commit_index(const int32_t* spec_ids, const int32_t* accept_len,
+                                 int32_t* slot_ids, int32_t* freed_ids, int32_t B,
+                                 int32_t T, uint32_t* dev_err, void* stream);
+
+/*
+ * State pack / unpack for moving slot states between engines (TokenSpeed
+ * Qwen3.5 page, "Disaggregacion Prefill-Decode": slot ids -> offsets ->
+ * contiguous blocks for the transfer; this is the device half, no network).
+ * Record i of `staging` (gdn_state_record_bytes(dims) bytes each, 16-byte
+ * aligned, n records) is slot ids[i]: its SSM (fp32 [hv][dv][dk]) followed by
+ * its conv history ([W-1][C] in the conv dtype), byte for byte as in the pool.
+ *   pack:   record i <- slot ids[i]; id -1 gives a zero record; an id outside
+ *           the pool gives a zero record and GDN_DEV_ERR_SLOT_OOB.
+ *   unpack: slot ids[i] <- record i; -1 skips; an id outside the pool skips
+ *           and sets GDN_DEV_ERR_SLOT_OOB.  ids must be distinct (precondition).
+ *   staging_bytes >= n * record bytes, else GDN_ERR_INVALID_ARG.
+ */
+size_t gdn_state_record_bytes(const gdn_dims* dims);
+gdn_status gdn_state_pack(const gdn_dims* dims, gdn_pool pool, const int32_t* ids, int32_t n,
+                          void* staging, size_t staging_bytes, uint32_t* dev_err, void* stream);
+gdn_status gdn_state_unpack(const gdn_dims* dims, const void* staging, size_t staging_bytes,
+                            gdn_pool pool, const int32_t* ids, int32_t n, uint32_t* dev_err,
+                            void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* gdn_status_string(int32_t status);
 
@@ -236,6 +275,8 @@ const char* gdn_status_string(int32_t status);
 #define GDN_K_SLOT_ZERO 3
 #define GDN_K_SPEC_COMMIT 4
 #define GDN_K_PREFILL 5
+#define GDN_K_COMMIT_INDEX 6
+#define GDN_K_STATE_PACK 7 /* pack and unpack */
 #define GDN_K_COUNT 8
 uint64_t gdn_launch_count(int32_t kernel);
 void gdn_launch_count_reset(void);

@@ -114,6 +114,36 @@ def test_null_and_negative_arguments(lib):
                                  None) == binding.OK
 
 
+def test_state_record_and_index_commit_arguments(lib):
+    d = _dims()
+    # SSM fp32 [32][128][128] + conv history bf16 [3][2*16*128 + 32*128]
+    rec = 32 * 128 * 128 * 4 + 3 * (2 * 16 * 128 + 32 * 128) * 2
+    assert lib.gdn_state_record_bytes(ctypes.byref(d)) == rec
+    assert lib.gdn_state_record_bytes(ctypes.byref(_dims(dk=48))) == 0
+    assert lib.gdn_state_record_bytes(None) == 0
+    pool = binding.CPool(0x10000, 0x20000, 4)
+    n0 = lib.gdn_launch_count(binding.K_STATE_PACK)
+    # staging one byte short of one record, misaligned, or absent
+    assert lib.gdn_state_pack(ctypes.byref(d), pool, 0x100, 1, 0x40000, rec - 1, None,
+                              None) == binding.ERR_INVALID_ARG
+    assert lib.gdn_state_unpack(ctypes.byref(d), 0x40008, 4 * rec, pool, 0x100, 1, None,
+                                None) == binding.ERR_INVALID_ARG
+    assert lib.gdn_state_pack(ctypes.byref(d), pool, 0x100, 1, None, 4 * rec, None,
+                              None) == binding.ERR_INVALID_ARG
+    assert lib.gdn_state_pack(ctypes.byref(d), pool, 0x100, -1, 0x40000, 4 * rec, None,
+                              None) == binding.ERR_INVALID_ARG
+    assert lib.gdn_state_unpack(ctypes.byref(d), 0x40000, 0, pool, None, 0, None,
+                                None) == binding.OK
+    assert lib.gdn_launch_count(binding.K_STATE_PACK) == n0
+    n0 = lib.gdn_launch_count(binding.K_COMMIT_INDEX)
+    assert lib.gdn_spec_commit_index(0x100, 0x200, 0x300, 0x400, 4, 0, None,
+                                     None) == binding.ERR_INVALID_ARG
+    assert lib.gdn_spec_commit_index(None, 0x200, 0x300, 0x400, 4, 2, None,
+                                     None) == binding.ERR_INVALID_ARG
+    assert lib.gdn_spec_commit_index(None, None, None, None, 0, 2, None, None) == binding.OK
+    assert lib.gdn_launch_count(binding.K_COMMIT_INDEX) == n0
+
+
 def test_launch_counters(lib):
     lib.gdn_launch_count_reset()
     assert all(lib.gdn_launch_count(k) == 0 for k in range(binding.K_COUNT))
