@@ -5,7 +5,8 @@
 // gated delta rule), specialised for dk = dv = 128, conv width 4.
 //
 //   plan:     per-sequence offsets of its 64-token chunks (absolute-aligned).
-//   features: one CTA per (chunk, QK head): conv1d + SiLU + L2 norm + gates
+//   features: one CTA per (chunk, QK head): the input tile arrives by TMA
+//             tensor copies; conv1d + SiLU + L2 norm + gates
 //             for the chunk's 64 tokens, written as bf16 operand images in the
 //             tensor core's 128B-swizzled shared-memory layout, so the chain
 //             kernel fetches each with a single bulk copy:
@@ -30,6 +31,8 @@
 //             by one thread and completed through tcgen05.commit -> mbarrier.
 //   The conv histories of checkpoints and of the final state come from the
 //   history kernel of prefill.cu.
+#include <cuda.h>  // CUtensorMap (the encoder is fetched through the runtime)
+
 #include "gdn_common.cuh"
 #include "umma.cuh"
 
@@ -146,18 +149,27 @@ __device__ __forceinline__ int seq_of_chunk(const int32_t* base, int n_seq, int 
 // ---------------------------------------------------------------------------
 // features: grid (n_chunks_max, hk), 256 threads, one CTA per (chunk, QK head):
 // q and k of QK head hq and v of the G V heads reading it.  The CTA stages its
-// input tile (3 rows before the chunk + its 64 rows, all 256 + G*128 channels)
-// in shared memory with cp.async (rows before the sequence from the conv
-// history, rows past it as zeros).  Then each lane walks 8 consecutive rows of one 8-channel
-// group (a sliding window of 4 staged rows): conv1d, SiLU, for q/k the row's
-// L2 norm by a 16-lane shuffle reduction (a warp holds one row's 16 q groups
-// and 16 k groups), and one 16-byte store into the swizzled operand image.
+// input tile (3 rows before the chunk + its 64 rows) as 2 + G parts of 128
+// channels (q, k, then each V head), each brought by one TMA tensor copy of
+// 128 channels x 67 packed token rows; rows outside the tensor arrive as
+// zeros, and the up to 3 rows just before the sequence start are then
+// overwritten from the conv history (rows further out, or past the sequence
+// end, only feed outputs that are zeroed).  Then each lane walks 8 consecutive
+// rows of one 8-channel group (a sliding window of 4 staged rows): conv1d,
+// SiLU, for q/k the row's L2 norm by a 16-lane shuffle reduction (a warp holds
+// one row's 16 q groups and 16 k groups), and one 16-byte store into the
+// swizzled operand image.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_addr(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
+constexpr int kTileRows = kC + 3;
+// 2D tensor copy global -> shared (box of the tensor map at (x, y)); rows
+// outside the tensor are filled with zeros
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3}], [%4];\n" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
 }
 __device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8]) {
   const uint4 u = *reinterpret_cast<const uint4*>(p);
@@ -179,7 +191,7 @@ __device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
 // r .. r+3 = positions P+r-3 .. P+r); zero outside the sequence.  The fast
 // exponential and division are far finer than the bf16 operands they feed.
 // emit(r, y) receives each row's 8 results.
-template <typename Tact, class Emit>
+template <bool kFull, typename Tact, class Emit>
 __device__ __forceinline__ void conv_walk8(const Tact* xs, int nch, int r0, int lc, const float (&w)[8][4],
                                            int64_t P, int64_t p0, int64_t p1, Emit emit) {
   float x[4][8];
@@ -189,7 +201,7 @@ __device__ __forceinline__ void conv_walk8(const Tact* xs, int nch, int r0, int 
   for (int k = 0; k < 8; ++k) {
     const int r = r0 + k;
     load8(xs + (size_t)(r + 3) * nch + lc, x[(k + 3) & 3]);
-    const bool valid = P + r >= p0 && P + r < p1;
+    const bool valid = kFull || (P + r >= p0 && P + r < p1);  // kFull: the chunk is inside
     float y[8];
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
@@ -204,10 +216,10 @@ __device__ __forceinline__ void conv_walk8(const Tact* xs, int nch, int r0, int 
 }
 
 template <typename Tact, typename Tconv>
-__global__ void __launch_bounds__(kTh, 3) tc_features_kernel(const TcArgs a) {
+__global__ void __launch_bounds__(kTh, 3) tc_features_kernel(const TcArgs a, const __grid_constant__ CUtensorMap qmap) {
   pdl_wait();
   pdl_trigger();
-  extern __shared__ __align__(16) unsigned char fsm[];
+  extern __shared__ __align__(16) unsigned char fsm_raw[];
   const int gc = blockIdx.x, hq = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (gc >= a.chunk_base[a.n_seq]) return;
@@ -218,35 +230,26 @@ __global__ void __launch_bounds__(kTh, 3) tc_features_kernel(const TcArgs a) {
   if (slot_class(slot, a.num_slots)) return;
   const int64_t P = (p0 / kC + (gc - a.chunk_base[n])) * kC;  // absolute position of row 0
   const int64_t p1 = p0 + len;
-  const int GD = a.G * kD;
-  const int nch = 2 * kD + GD;               // local channels: q | k | v of the G heads
-  Tact* xs = reinterpret_cast<Tact*>(fsm);   // [kC + 3][nch], row i = position P - 3 + i
-  const Tact* qkv = reinterpret_cast<const Tact*>(a.qkv);
-  const Tconv* hist = reinterpret_cast<const Tconv*>(a.conv) + (size_t)slot * 3 * a.C;
-  auto gchan = [&](int lc) -> size_t {  // global channel of local channel lc
-    if (lc < kD) return (size_t)hq * kD + lc;
-    if (lc < 2 * kD) return (size_t)a.hk * kD + (size_t)hq * kD + (lc - kD);
-    return 2 * (size_t)a.hk * kD + (size_t)hq * GD + (lc - 2 * kD);
+  const int nparts = 2 + a.G;
+  // part p: [67 rows][128 channels]; 128-byte aligned for the tensor copies
+  Tact* xs = reinterpret_cast<Tact*>(fsm_raw + ((128u - (smem_addr(fsm_raw) & 127u)) & 127u));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(xs + (size_t)nparts * kTileRows * kD);
+  auto part = [&](int q) { return xs + (size_t)q * kTileRows * kD; };
+  auto part_chan = [&](int q) -> int {  // first global channel of part q
+    return q < 2 ? (q * a.hk + hq) * kD : (2 * a.hk + hq * a.G + (q - 2)) * kD;
   };
-  constexpr int EPC = 16 / sizeof(Tact);     // elements per 16-byte piece
-  const int cpr = nch / EPC;                 // pieces per tile row
-  for (int e = tid; e < (kC + 3) * cpr; e += kTh) {
-    const int i = e / cpr, pc = e % cpr;
-    const int64_t pos = P - 3 + i;
-    Tact* dst = xs + (size_t)i * nch + pc * EPC;
-    const size_t c = gchan(pc * EPC);
-    if (pos >= p0 && pos < p1) {
-      cp_async16(dst, qkv + (size_t)(t0 + pos - p0) * a.C + c);
-    } else if (pos < p0 && pos >= p0 - 3) {
-      const Tconv* src = hist + (size_t)(3 - (p0 - pos)) * a.C + c;
-#pragma unroll
-      for (int k = 0; k < EPC; ++k) dst[k] = from_f32<Tact>(to_f32(src[k]));
-    } else {
-#pragma unroll
-      for (int k = 0; k < EPC; ++k) dst[k] = from_f32<Tact>(0.f);
-    }
+  const Tconv* hist = reinterpret_cast<const Tconv*>(a.conv) + (size_t)slot * 3 * a.C;
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
   }
-  // gates (rows outside the sequence: g = beta = 0)
+  __syncthreads();
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar, (uint32_t)(nparts * kTileRows * kD * sizeof(Tact)));
+    const int32_t row0 = (int32_t)(t0 + (P - 3 - p0));  // packed row of tile row 0 (may be < 0)
+    for (int q = 0; q < nparts; ++q) tma_load_2d(part(q), &qmap, part_chan(q), row0, bar);
+  }
+  // gates (rows outside the sequence: g = beta = 0), while the tile lands
   for (int e = tid; e < kC * a.G; e += kTh) {
     const int r = e % kC, gi = e / kC;
     const int h = hq * a.G + gi;
@@ -263,23 +266,50 @@ __global__ void __launch_bounds__(kTh, 3) tc_features_kernel(const TcArgs a) {
     gt[r] = gv;
     gt[kC + r] = bv;
   }
-  cp_async_wait_all();
-  __syncthreads();
+  const bool late = !mbar_wait(bar, 0);
+  if (__syncthreads_or(late)) {
+    // leave only once the copies into this CTA's shared memory have landed
+    if (tid == 0) {
+      report(a.err, GDN_DEV_ERR_TIMEOUT);
+      mbar_wait(bar, 0);
+    }
+    return;
+  }
+  // the up to 3 rows just before the sequence start come from the conv history
+  {
+    const int64_t lo = (P - 3 > p0 - 3) ? P - 3 : p0 - 3;
+    const int64_t hi = (P + kC < p0) ? P + kC : p0;
+    if (lo < hi) {
+      const int per_row = nparts * (kD / 8);  // 8-channel pieces
+      const int nh = (int)(hi - lo);
+      for (int e = tid; e < nh * per_row; e += kTh) {
+        const int64_t pos = lo + e / per_row;
+        const int q = (e % per_row) / (kD / 8), c = 8 * (e % (kD / 8));
+        const Tconv* src = hist + (size_t)(3 - (p0 - pos)) * a.C + part_chan(q) + c;
+        Tact* dst = part(q) + (size_t)(pos - (P - 3)) * kD + c;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) dst[k] = from_f32<Tact>(to_f32(src[k]));
+      }
+      __syncthreads();
+    }
+  }
+  const bool full = P >= p0 && P + kC <= p1;  // every row of the chunk is in the sequence
 
   // q and k: warp w walks rows 8w .. 8w+7; lane l < 16 is q channels 8l .. 8l+7,
   // lane 16 + l the same k channels
   {
-    const int lc = 8 * lane;  // local channel (q: 0..127, k: 128..255)
+    const bool isq = lane < 16;
+    const int lc = 8 * (lane & 15);  // channel within the part
+    const Tact* xp = part(isq ? 0 : 1);
     float w[8][4];
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-      const float4 w4 = *reinterpret_cast<const float4*>(a.conv_w + gchan(lc + c) * 4);
+      const float4 w4 = *reinterpret_cast<const float4*>(a.conv_w + (size_t)(part_chan(isq ? 0 : 1) + lc + c) * 4);
       w[c][0] = w4.x; w[c][1] = w4.y; w[c][2] = w4.z; w[c][3] = w4.w;
     }
-    const bool isq = lane < 16;
     const float qscale = isq ? rsqrtf((float)kD) : 1.f;
     uint8_t* kq = a.ws_kq + ((size_t)gc * a.hk + hq) * kKQBytes;
-    conv_walk8(xs, nch, 8 * warp, lc, w, P, p0, p1, [&](int r, float (&y)[8]) {
+    auto emit = [&](int r, float (&y)[8]) {
       float ss = 0.f;
 #pragma unroll
       for (int c = 0; c < 8; ++c) ss = fmaf(y[c], y[c], ss);
@@ -289,26 +319,33 @@ __global__ void __launch_bounds__(kTh, 3) tc_features_kernel(const TcArgs a) {
 #pragma unroll
       for (int c = 0; c < 8; ++c) y[c] *= sc;
       const int R = isq ? kC + r : r;  // image rows: k^ 0..63, q^ 64..127
-      *reinterpret_cast<uint4*>(kq + umma::sw128_off(R, 8 * (lane & 15), 128 * 128)) = umma::pack8_bf16(y);
-    });
+      *reinterpret_cast<uint4*>(kq + umma::sw128_off(R, lc, 128 * 128)) = umma::pack8_bf16(y);
+    };
+    if (full)
+      conv_walk8<true>(xp, kD, 8 * warp, lc, w, P, p0, p1, emit);
+    else
+      conv_walk8<false>(xp, kD, 8 * warp, lc, w, P, p0, p1, emit);
   }
   // v: (8-channel group, 8-row block) items, G*16 groups per row
   {
     const int gpr = a.G * (kD / 8);
     for (int e = tid; e < 8 * gpr; e += kTh) {
       const int ch = e % gpr, rb = e / gpr;
-      const int lc = 2 * kD + 8 * ch;
+      const int gi = ch / (kD / 8), d = 8 * (ch % (kD / 8));
       float w[8][4];
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        const float4 w4 = *reinterpret_cast<const float4*>(a.conv_w + gchan(lc + c) * 4);
+        const float4 w4 = *reinterpret_cast<const float4*>(a.conv_w + (size_t)(part_chan(2 + gi) + d + c) * 4);
         w[c][0] = w4.x; w[c][1] = w4.y; w[c][2] = w4.z; w[c][3] = w4.w;
       }
-      const int h = hq * a.G + ch / (kD / 8), d = 8 * (ch % (kD / 8));
-      uint8_t* vimg = a.ws_v + ((size_t)gc * a.hv + h) * kVBytes;
-      conv_walk8(xs, nch, 8 * rb, lc, w, P, p0, p1, [&](int r, float (&y)[8]) {
+      uint8_t* vimg = a.ws_v + ((size_t)gc * a.hv + hq * a.G + gi) * kVBytes;
+      auto emit = [&](int r, float (&y)[8]) {
         *reinterpret_cast<uint4*>(vimg + umma::sw128_off(r, d, 64 * 128)) = umma::pack8_bf16(y);
-      });
+      };
+      if (full)
+        conv_walk8<true>(part(2 + gi), kD, 8 * rb, d, w, P, p0, p1, emit);
+      else
+        conv_walk8<false>(part(2 + gi), kD, 8 * rb, d, w, P, p0, p1, emit);
     }
   }
 }
@@ -981,12 +1018,47 @@ static TcLayout tc_layout(const gdn_dims& d, int32_t n_seq, int64_t total) {
   return L;
 }
 
+static size_t features_smem(int G, size_t esz) {
+  return (size_t)(2 + G) * kTileRows * kD * esz + 128 /* alignment */ + 16 /* mbarrier */;
+}
+
+// The features kernel's view of qkv: a 2D tensor [total rows][C channels],
+// copied in boxes of 128 channels x 67 rows.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+static EncodeTiledFn encode_tiled() {
+  static const EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return (EncodeTiledFn) nullptr;
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+static cudaError_t qkv_tensor_map(CUtensorMap* map, const void* qkv, int64_t total, int32_t C, size_t esz) {
+  const EncodeTiledFn enc = encode_tiled();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dim[2] = {(cuuint64_t)C, (cuuint64_t)(total > 0 ? total : 1)};
+  const cuuint64_t stride[1] = {(cuuint64_t)C * esz};
+  const cuuint32_t box[2] = {(cuuint32_t)kD, (cuuint32_t)kTileRows};
+  const cuuint32_t estride[2] = {1, 1};
+  const CUresult r =
+      enc(map, esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+          const_cast<void*>(qkv), dim, stride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 bool prefill_tc_supported(const gdn_dims& d, const void* qkv, const void* out, const gdn_params& p) {
   if (d.dk != kD || d.dv != kD || d.conv_width != 4) return false;
   if (d.hv / d.hk > 8) return false;
   // the features kernel stages (64 + 3) rows of the CTA's 256 + G*128 channels
-  if ((size_t)(kC + 3) * (2 * kD + (size_t)(d.hv / d.hk) * kD) * dtype_size(d.act_dtype) > 227u * 1024u)
-    return false;
+  if (features_smem(d.hv / d.hk, dtype_size(d.act_dtype)) > 227u * 1024u) return false;
   if (!aligned(qkv, 16) || !aligned(out, 16) || !aligned(p.conv_w, 16)) return false;
   return true;
 }
@@ -1000,10 +1072,12 @@ static cudaError_t launch_tc_t(const TcArgs& a, cudaStream_t s) {
   cudaError_t e = launch_plain(plan_kernel, dim3(1), dim3(1024), 0, s, dim3(1), a);
   if (e != cudaSuccess) return e;
   auto fk = tc_features_kernel<Tact, Tconv>;
-  const size_t fsm = (size_t)(kC + 3) * (2 * kD + a.G * kD) * sizeof(Tact);
+  const size_t fsm = features_smem(a.G, sizeof(Tact));
   if ((e = cudaFuncSetAttribute(fk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsm)) != cudaSuccess)
     return e;
-  e = launch_plain(fk, dim3((unsigned)a.n_chunks_max, (unsigned)a.hk), dim3(kTh), fsm, s, dim3(1), a);
+  CUtensorMap qmap;
+  if ((e = qkv_tensor_map(&qmap, a.qkv, a.total, a.C, sizeof(Tact))) != cudaSuccess) return e;
+  e = launch_plain(fk, dim3((unsigned)a.n_chunks_max, (unsigned)a.hk), dim3(kTh), fsm, s, dim3(1), a, qmap);
   if (e != cudaSuccess) return e;
   auto ck = tc_chain_kernel<Tact>;
   const size_t csm = sizeof(ChainSmem) + 1024;
