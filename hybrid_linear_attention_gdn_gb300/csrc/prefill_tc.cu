@@ -249,7 +249,17 @@ __global__ void __launch_bounds__(kTh, 3) tc_features_kernel(const TcArgs a, con
     const int32_t row0 = (int32_t)(t0 + (P - 3 - p0));  // packed row of tile row 0 (may be < 0)
     for (int q = 0; q < nparts; ++q) tma_load_2d(part(q), &qmap, part_chan(q), row0, bar);
   }
-  // gates (rows outside the sequence: g = beta = 0), while the tile lands
+  // this lane's q/k conv weights (lane l < 16: q channels 8l .. 8l+7, lane
+  // 16 + l the same k channels) and the gates, while the tile lands
+  const bool isq = lane < 16;
+  const int lc = 8 * (lane & 15);  // channel within the part
+  float w[8][4];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const float4 w4 = *reinterpret_cast<const float4*>(a.conv_w + (size_t)(part_chan(isq ? 0 : 1) + lc + c) * 4);
+    w[c][0] = w4.x; w[c][1] = w4.y; w[c][2] = w4.z; w[c][3] = w4.w;
+  }
+  // gates (rows outside the sequence: g = beta = 0)
   for (int e = tid; e < kC * a.G; e += kTh) {
     const int r = e % kC, gi = e / kC;
     const int h = hq * a.G + gi;
@@ -295,18 +305,9 @@ __global__ void __launch_bounds__(kTh, 3) tc_features_kernel(const TcArgs a, con
   }
   const bool full = P >= p0 && P + kC <= p1;  // every row of the chunk is in the sequence
 
-  // q and k: warp w walks rows 8w .. 8w+7; lane l < 16 is q channels 8l .. 8l+7,
-  // lane 16 + l the same k channels
+  // q and k: warp w walks rows 8w .. 8w+7
   {
-    const bool isq = lane < 16;
-    const int lc = 8 * (lane & 15);  // channel within the part
     const Tact* xp = part(isq ? 0 : 1);
-    float w[8][4];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const float4 w4 = *reinterpret_cast<const float4*>(a.conv_w + (size_t)(part_chan(isq ? 0 : 1) + lc + c) * 4);
-      w[c][0] = w4.x; w[c][1] = w4.y; w[c][2] = w4.z; w[c][3] = w4.w;
-    }
     const float qscale = isq ? rsqrtf((float)kD) : 1.f;
     uint8_t* kq = a.ws_kq + ((size_t)gc * a.hk + hq) * kKQBytes;
     auto emit = [&](int r, float (&y)[8]) {
@@ -332,20 +333,20 @@ __global__ void __launch_bounds__(kTh, 3) tc_features_kernel(const TcArgs a, con
     for (int e = tid; e < 8 * gpr; e += kTh) {
       const int ch = e % gpr, rb = e / gpr;
       const int gi = ch / (kD / 8), d = 8 * (ch % (kD / 8));
-      float w[8][4];
+      float wv[8][4];
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         const float4 w4 = *reinterpret_cast<const float4*>(a.conv_w + (size_t)(part_chan(2 + gi) + d + c) * 4);
-        w[c][0] = w4.x; w[c][1] = w4.y; w[c][2] = w4.z; w[c][3] = w4.w;
+        wv[c][0] = w4.x; wv[c][1] = w4.y; wv[c][2] = w4.z; wv[c][3] = w4.w;
       }
       uint8_t* vimg = a.ws_v + ((size_t)gc * a.hv + hq * a.G + gi) * kVBytes;
       auto emit = [&](int r, float (&y)[8]) {
         *reinterpret_cast<uint4*>(vimg + umma::sw128_off(r, d, 64 * 128)) = umma::pack8_bf16(y);
       };
       if (full)
-        conv_walk8<true>(part(2 + gi), kD, 8 * rb, d, w, P, p0, p1, emit);
+        conv_walk8<true>(part(2 + gi), kD, 8 * rb, d, wv, P, p0, p1, emit);
       else
-        conv_walk8<false>(part(2 + gi), kD, 8 * rb, d, w, P, p0, p1, emit);
+        conv_walk8<false>(part(2 + gi), kD, 8 * rb, d, wv, P, p0, p1, emit);
     }
   }
 }
