@@ -171,6 +171,21 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
       : "memory");
 }
+// 2D tensor copy shared -> global (box of the tensor map at (x, y), x, y >= 0),
+// tracked by the issuing thread's bulk group
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];\n" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_addr(src)), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+// the issuing thread's bulk stores have read their shared-memory source
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
+// ... all but the most recent bulk group
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;\n" ::: "memory"); }
+// ... and completed their global writes
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
 __device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8]) {
   const uint4 u = *reinterpret_cast<const uint4*>(p);
   const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
@@ -375,6 +390,7 @@ struct __align__(1024) ChainSmem {
   uint64_t ld_full[2], mma_bar, kq_bar;
   uint64_t p_bar;    // P of the current chunk complete (its [K;Q] K^T buffer long read)
   uint64_t st_bar;   // compute warps wrote the state image and read O1 (one arrival per warp)
+  uint64_t ck_bar;   // a checkpoint's tensor stores have read the Delta tiles
   uint32_t tmem_base;
 };
 
@@ -596,7 +612,8 @@ __device__ __forceinline__ void solve_T(const float* A, float* X, float* Y, cons
 }
 
 template <typename Tact>
-__global__ void __launch_bounds__(kChainThreads, 1) tc_chain_kernel(const TcArgs a) {
+__global__ void __launch_bounds__(kChainThreads, 1)
+    tc_chain_kernel(const TcArgs a, const __grid_constant__ CUtensorMap omap, const __grid_constant__ CUtensorMap cmap) {
   pdl_wait();
   pdl_trigger();
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -630,6 +647,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) tc_chain_kernel(const TcArgs
     mbar_init(&S.kq_bar, 1);
     mbar_init(&S.p_bar, 1);
     mbar_init(&S.st_bar, kTh / 32);
+    mbar_init(&S.ck_bar, 1);
     fence_mbar_init();
   }
   if (warp == 0) umma::tmem_alloc(&S.tmem_base, TM_COLS);
@@ -645,6 +663,41 @@ __global__ void __launch_bounds__(kChainThreads, 1) tc_chain_kernel(const TcArgs
   constexpr uint32_t ID_64_MK = umma::idesc_bf16(128, 64, true, false);
   constexpr uint32_t ID_64_KM = umma::idesc_bf16(128, 64, false, true);
   constexpr uint32_t ID_128_KM = umma::idesc_bf16(128, 128, false, true);
+  // bf16 outputs: the output tiles and checkpoints leave by TMA tensor stores
+  // (fp32 outputs stage 32 KB, which overlaps the checkpoint boxes)
+  constexpr bool kTmaStores = sizeof(Tact) == 2;
+  // checkpoint slot of a block boundary at the end of chunk c (-1: none).
+  // The block is kpc chunks (the host checks it is a multiple of 64 tokens);
+  // chunk c ends at the absolute chunk boundary p0 / 64 + c + 1, a block
+  // boundary when q = (p0 / 64) mod kpc + c + 1 is a multiple of kpc, with
+  // checkpoint index q / kpc - 1; a last chunk cut short ends on none.
+  const int kpc = a.ckpt_block / kC;
+  const bool kpc_pow2 = (kpc & (kpc - 1)) == 0;
+  const int kpc_sh = __ffs(kpc) - 1;
+  const int q0 = (int)((p0 / kC) % kpc);
+  const bool last_full = (p1 & (kC - 1)) == 0;
+  auto ckpt_slot = [&](int c) -> int32_t {
+    if (c == nch - 1 && !last_full) return -1;
+    const int q = q0 + c + 1;
+    const int rem = kpc_pow2 ? (q & (kpc - 1)) : q % kpc;
+    if (rem != 0) return -1;
+    const int idx = (kpc_pow2 ? (q >> kpc_sh) : q / kpc) - 1;
+    if (idx >= a.max_ckpt) return -1;
+    const int32_t id = a.ckpt_ids[(size_t)n * a.max_ckpt + idx];
+    return slot_class(id, a.ck_num_slots) == 0 ? id : -1;
+  };
+  // the four tensor stores of a checkpoint staged by the compute warps (state
+  // columns 0..63 in the Delta tiles, 64..127 in the chunk's [K;Q] tile) as
+  // two bulk groups, the Delta tiles' first
+  auto store_ckpt = [&](int32_t cid, int buf) {
+    const int32_t y = (int32_t)(((int64_t)cid * a.hv + h) * kD);
+    tma_store_2d(&cmap, S.dt, 0, y);
+    tma_store_2d(&cmap, S.dtt, 32, y);
+    bulk_commit();
+    tma_store_2d(&cmap, S.kq[buf], 64, y);
+    tma_store_2d(&cmap, S.kq[buf] + 16384, 96, y);
+    bulk_commit();
+  };
 
   if (warp == kIssueWarp) {
     // Issue warp, one lane: operand loads one chunk ahead; [K;Q] K^T of chunk
@@ -677,7 +730,8 @@ __global__ void __launch_bounds__(kChainThreads, 1) tc_chain_kernel(const TcArgs
         issue_kq(0);
       }
       for (int c = 0; c < nch && ok; ++c) {
-        // O1 of chunk c, after the state entering it reached its image
+        // O1 of chunk c, after the state entering it reached its image (and,
+        // at a checkpoint, was staged for its tensor stores)
         ok = mbar_wait(&S.st_bar, c & 1);
         if (!ok) break;
         umma::fence_after();
@@ -690,7 +744,16 @@ __global__ void __launch_bounds__(kChainThreads, 1) tc_chain_kernel(const TcArgs
         }
         umma::commit(&S.kq_bar);
         kq_issued = c + 1;
+        const int32_t ck_prev = (kTmaStores && c > 0) ? ckpt_slot(c - 1) : -1;
+        if (ck_prev >= 0) {
+          store_ckpt(ck_prev, (c - 1) & 1);
+          // the Delta tiles are free for chunk c's extraction ...
+          bulk_wait_read_1();
+          mbar_arrive(&S.ck_bar);
+        }
         if (c + 1 >= nch) break;
+        // ... and the [K;Q] tile for chunk c + 1's operands
+        if (ck_prev >= 0) bulk_wait_read();
         // chunk c+1 into the buffer of chunk c-1, whose last reader (its state
         // update) finished before st_bar completed
         issue_load(c + 1);
@@ -702,6 +765,15 @@ __global__ void __launch_bounds__(kChainThreads, 1) tc_chain_kernel(const TcArgs
         umma::fence_after();
         issue_kq(c + 1);
       }
+      // the last chunk's checkpoint
+      if (ok && kTmaStores) {
+        const int32_t ck_last = ckpt_slot(nch - 1);
+        if (ck_last >= 0) {
+          ok = mbar_wait(&S.st_bar, nch & 1);
+          if (ok) store_ckpt(ck_last, (nch - 1) & 1);
+        }
+      }
+      if (kTmaStores) bulk_wait_all();
       if (!ok) {
         report(a.err, GDN_DEV_ERR_TIMEOUT);
         // let issued loads and products land before shared memory and TMEM go away
@@ -733,7 +805,8 @@ __global__ void __launch_bounds__(kChainThreads, 1) tc_chain_kernel(const TcArgs
     umma::fence_proxy_async();
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.st_bar);
-    uint32_t mph = 0;
+    uint32_t mph = 0, ckph = 0;
+    bool prev_ck = false;  // the previous chunk wrote a checkpoint
     bool bad = false;  // this thread saw a bounded wait expire
     float* Af = S.ax[0];
     float* Xf = S.ax[1];
@@ -774,6 +847,11 @@ __global__ void __launch_bounds__(kChainThreads, 1) tc_chain_kernel(const TcArgs
       // the copy's completion itself before reading the gates)
       if (!mbar_wait(&S.ld_full[buf], (c >> 1) & 1)) bad = true;
       if (!(alive = cta_wait(&S.kq_bar, c & 1, bad))) break;
+      if (kTmaStores && prev_ck) {
+        // the previous chunk's checkpoint stores have read the Delta tiles
+        if (!(alive = cta_wait(&S.ck_bar, ckph, bad))) break;
+        ckph ^= 1;
+      }
       umma::fence_after();
       const uint32_t kq = smem_addr(S.kq[buf]), vv = smem_addr(S.v[buf]);
       const uint32_t st = smem_addr(S.st);
@@ -823,6 +901,9 @@ __global__ void __launch_bounds__(kChainThreads, 1) tc_chain_kernel(const TcArgs
           }
         }
       }
+      // the previous chunk's output tile (its tensor store's source is the
+      // solve's scratch) has been read
+      if (kTmaStores && tid == 0) bulk_wait_read();
       umma::fence_before();
       compute_sync();
       // T = X diag(beta) and T' = X diag(beta e^b) as bf16 K-major tiles
@@ -946,30 +1027,50 @@ __global__ void __launch_bounds__(kChainThreads, 1) tc_chain_kernel(const TcArgs
         for (int i = 0; i < 32; ++i) ot[(32 * half + i) * kD + lrow] = from_f32<Tact>(fmaf(o1[i], ebr[i], o2[i]));
       }
       umma::store_row64(S.st + half * (128 * 128), lrow, sreg);
-      // checkpoint at a block boundary
-      const int64_t pend = P + kC < p1 ? P + kC : p1;
-      if (pend % a.ckpt_block == 0) {
-        const int64_t idx = pend / a.ckpt_block - p0 / a.ckpt_block - 1;
-        if (idx >= 0 && idx < a.max_ckpt) {
-          const int32_t cid = a.ckpt_ids[(size_t)n * a.max_ckpt + idx];
-          if (slot_class(cid, a.ck_num_slots) == 0) {
-            float* cS = a.ck_ssm + (((size_t)cid * a.hv + h) * kD + lrow) * kD + 64 * half;
+      // checkpoint slot of a block boundary at this chunk's end (-1: none)
+      const int32_t cid = ckpt_slot(c);
+      prev_ck = cid >= 0;
+      if (cid >= 0) {
+        if (kTmaStores) {
+          // the fp32 rows, 128B-swizzled, into four 16 KB boxes (32 columns x
+          // 128 rows): columns 0..63 in the Delta tiles, 64..127 in chunk c's
+          // [K;Q] tile, both dead now; the issue warp writes them out with
+          // four tensor stores after st_bar (instead of 512-byte-strided row
+          // stores) and holds both tiles until the stores have read them
+          uint8_t* box = half ? S.kq[buf] : S.dt;
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              *reinterpret_cast<float4*>(cS + 4 * i) =
-                  make_float4(sreg[4 * i], sreg[4 * i + 1], sreg[4 * i + 2], sreg[4 * i + 3]);
-          }
+          for (int bl = 0; bl < 2; ++bl)
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              *reinterpret_cast<float4*>(box + bl * 16384 + lrow * 128 + ((j ^ (lrow & 7)) << 4)) =
+                  make_float4(sreg[32 * bl + 4 * j], sreg[32 * bl + 4 * j + 1], sreg[32 * bl + 4 * j + 2],
+                              sreg[32 * bl + 4 * j + 3]);
+        } else {
+          float* cS = a.ck_ssm + (((size_t)cid * a.hv + h) * kD + lrow) * kD + 64 * half;
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            *reinterpret_cast<float4*>(cS + 4 * i) =
+                make_float4(sreg[4 * i], sreg[4 * i + 1], sreg[4 * i + 2], sreg[4 * i + 3]);
         }
       }
-      // state image written, O1 read: the issue warp may start chunk c + 1's O1
+      // state image (and checkpoint) written, O1 read: the issue warp may
+      // start chunk c + 1's O1
       umma::fence_proxy_async();
       umma::fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.st_bar);
       compute_sync();
-      // output rows of the chunk's tokens: 16-byte stores of whole rows (the
-      // staging tile is next written after the following chunk's first barrier)
-      {
+      // a chunk inside the sequence leaves as one tensor store of its staged
+      // 64 x 128 output tile
+      const bool full = P >= p0 && P + kC <= p1;
+      if (kTmaStores && full && tid == 0) {
+        tma_store_2d(&omap, S.wt, h * kD, (int32_t)(t0 + (P - p0)));
+        bulk_commit();
+      }
+      // otherwise output rows of the chunk's tokens: 16-byte stores of whole
+      // rows (the staging tile is next written after the following chunk's
+      // first barrier)
+      if (!(kTmaStores && full)) {
         constexpr int EPC = 16 / sizeof(Tact), CPR = kD / EPC;
         const Tact* ot = reinterpret_cast<const Tact*>(S.wt);
         for (int e = tid; e < kC * CPR; e += kTh) {
@@ -990,6 +1091,8 @@ __global__ void __launch_bounds__(kChainThreads, 1) tc_chain_kernel(const TcArgs
             make_float4(sreg[4 * i], sreg[4 * i + 1], sreg[4 * i + 2], sreg[4 * i + 3]);
     }
   }
+  // the tensor stores have landed before the CTA's shared memory goes away
+  if (kTmaStores && tid == 0) bulk_wait_all();
   umma::fence_before();
   __syncthreads();
   if (warp == 0) umma::tmem_dealloc(tmem, TM_COLS);
@@ -1041,17 +1144,20 @@ static EncodeTiledFn encode_tiled() {
   return fn;
 }
 
-static cudaError_t qkv_tensor_map(CUtensorMap* map, const void* qkv, int64_t total, int32_t C, size_t esz) {
+// A row-major 2D tensor [rows][cols] of 2- or 4-byte elements, copied in
+// boxes of box_cols x box_rows.
+static cudaError_t tensor_map_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, size_t esz,
+                                 uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swz) {
   const EncodeTiledFn enc = encode_tiled();
   if (!enc) return cudaErrorNotSupported;
-  const cuuint64_t dim[2] = {(cuuint64_t)C, (cuuint64_t)(total > 0 ? total : 1)};
-  const cuuint64_t stride[1] = {(cuuint64_t)C * esz};
-  const cuuint32_t box[2] = {(cuuint32_t)kD, (cuuint32_t)kTileRows};
+  const cuuint64_t dim[2] = {(cuuint64_t)cols, (cuuint64_t)(rows > 0 ? rows : 1)};
+  const cuuint64_t stride[1] = {(cuuint64_t)cols * esz};
+  const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estride[2] = {1, 1};
   const CUresult r =
       enc(map, esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
-          const_cast<void*>(qkv), dim, stride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+          const_cast<void*>(base), dim, stride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
@@ -1076,15 +1182,31 @@ static cudaError_t launch_tc_t(const TcArgs& a, cudaStream_t s) {
   const size_t fsm = features_smem(a.G, sizeof(Tact));
   if ((e = cudaFuncSetAttribute(fk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsm)) != cudaSuccess)
     return e;
+  // qkv [total][C], boxes of 128 channels x 67 rows
   CUtensorMap qmap;
-  if ((e = qkv_tensor_map(&qmap, a.qkv, a.total, a.C, sizeof(Tact))) != cudaSuccess) return e;
+  if ((e = tensor_map_2d(&qmap, a.qkv, a.total, a.C, sizeof(Tact), kD, kTileRows, CU_TENSOR_MAP_SWIZZLE_NONE)) !=
+      cudaSuccess)
+    return e;
   e = launch_plain(fk, dim3((unsigned)a.n_chunks_max, (unsigned)a.hk), dim3(kTh), fsm, s, dim3(1), a, qmap);
   if (e != cudaSuccess) return e;
   auto ck = tc_chain_kernel<Tact>;
   const size_t csm = sizeof(ChainSmem) + 1024;
   if ((e = cudaFuncSetAttribute(ck, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csm)) != cudaSuccess)
     return e;
-  return launch_plain(ck, dim3((unsigned)a.hv, (unsigned)a.n_seq), dim3(kChainThreads), csm, s, dim3(1), a);
+  // out [total][hv * 128] in boxes of one V head x 64 tokens; checkpoint
+  // states [slots * hv * 128 rows][128] fp32 in 128B-swizzled boxes of 32 x 128
+  // (over the working pool when there is no checkpoint pool: never used then)
+  CUtensorMap omap, cmap;
+  if ((e = tensor_map_2d(&omap, a.out, a.total, (int64_t)a.hv * kD, sizeof(Tact), kD, kC,
+                         CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
+    return e;
+  const bool has_ck = a.ck_ssm != nullptr && a.ck_num_slots > 0;
+  if ((e = tensor_map_2d(&cmap, has_ck ? a.ck_ssm : a.ssm,
+                         (int64_t)(has_ck ? a.ck_num_slots : a.num_slots) * a.hv * kD, kD, 4, 32, kD,
+                         CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+    return e;
+  return launch_plain(ck, dim3((unsigned)a.hv, (unsigned)a.n_seq), dim3(kChainThreads), csm, s, dim3(1), a, omap,
+                      cmap);
 }
 
 cudaError_t prefill_tc_launch(const gdn_dims& d, const gdn_pool& pool, const gdn_pool& ckpt,
