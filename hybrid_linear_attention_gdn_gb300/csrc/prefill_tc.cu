@@ -20,14 +20,15 @@
 //             lane, 64 columns per thread); a bf16 copy in shared memory is the
 //             MMA operand.  Per chunk (transposed so that M = 128 throughout):
 //               [K;Q] K^T             -> K K^T (A), Q K^T (masked, decayed)
+//               S^T [K;Q]^T           -> S^T K^T, O1 = S^T Q^T (before T)
 //               T = (I + A)^-1 diag(beta)   (fp32, CUDA cores, blocked)
-//               U^T = V^T T^T,  W^T = K^T (T diag(e^b))^T
-//               P = S^T W^T,  O1 = S^T Q^T
-//               Delta^T = U^T - P
+//               Delta^T = (V^T - S^T K^T diag(e^b)) T^T
+//                 (the WY form's U - W S with W = T diag(e^b) K, regrouped
+//                 so that only T-free operands meet the state)
 //               D2 = (Delta^T diag(e^{b_last - b})) K,  O2 = Delta^T (QK^T (.) Gamma)^T
 //               S^T <- e^{b_last} S^T + D2,  O = O1 diag(e^b) + O2
 //             Every product is one tcgen05.mma chain (bf16 in, fp32 TMEM
-//             accumulators; 7 groups, 40 MMA instructions per chunk), issued
+//             accumulators; 6 groups, 32 MMA instructions per chunk), issued
 //             by one thread and completed through tcgen05.commit -> mbarrier.
 //   The conv histories of checkpoints and of the final state come from the
 //   history kernel of prefill.cu.
@@ -46,11 +47,11 @@ constexpr uint32_t kKQBytes = 2 * 128 * 128;  // [K;Q] image: 2 blocks x 128 row
 constexpr uint32_t kVBytes = 2 * 64 * 128;    // V image: 2 atoms x 64 rows x 128 B
 constexpr uint32_t kGateBytes = 2 * kC * 4;   // g[64], beta[64]
 
-// TMEM columns.  [K;Q] K^T is double-buffered by chunk parity (TM_KQ + 192
+// TMEM columns.  [K;Q] K^T is double-buffered by chunk parity (TM_KQ + 64
 // for odd chunks, so the next chunk's product can run while this one is
-// read); P reuses W's columns (W is converted to bf16 before P is computed).
-constexpr uint32_t TM_KQ = 0, TM_U = 64, TM_W = 128, TM_P = 128, TM_KQ_ODD = 192, TM_O1 = 256, TM_O2 = 320,
-                   TM_D2 = 384, TM_COLS = 512;
+// read); S^T [K;Q]^T is one 128-column product: S^T K^T, then O1 = S^T Q^T.
+constexpr uint32_t TM_KQ = 0, TM_KQ_ODD = 64, TM_SK = 128, TM_O1 = 192, TM_DL = 256, TM_O2 = 320, TM_D2 = 384,
+                   TM_COLS = 512;
 __host__ __device__ constexpr uint32_t tm_kq(int c) { return (c & 1) ? TM_KQ_ODD : TM_KQ; }
 
 struct TcArgs {
@@ -374,7 +375,7 @@ struct __align__(1024) ChainSmem {
   uint8_t kq[2][kKQBytes];
   uint8_t v[2][kVBytes];
   uint8_t st[2 * 128 * 128];  // S^T bf16 operand (K-major, 2 blocks of 64 dk)
-  uint8_t wt[128 * 128];      // W^T (MN-major B: 128 dk rows x 64 tokens); solve scratch
+  uint8_t wt[128 * 128];      // solve scratch; -S^T K^T diag(e^b) (K-major A); O staging
   union {
     struct {
       uint8_t dt[128 * 128];   // Delta^T (K-major A: 128 dv rows x 64 tokens)
@@ -383,12 +384,11 @@ struct __align__(1024) ChainSmem {
     float ax[2][64 * kAXStride];  // A and X (fp32) in the solve
   };
   uint8_t tm[64 * 128];       // T (K-major B: 64 rows x 64)
-  uint8_t tp[64 * 128];       // T diag(e^b)
   uint8_t qk[64 * 128];       // QK^T (.) Gamma (.) lower-incl
   float gates[2][2][kC];
   float b[2][kC], eb[2][kC], ebl[2][kC];  // by chunk parity
   uint64_t ld_full[2], mma_bar, kq_bar;
-  uint64_t p_bar;    // P of the current chunk complete (its [K;Q] K^T buffer long read)
+  uint64_t p_bar;    // Delta of the current chunk complete (its [K;Q] K^T buffer long read)
   uint64_t st_bar;   // compute warps wrote the state image and read O1 (one arrival per warp)
   uint64_t ck_bar;   // a checkpoint's tensor stores have read the Delta tiles
   uint32_t tmem_base;
@@ -459,24 +459,17 @@ __device__ __forceinline__ uint32_t t_off(int r, int c) {
 
 struct TOut {
   uint8_t* tm;        // T = X diag(beta)
-  uint8_t* tp;        // T' = X diag(beta e^b)
   const float* beta;  // [64]
-  const float* eb;    // [64]
 };
 
-// T and T' entries (r, c), (r, c + 1) (c even) as bf16 pairs; bc/ec are
-// beta and e^b of the two columns (loaded once per lane by the caller)
-__device__ __forceinline__ void put_t_pair(const TOut& o, int r, int c, float x0, float x1, const float2& bc,
-                                           const float2& ec) {
-  const float t0 = x0 * bc.x, t1 = x1 * bc.y;
-  const uint32_t off = t_off(r, c);
-  *reinterpret_cast<__nv_bfloat162*>(o.tm + off) = __floats2bfloat162_rn(t0, t1);
-  *reinterpret_cast<__nv_bfloat162*>(o.tp + off) = __floats2bfloat162_rn(t0 * ec.x, t1 * ec.y);
+// T entries (r, c), (r, c + 1) (c even) as a bf16 pair; bc is beta of the
+// two columns (loaded once per lane by the caller)
+__device__ __forceinline__ void put_t_pair(const TOut& o, int r, int c, float x0, float x1, const float2& bc) {
+  *reinterpret_cast<__nv_bfloat162*>(o.tm + t_off(r, c)) = __floats2bfloat162_rn(x0 * bc.x, x1 * bc.y);
 }
 
 // X = (I + A)^-1 for the 64 x 64 strictly lower A (fp32), written out as the
-// lower triangles of T = X diag(beta) and T' = X diag(beta e^b) (their upper
-// triangles stay zero).  8 x 8 diagonal blocks by substitution, then merged
+// lower triangle of T = X diag(beta) (its upper triangle stays zero).  8 x 8 diagonal blocks by substitution, then merged
 // 8 -> 16 -> 32 -> 64 with X_ba = -X_b (A_ba X_a), the products on warp-level
 // tf32 MMAs (T is rounded to bf16 afterwards, far coarser than tf32).  Each
 // output column tile j of X_ba needs only column tile j of A_ba X_a, so a warp
@@ -490,7 +483,7 @@ __device__ __forceinline__ void solve_T(const float* A, float* X, float* Y, cons
   const int g = lane >> 2, t = lane & 3;
   // 8 x 8 diagonal blocks: warp w, lane l < 4 = columns 2l and 2l+1 of block
   // w (two independent substitutions), written as fp32 pairs to X and bf16
-  // pairs to T and T'
+  // pairs to T
   if (lane < 4) {
     const int o = 8 * warp, c0 = 2 * lane;
     float a[28];
@@ -499,7 +492,6 @@ __device__ __forceinline__ void solve_T(const float* A, float* X, float* Y, cons
 #pragma unroll
       for (int m = 0; m < r; ++m, ++i) a[i] = A[ix(o + r, o + m)];
     const float2 bc = make_float2(to.beta[o + c0], to.beta[o + c0 + 1]);
-    const float2 ec = make_float2(to.eb[o + c0], to.eb[o + c0 + 1]);
     float x0[8], x1[8];
 #pragma unroll
     for (int r = 0, i = 0; r < 8; ++r) {
@@ -516,7 +508,7 @@ __device__ __forceinline__ void solve_T(const float* A, float* X, float* Y, cons
     for (int r = 0; r < 8; ++r)
       if (r >= c0) {
         *reinterpret_cast<float2*>(X + ix(o + r, o + c0)) = make_float2(x0[r], x1[r]);
-        put_t_pair(to, o + r, o + c0, x0[r], x1[r], bc, ec);
+        put_t_pair(to, o + r, o + c0, x0[r], x1[r], bc);
       }
   }
   compute_sync();
@@ -529,7 +521,6 @@ __device__ __forceinline__ void solve_T(const float* A, float* X, float* Y, cons
     frag_b(fb[0], 0, [&](int k, int c) { return k >= c ? X[ix(o + k, o + c)] : 0.f; });
     frag_a(fx[0], 0, [&](int r, int k) { return (r < 8 && k <= r) ? X[ix(o + 8 + r, o + 8 + k)] : 0.f; });
     const float2 bc = make_float2(to.beta[o + 2 * t], to.beta[o + 2 * t + 1]);
-    const float2 ec = make_float2(to.eb[o + 2 * t], to.eb[o + 2 * t + 1]);
     float d[4];
     tile_mm<1>(d, fa, fb);
     Ys[g * 8 + 2 * t] = d[0];
@@ -539,7 +530,7 @@ __device__ __forceinline__ void solve_T(const float* A, float* X, float* Y, cons
     tile_mm<1>(d, fx, fy);
     X[ix(o + 8 + g, o + 2 * t)] = -d[0];
     X[ix(o + 8 + g, o + 2 * t + 1)] = -d[1];
-    put_t_pair(to, o + 8 + g, o + 2 * t, -d[0], -d[1], bc, ec);
+    put_t_pair(to, o + 8 + g, o + 2 * t, -d[0], -d[1], bc);
   }
   compute_sync();
   // 16 -> 32: warps 0..3 = (pair q, column tile j)
@@ -555,7 +546,6 @@ __device__ __forceinline__ void solve_T(const float* A, float* X, float* Y, cons
     }
     const int cc = o + 8 * j + 2 * t;
     const float2 bc = make_float2(to.beta[cc], to.beta[cc + 1]);
-    const float2 ec = make_float2(to.eb[cc], to.eb[cc + 1]);
     float d[4];
     tile_mm<2>(d, fa, fb);
     Ys[g * 8 + 2 * t] = d[0];
@@ -570,8 +560,8 @@ __device__ __forceinline__ void solve_T(const float* A, float* X, float* Y, cons
     X[ix(o + 16 + g, cc + 1)] = -d[1];
     X[ix(o + 24 + g, cc)] = -d[2];
     X[ix(o + 24 + g, cc + 1)] = -d[3];
-    put_t_pair(to, o + 16 + g, cc, -d[0], -d[1], bc, ec);
-    put_t_pair(to, o + 24 + g, cc, -d[2], -d[3], bc, ec);
+    put_t_pair(to, o + 16 + g, cc, -d[0], -d[1], bc);
+    put_t_pair(to, o + 24 + g, cc, -d[2], -d[3], bc);
   }
   compute_sync();
   // 32 -> 64: warps = (column tile j, row half mh); the two warps of a column
@@ -594,7 +584,6 @@ __device__ __forceinline__ void solve_T(const float* A, float* X, float* Y, cons
     }
     const int cc = 8 * j + 2 * t;
     const float2 bc = make_float2(to.beta[cc], to.beta[cc + 1]);
-    const float2 ec = make_float2(to.eb[cc], to.eb[cc + 1]);
     float d[4];
     tile_mm<4>(d, fa, fb);
     const int yr = 16 * mh + g;
@@ -606,8 +595,8 @@ __device__ __forceinline__ void solve_T(const float* A, float* X, float* Y, cons
 #pragma unroll
     for (int s = 0; s < 4; ++s) frag_b(fy[s], 8 * s, [&](int k, int c) { return Ys[k * 8 + c]; });
     tile_mm<4>(d, fx, fy);
-    put_t_pair(to, 32 + yr, cc, -d[0], -d[1], bc, ec);
-    put_t_pair(to, 40 + yr, cc, -d[2], -d[3], bc, ec);
+    put_t_pair(to, 32 + yr, cc, -d[0], -d[1], bc);
+    put_t_pair(to, 40 + yr, cc, -d[2], -d[3], bc);
   }
 }
 
@@ -661,8 +650,8 @@ __global__ void __launch_bounds__(kChainThreads, 1)
 
   constexpr uint32_t ID_64_KK = umma::idesc_bf16(128, 64, false, false);
   constexpr uint32_t ID_64_MK = umma::idesc_bf16(128, 64, true, false);
-  constexpr uint32_t ID_64_KM = umma::idesc_bf16(128, 64, false, true);
   constexpr uint32_t ID_128_KM = umma::idesc_bf16(128, 128, false, true);
+  constexpr uint32_t ID_128_KK = umma::idesc_bf16(128, 128, false, false);
   // bf16 outputs: the output tiles and checkpoints leave by TMA tensor stores
   // (fp32 outputs stage 32 KB, which overlaps the checkpoint boxes)
   constexpr bool kTmaStores = sizeof(Tact) == 2;
@@ -701,10 +690,11 @@ __global__ void __launch_bounds__(kChainThreads, 1)
 
   if (warp == kIssueWarp) {
     // Issue warp, one lane: operand loads one chunk ahead; [K;Q] K^T of chunk
-    // c + 1 into its TMEM buffer once chunk c's P is done (it runs on the
-    // tensor core during chunk c's Delta, which uses no tensor core) and O1 =
-    // S^T Q^T of chunk c + 1 once the state leaving chunk c is in its image (it
-    // runs under chunk c's output stores); each chunk's pair completes on kq_bar.
+    // c + 1 into its TMEM buffer once chunk c's Delta products are done (it
+    // runs on the tensor core during chunk c's Delta conversion, which uses no
+    // tensor core) and S^T [K;Q]^T of chunk c + 1 once the state leaving
+    // chunk c is in its image (it runs under chunk c's output stores); each
+    // chunk's pair completes on kq_bar.
     if (lane == 0 && nch > 0) {
       auto issue_load = [&](int c) {
         const int gc = gc0 + c, buf = c & 1;
@@ -735,12 +725,13 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         ok = mbar_wait(&S.st_bar, c & 1);
         if (!ok) break;
         umma::fence_after();
-        const uint64_t dq = umma::desc(smem_addr(S.kq[c & 1]) + 8192, 16, 1024);
+        // S^T [K;Q]^T: S^T K^T (for this chunk's Delta) and O1 = S^T Q^T
+        const uint64_t dkq = umma::desc(smem_addr(S.kq[c & 1]), 16, 1024);
         const uint64_t dst = umma::desc(smem_addr(S.st), 16, 1024);
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
           const uint32_t ko = (s >> 2) * 16384 + (s & 3) * 32;
-          umma::mma_bf16(tmem + TM_O1, umma::adv(dst, ko), umma::adv(dq, ko), ID_64_KK, s > 0);
+          umma::mma_bf16(tmem + TM_SK, umma::adv(dst, ko), umma::adv(dkq, ko), ID_128_KK, s > 0);
         }
         umma::commit(&S.kq_bar);
         kq_issued = c + 1;
@@ -758,7 +749,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         // update) finished before st_bar completed
         issue_load(c + 1);
         issued = c + 2;
-        // [K;Q] K^T of chunk c + 1, after chunk c's P (its TMEM buffer was last
+        // [K;Q] K^T of chunk c + 1, after chunk c's Delta (its TMEM buffer was last
         // read by chunk c - 1's extraction)
         ok = mbar_wait(&S.p_bar, c & 1) && mbar_wait(&S.ld_full[(c + 1) & 1], ((c + 1) >> 1) & 1);
         if (!ok) break;
@@ -796,9 +787,8 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       sreg[4 * i + 3] = v.w;
     }
     umma::store_row64(S.st + half * (128 * 128), lrow, sreg);
-    // T and T' are lower triangular: their upper triangles are written only here
-    for (int e = tid; e < 2 * 64 * 128 / 16; e += kTh)
-      reinterpret_cast<uint4*>(e < 512 ? S.tm : S.tp)[e & 511] = make_uint4(0u, 0u, 0u, 0u);
+    // T is lower triangular: its upper triangle is written only here
+    for (int e = tid; e < 64 * 128 / 16; e += kTh) reinterpret_cast<uint4*>(S.tm)[e] = make_uint4(0u, 0u, 0u, 0u);
 
     // the state image and the T tiles reach the tensor core's proxy; then
     // the issue warp may read the image
@@ -906,66 +896,64 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       if (kTmaStores && tid == 0) bulk_wait_read();
       umma::fence_before();
       compute_sync();
-      // T = X diag(beta) and T' = X diag(beta e^b) as bf16 K-major tiles
-      solve_T(Af, Xf, Yf, TOut{S.tm, S.tp, S.gates[buf][1], eb});
+      // T = X diag(beta) as a bf16 K-major tile
+      solve_T(Af, Xf, Yf, TOut{S.tm, S.gates[buf][1]});
       umma::fence_proxy_async();
       compute_sync();
-      // U^T = V^T T^T ; W^T = K^T T'^T
+      // Delta^T = (V^T - S^T K^T diag(e^b)) T^T, as two products into one
+      // accumulator: V^T T^T now, and (-S^T K^T diag(e^b)) T^T once its bf16
+      // K-major image (128 dv rows x 64 tokens, in the solve's scratch tile)
+      // is written; S^T K^T came with O1
       if (tid == 0) {
         umma::fence_after();
-        const uint64_t dv = umma::desc(vv, 64 * 128, 1024), dkm = umma::desc(kq, 16384, 1024);
-        const uint64_t dtm = umma::desc(smem_addr(S.tm), 16, 1024), dtp = umma::desc(smem_addr(S.tp), 16, 1024);
+        const uint64_t dv = umma::desc(vv, 64 * 128, 1024), dtm = umma::desc(smem_addr(S.tm), 16, 1024);
 #pragma unroll
         for (int s = 0; s < 4; ++s)
-          umma::mma_bf16(tmem + TM_U, umma::adv(dv, s * 2048), umma::adv(dtm, s * 32), ID_64_MK, s > 0);
-#pragma unroll
-        for (int s = 0; s < 4; ++s)
-          umma::mma_bf16(tmem + TM_W, umma::adv(dkm, s * 2048), umma::adv(dtp, s * 32), ID_64_MK, s > 0);
-        umma::commit(&S.mma_bar);
+          umma::mma_bf16(tmem + TM_DL, umma::adv(dv, s * 2048), umma::adv(dtm, s * 32), ID_64_MK, s > 0);
       }
-      if (!(alive = cta_wait(&S.mma_bar, mph, bad))) break;
-      mph ^= 1;
-      umma::fence_after();
-      // W^T -> bf16 MN-major B tile (row = dk, 64 tokens)
       {
         float v[32];
-        umma::tmem_ld32(tlane + TM_W + 32 * half, v);
+        umma::tmem_ld32(tlane + TM_SK + 32 * half, v);
+        float e[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 e4 = *reinterpret_cast<const float4*>(eb + 32 * half + 4 * i);
+          e[4 * i] = e4.x;
+          e[4 * i + 1] = e4.y;
+          e[4 * i + 2] = e4.z;
+          e[4 * i + 3] = e4.w;
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = -v[i] * e[i];
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
           const int cch = 4 * half + ch;
-          *reinterpret_cast<uint4*>(S.wt + (lrow >> 3) * 1024 + (lrow & 7) * 128 +
-                                    ((cch ^ (lrow & 7)) << 4)) = umma::pack8_bf16(v + 8 * ch);
+          *reinterpret_cast<uint4*>(S.wt + (lrow >> 3) * 1024 + (lrow & 7) * 128 + ((cch ^ (lrow & 7)) << 4)) =
+              umma::pack8_bf16(v + 8 * ch);
         }
       }
       umma::fence_proxy_async();
       umma::fence_before();
       compute_sync();
-      // P = S^T W^T
       if (tid == 0) {
         umma::fence_after();
-        const uint64_t dst = umma::desc(st, 16, 1024), dwt = umma::desc(smem_addr(S.wt), 0, 1024);
+        const uint64_t dsk = umma::desc(smem_addr(S.wt), 16, 1024), dtm = umma::desc(smem_addr(S.tm), 16, 1024);
 #pragma unroll
-        for (int s = 0; s < 8; ++s) {
-          const uint32_t ko = (s >> 2) * 16384 + (s & 3) * 32;
-          umma::mma_bf16(tmem + TM_P, umma::adv(dst, ko), umma::adv(dwt, s * 2048), ID_64_KM, s > 0);
-        }
+        for (int s = 0; s < 4; ++s)
+          umma::mma_bf16(tmem + TM_DL, umma::adv(dsk, s * 32), umma::adv(dtm, s * 32), ID_64_KK, true);
         umma::commit(&S.mma_bar);
         umma::commit(&S.p_bar);
       }
       if (!(alive = cta_wait(&S.mma_bar, mph, bad))) break;
       mph ^= 1;
       umma::fence_after();
-      // Delta^T = U^T - P, and its columns scaled by e^{b_last - b}
+      // Delta^T to bf16, and its columns scaled by e^{b_last - b}
       {
         const float* ebl = S.ebl[buf];
-        float u[32], p[32], d[32], dd[32];
-        umma::tmem_ld32(tlane + TM_U + 32 * half, u);
-        umma::tmem_ld32(tlane + TM_P + 32 * half, p);
+        float d[32], dd[32];
+        umma::tmem_ld32(tlane + TM_DL + 32 * half, d);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          d[i] = u[i] - p[i];
-          dd[i] = d[i] * ebl[32 * half + i];
-        }
+        for (int i = 0; i < 32; ++i) dd[i] = d[i] * ebl[32 * half + i];
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
           const int cch = 4 * half + ch;
@@ -1021,7 +1009,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
           ebr[4 * i + 2] = e4.z;
           ebr[4 * i + 3] = e4.w;
         }
-        // stage O as [token][dv] in the (now free) W^T tile
+        // stage O as [token][dv] in the (now free) scratch tile
         Tact* ot = reinterpret_cast<Tact*>(S.wt);
 #pragma unroll
         for (int i = 0; i < 32; ++i) ot[(32 * half + i) * kD + lrow] = from_f32<Tact>(fmaf(o1[i], ebr[i], o2[i]));

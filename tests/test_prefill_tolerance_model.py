@@ -4,8 +4,8 @@ The workload fixes the intra-chunk WY/UT contractions of the chunked prefill
 as bf16 products with fp32 accumulation.  This model evaluates the chunk form
 (the Gated DeltaNet chunkwise WY/UT form, Yang et al., NeurIPS 2024, with the
 gated decay) in float64 twice on the workload's distributions: exactly, and
-with every contraction operand rounded to bf16 (q^, k^, v, T, the decayed T,
-W, S, the masked Q K^T, Delta) and the output rounded to bf16.  The gap between
+with every contraction operand rounded to bf16 (q^, k^, v, T, S, the decayed
+K S^T, the masked Q K^T, Delta) and the output rounded to bf16.  The gap between
 the two is the error that bf16 operands alone cause; the GPU bounds in
 tests/helpers.py sit above it:
 
@@ -62,10 +62,12 @@ def _chunk_form(q, k, v, g, beta, S, rounded, ckpt_every=256, C=64):
         A = be[:, None] * (K @ K.T) * gam * low
         X = np.linalg.inv(np.eye(n) + A)
         T = X * be[None, :]
-        U = r(T) @ V
-        Wm = r(T * np.exp(bcum)[None, :]) @ K
+        # Delta = T V - T (diag(e^b) K S^T): the state-dependent operand is
+        # formed before T is known (K S^T from the bf16 state image, scaled
+        # by e^b and rounded), both products accumulate in fp32
         Sb = r(S)
-        D = U - r(Wm) @ Sb.T
+        E = r(np.exp(bcum)[:, None] * (K @ Sb.T))
+        D = r(T) @ V - r(T) @ E
         QK = (Q @ K.T) * gam
         out[sl] = np.exp(bcum)[:, None] * (Q @ Sb.T) + r(QK) @ r(D)
         S = np.exp(bcum[-1]) * S + r(D * np.exp(bcum[-1] - bcum)[:, None]).T @ K
