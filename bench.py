@@ -600,7 +600,44 @@ def measure_rows(gdn, synth, dev, stream, hbm_peak, bf16_peak, which="all", pref
         "workspace_bytes": wsb}
     del qkv, a, b, pout, wsp
     torch.cuda.synchronize()
+    if full:
+        rows["mixed_b64_plus_4x256"] = _mixed_row(gdn, synth, dims, pool, params, perm, g, dev, stream)
     return rows
+
+
+def _mixed_row(gdn, synth, dims, pool, params, perm, g, dev, stream):
+    """Decode-first mixed batch: 64 decode tokens plus 4 continuations of 256
+    tokens from unaligned prefixes, through gdn_mixed_step; beside it the same
+    batch sent whole through the chunked prefill (decode rows as 1-token
+    sequences)."""
+    import torch
+    shape = synth.QWEN
+    n_dec, L, starts = 64, 256, [1000, 3077, 517, 8191]
+    lens = [1] * n_dec + [L] * 4
+    n = len(lens)
+    total = sum(lens)
+    cu = torch.tensor([0] + list(torch.tensor(lens).cumsum(0).tolist()), dtype=torch.int32, device=dev)
+    sp = torch.tensor([4096 + 7 * i for i in range(n_dec)] + starts, dtype=torch.int64, device=dev)
+    sets = [perm[k * n:(k + 1) * n].to(dev) for k in range(2 if perm.numel() >= 2 * n else 1)]
+    qkv, a, b = (t.to(dev) for t in synth.tokens(shape, g, (total,)))
+    out = torch.empty((total, shape.hv, shape.dv), dtype=torch.bfloat16, device=dev)
+    ck = gdn.StatePool.empty(dims, 2 * n, dev)
+    ck_ids = torch.arange(2 * n, dtype=torch.int32, device=dev).reshape(n, 2)
+    ws = torch.empty(gdn.chunk_prefill_workspace_size(dims, n, total), dtype=torch.uint8, device=dev)
+
+    def fm(i):
+        gdn.mixed_step(dims, pool, ck, params, sets[i % len(sets)], cu, sp, total, n_dec, ck_ids, 256, qkv, a, b,
+                       out, ws)
+
+    def fp(i):
+        gdn.chunk_prefill(dims, pool, ck, params, sets[i % len(sets)], cu, sp, total, ck_ids, 256, qkv, a, b, out,
+                          ws)
+    fm(0)
+    fp(0)
+    ms_m = _events_time(fm, 20, stream)
+    ms_p = _events_time(fp, 20, stream)
+    return {"ms": ms_m, "tokens_per_s": total / (ms_m * 1e-3), "ms_all_through_prefill": ms_p,
+            "batch": f"{n_dec} decode + 4 x {L} continuation tokens"}
 
 
 def main():

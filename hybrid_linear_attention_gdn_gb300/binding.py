@@ -67,6 +67,8 @@ EXPORTS = {
                            _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P], _I32),
     "gdn_chunk_prefill_noalloc": ([_PD, CPool, CPool, _PP, _P, _P, _P, _I32, _I64, _P, _I32,
                                    _I32, _P, _P, _P, _P, _P, _P], _I32),
+    "gdn_mixed_step": ([_PD, CPool, CPool, _PP, _P, _P, _P, _I32, _I32, _I64, _P, _I32, _I32, _P, _P,
+                        _P, _P, _P, ctypes.c_size_t, _P, _P], _I32),
     "gdn_slot_copy": ([_PD, CPool, CPool, _P, _P, _I32, _P, _P], _I32),
     "gdn_slot_zero": ([_PD, CPool, _P, _I32, _P, _P], _I32),
     "gdn_spec_commit_index": ([_P, _P, _P, _P, _I32, _I32, _P, _P], _I32),
@@ -275,6 +277,24 @@ def chunk_prefill_noalloc(dims: Dims, pool: StatePool, ckpt: StatePool, params: 
                                      _ptr(qkv), _ptr(a), _ptr(b), _ptr(out), _ptr(dev_err),
                                      _stream(stream))
     _check("gdn_chunk_prefill_noalloc", st)
+
+
+def mixed_step(dims: Dims, pool: StatePool, ckpt: StatePool, params: LayerParams, slot_ids,
+               cu_seqlens, start_pos, total_tokens: int, n_decode: int, ckpt_ids, ckpt_block: int,
+               qkv, a, b, out, workspace, dev_err=None, stream=None):
+    """Decode-first mixed batch: sequences 0 .. n_decode-1 are single-token
+    decode requests on rows 0 .. n_decode-1, the rest chunked-prefill
+    continuations at their cu_seqlens offsets."""
+    L = load()
+    n_seq = int(slot_ids.shape[0])
+    max_ckpt = int(ckpt_ids.shape[1]) if ckpt_ids is not None and ckpt_ids.dim() == 2 else 0
+    cd, cp = dims.c(), params.c()
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = L.gdn_mixed_step(ctypes.byref(cd), pool.c(), ckpt.c(), ctypes.byref(cp), _ptr(slot_ids),
+                          _ptr(cu_seqlens), _ptr(start_pos), n_seq, int(n_decode), int(total_tokens),
+                          _ptr(ckpt_ids), max_ckpt, int(ckpt_block), _ptr(qkv), _ptr(a), _ptr(b),
+                          _ptr(out), _ptr(workspace), ws_bytes, _ptr(dev_err), _stream(stream))
+    _check("gdn_mixed_step", st)
 
 
 def slot_copy(dims: Dims, src: StatePool, dst: StatePool, src_ids, dst_ids, dev_err=None,

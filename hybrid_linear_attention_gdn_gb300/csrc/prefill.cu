@@ -507,14 +507,14 @@ extern "C" size_t gdn_chunk_prefill_workspace_size(const gdn_dims* dims, int32_t
   return total_tokens == 0 ? 0 : (v1 > tc ? v1 : tc);
 }
 
-extern "C" gdn_status gdn_chunk_prefill(const gdn_dims* dims, gdn_pool pool, gdn_pool ckpt,
-                                        const gdn_params* params, const int32_t* slot_ids,
-                                        const int32_t* cu_seqlens, const int64_t* start_pos,
-                                        int32_t n_seq, int64_t total_tokens,
-                                        const int32_t* ckpt_ids, int32_t max_ckpt,
-                                        int32_t ckpt_block, const void* qkv, const void* a,
-                                        const void* b, void* out, void* workspace,
-                                        size_t workspace_bytes, uint32_t* dev_err, void* stream) {
+// The chunked prefill: host-side checks, then (launch = true) the kernels.
+static gdn_status chunk_prefill_impl(bool launch, const gdn_dims* dims, gdn_pool pool, gdn_pool ckpt,
+                                     const gdn_params* params, const int32_t* slot_ids,
+                                     const int32_t* cu_seqlens, const int64_t* start_pos, int32_t n_seq,
+                                     int64_t total_tokens, const int32_t* ckpt_ids, int32_t max_ckpt,
+                                     int32_t ckpt_block, const void* qkv, const void* a, const void* b,
+                                     void* out, void* workspace, size_t workspace_bytes, uint32_t* dev_err,
+                                     void* stream) {
   using namespace gdn;
   gdn_status st = check_dims(dims);
   if (st != GDN_OK) return st;
@@ -535,6 +535,7 @@ extern "C" gdn_status gdn_chunk_prefill(const gdn_dims* dims, gdn_pool pool, gdn
   if (total_tokens > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
     return GDN_ERR_INVALID_ARG;
   if (dims->hv / dims->hk * dims->dv + 2 * dims->dk > 4096) return GDN_ERR_UNSUPPORTED;
+  if (!launch) return GDN_OK;
   PrefillArgs p = {};
   p.ssm = pool.ssm;
   p.conv = pool.conv;
@@ -588,6 +589,57 @@ extern "C" gdn_status gdn_chunk_prefill(const gdn_dims* dims, gdn_pool pool, gdn
   }
   if (e == cudaSuccess) count_launch(GDN_K_PREFILL);
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+extern "C" gdn_status gdn_chunk_prefill(const gdn_dims* dims, gdn_pool pool, gdn_pool ckpt,
+                                        const gdn_params* params, const int32_t* slot_ids,
+                                        const int32_t* cu_seqlens, const int64_t* start_pos,
+                                        int32_t n_seq, int64_t total_tokens,
+                                        const int32_t* ckpt_ids, int32_t max_ckpt,
+                                        int32_t ckpt_block, const void* qkv, const void* a,
+                                        const void* b, void* out, void* workspace,
+                                        size_t workspace_bytes, uint32_t* dev_err, void* stream) {
+  return chunk_prefill_impl(true, dims, pool, ckpt, params, slot_ids, cu_seqlens, start_pos, n_seq,
+                            total_tokens, ckpt_ids, max_ckpt, ckpt_block, qkv, a, b, out, workspace,
+                            workspace_bytes, dev_err, stream);
+}
+
+// Mixed batch, decode-first: the decode rows through the decode kernel, the
+// continuations through the chunked prefill (rows at their absolute offsets,
+// so only the per-sequence arrays are offset).  The prefill half is checked
+// before anything is launched, so a host-side error launches nothing.
+extern "C" gdn_status gdn_mixed_step(const gdn_dims* dims, gdn_pool pool, gdn_pool ckpt,
+                                     const gdn_params* params, const int32_t* slot_ids,
+                                     const int32_t* cu_seqlens, const int64_t* start_pos,
+                                     int32_t n_seq, int32_t n_decode, int64_t total_tokens,
+                                     const int32_t* ckpt_ids, int32_t max_ckpt, int32_t ckpt_block,
+                                     const void* qkv, const void* a, const void* b, void* out,
+                                     void* workspace, size_t workspace_bytes, uint32_t* dev_err,
+                                     void* stream) {
+  using namespace gdn;
+  gdn_status st = check_dims(dims);
+  if (st != GDN_OK) return st;
+  if (n_seq < 0 || n_decode < 0 || n_decode > n_seq || (int64_t)n_decode > total_tokens || max_ckpt < 0)
+    return GDN_ERR_INVALID_ARG;
+  const int32_t n_pre = n_seq - n_decode;
+  if (n_pre > 0 && (!slot_ids || !cu_seqlens || !start_pos || (max_ckpt > 0 && !ckpt_ids)))
+    return GDN_ERR_INVALID_ARG;
+  const int32_t* pre_ids = n_pre > 0 ? slot_ids + n_decode : nullptr;
+  const int32_t* pre_cu = n_pre > 0 ? cu_seqlens + n_decode : nullptr;
+  const int64_t* pre_sp = n_pre > 0 ? start_pos + n_decode : nullptr;
+  const int32_t* pre_ck = (n_pre > 0 && max_ckpt > 0) ? ckpt_ids + (size_t)n_decode * max_ckpt : nullptr;
+  if (n_pre > 0 &&
+      (st = chunk_prefill_impl(false, dims, pool, ckpt, params, pre_ids, pre_cu, pre_sp, n_pre, total_tokens,
+                               pre_ck, max_ckpt, ckpt_block, qkv, a, b, out, workspace, workspace_bytes,
+                               dev_err, stream)) != GDN_OK)
+    return st;
+  if (n_decode > 0 &&
+      (st = gdn_decode_step(dims, pool, params, slot_ids, n_decode, qkv, a, b, out, dev_err, stream)) != GDN_OK)
+    return st;
+  if (n_pre == 0) return GDN_OK;
+  return chunk_prefill_impl(true, dims, pool, ckpt, params, pre_ids, pre_cu, pre_sp, n_pre, total_tokens,
+                            pre_ck, max_ckpt, ckpt_block, qkv, a, b, out, workspace, workspace_bytes, dev_err,
+                            stream);
 }
 
 // ---------------------------------------------------------------------------

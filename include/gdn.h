@@ -209,6 +209,35 @@ gdn_status gdn_chunk_prefill_noalloc(const gdn_dims* dims, gdn_pool pool,
                                      uint32_t* dev_err, void* stream);
 
 /*
+ * Mixed batch: decode requests and prefill continuations in one packed batch
+ * (TokenSpeed talk, "Kernel: 让 MLA 真正跑满 GPU": agent turns append a few
+ * hundred tokens after a prefix hit, so batches are variable-length with no
+ * padding; TokenSpeed Qwen3.5 page, "Scheduler dual": decode updates the
+ * working slot in place).  Decode-first layout: sequences 0 .. n_decode-1 are
+ * single-token decode requests whose tokens are rows 0 .. n_decode-1 of qkv /
+ * a / b / out (cu_seqlens[i] = i for i <= n_decode; precondition); they take
+ * exactly the gdn_decode_step update (no checkpoints; their start_pos and
+ * ckpt_ids rows are not read).  Sequences n_decode .. n_seq-1 take exactly the
+ * gdn_chunk_prefill update from any start position (the first chunk may
+ * begin anywhere inside a 64-token chunk), with rows indexed by their absolute
+ * cu_seqlens offsets.  All arguments as for gdn_chunk_prefill; the workspace
+ * size gdn_chunk_prefill_workspace_size(dims, n_seq, total_tokens) suffices.
+ * 0 <= n_decode <= min(n_seq, total_tokens), else GDN_ERR_INVALID_ARG.  Slot
+ * ids must be distinct across the whole batch (precondition).  One call, on
+ * one stream, with no host synchronisation: the decode rows go to the decode
+ * kernel and the continuations to the chunked prefill, each at its own
+ * roofline.
+ */
+gdn_status gdn_mixed_step(const gdn_dims* dims, gdn_pool pool, gdn_pool ckpt,
+                          const gdn_params* params, const int32_t* slot_ids,
+                          const int32_t* cu_seqlens, const int64_t* start_pos,
+                          int32_t n_seq, int32_t n_decode, int64_t total_tokens,
+                          const int32_t* ckpt_ids, int32_t max_ckpt, int32_t ckpt_block,
+                          const void* qkv, const void* a, const void* b, void* out,
+                          void* workspace, size_t workspace_bytes, uint32_t* dev_err,
+                          void* stream);
+
+/*
  * Copy-on-write from a clean slot (TokenSpeed Qwen3.5 page, "Riesgo de
  * correctitud: estado obsoleto": a reused working slot is made safe by a copy
  * from a checkpoint known to be clean, or by explicit zeroing).

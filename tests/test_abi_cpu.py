@@ -144,6 +144,25 @@ def test_state_record_and_index_commit_arguments(lib):
     assert lib.gdn_launch_count(binding.K_COMMIT_INDEX) == n0
 
 
+def test_mixed_step_arguments(lib):
+    d = _dims()
+    pool = binding.CPool(0x10000, 0x20000, 4)
+    p = binding.CParams(0x1000, 0x2000, 0x3000)
+    args = lambda n_seq, n_dec, total, blk=256: (  # noqa: E731
+        ctypes.byref(d), pool, pool, ctypes.byref(p), 0x100, 0x200, 0x300, n_seq, n_dec, total,
+        None, 0, blk, 0x400, 0x500, 0x600, 0x700, 0x800, 1 << 30, None, None)
+    n_dec0 = lib.gdn_launch_count(binding.K_DECODE)
+    n_pre0 = lib.gdn_launch_count(binding.K_PREFILL)
+    assert lib.gdn_mixed_step(*args(2, 3, 10)) == binding.ERR_INVALID_ARG   # n_decode > n_seq
+    assert lib.gdn_mixed_step(*args(4, 3, 2)) == binding.ERR_INVALID_ARG    # n_decode > tokens
+    assert lib.gdn_mixed_step(*args(4, -1, 10)) == binding.ERR_INVALID_ARG
+    # the prefill half is checked before the decode half launches
+    assert lib.gdn_mixed_step(*args(4, 2, 10, blk=100)) == binding.ERR_INVALID_ARG
+    assert lib.gdn_mixed_step(*args(0, 0, 0)) == binding.OK
+    assert lib.gdn_launch_count(binding.K_DECODE) == n_dec0
+    assert lib.gdn_launch_count(binding.K_PREFILL) == n_pre0
+
+
 def test_launch_counters(lib):
     lib.gdn_launch_count_reset()
     assert all(lib.gdn_launch_count(k) == 0 for k in range(binding.K_COUNT))

@@ -1,0 +1,151 @@
+"""GPU mixed batches (decode-first: single-token decode requests, then chunked
+prefill continuations from arbitrary positions) against the oracle's decode
+step and token-by-token prefill, and bit-exact against the same rows sent
+through gdn_decode_step and gdn_chunk_prefill separately."""
+import numpy as np
+import pytest
+import torch
+
+import hybrid_linear_attention_gdn_gb300 as gdn
+import oracle
+from hybrid_linear_attention_gdn_gb300 import StatePool, synth
+from helpers import (STATE_TOL_1, Setup, assert_out_close, conv_bits_equal, max_rel_l2, out_tol,
+                     prefill_row_tol, prefill_state_tol, prefill_tol, to_np)
+
+pytestmark = pytest.mark.gpu
+
+BLK = 256
+
+
+def _batch(st: Setup, n_dec, lens, starts, n_slots):
+    """Ids, cu_seqlens (decode rows first), start positions, checkpoint ids and
+    tokens of one decode-first mixed batch."""
+    n = n_dec + len(lens)
+    ids = synth.slot_ids(n_slots, n, st.gen)
+    seq_lens = [1] * n_dec + list(lens)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(seq_lens)]), dtype=torch.int32)
+    sp = torch.tensor([0] * n_dec + list(starts), dtype=torch.int64)
+    max_ck = max(1, max(((s + L) // BLK - s // BLK for s, L in zip(starts, lens)), default=1))
+    ck_ids = torch.full((n, max_ck), -1, dtype=torch.int32)
+    n_ck = len(lens) * max_ck + 2
+    if lens:
+        ck_ids[n_dec:] = synth.slot_ids(n_ck, len(lens) * max_ck, st.gen).reshape(len(lens), max_ck)
+    qkv, a, b = st.tokens((int(cu[-1]),))
+    return ids, cu, sp, ck_ids, n_ck, qkv, a, b
+
+
+def _ck_pool(st, n):
+    p = StatePool.empty(st.dims, n, "cuda")
+    p.ssm.fill_(-5.0)
+    p.conv.fill_(9.0)
+    return p
+
+
+def _workspace(dims, n_seq, total):
+    nbytes = gdn.chunk_prefill_workspace_size(dims, n_seq, total)
+    return torch.empty(max(nbytes, 1), dtype=torch.uint8, device="cuda")
+
+
+CASES = [
+    # (shape, decode requests, continuation lengths, their start positions)
+    (synth.QWEN, 6, [200, 1, 70, 129], [200, 77, 4101, 63]),
+    (synth.QWEN, 16, [], []),
+    (synth.QWEN, 0, [300, 9], [512, 1001]),
+    (synth.TINY, 3, [37, 130, 1], [5, 64, 300]),
+]
+IDS = ["qwen_6_decode_4_continuations", "qwen_decode_only", "qwen_prefill_only", "tiny_mixed"]
+
+
+@pytest.mark.parametrize("shape,n_dec,lens,starts", CASES, ids=IDS)
+def test_mixed_step_vs_oracle(cuda, shape, n_dec, lens, starts):
+    n_slots = 16 if shape is synth.TINY else 24
+    st = Setup(shape, seed=50, num_slots=n_slots)
+    ids, cu, sp, ck_ids, n_ck, qkv, a, b = _batch(st, n_dec, lens, starts, n_slots)
+    n, total = ids.shape[0], int(cu[-1])
+    ck = _ck_pool(st, n_ck)
+    out = torch.full((total, shape.hv, shape.dv), 3.0, dtype=shape.act_dtype, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gdn.mixed_step(st.dims, st.pool, ck, st.params, ids.cuda(), cu.cuda(), sp.cuda(), total, n_dec,
+                   ck_ids.cuda(), BLK, qkv.cuda(), a.cuda(), b.cuda(), out, _workspace(st.dims, n, total),
+                   err)
+    # the oracle: decode steps for the first rows, token-by-token prefill for the rest
+    ock = oracle.Pool(np.full((n_ck, shape.hv, shape.dv, shape.dk), -5.0),
+                      np.full((n_ck, shape.w - 1, shape.channels), 9.0))
+    o_dec = o_pre = None
+    if n_dec:
+        o_dec, e1 = oracle.decode_step(st.od, st.opool, st.oparams, ids[:n_dec].numpy(),
+                                       to_np(qkv[:n_dec]), to_np(a[:n_dec]), to_np(b[:n_dec]))
+        assert e1 == 0
+    if lens:
+        o_pre, e2 = oracle.prefill(st.od, st.opool, ock, st.oparams, ids[n_dec:].numpy(),
+                                   (cu[n_dec:] - n_dec).numpy(), sp[n_dec:].numpy(),
+                                   ck_ids[n_dec:].numpy(), BLK, to_np(qkv[n_dec:]), to_np(a[n_dec:]),
+                                   to_np(b[n_dec:]))
+        assert e2 == 0
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    if n_dec:
+        assert_out_close(out[:n_dec], o_dec, shape.dv, out_tol(shape))
+        dec = ids[:n_dec].tolist()
+        assert max_rel_l2(to_np(st.pool.ssm[dec]), st.opool.ssm[dec], shape.dv * shape.dk) <= STATE_TOL_1
+        assert conv_bits_equal(st.pool.conv[dec], st.opool.conv[dec])
+    if lens:
+        assert_out_close(out[n_dec:], o_pre, shape.dv, prefill_tol(shape), row_floor_rms=True,
+                         row_tol=prefill_row_tol(shape))
+        pre = ids[n_dec:].tolist()
+        stol = prefill_state_tol(shape)
+        assert max_rel_l2(to_np(st.pool.ssm[pre]), st.opool.ssm[pre], shape.dv * shape.dk) <= stol
+        assert conv_bits_equal(st.pool.conv[pre], st.opool.conv[pre])
+        written = [i for i in range(n_ck) if not np.all(ock.ssm[i] == -5.0)]
+        assert len(written) == sum((s + L) // BLK - s // BLK for s, L in zip(starts, lens))
+        if written:
+            assert max_rel_l2(to_np(ck.ssm[written]), ock.ssm[written], shape.dv * shape.dk) <= stol
+        assert conv_bits_equal(ck.conv, ock.conv)
+    # untouched slots keep their values
+    rest = [s for s in range(n_slots) if s not in ids.tolist()]
+    assert torch.equal(st.pool.ssm[rest].cpu(), torch.from_numpy(st.opool.ssm[rest]).float())
+
+
+@pytest.mark.parametrize("shape,n_dec,lens,starts", CASES, ids=IDS)
+def test_mixed_step_equals_separate_calls(cuda, shape, n_dec, lens, starts):
+    """Bit for bit the decode step on the decode rows and the chunked prefill on
+    the rest, called one after the other."""
+    n_slots = 16 if shape is synth.TINY else 24
+    st = Setup(shape, seed=51, num_slots=n_slots)
+    ids, cu, sp, ck_ids, n_ck, qkv, a, b = _batch(st, n_dec, lens, starts, n_slots)
+    n, total = ids.shape[0], int(cu[-1])
+    q, av, bv = qkv.cuda(), a.cuda(), b.cuda()
+    pool2 = StatePool(st.pool.ssm.clone(), st.pool.conv.clone())
+    ck1, ck2 = _ck_pool(st, n_ck), _ck_pool(st, n_ck)
+    out1 = torch.zeros((total, shape.hv, shape.dv), dtype=shape.act_dtype, device="cuda")
+    out2 = torch.zeros_like(out1)
+    ws = _workspace(st.dims, n, total)
+    n_dec0 = gdn.launch_count(gdn.K_DECODE)
+    gdn.mixed_step(st.dims, st.pool, ck1, st.params, ids.cuda(), cu.cuda(), sp.cuda(), total, n_dec,
+                   ck_ids.cuda(), BLK, q, av, bv, out1, ws)
+    assert gdn.launch_count(gdn.K_DECODE) == n_dec0 + (1 if n_dec else 0)
+    if n_dec:
+        gdn.decode_step(st.dims, pool2, st.params, ids[:n_dec].cuda(), q[:n_dec], av[:n_dec], bv[:n_dec],
+                        out2[:n_dec])
+    if lens:
+        gdn.chunk_prefill(st.dims, pool2, ck2, st.params, ids[n_dec:].cuda(), (cu[n_dec:] - n_dec).cuda(),
+                          sp[n_dec:].cuda(), total - n_dec, ck_ids[n_dec:].cuda(), BLK, q[n_dec:],
+                          av[n_dec:], bv[n_dec:], out2[n_dec:], ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out1, out2)
+    assert torch.equal(st.pool.ssm, pool2.ssm) and torch.equal(st.pool.conv, pool2.conv)
+    assert torch.equal(ck1.ssm, ck2.ssm) and torch.equal(ck1.conv, ck2.conv)
+
+
+def test_mixed_step_bad_arguments(cuda):
+    st = Setup(synth.TINY, seed=52)
+    ids = torch.tensor([0, 1, 2], dtype=torch.int32, device="cuda")
+    cu = torch.tensor([0, 1, 2, 5], dtype=torch.int32, device="cuda")
+    sp = torch.zeros(3, dtype=torch.int64, device="cuda")
+    qkv, a, b = (t.cuda() for t in st.tokens((5,)))
+    out = torch.empty((5, 4, 16), dtype=torch.float32, device="cuda")
+    ck = _ck_pool(st, 2)
+    ws = _workspace(st.dims, 3, 5)
+    with pytest.raises(gdn.GdnError) as e:
+        gdn.mixed_step(st.dims, st.pool, ck, st.params, ids, cu, sp, 5, 4, None, BLK, qkv, a, b, out, ws)
+    assert e.value.status == gdn.binding.ERR_INVALID_ARG

@@ -42,7 +42,8 @@ def _ck_pool(st, n):
     (synth.QWEN, [70, 200, 513], [0, 128, 0], 256, "cuda"),
     (synth.QWEN.replace(hk=2, hv=8, dk=64, dv=64), [129, 64, 3], [0, 192, 61], 64, "tc"),
     (synth.TINY, [700, 65, 260], [3, 0, 130], 64, "tc"),
-], ids=["tiny", "qwen", "qwen_fp32_path", "dk64_g4", "tiny_ten_checkpoints"])
+    (synth.QWEN, [200, 1, 70, 129], [200, 77, 4101, 63], 256, "tc"),
+], ids=["tiny", "qwen", "qwen_fp32_path", "dk64_g4", "tiny_ten_checkpoints", "qwen_unaligned_continuations"])
 def test_prefill_vs_token_recurrence(cuda, monkeypatch, shape, lens, starts, blk, path):
     """path "cuda" forces the fp32 CUDA-core prefill (the library reads
     GDN_PREFILL_PATH on every call); it meets the stated 2e-3."""
