@@ -37,8 +37,9 @@ from dataclasses import dataclass
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "gdn_oracle.c")
-_OUT_DIR = os.path.join(_HERE, "_build")
+# a mutated copy of the source (tests/test_oracle_mutations.py) builds elsewhere
+_SRC = os.environ.get("GDN_ORACLE_SRC", os.path.join(_HERE, "gdn_oracle.c"))
+_OUT_DIR = os.environ.get("GDN_ORACLE_BUILD_DIR", os.path.join(_HERE, "_build"))
 _SO = os.path.join(_OUT_DIR, "liborc_gdn.so")
 _lock = threading.Lock()
 _lib = None
@@ -273,6 +274,20 @@ def state_unpack(dims: Dims, st_ssm, st_conv, pool: Pool, ids):
                             ctypes.c_int32(ids.shape[0]), ctypes.byref(err))
     assert rc == 0
     return err.value
+
+
+def gated_rmsnorm(dims: Dims, o, z, w, eps=1e-6):
+    """Readout epilogue y = o / sqrt(mean(o^2) + eps) * w * silu(z) per
+    (token, V head) row; o, z [n_tok][hv][dv], w [dv].  Returns y."""
+    L = lib()
+    o, z, w = _f64(o), _f64(z), _f64(w)
+    assert o.shape == z.shape and o.shape[1:] == (dims.hv, dims.dv) and w.shape == (dims.dv,)
+    y = np.zeros_like(o)
+    cd = dims.c()
+    rc = L.orc_gated_rmsnorm(ctypes.byref(cd), _ptr(o), _ptr(z), _ptr(w), ctypes.c_double(eps),
+                             ctypes.c_int64(o.shape[0]), _ptr(y))
+    assert rc == 0
+    return y
 
 
 def _prefill_common(dims, slot_ids, cu_seqlens, start_pos, ckpt_ids, qkv, a, b):

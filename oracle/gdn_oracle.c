@@ -418,6 +418,28 @@ int orc_state_unpack(const orc_dims* d, const double* st_ssm, const double* st_c
   return 0;
 }
 
+/* ---- readout epilogue: gated RMS norm ----------------------------------
+ * Not written on the pages.  The published Gated DeltaNet block normalises
+ * each head's readout and gates it with a SiLU of a separate projection z:
+ * for every (token, V head) row o of dv values,
+ *   y = o / sqrt(mean(o^2) + eps) * w * silu(z)
+ * with w [dv] a learned weight shared by the heads.  o, z, y are
+ * [n_tok][hv][dv]; y may alias o. */
+int orc_gated_rmsnorm(const orc_dims* d, const double* o, const double* z, const double* w,
+                      double eps, int64_t n_tok, double* y) {
+  if (check_dims(d) || n_tok < 0 || eps < 0.0) return 1;
+  int64_t rows = n_tok * d->hv, dv = d->dv;
+  for (int64_t r = 0; r < rows; ++r) {
+    const double* orow = o + r * dv;
+    double ss = 0.0;
+    for (int64_t j = 0; j < dv; ++j) ss += orow[j] * orow[j];
+    double inv = 1.0 / sqrt(ss / (double)dv + eps);
+    for (int64_t j = 0; j < dv; ++j)
+      y[r * dv + j] = orow[j] * inv * w[j] * orc_silu(z[r * dv + j]);
+  }
+  return 0;
+}
+
 /* ---- a8: prefill, token by token (the plain definition) -----------------
  * Sequence n owns tokens [cu_seqlens[n], cu_seqlens[n+1]) of qkv [Ttot][C]
  * (a,b [Ttot][hv], out [Ttot][hv][dv]); its first token sits at absolute

@@ -402,6 +402,11 @@ def test_state_pack_unpack():
     expect.conv[2] = 0.0
     np.testing.assert_array_equal(dst.ssm, expect.ssm)
     np.testing.assert_array_equal(dst.conv, expect.conv)
+    # padding alone is not an error; an id outside the pool alone is, either way
+    assert oracle.state_pack(d, pool, [-1, 2, -1])[2] == 0
+    assert oracle.state_pack(d, pool, [2, 8])[2] == oracle.ERR_SLOT_OOB
+    assert oracle.state_unpack(d, st_ssm[:2], st_conv[:2], dst, [-1, 4]) == 0
+    assert oracle.state_unpack(d, st_ssm[:1], st_conv[:1], dst, [-3]) == oracle.ERR_SLOT_OOB
 
 
 # ----------------------------------------------------------------- prefill
@@ -506,3 +511,57 @@ def test_prefill_padding_and_oob():
     assert np.all(out[:10] == 0) and np.any(out[10:] != 0)
     assert np.array_equal(pool.ssm[[0, 1, 3]], before.ssm[[0, 1, 3]])
     assert np.all(ck.ssm == 0)
+
+
+# ---- readout epilogue: gated RMS norm ------------------------------------
+
+def test_gated_rmsnorm_hand_worked():
+    """dv = 2, o = (3, 4): mean(o^2) = 12.5, so with eps = 0 the normalised row
+    is (3, 4) / sqrt(12.5) = (1.2, 1.6) / sqrt(2); w = (1, 2) and z = 40
+    (silu(40) = 40 to 1e-15) give (48/sqrt(2), 128/sqrt(2))."""
+    d = oracle.Dims(1, 1, 2, 2)
+    y = oracle.gated_rmsnorm(d, np.array([[[3.0, 4.0]]]), np.full((1, 1, 2), 40.0),
+                             np.array([1.0, 2.0]), eps=0.0)
+    assert np.allclose(y[0, 0], [48.0 / math.sqrt(2.0), 128.0 / math.sqrt(2.0)], rtol=1e-14, atol=0)
+
+
+def test_gated_rmsnorm_constant_row_and_gate():
+    """A constant row c normalises to sign(c) (mean, not sum, of squares), and
+    the gate is silu(z) = z sigmoid(z), not sigmoid(z)."""
+    d = oracle.Dims(2, 4, 16, 16)
+    o = np.full((1, 4, 16), -0.37)
+    w = np.ones(16)
+    y = oracle.gated_rmsnorm(d, o, np.full((1, 4, 16), 40.0), w, eps=0.0)
+    assert np.allclose(y, -40.0, rtol=1e-14, atol=0)
+    z2 = np.full((1, 4, 16), 2.0)
+    y2 = oracle.gated_rmsnorm(d, o, z2, w, eps=0.0)
+    assert np.allclose(y2, -2.0 / (1.0 + math.exp(-2.0)), rtol=1e-14, atol=0)
+    # eps enters as mean(o^2) + eps
+    y3 = oracle.gated_rmsnorm(d, o, np.full((1, 4, 16), 40.0), w, eps=0.37 ** 2 * 3)
+    assert np.allclose(y3, -40.0 / 2.0, rtol=1e-14, atol=0)
+
+
+def test_gated_rmsnorm_per_row_invariants():
+    """eps = 0: each (token, head) row of y / (w silu(z)) has RMS 1 whatever the
+    rows' scales; y is odd and scale-free in o; w indexes dv; z = 0 gives 0; a
+    zero row with eps > 0 gives zeros."""
+    rng = np.random.default_rng(3)
+    d = oracle.Dims(2, 4, 16, 8)
+    o = rng.standard_normal((5, 4, 8)) * rng.uniform(0.01, 100.0, (5, 4, 1))
+    z = rng.standard_normal((5, 4, 8)) + 3.0
+    w = rng.uniform(0.5, 2.0, 8)
+    y = oracle.gated_rmsnorm(d, o, z, w, eps=0.0)
+    silu = z / (1.0 + np.exp(-z))
+    g = y / (w * silu)
+    assert np.allclose(np.sqrt(np.mean(g ** 2, axis=2)), 1.0, rtol=1e-13)
+    assert np.allclose(g * np.sqrt(np.mean(o ** 2, axis=2, keepdims=True)), o, rtol=1e-12)
+    assert np.allclose(oracle.gated_rmsnorm(d, -7.5 * o, z, w, eps=0.0), -y, rtol=1e-13)
+    onehot = np.zeros(8)
+    onehot[5] = 1.0
+    y1 = oracle.gated_rmsnorm(d, o, z, onehot, eps=0.0)
+    assert np.all(y1[:, :, [0, 1, 2, 3, 4, 6, 7]] == 0.0) and np.all(y1[:, :, 5] != 0.0)
+    assert np.all(oracle.gated_rmsnorm(d, o, np.zeros_like(z), w) == 0.0)
+    o0 = o.copy()
+    o0[2, 1] = 0.0
+    y0 = oracle.gated_rmsnorm(d, o0, z, w, eps=1e-6)
+    assert np.all(y0[2, 1] == 0.0) and np.all(np.isfinite(y0))
