@@ -602,6 +602,19 @@ def measure_rows(gdn, synth, dev, stream, hbm_peak, bf16_peak, which="all", pref
     torch.cuda.synchronize()
     if full:
         rows["mixed_b64_plus_4x256"] = _mixed_row(gdn, synth, dims, pool, params, perm, g, dev, stream)
+        # readout epilogue over a 4 x 8192-token prefill output: o and z read,
+        # y written in place (3 x 256 bytes per (token, V head) row)
+        n_tok = 32768
+        eo = synth.normal((n_tok, shape.hv, shape.dv), 0.7, g, shape.act_dtype).to(dev)
+        ez = synth.normal((n_tok, shape.hv, shape.dv), 1.5, g, shape.act_dtype).to(dev)
+        ew = torch.ones(shape.dv, dtype=torch.float32, device=dev)
+
+        def fe(i):
+            gdn.gated_rmsnorm(dims, eo, ez, ew, 1e-6)
+        fe(0)
+        rows["gated_rmsnorm_32768_tokens"] = frac(3 * n_tok * shape.hv * shape.dv * 2,
+                                                  _events_time(fe, 20, stream))
+        del eo, ez
     return rows
 
 

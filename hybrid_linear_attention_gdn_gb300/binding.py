@@ -21,8 +21,8 @@ F32, BF16 = 0, 1
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_SCRATCH_LIMIT = 0, 1, 2, 3, 4
 DEV_ERR_SLOT_OOB, DEV_ERR_TIMEOUT, DEV_ERR_SEQLENS = 1, 2, 4
 (K_DECODE, K_SPEC_VERIFY, K_SLOT_COPY, K_SLOT_ZERO, K_SPEC_COMMIT, K_PREFILL, K_COMMIT_INDEX,
- K_STATE_PACK) = range(8)
-K_COUNT = 8
+ K_STATE_PACK, K_GATED_RMSNORM) = range(9)
+K_COUNT = 9
 
 _DT_CODE = {torch.float32: F32, torch.bfloat16: BF16}
 
@@ -75,6 +75,7 @@ EXPORTS = {
     "gdn_state_record_bytes": ([_PD], ctypes.c_size_t),
     "gdn_state_pack": ([_PD, CPool, _P, _I32, _P, ctypes.c_size_t, _P, _P], _I32),
     "gdn_state_unpack": ([_PD, _P, ctypes.c_size_t, CPool, _P, _I32, _P, _P], _I32),
+    "gdn_gated_rmsnorm": ([_PD, _P, _P, _P, ctypes.c_float, _I64, _P, _P], _I32),
     "gdn_status_string": ([_I32], ctypes.c_char_p),
     "gdn_launch_count": ([_I32], ctypes.c_uint64),
     "gdn_launch_count_reset": ([], None),
@@ -350,6 +351,20 @@ def state_unpack(dims: Dims, staging, pool: StatePool, ids, dev_err=None, stream
     st = L.gdn_state_unpack(ctypes.byref(cd), _ptr(staging), _nbytes(staging), pool.c(),
                             _ptr(ids), int(ids.shape[0]), _ptr(dev_err), _stream(stream))
     _check("gdn_state_unpack", st)
+
+
+def gated_rmsnorm(dims: Dims, o, z, weight, eps: float = 1e-6, y=None, stream=None):
+    """Readout epilogue y = o / sqrt(mean(o^2) + eps) * weight * silu(z) per
+    (token, V head) row; o, z [n_tok][hv][dv] in the activation dtype, weight
+    [dv] fp32.  y defaults to o (in place).  Returns y."""
+    L = load()
+    if y is None:
+        y = o
+    cd = dims.c()
+    st = L.gdn_gated_rmsnorm(ctypes.byref(cd), _ptr(o), _ptr(z), _ptr(weight), float(eps),
+                             int(o.shape[0]), _ptr(y), _stream(stream))
+    _check("gdn_gated_rmsnorm", st)
+    return y
 
 
 def launch_count(kernel: int) -> int:

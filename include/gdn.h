@@ -149,9 +149,11 @@ gdn_status gdn_spec_commit(const gdn_dims* dims, gdn_pool spec, gdn_pool work,
  * ckpt_ids[n][P/ckpt_block - floor(start_pos[n]/ckpt_block) - 1] of `ckpt`
  * (-1 or an index >= max_ckpt: skipped).  The intra-chunk work uses chunks
  * of 64 tokens aligned to absolute positions.
- *   cu_seqlens [n_seq+1] int32 (device): cu_seqlens[0] = 0, non-decreasing,
- *     cu_seqlens[n_seq] = total_tokens; a sequence violating this (or with
- *     start_pos < 0) is skipped and sets GDN_DEV_ERR_SEQLENS
+ *   cu_seqlens [n_seq+1] int32 (device): absolute row offsets, non-decreasing,
+ *     0 <= cu_seqlens[0], cu_seqlens[n_seq] <= total_tokens (usually 0 and
+ *     total_tokens; rows outside them are not written and do not affect the
+ *     results); a sequence whose rows fall outside [0, total_tokens) (or
+ *     with start_pos < 0) is skipped and sets GDN_DEV_ERR_SEQLENS
  *   start_pos [n_seq] int64 (device)
  *   ckpt_ids [n_seq][max_ckpt] int32; ckpt_block a positive multiple of 64;
  *     max_ckpt above 262,140 returns GDN_ERR_UNSUPPORTED
@@ -294,6 +296,21 @@ gdn_status gdn_state_unpack(const gdn_dims* dims, const void* staging, size_t st
                             gdn_pool pool, const int32_t* ids, int32_t n, uint32_t* dev_err,
                             void* stream);
 
+/*
+ * Readout epilogue: gated RMS norm.  Not written on the pages; the published
+ * Gated DeltaNet block normalises each head's readout and gates it with the
+ * SiLU of a separate projection z.  For every (token, V head) row o of dv
+ * values:  y = o / sqrt(mean(o^2) + eps) * weight * silu(z).
+ *   o, z, y  [n_tokens][hv][dv] in the activation dtype, device; y may be o
+ *            (in place); any other overlap is undefined;
+ *   weight   [dv] fp32, device, shared by the heads;  eps >= 0.
+ * Applies to the outputs of any call above (decode, verify, prefill, mixed).
+ * Statuses as above; n_tokens = 0 launches nothing.
+ */
+gdn_status gdn_gated_rmsnorm(const gdn_dims* dims, const void* o, const void* z,
+                             const float* weight, float eps, int64_t n_tokens, void* y,
+                             void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* gdn_status_string(int32_t status);
 
@@ -306,7 +323,8 @@ const char* gdn_status_string(int32_t status);
 #define GDN_K_PREFILL 5
 #define GDN_K_COMMIT_INDEX 6
 #define GDN_K_STATE_PACK 7 /* pack and unpack */
-#define GDN_K_COUNT 8
+#define GDN_K_GATED_RMSNORM 8
+#define GDN_K_COUNT 9
 uint64_t gdn_launch_count(int32_t kernel);
 void gdn_launch_count_reset(void);
 

@@ -163,6 +163,20 @@ def test_mixed_step_arguments(lib):
     assert lib.gdn_launch_count(binding.K_PREFILL) == n_pre0
 
 
+def test_gated_rmsnorm_arguments(lib):
+    d = _dims()
+    n0 = lib.gdn_launch_count(binding.K_GATED_RMSNORM)
+    call = lambda n, eps, o=0x100, z=0x200, w=0x300, y=0x400: lib.gdn_gated_rmsnorm(  # noqa: E731
+        ctypes.byref(d), o, z, w, eps, n, y, None)
+    assert call(-1, 1e-6) == binding.ERR_INVALID_ARG
+    assert call(4, -1.0) == binding.ERR_INVALID_ARG
+    assert call(4, float("nan")) == binding.ERR_INVALID_ARG
+    assert call(4, 1e-6, w=None) == binding.ERR_INVALID_ARG
+    assert call(0, 1e-6) == binding.OK
+    assert lib.gdn_gated_rmsnorm(None, 0x100, 0x200, 0x300, 1e-6, 4, 0x400, None) == binding.ERR_INVALID_ARG
+    assert lib.gdn_launch_count(binding.K_GATED_RMSNORM) == n0
+
+
 def test_launch_counters(lib):
     lib.gdn_launch_count_reset()
     assert all(lib.gdn_launch_count(k) == 0 for k in range(binding.K_COUNT))

@@ -1,0 +1,82 @@
+"""GPU readout epilogue (gated RMS norm) against the oracle: on random rows of
+every supported width and on the real readout of a decode step, in place and
+out of place."""
+import numpy as np
+import pytest
+import torch
+
+import hybrid_linear_attention_gdn_gb300 as gdn
+import oracle
+from hybrid_linear_attention_gdn_gb300 import synth
+from helpers import Setup, assert_out_close, odims, out_tol, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _rows(shape, n_tok, seed):
+    g = synth.generator(seed)
+    o = synth.normal((n_tok, shape.hv, shape.dv), 0.7, g, shape.act_dtype)
+    z = synth.normal((n_tok, shape.hv, shape.dv), 1.5, g, shape.act_dtype)
+    w = 1.0 + synth.normal((shape.dv,), 0.2, g)
+    return o, z, w
+
+
+@pytest.mark.parametrize("shape,n_tok", [
+    (synth.QWEN, 64), (synth.QWEN, 3), (synth.TINY, 37),
+    (synth.QWEN.replace(hk=2, hv=8, dk=64, dv=64), 11),
+    (synth.QWEN.replace(act="f32", conv="f32", hk=4, hv=8, dv=200), 5),
+], ids=["qwen_b64", "qwen_3", "tiny_f32_dv16", "dv64", "f32_dv200_ragged"])
+def test_gated_rmsnorm_vs_oracle(cuda, shape, n_tok):
+    o, z, w = _rows(shape, n_tok, 60 + n_tok)
+    od = odims(shape)
+    ref = oracle.gated_rmsnorm(od, to_np(o), to_np(z), w.double().numpy(), eps=1e-6)
+    o_d, z_d, w_d = o.cuda(), z.cuda(), w.cuda()
+    y = torch.full_like(o_d, 5.0)
+    n0 = gdn.launch_count(gdn.K_GATED_RMSNORM)
+    gdn.gated_rmsnorm(gdn.Dims.of(shape), o_d, z_d, w_d, 1e-6, y)
+    torch.cuda.synchronize()
+    assert gdn.launch_count(gdn.K_GATED_RMSNORM) == n0 + 1
+    assert torch.equal(o_d.cpu(), o)  # out of place: o untouched
+    assert_out_close(y, ref, shape.dv, out_tol(shape))
+    # in place gives the same bits
+    gdn.gated_rmsnorm(gdn.Dims.of(shape), o_d, z_d, w_d, 1e-6)
+    torch.cuda.synchronize()
+    assert torch.equal(o_d, y)
+
+
+def test_decode_readout_then_epilogue(cuda):
+    """The epilogue on a decode step's own output, both against the oracle's
+    decode step followed by the oracle's epilogue."""
+    shape = synth.QWEN
+    st = Setup(shape, seed=61, num_slots=80)
+    B = 64
+    ids = synth.slot_ids(80, B, st.gen)
+    qkv, a, b = st.tokens((B,))
+    out = torch.empty((B, shape.hv, shape.dv), dtype=shape.act_dtype, device="cuda")
+    gdn.decode_step(st.dims, st.pool, st.params, ids.cuda(), qkv.cuda(), a.cuda(), b.cuda(), out)
+    _, z, w = _rows(shape, B, 62)
+    gdn.gated_rmsnorm(st.dims, out, z.cuda(), w.cuda(), 1e-6)
+    o_ref, err = oracle.decode_step(st.od, st.opool, st.oparams, ids.numpy(), to_np(qkv), to_np(a),
+                                    to_np(b))
+    assert err == 0
+    y_ref = oracle.gated_rmsnorm(st.od, o_ref, to_np(z), w.double().numpy(), eps=1e-6)
+    torch.cuda.synchronize()
+    # the decode output is rounded to bf16 before the norm: its 2^-9 error
+    # passes through the (scale-free) norm, plus the epilogue's own rounding
+    assert_out_close(out, y_ref, shape.dv, 2 * out_tol(shape))
+
+
+def test_gated_rmsnorm_zero_rows_and_empty(cuda):
+    shape = synth.QWEN
+    o, z, w = _rows(shape, 4, 63)
+    o[1] = 0.0
+    o_d = o.cuda()
+    gdn.gated_rmsnorm(gdn.Dims.of(shape), o_d, z.cuda(), w.cuda(), 1e-6)
+    torch.cuda.synchronize()
+    assert torch.all(o_d[1] == 0) and torch.all(torch.isfinite(o_d.float()))
+    n0 = gdn.launch_count(gdn.K_GATED_RMSNORM)
+    e = torch.empty((0, shape.hv, shape.dv), dtype=shape.act_dtype, device="cuda")
+    gdn.gated_rmsnorm(gdn.Dims.of(shape), e, e, w.cuda(), 1e-6)
+    assert gdn.launch_count(gdn.K_GATED_RMSNORM) == n0
+    with pytest.raises(gdn.GdnError):
+        gdn.gated_rmsnorm(gdn.Dims.of(shape), o_d, z.cuda(), w.cuda(), -1.0)
