@@ -276,6 +276,26 @@ def state_unpack(dims: Dims, st_ssm, st_conv, pool: Pool, ids):
     return err.value
 
 
+def kda_decode_step(dims: Dims, pool: Pool, params: Params, slot_ids, qkv, a, b):
+    """KDA decode (per-key-channel decay): as decode_step, with a [B][hv][dk]
+    gate logits and params.dt_bias [hv][dk].  In place on ``pool``.  Returns
+    (out, err)."""
+    L = lib()
+    slot_ids = _i32(slot_ids)
+    B = slot_ids.shape[0]
+    qkv, a, b = _f64(qkv), _f64(a), _f64(b)
+    assert qkv.shape == (B, dims.channels) and a.shape == (B, dims.hv, dims.dk)
+    assert b.shape == (B, dims.hv) and params.dt_bias.shape == (dims.hv, dims.dk)
+    out = np.zeros((B, dims.hv, dims.dv), np.float64)
+    err = ctypes.c_uint32(0)
+    cd, cpa = dims.c(), params.c()
+    rc = L.orc_kda_decode_step(ctypes.byref(cd), pool.c(), ctypes.byref(cpa), _ptr(slot_ids),
+                               ctypes.c_int32(B), _ptr(qkv), _ptr(a), _ptr(b), _ptr(out),
+                               ctypes.byref(err))
+    assert rc == 0
+    return out, err.value
+
+
 def gated_rmsnorm(dims: Dims, o, z, w, eps=1e-6):
     """Readout epilogue y = o / sqrt(mean(o^2) + eps) * w * silu(z) per
     (token, V head) row; o, z [n_tok][hv][dv], w [dv].  Returns y."""

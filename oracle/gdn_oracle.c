@@ -418,6 +418,74 @@ int orc_state_unpack(const orc_dims* d, const double* st_ssm, const double* st_c
   return 0;
 }
 
+/* ---- KDA: the delta rule with a per-key-channel decay --------------------
+ * The pages name Kimi Delta Attention (Kimi K3) as the second linear-
+ * attention family beside GDN and do not write it.  It follows the published
+ * formulation (Kimi Linear, 2025): the scalar decay of the gated delta rule
+ * becomes a decay per key channel,
+ *   S_t = (I - b_t k_t k_t^T) Diag(a_t) S_{t-1} + b_t k_t v_t^T,  o_t = S_t^T q_t,
+ * a_t[c] = exp(g_c), g_c = -exp(A_log[h]) * softplus(a[h][c] + dt_bias[h][c]).
+ * In the transposed storage St[dv][dk] (row j = column j of S):
+ *   u_j = v_j - sum_i a_i St[j][i] k_i
+ *   St[j][i] <- a_i St[j][i] + b u_j k_i
+ *   o_j = sum_i St[j][i] q_i   (updated state) */
+void orc_kda_core(int32_t dk, int32_t dv, double* St, const double* k, const double* v,
+                  const double* q, const double* alpha, double beta, double* o) {
+  for (int32_t j = 0; j < dv; ++j) {
+    double* row = St + (int64_t)j * dk;
+    double sk = 0.0;
+    for (int32_t i = 0; i < dk; ++i) sk += alpha[i] * row[i] * k[i];
+    double u = v[j] - sk;
+    for (int32_t i = 0; i < dk; ++i) row[i] = alpha[i] * row[i] + beta * u * k[i];
+    double oj = 0.0;
+    for (int32_t i = 0; i < dk; ++i) oj += row[i] * q[i];
+    o[j] = oj;
+  }
+}
+
+/* KDA decode: as orc_decode_step (same pool, conv, norms, beta), with the
+ * gate logits a [B][hv][dk] and dt_bias [hv][dk] per key channel. */
+int orc_kda_decode_step(const orc_dims* d, orc_pool pool, const orc_params* p,
+                        const int32_t* slot_ids, int32_t B, const double* qkv,
+                        const double* a, const double* b, double* out, uint32_t* err) {
+  if (check_dims(d)) return 1;
+  int64_t C = n_chan(d), HVDV = (int64_t)d->hv * d->dv;
+  int dk = d->dk, G = d->hv / d->hk;
+  double qscale = 1.0 / sqrt((double)dk);
+  int64_t fail = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : fail)
+  for (int32_t r = 0; r < B; ++r) {
+    int32_t s = slot_ids[r];
+    int cls = slot_class(s, pool.num_slots);
+    double* o = out + r * HVDV;
+    if (cls) {
+      if (cls == 2) fail |= ORC_ERR_SLOT_OOB;
+      for (int64_t i = 0; i < HVDV; ++i) o[i] = 0.0;
+      continue;
+    }
+    double* y = (double*)malloc(sizeof(double) * (C + 3 * (int64_t)dk));
+    double *qh = y + C, *kh = qh + dk, *al = kh + dk;
+    double* conv = pool.conv + s * conv_elems(d);
+    orc_conv_silu(d, conv, qkv + r * C, p->conv_w, y);
+    conv_shift(d, conv, qkv + r * C);
+    for (int h = 0; h < d->hv; ++h) {
+      int hq = h / G;
+      orc_l2norm(dk, y + (int64_t)hq * dk, qscale, qh);
+      orc_l2norm(dk, y + (int64_t)(d->hk + hq) * dk, 1.0, kh);
+      const double* ah = a + ((int64_t)r * d->hv + h) * dk;
+      for (int c = 0; c < dk; ++c)
+        al[c] = exp(orc_gate_g(p->A_log[h], p->dt_bias[(int64_t)h * dk + c], ah[c]));
+      double beta = orc_sigmoid(b[(int64_t)r * d->hv + h]);
+      orc_kda_core(dk, d->dv, pool.ssm + s * ssm_elems(d) + (int64_t)h * d->dv * dk, kh,
+                   y + 2 * (int64_t)d->hk * dk + (int64_t)h * d->dv, qh, al, beta,
+                   o + (int64_t)h * d->dv);
+    }
+    free(y);
+  }
+  if (err) *err |= (uint32_t)fail;
+  return 0;
+}
+
 /* ---- readout epilogue: gated RMS norm ----------------------------------
  * Not written on the pages.  The published Gated DeltaNet block normalises
  * each head's readout and gates it with a SiLU of a separate projection z:

@@ -20,7 +20,8 @@ PINS = os.path.join(ROOT, "tests", "test_oracle_pins.py")
 MUTATIONS = {
     "delta_term_sign": ("double u = v[j] - alpha * sk;", "double u = v[j] + alpha * sk;"),
     "decay_dropped": ("row[i] = alpha * row[i] + beta * u * k[i];", "row[i] = row[i] + beta * u * k[i];"),
-    "readout_uses_k": ("oj += row[i] * q[i];", "oj += row[i] * k[i];"),
+    "readout_uses_k": ("oj += row[i] * q[i];\n    o[j] = oj;\n  }\n}\n\n/* Features",
+                       "oj += row[i] * k[i];\n    o[j] = oj;\n  }\n}\n\n/* Features"),
     "query_scale_missing": ("double qscale = 1.0 / sqrt((double)d->dk);", "double qscale = 1.0;"),
     "gqa_map_modulo": ("    int hq = h / G;\n    orc_delta_core", "    int hq = h % d->hk;\n    orc_delta_core"),
     "conv_taps_reversed": ("acc += conv_w[c * W + i] * hist[i * C + c];",
@@ -40,6 +41,9 @@ MUTATIONS = {
     "chunk_state_decay_dropped": ("v += exp(blast - bcum[c]) * KR(c)[m] * Dm[c * dv + j];",
                                   "v += KR(c)[m] * Dm[c * dv + j];"),
     "chunk_gamma_sign": ("kk * exp(bcum[r] - bcum[c]);", "kk * exp(0.5 * (bcum[r] - bcum[c]));"),
+    "kda_u_without_decay": ("sk += alpha[i] * row[i] * k[i];", "sk += row[i] * k[i];"),
+    "kda_state_without_decay": ("row[i] = alpha[i] * row[i] + beta * u * k[i];",
+                                "row[i] = row[i] + beta * u * k[i];"),
     "rmsnorm_sum_not_mean": ("double inv = 1.0 / sqrt(ss / (double)dv + eps);",
                              "double inv = 1.0 / sqrt(ss + eps);"),
     "rmsnorm_gate_sigmoid": ("orc_silu(z[r * dv + j])", "orc_sigmoid(z[r * dv + j])"),

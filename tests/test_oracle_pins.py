@@ -565,3 +565,82 @@ def test_gated_rmsnorm_per_row_invariants():
     o0[2, 1] = 0.0
     y0 = oracle.gated_rmsnorm(d, o0, z, w, eps=1e-6)
     assert np.all(y0[2, 1] == 0.0) and np.all(np.isfinite(y0))
+
+
+# ---- KDA: per-key-channel decay --------------------------------------------
+
+def _kda_inputs(seed, shape=synth.TINY):
+    g, pool, params = _tiny_setup(seed, shape)
+    qkv, a, b = synth.tokens(shape, g, (3,))
+    return g, pool, params, qkv.double().numpy(), a.double().numpy(), b.double().numpy()
+
+
+def test_kda_with_uniform_gates_is_gdn():
+    """Every key channel of a head given the head's own gate logit and bias:
+    the per-channel decay is the scalar one, and KDA is the GDN step."""
+    shape = synth.TINY
+    d = _dims(shape)
+    _, pool, params, qkv, a, b = _kda_inputs(70)
+    ids = np.array([6, 1, 3], np.int32)
+    pool2 = pool.copy()
+    a_kda = np.repeat(a[:, :, None], d.dk, axis=2)
+    p_kda = oracle.Params(params.conv_w, params.A_log,
+                          np.repeat(params.dt_bias[:, None], d.dk, axis=1) + 0.0)
+    o1, e1 = oracle.decode_step(d, pool, params, ids, qkv, a, b)
+    o2, e2 = oracle.kda_decode_step(d, pool2, p_kda, ids, qkv, a_kda, b)
+    assert e1 == e2 == 0
+    np.testing.assert_allclose(o2, o1, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(pool2.ssm, pool.ssm, rtol=1e-12, atol=1e-13)
+    np.testing.assert_array_equal(pool2.conv, pool.conv)
+
+
+def test_kda_per_channel_forgetting():
+    """A_log = 0, beta = 0 (b = -inf): a channel whose logit is +1e30 decays
+    to 0 (alpha = exp(-softplus(1e30)) = 0), one at -1e30 keeps its value
+    (alpha = 1); the readout is the kept columns times q_hat."""
+    shape = synth.TINY
+    d = _dims(shape)
+    _, pool, params, qkv, _, _ = _kda_inputs(71)
+    ids = np.array([2], np.int32)
+    p0 = oracle.Params(params.conv_w, np.zeros(d.hv), np.zeros((d.hv, d.dk)))
+    keep = (np.arange(d.dk) % 3) != 0
+    a = np.where(keep, -1e30, 1e30)[None, None, :].repeat(d.hv, axis=1)
+    b = np.full((1, d.hv), -np.inf)
+    S0 = pool.ssm[2].copy()
+    y = oracle.conv_silu(d, pool.conv[2], qkv[0], params.conv_w)
+    o, err = oracle.kda_decode_step(d, pool, p0, ids, qkv[:1], a, b)
+    assert err == 0
+    np.testing.assert_array_equal(pool.ssm[2][:, :, ~keep], 0.0)
+    np.testing.assert_array_equal(pool.ssm[2][:, :, keep], S0[:, :, keep])
+    G = d.hv // d.hk
+    for h in range(d.hv):
+        qraw = y[(h // G) * d.dk:(h // G + 1) * d.dk]
+        qh = qraw / math.sqrt(qraw @ qraw + EPS) / math.sqrt(d.dk)
+        np.testing.assert_allclose(o[0, h], S0[h][:, keep] @ qh[keep], rtol=1e-12, atol=1e-14)
+
+
+def test_kda_retrieval_for_any_channel_decay():
+    """beta = 1: S_new^T k_hat = v (1 - delta) + delta S^T (alpha . k_hat),
+    delta = eps / (|k|^2 + eps), whatever the per-channel alpha."""
+    shape = synth.TINY
+    d = _dims(shape)
+    g, pool, params, qkv, _, _ = _kda_inputs(72)
+    ids = np.array([4], np.int32)
+    dt = synth.normal((d.hv, d.dk), 1.0, g).double().numpy()
+    pk = oracle.Params(params.conv_w, params.A_log, dt)
+    a = synth.normal((1, d.hv, d.dk), 1.5, g).double().numpy()
+    b = np.full((1, d.hv), np.inf)
+    S0 = pool.ssm[4].copy()
+    y = oracle.conv_silu(d, pool.conv[4], qkv[0], params.conv_w)
+    oracle.kda_decode_step(d, pool, pk, ids, qkv[:1], a, b)
+    G = d.hv // d.hk
+    for h in range(d.hv):
+        hq = h // G
+        kraw = y[d.hk * d.dk + hq * d.dk: d.hk * d.dk + (hq + 1) * d.dk]
+        kh = kraw / math.sqrt(kraw @ kraw + EPS)
+        delta = EPS / (kraw @ kraw + EPS)
+        vv = y[2 * d.hk * d.dk + h * d.dv: 2 * d.hk * d.dk + (h + 1) * d.dv]
+        alpha = np.exp([oracle.gate_g(pk.A_log[h], dt[h, c], a[0, h, c]) for c in range(d.dk)])
+        assert np.ptp(alpha) > 0.1  # the decays really differ by channel
+        np.testing.assert_allclose(pool.ssm[4, h] @ kh, vv * (1 - delta) + delta * (S0[h] @ (alpha * kh)),
+                                   rtol=1e-11, atol=1e-12)
