@@ -601,6 +601,25 @@ def measure_rows(gdn, synth, dev, stream, hbm_peak, bf16_peak, which="all", pref
     del qkv, a, b, pout, wsp
     torch.cuda.synchronize()
     if full:
+        # KDA decode, batch 64: the per-channel gate logits replace the per-head
+        # ones (+ 32 x 128 x 2 bytes per token) and dt_bias is per channel
+        kp = gdn.LayerParams(params.conv_w, params.A_log,
+                             synth.normal((shape.hv, shape.dk), 0.5, g).to(dev))
+        ksets = [perm[k * 64:(k + 1) * 64].to(dev) for k in range(8)]
+        kin = [(synth.tokens(shape, g, (64,))[0].to(dev),
+                synth.normal((64, shape.hv, shape.dk), 1.0, g, shape.act_dtype).to(dev),
+                synth.tokens(shape, g, (64,))[2].to(dev)) for _ in range(8)]
+        kout = torch.empty((64, shape.hv, shape.dv), dtype=torch.bfloat16, device=dev)
+
+        def fk(i):
+            q, ka, kb = kin[i % 8]
+            gdn.kda_decode_step(dims, pool, kp, ksets[i % 8], q, ka, kb, kout)
+        fk(0)
+        kbytes = 64 * (DECODE_TOKEN_BYTES - 2 * 32 * 2 + 32 * 128 * 2 + 32 * 2) + DECODE_STEP_PARAM_BYTES \
+            + 32 * 128 * 4
+        rk = frac(kbytes, _events_time(fk, reps, stream))
+        rk["tokens_per_s"] = 64 / (rk["ms"] * 1e-3)
+        rows["kda_decode_b64"] = rk
         rows["mixed_b64_plus_4x256"] = _mixed_row(gdn, synth, dims, pool, params, perm, g, dev, stream)
         # readout epilogue over a 4 x 8192-token prefill output: o and z read,
         # y written in place (3 x 256 bytes per (token, V head) row)

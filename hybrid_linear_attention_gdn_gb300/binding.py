@@ -21,8 +21,8 @@ F32, BF16 = 0, 1
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_SCRATCH_LIMIT = 0, 1, 2, 3, 4
 DEV_ERR_SLOT_OOB, DEV_ERR_TIMEOUT, DEV_ERR_SEQLENS = 1, 2, 4
 (K_DECODE, K_SPEC_VERIFY, K_SLOT_COPY, K_SLOT_ZERO, K_SPEC_COMMIT, K_PREFILL, K_COMMIT_INDEX,
- K_STATE_PACK, K_GATED_RMSNORM) = range(9)
-K_COUNT = 9
+ K_STATE_PACK, K_GATED_RMSNORM, K_KDA_DECODE) = range(10)
+K_COUNT = 10
 
 _DT_CODE = {torch.float32: F32, torch.bfloat16: BF16}
 
@@ -60,6 +60,7 @@ _PP = ctypes.POINTER(CParams)
 
 EXPORTS = {
     "gdn_decode_step": ([_PD, CPool, _PP, _P, _I32, _P, _P, _P, _P, _P, _P], _I32),
+    "gdn_kda_decode_step": ([_PD, CPool, _PP, _P, _I32, _P, _P, _P, _P, _P, _P], _I32),
     "gdn_spec_verify": ([_PD, CPool, CPool, _PP, _P, _P, _I32, _I32, _P, _P, _P, _P, _P, _P], _I32),
     "gdn_spec_commit": ([_PD, CPool, CPool, _P, _P, _P, _I32, _I32, _P, _P], _I32),
     "gdn_chunk_prefill_workspace_size": ([_PD, _I32, _I64], ctypes.c_size_t),
@@ -211,6 +212,18 @@ def decode_step(dims: Dims, pool: StatePool, params: LayerParams, slot_ids, qkv,
                            int(slot_ids.shape[0]), _ptr(qkv), _ptr(a), _ptr(b), _ptr(out),
                            _ptr(dev_err), _stream(stream))
     _check("gdn_decode_step", st)
+
+
+def kda_decode_step(dims: Dims, pool: StatePool, params: LayerParams, slot_ids, qkv, a, b, out,
+                    dev_err=None, stream=None):
+    """KDA decode: the gated delta rule with one decay per key channel; a is
+    [B][hv][dk] gate logits and params.dt_bias [hv][dk]."""
+    L = load()
+    cd, cp = dims.c(), params.c()
+    st = L.gdn_kda_decode_step(ctypes.byref(cd), pool.c(), ctypes.byref(cp), _ptr(slot_ids),
+                               int(slot_ids.shape[0]), _ptr(qkv), _ptr(a), _ptr(b), _ptr(out),
+                               _ptr(dev_err), _stream(stream))
+    _check("gdn_kda_decode_step", st)
 
 
 def spec_verify(dims: Dims, work: StatePool, spec: StatePool, params: LayerParams, slot_ids,

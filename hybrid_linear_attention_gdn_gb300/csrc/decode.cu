@@ -134,13 +134,18 @@ __device__ __forceinline__ void block_norms(const float* sq, const float* sk, fl
 // ---------------------------------------------------------------------------
 // Decode: one token per request.
 // ---------------------------------------------------------------------------
-template <int DK, int NIT, typename Tact, typename Tconv>
+// KDA (Kimi Delta Attention, the per-key-channel decay variant: a [B][hv][dk]
+// gate logits, dt_bias [hv][dk]): column i of St decays by its own alpha_i,
+//   u = v - St (alpha . k^) ; St' = St diag(alpha) + beta u k^T ;
+//   o = St (alpha . q^) + beta u (k^ . q^).
+template <int DK, int NIT, typename Tact, typename Tconv, bool KDA>
 __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const StepArgs a) {
   pdl_wait();
   pdl_trigger();
   using M = RowMap<DK>;
   constexpr int R = NIT * M::RI;
   __shared__ float sq[DK], sk[DK], sv[R], so[R];
+  __shared__ float sal[KDA ? DK : 1];
   __shared__ float sraw[kMaxW][2 * DK];
   __shared__ float sred[3][kWarps];
   __shared__ float sscal[8];
@@ -218,17 +223,30 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const StepArgs a) {
     sscal[3] = rq;
     sscal[4] = rk;
     sscal[5] = sscal[2] * rq * rk;  // k^ . q^
-    sscal[6] = gate_alpha(a.A_log[h], a.dt_bias[h], to_f32(av[h]));
+    if (!KDA) sscal[6] = gate_alpha(a.A_log[h], a.dt_bias[h], to_f32(av[h]));
     sscal[7] = sigmoid_f(to_f32(bv[h]));
   }
+  if (KDA) {
+    const Tact* av = reinterpret_cast<const Tact*>(a.a) + ((size_t)r * a.hv + h) * DK;
+    for (int i = tid; i < DK; i += kThreads)
+      sal[i] = gate_alpha(a.A_log[h], a.dt_bias[(size_t)h * DK + i], to_f32(av[i]));
+  }
   __syncthreads();
-  const float rq = sscal[3], rk = sscal[4], kq = sscal[5], alpha = sscal[6], beta = sscal[7];
-  float4 kk[4], qq[4];
+  const float rq = sscal[3], rk = sscal[4], kq = sscal[5], alpha = KDA ? 1.f : sscal[6], beta = sscal[7];
+  // kk = k^ (the rank-1 term); qq = alpha . q^ and, inside the dot product,
+  // alpha . k^ (KDA; the scalar alpha of GDN is applied to the dot products)
+  float4 kk[4], qq[4], al[4];
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const int col = M::col(c, seg);
     kk[c] = make_float4(sk[col] * rk, sk[col + 1] * rk, sk[col + 2] * rk, sk[col + 3] * rk);
     qq[c] = make_float4(sq[col] * rq, sq[col + 1] * rq, sq[col + 2] * rq, sq[col + 3] * rq);
+    if (KDA) {
+      al[c] = make_float4(sal[col], sal[col + 1], sal[col + 2], sal[col + 3]);
+      qq[c] = make_float4(qq[c].x * al[c].x, qq[c].y * al[c].y, qq[c].z * al[c].z, qq[c].w * al[c].w);
+    } else {
+      al[c] = make_float4(alpha, alpha, alpha, alpha);
+    }
   }
 
   // 4. gated delta rule + readout, row by row
@@ -240,7 +258,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const StepArgs a) {
     float dk_ = 0.f, dq_ = 0.f;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      dk_ += dot4(s[it][c], kk[c]);
+      dk_ += KDA ? dot4(make_float4(s[it][c].x * al[c].x, s[it][c].y * al[c].y, s[it][c].z * al[c].z,
+                                    s[it][c].w * al[c].w),
+                        kk[c])
+                 : dot4(s[it][c], kk[c]);
       dq_ += dot4(s[it][c], qq[c]);
     }
 #pragma unroll
@@ -254,10 +275,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const StepArgs a) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         float4 v = s[it][c];
-        v.x = fmaf(bu, kk[c].x, alpha * v.x);
-        v.y = fmaf(bu, kk[c].y, alpha * v.y);
-        v.z = fmaf(bu, kk[c].z, alpha * v.z);
-        v.w = fmaf(bu, kk[c].w, alpha * v.w);
+        v.x = fmaf(bu, kk[c].x, al[c].x * v.x);
+        v.y = fmaf(bu, kk[c].y, al[c].y * v.y);
+        v.z = fmaf(bu, kk[c].z, al[c].z * v.z);
+        v.w = fmaf(bu, kk[c].w, al[c].w * v.w);
         st_stream(dst + M::col(c, seg) / 4, v);
       }
       if (seg == 0) so[row] = fmaf(bu, kq, alpha * dq_);
@@ -453,11 +474,12 @@ __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const StepArgs a) {
 // host side
 // ---------------------------------------------------------------------------
 template <int DK, int NIT, typename Tact, typename Tconv>
-cudaError_t launch_decode_t(const StepArgs& a, cudaStream_t s) {
+cudaError_t launch_decode_t(const StepArgs& a, bool kda, cudaStream_t s) {
   // the G*P CTAs of a QK head form one cluster (shared q/k history writer)
   const dim3 cluster(a.G * a.P > 1 ? (unsigned)(a.G * a.P) : 1u);
-  return launch_pdl(decode_kernel<DK, NIT, Tact, Tconv>, dim3((unsigned)(a.hv * a.P), (unsigned)a.B),
-                    dim3(kThreads), 0, s, cluster, a);
+  const dim3 grid((unsigned)(a.hv * a.P), (unsigned)a.B);
+  if (kda) return launch_pdl(decode_kernel<DK, NIT, Tact, Tconv, true>, grid, dim3(kThreads), 0, s, cluster, a);
+  return launch_pdl(decode_kernel<DK, NIT, Tact, Tconv, false>, grid, dim3(kThreads), 0, s, cluster, a);
 }
 
 template <int DK, int NIT, typename Tact, typename Tconv>
@@ -473,15 +495,15 @@ cudaError_t launch_verify_t(const StepArgs& a, cudaStream_t s) {
 }
 
 template <int DK, int NIT>
-cudaError_t dispatch_dtype(bool verify, const StepArgs& a, int act, int cv, cudaStream_t s) {
+cudaError_t dispatch_dtype(bool verify, bool kda, const StepArgs& a, int act, int cv, cudaStream_t s) {
   if (act == GDN_F32 && cv == GDN_F32)
     return verify ? launch_verify_t<DK, NIT, float, float>(a, s)
-                  : launch_decode_t<DK, NIT, float, float>(a, s);
+                  : launch_decode_t<DK, NIT, float, float>(a, kda, s);
   if (act == GDN_BF16 && cv == GDN_BF16)
     return verify ? launch_verify_t<DK, NIT, __nv_bfloat16, __nv_bfloat16>(a, s)
-                  : launch_decode_t<DK, NIT, __nv_bfloat16, __nv_bfloat16>(a, s);
+                  : launch_decode_t<DK, NIT, __nv_bfloat16, __nv_bfloat16>(a, kda, s);
   return verify ? launch_verify_t<DK, NIT, __nv_bfloat16, float>(a, s)
-                : launch_decode_t<DK, NIT, __nv_bfloat16, float>(a, s);
+                : launch_decode_t<DK, NIT, __nv_bfloat16, float>(a, kda, s);
 }
 
 // rows-per-CTA choice: fewer rows (more CTAs, smaller clusters of work) when
@@ -539,7 +561,7 @@ bool use_tma_verify(const gdn_dims& d, int32_t B, int32_t T, const void* qkv, co
   return (long)B * d.hv >= 6L * sm_count();
 }
 
-gdn_status run_step(bool verify, const gdn_dims* dims, const gdn_pool& work, const gdn_pool* spec,
+gdn_status run_step(bool verify, bool kda, const gdn_dims* dims, const gdn_pool& work, const gdn_pool* spec,
                     const gdn_params* params, const int32_t* slot_ids, const int32_t* spec_ids,
                     int32_t B, int32_t T, const void* qkv, const void* a, const void* b, void* out,
                     uint32_t* dev_err, void* stream) {
@@ -556,9 +578,11 @@ gdn_status run_step(bool verify, const gdn_dims* dims, const gdn_pool& work, con
   const int G = dims->hv / dims->hk;
   if (G > 8) return GDN_ERR_UNSUPPORTED;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  if (!verify && use_tma_decode(*dims, B, qkv, *params)) {
-    cudaError_t e = decode_tma_launch(*dims, work, *params, slot_ids, B, qkv, a, b, out, dev_err, cs);
-    if (e == cudaSuccess) count_launch(GDN_K_DECODE);
+  // KDA's gate logits and dt_bias reach the TMA-fed kernel by bulk copies
+  const bool kda_aligned = !kda || (aligned(a, 16) && aligned(params->dt_bias, 16));
+  if (!verify && kda_aligned && use_tma_decode(*dims, B, qkv, *params)) {
+    cudaError_t e = decode_tma_launch(*dims, work, *params, slot_ids, B, qkv, a, b, out, dev_err, kda, cs);
+    if (e == cudaSuccess) count_launch(kda ? GDN_K_KDA_DECODE : GDN_K_DECODE);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
   }
   if (verify && use_tma_verify(*dims, B, T, qkv, *params)) {
@@ -602,18 +626,18 @@ gdn_status run_step(bool verify, const gdn_dims* dims, const gdn_pool& work, con
   const int act = dims->act_dtype, cv = dims->conv_dtype;
   cudaError_t e = cudaErrorInvalidValue;
   switch (dims->dk) {
-    case 16: e = dispatch_dtype<16, 1>(verify, s, act, cv, cs); break;
+    case 16: e = dispatch_dtype<16, 1>(verify, kda, s, act, cv, cs); break;
     case 64:
-      e = nit == 1 ? dispatch_dtype<64, 1>(verify, s, act, cv, cs)
-                   : dispatch_dtype<64, 2>(verify, s, act, cv, cs);
+      e = nit == 1 ? dispatch_dtype<64, 1>(verify, kda, s, act, cv, cs)
+                   : dispatch_dtype<64, 2>(verify, kda, s, act, cv, cs);
       break;
     case 128:
-      e = nit == 1   ? dispatch_dtype<128, 1>(verify, s, act, cv, cs)
-          : nit == 2 ? dispatch_dtype<128, 2>(verify, s, act, cv, cs)
-                     : dispatch_dtype<128, 4>(verify, s, act, cv, cs);
+      e = nit == 1   ? dispatch_dtype<128, 1>(verify, kda, s, act, cv, cs)
+          : nit == 2 ? dispatch_dtype<128, 2>(verify, kda, s, act, cv, cs)
+                     : dispatch_dtype<128, 4>(verify, kda, s, act, cv, cs);
       break;
   }
-  if (e == cudaSuccess) count_launch(verify ? GDN_K_SPEC_VERIFY : GDN_K_DECODE);
+  if (e == cudaSuccess) count_launch(kda ? GDN_K_KDA_DECODE : verify ? GDN_K_SPEC_VERIFY : GDN_K_DECODE);
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
@@ -624,7 +648,15 @@ extern "C" gdn_status gdn_decode_step(const gdn_dims* dims, gdn_pool pool, const
                                       const int32_t* slot_ids, int32_t B, const void* qkv,
                                       const void* a, const void* b, void* out, uint32_t* dev_err,
                                       void* stream) {
-  return gdn::run_step(false, dims, pool, nullptr, params, slot_ids, nullptr, B, 1, qkv, a, b, out,
+  return gdn::run_step(false, false, dims, pool, nullptr, params, slot_ids, nullptr, B, 1, qkv, a, b, out,
+                       dev_err, stream);
+}
+
+extern "C" gdn_status gdn_kda_decode_step(const gdn_dims* dims, gdn_pool pool, const gdn_params* params,
+                                          const int32_t* slot_ids, int32_t B, const void* qkv,
+                                          const void* a, const void* b, void* out, uint32_t* dev_err,
+                                          void* stream) {
+  return gdn::run_step(false, true, dims, pool, nullptr, params, slot_ids, nullptr, B, 1, qkv, a, b, out,
                        dev_err, stream);
 }
 
@@ -633,6 +665,6 @@ extern "C" gdn_status gdn_spec_verify(const gdn_dims* dims, gdn_pool work, gdn_p
                                       const int32_t* spec_ids, int32_t B, int32_t T,
                                       const void* qkv, const void* a, const void* b, void* out,
                                       uint32_t* dev_err, void* stream) {
-  return gdn::run_step(true, dims, work, &spec, params, slot_ids, spec_ids, B, T, qkv, a, b, out,
+  return gdn::run_step(true, false, dims, work, &spec, params, slot_ids, spec_ids, B, T, qkv, a, b, out,
                        dev_err, stream);
 }

@@ -19,12 +19,18 @@
 // The producer runs up to STAGES chunks (and the next bundle) ahead, so HBM
 // reads continue while the consumers are in an item's prologue.
 //
+// KDA (the per-key-channel decay variant: gate logits a [B][hv][dk], dt_bias
+// [hv][dk]) uses the same walk with one alpha per (V head, key channel), kept
+// in shared memory per item: u = v - St (alpha . k^), St' = St diag(alpha) +
+// beta u k^T, o = St (alpha . q^) + beta u (k^ . q^).
+//
 // Every mbarrier wait is bounded (1 s); on a timeout the CTA sets
 // GDN_DEV_ERR_TIMEOUT, stops issuing, waits (bounded) for the copies it has in
 // flight and returns.
 #include "gdn_common.cuh"
 #include "decode_tma.cuh"
 
+#include <cstddef>
 #include <cstdlib>
 
 namespace gdn {
@@ -43,22 +49,36 @@ constexpr int kMaxGR = 256;        // G * dv rows per item, at most
 constexpr int kMaxCh = 2 * kDK + kMaxGR;
 constexpr int kBarCons = 1;        // named barrier of the consumer warps
 
-template <typename Tact, typename Tconv, int STAGES>
+template <typename Tact, typename Tconv, int STAGES, bool KDA>
 struct __align__(128) TmaSmem {
   float ring[STAGES][kStageFloats];
-  struct Bundle {
+  // every member is a bulk-copy destination: 16-byte aligned, and so is the
+  // size, so that bundle[1] is too
+  struct __align__(16) Bundle {
     Tconv hist[kW - 1][kMaxCh];  // [q | k | v of the group] per history row
     Tact x[kMaxCh];
     float w[kMaxCh * kW];
+    __align__(16) Tact ga[KDA ? kMaxGR / kRows * kDK : 8];      // KDA: gate logits of the G V heads
+    __align__(16) float gdt[KDA ? kMaxGR / kRows * kDK : 4];   // KDA: their dt_bias
   } bundle[2];
   float sy[kMaxCh];    // conv + SiLU output: q, k, v of the group
   float so[kMaxGR];    // readout of the group's rows
   float sred[3][kCW];
   float sgate[2][8];   // alpha, beta per V head of the group
+  float sal[KDA ? 8 : 1][kDK];  // KDA: alpha per (V head of the group, key channel)
   float snorm[4];      // rq, rk, k^.q^
   uint64_t full[STAGES], empty[STAGES], bfull[2], bempty[2];
   int abort;
 };
+
+template <typename Tact, typename Tconv, int STAGES, bool KDA>
+constexpr bool bundle_aligned() {
+  using SMt = TmaSmem<Tact, Tconv, STAGES, KDA>;
+  using B = typename SMt::Bundle;
+  return sizeof(B) % 16 == 0 && offsetof(B, x) % 16 == 0 && offsetof(B, w) % 16 == 0 &&
+         offsetof(B, ga) % 16 == 0 && offsetof(B, gdt) % 16 == 0 && offsetof(SMt, bundle) % 16 == 0 &&
+         offsetof(SMt, ring) % 16 == 0;
+}
 
 struct TmaArgs {
   float* ssm;
@@ -76,9 +96,9 @@ struct TmaArgs {
   int32_t hk, hv, dv, C, G, n_items;
 };
 
-template <typename Tact, typename Tconv, int STAGES, int MINB>
+template <typename Tact, typename Tconv, int STAGES, int MINB, bool KDA>
 __global__ void __launch_bounds__(kThr, MINB) decode_tma_kernel(const TmaArgs a) {
-  using SM = TmaSmem<Tact, Tconv, STAGES>;
+  using SM = TmaSmem<Tact, Tconv, STAGES, KDA>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   SM& S = *reinterpret_cast<SM*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -109,7 +129,8 @@ __global__ void __launch_bounds__(kThr, MINB) decode_tma_kernel(const TmaArgs a)
     // ------------------------------------------------------------ producer
     if (lane != 0) return;
     const uint32_t esz_c = sizeof(Tconv), esz_a = sizeof(Tact);
-    const uint32_t bundle_bytes = (kW - 1) * nch * esz_c + nch * esz_a + nch * kW * 4;
+    const uint32_t bundle_bytes =
+        (kW - 1) * nch * esz_c + nch * esz_a + nch * kW * 4 + (KDA ? a.G * kDK * (esz_a + 4) : 0);
     uint32_t n = 0, vk = 0;
     bool ok = true;
     for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
@@ -136,6 +157,12 @@ __global__ void __launch_bounds__(kThr, MINB) decode_tma_kernel(const TmaArgs a)
       bulk_g2s(&B.w[0], a.conv_w + cq * kW, kDK * kW * 4, &S.bfull[bb]);
       bulk_g2s(&B.w[kDK * kW], a.conv_w + ck * kW, kDK * kW * 4, &S.bfull[bb]);
       bulk_g2s(&B.w[2 * kDK * kW], a.conv_w + cv * kW, GR * kW * 4, &S.bfull[bb]);
+      if (KDA) {
+        const size_t h0 = (size_t)hq * a.G;
+        bulk_g2s(&B.ga[0], reinterpret_cast<const Tact*>(a.a) + ((size_t)r * a.hv + h0) * kDK,
+                 a.G * kDK * esz_a, &S.bfull[bb]);
+        bulk_g2s(&B.gdt[0], a.dt_bias + h0 * kDK, a.G * kDK * 4, &S.bfull[bb]);
+      }
       ++vk;
       const float* src = a.ssm + ((size_t)slot * a.hv + (size_t)hq * a.G) * a.dv * kDK;
       for (int c = 0; c < nchunks; ++c, ++n) {
@@ -198,11 +225,19 @@ __global__ void __launch_bounds__(kThr, MINB) decode_tma_kernel(const TmaArgs a)
       hist[a.C + c] = B.hist[2][i];
       hist[2 * (size_t)a.C + c] = from_f32<Tconv>(xv);
     }
+    if (KDA) {
+      for (int e = tid; e < a.G * kDK; e += kCons) {
+        const int gi = e / kDK, h = hq * a.G + gi;
+        S.sal[gi][e % kDK] = gate_alpha(a.A_log[h], B.gdt[e], to_f32(B.ga[e]));
+      }
+    }
     if (tid < a.G) {
       const int h = hq * a.G + tid;
-      const float av = to_f32(reinterpret_cast<const Tact*>(a.a)[(size_t)r * a.hv + h]);
       const float bv = to_f32(reinterpret_cast<const Tact*>(a.b)[(size_t)r * a.hv + h]);
-      S.sgate[0][tid] = gate_alpha(a.A_log[h], a.dt_bias[h], av);
+      if (!KDA) {
+        const float av = to_f32(reinterpret_cast<const Tact*>(a.a)[(size_t)r * a.hv + h]);
+        S.sgate[0][tid] = gate_alpha(a.A_log[h], a.dt_bias[h], av);
+      }
       S.sgate[1][tid] = sigmoid_f(bv);
     }
     named_sync(kBarCons, kCons);
@@ -255,23 +290,37 @@ __global__ void __launch_bounds__(kThr, MINB) decode_tma_kernel(const TmaArgs a)
       qq[c] = make_float4(q4.x * rq, q4.y * rq, q4.z * rq, q4.w * rq);
     }
     float* dst_base = a.ssm + ((size_t)slot * a.hv + (size_t)hq * a.G) * a.dv * kDK;
+    // KDA: this lane's alphas of the current V head (a chunk's 32 rows belong
+    // to one head; reloaded only when the head changes)
+    float4 al[4];
+    int g_al = -1;
     for (int c = 0; c < nchunks; ++c, ++n) {
       const int st = n % STAGES;
       if (!*abort_flag && !mbar_wait(&S.full[st], (n / STAGES) & 1)) *abort_flag = 1;
       if (*abort_flag) continue;
       const int grow = c * kRows + rloc;  // row within the group
       const int g = grow / a.dv;
-      const float alpha = S.sgate[0][g], beta = S.sgate[1][g];
+      const float alpha = KDA ? 1.f : S.sgate[0][g], beta = S.sgate[1][g];
       const float* srow = S.ring[st] + rloc * kDK;
       float4 s4[4];
+      if (g != g_al) {
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc)
-        s4[cc] = *reinterpret_cast<const float4*>(srow + cc * 4 * kLPR + seg * 4);
+        for (int cc = 0; cc < 4; ++cc)
+          al[cc] = KDA ? *reinterpret_cast<const float4*>(&S.sal[KDA ? g : 0][cc * 4 * kLPR + seg * 4])
+                       : make_float4(alpha, alpha, alpha, alpha);
+        g_al = g;
+      }
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) s4[cc] = *reinterpret_cast<const float4*>(srow + cc * 4 * kLPR + seg * 4);
       float dk_ = 0.f, dq_ = 0.f;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
-        dk_ += s4[cc].x * kk[cc].x + s4[cc].y * kk[cc].y + s4[cc].z * kk[cc].z + s4[cc].w * kk[cc].w;
-        dq_ += s4[cc].x * qq[cc].x + s4[cc].y * qq[cc].y + s4[cc].z * qq[cc].z + s4[cc].w * qq[cc].w;
+        // KDA: the decayed row St diag(alpha) meets k^ and q^
+        const float4 sa = KDA ? make_float4(s4[cc].x * al[cc].x, s4[cc].y * al[cc].y, s4[cc].z * al[cc].z,
+                                            s4[cc].w * al[cc].w)
+                              : s4[cc];
+        dk_ += sa.x * kk[cc].x + sa.y * kk[cc].y + sa.z * kk[cc].z + sa.w * kk[cc].w;
+        dq_ += sa.x * qq[cc].x + sa.y * qq[cc].y + sa.z * qq[cc].z + sa.w * qq[cc].w;
       }
       __syncwarp();  // every lane has consumed its part of the stage
       if (lane == 0) mbar_arrive(&S.empty[st]);  // the producer may refill it
@@ -285,10 +334,10 @@ __global__ void __launch_bounds__(kThr, MINB) decode_tma_kernel(const TmaArgs a)
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         float4 v = s4[cc];
-        v.x = fmaf(bu, kk[cc].x, alpha * v.x);
-        v.y = fmaf(bu, kk[cc].y, alpha * v.y);
-        v.z = fmaf(bu, kk[cc].z, alpha * v.z);
-        v.w = fmaf(bu, kk[cc].w, alpha * v.w);
+        v.x = fmaf(bu, kk[cc].x, al[cc].x * v.x);
+        v.y = fmaf(bu, kk[cc].y, al[cc].y * v.y);
+        v.z = fmaf(bu, kk[cc].z, al[cc].z * v.z);
+        v.w = fmaf(bu, kk[cc].w, al[cc].w * v.w);
         st_stream(drow + (cc * 4 * kLPR + seg * 4) / 4, v);
       }
       if (seg == 0) S.so[grow] = fmaf(bu, kq, alpha * dq_);
@@ -300,10 +349,11 @@ __global__ void __launch_bounds__(kThr, MINB) decode_tma_kernel(const TmaArgs a)
   if (*abort_flag && tid == 0) report(a.err, GDN_DEV_ERR_TIMEOUT);
 }
 
-template <typename Tact, typename Tconv, int STAGES, int MINB>
+template <typename Tact, typename Tconv, int STAGES, int MINB, bool KDA>
 cudaError_t launch_tma(const TmaArgs& a, cudaStream_t s) {
-  using SM = TmaSmem<Tact, Tconv, STAGES>;
-  auto k = decode_tma_kernel<Tact, Tconv, STAGES, MINB>;
+  using SM = TmaSmem<Tact, Tconv, STAGES, KDA>;
+  static_assert(bundle_aligned<Tact, Tconv, STAGES, KDA>(), "bulk-copy destinations must be 16-byte aligned");
+  auto k = decode_tma_kernel<Tact, Tconv, STAGES, MINB, KDA>;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -323,11 +373,11 @@ cudaError_t launch_tma(const TmaArgs& a, cudaStream_t s) {
 // 32: 0.76 vs 0.71 of HBM peak; batch 48: 0.82 vs 0.80), one per SM above
 // (batch 64: 0.88 vs 0.83; batch 128: 0.93 vs 0.89).
 template <typename Tact, typename Tconv>
-cudaError_t launch_tma_dt(const TmaArgs& a, cudaStream_t s) {
+cudaError_t launch_tma_dt(const TmaArgs& a, bool kda, cudaStream_t s) {
   const int forced = tma_ctas_per_sm();
   const bool two = forced ? forced == 2 : a.n_items < 6 * sm_count();
-  if (two) return launch_tma<Tact, Tconv, 4, 2>(a, s);
-  return launch_tma<Tact, Tconv, 10, 1>(a, s);
+  if (kda) return two ? launch_tma<Tact, Tconv, 4, 2, true>(a, s) : launch_tma<Tact, Tconv, 10, 1, true>(a, s);
+  return two ? launch_tma<Tact, Tconv, 4, 2, false>(a, s) : launch_tma<Tact, Tconv, 10, 1, false>(a, s);
 }
 
 }  // namespace
@@ -365,7 +415,7 @@ bool decode_tma_supported(const gdn_dims& d, const void* qkv, const gdn_params& 
 
 cudaError_t decode_tma_launch(const gdn_dims& d, const gdn_pool& pool, const gdn_params& p,
                               const int32_t* slot_ids, int32_t B, const void* qkv, const void* av,
-                              const void* bv, void* out, uint32_t* dev_err, cudaStream_t s) {
+                              const void* bv, void* out, uint32_t* dev_err, bool kda, cudaStream_t s) {
   TmaArgs a;
   a.ssm = pool.ssm;
   a.conv = pool.conv;
@@ -386,9 +436,9 @@ cudaError_t decode_tma_launch(const gdn_dims& d, const gdn_pool& pool, const gdn
   a.G = d.hv / d.hk;
   a.n_items = B * d.hk;
   if (d.act_dtype == GDN_BF16 && d.conv_dtype == GDN_BF16)
-    return launch_tma_dt<__nv_bfloat16, __nv_bfloat16>(a, s);
-  if (d.act_dtype == GDN_BF16) return launch_tma_dt<__nv_bfloat16, float>(a, s);
-  return launch_tma_dt<float, float>(a, s);
+    return launch_tma_dt<__nv_bfloat16, __nv_bfloat16>(a, kda, s);
+  if (d.act_dtype == GDN_BF16) return launch_tma_dt<__nv_bfloat16, float>(a, kda, s);
+  return launch_tma_dt<float, float>(a, kda, s);
 }
 
 }  // namespace gdn

@@ -5,9 +5,10 @@
 namespace gdn {
 // True when the shape, dtypes and pointer alignment fit the TMA-fed kernel.
 bool decode_tma_supported(const gdn_dims& d, const void* qkv, const gdn_params& p);
+// kda: the per-key-channel decay variant (a [B][hv][dk], dt_bias [hv][dk])
 cudaError_t decode_tma_launch(const gdn_dims& d, const gdn_pool& pool, const gdn_params& p,
                               const int32_t* slot_ids, int32_t B, const void* qkv, const void* a,
-                              const void* b, void* out, uint32_t* dev_err, cudaStream_t s);
+                              const void* b, void* out, uint32_t* dev_err, bool kda, cudaStream_t s);
 int sm_count();
 // CTAs per SM for the persistent kernels: 0 = the default choice of each
 // kernel, 1 or 2 forced by GDN_TMA_CTAS (for measurement).

@@ -109,6 +109,24 @@ gdn_status gdn_decode_step(const gdn_dims* dims, gdn_pool pool,
                            void* stream);
 
 /*
+ * KDA decode (TokenSpeed talk, "为什么 Agentic 推理需要新推理引擎": Kimi K3's KDA
+ * is the second linear-attention family whose SSM + conv state the engine
+ * keeps; the pages do not write it).  The published Kimi Delta Attention step:
+ * the gated delta rule with one decay per key channel,
+ *   S <- (I - beta k^ k^T) diag(alpha) S + beta k^ v^T,  o = S^T q^,
+ *   alpha_c = exp(-exp(A_log[h]) * softplus(a[h][c] + dt_bias[h][c])),
+ * over the same slot pool, conv history, q/k norms and beta as
+ * gdn_decode_step.  Arguments as for gdn_decode_step except:
+ *   a [B][hv][dk] (act_dtype): per-channel gate logits
+ *   params->dt_bias [hv][dk] float
+ */
+gdn_status gdn_kda_decode_step(const gdn_dims* dims, gdn_pool pool,
+                               const gdn_params* params, const int32_t* slot_ids,
+                               int32_t B, const void* qkv, const void* a,
+                               const void* b, void* out, uint32_t* dev_err,
+                               void* stream);
+
+/*
  * Speculative verify (TokenSpeed Qwen3.5 page, "Scheduler dual": spec_cache
  * of per-step conv/SSM snapshots for rollback).  Request r runs its T draft
  * tokens starting from working slot slot_ids[r], which is NOT modified; after
@@ -324,7 +342,8 @@ const char* gdn_status_string(int32_t status);
 #define GDN_K_COMMIT_INDEX 6
 #define GDN_K_STATE_PACK 7 /* pack and unpack */
 #define GDN_K_GATED_RMSNORM 8
-#define GDN_K_COUNT 9
+#define GDN_K_KDA_DECODE 9
+#define GDN_K_COUNT 10
 uint64_t gdn_launch_count(int32_t kernel);
 void gdn_launch_count_reset(void);
 

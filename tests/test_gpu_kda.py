@@ -1,0 +1,113 @@
+"""GPU KDA decode (per-key-channel decay) against the oracle's KDA step: the
+Qwen3.5-shaped layer at several batches, other shapes, 32 chained steps,
+padding, and uniform gates reducing to the GDN step."""
+import numpy as np
+import pytest
+import torch
+
+import hybrid_linear_attention_gdn_gb300 as gdn
+import oracle
+from hybrid_linear_attention_gdn_gb300 import LayerParams, synth
+from helpers import (STATE_TOL_1, STATE_TOL_64, Setup, assert_out_close, conv_bits_equal, max_rel_l2,
+                     out_tol, to_np)
+
+pytestmark = pytest.mark.gpu
+
+
+def _kda_params(st: Setup, seed):
+    """The layer's conv weights and A_log with a per-channel dt_bias [hv][dk]."""
+    g = synth.generator(seed)
+    dt = synth.normal((st.shape.hv, st.shape.dk), 0.5, g)
+    params = LayerParams(st.params.conv_w, st.params.A_log, dt.cuda())
+    oparams = oracle.Params(st.oparams.conv_w, st.oparams.A_log, dt.double().numpy())
+    return params, oparams
+
+
+def _gates(st: Setup, lead):
+    """Per-channel gate logits [*lead][hv][dk] in the activation dtype."""
+    return synth.normal(lead + (st.shape.hv, st.shape.dk), 1.0, st.gen, st.shape.act_dtype)
+
+
+@pytest.mark.parametrize("shape,B", [
+    (synth.QWEN, 64), (synth.QWEN, 16), (synth.QWEN, 1), (synth.TINY, 5),
+    (synth.QWEN.replace(hk=2, hv=8, dk=64, dv=64), 7),
+    (synth.QWEN.replace(act="f32", conv="f32", hk=4, hv=8), 9),
+], ids=["qwen_b64", "qwen_b16", "qwen_b1", "tiny_f32", "dk64_g4", "f32_b9"])
+def test_kda_decode_vs_oracle(cuda, shape, B):
+    n_slots = 8 if shape is synth.TINY else 80
+    st = Setup(shape, seed=80 + B, num_slots=n_slots)
+    params, oparams = _kda_params(st, 81)
+    ids = synth.slot_ids(n_slots, B, st.gen)
+    qkv, _, b = st.tokens((B,))
+    a = _gates(st, (B,))
+    out = torch.empty((B, shape.hv, shape.dv), dtype=shape.act_dtype, device="cuda")
+    n0 = gdn.launch_count(gdn.K_KDA_DECODE)
+    gdn.kda_decode_step(st.dims, st.pool, params, ids.cuda(), qkv.cuda(), a.cuda(), b.cuda(), out)
+    o_ref, err = oracle.kda_decode_step(st.od, st.opool, oparams, ids.numpy(), to_np(qkv), to_np(a),
+                                        to_np(b))
+    torch.cuda.synchronize()
+    assert err == 0 and gdn.launch_count(gdn.K_KDA_DECODE) == n0 + 1
+    assert_out_close(out, o_ref, shape.dv, out_tol(shape))
+    used = ids.tolist()
+    assert max_rel_l2(to_np(st.pool.ssm[used]), st.opool.ssm[used], shape.dv * shape.dk) <= STATE_TOL_1
+    assert conv_bits_equal(st.pool.conv, st.opool.conv)
+    rest = [s for s in range(n_slots) if s not in used]
+    assert torch.equal(st.pool.ssm[rest].cpu(), torch.from_numpy(st.opool.ssm[rest]).float())
+
+
+def test_kda_32_chained_steps(cuda):
+    shape = synth.QWEN
+    st = Setup(shape, seed=82, num_slots=24)
+    params, oparams = _kda_params(st, 83)
+    B = 12
+    ids = synth.slot_ids(24, B, st.gen)
+    out = torch.empty((B, shape.hv, shape.dv), dtype=shape.act_dtype, device="cuda")
+    for _ in range(32):
+        qkv, _, b = st.tokens((B,))
+        a = _gates(st, (B,))
+        gdn.kda_decode_step(st.dims, st.pool, params, ids.cuda(), qkv.cuda(), a.cuda(), b.cuda(), out)
+        o_ref, _ = oracle.kda_decode_step(st.od, st.opool, oparams, ids.numpy(), to_np(qkv), to_np(a),
+                                          to_np(b))
+    torch.cuda.synchronize()
+    assert_out_close(out, o_ref, shape.dv, out_tol(shape))
+    used = ids.tolist()
+    assert max_rel_l2(to_np(st.pool.ssm[used]), st.opool.ssm[used], shape.dv * shape.dk) <= STATE_TOL_64
+    assert conv_bits_equal(st.pool.conv[used], st.opool.conv[used])
+
+
+def test_kda_uniform_gates_is_the_gdn_step(cuda):
+    """Every channel of a head given the head's gate logit and bias: the KDA
+    kernel lands on the oracle's GDN step."""
+    shape = synth.QWEN
+    st = Setup(shape, seed=84, num_slots=40)
+    B = 32
+    ids = synth.slot_ids(40, B, st.gen)
+    qkv, a, b = st.tokens((B,))
+    a_kda = a[:, :, None].expand(B, shape.hv, shape.dk).contiguous()
+    dt = st.params.dt_bias[:, None].expand(shape.hv, shape.dk).contiguous()
+    params = LayerParams(st.params.conv_w, st.params.A_log, dt)
+    out = torch.empty((B, shape.hv, shape.dv), dtype=shape.act_dtype, device="cuda")
+    gdn.kda_decode_step(st.dims, st.pool, params, ids.cuda(), qkv.cuda(), a_kda.cuda(), b.cuda(), out)
+    o_ref, _ = oracle.decode_step(st.od, st.opool, st.oparams, ids.numpy(), to_np(qkv), to_np(a), to_np(b))
+    torch.cuda.synchronize()
+    assert_out_close(out, o_ref, shape.dv, out_tol(shape))
+    used = ids.tolist()
+    assert max_rel_l2(to_np(st.pool.ssm[used]), st.opool.ssm[used], shape.dv * shape.dk) <= STATE_TOL_1
+
+
+def test_kda_padding_and_bad_ids(cuda):
+    shape = synth.QWEN
+    st = Setup(shape, seed=85, num_slots=10)
+    params, oparams = _kda_params(st, 86)
+    ids = torch.tensor([3, -1, 10, 7], dtype=torch.int32)
+    qkv, _, b = st.tokens((4,))
+    a = _gates(st, (4,))
+    out = torch.full((4, shape.hv, shape.dv), 9.0, dtype=shape.act_dtype, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gdn.kda_decode_step(st.dims, st.pool, params, ids.cuda(), qkv.cuda(), a.cuda(), b.cuda(), out, err)
+    o_ref, e = oracle.kda_decode_step(st.od, st.opool, oparams, ids.numpy(), to_np(qkv), to_np(a), to_np(b))
+    torch.cuda.synchronize()
+    assert int(err.item()) == e == gdn.DEV_ERR_SLOT_OOB
+    assert torch.all(out[1:3] == 0)
+    assert_out_close(out[[0, 3]], o_ref[[0, 3]], shape.dv, out_tol(shape))
+    assert max_rel_l2(to_np(st.pool.ssm), st.opool.ssm, shape.dv * shape.dk) <= STATE_TOL_1
