@@ -48,8 +48,8 @@ DECODE_STEP_PARAM_BYTES = 8192 * 4 * 4 + 2 * 32 * 4
 # the sha256 of the kernel source it was captured on; reported only while the
 # source is unchanged.
 DECODE_TRAFFIC = {
-    "bytes_per_launch": 138589952 + 77269760,
-    "source_sha256": "2e9d5e5e7003eb310806993e46828ac6483cb1133ee1968b0190ff19a570d534",
+    "bytes_per_launch": 138589440 + 78073856,
+    "source_sha256": "5e61f0355ea21948c588c68cc2ad99a9a58d4a2e91d69b0250e34bab30c41f43",
     "case": "batch 64 over a 128-slot pool (same requests per launch as the headline), one launch after "
             "5 warm-up launches; written bytes fall short of the 138 MB of state written because part "
             "of it is still dirty in L2 when the kernel ends",
