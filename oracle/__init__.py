@@ -296,6 +296,25 @@ def kda_decode_step(dims: Dims, pool: Pool, params: Params, slot_ids, qkv, a, b)
     return out, err.value
 
 
+def kda_spec_verify(dims: Dims, work: Pool, spec: Pool, params: Params, slot_ids, spec_ids, qkv, a, b):
+    """KDA verify: T draft tokens per request from the working slot (only
+    read), the state after draft t into spec slot spec_ids[r][t]; a
+    [B][T][hv][dk].  Returns (out [B][T][hv][dv], err)."""
+    L = lib()
+    slot_ids, spec_ids = _i32(slot_ids), _i32(spec_ids)
+    B, T = spec_ids.shape
+    qkv, a, b = _f64(qkv), _f64(a), _f64(b)
+    assert qkv.shape == (B, T, dims.channels) and a.shape == (B, T, dims.hv, dims.dk)
+    out = np.zeros((B, T, dims.hv, dims.dv), np.float64)
+    err = ctypes.c_uint32(0)
+    cd, cpa = dims.c(), params.c()
+    rc = L.orc_kda_spec_verify(ctypes.byref(cd), work.c(), spec.c(), ctypes.byref(cpa), _ptr(slot_ids),
+                               _ptr(spec_ids), ctypes.c_int32(B), ctypes.c_int32(T), _ptr(qkv), _ptr(a),
+                               _ptr(b), _ptr(out), ctypes.byref(err))
+    assert rc == 0
+    return out, err.value
+
+
 def gated_rmsnorm(dims: Dims, o, z, w, eps=1e-6):
     """Readout epilogue y = o / sqrt(mean(o^2) + eps) * w * silu(z) per
     (token, V head) row; o, z [n_tok][hv][dv], w [dv].  Returns y."""

@@ -443,6 +443,28 @@ void orc_kda_core(int32_t dk, int32_t dv, double* St, const double* k, const dou
   }
 }
 
+/* One KDA token on one slot (conv history and SSM state updated in place):
+ * a_t [hv][dk] gate logits, b_t [hv], o [hv][dv].  work: C + 3 dk doubles. */
+static void kda_token_step(const orc_dims* d, const orc_params* p, double* ssm, double* conv,
+                           const double* x, const double* a_t, const double* b_t, double* o,
+                           double* work) {
+  int64_t C = n_chan(d);
+  int dk = d->dk, G = d->hv / d->hk;
+  double *y = work, *qh = y + C, *kh = qh + dk, *al = kh + dk;
+  orc_conv_silu(d, conv, x, p->conv_w, y);
+  conv_shift(d, conv, x);
+  for (int h = 0; h < d->hv; ++h) {
+    int hq = h / G;
+    orc_l2norm(dk, y + (int64_t)hq * dk, 1.0 / sqrt((double)dk), qh);
+    orc_l2norm(dk, y + (int64_t)(d->hk + hq) * dk, 1.0, kh);
+    for (int c = 0; c < dk; ++c)
+      al[c] = exp(orc_gate_g(p->A_log[h], p->dt_bias[(int64_t)h * dk + c], a_t[(int64_t)h * dk + c]));
+    orc_kda_core(dk, d->dv, ssm + (int64_t)h * d->dv * dk, kh,
+                 y + 2 * (int64_t)d->hk * dk + (int64_t)h * d->dv, qh, al, orc_sigmoid(b_t[h]),
+                 o + (int64_t)h * d->dv);
+  }
+}
+
 /* KDA decode: as orc_decode_step (same pool, conv, norms, beta), with the
  * gate logits a [B][hv][dk] and dt_bias [hv][dk] per key channel. */
 int orc_kda_decode_step(const orc_dims* d, orc_pool pool, const orc_params* p,
@@ -450,8 +472,6 @@ int orc_kda_decode_step(const orc_dims* d, orc_pool pool, const orc_params* p,
                         const double* a, const double* b, double* out, uint32_t* err) {
   if (check_dims(d)) return 1;
   int64_t C = n_chan(d), HVDV = (int64_t)d->hv * d->dv;
-  int dk = d->dk, G = d->hv / d->hk;
-  double qscale = 1.0 / sqrt((double)dk);
   int64_t fail = 0;
 #pragma omp parallel for schedule(dynamic, 1) reduction(| : fail)
   for (int32_t r = 0; r < B; ++r) {
@@ -463,24 +483,51 @@ int orc_kda_decode_step(const orc_dims* d, orc_pool pool, const orc_params* p,
       for (int64_t i = 0; i < HVDV; ++i) o[i] = 0.0;
       continue;
     }
-    double* y = (double*)malloc(sizeof(double) * (C + 3 * (int64_t)dk));
-    double *qh = y + C, *kh = qh + dk, *al = kh + dk;
-    double* conv = pool.conv + s * conv_elems(d);
-    orc_conv_silu(d, conv, qkv + r * C, p->conv_w, y);
-    conv_shift(d, conv, qkv + r * C);
-    for (int h = 0; h < d->hv; ++h) {
-      int hq = h / G;
-      orc_l2norm(dk, y + (int64_t)hq * dk, qscale, qh);
-      orc_l2norm(dk, y + (int64_t)(d->hk + hq) * dk, 1.0, kh);
-      const double* ah = a + ((int64_t)r * d->hv + h) * dk;
-      for (int c = 0; c < dk; ++c)
-        al[c] = exp(orc_gate_g(p->A_log[h], p->dt_bias[(int64_t)h * dk + c], ah[c]));
-      double beta = orc_sigmoid(b[(int64_t)r * d->hv + h]);
-      orc_kda_core(dk, d->dv, pool.ssm + s * ssm_elems(d) + (int64_t)h * d->dv * dk, kh,
-                   y + 2 * (int64_t)d->hk * dk + (int64_t)h * d->dv, qh, al, beta,
-                   o + (int64_t)h * d->dv);
+    double* work = (double*)malloc(sizeof(double) * (C + 3 * (int64_t)d->dk));
+    kda_token_step(d, p, pool.ssm + s * ssm_elems(d), pool.conv + s * conv_elems(d), qkv + r * C,
+                   a + (int64_t)r * d->hv * d->dk, b + (int64_t)r * d->hv, o, work);
+    free(work);
+  }
+  if (err) *err |= (uint32_t)fail;
+  return 0;
+}
+
+/* KDA speculative verify: as orc_spec_verify, each draft a KDA token step;
+ * a [B][T][hv][dk]. */
+int orc_kda_spec_verify(const orc_dims* d, orc_pool work, orc_pool spec, const orc_params* p,
+                        const int32_t* slot_ids, const int32_t* spec_ids, int32_t B, int32_t T,
+                        const double* qkv, const double* a, const double* b, double* out,
+                        uint32_t* err) {
+  if (check_dims(d)) return 1;
+  int64_t C = n_chan(d), HVDV = (int64_t)d->hv * d->dv;
+  int64_t ns = ssm_elems(d), nc = conv_elems(d);
+  int64_t fail = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : fail)
+  for (int32_t r = 0; r < B; ++r) {
+    int32_t s = slot_ids[r];
+    int cls = slot_class(s, work.num_slots);
+    if (cls) {
+      if (cls == 2) fail |= ORC_ERR_SLOT_OOB;
+      for (int64_t i = 0; i < (int64_t)T * HVDV; ++i) out[(int64_t)r * T * HVDV + i] = 0.0;
+      continue;
     }
-    free(y);
+    double* st = (double*)malloc(sizeof(double) * (ns + nc + C + 3 * (int64_t)d->dk));
+    double* cv = st + ns;
+    double* wk = cv + nc;
+    memcpy(st, work.ssm + s * ns, sizeof(double) * ns);
+    memcpy(cv, work.conv + s * nc, sizeof(double) * nc);
+    for (int32_t t = 0; t < T; ++t) {
+      int64_t rt = (int64_t)r * T + t;
+      kda_token_step(d, p, st, cv, qkv + rt * C, a + rt * d->hv * d->dk, b + rt * d->hv,
+                     out + rt * HVDV, wk);
+      int32_t sid = spec_ids[rt];
+      int sc = slot_class(sid, spec.num_slots);
+      if (sc == 2) fail |= ORC_ERR_SLOT_OOB;
+      if (sc) continue;
+      memcpy(spec.ssm + sid * ns, st, sizeof(double) * ns);
+      memcpy(spec.conv + sid * nc, cv, sizeof(double) * nc);
+    }
+    free(st);
   }
   if (err) *err |= (uint32_t)fail;
   return 0;

@@ -644,3 +644,49 @@ def test_kda_retrieval_for_any_channel_decay():
         assert np.ptp(alpha) > 0.1  # the decays really differ by channel
         np.testing.assert_allclose(pool.ssm[4, h] @ kh, vv * (1 - delta) + delta * (S0[h] @ (alpha * kh)),
                                    rtol=1e-11, atol=1e-12)
+
+
+def test_kda_verify_then_commit_equals_L_kda_decode_steps():
+    """KDA verify leaves the working slot alone; committing draft L gives the
+    state of L KDA decode steps, and the first L outputs are theirs."""
+    shape = synth.TINY
+    d = _dims(shape)
+    g, pool, params = _tiny_setup(73)
+    pk = oracle.Params(params.conv_w, params.A_log, synth.normal((d.hv, d.dk), 0.5, g).double().numpy())
+    B, T = 2, 4
+    ids = np.array([1, 6], np.int32)
+    spec = oracle.Pool(np.full((B * T, d.hv, d.dv, d.dk), 7.25), np.full((B * T, d.w - 1, d.channels), -3.5))
+    spec_ids = np.arange(B * T, dtype=np.int32).reshape(B, T)
+    qkv, _, b = (t.double().numpy() for t in synth.tokens(shape, g, (B, T)))
+    a = synth.normal((B, T, d.hv, d.dk), 1.2, g).double().numpy()
+    before = pool.copy()
+    out, err = oracle.kda_spec_verify(d, pool, spec, pk, ids, spec_ids, qkv, a, b)
+    assert err == 0
+    assert np.array_equal(pool.ssm, before.ssm) and np.array_equal(pool.conv, before.conv)
+    for L in range(0, T + 1):
+        ref = before.copy()
+        for t in range(L):
+            o, _ = oracle.kda_decode_step(d, ref, pk, ids, qkv[:, t], a[:, t], b[:, t])
+            np.testing.assert_array_equal(out[:, t], o)
+        work = before.copy()
+        assert oracle.spec_commit(d, spec, work, spec_ids, np.full(B, L, np.int32), ids) == 0
+        np.testing.assert_array_equal(work.ssm, ref.ssm)
+        np.testing.assert_array_equal(work.conv, ref.conv)
+
+
+def test_kda_verify_with_uniform_gates_is_gdn_verify():
+    shape = synth.TINY
+    d = _dims(shape)
+    g, pool, params = _tiny_setup(74)
+    B, T = 3, 3
+    ids = np.array([0, 4, 7], np.int32)
+    mk = lambda: oracle.Pool(np.zeros((B * T, d.hv, d.dv, d.dk)), np.zeros((B * T, d.w - 1, d.channels)))  # noqa: E731
+    s1, s2 = mk(), mk()
+    spec_ids = np.arange(B * T, dtype=np.int32).reshape(B, T)
+    qkv, a, b = (t.double().numpy() for t in synth.tokens(shape, g, (B, T)))
+    pk = oracle.Params(params.conv_w, params.A_log, np.repeat(params.dt_bias[:, None], d.dk, axis=1) + 0.0)
+    o1, _ = oracle.spec_verify(d, pool, s1, params, ids, spec_ids, qkv, a, b)
+    o2, _ = oracle.kda_spec_verify(d, pool, s2, pk, ids, spec_ids, qkv, np.repeat(a[..., None], d.dk, axis=3), b)
+    np.testing.assert_allclose(o2, o1, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(s2.ssm, s1.ssm, rtol=1e-12, atol=1e-13)
+    np.testing.assert_array_equal(s2.conv, s1.conv)
