@@ -21,8 +21,8 @@ F32, BF16 = 0, 1
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_SCRATCH_LIMIT = 0, 1, 2, 3, 4
 DEV_ERR_SLOT_OOB, DEV_ERR_TIMEOUT, DEV_ERR_SEQLENS = 1, 2, 4
 (K_DECODE, K_SPEC_VERIFY, K_SLOT_COPY, K_SLOT_ZERO, K_SPEC_COMMIT, K_PREFILL, K_COMMIT_INDEX,
- K_STATE_PACK, K_GATED_RMSNORM, K_KDA_DECODE) = range(10)
-K_COUNT = 10
+ K_STATE_PACK, K_GATED_RMSNORM, K_KDA_DECODE, K_KDA_VERIFY) = range(11)
+K_COUNT = 11
 
 _DT_CODE = {torch.float32: F32, torch.bfloat16: BF16}
 
@@ -61,6 +61,7 @@ _PP = ctypes.POINTER(CParams)
 EXPORTS = {
     "gdn_decode_step": ([_PD, CPool, _PP, _P, _I32, _P, _P, _P, _P, _P, _P], _I32),
     "gdn_kda_decode_step": ([_PD, CPool, _PP, _P, _I32, _P, _P, _P, _P, _P, _P], _I32),
+    "gdn_kda_spec_verify": ([_PD, CPool, CPool, _PP, _P, _P, _I32, _I32, _P, _P, _P, _P, _P, _P], _I32),
     "gdn_spec_verify": ([_PD, CPool, CPool, _PP, _P, _P, _I32, _I32, _P, _P, _P, _P, _P, _P], _I32),
     "gdn_spec_commit": ([_PD, CPool, CPool, _P, _P, _P, _I32, _I32, _P, _P], _I32),
     "gdn_chunk_prefill_workspace_size": ([_PD, _I32, _I64], ctypes.c_size_t),
@@ -224,6 +225,18 @@ def kda_decode_step(dims: Dims, pool: StatePool, params: LayerParams, slot_ids, 
                                int(slot_ids.shape[0]), _ptr(qkv), _ptr(a), _ptr(b), _ptr(out),
                                _ptr(dev_err), _stream(stream))
     _check("gdn_kda_decode_step", st)
+
+
+def kda_spec_verify(dims: Dims, work: StatePool, spec: StatePool, params: LayerParams, slot_ids,
+                    spec_ids, qkv, a, b, out, dev_err=None, stream=None):
+    """KDA speculative verify; a is [B][T][hv][dk], params.dt_bias [hv][dk]."""
+    L = load()
+    B, T = spec_ids.shape
+    cd, cp = dims.c(), params.c()
+    st = L.gdn_kda_spec_verify(ctypes.byref(cd), work.c(), spec.c(), ctypes.byref(cp), _ptr(slot_ids),
+                               _ptr(spec_ids), int(B), int(T), _ptr(qkv), _ptr(a), _ptr(b), _ptr(out),
+                               _ptr(dev_err), _stream(stream))
+    _check("gdn_kda_spec_verify", st)
 
 
 def spec_verify(dims: Dims, work: StatePool, spec: StatePool, params: LayerParams, slot_ids,

@@ -302,9 +302,15 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const StepArgs a) {
 // ---------------------------------------------------------------------------
 // Speculative verify: T draft tokens per request from the working slot, which
 // is only read; the state after draft t goes to spec slot spec_ids[r][t].
-// The state rows stay in registers across the T steps.
+// The state rows stay in registers across the T steps.  KDA: the per-key-
+// channel decay of every draft step (a [B][T][hv][dk]) from a [T][dk] table.
 // ---------------------------------------------------------------------------
-template <int DK, int NIT, typename Tact, typename Tconv>
+// offset (floats) of the KDA alpha table in the verify kernel's shared memory
+__host__ __device__ constexpr size_t verify_alpha_off(int T, int nch, int R) {
+  return ((size_t)T * nch + (size_t)T * R + (size_t)T * 5 + 3) & ~(size_t)3;
+}
+
+template <int DK, int NIT, typename Tact, typename Tconv, bool KDA>
 __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const StepArgs a) {
   pdl_wait();
   pdl_trigger();
@@ -315,6 +321,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const StepArgs a) {
   float* sy = smem;                     // [T][NCH]  conv+SiLU outputs
   float* so = sy + (size_t)a.T * NCH;   // [T][R]    outputs
   float* sscal = so + (size_t)a.T * R;  // [T][5]    rq, rk, kq, alpha, beta
+  float* salk = smem + verify_alpha_off(a.T, NCH, R);  // KDA: [T][DK] alpha
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int r = blockIdx.y;
@@ -405,9 +412,18 @@ __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const StepArgs a) {
       sscal[t * 5 + 0] = rq;
       sscal[t * 5 + 1] = rk;
       sscal[t * 5 + 2] = pqk * rq * rk;
-      sscal[t * 5 + 3] = gate_alpha(a.A_log[h], a.dt_bias[h],
-                                    to_f32(reinterpret_cast<const Tact*>(a.a)[rt * a.hv + h]));
+      if (!KDA)
+        sscal[t * 5 + 3] = gate_alpha(a.A_log[h], a.dt_bias[h],
+                                      to_f32(reinterpret_cast<const Tact*>(a.a)[rt * a.hv + h]));
       sscal[t * 5 + 4] = sigmoid_f(to_f32(reinterpret_cast<const Tact*>(a.b)[rt * a.hv + h]));
+    }
+  }
+  if (KDA) {
+    for (int e = tid; e < T * DK; e += kThreads) {
+      const int t = e / DK, i = e % DK;
+      const size_t rt = (size_t)r * T + t;
+      salk[e] = gate_alpha(a.A_log[h], a.dt_bias[(size_t)h * DK + i],
+                           to_f32(reinterpret_cast<const Tact*>(a.a)[(rt * a.hv + h) * DK + i]));
     }
   }
   __syncthreads();
@@ -417,14 +433,16 @@ __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const StepArgs a) {
     const float* yk = yq + DK;
     const float* yv = yk + DK;
     const float rq = sscal[t * 5 + 0], rk = sscal[t * 5 + 1], kq = sscal[t * 5 + 2];
-    const float alpha = sscal[t * 5 + 3], beta = sscal[t * 5 + 4];
-    float4 kk[4], qq[4];
+    const float alpha = KDA ? 1.f : sscal[t * 5 + 3], beta = sscal[t * 5 + 4];
+    float4 kk[4], qq[4], al[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const float4 k4 = *reinterpret_cast<const float4*>(yk + M::col(c, seg));
       const float4 q4 = *reinterpret_cast<const float4*>(yq + M::col(c, seg));
       kk[c] = make_float4(k4.x * rk, k4.y * rk, k4.z * rk, k4.w * rk);
       qq[c] = make_float4(q4.x * rq, q4.y * rq, q4.z * rq, q4.w * rq);
+      al[c] = KDA ? *reinterpret_cast<const float4*>(salk + (size_t)t * DK + M::col(c, seg))
+                  : make_float4(alpha, alpha, alpha, alpha);
     }
     const int32_t sid = sids[t];
     float* Sp = slot_class(sid, a.spec_num_slots) == 0
@@ -436,8 +454,12 @@ __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const StepArgs a) {
       float dk_ = 0.f, dq_ = 0.f;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        dk_ += dot4(s[it][c], kk[c]);
-        dq_ += dot4(s[it][c], qq[c]);
+        // KDA: the decayed row St diag(alpha) meets k^ and q^
+        const float4 sa = KDA ? make_float4(s[it][c].x * al[c].x, s[it][c].y * al[c].y, s[it][c].z * al[c].z,
+                                            s[it][c].w * al[c].w)
+                              : s[it][c];
+        dk_ += dot4(sa, kk[c]);
+        dq_ += dot4(sa, qq[c]);
       }
 #pragma unroll
       for (int o = M::LPR / 2; o; o >>= 1) {
@@ -448,10 +470,10 @@ __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const StepArgs a) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         float4& v = s[it][c];
-        v.x = fmaf(bu, kk[c].x, alpha * v.x);
-        v.y = fmaf(bu, kk[c].y, alpha * v.y);
-        v.z = fmaf(bu, kk[c].z, alpha * v.z);
-        v.w = fmaf(bu, kk[c].w, alpha * v.w);
+        v.x = fmaf(bu, kk[c].x, al[c].x * v.x);
+        v.y = fmaf(bu, kk[c].y, al[c].y * v.y);
+        v.z = fmaf(bu, kk[c].z, al[c].z * v.z);
+        v.w = fmaf(bu, kk[c].w, al[c].w * v.w);
       }
       if (row < nrows) {
         if (Sp) {
@@ -483,10 +505,11 @@ cudaError_t launch_decode_t(const StepArgs& a, bool kda, cudaStream_t s) {
 }
 
 template <int DK, int NIT, typename Tact, typename Tconv>
-cudaError_t launch_verify_t(const StepArgs& a, cudaStream_t s) {
+cudaError_t launch_verify_t(const StepArgs& a, bool kda, cudaStream_t s) {
   constexpr int R = NIT * RowMap<DK>::RI;
-  const size_t smem = sizeof(float) * ((size_t)a.T * (2 * DK + R) + (size_t)a.T * R + (size_t)a.T * 5);
-  auto k = verify_kernel<DK, NIT, Tact, Tconv>;
+  const size_t smem = kda ? sizeof(float) * (verify_alpha_off(a.T, 2 * DK + R, R) + (size_t)a.T * DK)
+                          : sizeof(float) * ((size_t)a.T * (2 * DK + R) + (size_t)a.T * R + (size_t)a.T * 5);
+  auto k = kda ? verify_kernel<DK, NIT, Tact, Tconv, true> : verify_kernel<DK, NIT, Tact, Tconv, false>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -497,12 +520,12 @@ cudaError_t launch_verify_t(const StepArgs& a, cudaStream_t s) {
 template <int DK, int NIT>
 cudaError_t dispatch_dtype(bool verify, bool kda, const StepArgs& a, int act, int cv, cudaStream_t s) {
   if (act == GDN_F32 && cv == GDN_F32)
-    return verify ? launch_verify_t<DK, NIT, float, float>(a, s)
+    return verify ? launch_verify_t<DK, NIT, float, float>(a, kda, s)
                   : launch_decode_t<DK, NIT, float, float>(a, kda, s);
   if (act == GDN_BF16 && cv == GDN_BF16)
-    return verify ? launch_verify_t<DK, NIT, __nv_bfloat16, __nv_bfloat16>(a, s)
+    return verify ? launch_verify_t<DK, NIT, __nv_bfloat16, __nv_bfloat16>(a, kda, s)
                   : launch_decode_t<DK, NIT, __nv_bfloat16, __nv_bfloat16>(a, kda, s);
-  return verify ? launch_verify_t<DK, NIT, __nv_bfloat16, float>(a, s)
+  return verify ? launch_verify_t<DK, NIT, __nv_bfloat16, float>(a, kda, s)
                 : launch_decode_t<DK, NIT, __nv_bfloat16, float>(a, kda, s);
 }
 
@@ -585,7 +608,7 @@ gdn_status run_step(bool verify, bool kda, const gdn_dims* dims, const gdn_pool&
     if (e == cudaSuccess) count_launch(kda ? GDN_K_KDA_DECODE : GDN_K_DECODE);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
   }
-  if (verify && use_tma_verify(*dims, B, T, qkv, *params)) {
+  if (verify && !kda && use_tma_verify(*dims, B, T, qkv, *params)) {
     cudaError_t e = verify_tma_launch(*dims, work, *spec, *params, slot_ids, spec_ids, B, T, qkv, a,
                                       b, out, dev_err, cs);
     if (e == cudaSuccess) count_launch(GDN_K_SPEC_VERIFY);
@@ -637,7 +660,8 @@ gdn_status run_step(bool verify, bool kda, const gdn_dims* dims, const gdn_pool&
                      : dispatch_dtype<128, 4>(verify, kda, s, act, cv, cs);
       break;
   }
-  if (e == cudaSuccess) count_launch(kda ? GDN_K_KDA_DECODE : verify ? GDN_K_SPEC_VERIFY : GDN_K_DECODE);
+  if (e == cudaSuccess)
+    count_launch(kda ? (verify ? GDN_K_KDA_VERIFY : GDN_K_KDA_DECODE) : verify ? GDN_K_SPEC_VERIFY : GDN_K_DECODE);
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
@@ -657,6 +681,15 @@ extern "C" gdn_status gdn_kda_decode_step(const gdn_dims* dims, gdn_pool pool, c
                                           const void* a, const void* b, void* out, uint32_t* dev_err,
                                           void* stream) {
   return gdn::run_step(false, true, dims, pool, nullptr, params, slot_ids, nullptr, B, 1, qkv, a, b, out,
+                       dev_err, stream);
+}
+
+extern "C" gdn_status gdn_kda_spec_verify(const gdn_dims* dims, gdn_pool work, gdn_pool spec,
+                                          const gdn_params* params, const int32_t* slot_ids,
+                                          const int32_t* spec_ids, int32_t B, int32_t T, const void* qkv,
+                                          const void* a, const void* b, void* out, uint32_t* dev_err,
+                                          void* stream) {
+  return gdn::run_step(true, true, dims, work, &spec, params, slot_ids, spec_ids, B, T, qkv, a, b, out,
                        dev_err, stream);
 }
 

@@ -127,6 +127,18 @@ gdn_status gdn_kda_decode_step(const gdn_dims* dims, gdn_pool pool,
                                void* stream);
 
 /*
+ * KDA speculative verify: gdn_spec_verify with every draft step the KDA step
+ * of gdn_kda_decode_step (a [B][T][hv][dk] per-channel gate logits,
+ * params->dt_bias [hv][dk]).  Snapshots have the pool layout, so
+ * gdn_spec_commit and gdn_spec_commit_index apply unchanged.
+ */
+gdn_status gdn_kda_spec_verify(const gdn_dims* dims, gdn_pool work, gdn_pool spec,
+                               const gdn_params* params, const int32_t* slot_ids,
+                               const int32_t* spec_ids, int32_t B, int32_t T,
+                               const void* qkv, const void* a, const void* b,
+                               void* out, uint32_t* dev_err, void* stream);
+
+/*
  * Speculative verify (TokenSpeed Qwen3.5 page, "Scheduler dual": spec_cache
  * of per-step conv/SSM snapshots for rollback).  Request r runs its T draft
  * tokens starting from working slot slot_ids[r], which is NOT modified; after
@@ -343,7 +355,8 @@ const char* gdn_status_string(int32_t status);
 #define GDN_K_STATE_PACK 7 /* pack and unpack */
 #define GDN_K_GATED_RMSNORM 8
 #define GDN_K_KDA_DECODE 9
-#define GDN_K_COUNT 10
+#define GDN_K_KDA_VERIFY 10
+#define GDN_K_COUNT 11
 uint64_t gdn_launch_count(int32_t kernel);
 void gdn_launch_count_reset(void);
 

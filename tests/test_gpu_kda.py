@@ -1,6 +1,7 @@
-"""GPU KDA decode (per-key-channel decay) against the oracle's KDA step: the
+"""GPU KDA (per-key-channel decay) against the oracle: the decode step on the
 Qwen3.5-shaped layer at several batches, other shapes, 32 chained steps,
-padding, and uniform gates reducing to the GDN step."""
+padding, uniform gates reducing to the GDN step; the speculative verify with
+its snapshots, and verify in the working pool followed by the index commit."""
 import numpy as np
 import pytest
 import torch
@@ -111,3 +112,71 @@ def test_kda_padding_and_bad_ids(cuda):
     assert torch.all(out[1:3] == 0)
     assert_out_close(out[[0, 3]], o_ref[[0, 3]], shape.dv, out_tol(shape))
     assert max_rel_l2(to_np(st.pool.ssm), st.opool.ssm, shape.dv * shape.dk) <= STATE_TOL_1
+
+
+@pytest.mark.parametrize("shape,B,T", [
+    (synth.QWEN, 16, 8), (synth.QWEN, 3, 16), (synth.TINY, 2, 5),
+    (synth.QWEN.replace(act="f32", conv="f32", hk=4, hv=8), 5, 4),
+], ids=["qwen_b16_t8", "qwen_b3_t16", "tiny", "f32_b5_t4"])
+def test_kda_verify_vs_oracle(cuda, shape, B, T):
+    n_work = 8 if shape is synth.TINY else 40
+    st = Setup(shape, seed=90 + B, num_slots=n_work)
+    params, oparams = _kda_params(st, 91)
+    ids = synth.slot_ids(n_work, B, st.gen)
+    n_spec = B * T + 2
+    spec = gdn.StatePool.empty(st.dims, n_spec, "cuda")
+    spec.ssm.fill_(12345.5)
+    spec.conv.fill_(-77.0)
+    spec_ids = synth.slot_ids(n_spec, B * T, st.gen).reshape(B, T)
+    qkv, _, b = st.tokens((B, T))
+    a = _gates(st, (B, T))
+    before = st.pool.ssm.clone(), st.pool.conv.clone()
+    out = torch.empty((B, T, shape.hv, shape.dv), dtype=shape.act_dtype, device="cuda")
+    n0 = gdn.launch_count(gdn.K_KDA_VERIFY)
+    gdn.kda_spec_verify(st.dims, st.pool, spec, params, ids.cuda(), spec_ids.cuda(), qkv.cuda(), a.cuda(),
+                        b.cuda(), out)
+    ospec = oracle.Pool(np.full((n_spec, shape.hv, shape.dv, shape.dk), 12345.5),
+                        np.full((n_spec, shape.w - 1, shape.channels), -77.0))
+    o_ref, err = oracle.kda_spec_verify(st.od, st.opool, ospec, oparams, ids.numpy(), spec_ids.numpy(),
+                                        to_np(qkv), to_np(a), to_np(b))
+    torch.cuda.synchronize()
+    assert err == 0 and gdn.launch_count(gdn.K_KDA_VERIFY) == n0 + 1
+    assert torch.equal(st.pool.ssm, before[0]) and torch.equal(st.pool.conv, before[1])
+    assert_out_close(out, o_ref, shape.dv, out_tol(shape))
+    sids = spec_ids.flatten().tolist()
+    assert max_rel_l2(to_np(spec.ssm[sids]), ospec.ssm[sids], shape.dv * shape.dk) <= STATE_TOL_1 * 5
+    assert conv_bits_equal(spec.conv[sids], ospec.conv[sids])
+    unused = [s for s in range(n_spec) if s not in sids]
+    assert torch.all(spec.ssm[unused] == 12345.5)
+
+
+def test_kda_verify_in_place_then_commit_index(cuda):
+    """Snapshots in the working pool, then the index commit: each request lands
+    on the state of its first L KDA decode steps."""
+    shape = synth.QWEN
+    B, T = 8, 6
+    n_slots = B * (T + 1) + 4
+    st = Setup(shape, seed=92, num_slots=n_slots)
+    params, oparams = _kda_params(st, 93)
+    perm = synth.slot_ids(n_slots, B * (T + 1), st.gen)
+    ids, spec_ids = perm[:B].clone(), perm[B:].reshape(B, T).clone()
+    qkv, _, b = st.tokens((B, T))
+    a = _gates(st, (B, T))
+    before = st.pool.ssm.clone(), st.pool.conv.clone()
+    out = torch.empty((B, T, shape.hv, shape.dv), dtype=shape.act_dtype, device="cuda")
+    gdn.kda_spec_verify(st.dims, st.pool, st.pool, params, ids.cuda(), spec_ids.cuda(), qkv.cuda(), a.cuda(),
+                        b.cuda(), out)
+    L = synth.accept_lengths(B, T, st.gen)
+    L[1] = 0
+    d_slots = ids.cuda()
+    freed = torch.empty((B, T), dtype=torch.int32, device="cuda")
+    gdn.spec_commit_index(spec_ids.cuda(), L.cuda(), d_slots, freed)
+    ref = oracle.Pool(to_np(before[0]), to_np(before[1]))
+    for r in range(B):
+        for t in range(int(L[r])):
+            oracle.kda_decode_step(st.od, ref, oparams, ids[r:r + 1].numpy(), to_np(qkv[r:r + 1, t]),
+                                   to_np(a[r:r + 1, t]), to_np(b[r:r + 1, t]))
+    torch.cuda.synchronize()
+    new = d_slots.cpu().tolist()
+    assert max_rel_l2(to_np(st.pool.ssm[new]), ref.ssm[ids.tolist()], shape.dv * shape.dk) <= STATE_TOL_1 * 5
+    assert conv_bits_equal(st.pool.conv[new], ref.conv[ids.tolist()])
