@@ -620,6 +620,26 @@ def measure_rows(gdn, synth, dev, stream, hbm_peak, bf16_peak, which="all", pref
         rk = frac(kbytes, _events_time(fk, reps, stream))
         rk["tokens_per_s"] = 64 / (rk["ms"] * 1e-3)
         rows["kda_decode_b64"] = rk
+        # KDA verify, batch 32, T = 8, snapshots into a separate spec pool
+        Bk, Tk = 32, 8
+        kspec = gdn.StatePool.empty(dims, 2 * Bk * Tk, dev)
+        kss = [torch.arange(k * Bk * Tk, (k + 1) * Bk * Tk, dtype=torch.int32, device=dev).reshape(Bk, Tk)
+               for k in range(2)]
+        kws = [perm[k * Bk:(k + 1) * Bk].to(dev) for k in range(2)]
+        kvin = [(synth.tokens(shape, g, (Bk, Tk))[0].to(dev),
+                 synth.normal((Bk, Tk, shape.hv, shape.dk), 1.0, g, shape.act_dtype).to(dev),
+                 synth.tokens(shape, g, (Bk, Tk))[2].to(dev)) for _ in range(2)]
+        kvo = torch.empty((Bk, Tk, shape.hv, shape.dv), dtype=torch.bfloat16, device=dev)
+
+        def fkv(i):
+            q, ka, kb = kvin[i % 2]
+            gdn.kda_spec_verify(dims, pool, kspec, kp, kws[i % 2], kss[i % 2], q, ka, kb, kvo)
+        fkv(0)
+        kvb = Bk * (slot_bytes + Tk * (16384 + 32 * 128 * 2 + 64) + Tk * slot_bytes + Tk * 8192)
+        rkv = frac(kvb, _events_time(fkv, reps, stream))
+        rkv["draft_tokens_per_s"] = Bk * Tk / (rkv["ms"] * 1e-3)
+        rows["kda_verify_b32_t8"] = rkv
+        del kspec
         rows["mixed_b64_plus_4x256"] = _mixed_row(gdn, synth, dims, pool, params, perm, g, dev, stream)
         # readout epilogue over a 4 x 8192-token prefill output: o and z read,
         # y written in place (3 x 256 bytes per (token, V head) row)
