@@ -533,6 +533,52 @@ int orc_kda_spec_verify(const orc_dims* d, orc_pool work, orc_pool spec, const o
   return 0;
 }
 
+/* KDA prefill, token by token: the contract of orc_prefill (packed sequences,
+ * absolute start positions, block-aligned checkpoints of state and conv
+ * history) with every token a KDA token step; a [Ttot][hv][dk]. */
+int orc_kda_prefill(const orc_dims* d, orc_pool pool, orc_pool ckpt, const orc_params* p,
+                    const int32_t* slot_ids, const int32_t* cu_seqlens, const int64_t* start_pos,
+                    int32_t n_seq, const int32_t* ckpt_ids, int32_t max_ckpt, int32_t ckpt_block,
+                    const double* qkv, const double* a, const double* b, double* out, uint32_t* err) {
+  if (check_dims(d) || ckpt_block <= 0) return 1;
+  int64_t C = n_chan(d), HVDV = (int64_t)d->hv * d->dv;
+  int64_t ns = ssm_elems(d), nc = conv_elems(d);
+  int64_t fail = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : fail)
+  for (int32_t n = 0; n < n_seq; ++n) {
+    int32_t s = slot_ids[n];
+    int64_t t0 = cu_seqlens[n], t1 = cu_seqlens[n + 1];
+    int cls = slot_class(s, pool.num_slots);
+    if (cls) {
+      if (cls == 2) fail |= ORC_ERR_SLOT_OOB;
+      for (int64_t i = t0 * HVDV; i < t1 * HVDV; ++i) out[i] = 0.0;
+      continue;
+    }
+    double* ssm = pool.ssm + s * ns;
+    double* conv = pool.conv + s * nc;
+    double* wk = (double*)malloc(sizeof(double) * (C + 3 * (int64_t)d->dk));
+    int64_t p0 = start_pos[n];
+    int64_t blk0 = p0 / ckpt_block;
+    for (int64_t i = t0; i < t1; ++i) {
+      kda_token_step(d, p, ssm, conv, qkv + i * C, a + i * d->hv * d->dk, b + i * d->hv, out + i * HVDV,
+                     wk);
+      int64_t P = p0 + (i - t0) + 1;
+      if (P % ckpt_block) continue;
+      int64_t idx = P / ckpt_block - blk0 - 1;
+      if (idx < 0 || idx >= max_ckpt) continue;
+      int32_t cid = ckpt_ids[(int64_t)n * max_ckpt + idx];
+      int cc = slot_class(cid, ckpt.num_slots);
+      if (cc == 2) fail |= ORC_ERR_SLOT_OOB;
+      if (cc) continue;
+      memcpy(ckpt.ssm + cid * ns, ssm, sizeof(double) * ns);
+      memcpy(ckpt.conv + cid * nc, conv, sizeof(double) * nc);
+    }
+    free(wk);
+  }
+  if (err) *err |= (uint32_t)fail;
+  return 0;
+}
+
 /* ---- readout epilogue: gated RMS norm ----------------------------------
  * Not written on the pages.  The published Gated DeltaNet block normalises
  * each head's readout and gates it with a SiLU of a separate projection z:

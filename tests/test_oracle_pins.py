@@ -690,3 +690,39 @@ def test_kda_verify_with_uniform_gates_is_gdn_verify():
     np.testing.assert_allclose(o2, o1, rtol=1e-12, atol=1e-13)
     np.testing.assert_allclose(s2.ssm, s1.ssm, rtol=1e-12, atol=1e-13)
     np.testing.assert_array_equal(s2.conv, s1.conv)
+
+
+def test_kda_prefill_equals_kda_decode_steps_and_checkpoints():
+    """KDA prefill of two sequences (one resumed mid-block) = their tokens as
+    KDA decode steps; each checkpoint holds the state after its block boundary."""
+    shape = synth.TINY
+    d = _dims(shape)
+    g, pool, params = _tiny_setup(75)
+    pk = oracle.Params(params.conv_w, params.A_log, synth.normal((d.hv, d.dk), 0.5, g).double().numpy())
+    lens, starts, blk = [70, 33], [0, 50], 32
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    ids = np.array([3, 6], np.int32)
+    qkv, _, b = (t.double().numpy() for t in synth.tokens(shape, g, (int(cu[-1]),)))
+    a = synth.normal((int(cu[-1]), d.hv, d.dk), 1.0, g).double().numpy()
+    ck = oracle.Pool(np.full((6, d.hv, d.dv, d.dk), -9.0), np.full((6, d.w - 1, d.channels), 4.0))
+    ck_ids = np.array([[0, 1, 2], [3, 4, 5]], np.int32)
+    ref = pool.copy()
+    out, err = oracle.kda_prefill(d, pool, ck, pk, ids, cu, starts, ck_ids, blk, qkv, a, b)
+    assert err == 0
+    expect_ck = {}
+    for n in range(2):
+        for i in range(cu[n], cu[n + 1]):
+            o, _ = oracle.kda_decode_step(d, ref, pk, ids[n:n + 1], qkv[i:i + 1], a[i:i + 1], b[i:i + 1])
+            np.testing.assert_array_equal(out[i], o[0])
+            P = starts[n] + (i - cu[n]) + 1
+            if P % blk == 0:
+                expect_ck[int(ck_ids[n][P // blk - starts[n] // blk - 1])] = (ref.ssm[ids[n]].copy(),
+                                                                            ref.conv[ids[n]].copy())
+    np.testing.assert_array_equal(pool.ssm, ref.ssm)
+    np.testing.assert_array_equal(pool.conv, ref.conv)
+    # sequence 0: boundaries 32, 64; sequence 1 (50 .. 83): 64
+    assert sorted(expect_ck) == [0, 1, 3]
+    for cid, (s_, c_) in expect_ck.items():
+        np.testing.assert_array_equal(ck.ssm[cid], s_)
+        np.testing.assert_array_equal(ck.conv[cid], c_)
+    assert np.all(ck.ssm[[2, 4, 5]] == -9.0)
