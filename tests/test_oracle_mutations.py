@@ -32,8 +32,9 @@ MUTATIONS = {
     "sigmoid_sign": ("return 1.0 / (1.0 + exp(-x)); }", "return 1.0 / (1.0 + exp(x)); }"),
     "norm_eps_missing": ("double r = 1.0 / sqrt(ss + ORC_EPS);", "double r = 1.0 / sqrt(ss);"),
     "alpha_is_g": ("f->alpha[h] = exp(f->g[h]);", "f->alpha[h] = f->g[h];"),
-    "checkpoint_index": ("if (P % ckpt_block) continue;\n      int64_t idx = P / ckpt_block - blk0 - 1;",
-                         "if (P % ckpt_block) continue;\n      int64_t idx = P / ckpt_block - blk0;"),
+    "checkpoint_index": ("int64_t P = pos + 1;\n      if (P % ckpt_block) continue;\n      int64_t idx = P / ckpt_block - blk0 - 1;",
+                         "int64_t P = pos + 1;\n      if (P % ckpt_block) continue;\n      int64_t idx = P / ckpt_block - blk0;"),
+    "kda_checkpoint_after_next_token": ("int64_t P = p0 + (i - t0) + 1;", "int64_t P = p0 + (i - t0);"),
     "zero_keeps_conv": ("pool.conv[ids[i] * nc + e] = 0.0;", "pool.conv[ids[i] * nc + e] = 1.0;"),
     "commit_index_freed": ("if (t != L - 1) fr[k++] = sp[t];", "if (t != L - 1) fr[k++] = slot_ids[r];"),
     "pack_error_bit": ("if (c == 2 && err) *err |= ORC_ERR_SLOT_OOB;\n    for (int64_t e = 0; e < ns; ++e) st_ssm",
