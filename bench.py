@@ -640,6 +640,29 @@ def measure_rows(gdn, synth, dev, stream, hbm_peak, bf16_peak, which="all", pref
         rkv["draft_tokens_per_s"] = Bk * Tk / (rkv["ms"] * 1e-3)
         rows["kda_verify_b32_t8"] = rkv
         del kspec
+        # KDA prefill (recurrent form), 4 sequences x 8192 tokens, checkpoints
+        # every 256: per token qkv, the per-channel gate logits, beta and out
+        nK, SK = 4, 8192
+        kt = nK * SK
+        kpq = synth.tokens(shape, g, (kt,))
+        kpin = (kpq[0].to(dev), synth.normal((kt, shape.hv, shape.dk), 1.0, g, shape.act_dtype).to(dev),
+                kpq[2].to(dev))
+        del kpq
+        kcu = torch.arange(0, kt + 1, SK, dtype=torch.int32, device=dev)
+        ksp = torch.zeros(nK, dtype=torch.int64, device=dev)
+        kck = gdn.StatePool.empty(dims, nK * (SK // 256), dev)
+        kck_ids = torch.arange(nK * (SK // 256), dtype=torch.int32, device=dev).reshape(nK, SK // 256)
+        kpo = torch.empty((kt, shape.hv, shape.dv), dtype=torch.bfloat16, device=dev)
+        kpids = [perm[k * nK:(k + 1) * nK].to(dev) for k in range(4)]
+
+        def fkp(i):
+            gdn.kda_prefill(dims, pool, kck, kp, kpids[i % 4], kcu, ksp, kt, kck_ids, 256, *kpin, kpo)
+        fkp(0)
+        kpbytes = kt * (16384 + 32 * 128 * 2 + 64 + 8192) + (nK * (SK // 256) + 2 * nK) * slot_bytes
+        rkp = frac(kpbytes, _events_time(fkp, 3, stream))
+        rkp["tokens_per_s"] = kt / (rkp["ms"] * 1e-3)
+        rows[f"kda_prefill_{nK}x{SK}"] = rkp
+        del kpin, kck, kpo
         rows["mixed_b64_plus_4x256"] = _mixed_row(gdn, synth, dims, pool, params, perm, g, dev, stream)
         # readout epilogue over a 4 x 8192-token prefill output: o and z read,
         # y written in place (3 x 256 bytes per (token, V head) row)

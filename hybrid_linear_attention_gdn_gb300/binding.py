@@ -21,8 +21,8 @@ F32, BF16 = 0, 1
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_SCRATCH_LIMIT = 0, 1, 2, 3, 4
 DEV_ERR_SLOT_OOB, DEV_ERR_TIMEOUT, DEV_ERR_SEQLENS = 1, 2, 4
 (K_DECODE, K_SPEC_VERIFY, K_SLOT_COPY, K_SLOT_ZERO, K_SPEC_COMMIT, K_PREFILL, K_COMMIT_INDEX,
- K_STATE_PACK, K_GATED_RMSNORM, K_KDA_DECODE, K_KDA_VERIFY) = range(11)
-K_COUNT = 11
+ K_STATE_PACK, K_GATED_RMSNORM, K_KDA_DECODE, K_KDA_VERIFY, K_KDA_PREFILL) = range(12)
+K_COUNT = 12
 
 _DT_CODE = {torch.float32: F32, torch.bfloat16: BF16}
 
@@ -64,6 +64,8 @@ EXPORTS = {
     "gdn_kda_spec_verify": ([_PD, CPool, CPool, _PP, _P, _P, _I32, _I32, _P, _P, _P, _P, _P, _P], _I32),
     "gdn_spec_verify": ([_PD, CPool, CPool, _PP, _P, _P, _I32, _I32, _P, _P, _P, _P, _P, _P], _I32),
     "gdn_spec_commit": ([_PD, CPool, CPool, _P, _P, _P, _I32, _I32, _P, _P], _I32),
+    "gdn_kda_prefill": ([_PD, CPool, CPool, _PP, _P, _P, _P, _I32, _I64, _P, _I32, _I32, _P, _P, _P,
+                         _P, _P, _P], _I32),
     "gdn_chunk_prefill_workspace_size": ([_PD, _I32, _I64], ctypes.c_size_t),
     "gdn_chunk_prefill": ([_PD, CPool, CPool, _PP, _P, _P, _P, _I32, _I64, _P, _I32, _I32,
                            _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P], _I32),
@@ -281,6 +283,23 @@ def chunk_prefill(dims: Dims, pool: StatePool, ckpt: StatePool, params: LayerPar
                              _ptr(qkv), _ptr(a), _ptr(b), _ptr(out), _ptr(workspace), ws_bytes,
                              _ptr(dev_err), _stream(stream))
     _check("gdn_chunk_prefill", st)
+
+
+def kda_prefill(dims: Dims, pool: StatePool, ckpt: StatePool, params: LayerParams, slot_ids, cu_seqlens,
+                start_pos, total_tokens: int, ckpt_ids, ckpt_block: int, qkv, a, b, out, dev_err=None,
+                stream=None):
+    """KDA prefill in the recurrent form: chunk_prefill's contract with
+    per-key-channel gate logits a [total][hv][dk] and dt_bias [hv][dk]; it
+    needs no workspace."""
+    L = load()
+    n_seq = int(slot_ids.shape[0])
+    max_ckpt = int(ckpt_ids.shape[1]) if ckpt_ids is not None and ckpt_ids.dim() == 2 else 0
+    cd, cp = dims.c(), params.c()
+    st = L.gdn_kda_prefill(ctypes.byref(cd), pool.c(), ckpt.c(), ctypes.byref(cp), _ptr(slot_ids),
+                           _ptr(cu_seqlens), _ptr(start_pos), n_seq, int(total_tokens), _ptr(ckpt_ids),
+                           max_ckpt, int(ckpt_block), _ptr(qkv), _ptr(a), _ptr(b), _ptr(out), _ptr(dev_err),
+                           _stream(stream))
+    _check("gdn_kda_prefill", st)
 
 
 NOALLOC_SCRATCH_BYTES = 64 << 20

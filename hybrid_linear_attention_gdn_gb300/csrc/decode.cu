@@ -25,6 +25,7 @@
 // have long arrived.  No distributed shared memory and no multicast is used.
 #include "gdn_common.cuh"
 #include "decode_tma.cuh"
+#include "prefill_tc.cuh"
 
 #include <cstdlib>
 #include <cstring>
@@ -493,6 +494,320 @@ __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const StepArgs a) {
 }
 
 // ---------------------------------------------------------------------------
+// KDA prefill, the recurrent form (fp32, CUDA cores): one CTA per (sequence,
+// V head, row part) walks the sequence token by token in windows of kTW
+// tokens.  The raw inputs of window w+1 (the CTA's qkv channels and the gate
+// logits) are copied into shared memory (cp.async, double-buffered) while
+// window w is computed: conv1d + SiLU from the staged inputs and the conv
+// history (shared memory, one column per channel, owned by the thread that
+// convolves it), per-token norms, beta and the per-key-channel alphas, then
+// the KDA update of the CTA's state rows, which stay in registers for the
+// whole sequence.  At every block boundary the rows go to their checkpoint
+// slot; at the end to the working slot.  The conv histories of the
+// checkpoints and of the final state come from the prefill's history kernel.
+// ---------------------------------------------------------------------------
+constexpr int kTW = 16;
+
+struct KdaPrefillArgs {
+  float* ssm;
+  const void* conv;
+  int32_t num_slots;
+  float* ck_ssm;
+  int32_t ck_num_slots;
+  const float* conv_w;
+  const float* A_log;
+  const float* dt_bias;  // [hv][dk]
+  const int32_t* slot_ids;
+  const int32_t* cu_seqlens;
+  const int64_t* start_pos;
+  int64_t total;
+  const int32_t* ckpt_ids;
+  int32_t max_ckpt;
+  int32_t ckpt_block;
+  const void* qkv;
+  const void* a;  // [total][hv][dk]
+  const void* b;
+  void* out;
+  uint32_t* err;
+  int32_t hk, hv, dv, W, C, G, P;
+};
+
+// shared memory of kda_prefill_kernel (byte offsets, each 16-byte aligned)
+template <int DK, int NIT, typename Tact>
+struct KdaPrefillSmem {
+  static constexpr int R = NIT * RowMap<DK>::RI;
+  static constexpr int NCH = 2 * DK + R;  // q, k and the CTA's v rows
+  static constexpr size_t xr = 0;                                             // [2][kTW][NCH] raw inputs
+  static constexpr size_t ga = xr + 2 * kTW * NCH * sizeof(Tact);             // [2][kTW][DK] gate logits
+  static constexpr size_t xh = ga + 2 * kTW * DK * sizeof(Tact);              // [kMaxW-1][NCH] conv history
+  static constexpr size_t cw = xh + (kMaxW - 1) * NCH * sizeof(float);        // [kMaxW][NCH] conv weights
+  static constexpr size_t sy = cw + kMaxW * NCH * sizeof(float);              // [kTW][NCH] conv + SiLU
+  static constexpr size_t so = sy + kTW * NCH * sizeof(float);                // [kTW][R] outputs
+  static constexpr size_t sc = so + kTW * R * sizeof(float);                  // [kTW][4] rq, rk, k^.q^, beta
+  static constexpr size_t al = sc + kTW * 4 * sizeof(float);                  // [kTW][DK] alphas
+  static constexpr size_t sb = al + kTW * DK * sizeof(float);                 // [2][kTW] beta logits
+  static constexpr size_t bytes = sb + 2 * kTW * sizeof(float);
+  static_assert(ga % 16 == 0 && xh % 16 == 0 && cw % 16 == 0 && sy % 16 == 0 && so % 16 == 0 && al % 16 == 0,
+                "shared arrays must start 16-byte aligned");
+};
+
+// Raw inputs of tokens [tok, tok + nt) into the staging buffers: the CTA's
+// channels of qkv (q, k, then its v rows) and the head's gate logits.  ASYNC:
+// 16-byte cp.async pieces (every segment start and length a multiple of 16
+// bytes, checked on the host); otherwise element copies.
+template <int DK, int NIT, typename Tact, bool ASYNC>
+__device__ __forceinline__ void kda_stage(const KdaPrefillArgs& a, Tact* xr, Tact* gs, int64_t tok, int nt,
+                                          int nrows, int hq, int h, int row0) {
+  using L = KdaPrefillSmem<DK, NIT, Tact>;
+  const Tact* qkv = reinterpret_cast<const Tact*>(a.qkv);
+  const Tact* ga = reinterpret_cast<const Tact*>(a.a);
+  const int nch = 2 * DK + nrows;
+  if constexpr (ASYNC) {
+    constexpr int E = 16 / sizeof(Tact);  // elements per piece
+    const int per_row = nch / E;
+    for (int p = threadIdx.x; p < nt * per_row; p += kThreads) {
+      const int t = p / per_row, e = (p % per_row) * E;
+      cp_async16(xr + t * L::NCH + e, qkv + (size_t)(tok + t) * a.C + channel_of<DK>(e, hq, h, a.hk, a.dv, row0));
+    }
+    for (int p = threadIdx.x; p < nt * (DK / E); p += kThreads) {
+      const int t = p / (DK / E), e = (p % (DK / E)) * E;
+      cp_async16(gs + t * DK + e, ga + ((size_t)(tok + t) * a.hv + h) * DK + e);
+    }
+  } else {
+    for (int p = threadIdx.x; p < nt * nch; p += kThreads) {
+      const int t = p / nch, e = p % nch;
+      xr[t * L::NCH + e] = qkv[(size_t)(tok + t) * a.C + channel_of<DK>(e, hq, h, a.hk, a.dv, row0)];
+    }
+    for (int p = threadIdx.x; p < nt * DK; p += kThreads) {
+      const int t = p / DK, e = p % DK;
+      gs[t * DK + e] = ga[((size_t)(tok + t) * a.hv + h) * DK + e];
+    }
+  }
+}
+
+template <int DK, int NIT, typename Tact, typename Tconv, bool ASYNC>
+__global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const KdaPrefillArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  using M = RowMap<DK>;
+  using L = KdaPrefillSmem<DK, NIT, Tact>;
+  constexpr int R = L::R, NCH = L::NCH;
+  constexpr int kCPT = (NCH + kThreads - 1) / kThreads;  // channels per thread
+  static_assert(kThreads % DK == 0, "a thread's gate channel must be fixed");
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  Tact* xr = reinterpret_cast<Tact*>(smem_raw + L::xr);
+  Tact* gs = reinterpret_cast<Tact*>(smem_raw + L::ga);
+  float* xh = reinterpret_cast<float*>(smem_raw + L::xh);
+  float* cwt = reinterpret_cast<float*>(smem_raw + L::cw);
+  float* sy = reinterpret_cast<float*>(smem_raw + L::sy);
+  float* so = reinterpret_cast<float*>(smem_raw + L::so);
+  float* sscal = reinterpret_cast<float*>(smem_raw + L::sc);
+  float* salk = reinterpret_cast<float*>(smem_raw + L::al);
+  float* sb = reinterpret_cast<float*>(smem_raw + L::sb);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n = blockIdx.y;
+  const int h = blockIdx.x / a.P, p = blockIdx.x % a.P;
+  const int hq = h / a.G;
+  const int row0 = p * R;
+  const int nrows = min(R, a.dv - row0);
+  const int64_t t0 = a.cu_seqlens[n], t1 = a.cu_seqlens[n + 1], len = t1 - t0, p0 = a.start_pos[n];
+  if (t0 < 0 || len < 0 || t1 > a.total || p0 < 0) {
+    if (blockIdx.x == 0 && tid == 0) report(a.err, GDN_DEV_ERR_SEQLENS);
+    return;
+  }
+  Tact* out = reinterpret_cast<Tact*>(a.out);
+  const int32_t slot = a.slot_ids[n];
+  const int cls = slot_class(slot, a.num_slots);
+  if (cls) {
+    if (cls == 2 && blockIdx.x == 0 && tid == 0) report(a.err, GDN_DEV_ERR_SLOT_OOB);
+    for (int64_t e = tid; e < len * nrows; e += kThreads)
+      out[((t0 + e / nrows) * a.hv + h) * a.dv + row0 + e % nrows] = from_f32<Tact>(0.f);
+    return;
+  }
+  if (len == 0) return;
+
+  const Tact* gb = reinterpret_cast<const Tact*>(a.b);
+  // the first window's inputs in flight before anything else
+  kda_stage<DK, NIT, Tact, ASYNC>(a, xr, gs, t0, len < kTW ? (int)len : kTW, nrows, hq, h, row0);
+  if constexpr (ASYNC) cp_async_commit();
+  if (tid < kTW && tid < len) sb[tid] = to_f32(gb[(size_t)(t0 + tid) * a.hv + h]);
+
+  const int seg = lane % M::LPR;
+  const int rloc = warp * M::RW + lane / M::LPR;
+  float* St = a.ssm + (((size_t)slot * a.hv + h) * a.dv + row0) * DK;
+  float4 s[NIT][4];
+  load_rows<DK, NIT>(s, St, nrows, rloc, seg);
+
+  // conv weights and history, right-aligned in kMaxW taps (the newest input
+  // last; the taps before the width are zero), one column per channel
+  const Tconv* hist = reinterpret_cast<const Tconv*>(a.conv) + (size_t)slot * (a.W - 1) * a.C;
+  const int lead = kMaxW - a.W;
+  for (int i = tid; i < 2 * DK + nrows; i += kThreads) {
+    const int ch = channel_of<DK>(i, hq, h, a.hk, a.dv, row0);
+#pragma unroll
+    for (int j = 0; j < kMaxW; ++j) cwt[j * NCH + i] = j >= lead ? a.conv_w[(size_t)ch * a.W + (j - lead)] : 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxW - 1; ++j) xh[j * NCH + i] = j >= lead ? to_f32(hist[(size_t)(j - lead) * a.C + ch]) : 0.f;
+  }
+  const float A_log = a.A_log[h];
+  const float dtb = a.dt_bias[(size_t)h * DK + tid % DK];  // the alphas this thread computes are of channel tid % DK
+  const int64_t blk0 = p0 / a.ckpt_block;
+  if constexpr (ASYNC) cp_async_wait_all();
+  __syncthreads();
+
+  for (int64_t w0 = 0; w0 < len; w0 += kTW) {
+    const int cur = (int)((w0 / kTW) & 1), nxt = cur ^ 1;
+    const int nt = len - w0 < kTW ? (int)(len - w0) : kTW;
+    const int64_t wn = w0 + kTW;
+    const int ntn = wn >= len ? 0 : (len - wn < kTW ? (int)(len - wn) : kTW);
+    // 0. the next window's inputs
+    float bnext = 0.f;
+    if (ntn > 0) {
+      kda_stage<DK, NIT, Tact, ASYNC>(a, xr + nxt * kTW * NCH, gs + nxt * kTW * DK, t0 + wn, ntn, nrows, hq, h, row0);
+      if constexpr (ASYNC) cp_async_commit();
+      if (tid < ntn) bnext = to_f32(gb[(size_t)(t0 + wn + tid) * a.hv + h]);
+    }
+    const Tact* x = xr + cur * kTW * NCH;
+    const Tact* gw = gs + cur * kTW * DK;
+    // 1. conv1d + SiLU of the window's tokens (oldest tap first)
+#pragma unroll
+    for (int ci = 0; ci < kCPT; ++ci) {
+      const int i = tid + ci * kThreads;
+      if (i < 2 * DK + nrows) {
+        float w[kMaxW], win[kMaxW - 1];
+#pragma unroll
+        for (int j = 0; j < kMaxW; ++j) w[j] = cwt[j * NCH + i];
+#pragma unroll
+        for (int j = 0; j < kMaxW - 1; ++j) win[j] = xh[j * NCH + i];
+        for (int t = 0; t < nt; ++t) {
+          const float xv = to_f32(x[t * NCH + i]);
+          float acc = 0.f;
+#pragma unroll
+          for (int j = 0; j < kMaxW - 1; ++j) acc = fmaf(w[j], win[j], acc);
+          acc = fmaf(w[kMaxW - 1], xv, acc);
+          sy[t * NCH + i] = silu_f(acc);
+#pragma unroll
+          for (int j = 0; j < kMaxW - 2; ++j) win[j] = win[j + 1];
+          win[kMaxW - 2] = xv;
+        }
+#pragma unroll
+        for (int j = 0; j < kMaxW - 1; ++j) xh[j * NCH + i] = win[j];
+      }
+    }
+    __syncthreads();
+    // 2. per token: q/k norms, k^.q^, beta (a warp per token) and the alphas
+    for (int t = warp; t < nt; t += kWarps) {
+      const float* yq = sy + t * NCH;
+      const float* yk = yq + DK;
+      float pq = 0.f, pk = 0.f, pqk = 0.f;
+      for (int i = lane; i < DK; i += 32) {
+        pq = fmaf(yq[i], yq[i], pq);
+        pk = fmaf(yk[i], yk[i], pk);
+        pqk = fmaf(yq[i], yk[i], pqk);
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        pq += __shfl_xor_sync(0xffffffffu, pq, o);
+        pk += __shfl_xor_sync(0xffffffffu, pk, o);
+        pqk += __shfl_xor_sync(0xffffffffu, pqk, o);
+      }
+      if (lane == 0) {
+        const float rq = rsqrtf(pq + kNormEps) * rsqrtf((float)DK);
+        const float rk = rsqrtf(pk + kNormEps);
+        sscal[t * 4 + 0] = rq;
+        sscal[t * 4 + 1] = rk;
+        sscal[t * 4 + 2] = pqk * rq * rk;
+        sscal[t * 4 + 3] = sigmoid_f(sb[cur * kTW + t]);
+      }
+    }
+    for (int e = tid; e < nt * DK; e += kThreads) salk[e] = gate_alpha(A_log, dtb, to_f32(gw[e]));
+    __syncthreads();
+    // 3. the recurrence over the window's tokens
+    for (int t = 0; t < nt; ++t) {
+      const float* yq = sy + t * NCH;
+      const float* yk = yq + DK;
+      const float* yv = yk + DK;
+      const float rq = sscal[t * 4 + 0], rk = sscal[t * 4 + 1], kq = sscal[t * 4 + 2], beta = sscal[t * 4 + 3];
+      float4 kk[4], qq[4], al[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float4 k4 = *reinterpret_cast<const float4*>(yk + M::col(c, seg));
+        const float4 q4 = *reinterpret_cast<const float4*>(yq + M::col(c, seg));
+        kk[c] = make_float4(k4.x * rk, k4.y * rk, k4.z * rk, k4.w * rk);
+        qq[c] = make_float4(q4.x * rq, q4.y * rq, q4.z * rq, q4.w * rq);
+        al[c] = *reinterpret_cast<const float4*>(salk + t * DK + M::col(c, seg));
+      }
+      // a block boundary after this token: its checkpoint slot
+      const int64_t P = p0 + w0 + t + 1;
+      float* ck = nullptr;
+      if (P % a.ckpt_block == 0) {
+        const int64_t idx = P / a.ckpt_block - blk0 - 1;
+        if (idx >= 0 && idx < a.max_ckpt) {
+          const int32_t cid = a.ckpt_ids[(size_t)n * a.max_ckpt + idx];
+          const int cc = slot_class(cid, a.ck_num_slots);
+          if (cc == 0) ck = a.ck_ssm + (((size_t)cid * a.hv + h) * a.dv + row0) * DK;
+          else if (cc == 2 && tid == 0) report(a.err, GDN_DEV_ERR_SLOT_OOB);
+        }
+      }
+#pragma unroll
+      for (int it = 0; it < NIT; ++it) {
+        const int row = it * M::RI + rloc;
+        float dk_ = 0.f, dq_ = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float4 sa = make_float4(s[it][c].x * al[c].x, s[it][c].y * al[c].y, s[it][c].z * al[c].z,
+                                        s[it][c].w * al[c].w);
+          dk_ += dot4(sa, kk[c]);
+          dq_ += dot4(sa, qq[c]);
+        }
+#pragma unroll
+        for (int o = M::LPR / 2; o; o >>= 1) {
+          dk_ += __shfl_xor_sync(0xffffffffu, dk_, o);
+          dq_ += __shfl_xor_sync(0xffffffffu, dq_, o);
+        }
+        const float bu = row < nrows ? beta * (yv[row] - dk_) : 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float4& v = s[it][c];
+          v.x = fmaf(bu, kk[c].x, al[c].x * v.x);
+          v.y = fmaf(bu, kk[c].y, al[c].y * v.y);
+          v.z = fmaf(bu, kk[c].z, al[c].z * v.z);
+          v.w = fmaf(bu, kk[c].w, al[c].w * v.w);
+        }
+        if (row < nrows) {
+          if (ck) {
+            float4* dst = reinterpret_cast<float4*>(ck + (size_t)row * DK);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) st_stream(dst + M::col(c, seg) / 4, s[it][c]);
+          }
+          if (seg == 0) so[t * R + row] = fmaf(bu, kq, dq_);
+        }
+      }
+    }
+    __syncthreads();
+    // 4. the window's outputs; the next window's beta logits and inputs land
+    for (int e = tid; e < nt * nrows; e += kThreads) {
+      const int t = e / nrows, i = e % nrows;
+      out[((size_t)(t0 + w0 + t) * a.hv + h) * a.dv + row0 + i] = from_f32<Tact>(so[t * R + i]);
+    }
+    if (tid < ntn) sb[nxt * kTW + tid] = bnext;
+    if constexpr (ASYNC) cp_async_wait_all();
+    __syncthreads();
+  }
+  // the final state
+#pragma unroll
+  for (int it = 0; it < NIT; ++it) {
+    const int row = it * M::RI + rloc;
+    if (row < nrows) {
+      float4* dst = reinterpret_cast<float4*>(St + (size_t)row * DK);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) st_stream(dst + M::col(c, seg) / 4, s[it][c]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 template <int DK, int NIT, typename Tact, typename Tconv>
@@ -527,6 +842,26 @@ cudaError_t dispatch_dtype(bool verify, bool kda, const StepArgs& a, int act, in
                   : launch_decode_t<DK, NIT, __nv_bfloat16, __nv_bfloat16>(a, kda, s);
   return verify ? launch_verify_t<DK, NIT, __nv_bfloat16, float>(a, kda, s)
                 : launch_decode_t<DK, NIT, __nv_bfloat16, float>(a, kda, s);
+}
+
+template <int DK, int NIT, typename Tact, typename Tconv>
+cudaError_t launch_kda_prefill_t(const KdaPrefillArgs& a, int32_t n_seq, bool async, cudaStream_t s) {
+  const size_t smem = KdaPrefillSmem<DK, NIT, Tact>::bytes;
+  auto k = async ? kda_prefill_kernel<DK, NIT, Tact, Tconv, true> : kda_prefill_kernel<DK, NIT, Tact, Tconv, false>;
+  if (smem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  return launch_pdl(k, dim3((unsigned)(a.hv * a.P), (unsigned)n_seq), dim3(kThreads), smem, s, dim3(1), a);
+}
+
+template <int DK, int NIT>
+cudaError_t dispatch_kda_prefill(const KdaPrefillArgs& a, int32_t n_seq, int act, int cv, bool async,
+                                 cudaStream_t s) {
+  if (act == GDN_F32 && cv == GDN_F32) return launch_kda_prefill_t<DK, NIT, float, float>(a, n_seq, async, s);
+  if (act == GDN_BF16 && cv == GDN_BF16)
+    return launch_kda_prefill_t<DK, NIT, __nv_bfloat16, __nv_bfloat16>(a, n_seq, async, s);
+  return launch_kda_prefill_t<DK, NIT, __nv_bfloat16, float>(a, n_seq, async, s);
 }
 
 // rows-per-CTA choice: fewer rows (more CTAs, smaller clusters of work) when
@@ -700,4 +1035,74 @@ extern "C" gdn_status gdn_spec_verify(const gdn_dims* dims, gdn_pool work, gdn_p
                                       uint32_t* dev_err, void* stream) {
   return gdn::run_step(true, false, dims, work, &spec, params, slot_ids, spec_ids, B, T, qkv, a, b, out,
                        dev_err, stream);
+}
+
+extern "C" gdn_status gdn_kda_prefill(const gdn_dims* dims, gdn_pool pool, gdn_pool ckpt,
+                                      const gdn_params* params, const int32_t* slot_ids,
+                                      const int32_t* cu_seqlens, const int64_t* start_pos, int32_t n_seq,
+                                      int64_t total_tokens, const int32_t* ckpt_ids, int32_t max_ckpt,
+                                      int32_t ckpt_block, const void* qkv, const void* a, const void* b,
+                                      void* out, uint32_t* dev_err, void* stream) {
+  using namespace gdn;
+  gdn_status st = check_dims(dims);
+  if (st != GDN_OK) return st;
+  if (n_seq < 0 || total_tokens < 0 || max_ckpt < 0) return GDN_ERR_INVALID_ARG;
+  if (ckpt_block <= 0 || ckpt_block % 64) return GDN_ERR_INVALID_ARG;
+  if (n_seq == 0) return GDN_OK;
+  if (n_seq > 65535 || total_tokens > 2147483647LL || max_ckpt > 4 * 65535) return GDN_ERR_UNSUPPORTED;
+  if ((st = check_pool(*dims, pool)) != GDN_OK) return st;
+  if (max_ckpt > 0 && (st = check_pool(*dims, ckpt)) != GDN_OK) return st;
+  if (!params || !params->conv_w || !params->A_log || !params->dt_bias) return GDN_ERR_INVALID_ARG;
+  if (!slot_ids || !cu_seqlens || !start_pos || (max_ckpt > 0 && !ckpt_ids)) return GDN_ERR_INVALID_ARG;
+  if (total_tokens > 0 && (!qkv || !a || !b || !out)) return GDN_ERR_INVALID_ARG;
+  const int G = dims->hv / dims->hk;
+  KdaPrefillArgs k = {};
+  k.ssm = pool.ssm;
+  k.conv = pool.conv;
+  k.num_slots = pool.num_slots;
+  k.ck_ssm = ckpt.ssm;
+  k.ck_num_slots = max_ckpt > 0 ? ckpt.num_slots : 0;
+  k.conv_w = params->conv_w;
+  k.A_log = params->A_log;
+  k.dt_bias = params->dt_bias;
+  k.slot_ids = slot_ids;
+  k.cu_seqlens = cu_seqlens;
+  k.start_pos = start_pos;
+  k.total = total_tokens;
+  k.ckpt_ids = ckpt_ids;
+  k.max_ckpt = max_ckpt;
+  k.ckpt_block = ckpt_block;
+  k.qkv = qkv;
+  k.a = a;
+  k.b = b;
+  k.out = out;
+  k.err = dev_err;
+  k.hk = dims->hk;
+  k.hv = dims->hv;
+  k.dv = dims->dv;
+  k.W = dims->conv_width;
+  k.C = (int32_t)channels(*dims);
+  k.G = G;
+  // rows per CTA: the kernel's NIT row groups of kWarps * 32 / (dk / 16) rows
+  const int rows = (dims->dk == 128 ? 2 : 1) * kWarps * (32 / (dims->dk / 16));
+  k.P = (dims->dv + rows - 1) / rows;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const int act = dims->act_dtype, cv = dims->conv_dtype;
+  // 16-byte staging copies: qkv and a 16-byte aligned, and every channel
+  // segment (q and k heads, the v rows of a CTA, a gate row) and row stride a
+  // multiple of 16 bytes (the CTA row counts are multiples of 8)
+  const size_t es = dtype_size(act);
+  const bool async = aligned(qkv, 16) && aligned(a, 16) && ((size_t)dims->dk * es) % 16 == 0 &&
+                     ((size_t)dims->dv * es) % 16 == 0 && ((size_t)k.C * es) % 16 == 0;
+  cudaError_t e = cudaErrorInvalidValue;
+  switch (dims->dk) {
+    case 16: e = dispatch_kda_prefill<16, 1>(k, n_seq, act, cv, async, cs); break;
+    case 64: e = dispatch_kda_prefill<64, 1>(k, n_seq, act, cv, async, cs); break;
+    case 128: e = dispatch_kda_prefill<128, 2>(k, n_seq, act, cv, async, cs); break;
+  }
+  if (e == cudaSuccess)
+    e = conv_history_launch(*dims, pool, ckpt, slot_ids, cu_seqlens, start_pos, n_seq, total_tokens, ckpt_ids,
+                            max_ckpt, ckpt_block, qkv, dev_err, cs);
+  if (e == cudaSuccess) count_launch(GDN_K_KDA_PREFILL);
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }

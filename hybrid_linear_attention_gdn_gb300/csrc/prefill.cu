@@ -496,6 +496,40 @@ bool use_tc_prefill(const gdn_dims& d, const void* qkv, const void* out, const g
 }
 
 }  // namespace
+
+// The conv histories of a prefill's checkpoints and of its final state, for
+// prefill paths that write only the SSM states (the KDA recurrence).
+cudaError_t conv_history_launch(const gdn_dims& d, const gdn_pool& pool, const gdn_pool& ckpt,
+                                const int32_t* slot_ids, const int32_t* cu_seqlens, const int64_t* start_pos,
+                                int32_t n_seq, int64_t total, const int32_t* ckpt_ids, int32_t max_ckpt,
+                                int32_t ckpt_block, const void* qkv, uint32_t* dev_err, cudaStream_t s) {
+  PrefillArgs p = {};
+  p.ssm = pool.ssm;
+  p.conv = pool.conv;
+  p.num_slots = pool.num_slots;
+  p.ck_ssm = ckpt.ssm;
+  p.ck_conv = ckpt.conv;
+  p.ck_num_slots = max_ckpt > 0 ? ckpt.num_slots : 0;
+  p.slot_ids = slot_ids;
+  p.cu_seqlens = cu_seqlens;
+  p.start_pos = start_pos;
+  p.n_seq = n_seq;
+  p.total = total;
+  p.ckpt_ids = ckpt_ids;
+  p.max_ckpt = max_ckpt;
+  p.ckpt_block = ckpt_block;
+  p.qkv = qkv;
+  p.err = dev_err;
+  p.hk = d.hk;
+  p.hv = d.hv;
+  p.dk = d.dk;
+  p.dv = d.dv;
+  p.W = d.conv_width;
+  p.C = (int32_t)channels(d);
+  p.G = d.hv / d.hk;
+  return launch_history(p, d.act_dtype, d.conv_dtype, s);
+}
+
 }  // namespace gdn
 
 // Sized for either path (the tensor-core path needs about half of it).

@@ -11,4 +11,9 @@ cudaError_t prefill_tc_launch(const gdn_dims& d, const gdn_pool& pool, const gdn
                               const int32_t* ckpt_ids, int32_t max_ckpt, int32_t ckpt_block,
                               const void* qkv, const void* a, const void* b, void* out,
                               void* workspace, uint32_t* dev_err, cudaStream_t s);
+// conv histories of a prefill's checkpoints and final state (prefill.cu)
+cudaError_t conv_history_launch(const gdn_dims& d, const gdn_pool& pool, const gdn_pool& ckpt,
+                                const int32_t* slot_ids, const int32_t* cu_seqlens, const int64_t* start_pos,
+                                int32_t n_seq, int64_t total, const int32_t* ckpt_ids, int32_t max_ckpt,
+                                int32_t ckpt_block, const void* qkv, uint32_t* dev_err, cudaStream_t s);
 }  // namespace gdn

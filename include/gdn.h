@@ -139,6 +139,21 @@ gdn_status gdn_kda_spec_verify(const gdn_dims* dims, gdn_pool work, gdn_pool spe
                                void* out, uint32_t* dev_err, void* stream);
 
 /*
+ * KDA prefill (the recurrent form, fp32): the contract of gdn_chunk_prefill
+ * (packed sequences from any start position, block-aligned checkpoints of SSM
+ * state and conv history, final state into the working slot) with every
+ * token the KDA step of gdn_kda_decode_step; a [total_tokens][hv][dk],
+ * params->dt_bias [hv][dk].  Token by token, so it needs no workspace;
+ * ckpt_block a positive multiple of 64.
+ */
+gdn_status gdn_kda_prefill(const gdn_dims* dims, gdn_pool pool, gdn_pool ckpt,
+                           const gdn_params* params, const int32_t* slot_ids,
+                           const int32_t* cu_seqlens, const int64_t* start_pos, int32_t n_seq,
+                           int64_t total_tokens, const int32_t* ckpt_ids, int32_t max_ckpt,
+                           int32_t ckpt_block, const void* qkv, const void* a, const void* b,
+                           void* out, uint32_t* dev_err, void* stream);
+
+/*
  * Speculative verify (TokenSpeed Qwen3.5 page, "Scheduler dual": spec_cache
  * of per-step conv/SSM snapshots for rollback).  Request r runs its T draft
  * tokens starting from working slot slot_ids[r], which is NOT modified; after
@@ -356,7 +371,8 @@ const char* gdn_status_string(int32_t status);
 #define GDN_K_GATED_RMSNORM 8
 #define GDN_K_KDA_DECODE 9
 #define GDN_K_KDA_VERIFY 10
-#define GDN_K_COUNT 11
+#define GDN_K_KDA_PREFILL 11 /* the recurrence and its conv-history kernel */
+#define GDN_K_COUNT 12
 uint64_t gdn_launch_count(int32_t kernel);
 void gdn_launch_count_reset(void);
 

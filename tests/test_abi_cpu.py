@@ -163,6 +163,25 @@ def test_mixed_step_arguments(lib):
     assert lib.gdn_launch_count(binding.K_PREFILL) == n_pre0
 
 
+def test_kda_prefill_arguments(lib):
+    d = _dims()
+    pool = binding.CPool(0x10000, 0x20000, 4)
+    p = binding.CParams(0x1000, 0x2000, 0x3000)
+    args = lambda n_seq, total, blk=256, params=p, slots=0x100: (  # noqa: E731
+        ctypes.byref(d), pool, pool, ctypes.byref(params) if params else None, slots, 0x200, 0x300, n_seq,
+        total, None, 0, blk, 0x400, 0x500, 0x600, 0x700, None, None)
+    n0 = lib.gdn_launch_count(binding.K_KDA_PREFILL)
+    assert lib.gdn_kda_prefill(*args(2, 10, blk=100)) == binding.ERR_INVALID_ARG  # block not a multiple of 64
+    assert lib.gdn_kda_prefill(*args(2, 10, blk=0)) == binding.ERR_INVALID_ARG
+    assert lib.gdn_kda_prefill(*args(-1, 10)) == binding.ERR_INVALID_ARG
+    assert lib.gdn_kda_prefill(*args(2, -1)) == binding.ERR_INVALID_ARG
+    assert lib.gdn_kda_prefill(*args(70000, 10)) == binding.ERR_UNSUPPORTED
+    assert lib.gdn_kda_prefill(*args(2, 10, params=None)) == binding.ERR_INVALID_ARG
+    assert lib.gdn_kda_prefill(*args(2, 10, slots=None)) == binding.ERR_INVALID_ARG
+    assert lib.gdn_kda_prefill(*args(0, 0)) == binding.OK
+    assert lib.gdn_launch_count(binding.K_KDA_PREFILL) == n0
+
+
 def test_gated_rmsnorm_arguments(lib):
     d = _dims()
     n0 = lib.gdn_launch_count(binding.K_GATED_RMSNORM)
