@@ -508,6 +508,27 @@ __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const StepArgs a) {
 // ---------------------------------------------------------------------------
 constexpr int kTW = 16;
 
+// Packed fp32 pairs (Blackwell f32x2 instructions, round to nearest: each
+// half is bit-identical to the scalar operation).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}\n"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mul.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}\n"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 lo2(float4 v) { return make_float2(v.x, v.y); }
+__device__ __forceinline__ float2 hi2(float4 v) { return make_float2(v.z, v.w); }
+
 struct KdaPrefillArgs {
   float* ssm;
   const void* conv;
@@ -650,9 +671,12 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const KdaPrefi
 #pragma unroll
     for (int j = 0; j < kMaxW - 1; ++j) xh[j * NCH + i] = j >= lead ? to_f32(hist[(size_t)(j - lead) * a.C + ch]) : 0.f;
   }
-  const float A_log = a.A_log[h];
+  const float eA = expf(a.A_log[h]);
   const float dtb = a.dt_bias[(size_t)h * DK + tid % DK];  // the alphas this thread computes are of channel tid % DK
   const int64_t blk0 = p0 / a.ckpt_block;
+  // the next block boundary (absolute position) and its checkpoint index
+  int64_t next_bd = (blk0 + 1) * a.ckpt_block;
+  int64_t ck_idx = 0;
   if constexpr (ASYNC) cp_async_wait_all();
   __syncthreads();
 
@@ -680,16 +704,20 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const KdaPrefi
         for (int j = 0; j < kMaxW; ++j) w[j] = cwt[j * NCH + i];
 #pragma unroll
         for (int j = 0; j < kMaxW - 1; ++j) win[j] = xh[j * NCH + i];
-        for (int t = 0; t < nt; ++t) {
-          const float xv = to_f32(x[t * NCH + i]);
-          float acc = 0.f;
+        // unrolled: the tokens' products and SiLUs are independent
 #pragma unroll
-          for (int j = 0; j < kMaxW - 1; ++j) acc = fmaf(w[j], win[j], acc);
-          acc = fmaf(w[kMaxW - 1], xv, acc);
-          sy[t * NCH + i] = silu_f(acc);
+        for (int t = 0; t < kTW; ++t) {
+          if (t < nt) {
+            const float xv = to_f32(x[t * NCH + i]);
+            float acc = 0.f;
 #pragma unroll
-          for (int j = 0; j < kMaxW - 2; ++j) win[j] = win[j + 1];
-          win[kMaxW - 2] = xv;
+            for (int j = 0; j < kMaxW - 1; ++j) acc = fmaf(w[j], win[j], acc);
+            acc = fmaf(w[kMaxW - 1], xv, acc);
+            sy[t * NCH + i] = __fdividef(acc, 1.f + exp_ftz(-acc));  // SiLU
+#pragma unroll
+            for (int j = 0; j < kMaxW - 2; ++j) win[j] = win[j + 1];
+            win[kMaxW - 2] = xv;
+          }
         }
 #pragma unroll
         for (int j = 0; j < kMaxW - 1; ++j) xh[j * NCH + i] = win[j];
@@ -721,7 +749,8 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const KdaPrefi
         sscal[t * 4 + 3] = sigmoid_f(sb[cur * kTW + t]);
       }
     }
-    for (int e = tid; e < nt * DK; e += kThreads) salk[e] = gate_alpha(A_log, dtb, to_f32(gw[e]));
+    // alpha = exp(-exp(A_log) * softplus(a + dt_bias))
+    for (int e = tid; e < nt * DK; e += kThreads) salk[e] = expf(-eA * softplus_f(to_f32(gw[e]) + dtb));
     __syncthreads();
     // 3. the recurrence over the window's tokens
     for (int t = 0; t < nt; ++t) {
@@ -729,21 +758,20 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const KdaPrefi
       const float* yk = yq + DK;
       const float* yv = yk + DK;
       const float rq = sscal[t * 4 + 0], rk = sscal[t * 4 + 1], kq = sscal[t * 4 + 2], beta = sscal[t * 4 + 3];
-      float4 kk[4], qq[4], al[4];
+      // unnormalised q and k: the norms scale the dot products and the update
+      float4 kr[4], qr[4], al[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const float4 k4 = *reinterpret_cast<const float4*>(yk + M::col(c, seg));
-        const float4 q4 = *reinterpret_cast<const float4*>(yq + M::col(c, seg));
-        kk[c] = make_float4(k4.x * rk, k4.y * rk, k4.z * rk, k4.w * rk);
-        qq[c] = make_float4(q4.x * rq, q4.y * rq, q4.z * rq, q4.w * rq);
+        kr[c] = *reinterpret_cast<const float4*>(yk + M::col(c, seg));
+        qr[c] = *reinterpret_cast<const float4*>(yq + M::col(c, seg));
         al[c] = *reinterpret_cast<const float4*>(salk + t * DK + M::col(c, seg));
       }
       // a block boundary after this token: its checkpoint slot
-      const int64_t P = p0 + w0 + t + 1;
       float* ck = nullptr;
-      if (P % a.ckpt_block == 0) {
-        const int64_t idx = P / a.ckpt_block - blk0 - 1;
-        if (idx >= 0 && idx < a.max_ckpt) {
+      if (p0 + w0 + t + 1 == next_bd) {
+        const int64_t idx = ck_idx++;
+        next_bd += a.ckpt_block;
+        if (idx < a.max_ckpt) {
           const int32_t cid = a.ckpt_ids[(size_t)n * a.max_ckpt + idx];
           const int cc = slot_class(cid, a.ck_num_slots);
           if (cc == 0) ck = a.ck_ssm + (((size_t)cid * a.hv + h) * a.dv + row0) * DK;
@@ -753,27 +781,30 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const KdaPrefi
 #pragma unroll
       for (int it = 0; it < NIT; ++it) {
         const int row = it * M::RI + rloc;
-        float dk_ = 0.f, dq_ = 0.f;
+        // the rows become St diag(alpha) in place; the update adds beta u k^T
+        float2 dk2 = make_float2(0.f, 0.f), dq2 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const float4 sa = make_float4(s[it][c].x * al[c].x, s[it][c].y * al[c].y, s[it][c].z * al[c].z,
-                                        s[it][c].w * al[c].w);
-          dk_ += dot4(sa, kk[c]);
-          dq_ += dot4(sa, qq[c]);
+          float4& v = s[it][c];
+          const float2 lo = mul2(lo2(v), lo2(al[c])), hi = mul2(hi2(v), hi2(al[c]));
+          v = make_float4(lo.x, lo.y, hi.x, hi.y);
+          dk2 = fma2(hi, hi2(kr[c]), fma2(lo, lo2(kr[c]), dk2));
+          dq2 = fma2(hi, hi2(qr[c]), fma2(lo, lo2(qr[c]), dq2));
         }
+        float dk_ = dk2.x + dk2.y, dq_ = dq2.x + dq2.y;
 #pragma unroll
         for (int o = M::LPR / 2; o; o >>= 1) {
           dk_ += __shfl_xor_sync(0xffffffffu, dk_, o);
           dq_ += __shfl_xor_sync(0xffffffffu, dq_, o);
         }
-        const float bu = row < nrows ? beta * (yv[row] - dk_) : 0.f;
+        dq_ *= rq;
+        const float bu = row < nrows ? beta * (yv[row] - dk_ * rk) : 0.f;
+        const float2 buk = make_float2(bu * rk, bu * rk);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           float4& v = s[it][c];
-          v.x = fmaf(bu, kk[c].x, al[c].x * v.x);
-          v.y = fmaf(bu, kk[c].y, al[c].y * v.y);
-          v.z = fmaf(bu, kk[c].z, al[c].z * v.z);
-          v.w = fmaf(bu, kk[c].w, al[c].w * v.w);
+          const float2 lo = fma2(buk, lo2(kr[c]), lo2(v)), hi = fma2(buk, hi2(kr[c]), hi2(v));
+          v = make_float4(lo.x, lo.y, hi.x, hi.y);
         }
         if (row < nrows) {
           if (ck) {
