@@ -310,6 +310,20 @@ def run_ours(args):
     tok_s = whole_job_rate(B_HEAD * args.steps, ws, ms)
     step_bytes = B_HEAD * DECODE_TOKEN_BYTES + DECODE_STEP_PARAM_BYTES
     achieved = step_bytes / (ms_step * 1e-3) / 1e9
+    # per-step distribution: a separate pass after the timed one, an event
+    # around every step (the events themselves add a little to each step)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    evs[0].record(stream)
+    for i in range(args.steps):
+        step(i)
+        evs[i + 1].record(stream)
+    evs[-1].synchronize()
+    per_step = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps))
+
+    def pct(q):
+        return per_step[min(len(per_step) - 1, int(q * (len(per_step) - 1) + 0.5))]
+    step_stats = {"median": statistics.median(per_step), "p10": pct(0.10), "p90": pct(0.90),
+                  "how": "separate pass, CUDA events around each step"}
     src = os.path.join(ROOT, "hybrid_linear_attention_gdn_gb300", "csrc", "decode_tma.cu")
     traffic = DECODE_TRAFFIC["bytes_per_launch"] if DECODE_TRAFFIC["source_sha256"] == _sha(src) else None
 
@@ -395,7 +409,7 @@ def run_ours(args):
     cpu = None if (ws > 1 or args.no_cpu) else _cpu_baseline()
     line = {
         "metric": METRIC, "value": tok_s, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": ms_step, "step_ms": step_stats, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": headline_config(n_slots, n_sets, ws),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",

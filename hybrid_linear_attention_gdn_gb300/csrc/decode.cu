@@ -974,10 +974,10 @@ gdn_status run_step(bool verify, bool kda, const gdn_dims* dims, const gdn_pool&
     if (e == cudaSuccess) count_launch(kda ? GDN_K_KDA_DECODE : GDN_K_DECODE);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
   }
-  if (verify && !kda && use_tma_verify(*dims, B, T, qkv, *params)) {
+  if (verify && kda_aligned && use_tma_verify(*dims, B, T, qkv, *params)) {
     cudaError_t e = verify_tma_launch(*dims, work, *spec, *params, slot_ids, spec_ids, B, T, qkv, a,
-                                      b, out, dev_err, cs);
-    if (e == cudaSuccess) count_launch(GDN_K_SPEC_VERIFY);
+                                      b, out, dev_err, kda, cs);
+    if (e == cudaSuccess) count_launch(kda ? GDN_K_KDA_VERIFY : GDN_K_SPEC_VERIFY);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
   }
   StepArgs s = {};

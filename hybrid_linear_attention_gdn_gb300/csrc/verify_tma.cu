@@ -20,8 +20,13 @@
 //     T drafts, each draft's rows streamed to its spec slot with 128-bit stores.
 // Snapshot writes are T times the state reads, so HBM time is mostly stores.
 // All waits are bounded (GDN_DEV_ERR_TIMEOUT).
+//
+// KDA (one decay per key channel): the bundle also carries the T drafts' gate
+// logits of the V head and its dt_bias row; the consumers turn them into an
+// alpha table [T][dk] and scale each row by it in place before its products.
 #include "gdn_common.cuh"
 
+#include <cstddef>
 #include <cstdlib>
 #include "decode_tma.cuh"
 
@@ -45,21 +50,34 @@ constexpr int kBarCons = 1;
 // MT: drafts the shared-memory layout holds (T <= MT).  The T <= 8 layout is
 // small enough for two CTAs per SM, so one CTA's prologue overlaps the other's
 // stream of snapshot stores.
-template <typename Tact, typename Tconv, int STAGES, int MT>
+template <typename Tact, typename Tconv, int STAGES, int MT, bool KDA>
 struct __align__(128) VSmem {
   float ring[STAGES][kStageFloats];
-  struct Bundle {
+  // every member a multiple of 16 bytes long, so that every bulk-copy
+  // destination in both bundles is 16-byte aligned
+  struct __align__(16) Bundle {
     Tconv hist[kW - 1][kMaxCh];
     Tact x[MT][kMaxCh];
     float w[kMaxCh * kW];
+    Tact ga[KDA ? MT : 1][KDA ? kDK : 8];  // KDA: the drafts' gate logits of the V head
+    float gdt[KDA ? kDK : 4];              // KDA: its dt_bias row
   } bundle[2];
   float sy[MT][kMaxCh];   // conv + SiLU per draft: q | k | v rows
   float so[MT][kMaxR];    // readout per draft
   float snorm[MT][3];     // rq, rk, k^.q^ per draft
   float sgate[MT][2];     // alpha, beta per draft
+  float sal[KDA ? MT : 1][kDK];  // KDA: alpha per draft and key channel
   uint64_t full[STAGES], empty[STAGES], bfull[2], bempty[2];
   int abort;
 };
+
+template <typename Tact, typename Tconv, int STAGES, int MT, bool KDA>
+__host__ __device__ constexpr bool vbundle_aligned() {
+  using V = VSmem<Tact, Tconv, STAGES, MT, KDA>;
+  using B = typename V::Bundle;
+  return sizeof(B) % 16 == 0 && offsetof(B, x) % 16 == 0 && offsetof(B, w) % 16 == 0 &&
+         offsetof(B, ga) % 16 == 0 && offsetof(B, gdt) % 16 == 0 && offsetof(V, bundle) % 16 == 0;
+}
 
 struct VArgs {
   const float* ssm;
@@ -81,11 +99,12 @@ struct VArgs {
   int32_t hk, hv, dv, C, G, P, T, n_items;
 };
 
-template <typename Tact, typename Tconv, int STAGES, int MT, int MINB>
+template <typename Tact, typename Tconv, int STAGES, int MT, int MINB, bool KDA>
 __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
   pdl_wait();
   pdl_trigger();
-  using SM = VSmem<Tact, Tconv, STAGES, MT>;
+  using SM = VSmem<Tact, Tconv, STAGES, MT, KDA>;
+  static_assert(vbundle_aligned<Tact, Tconv, STAGES, MT, KDA>(), "bundle members must stay 16-byte aligned");
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   SM& S = *reinterpret_cast<SM*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -114,7 +133,8 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
     // ------------------------------------------------------------ producer
     if (lane != 0) return;
     const uint32_t ec = sizeof(Tconv), ea = sizeof(Tact);
-    const uint32_t bundle_bytes = (kW - 1) * nch * ec + T * nch * ea + nch * kW * 4;
+    const uint32_t bundle_bytes =
+        (kW - 1) * nch * ec + T * nch * ea + nch * kW * 4 + (KDA ? T * kDK * ea + kDK * 4 : 0u);
     uint32_t n = 0, vk = 0;
     bool ok = true;
     for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
@@ -144,6 +164,12 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
       bulk_g2s(&Bd.w[0], a.conv_w + cq * kW, kDK * kW * 4, &S.bfull[bb]);
       bulk_g2s(&Bd.w[kDK * kW], a.conv_w + ck * kW, kDK * kW * 4, &S.bfull[bb]);
       bulk_g2s(&Bd.w[2 * kDK * kW], a.conv_w + cv * kW, R * kW * 4, &S.bfull[bb]);
+      if constexpr (KDA) {
+        for (int t = 0; t < T; ++t)
+          bulk_g2s(&Bd.ga[t][0], reinterpret_cast<const Tact*>(a.a) + (((size_t)r * T + t) * a.hv + h) * kDK,
+                   kDK * ea, &S.bfull[bb]);
+        bulk_g2s(&Bd.gdt[0], a.dt_bias + (size_t)h * kDK, kDK * 4, &S.bfull[bb]);
+      }
       ++vk;
       const float* src = a.ssm + (((size_t)slot * a.hv + h) * a.dv + (size_t)p * R) * kDK;
       for (int c = 0; c < nchunks; ++c, ++n) {
@@ -221,9 +247,18 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
     }
     if (tid < T) {
       const size_t rt = (size_t)r * T + tid;
-      S.sgate[tid][0] = gate_alpha(a.A_log[h], a.dt_bias[h],
-                                   to_f32(reinterpret_cast<const Tact*>(a.a)[rt * a.hv + h]));
+      S.sgate[tid][0] = KDA ? 1.f
+                            : gate_alpha(a.A_log[h], a.dt_bias[h],
+                                         to_f32(reinterpret_cast<const Tact*>(a.a)[rt * a.hv + h]));
       S.sgate[tid][1] = sigmoid_f(to_f32(reinterpret_cast<const Tact*>(a.b)[rt * a.hv + h]));
+    }
+    if constexpr (KDA) {
+      // alpha[t][c] = exp(-exp(A_log) softplus(a[t][c] + dt_bias[c])), from the bundle
+      const float A_log = a.A_log[h];
+      for (int e = tid; e < T * kDK; e += kCons) {
+        const int t = e / kDK, c = e % kDK;
+        S.sal[t][c] = gate_alpha(A_log, Bd.gdt[c], to_f32(Bd.ga[t][c]));
+      }
     }
     named_sync(kBarCons, kCons);
     mbar_arrive(&S.bempty[bb]);
@@ -273,6 +308,11 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
           const float4 q4 = *reinterpret_cast<const float4*>(&S.sy[t][col]);
           kk[cc] = make_float4(k4.x * rk, k4.y * rk, k4.z * rk, k4.w * rk);
           qq[cc] = make_float4(q4.x * rq, q4.y * rq, q4.z * rq, q4.w * rq);
+          if constexpr (KDA) {
+            // the row becomes St diag(alpha) before its products
+            const float4 al = *reinterpret_cast<const float4*>(&S.sal[t][col]);
+            s4[cc] = make_float4(s4[cc].x * al.x, s4[cc].y * al.y, s4[cc].z * al.z, s4[cc].w * al.w);
+          }
         }
         float dk_ = 0.f, dq_ = 0.f;
 #pragma unroll
@@ -285,13 +325,14 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
           dk_ += __shfl_xor_sync(0xffffffffu, dk_, o);
           dq_ += __shfl_xor_sync(0xffffffffu, dq_, o);
         }
+        // KDA: alpha is 1 here (the rows carry the per-channel decay already)
         const float bu = beta * (S.sy[t][2 * kDK + row] - alpha * dk_);
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
-          s4[cc].x = fmaf(bu, kk[cc].x, alpha * s4[cc].x);
-          s4[cc].y = fmaf(bu, kk[cc].y, alpha * s4[cc].y);
-          s4[cc].z = fmaf(bu, kk[cc].z, alpha * s4[cc].z);
-          s4[cc].w = fmaf(bu, kk[cc].w, alpha * s4[cc].w);
+          s4[cc].x = fmaf(bu, kk[cc].x, KDA ? s4[cc].x : alpha * s4[cc].x);
+          s4[cc].y = fmaf(bu, kk[cc].y, KDA ? s4[cc].y : alpha * s4[cc].y);
+          s4[cc].z = fmaf(bu, kk[cc].z, KDA ? s4[cc].z : alpha * s4[cc].z);
+          s4[cc].w = fmaf(bu, kk[cc].w, KDA ? s4[cc].w : alpha * s4[cc].w);
         }
         const int32_t sid = sids[t];
         if (slot_class(sid, a.spec_num_slots) == 0) {
@@ -316,10 +357,10 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
   if (*abort_flag && tid == 0) report(a.err, GDN_DEV_ERR_TIMEOUT);
 }
 
-template <typename Tact, typename Tconv, int STAGES, int MT, int MINB>
+template <typename Tact, typename Tconv, int STAGES, int MT, int MINB, bool KDA>
 cudaError_t launch_v(const VArgs& a, cudaStream_t s) {
-  using SM = VSmem<Tact, Tconv, STAGES, MT>;
-  auto k = verify_tma_kernel<Tact, Tconv, STAGES, MT, MINB>;
+  using SM = VSmem<Tact, Tconv, STAGES, MT, KDA>;
+  auto k = verify_tma_kernel<Tact, Tconv, STAGES, MT, MINB, KDA>;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -333,10 +374,19 @@ cudaError_t launch_v(const VArgs& a, cudaStream_t s) {
   return launch_plain(k, dim3((unsigned)grid), dim3(kThr), sizeof(SM), s, dim3(1), a);
 }
 
-template <typename Tact, typename Tconv>
+template <typename Tact, typename Tconv, bool KDA>
 cudaError_t launch_v_dt(const VArgs& a, cudaStream_t s) {
-  if (a.T <= 8 && tma_ctas_per_sm() != 1) return launch_v<Tact, Tconv, 3, 8, 2>(a, s);
-  return launch_v<Tact, Tconv, 4, kMaxT, 1>(a, s);
+  // the two-CTA layout only where two fit on an SM (not KDA with fp32 activations)
+  constexpr bool kTwoFit = 2 * (sizeof(VSmem<Tact, Tconv, 3, 8, KDA>) + 1024) <= 228 * 1024;
+  if (kTwoFit && a.T <= 8 && tma_ctas_per_sm() != 1) return launch_v<Tact, Tconv, 3, 8, 2, KDA>(a, s);
+  return launch_v<Tact, Tconv, 4, kMaxT, 1, KDA>(a, s);
+}
+
+template <bool KDA>
+cudaError_t launch_v_kda(const gdn_dims& d, const VArgs& a, cudaStream_t s) {
+  if (d.act_dtype == GDN_BF16 && d.conv_dtype == GDN_BF16) return launch_v_dt<__nv_bfloat16, __nv_bfloat16, KDA>(a, s);
+  if (d.act_dtype == GDN_BF16) return launch_v_dt<__nv_bfloat16, float, KDA>(a, s);
+  return launch_v_dt<float, float, KDA>(a, s);
 }
 
 }  // namespace
@@ -355,7 +405,7 @@ bool verify_tma_supported(const gdn_dims& d, int32_t T, const void* qkv, const g
 cudaError_t verify_tma_launch(const gdn_dims& d, const gdn_pool& work, const gdn_pool& spec,
                               const gdn_params& p, const int32_t* slot_ids, const int32_t* spec_ids,
                               int32_t B, int32_t T, const void* qkv, const void* av, const void* bv,
-                              void* out, uint32_t* dev_err, cudaStream_t s) {
+                              void* out, uint32_t* dev_err, bool kda, cudaStream_t s) {
   VArgs a;
   a.ssm = work.ssm;
   a.conv = work.conv;
@@ -392,10 +442,7 @@ cudaError_t verify_tma_launch(const gdn_dims& d, const gdn_pool& work, const gdn
   if (d.dv % P || (d.dv / P) % kRows || d.dv / P > kMaxR) return cudaErrorInvalidValue;
   a.P = P;
   a.n_items = B * d.hv * P;
-  if (d.act_dtype == GDN_BF16 && d.conv_dtype == GDN_BF16)
-    return launch_v_dt<__nv_bfloat16, __nv_bfloat16>(a, s);
-  if (d.act_dtype == GDN_BF16) return launch_v_dt<__nv_bfloat16, float>(a, s);
-  return launch_v_dt<float, float>(a, s);
+  return kda ? launch_v_kda<true>(d, a, s) : launch_v_kda<false>(d, a, s);
 }
 
 }  // namespace gdn

@@ -114,11 +114,21 @@ def test_kda_padding_and_bad_ids(cuda):
     assert max_rel_l2(to_np(st.pool.ssm), st.opool.ssm, shape.dv * shape.dk) <= STATE_TOL_1
 
 
-@pytest.mark.parametrize("shape,B,T", [
-    (synth.QWEN, 16, 8), (synth.QWEN, 3, 16), (synth.TINY, 2, 5),
-    (synth.QWEN.replace(act="f32", conv="f32", hk=4, hv=8), 5, 4),
-], ids=["qwen_b16_t8", "qwen_b3_t16", "tiny", "f32_b5_t4"])
-def test_kda_verify_vs_oracle(cuda, shape, B, T):
+@pytest.mark.parametrize("shape,B,T,path", [
+    (synth.QWEN, 16, 8, "auto"), (synth.QWEN, 3, 16, "auto"), (synth.TINY, 2, 5, "auto"),
+    (synth.QWEN.replace(act="f32", conv="f32", hk=4, hv=8), 5, 4, "auto"),
+    (synth.QWEN, 32, 8, "auto"),
+    (synth.QWEN, 3, 16, "tma"), (synth.QWEN, 7, 5, "tma"),
+    (synth.QWEN.replace(act="f32", conv="f32", hk=4, hv=8), 5, 4, "tma"),
+    (synth.QWEN.replace(conv="f32"), 4, 8, "tma"),
+], ids=["qwen_b16_t8", "qwen_b3_t16", "tiny", "f32_b5_t4", "qwen_b32_t8_persistent", "qwen_b3_t16_tma",
+        "qwen_b7_t5_tma", "f32_b5_t4_tma", "bf16_f32conv_b4_t8_tma"])
+def test_kda_verify_vs_oracle(cuda, monkeypatch, shape, B, T, path):
+    """path "tma" forces the persistent TMA-fed verify kernel (the library reads
+    GDN_DECODE_PATH on every call); batch 32 of the Qwen layer takes it by
+    itself (1024 (request, V head) items, at least 6 per SM)."""
+    if path == "tma":
+        monkeypatch.setenv("GDN_DECODE_PATH", "tma")
     n_work = 8 if shape is synth.TINY else 40
     st = Setup(shape, seed=90 + B, num_slots=n_work)
     params, oparams = _kda_params(st, 91)
