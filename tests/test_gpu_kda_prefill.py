@@ -2,7 +2,8 @@
 KDA prefill: outputs, final states, checkpoint states and conv histories on
 packed sequences from arbitrary start positions; uniform gates land on the
 GDN prefill; a prefill continued by KDA decode steps; resuming from a copied
-checkpoint is bit exact; padding and bad ids."""
+checkpoint is bit exact; padding and bad ids; the full 4 x 8192 workload on
+its causal prefix."""
 import numpy as np
 import pytest
 import torch
@@ -205,3 +206,37 @@ def test_kda_prefill_padding_bad_ids_and_empty(cuda):
     assert gdn.launch_count(gdn.K_KDA_PREFILL) == n0
     with pytest.raises(gdn.GdnError):
         _run(st, ck, params, ids, lens, starts, ck_ids, 100, qkv, a, b)  # block not a multiple of 64
+
+
+def test_kda_prefill_four_by_8192_causal_prefix(cuda):
+    """The full 4 x 8192-token workload (checkpoints every 256) in the launch
+    shape the benchmark times.  The recurrence is causal, so the outputs of each
+    sequence's first 1024 tokens and its first four checkpoints are those of the
+    oracle run on that prefix alone; every later checkpoint is written and
+    finite."""
+    shape = synth.QWEN
+    st = Setup(shape, seed=149, num_slots=8)
+    params, oparams = _kda_params(st, 150)
+    S, pre, blk = 8192, 1024, 256
+    ids = torch.tensor([5, 1, 6, 2], dtype=torch.int32)
+    ck_ids = torch.arange(128, dtype=torch.int32).reshape(4, 32)
+    ck = _ck_pool(st, 128)
+    qkv, _, b = st.tokens((4 * S,))
+    a = _gates(st, 4 * S)
+    ssm0, conv0 = st.opool.ssm.copy(), st.opool.conv.copy()
+    out, _, _ = _run(st, ck, params, ids, [S] * 4, [0] * 4, ck_ids, blk, qkv, a, b)
+    torch.cuda.synchronize()
+    for n in range(4):
+        t0 = S * n
+        opool = oracle.Pool(ssm0[[int(ids[n])]].copy(), conv0[[int(ids[n])]].copy())
+        ock = _ock_pool(shape, 4)
+        o_ref, err = oracle.kda_prefill(st.od, opool, ock, oparams, [0], [0, pre], [0],
+                                        np.arange(4, dtype=np.int32).reshape(1, 4), blk,
+                                        to_np(qkv[t0:t0 + pre]), to_np(a[t0:t0 + pre]), to_np(b[t0:t0 + pre]))
+        assert err == 0
+        assert_out_close(out[t0:t0 + pre], o_ref, shape.dv, PREFILL_TOL, row_floor_rms=True)
+        cks = ck_ids[n].tolist()
+        assert max_rel_l2(to_np(ck.ssm[cks[:4]]), ock.ssm, shape.dv * shape.dk) <= PREFILL_TOL
+        assert conv_bits_equal(ck.conv[cks[:4]], ock.conv)
+        later = ck.ssm[cks[4:]]
+        assert torch.all(torch.isfinite(later)) and not torch.any(torch.all(later.flatten(1) == -5.0, dim=1))
