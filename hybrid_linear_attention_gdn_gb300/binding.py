@@ -80,6 +80,7 @@ EXPORTS = {
     "gdn_state_pack": ([_PD, CPool, _P, _I32, _P, ctypes.c_size_t, _P, _P], _I32),
     "gdn_state_unpack": ([_PD, _P, ctypes.c_size_t, CPool, _P, _I32, _P, _P], _I32),
     "gdn_gated_rmsnorm": ([_PD, _P, _P, _P, ctypes.c_float, _I64, _P, _P], _I32),
+    "gdn_selftest_wait_timeout": ([_P, _P], _I32),
     "gdn_status_string": ([_I32], ctypes.c_char_p),
     "gdn_launch_count": ([_I32], ctypes.c_uint64),
     "gdn_launch_count_reset": ([], None),
@@ -300,6 +301,13 @@ def kda_prefill(dims: Dims, pool: StatePool, ckpt: StatePool, params: LayerParam
                            max_ckpt, int(ckpt_block), _ptr(qkv), _ptr(a), _ptr(b), _ptr(out), _ptr(dev_err),
                            _stream(stream))
     _check("gdn_kda_prefill", st)
+
+
+def selftest_wait_timeout(dev_err, stream=None):
+    """Run the device-side failure-path self-test: a bounded wait that nothing
+    satisfies expires after the library's wait limit and sets DEV_ERR_TIMEOUT
+    in dev_err (an int32 device tensor)."""
+    _check("gdn_selftest_wait_timeout", load().gdn_selftest_wait_timeout(_ptr(dev_err), _stream(stream)))
 
 
 NOALLOC_SCRATCH_BYTES = 64 << 20

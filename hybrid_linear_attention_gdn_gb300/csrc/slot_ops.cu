@@ -296,3 +296,31 @@ extern "C" gdn_status gdn_state_unpack(const gdn_dims* dims, const void* staging
   return gdn::launch_state_xfer(false, dims, pool, ids, n, staging, staging_bytes, dev_err,
                                 stream);
 }
+
+// ---------------------------------------------------------------------------
+// Self-test of the bounded waits that every mbarrier-fed kernel here relies on:
+// one CTA waits on a barrier phase that nothing completes; the wait gives up
+// after the library's limit (kWaitLimitNs), the kernel records
+// GDN_DEV_ERR_TIMEOUT and returns, and the context stays usable.
+// ---------------------------------------------------------------------------
+namespace gdn {
+namespace {
+__global__ void wait_selftest_kernel(uint32_t* err) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !mbar_wait(&bar, 0)) report(err, GDN_DEV_ERR_TIMEOUT);
+}
+}  // namespace
+}  // namespace gdn
+
+extern "C" gdn_status gdn_selftest_wait_timeout(uint32_t* dev_err, void* stream) {
+  using namespace gdn;
+  if (!dev_err) return GDN_ERR_INVALID_ARG;
+  const cudaError_t e = launch_plain(wait_selftest_kernel, dim3(1), dim3(32), 0,
+                                     reinterpret_cast<cudaStream_t>(stream), dim3(1), dev_err);
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}

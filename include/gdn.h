@@ -356,6 +356,17 @@ gdn_status gdn_gated_rmsnorm(const gdn_dims* dims, const void* o, const void* z,
                              const float* weight, float eps, int64_t n_tokens, void* y,
                              void* stream);
 
+/*
+ * Self-test of the device-side failure path: one CTA waits on a barrier phase
+ * that nothing completes; the bounded wait gives up after the library's wait
+ * limit (1 s), GDN_DEV_ERR_TIMEOUT is OR-ed into *dev_err (device, required)
+ * and the kernel returns, leaving the context usable.  Every kernel of this
+ * library that waits on another agent (a copy engine, a tensor-core product,
+ * a producer warp) waits the same way.  GDN_ERR_INVALID_ARG when dev_err is
+ * null.
+ */
+gdn_status gdn_selftest_wait_timeout(uint32_t* dev_err, void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* gdn_status_string(int32_t status);
 

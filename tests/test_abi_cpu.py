@@ -196,6 +196,10 @@ def test_gated_rmsnorm_arguments(lib):
     assert lib.gdn_launch_count(binding.K_GATED_RMSNORM) == n0
 
 
+def test_selftest_needs_an_error_word(lib):
+    assert lib.gdn_selftest_wait_timeout(None, None) == binding.ERR_INVALID_ARG
+
+
 def test_launch_counters(lib):
     lib.gdn_launch_count_reset()
     assert all(lib.gdn_launch_count(k) == 0 for k in range(binding.K_COUNT))
