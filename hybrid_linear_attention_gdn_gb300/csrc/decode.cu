@@ -26,6 +26,7 @@
 #include "gdn_common.cuh"
 #include "decode_tma.cuh"
 #include "prefill_tc.cuh"
+#include "kda_chunk.cuh"
 
 #include <cstdlib>
 #include <cstring>
@@ -1126,7 +1127,16 @@ extern "C" gdn_status gdn_kda_prefill(const gdn_dims* dims, gdn_pool pool, gdn_p
   const bool async = aligned(qkv, 16) && aligned(a, 16) && ((size_t)dims->dk * es) % 16 == 0 &&
                      ((size_t)dims->dv * es) % 16 == 0 && ((size_t)k.C * es) % 16 == 0;
   cudaError_t e = cudaErrorInvalidValue;
-  switch (dims->dk) {
+  // the token recurrence; GDN_KDA_PREFILL_PATH=chunked takes the chunked form
+  // on CUDA cores where it applies (correct, but bound by its shared-memory
+  // loads: 12.2 against 9.2 ms at 4 x 8192; the skeleton for tensor-core
+  // products), read on every call
+  const char* kp = std::getenv("GDN_KDA_PREFILL_PATH");
+  const bool chunked = kda_chunk_supported(*dims) && kp && !std::strcmp(kp, "chunked");
+  if (chunked)
+    e = kda_chunk_launch(*dims, pool, ckpt, *params, slot_ids, cu_seqlens, start_pos, n_seq, total_tokens, ckpt_ids,
+                         max_ckpt, ckpt_block, qkv, a, b, out, dev_err, cs);
+  else switch (dims->dk) {
     case 16: e = dispatch_kda_prefill<16, 1>(k, n_seq, act, cv, async, cs); break;
     case 64: e = dispatch_kda_prefill<64, 1>(k, n_seq, act, cv, async, cs); break;
     case 128: e = dispatch_kda_prefill<128, 2>(k, n_seq, act, cv, async, cs); break;

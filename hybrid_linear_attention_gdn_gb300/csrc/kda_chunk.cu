@@ -1,0 +1,490 @@
+// KDA prefill, chunked form on CUDA cores (dk = 128, dv <= 128), fp32.
+//
+// The per-key-channel gated delta rule (Kimi Delta Attention, Kimi Linear
+// 2025: St <- St diag(alpha_t) + beta_t (v_t - St diag(alpha_t) k_t) k_t^T,
+// o_t = St q_t) over windows of 16 tokens aligned to absolute positions (so
+// every block-aligned checkpoint falls on a window end).  Inside a window,
+// with a_t = prod_{m<=t} alpha_m (per channel, from the window start),
+//   K~_t = k_t (.) a_t,   Q~_t = q_t (.) a_t,   K-_t = k_t (.) prod_{t<m} alpha_m,
+//   A'[t][j] = sum_c k_t k_j prod_{j<m<=t} alpha_m   (t > j),
+//   M[t][j]  = sum_c q_t k_j prod_{j<m<=t} alpha_m   (t >= j),
+//   T = (I + diag(beta) A')^-1 diag(beta),
+// the window is, for every state row (a row of St):
+//   X = v - St K~^T,  Delta = X T^T,  o = St Q~^T + M Delta,
+//   St <- St diag(a_last) + Delta K-.
+// This is the window-level unrolling of the token step (the same algebra as
+// the chunkwise WY form of the Gated DeltaNet paper with the decay kept per
+// channel); every decay factor is a product of alphas over a token range,
+// formed by running products, so none can overflow.  The 16 products of a
+// row are independent, unlike the token recurrence's dependent chain.
+//
+// One CTA per (sequence, V head), 256 threads: thread 2r + h holds columns
+// 64h .. 64h+63 of state row r in registers for the whole sequence.  The raw
+// inputs of window w+1 are staged by cp.async while window w is computed.
+#include "gdn_common.cuh"
+#include "kda_chunk.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kCk = 16;          // window
+constexpr int kCkThreads = 256;
+constexpr int kD = 128;          // dk
+constexpr int kMaxV = 128;       // dv
+constexpr int kCh = 2 * kD + kMaxV;
+constexpr int kCkMaxW = 8;       // conv taps held (right-aligned)
+
+struct KdaChunkArgs {
+  float* ssm;
+  const void* conv;
+  int32_t num_slots;
+  float* ck_ssm;
+  int32_t ck_num_slots;
+  const float* conv_w;
+  const float* A_log;
+  const float* dt_bias;  // [hv][dk]
+  const int32_t* slot_ids;
+  const int32_t* cu_seqlens;
+  const int64_t* start_pos;
+  int64_t total;
+  const int32_t* ckpt_ids;
+  int32_t max_ckpt;
+  int32_t ckpt_block;
+  const void* qkv;
+  const void* a;  // [total][hv][dk]
+  const void* b;
+  void* out;
+  uint32_t* err;
+  int32_t hk, hv, dv, W, C, G;
+};
+
+template <typename Tact>
+struct __align__(16) CkSmem {
+  Tact xr[2][kCk][kCh];     // raw inputs (q | k | v rows), double-buffered
+  Tact ga[2][kCk][kD];      // gate logits, double-buffered
+  float bl[2][kCk];         // beta logits, double-buffered
+  float xh[kCkMaxW - 1][kCh];  // conv history, one column per channel
+  float cw[kCkMaxW][kCh];   // conv weights, right-aligned
+  float sy[kCk][kCh];       // conv + SiLU; q and k normalised in place
+  float al[kCk][kD];        // log alpha (0 past the window's end)
+  float lb[kCk][kD + 1];    // cumulative log alpha from the window start (rows padded: bank spread)
+  float kp[kCk][kD + 1];    // k^, rows padded
+  float qp[kCk][kD + 1];    // q^, rows padded
+  float kt[kCk][kD];        // K~
+  float qt[kCk][kD];        // Q~
+  float kb[kCk][kD];        // K-
+  float dec[kD];            // a_last: the window's decay of the state
+  float A[kCk][kCk];        // A' (t > j)
+  float M[kCk][kCk];        // M (t >= j)
+  float T[kCk][kCk];        // T (lower triangle with the diagonal, zero above)
+  float beta[kCk];
+  float so[kCk][kMaxV];     // the window's outputs
+};
+
+__device__ __forceinline__ float2 fma2c(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}\n"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+// first global channel of staged channel i (q, k of the QK head, then v rows)
+__device__ __forceinline__ int ck_channel(int i, int hq, int h, int hk, int dv) {
+  if (i < kD) return hq * kD + i;
+  if (i < 2 * kD) return hk * kD + hq * kD + (i - kD);
+  return 2 * hk * kD + h * dv + (i - 2 * kD);
+}
+
+// raw inputs of tokens [tok, tok + nt) into the staging buffers (ASYNC:
+// 16-byte cp.async pieces, every segment a multiple of 16 bytes)
+template <typename Tact, bool ASYNC>
+__device__ __forceinline__ void ck_stage(const KdaChunkArgs& a, Tact (*xr)[kCh], Tact (*gs)[kD], int64_t tok, int nt,
+                                         int hq, int h) {
+  const Tact* qkv = reinterpret_cast<const Tact*>(a.qkv);
+  const Tact* ga = reinterpret_cast<const Tact*>(a.a);
+  const int nch = 2 * kD + a.dv;
+  if constexpr (ASYNC) {
+    constexpr int E = 16 / sizeof(Tact);
+    const int per_row = nch / E;
+    for (int p = threadIdx.x; p < nt * per_row; p += kCkThreads) {
+      const int t = p / per_row, e = (p % per_row) * E;
+      cp_async16(&xr[t][e], qkv + (size_t)(tok + t) * a.C + ck_channel(e, hq, h, a.hk, a.dv));
+    }
+    for (int p = threadIdx.x; p < nt * (kD / E); p += kCkThreads) {
+      const int t = p / (kD / E), e = (p % (kD / E)) * E;
+      cp_async16(&gs[t][e], ga + ((size_t)(tok + t) * a.hv + h) * kD + e);
+    }
+  } else {
+    for (int p = threadIdx.x; p < nt * nch; p += kCkThreads) {
+      const int t = p / nch, e = p % nch;
+      xr[t][e] = qkv[(size_t)(tok + t) * a.C + ck_channel(e, hq, h, a.hk, a.dv)];
+    }
+    for (int p = threadIdx.x; p < nt * kD; p += kCkThreads) {
+      const int t = p / kD, e = p % kD;
+      gs[t][e] = ga[((size_t)(tok + t) * a.hv + h) * kD + e];
+    }
+  }
+}
+
+template <typename Tact, typename Tconv, bool ASYNC>
+__global__ void __launch_bounds__(kCkThreads, 1) kda_chunk_kernel(const KdaChunkArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  CkSmem<Tact>& S = *reinterpret_cast<CkSmem<Tact>*>(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int h = blockIdx.x, n = blockIdx.y, hq = h / a.G;
+  const int dv = a.dv, nch = 2 * kD + dv;
+  const int64_t t0 = a.cu_seqlens[n], t1 = a.cu_seqlens[n + 1], len = t1 - t0, p0 = a.start_pos[n];
+  if (t0 < 0 || len < 0 || t1 > a.total || p0 < 0) {
+    if (h == 0 && tid == 0) report(a.err, GDN_DEV_ERR_SEQLENS);
+    return;
+  }
+  Tact* out = reinterpret_cast<Tact*>(a.out);
+  const int32_t slot = a.slot_ids[n];
+  const int cls = slot_class(slot, a.num_slots);
+  if (cls) {
+    if (cls == 2 && h == 0 && tid == 0) report(a.err, GDN_DEV_ERR_SLOT_OOB);
+    for (int64_t e = tid; e < len * dv; e += kCkThreads)
+      out[((t0 + e / dv) * a.hv + h) * dv + e % dv] = from_f32<Tact>(0.f);
+    return;
+  }
+  if (len == 0) return;
+
+  // windows aligned to absolute multiples of 16: the first ends at the next one
+  const int first = len < kCk - (int)(p0 % kCk) ? (int)len : kCk - (int)(p0 % kCk);
+  const Tact* gb = reinterpret_cast<const Tact*>(a.b);
+  ck_stage<Tact, ASYNC>(a, S.xr[0], S.ga[0], t0, first, hq, h);
+  if constexpr (ASYNC) cp_async_commit();
+  if (tid < first) S.bl[0][tid] = to_f32(gb[(size_t)(t0 + tid) * a.hv + h]);
+
+  // this thread's state row half: row r, columns 64 hf .. +63
+  const int r = tid >> 1, hf = tid & 1;
+  const bool rv = r < dv;
+  float* St = a.ssm + (((size_t)slot * a.hv + h) * dv + r) * kD + 64 * hf;
+  float s[64];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float4 v = rv ? *reinterpret_cast<const float4*>(St + 4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    s[4 * i] = v.x;
+    s[4 * i + 1] = v.y;
+    s[4 * i + 2] = v.z;
+    s[4 * i + 3] = v.w;
+  }
+  // conv weights and history, right-aligned in kCkMaxW taps
+  const Tconv* hist = reinterpret_cast<const Tconv*>(a.conv) + (size_t)slot * (a.W - 1) * a.C;
+  const int lead = kCkMaxW - a.W;
+  for (int i = tid; i < nch; i += kCkThreads) {
+    const int ch = ck_channel(i, hq, h, a.hk, dv);
+#pragma unroll
+    for (int j = 0; j < kCkMaxW; ++j) S.cw[j][i] = j >= lead ? a.conv_w[(size_t)ch * a.W + (j - lead)] : 0.f;
+#pragma unroll
+    for (int j = 0; j < kCkMaxW - 1; ++j)
+      S.xh[j][i] = j >= lead ? to_f32(hist[(size_t)(j - lead) * a.C + ch]) : 0.f;
+  }
+  const float eA = expf(a.A_log[h]);
+  const float dtb = a.dt_bias[(size_t)h * kD + (tid & (kD - 1))];  // alpha channel of this thread
+  const int64_t blk0 = p0 / a.ckpt_block;
+  int64_t next_bd = (blk0 + 1) * a.ckpt_block;
+  int64_t ck_idx = 0;
+  if constexpr (ASYNC) cp_async_wait_all();
+  __syncthreads();
+
+  int cur = 0;
+  for (int64_t w0 = 0; w0 < len; cur ^= 1) {
+    const int nt = w0 == 0 ? first : (len - w0 < kCk ? (int)(len - w0) : kCk);
+    const int64_t wn = w0 + nt;
+    const int ntn = wn >= len ? 0 : (len - wn < kCk ? (int)(len - wn) : kCk);
+    const int nxt = cur ^ 1;
+    // 0. the next window's inputs
+    float bnext = 0.f;
+    if (ntn > 0) {
+      ck_stage<Tact, ASYNC>(a, S.xr[nxt], S.ga[nxt], t0 + wn, ntn, hq, h);
+      if constexpr (ASYNC) cp_async_commit();
+      if (tid < ntn) bnext = to_f32(gb[(size_t)(t0 + wn + tid) * a.hv + h]);
+    }
+    // 1. conv1d + SiLU (tokens past the window's end: zero)
+#pragma unroll
+    for (int ci = 0; ci < 2; ++ci) {
+      const int i = tid + ci * kCkThreads;
+      if (i < nch) {
+        float w[kCkMaxW], win[kCkMaxW - 1];
+#pragma unroll
+        for (int j = 0; j < kCkMaxW; ++j) w[j] = S.cw[j][i];
+#pragma unroll
+        for (int j = 0; j < kCkMaxW - 1; ++j) win[j] = S.xh[j][i];
+#pragma unroll
+        for (int t = 0; t < kCk; ++t) {
+          if (t < nt) {
+            const float xv = to_f32(S.xr[cur][t][i]);
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < kCkMaxW - 1; ++j) acc = fmaf(w[j], win[j], acc);
+            acc = fmaf(w[kCkMaxW - 1], xv, acc);
+            S.sy[t][i] = __fdividef(acc, 1.f + exp_ftz(-acc));
+#pragma unroll
+            for (int j = 0; j < kCkMaxW - 2; ++j) win[j] = win[j + 1];
+            win[kCkMaxW - 2] = xv;
+          } else {
+            S.sy[t][i] = 0.f;
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < kCkMaxW - 1; ++j) S.xh[j][i] = win[j];
+      }
+    }
+    // log alpha = -exp(A_log) softplus(a + dt_bias) (0 past the window's end)
+    for (int e = tid; e < kCk * kD; e += kCkThreads) {
+      const int t = e / kD, c = e % kD;
+      S.al[t][c] = t < nt ? -eA * softplus_f(to_f32(S.ga[cur][t][c]) + dtb) : 0.f;
+    }
+    __syncthreads();
+    // 2. per token (a warp per token): q, k normalised in place, beta
+    for (int t = warp; t < kCk; t += kCkThreads / 32) {
+      float* yq = S.sy[t];
+      float* yk = yq + kD;
+      float pq = 0.f, pk = 0.f;
+      for (int i = lane; i < kD; i += 32) {
+        pq = fmaf(yq[i], yq[i], pq);
+        pk = fmaf(yk[i], yk[i], pk);
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        pq += __shfl_xor_sync(0xffffffffu, pq, o);
+        pk += __shfl_xor_sync(0xffffffffu, pk, o);
+      }
+      const float rq = rsqrtf(pq + kNormEps) * rsqrtf((float)kD), rk = rsqrtf(pk + kNormEps);
+      for (int i = lane; i < kD; i += 32) {
+        yq[i] *= rq;
+        yk[i] *= rk;
+      }
+      if (lane == 0) S.beta[t] = t < nt ? sigmoid_f(S.bl[cur][t]) : 0.f;
+    }
+    __syncthreads();
+    // 3a. per channel (threads 0-127): the cumulative log decay from the
+    //     window start, K~, Q~ (decay to token t), K- (decay from token t to
+    //     the window's end), the window's decay, and padded copies of k^, q^
+    if (tid < kD) {
+      const int c = tid;
+      float lbv[kCk];
+      float acc = 0.f;
+#pragma unroll
+      for (int t = 0; t < kCk; ++t) {
+        acc += S.al[t][c];
+        lbv[t] = acc;
+      }
+#pragma unroll
+      for (int t = 0; t < kCk; ++t) {
+        const float kv = S.sy[t][kD + c], qv = S.sy[t][c];
+        const float ef = __expf(lbv[t]), eb = __expf(acc - lbv[t]);
+        S.kt[t][c] = kv * ef;
+        S.qt[t][c] = qv * ef;
+        S.kb[t][c] = kv * eb;
+        S.lb[t][c] = lbv[t];
+        S.kp[t][c] = kv;
+        S.qp[t][c] = qv;
+      }
+      S.dec[c] = __expf(acc);
+    }
+    __syncthreads();
+    // 3b. A' and M, a thread per (t, j): the decay between tokens j and t of
+    //     every channel is exp(lb[t] - lb[j]) (at most 1)
+    {
+      const int t = tid >> 4, j = tid & 15;
+      if (t >= j) {
+        float vk = 0.f, vq = 0.f;
+#pragma unroll 8
+        for (int c = 0; c < kD; ++c) {
+          const float f = S.kp[j][c] * __expf(S.lb[t][c] - S.lb[j][c]);
+          vk = fmaf(S.kp[t][c], f, vk);
+          vq = fmaf(S.qp[t][c], f, vq);
+        }
+        S.A[t][j] = vk;  // used below the diagonal only
+        S.M[t][j] = vq;
+      }
+    }
+    __syncthreads();
+    // 4. T = (I + diag(beta) A')^-1 diag(beta): lane j of warp 0 solves column j
+    if (warp == 0 && lane < kCk) {
+      const int j = lane;
+      float x[kCk];
+#pragma unroll
+      for (int t = 0; t < kCk; ++t) {
+        float acc = 0.f;
+#pragma unroll
+        for (int m = 0; m < t; ++m) acc = fmaf(S.A[t][m], x[m], acc);
+        x[t] = t < j ? 0.f : (t == j ? 1.f : -S.beta[t] * acc);
+      }
+      const float bj = S.beta[j];
+#pragma unroll
+      for (int t = 0; t < kCk; ++t) S.T[t][j] = x[t] * bj;
+    }
+    __syncthreads();
+    // 5. every state row: X = v - St K~^T, O1 = St Q~^T (the two halves of a
+    //    row summed by one shuffle), Delta = X T^T, o = O1 + M Delta,
+    //    St <- St diag(a_last) + Delta K-
+    {
+      // independent accumulators per token (the column loop outermost)
+      float2 ak[kCk], aq[kCk];
+#pragma unroll
+      for (int t = 0; t < kCk; ++t) ak[t] = aq[t] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float2 s0 = make_float2(s[4 * i], s[4 * i + 1]), s1 = make_float2(s[4 * i + 2], s[4 * i + 3]);
+#pragma unroll
+        for (int t = 0; t < kCk; ++t) {
+          const float4 kv = reinterpret_cast<const float4*>(&S.kt[t][64 * hf])[i];
+          const float4 qv = reinterpret_cast<const float4*>(&S.qt[t][64 * hf])[i];
+          ak[t] = fma2c(s1, make_float2(kv.z, kv.w), fma2c(s0, make_float2(kv.x, kv.y), ak[t]));
+          aq[t] = fma2c(s1, make_float2(qv.z, qv.w), fma2c(s0, make_float2(qv.x, qv.y), aq[t]));
+        }
+      }
+      float xk[kCk], xq[kCk];
+#pragma unroll
+      for (int t = 0; t < kCk; ++t) {
+        xk[t] = ak[t].x + ak[t].y;
+        xq[t] = aq[t].x + aq[t].y;
+      }
+#pragma unroll
+      for (int t = 0; t < kCk; ++t) {
+        xk[t] += __shfl_xor_sync(0xffffffffu, xk[t], 1);
+        xq[t] += __shfl_xor_sync(0xffffffffu, xq[t], 1);
+      }
+      // X in xk, then Delta in xk (row r's value of each token)
+#pragma unroll
+      for (int t = 0; t < kCk; ++t) xk[t] = (rv ? S.sy[t][2 * kD + r] : 0.f) - xk[t];
+      float dl[kCk];
+#pragma unroll
+      for (int t = 0; t < kCk; ++t) {
+        float acc = 0.f;
+#pragma unroll
+        for (int j = 0; j <= t; ++j) acc = fmaf(S.T[t][j], xk[j], acc);
+        dl[t] = acc;
+      }
+      if (hf == 0 && rv) {
+#pragma unroll
+        for (int t = 0; t < kCk; ++t) {
+          float o = xq[t];
+#pragma unroll
+          for (int j = 0; j <= t; ++j) o = fmaf(S.M[t][j], dl[j], o);
+          if (t < nt) S.so[t][r] = o;
+        }
+      }
+      // St diag(a_last), then the tokens outermost: every state element is
+      // its own accumulator
+      const float4* d4 = reinterpret_cast<const float4*>(&S.dec[64 * hf]);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float4 dv4 = d4[i];
+        s[4 * i] *= dv4.x;
+        s[4 * i + 1] *= dv4.y;
+        s[4 * i + 2] *= dv4.z;
+        s[4 * i + 3] *= dv4.w;
+      }
+#pragma unroll
+      for (int t = 0; t < kCk; ++t) {
+        const float2 d2 = make_float2(dl[t], dl[t]);
+        const float4* k4 = reinterpret_cast<const float4*>(&S.kb[t][64 * hf]);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float4 kv = k4[i];
+          const float2 s0 = fma2c(d2, make_float2(kv.x, kv.y), make_float2(s[4 * i], s[4 * i + 1]));
+          const float2 s1 = fma2c(d2, make_float2(kv.z, kv.w), make_float2(s[4 * i + 2], s[4 * i + 3]));
+          s[4 * i] = s0.x;
+          s[4 * i + 1] = s0.y;
+          s[4 * i + 2] = s1.x;
+          s[4 * i + 3] = s1.y;
+        }
+      }
+    }
+    // a block boundary at the window's end: the rows to its checkpoint slot
+    if (p0 + wn == next_bd) {
+      const int64_t idx = ck_idx++;
+      next_bd += a.ckpt_block;
+      if (idx < a.max_ckpt) {
+        const int32_t cid = a.ckpt_ids[(size_t)n * a.max_ckpt + idx];
+        const int cc = slot_class(cid, a.ck_num_slots);
+        if (cc == 0 && rv) {
+          float4* dst = reinterpret_cast<float4*>(a.ck_ssm + (((size_t)cid * a.hv + h) * dv + r) * kD + 64 * hf);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) st_stream(dst + i, make_float4(s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3]));
+        } else if (cc == 2 && tid == 0) {
+          report(a.err, GDN_DEV_ERR_SLOT_OOB);
+        }
+      }
+    }
+    __syncthreads();
+    // 6. the window's outputs; the next window's beta logits and inputs land
+    for (int e = tid; e < nt * dv; e += kCkThreads) {
+      const int t = e / dv, i = e % dv;
+      out[((size_t)(t0 + w0 + t) * a.hv + h) * dv + i] = from_f32<Tact>(S.so[t][i]);
+    }
+    if (tid < ntn) S.bl[nxt][tid] = bnext;
+    if constexpr (ASYNC) cp_async_wait_all();
+    __syncthreads();
+    w0 = wn;
+  }
+  if (rv) {
+    float4* dst = reinterpret_cast<float4*>(St);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) st_stream(dst + i, make_float4(s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3]));
+  }
+}
+
+template <typename Tact, typename Tconv>
+cudaError_t launch_ck_t(const KdaChunkArgs& a, int32_t n_seq, bool async, cudaStream_t s) {
+  const size_t smem = sizeof(CkSmem<Tact>);
+  auto k = async ? kda_chunk_kernel<Tact, Tconv, true> : kda_chunk_kernel<Tact, Tconv, false>;
+  const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k, dim3((unsigned)a.hv, (unsigned)n_seq), dim3(kCkThreads), smem, s, dim3(1), a);
+}
+
+}  // namespace
+
+bool kda_chunk_supported(const gdn_dims& d) { return d.dk == kD && d.dv <= kMaxV && d.dv % 4 == 0; }
+
+cudaError_t kda_chunk_launch(const gdn_dims& d, const gdn_pool& pool, const gdn_pool& ckpt, const gdn_params& p,
+                             const int32_t* slot_ids, const int32_t* cu_seqlens, const int64_t* start_pos,
+                             int32_t n_seq, int64_t total, const int32_t* ckpt_ids, int32_t max_ckpt,
+                             int32_t ckpt_block, const void* qkv, const void* av, const void* bv, void* out,
+                             uint32_t* dev_err, cudaStream_t s) {
+  KdaChunkArgs k = {};
+  k.ssm = pool.ssm;
+  k.conv = pool.conv;
+  k.num_slots = pool.num_slots;
+  k.ck_ssm = ckpt.ssm;
+  k.ck_num_slots = max_ckpt > 0 ? ckpt.num_slots : 0;
+  k.conv_w = p.conv_w;
+  k.A_log = p.A_log;
+  k.dt_bias = p.dt_bias;
+  k.slot_ids = slot_ids;
+  k.cu_seqlens = cu_seqlens;
+  k.start_pos = start_pos;
+  k.total = total;
+  k.ckpt_ids = ckpt_ids;
+  k.max_ckpt = max_ckpt;
+  k.ckpt_block = ckpt_block;
+  k.qkv = qkv;
+  k.a = av;
+  k.b = bv;
+  k.out = out;
+  k.err = dev_err;
+  k.hk = d.hk;
+  k.hv = d.hv;
+  k.dv = d.dv;
+  k.W = d.conv_width;
+  k.C = (int32_t)channels(d);
+  k.G = d.hv / d.hk;
+  const size_t es = dtype_size(d.act_dtype);
+  const bool async = aligned(qkv, 16) && aligned(av, 16) && ((size_t)d.dv * es) % 16 == 0 &&
+                     ((size_t)k.C * es) % 16 == 0;
+  if (d.act_dtype == GDN_F32 && d.conv_dtype == GDN_F32) return launch_ck_t<float, float>(k, n_seq, async, s);
+  if (d.act_dtype == GDN_BF16 && d.conv_dtype == GDN_BF16)
+    return launch_ck_t<__nv_bfloat16, __nv_bfloat16>(k, n_seq, async, s);
+  return launch_ck_t<__nv_bfloat16, float>(k, n_seq, async, s);
+}
+
+}  // namespace gdn
