@@ -1127,12 +1127,11 @@ extern "C" gdn_status gdn_kda_prefill(const gdn_dims* dims, gdn_pool pool, gdn_p
   const bool async = aligned(qkv, 16) && aligned(a, 16) && ((size_t)dims->dk * es) % 16 == 0 &&
                      ((size_t)dims->dv * es) % 16 == 0 && ((size_t)k.C * es) % 16 == 0;
   cudaError_t e = cudaErrorInvalidValue;
-  // the token recurrence; GDN_KDA_PREFILL_PATH=chunked takes the chunked form
-  // on CUDA cores where it applies (correct, but bound by its shared-memory
-  // loads: 12.2 against 9.2 ms at 4 x 8192; the skeleton for tensor-core
-  // products), read on every call
+  // the chunked form where it applies (dk 128, dv <= 128: 8.3 against 9.2 ms
+  // for the token recurrence at 4 x 8192); GDN_KDA_PREFILL_PATH=recurrent
+  // forces the recurrence, read on every call
   const char* kp = std::getenv("GDN_KDA_PREFILL_PATH");
-  const bool chunked = kda_chunk_supported(*dims) && kp && !std::strcmp(kp, "chunked");
+  const bool chunked = kda_chunk_supported(*dims) && !(kp && !std::strcmp(kp, "recurrent"));
   if (chunked)
     e = kda_chunk_launch(*dims, pool, ckpt, *params, slot_ids, cu_seqlens, start_pos, n_seq, total_tokens, ckpt_ids,
                          max_ckpt, ckpt_block, qkv, a, b, out, dev_err, cs);

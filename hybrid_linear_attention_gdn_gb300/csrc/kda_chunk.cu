@@ -33,6 +33,12 @@ constexpr int kD = 128;          // dk
 constexpr int kMaxV = 128;       // dv
 constexpr int kCh = 2 * kD + kMaxV;
 constexpr int kCkMaxW = 8;       // conv taps held (right-aligned)
+// padded row strides (floats) so that the tensor-core fragment loads hit 32
+// distinct banks: K~ and Q~ rows are read at (row g, column tq), K- at (row
+// tq, column g), T and M at (row g, column tq)
+constexpr int kKQS = kD + 4;     // 132
+constexpr int kKBS = kD + 8;     // 136
+constexpr int kTS = kCk + 4;     // 20
 
 struct KdaChunkArgs {
   float* ssm;
@@ -70,13 +76,13 @@ struct __align__(16) CkSmem {
   float lb[kCk][kD + 1];    // cumulative log alpha from the window start (rows padded: bank spread)
   float kp[kCk][kD + 1];    // k^, rows padded
   float qp[kCk][kD + 1];    // q^, rows padded
-  float kt[kCk][kD];        // K~
-  float qt[kCk][kD];        // Q~
-  float kb[kCk][kD];        // K-
+  float kt[kCk][kKQS];      // K~
+  float qt[kCk][kKQS];      // Q~
+  float kb[kCk][kKBS];      // K-
   float dec[kD];            // a_last: the window's decay of the state
   float A[kCk][kCk];        // A' (t > j)
-  float M[kCk][kCk];        // M (t >= j)
-  float T[kCk][kCk];        // T (lower triangle with the diagonal, zero above)
+  float M[kCk][kTS];        // M (t >= j)
+  float T[kCk][kTS];        // T (lower triangle with the diagonal, zero above)
   float beta[kCk];
   float so[kCk][kMaxV];     // the window's outputs
 };
@@ -88,6 +94,54 @@ __device__ __forceinline__ float2 fma2c(float2 a, float2 b, float2 c) {
       : "=f"(d.x), "=f"(d.y)
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
   return d;
+}
+
+// Warp-level tf32 tensor-core product (m16n8k8, fp32 accumulate).  Lane =
+// 4 g + tq; A holds (g, tq), (g + 8, tq), (g, tq + 4), (g + 8, tq + 4); B holds
+// (tq, g), (tq + 4, g); C/D hold (g, 2tq), (g, 2tq + 1), (g + 8, 2tq), (g + 8, 2tq + 1).
+__device__ __forceinline__ uint32_t tf32_rna(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;\n" : "=r"(r) : "f"(x));
+  return r;
+}
+// x = hi + lo, both tf32: the split that lets three tf32 products carry an
+// fp32 product (hi*hi + hi*lo + lo*hi; lo*lo is below fp32's rounding)
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+  hi = tf32_rna(x);
+  lo = tf32_rna(x - __uint_as_float(hi));
+}
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// d += a b in split tf32: a = (ah, al), b = (b0, b1) split inside
+__device__ __forceinline__ void mma3(float (&d)[4], const uint32_t (&ah)[4], const uint32_t (&al)[4], float b0,
+                                     float b1) {
+  uint32_t bh0, bl0, bh1, bl1;
+  split_tf32(b0, bh0, bl0);
+  split_tf32(b1, bh1, bl1);
+  mma_tf32(d, al, bh0, bh1);
+  mma_tf32(d, ah, bl0, bl1);
+  mma_tf32(d, ah, bh0, bh1);
+}
+// The A fragment of an 8-column group from the same group in the C layout
+// (c[0..3] = (g, 2tq), (g, 2tq + 1), (g + 8, 2tq), (g + 8, 2tq + 1)): quad
+// shuffles, then the split
+__device__ __forceinline__ void c_to_a(const float (&c)[4], uint32_t (&ah)[4], uint32_t (&al)[4]) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, tq = lane & 3;
+  const int lo = (g << 2) | (tq >> 1), hi = lo + 2;
+  const bool odd = tq & 1;
+  const float x0 = __shfl_sync(0xffffffffu, c[0], lo), x1 = __shfl_sync(0xffffffffu, c[1], lo);
+  const float y0 = __shfl_sync(0xffffffffu, c[2], lo), y1 = __shfl_sync(0xffffffffu, c[3], lo);
+  const float u0 = __shfl_sync(0xffffffffu, c[0], hi), u1 = __shfl_sync(0xffffffffu, c[1], hi);
+  const float z0 = __shfl_sync(0xffffffffu, c[2], hi), z1 = __shfl_sync(0xffffffffu, c[3], hi);
+  split_tf32(odd ? x1 : x0, ah[0], al[0]);  // (g, tq)
+  split_tf32(odd ? y1 : y0, ah[1], al[1]);  // (g + 8, tq)
+  split_tf32(odd ? u1 : u0, ah[2], al[2]);  // (g, tq + 4)
+  split_tf32(odd ? z1 : z0, ah[3], al[3]);  // (g + 8, tq + 4)
 }
 
 // first global channel of staged channel i (q, k of the QK head, then v rows)
@@ -160,18 +214,23 @@ __global__ void __launch_bounds__(kCkThreads, 1) kda_chunk_kernel(const KdaChunk
   if constexpr (ASYNC) cp_async_commit();
   if (tid < first) S.bl[0][tid] = to_f32(gb[(size_t)(t0 + tid) * a.hv + h]);
 
-  // this thread's state row half: row r, columns 64 hf .. +63
-  const int r = tid >> 1, hf = tid & 1;
-  const bool rv = r < dv;
-  float* St = a.ssm + (((size_t)slot * a.hv + h) * dv + r) * kD + 64 * hf;
-  float s[64];
+  // this thread's state: rows rA = 16 warp + g and rB = rA + 8, in the
+  // tensor core's C layout: sc[j] = (rA, 8j + 2tq), (rA, 8j + 2tq + 1),
+  // (rB, 8j + 2tq), (rB, 8j + 2tq + 1)
+  const int g = lane >> 2, tq = lane & 3;
+  const int rA = 16 * warp + g, rB = rA + 8;
+  const bool vA = rA < dv, vB = rB < dv;
+  float* StA = a.ssm + (((size_t)slot * a.hv + h) * dv + rA) * kD;
+  float* StB = StA + 8 * kD;
+  float sc[16][4];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const float4 v = rv ? *reinterpret_cast<const float4*>(St + 4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
-    s[4 * i] = v.x;
-    s[4 * i + 1] = v.y;
-    s[4 * i + 2] = v.z;
-    s[4 * i + 3] = v.w;
+  for (int j = 0; j < 16; ++j) {
+    const float2 x = vA ? *reinterpret_cast<const float2*>(StA + 8 * j + 2 * tq) : make_float2(0.f, 0.f);
+    const float2 y = vB ? *reinterpret_cast<const float2*>(StB + 8 * j + 2 * tq) : make_float2(0.f, 0.f);
+    sc[j][0] = x.x;
+    sc[j][1] = x.y;
+    sc[j][2] = y.x;
+    sc[j][3] = y.y;
   }
   // conv weights and history, right-aligned in kCkMaxW taps
   const Tconv* hist = reinterpret_cast<const Tconv*>(a.conv) + (size_t)slot * (a.W - 1) * a.C;
@@ -303,6 +362,9 @@ __global__ void __launch_bounds__(kCkThreads, 1) kda_chunk_kernel(const KdaChunk
         }
         S.A[t][j] = vk;  // used below the diagonal only
         S.M[t][j] = vq;
+      } else {
+        S.A[t][j] = 0.f;  // M enters a full 16 x 16 product: zero above the diagonal
+        S.M[t][j] = 0.f;
       }
     }
     __syncthreads();
@@ -322,80 +384,82 @@ __global__ void __launch_bounds__(kCkThreads, 1) kda_chunk_kernel(const KdaChunk
       for (int t = 0; t < kCk; ++t) S.T[t][j] = x[t] * bj;
     }
     __syncthreads();
-    // 5. every state row: X = v - St K~^T, O1 = St Q~^T (the two halves of a
-    //    row summed by one shuffle), Delta = X T^T, o = O1 + M Delta,
-    //    St <- St diag(a_last) + Delta K-
+    // 5. the state rows on the tensor cores (split tf32, fp32 accuracy), a
+    //    warp per 16 rows: Xk = St K~^T and Xq = St Q~^T (16 rows x 16 tokens),
+    //    Delta = (v - Xk) T^T, o = Xq + Delta M^T, St <- St diag(a_last) + Delta K-
     {
-      // independent accumulators per token (the column loop outermost)
-      float2 ak[kCk], aq[kCk];
+      float xk[2][4], xq[2][4];
 #pragma unroll
-      for (int t = 0; t < kCk; ++t) ak[t] = aq[t] = make_float2(0.f, 0.f);
+      for (int nt2 = 0; nt2 < 2; ++nt2)
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float2 s0 = make_float2(s[4 * i], s[4 * i + 1]), s1 = make_float2(s[4 * i + 2], s[4 * i + 3]);
+        for (int i = 0; i < 4; ++i) xk[nt2][i] = xq[nt2][i] = 0.f;
 #pragma unroll
-        for (int t = 0; t < kCk; ++t) {
-          const float4 kv = reinterpret_cast<const float4*>(&S.kt[t][64 * hf])[i];
-          const float4 qv = reinterpret_cast<const float4*>(&S.qt[t][64 * hf])[i];
-          ak[t] = fma2c(s1, make_float2(kv.z, kv.w), fma2c(s0, make_float2(kv.x, kv.y), ak[t]));
-          aq[t] = fma2c(s1, make_float2(qv.z, qv.w), fma2c(s0, make_float2(qv.x, qv.y), aq[t]));
+      for (int kk = 0; kk < 16; ++kk) {
+        uint32_t ah[4], al[4];
+        c_to_a(sc[kk], ah, al);
+#pragma unroll
+        for (int nt2 = 0; nt2 < 2; ++nt2) {
+          const float* kr = &S.kt[8 * nt2 + g][8 * kk + tq];
+          const float* qr = &S.qt[8 * nt2 + g][8 * kk + tq];
+          mma3(xk[nt2], ah, al, kr[0], kr[4]);
+          mma3(xq[nt2], ah, al, qr[0], qr[4]);
         }
       }
-      float xk[kCk], xq[kCk];
+      // X = v - Xk (rows past dv: 0), in place
 #pragma unroll
-      for (int t = 0; t < kCk; ++t) {
-        xk[t] = ak[t].x + ak[t].y;
-        xq[t] = aq[t].x + aq[t].y;
+      for (int nt2 = 0; nt2 < 2; ++nt2) {
+        const int tok = 8 * nt2 + 2 * tq;
+        xk[nt2][0] = (vA ? S.sy[tok][2 * kD + rA] : 0.f) - xk[nt2][0];
+        xk[nt2][1] = (vA ? S.sy[tok + 1][2 * kD + rA] : 0.f) - xk[nt2][1];
+        xk[nt2][2] = (vB ? S.sy[tok][2 * kD + rB] : 0.f) - xk[nt2][2];
+        xk[nt2][3] = (vB ? S.sy[tok + 1][2 * kD + rB] : 0.f) - xk[nt2][3];
       }
+      // Delta = X T^T (K = the 16 tokens j, B[j][t'] = T[t'][j])
+      float dl[2][4];
 #pragma unroll
-      for (int t = 0; t < kCk; ++t) {
-        xk[t] += __shfl_xor_sync(0xffffffffu, xk[t], 1);
-        xq[t] += __shfl_xor_sync(0xffffffffu, xq[t], 1);
-      }
-      // X in xk, then Delta in xk (row r's value of each token)
+      for (int nt2 = 0; nt2 < 2; ++nt2)
 #pragma unroll
-      for (int t = 0; t < kCk; ++t) xk[t] = (rv ? S.sy[t][2 * kD + r] : 0.f) - xk[t];
-      float dl[kCk];
+        for (int i = 0; i < 4; ++i) dl[nt2][i] = 0.f;
 #pragma unroll
-      for (int t = 0; t < kCk; ++t) {
-        float acc = 0.f;
+      for (int kj = 0; kj < 2; ++kj) {
+        uint32_t ah[4], al[4];
+        c_to_a(xk[kj], ah, al);
 #pragma unroll
-        for (int j = 0; j <= t; ++j) acc = fmaf(S.T[t][j], xk[j], acc);
-        dl[t] = acc;
-      }
-      if (hf == 0 && rv) {
-#pragma unroll
-        for (int t = 0; t < kCk; ++t) {
-          float o = xq[t];
-#pragma unroll
-          for (int j = 0; j <= t; ++j) o = fmaf(S.M[t][j], dl[j], o);
-          if (t < nt) S.so[t][r] = o;
+        for (int nt2 = 0; nt2 < 2; ++nt2) {
+          const float* tr = &S.T[8 * nt2 + g][8 * kj + tq];
+          mma3(dl[nt2], ah, al, tr[0], tr[4]);
         }
       }
-      // St diag(a_last), then the tokens outermost: every state element is
-      // its own accumulator
-      const float4* d4 = reinterpret_cast<const float4*>(&S.dec[64 * hf]);
+      // o = Xq + Delta M^T; St <- St diag(a_last) + Delta K- (Delta as A)
+      uint32_t dh[2][4], dlo[2][4];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float4 dv4 = d4[i];
-        s[4 * i] *= dv4.x;
-        s[4 * i + 1] *= dv4.y;
-        s[4 * i + 2] *= dv4.z;
-        s[4 * i + 3] *= dv4.w;
+      for (int kj = 0; kj < 2; ++kj) c_to_a(dl[kj], dh[kj], dlo[kj]);
+#pragma unroll
+      for (int kj = 0; kj < 2; ++kj)
+#pragma unroll
+        for (int nt2 = 0; nt2 < 2; ++nt2) {
+          const float* mr = &S.M[8 * nt2 + g][8 * kj + tq];
+          mma3(xq[nt2], dh[kj], dlo[kj], mr[0], mr[4]);
+        }
+#pragma unroll
+      for (int nt2 = 0; nt2 < 2; ++nt2) {
+        const int tok = 8 * nt2 + 2 * tq;
+        if (vA && tok < nt) S.so[tok][rA] = xq[nt2][0];
+        if (vA && tok + 1 < nt) S.so[tok + 1][rA] = xq[nt2][1];
+        if (vB && tok < nt) S.so[tok][rB] = xq[nt2][2];
+        if (vB && tok + 1 < nt) S.so[tok + 1][rB] = xq[nt2][3];
       }
 #pragma unroll
-      for (int t = 0; t < kCk; ++t) {
-        const float2 d2 = make_float2(dl[t], dl[t]);
-        const float4* k4 = reinterpret_cast<const float4*>(&S.kb[t][64 * hf]);
+      for (int j = 0; j < 16; ++j) {
+        const float d0 = S.dec[8 * j + 2 * tq], d1 = S.dec[8 * j + 2 * tq + 1];
+        sc[j][0] *= d0;
+        sc[j][1] *= d1;
+        sc[j][2] *= d0;
+        sc[j][3] *= d1;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float4 kv = k4[i];
-          const float2 s0 = fma2c(d2, make_float2(kv.x, kv.y), make_float2(s[4 * i], s[4 * i + 1]));
-          const float2 s1 = fma2c(d2, make_float2(kv.z, kv.w), make_float2(s[4 * i + 2], s[4 * i + 3]));
-          s[4 * i] = s0.x;
-          s[4 * i + 1] = s0.y;
-          s[4 * i + 2] = s1.x;
-          s[4 * i + 3] = s1.y;
+        for (int kj = 0; kj < 2; ++kj) {
+          const float* br = &S.kb[8 * kj + tq][8 * j + g];
+          mma3(sc[j], dh[kj], dlo[kj], br[0], br[4 * kKBS]);
         }
       }
     }
@@ -406,10 +470,13 @@ __global__ void __launch_bounds__(kCkThreads, 1) kda_chunk_kernel(const KdaChunk
       if (idx < a.max_ckpt) {
         const int32_t cid = a.ckpt_ids[(size_t)n * a.max_ckpt + idx];
         const int cc = slot_class(cid, a.ck_num_slots);
-        if (cc == 0 && rv) {
-          float4* dst = reinterpret_cast<float4*>(a.ck_ssm + (((size_t)cid * a.hv + h) * dv + r) * kD + 64 * hf);
+        if (cc == 0) {
+          float* dA = a.ck_ssm + (((size_t)cid * a.hv + h) * dv + rA) * kD;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) st_stream(dst + i, make_float4(s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3]));
+          for (int j = 0; j < 16; ++j) {
+            if (vA) *reinterpret_cast<float2*>(dA + 8 * j + 2 * tq) = make_float2(sc[j][0], sc[j][1]);
+            if (vB) *reinterpret_cast<float2*>(dA + 8 * kD + 8 * j + 2 * tq) = make_float2(sc[j][2], sc[j][3]);
+          }
         } else if (cc == 2 && tid == 0) {
           report(a.err, GDN_DEV_ERR_SLOT_OOB);
         }
@@ -426,10 +493,10 @@ __global__ void __launch_bounds__(kCkThreads, 1) kda_chunk_kernel(const KdaChunk
     __syncthreads();
     w0 = wn;
   }
-  if (rv) {
-    float4* dst = reinterpret_cast<float4*>(St);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) st_stream(dst + i, make_float4(s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3]));
+  for (int j = 0; j < 16; ++j) {
+    if (vA) *reinterpret_cast<float2*>(StA + 8 * j + 2 * tq) = make_float2(sc[j][0], sc[j][1]);
+    if (vB) *reinterpret_cast<float2*>(StB + 8 * j + 2 * tq) = make_float2(sc[j][2], sc[j][3]);
   }
 }
 

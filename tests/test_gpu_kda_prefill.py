@@ -1,4 +1,4 @@
-"""GPU KDA prefill (the recurrent form, and the opt-in chunked form) against the oracle's token-by-token
+"""GPU KDA prefill (the chunked form, and the token recurrence) against the oracle's token-by-token
 KDA prefill: outputs, final states, checkpoint states and conv histories on
 packed sequences from arbitrary start positions; uniform gates land on the
 GDN prefill; a prefill continued by KDA decode steps; resuming from a copied
@@ -55,22 +55,24 @@ def _n_ck(starts, lens, blk):
 
 
 @pytest.mark.parametrize("shape,lens,starts,blk,path", [
-    (synth.TINY, [1, 37, 130, 300, 0], [0, 64, 100, 256, 5], 64, "recurrent"),
+    (synth.TINY, [1, 37, 130, 300, 0], [0, 64, 100, 256, 5], 64, "chunked"),
     (synth.QWEN, [70, 200, 513], [0, 128, 0], 256, "recurrent"),
-    (synth.QWEN.replace(hk=2, hv=8, dk=64, dv=64), [129, 64, 3], [0, 192, 61], 64, "recurrent"),
+    (synth.QWEN.replace(hk=2, hv=8, dk=64, dv=64), [129, 64, 3], [0, 192, 61], 64, "chunked"),
     (synth.QWEN.replace(act="f32", conv="f32", hk=4, hv=8), [100, 17], [30, 0], 64, "recurrent"),
     (synth.QWEN, [200, 1, 70, 129], [200, 77, 4101, 63], 256, "recurrent"),
     (synth.QWEN, [70, 200, 513], [0, 128, 0], 256, "chunked"),
     (synth.QWEN.replace(act="f32", conv="f32", hk=4, hv=8), [100, 17], [30, 0], 64, "chunked"),
     (synth.QWEN, [200, 1, 70, 129], [200, 77, 4101, 63], 256, "chunked"),
     (synth.QWEN.replace(conv="f32", dv=96), [33, 300], [5, 64], 64, "chunked"),
-], ids=["tiny", "qwen", "dk64_g4", "f32", "qwen_unaligned_continuations", "qwen_chunked", "f32_chunked",
-        "qwen_unaligned_continuations_chunked", "dv96_f32conv_chunked"])
+], ids=["tiny", "qwen_recurrent", "dk64_g4", "f32_recurrent", "qwen_unaligned_continuations_recurrent", "qwen",
+        "f32", "qwen_unaligned_continuations", "dv96_f32conv"])
 def test_kda_prefill_vs_oracle(cuda, monkeypatch, shape, lens, starts, blk, path):
-    """path "chunked" takes the chunked form (dk 128, dv <= 128; the library
-    reads GDN_KDA_PREFILL_PATH on every call), "recurrent" the default."""
-    if path == "chunked":
-        monkeypatch.setenv("GDN_KDA_PREFILL_PATH", "chunked")
+    """path "recurrent" forces the token recurrence (the library reads
+    GDN_KDA_PREFILL_PATH on every call); "chunked" is the default, which
+    takes the chunked form where it applies (dk 128, dv <= 128) and the
+    recurrence elsewhere (the tiny and dk 64 cases)."""
+    if path == "recurrent":
+        monkeypatch.setenv("GDN_KDA_PREFILL_PATH", "recurrent")
     n = len(lens)
     n_slots = 8 if shape.dk == 16 else 12
     st = Setup(shape, seed=140, num_slots=n_slots)
