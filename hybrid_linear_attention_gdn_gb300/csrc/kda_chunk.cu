@@ -24,6 +24,8 @@
 #include "gdn_common.cuh"
 #include "kda_chunk.cuh"
 
+#include <cstddef>
+
 namespace gdn {
 namespace {
 
@@ -73,9 +75,9 @@ struct __align__(16) CkSmem {
   float cw[kCkMaxW][kCh];   // conv weights, right-aligned
   float sy[kCk][kCh];       // conv + SiLU; q and k normalised in place
   float al[kCk][kD];        // log alpha (0 past the window's end)
-  float lb[kCk][kD + 1];    // cumulative log alpha from the window start (rows padded: bank spread)
-  float kp[kCk][kD + 1];    // k^, rows padded
-  float qp[kCk][kD + 1];    // q^, rows padded
+  float lb[kCk][kKQS];      // cumulative log alpha from the window start (padded rows)
+  float kp[kCk][kKQS];      // k^ (padded rows)
+  float qp[kCk][kKQS];      // q^ (padded rows)
   float kt[kCk][kKQS];      // K~
   float qt[kCk][kKQS];      // Q~
   float kb[kCk][kKBS];      // K-
@@ -83,6 +85,8 @@ struct __align__(16) CkSmem {
   float A[kCk][kCk];        // A' (t > j)
   float M[kCk][kTS];        // M (t >= j)
   float T[kCk][kTS];        // T (lower triangle with the diagonal, zero above)
+  float Pm[kCk][kCk + 1];   // powers of L = diag(beta) A' in the solve
+  float Xm[kCk][kCk + 1];   // (I + L)^-1 in the making
   float beta[kCk];
   float so[kCk][kMaxV];     // the window's outputs
 };
@@ -186,8 +190,13 @@ template <typename Tact, typename Tconv, bool ASYNC>
 __global__ void __launch_bounds__(kCkThreads, 1) kda_chunk_kernel(const KdaChunkArgs a) {
   pdl_wait();
   pdl_trigger();
+  using SMT = CkSmem<Tact>;
+  static_assert(offsetof(SMT, ga) % 16 == 0 && offsetof(SMT, lb) % 16 == 0 && offsetof(SMT, kp) % 16 == 0 &&
+                    offsetof(SMT, qp) % 16 == 0 && offsetof(SMT, kt) % 16 == 0 && offsetof(SMT, qt) % 16 == 0 &&
+                    offsetof(SMT, kb) % 16 == 0 && offsetof(SMT, dec) % 16 == 0,
+                "vector-accessed shared arrays must start 16-byte aligned");
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  CkSmem<Tact>& S = *reinterpret_cast<CkSmem<Tact>*>(smem_raw);
+  SMT& S = *reinterpret_cast<SMT*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int h = blockIdx.x, n = blockIdx.y, hq = h / a.G;
   const int dv = a.dv, nch = 2 * kD + dv;
@@ -297,7 +306,8 @@ __global__ void __launch_bounds__(kCkThreads, 1) kda_chunk_kernel(const KdaChunk
     // log alpha = -exp(A_log) softplus(a + dt_bias) (0 past the window's end)
     for (int e = tid; e < kCk * kD; e += kCkThreads) {
       const int t = e / kD, c = e % kD;
-      S.al[t][c] = t < nt ? -eA * softplus_f(to_f32(S.ga[cur][t][c]) + dtb) : 0.f;
+      const float x = to_f32(S.ga[cur][t][c]) + dtb;
+      S.al[t][c] = t < nt ? -eA * (x > 20.f ? x : __logf(1.f + __expf(x))) : 0.f;  // softplus
     }
     __syncthreads();
     // 2. per token (a warp per token): q, k normalised in place, beta
@@ -354,11 +364,17 @@ __global__ void __launch_bounds__(kCkThreads, 1) kda_chunk_kernel(const KdaChunk
       const int t = tid >> 4, j = tid & 15;
       if (t >= j) {
         float vk = 0.f, vq = 0.f;
-#pragma unroll 8
-        for (int c = 0; c < kD; ++c) {
-          const float f = S.kp[j][c] * __expf(S.lb[t][c] - S.lb[j][c]);
-          vk = fmaf(S.kp[t][c], f, vk);
-          vq = fmaf(S.qp[t][c], f, vq);
+#pragma unroll 4
+        for (int c = 0; c < kD; c += 4) {
+          const float4 kj = *reinterpret_cast<const float4*>(&S.kp[j][c]);
+          const float4 lj = *reinterpret_cast<const float4*>(&S.lb[j][c]);
+          const float4 lt = *reinterpret_cast<const float4*>(&S.lb[t][c]);
+          const float4 kt4 = *reinterpret_cast<const float4*>(&S.kp[t][c]);
+          const float4 qt4 = *reinterpret_cast<const float4*>(&S.qp[t][c]);
+          const float f0 = kj.x * __expf(lt.x - lj.x), f1 = kj.y * __expf(lt.y - lj.y);
+          const float f2 = kj.z * __expf(lt.z - lj.z), f3 = kj.w * __expf(lt.w - lj.w);
+          vk = fmaf(kt4.x, f0, fmaf(kt4.y, f1, fmaf(kt4.z, f2, fmaf(kt4.w, f3, vk))));
+          vq = fmaf(qt4.x, f0, fmaf(qt4.y, f1, fmaf(qt4.z, f2, fmaf(qt4.w, f3, vq))));
         }
         S.A[t][j] = vk;  // used below the diagonal only
         S.M[t][j] = vq;
@@ -368,20 +384,30 @@ __global__ void __launch_bounds__(kCkThreads, 1) kda_chunk_kernel(const KdaChunk
       }
     }
     __syncthreads();
-    // 4. T = (I + diag(beta) A')^-1 diag(beta): lane j of warp 0 solves column j
-    if (warp == 0 && lane < kCk) {
-      const int j = lane;
-      float x[kCk];
+    // 4. T = (I + L)^-1 diag(beta), L = diag(beta) A' strictly lower: by
+    //    doubling, (I + L)^-1 = (I - L)(I + L^2)(I + L^4)(I + L^8) (L^16 = 0),
+    //    a thread per entry
+    {
+      const int t = tid >> 4, j = tid & 15;
+      const float l = t > j ? S.beta[t] * S.A[t][j] : 0.f;
+      S.Pm[t][j] = l;
+      S.Xm[t][j] = (t == j ? 1.f : 0.f) - l;
+      __syncthreads();
 #pragma unroll
-      for (int t = 0; t < kCk; ++t) {
-        float acc = 0.f;
+      for (int k = 0; k < 3; ++k) {
+        float p2 = 0.f, xp = 0.f;
 #pragma unroll
-        for (int m = 0; m < t; ++m) acc = fmaf(S.A[t][m], x[m], acc);
-        x[t] = t < j ? 0.f : (t == j ? 1.f : -S.beta[t] * acc);
+        for (int m = 0; m < kCk; ++m) p2 = fmaf(S.Pm[t][m], S.Pm[m][j], p2);
+        __syncthreads();
+        S.Pm[t][j] = p2;
+        __syncthreads();
+#pragma unroll
+        for (int m = 0; m < kCk; ++m) xp = fmaf(S.Xm[t][m], S.Pm[m][j], xp);
+        __syncthreads();
+        S.Xm[t][j] += xp;
+        __syncthreads();
       }
-      const float bj = S.beta[j];
-#pragma unroll
-      for (int t = 0; t < kCk; ++t) S.T[t][j] = x[t] * bj;
+      S.T[t][j] = S.Xm[t][j] * S.beta[j];
     }
     __syncthreads();
     // 5. the state rows on the tensor cores (split tf32, fp32 accuracy), a
