@@ -78,13 +78,14 @@ struct __align__(16) CkSmem {
   float lb[kCk][kKQS];      // cumulative log alpha from the window start (padded rows)
   float kp[kCk][kKQS];      // k^ (padded rows)
   float qp[kCk][kKQS];      // q^ (padded rows)
-  float kt[kCk][kKQS];      // K~
-  float qt[kCk][kKQS];      // Q~
-  float kb[kCk][kKBS];      // K-
+  uint32_t kth[kCk][kKQS], ktl[kCk][kKQS];  // K~ as tf32 hi + lo
+  uint32_t qth[kCk][kKQS], qtl[kCk][kKQS];  // Q~ as tf32 hi + lo
+  uint32_t kbh[kCk][kKBS], kbl[kCk][kKBS];  // K- as tf32 hi + lo
   float dec[kD];            // a_last: the window's decay of the state
   float A[kCk][kCk];        // A' (t > j)
   float M[kCk][kTS];        // M (t >= j)
-  float T[kCk][kTS];        // T (lower triangle with the diagonal, zero above)
+  uint32_t Mh[kCk][kTS], Ml[kCk][kTS];  // M as tf32 hi + lo
+  uint32_t Th[kCk][kTS], Tl[kCk][kTS];  // T (lower triangle with the diagonal) as tf32 hi + lo
   float Pm[kCk][kCk + 1];   // powers of L = diag(beta) A' in the solve
   float Xm[kCk][kCk + 1];   // (I + L)^-1 in the making
   float beta[kCk];
@@ -121,16 +122,14 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-// d += a b in split tf32: a = (ah, al), b = (b0, b1) split inside
-__device__ __forceinline__ void mma3(float (&d)[4], const uint32_t (&ah)[4], const uint32_t (&al)[4], float b0,
-                                     float b1) {
-  uint32_t bh0, bl0, bh1, bl1;
-  split_tf32(b0, bh0, bl0);
-  split_tf32(b1, bh1, bl1);
+// d += a b with b already split (hi, lo)
+__device__ __forceinline__ void mma3s(float (&d)[4], const uint32_t (&ah)[4], const uint32_t (&al)[4], uint32_t bh0,
+                                      uint32_t bh1, uint32_t bl0, uint32_t bl1) {
   mma_tf32(d, al, bh0, bh1);
   mma_tf32(d, ah, bl0, bl1);
   mma_tf32(d, ah, bh0, bh1);
 }
+
 // The A fragment of an 8-column group from the same group in the C layout
 // (c[0..3] = (g, 2tq), (g, 2tq + 1), (g + 8, 2tq), (g + 8, 2tq + 1)): quad
 // shuffles, then the split
@@ -192,8 +191,7 @@ __global__ void __launch_bounds__(kCkThreads, 1) kda_chunk_kernel(const KdaChunk
   pdl_trigger();
   using SMT = CkSmem<Tact>;
   static_assert(offsetof(SMT, ga) % 16 == 0 && offsetof(SMT, lb) % 16 == 0 && offsetof(SMT, kp) % 16 == 0 &&
-                    offsetof(SMT, qp) % 16 == 0 && offsetof(SMT, kt) % 16 == 0 && offsetof(SMT, qt) % 16 == 0 &&
-                    offsetof(SMT, kb) % 16 == 0 && offsetof(SMT, dec) % 16 == 0,
+                    offsetof(SMT, qp) % 16 == 0 && offsetof(SMT, dec) % 16 == 0,
                 "vector-accessed shared arrays must start 16-byte aligned");
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SMT& S = *reinterpret_cast<SMT*>(smem_raw);
@@ -348,9 +346,9 @@ __global__ void __launch_bounds__(kCkThreads, 1) kda_chunk_kernel(const KdaChunk
       for (int t = 0; t < kCk; ++t) {
         const float kv = S.sy[t][kD + c], qv = S.sy[t][c];
         const float ef = __expf(lbv[t]), eb = __expf(acc - lbv[t]);
-        S.kt[t][c] = kv * ef;
-        S.qt[t][c] = qv * ef;
-        S.kb[t][c] = kv * eb;
+        split_tf32(kv * ef, S.kth[t][c], S.ktl[t][c]);
+        split_tf32(qv * ef, S.qth[t][c], S.qtl[t][c]);
+        split_tf32(kv * eb, S.kbh[t][c], S.kbl[t][c]);
         S.lb[t][c] = lbv[t];
         S.kp[t][c] = kv;
         S.qp[t][c] = qv;
@@ -407,7 +405,8 @@ __global__ void __launch_bounds__(kCkThreads, 1) kda_chunk_kernel(const KdaChunk
         S.Xm[t][j] += xp;
         __syncthreads();
       }
-      S.T[t][j] = S.Xm[t][j] * S.beta[j];
+      split_tf32(S.Xm[t][j] * S.beta[j], S.Th[t][j], S.Tl[t][j]);
+      split_tf32(S.M[t][j], S.Mh[t][j], S.Ml[t][j]);
     }
     __syncthreads();
     // 5. the state rows on the tensor cores (split tf32, fp32 accuracy), a
@@ -425,10 +424,9 @@ __global__ void __launch_bounds__(kCkThreads, 1) kda_chunk_kernel(const KdaChunk
         c_to_a(sc[kk], ah, al);
 #pragma unroll
         for (int nt2 = 0; nt2 < 2; ++nt2) {
-          const float* kr = &S.kt[8 * nt2 + g][8 * kk + tq];
-          const float* qr = &S.qt[8 * nt2 + g][8 * kk + tq];
-          mma3(xk[nt2], ah, al, kr[0], kr[4]);
-          mma3(xq[nt2], ah, al, qr[0], qr[4]);
+          const int r8 = 8 * nt2 + g, c8 = 8 * kk + tq;
+          mma3s(xk[nt2], ah, al, S.kth[r8][c8], S.kth[r8][c8 + 4], S.ktl[r8][c8], S.ktl[r8][c8 + 4]);
+          mma3s(xq[nt2], ah, al, S.qth[r8][c8], S.qth[r8][c8 + 4], S.qtl[r8][c8], S.qtl[r8][c8 + 4]);
         }
       }
       // X = v - Xk (rows past dv: 0), in place
@@ -452,8 +450,8 @@ __global__ void __launch_bounds__(kCkThreads, 1) kda_chunk_kernel(const KdaChunk
         c_to_a(xk[kj], ah, al);
 #pragma unroll
         for (int nt2 = 0; nt2 < 2; ++nt2) {
-          const float* tr = &S.T[8 * nt2 + g][8 * kj + tq];
-          mma3(dl[nt2], ah, al, tr[0], tr[4]);
+          const int r8 = 8 * nt2 + g, c8 = 8 * kj + tq;
+          mma3s(dl[nt2], ah, al, S.Th[r8][c8], S.Th[r8][c8 + 4], S.Tl[r8][c8], S.Tl[r8][c8 + 4]);
         }
       }
       // o = Xq + Delta M^T; St <- St diag(a_last) + Delta K- (Delta as A)
@@ -464,8 +462,8 @@ __global__ void __launch_bounds__(kCkThreads, 1) kda_chunk_kernel(const KdaChunk
       for (int kj = 0; kj < 2; ++kj)
 #pragma unroll
         for (int nt2 = 0; nt2 < 2; ++nt2) {
-          const float* mr = &S.M[8 * nt2 + g][8 * kj + tq];
-          mma3(xq[nt2], dh[kj], dlo[kj], mr[0], mr[4]);
+          const int r8 = 8 * nt2 + g, c8 = 8 * kj + tq;
+          mma3s(xq[nt2], dh[kj], dlo[kj], S.Mh[r8][c8], S.Mh[r8][c8 + 4], S.Ml[r8][c8], S.Ml[r8][c8 + 4]);
         }
 #pragma unroll
       for (int nt2 = 0; nt2 < 2; ++nt2) {
@@ -484,8 +482,8 @@ __global__ void __launch_bounds__(kCkThreads, 1) kda_chunk_kernel(const KdaChunk
         sc[j][3] *= d1;
 #pragma unroll
         for (int kj = 0; kj < 2; ++kj) {
-          const float* br = &S.kb[8 * kj + tq][8 * j + g];
-          mma3(sc[j], dh[kj], dlo[kj], br[0], br[4 * kKBS]);
+          const int r8 = 8 * kj + tq, c8 = 8 * j + g;
+          mma3s(sc[j], dh[kj], dlo[kj], S.kbh[r8][c8], S.kbh[r8 + 4][c8], S.kbl[r8][c8], S.kbl[r8 + 4][c8]);
         }
       }
     }
