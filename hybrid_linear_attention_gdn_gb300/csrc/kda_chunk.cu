@@ -1,4 +1,4 @@
-// KDA prefill, chunked form on CUDA cores (dk = 128, dv <= 128), fp32.
+// KDA prefill, chunked form (dk = 128, dv <= 128), fp32 accuracy.
 //
 // The per-key-channel gated delta rule (Kimi Delta Attention, Kimi Linear
 // 2025: St <- St diag(alpha_t) + beta_t (v_t - St diag(alpha_t) k_t) k_t^T,
@@ -12,14 +12,15 @@
 // the window is, for every state row (a row of St):
 //   X = v - St K~^T,  Delta = X T^T,  o = St Q~^T + M Delta,
 //   St <- St diag(a_last) + Delta K-.
-// This is the window-level unrolling of the token step (the same algebra as
-// the chunkwise WY form of the Gated DeltaNet paper with the decay kept per
-// channel); every decay factor is a product of alphas over a token range,
-// formed by running products, so none can overflow.  The 16 products of a
-// row are independent, unlike the token recurrence's dependent chain.
+// This is the window-level unrolling of the token step (the chunkwise WY
+// algebra of the Gated DeltaNet paper with the decay kept per channel).  Every
+// decay factor is a product of alphas over a token range, at most 1, formed
+// from cumulative logs, so none can overflow.
 //
-// One CTA per (sequence, V head), 256 threads: thread 2r + h holds columns
-// 64h .. 64h+63 of state row r in registers for the whole sequence.  The raw
+// One CTA per (sequence, V head), 256 threads.  The state rows' products run
+// on the tensor cores (mma m16n8k8 tf32, operands split hi + lo so that three
+// products carry an fp32 product): warp w owns rows 16w .. 16w+15, held in
+// registers in the accumulator layout for the whole sequence.  The raw
 // inputs of window w+1 are staged by cp.async while window w is computed.
 #include "gdn_common.cuh"
 #include "kda_chunk.cuh"
