@@ -1,4 +1,4 @@
-// KDA prefill in the chunked form on CUDA cores (dk = 128, dv <= 128); see kda_chunk.cu.
+// KDA prefill in the chunked form (dk = 128, dv <= 128), the row products on the tensor cores; see kda_chunk.cu.
 #pragma once
 #include "gdn_common.cuh"
 
