@@ -80,3 +80,22 @@ def test_gated_rmsnorm_zero_rows_and_empty(cuda):
     assert gdn.launch_count(gdn.K_GATED_RMSNORM) == n0
     with pytest.raises(gdn.GdnError):
         gdn.gated_rmsnorm(gdn.Dims.of(shape), o_d, z.cuda(), w.cuda(), -1.0)
+
+
+def test_gated_rmsnorm_32768_tokens_sampled_rows(cuda):
+    """The benchmark's launch: 32768 tokens x 32 heads in place; 4096 sampled
+    (token, head) rows against the oracle (the norm is per row)."""
+    shape = synth.QWEN
+    n_tok = 32768
+    o, z, w = _rows(shape, n_tok, 64)
+    o_d = o.cuda()
+    gdn.gated_rmsnorm(gdn.Dims.of(shape), o_d, z.cuda(), w.cuda(), 1e-6)
+    torch.cuda.synchronize()
+    g = synth.generator(65)
+    tok = torch.randint(0, n_tok, (4096,), generator=g)
+    head = torch.randint(0, shape.hv, (4096,), generator=g)
+    one = odims(shape.replace(hk=1, hv=1))
+    ref = oracle.gated_rmsnorm(one, to_np(o[tok, head])[:, None, :], to_np(z[tok, head])[:, None, :],
+                               w.double().numpy(), eps=1e-6)
+    got = o_d.cpu()[tok, head][:, None, :]
+    assert_out_close(got, ref, shape.dv, out_tol(shape))

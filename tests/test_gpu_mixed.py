@@ -52,13 +52,16 @@ CASES = [
     (synth.QWEN, 16, [], []),
     (synth.QWEN, 0, [300, 9], [512, 1001]),
     (synth.TINY, 3, [37, 130, 1], [5, 64, 300]),
+    # the benchmark's batch: 64 decode requests + 4 continuations of 256 tokens
+    (synth.QWEN, 64, [256] * 4, [1000, 3077, 517, 8191]),
 ]
-IDS = ["qwen_6_decode_4_continuations", "qwen_decode_only", "qwen_prefill_only", "tiny_mixed"]
+IDS = ["qwen_6_decode_4_continuations", "qwen_decode_only", "qwen_prefill_only", "tiny_mixed",
+       "qwen_64_decode_4x256_bench_batch"]
 
 
 @pytest.mark.parametrize("shape,n_dec,lens,starts", CASES, ids=IDS)
 def test_mixed_step_vs_oracle(cuda, shape, n_dec, lens, starts):
-    n_slots = 16 if shape is synth.TINY else 24
+    n_slots = 16 if shape is synth.TINY else max(24, n_dec + len(lens) + 4)
     st = Setup(shape, seed=50, num_slots=n_slots)
     ids, cu, sp, ck_ids, n_ck, qkv, a, b = _batch(st, n_dec, lens, starts, n_slots)
     n, total = ids.shape[0], int(cu[-1])
@@ -110,7 +113,7 @@ def test_mixed_step_vs_oracle(cuda, shape, n_dec, lens, starts):
 def test_mixed_step_equals_separate_calls(cuda, shape, n_dec, lens, starts):
     """Bit for bit the decode step on the decode rows and the chunked prefill on
     the rest, called one after the other."""
-    n_slots = 16 if shape is synth.TINY else 24
+    n_slots = 16 if shape is synth.TINY else max(24, n_dec + len(lens) + 4)
     st = Setup(shape, seed=51, num_slots=n_slots)
     ids, cu, sp, ck_ids, n_ck, qkv, a, b = _batch(st, n_dec, lens, starts, n_slots)
     n, total = ids.shape[0], int(cu[-1])
