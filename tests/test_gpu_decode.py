@@ -49,13 +49,14 @@ def test_tiny_eight_steps(cuda):
     assert torch.equal(st.pool.conv[untouched], before[1])
 
 
-@pytest.mark.parametrize("B", [1, 3, 8, 16, 64])
+@pytest.mark.parametrize("B", [1, 3, 8, 16, 64, 128, 256])
 def test_qwen_one_step(cuda, B):
     """Qwen3.5-shaped layer (16 QK / 32 V heads, dk=dv=128, bf16), batches from
-    far below one work item per SM to several per SM."""
-    st = Setup(synth.QWEN, seed=1, num_slots=80)
-    ids = synth.slot_ids(80, B, st.gen)
-    untouched = [s for s in range(80) if s not in ids.tolist()][:8]
+    far below one work item per SM to many per SM (the benchmark's sweep)."""
+    n_slots = max(80, B + 16)
+    st = Setup(synth.QWEN, seed=1, num_slots=n_slots)
+    ids = synth.slot_ids(n_slots, B, st.gen)
+    untouched = [s for s in range(n_slots) if s not in ids.tolist()][:8]
     before = st.pool.ssm[untouched].clone()
     qkv, a, b = st.tokens((B,))
     out, o_ref, err = _step(st, ids, qkv, a, b)

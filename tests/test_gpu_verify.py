@@ -32,15 +32,17 @@ def _spec_pool(st: Setup, n):
     (synth.QWEN, 24, 16, "tma"),
     (synth.QWEN.replace(act="f32", conv="f32", hk=4, hv=8), 5, 6, None),
     (synth.QWEN.replace(hk=2, hv=8, dk=64, dv=64), 3, 3, None),
+    (synth.QWEN, 64, 8, None),
 ], ids=["tiny", "qwen_b16_t8", "qwen_b16_t8_persistent", "qwen_b32_t8", "qwen_b32_t8_per_head",
-        "qwen_b3_t4_persistent", "qwen_b24_t16", "qwen_b24_t16_persistent", "f32_b5_t6", "dk64_g4"])
+        "qwen_b3_t4_persistent", "qwen_b24_t16", "qwen_b24_t16_persistent", "f32_b5_t6", "dk64_g4",
+        "qwen_b64_t8"])
 def test_verify_then_commit(cuda, monkeypatch, shape, B, T, path):
     """path: None = the library's own choice (per-head kernel below six
     (request, V head) items per SM, the persistent TMA-fed kernel above);
     "tma" / "rows" force one (GDN_DECODE_PATH, read on every call)."""
     if path:
         monkeypatch.setenv("GDN_DECODE_PATH", path)
-    n_work = 8 if shape is synth.TINY else 48
+    n_work = 8 if shape is synth.TINY else max(48, B + 8)
     st = Setup(shape, seed=30, num_slots=n_work)
     ids = synth.slot_ids(n_work, B, st.gen)
     spec = _spec_pool(st, B * T + 3)
