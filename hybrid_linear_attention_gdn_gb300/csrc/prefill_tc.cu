@@ -987,7 +987,11 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       if (!(alive = cta_wait(&S.mma_bar, mph, bad))) break;
       mph ^= 1;
       umma::fence_after();
-      // S^T <- e^{b_last} S^T + D2 ; O = O1 diag(e^b) + O2
+      // S^T <- e^{b_last} S^T + D2; O1 read (the next chunk's S^T [K;Q]^T
+      // overwrites it); the state image and any checkpoint staging; then
+      // st_bar, so that the issue warp's next product runs under the output
+      // staging O = O1 diag(e^b) + O2
+      float o1[32];
       {
         const float dec = eb[kC - 1];
         float d2[32];
@@ -997,22 +1001,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         umma::tmem_ld32(tlane + TM_D2 + 64 * half + 32, d2);
 #pragma unroll
         for (int i = 0; i < 32; ++i) sreg[32 + i] = fmaf(dec, sreg[32 + i], d2[i]);
-        float o1[32], o2[32];
         umma::tmem_ld32(tlane + TM_O1 + 32 * half, o1);
-        umma::tmem_ld32(tlane + TM_O2 + 32 * half, o2);
-        float ebr[32];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 e4 = *reinterpret_cast<const float4*>(eb + 32 * half + 4 * i);
-          ebr[4 * i] = e4.x;
-          ebr[4 * i + 1] = e4.y;
-          ebr[4 * i + 2] = e4.z;
-          ebr[4 * i + 3] = e4.w;
-        }
-        // stage O as [token][dv] in the (now free) scratch tile
-        Tact* ot = reinterpret_cast<Tact*>(S.wt);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) ot[(32 * half + i) * kD + lrow] = from_f32<Tact>(fmaf(o1[i], ebr[i], o2[i]));
       }
       umma::store_row64(S.st + half * (128 * 128), lrow, sreg);
       // checkpoint slot of a block boundary at this chunk's end (-1: none)
@@ -1047,6 +1036,25 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       umma::fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.st_bar);
+      {
+        float o2[32];
+        umma::tmem_ld32(tlane + TM_O2 + 32 * half, o2);
+        float ebr[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 e4 = *reinterpret_cast<const float4*>(eb + 32 * half + 4 * i);
+          ebr[4 * i] = e4.x;
+          ebr[4 * i + 1] = e4.y;
+          ebr[4 * i + 2] = e4.z;
+          ebr[4 * i + 3] = e4.w;
+        }
+        // stage O as [token][dv] in the (now free) scratch tile
+        Tact* ot = reinterpret_cast<Tact*>(S.wt);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) ot[(32 * half + i) * kD + lrow] = from_f32<Tact>(fmaf(o1[i], ebr[i], o2[i]));
+      }
+      // the staged tile reaches the tensor store's proxy
+      umma::fence_proxy_async();
       compute_sync();
       // a chunk inside the sequence leaves as one tensor store of its staged
       // 64 x 128 output tile
