@@ -93,15 +93,6 @@ struct __align__(16) CkSmem {
   float so[kCk][kMaxV];     // the window's outputs
 };
 
-__device__ __forceinline__ float2 fma2c(float2 a, float2 b, float2 c) {
-  float2 d;
-  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
-      " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}\n"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-  return d;
-}
-
 // Warp-level tf32 tensor-core product (m16n8k8, fp32 accumulate).  Lane =
 // 4 g + tq; A holds (g, tq), (g + 8, tq), (g, tq + 4), (g + 8, tq + 4); B holds
 // (tq, g), (tq + 4, g); C/D hold (g, 2tq), (g, 2tq + 1), (g + 8, 2tq), (g + 8, 2tq + 1).
