@@ -64,8 +64,10 @@ def _n_ck(starts, lens, blk):
     (synth.QWEN.replace(act="f32", conv="f32", hk=4, hv=8), [100, 17], [30, 0], 64, "chunked"),
     (synth.QWEN, [200, 1, 70, 129], [200, 77, 4101, 63], 256, "chunked"),
     (synth.QWEN.replace(conv="f32", dv=96), [33, 300], [5, 64], 64, "chunked"),
+    # v rows of 200 bytes: the staging falls back to element copies
+    (synth.QWEN.replace(dv=100), [45, 130], [9, 0], 64, "chunked"),
 ], ids=["tiny", "qwen_recurrent", "dk64_g4", "f32_recurrent", "qwen_unaligned_continuations_recurrent", "qwen",
-        "f32", "qwen_unaligned_continuations", "dv96_f32conv"])
+        "f32", "qwen_unaligned_continuations", "dv96_f32conv", "dv100_element_staging"])
 def test_kda_prefill_vs_oracle(cuda, monkeypatch, shape, lens, starts, blk, path):
     """path "recurrent" forces the token recurrence (the library reads
     GDN_KDA_PREFILL_PATH on every call); "chunked" is the default, which
