@@ -139,12 +139,13 @@ gdn_status gdn_kda_spec_verify(const gdn_dims* dims, gdn_pool work, gdn_pool spe
                                void* out, uint32_t* dev_err, void* stream);
 
 /*
- * KDA prefill (the recurrent form, fp32): the contract of gdn_chunk_prefill
- * (packed sequences from any start position, block-aligned checkpoints of SSM
- * state and conv history, final state into the working slot) with every
- * token the KDA step of gdn_kda_decode_step; a [total_tokens][hv][dk],
- * params->dt_bias [hv][dk].  Token by token, so it needs no workspace;
- * ckpt_block a positive multiple of 64.
+ * KDA prefill: the contract of gdn_chunk_prefill (packed sequences from any
+ * start position, block-aligned checkpoints of SSM state and conv history,
+ * final state into the working slot) with every token the KDA step of
+ * gdn_kda_decode_step; a [total_tokens][hv][dk], params->dt_bias [hv][dk].
+ * fp32 accuracy: dk = 128 with dv <= 128 runs a 16-token chunked form (its
+ * products on the tensor cores in split tf32), other shapes the token
+ * recurrence.  Needs no workspace; ckpt_block a positive multiple of 64.
  */
 gdn_status gdn_kda_prefill(const gdn_dims* dims, gdn_pool pool, gdn_pool ckpt,
                            const gdn_params* params, const int32_t* slot_ids,
