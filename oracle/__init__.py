@@ -340,6 +340,32 @@ def kda_prefill(dims: Dims, pool: Pool, ckpt: Pool, params: Params, slot_ids, cu
     return out, err.value
 
 
+def kda_prefill_chunked(dims: Dims, pool: Pool, ckpt: Pool, params: Params, slot_ids, cu_seqlens, start_pos,
+                        ckpt_ids, ckpt_block, chunk, qkv, a, b):
+    """The KDA prefill evaluated in windows of `chunk` tokens (the window form:
+    A', M, T from per-channel cumulative log decays); cross-check only.
+    Returns (out, err)."""
+    L = lib()
+    slot_ids = _i32(slot_ids)
+    cu = _i32(cu_seqlens)
+    sp = np.ascontiguousarray(start_pos, dtype=np.int64)
+    ck = _i32(ckpt_ids)
+    if ck.ndim == 1:
+        ck = ck.reshape(slot_ids.shape[0], -1)
+    qkv, a, b = _f64(qkv), _f64(a), _f64(b)
+    ttot = int(cu[-1])
+    assert qkv.shape == (ttot, dims.channels) and a.shape == (ttot, dims.hv, dims.dk)
+    out = np.zeros((ttot, dims.hv, dims.dv), np.float64)
+    err = ctypes.c_uint32(0)
+    cd, cpa = dims.c(), params.c()
+    rc = L.orc_kda_prefill_chunked(ctypes.byref(cd), pool.c(), ckpt.c(), ctypes.byref(cpa), _ptr(slot_ids),
+                                   _ptr(cu), _ptr(sp), ctypes.c_int32(slot_ids.shape[0]), _ptr(ck),
+                                   ctypes.c_int32(ck.shape[1]), ctypes.c_int32(ckpt_block), ctypes.c_int32(chunk),
+                                   _ptr(qkv), _ptr(a), _ptr(b), _ptr(out), ctypes.byref(err))
+    assert rc == 0
+    return out, err.value
+
+
 def gated_rmsnorm(dims: Dims, o, z, w, eps=1e-6):
     """Readout epilogue y = o / sqrt(mean(o^2) + eps) * w * silu(z) per
     (token, V head) row; o, z [n_tok][hv][dv], w [dv].  Returns y."""

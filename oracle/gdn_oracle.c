@@ -579,6 +579,168 @@ int orc_kda_prefill(const orc_dims* d, orc_pool pool, orc_pool ckpt, const orc_p
   return 0;
 }
 
+/* ---- KDA prefill cross-check: the window (chunk) form (double) -----------
+ * Same contract as orc_kda_prefill, the state recurrence evaluated one window
+ * of `chunk` tokens at a time, windows aligned to absolute positions.  With the
+ * per-channel cumulative log decay lb_r[c] = sum_{m<=r} g_m[c] inside the window
+ * (r = 0 .. n-1) and, for every state row j (St[j][.]):
+ *   A'[r][m] = sum_c k_r[c] k_m[c] e^{lb_r[c] - lb_m[c]}   (r > m)
+ *   M[r][m]  = sum_c q_r[c] k_m[c] e^{lb_r[c] - lb_m[c]}   (r >= m)
+ *   (I + diag(beta) A') T = diag(beta)
+ *   X[r]     = v_r[j] - sum_c St[j][c] k_r[c] e^{lb_r[c]}
+ *   Delta[r] = sum_m T[r][m] X[m]
+ *   o_r[j]   = sum_c St[j][c] q_r[c] e^{lb_r[c]} + sum_{m<=r} M[r][m] Delta[m]
+ *   St'[j][c] = St[j][c] e^{lb_{n-1}[c]} + sum_r Delta[r] k_r[c] e^{lb_{n-1}[c] - lb_r[c]}
+ * ckpt_block must be a multiple of chunk. */
+int orc_kda_prefill_chunked(const orc_dims* d, orc_pool pool, orc_pool ckpt, const orc_params* p,
+                            const int32_t* slot_ids, const int32_t* cu_seqlens, const int64_t* start_pos,
+                            int32_t n_seq, const int32_t* ckpt_ids, int32_t max_ckpt, int32_t ckpt_block,
+                            int32_t chunk, const double* qkv, const double* a, const double* b, double* out,
+                            uint32_t* err) {
+  if (check_dims(d) || ckpt_block <= 0 || chunk <= 0 || ckpt_block % chunk) return 1;
+  int64_t C = n_chan(d), HVDV = (int64_t)d->hv * d->dv;
+  int64_t ns = ssm_elems(d), nc = conv_elems(d);
+  int dk = d->dk, dv = d->dv, G = d->hv / d->hk;
+  int64_t fail = 0;
+  for (int32_t n = 0; n < n_seq; ++n) {
+    int32_t s = slot_ids[n];
+    int64_t t0 = cu_seqlens[n], t1 = cu_seqlens[n + 1], L = t1 - t0;
+    int cls = slot_class(s, pool.num_slots);
+    if (cls) {
+      if (cls == 2) fail |= ORC_ERR_SLOT_OOB;
+      for (int64_t i = t0 * HVDV; i < t1 * HVDV; ++i) out[i] = 0.0;
+      continue;
+    }
+    int64_t p0 = start_pos[n], blk0 = p0 / ckpt_block;
+    /* per-token features and the conv history after every token */
+    double* fq = (double*)malloc(sizeof(double) * (L + 1) * d->hk * dk);
+    double* fk = (double*)malloc(sizeof(double) * (L + 1) * d->hk * dk);
+    double* fv = (double*)malloc(sizeof(double) * (L + 1) * d->hv * dv);
+    double* fg = (double*)malloc(sizeof(double) * (L + 1) * d->hv * dk);
+    double* fb = (double*)malloc(sizeof(double) * (L + 1) * d->hv);
+    double* hist_after = (double*)malloc(sizeof(double) * (L + 1) * nc);
+    double* conv = pool.conv + s * nc;
+    double* y = (double*)malloc(sizeof(double) * C);
+    for (int64_t i = 0; i < L; ++i) {
+      const double* x = qkv + (t0 + i) * C;
+      orc_conv_silu(d, conv, x, p->conv_w, y);
+      conv_shift(d, conv, x);
+      memcpy(hist_after + i * nc, conv, sizeof(double) * nc);
+      for (int hq = 0; hq < d->hk; ++hq) {
+        orc_l2norm(dk, y + (int64_t)hq * dk, 1.0 / sqrt((double)dk), fq + (i * d->hk + hq) * dk);
+        orc_l2norm(dk, y + (int64_t)(d->hk + hq) * dk, 1.0, fk + (i * d->hk + hq) * dk);
+      }
+      memcpy(fv + i * d->hv * dv, y + 2 * (int64_t)d->hk * dk, sizeof(double) * d->hv * dv);
+      for (int h = 0; h < d->hv; ++h) {
+        fb[i * d->hv + h] = orc_sigmoid(b[(t0 + i) * d->hv + h]);
+        for (int c = 0; c < dk; ++c)
+          fg[(i * d->hv + h) * dk + c] =
+              orc_gate_g(p->A_log[h], p->dt_bias[(int64_t)h * dk + c], a[((t0 + i) * d->hv + h) * dk + c]);
+      }
+    }
+    int64_t mc = chunk;
+    double* lb = (double*)malloc(sizeof(double) * mc * dk);
+    double* Ap = (double*)malloc(sizeof(double) * mc * mc);
+    double* Mm = (double*)malloc(sizeof(double) * mc * mc);
+    double* Tm = (double*)malloc(sizeof(double) * mc * mc);
+    double* X = (double*)malloc(sizeof(double) * mc);
+    double* D = (double*)malloc(sizeof(double) * mc);
+    double* rowbuf = (double*)malloc(sizeof(double) * dk);
+    /* checkpoint rows are written per head as the windows end; the conv history
+       of a checkpoint comes from hist_after */
+    for (int h = 0; h < d->hv; ++h) {
+      int hq = h / G;
+      double* St = pool.ssm + s * ns + (int64_t)h * dv * dk;
+      int64_t i = 0;
+      while (i < L) {
+        int64_t pos = p0 + i;
+        int64_t wend = (pos / chunk + 1) * chunk;
+        int64_t nr = wend - pos;
+        if (nr > L - i) nr = L - i;
+#define KQ(r) (fk + ((i + (r)) * d->hk + hq) * dk)
+#define QQ(r) (fq + ((i + (r)) * d->hk + hq) * dk)
+#define GG(r) (fg + ((i + (r)) * d->hv + h) * dk)
+        for (int c = 0; c < dk; ++c) {
+          double acc = 0.0;
+          for (int64_t r = 0; r < nr; ++r) {
+            acc += GG(r)[c];
+            lb[r * dk + c] = acc;
+          }
+        }
+        for (int64_t r = 0; r < nr; ++r)
+          for (int64_t m = 0; m < nr; ++m) {
+            double va = 0.0, vm = 0.0;
+            if (m <= r)
+              for (int c = 0; c < dk; ++c) {
+                double f = KQ(m)[c] * exp(lb[r * dk + c] - lb[m * dk + c]);
+                va += KQ(r)[c] * f;
+                vm += QQ(r)[c] * f;
+              }
+            Ap[r * nr + m] = m < r ? va : 0.0;
+            Mm[r * nr + m] = vm;
+          }
+        /* (I + diag(beta) A') T = diag(beta), row by row */
+        for (int64_t r = 0; r < nr; ++r) {
+          double br = fb[(i + r) * d->hv + h];
+          for (int64_t c = 0; c < nr; ++c) {
+            double v = (r == c) ? br : 0.0;
+            for (int64_t m = 0; m < r; ++m) v -= br * Ap[r * nr + m] * Tm[m * nr + c];
+            Tm[r * nr + c] = v;
+          }
+        }
+        for (int j = 0; j < dv; ++j) {
+          double* row = St + (int64_t)j * dk;
+          for (int64_t r = 0; r < nr; ++r) {
+            double sk = 0.0;
+            for (int c = 0; c < dk; ++c) sk += row[c] * KQ(r)[c] * exp(lb[r * dk + c]);
+            X[r] = fv[(i + r) * d->hv * dv + (int64_t)h * dv + j] - sk;
+          }
+          for (int64_t r = 0; r < nr; ++r) {
+            double v = 0.0;
+            for (int64_t m = 0; m <= r; ++m) v += Tm[r * nr + m] * X[m];
+            D[r] = v;
+          }
+          for (int64_t r = 0; r < nr; ++r) {
+            double sq = 0.0;
+            for (int c = 0; c < dk; ++c) sq += row[c] * QQ(r)[c] * exp(lb[r * dk + c]);
+            for (int64_t m = 0; m <= r; ++m) sq += Mm[r * nr + m] * D[m];
+            out[(t0 + i + r) * HVDV + (int64_t)h * dv + j] = sq;
+          }
+          for (int c = 0; c < dk; ++c) {
+            double last = lb[(nr - 1) * dk + c];
+            double v = row[c] * exp(last);
+            for (int64_t r = 0; r < nr; ++r) v += D[r] * KQ(r)[c] * exp(last - lb[r * dk + c]);
+            rowbuf[c] = v;
+          }
+          memcpy(row, rowbuf, sizeof(double) * dk);
+        }
+#undef KQ
+#undef QQ
+#undef GG
+        i += nr;
+        /* a block boundary at the window's end */
+        int64_t P = p0 + i;
+        if (P % ckpt_block == 0) {
+          int64_t idx = P / ckpt_block - blk0 - 1;
+          if (idx >= 0 && idx < max_ckpt) {
+            int32_t cid = ckpt_ids[(int64_t)n * max_ckpt + idx];
+            int cc = slot_class(cid, ckpt.num_slots);
+            if (cc == 2) fail |= ORC_ERR_SLOT_OOB;
+            if (cc == 0) {
+              memcpy(ckpt.ssm + cid * ns + (int64_t)h * dv * dk, St, sizeof(double) * dv * dk);
+              if (h == 0) memcpy(ckpt.conv + cid * nc, hist_after + (i - 1) * nc, sizeof(double) * nc);
+            }
+          }
+        }
+      }
+    }
+    free(fq); free(fk); free(fv); free(fg); free(fb); free(hist_after); free(y);
+    free(lb); free(Ap); free(Mm); free(Tm); free(X); free(D); free(rowbuf);
+  }
+  if (err) *err |= (uint32_t)fail;
+  return 0;
+}
+
 /* ---- readout epilogue: gated RMS norm ----------------------------------
  * Not written on the pages.  The published Gated DeltaNet block normalises
  * each head's readout and gates it with a SiLU of a separate projection z:

@@ -45,6 +45,8 @@ MUTATIONS = {
     "kda_u_without_decay": ("sk += alpha[i] * row[i] * k[i];", "sk += row[i] * k[i];"),
     "kda_state_without_decay": ("row[i] = alpha[i] * row[i] + beta * u * k[i];",
                                 "row[i] = row[i] + beta * u * k[i];"),
+    "kda_window_kbar_decay": ("for (int64_t r = 0; r < nr; ++r) v += D[r] * KQ(r)[c] * exp(last - lb[r * dk + c]);",
+                              "for (int64_t r = 0; r < nr; ++r) v += D[r] * KQ(r)[c] * exp(last);"),
     "rmsnorm_sum_not_mean": ("double inv = 1.0 / sqrt(ss / (double)dv + eps);",
                              "double inv = 1.0 / sqrt(ss + eps);"),
     "rmsnorm_gate_sigmoid": ("orc_silu(z[r * dv + j])", "orc_sigmoid(z[r * dv + j])"),

@@ -726,3 +726,36 @@ def test_kda_prefill_equals_kda_decode_steps_and_checkpoints():
         np.testing.assert_array_equal(ck.ssm[cid], s_)
         np.testing.assert_array_equal(ck.conv[cid], c_)
     assert np.all(ck.ssm[[2, 4, 5]] == -9.0)
+
+
+@pytest.mark.parametrize("chunk", [1, 4, 16, 32])
+@pytest.mark.parametrize("strong_decay", [False, True])
+def test_kda_window_form_equals_token_recurrence(chunk, strong_decay):
+    """The KDA prefill in windows of `chunk` tokens (A', M, T from per-channel
+    cumulative log decays; the algebra of the GPU's chunked form) equals the
+    token-by-token KDA prefill: outputs, final states, conv histories and
+    checkpoints, from aligned and unaligned starts, in double precision.  With
+    strong decays (A_log = ln 16) many decay factors underflow to zero."""
+    shape = synth.TINY
+    d = _dims(shape)
+    g, pool, params = _tiny_setup(90 + chunk)
+    A_log = np.full(d.hv, math.log(16.0)) if strong_decay else params.A_log
+    pk = oracle.Params(params.conv_w, A_log, synth.normal((d.hv, d.dk), 0.5, g).double().numpy())
+    lens, starts, blk = [70, 45, 9], [0, 50, 3], 32
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    ids = np.array([3, 6, 1], np.int32)
+    qkv, _, b = (t.double().numpy() for t in synth.tokens(shape, g, (int(cu[-1]),)))
+    a = synth.normal((int(cu[-1]), d.hv, d.dk), 1.0, g).double().numpy()
+    ck_ids = np.array([[0, 1, 2], [3, 4, 5], [6, 7, 8]], np.int32)
+    ck1 = oracle.Pool(np.full((9, d.hv, d.dv, d.dk), -9.0), np.full((9, d.w - 1, d.channels), 4.0))
+    ck2 = oracle.Pool(ck1.ssm.copy(), ck1.conv.copy())
+    pool2 = pool.copy()
+    o1, e1 = oracle.kda_prefill(d, pool, ck1, pk, ids, cu, starts, ck_ids, blk, qkv, a, b)
+    o2, e2 = oracle.kda_prefill_chunked(d, pool2, ck2, pk, ids, cu, starts, ck_ids, blk, chunk, qkv, a, b)
+    assert e1 == e2 == 0
+    np.testing.assert_allclose(o2, o1, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(pool2.ssm, pool.ssm, rtol=1e-10, atol=1e-12)
+    np.testing.assert_array_equal(pool2.conv, pool.conv)
+    np.testing.assert_allclose(ck2.ssm, ck1.ssm, rtol=1e-10, atol=1e-12)
+    np.testing.assert_array_equal(ck2.conv, ck1.conv)
+    assert not np.all(ck1.ssm[[0, 1, 3]] == -9.0)  # the boundaries 32, 64 (seq 0) and 64 (seq 1) were written
