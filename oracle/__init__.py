@@ -20,6 +20,13 @@ Every function mirrors one step of the hot path:
   in the chunkwise WY/UT form and exists only to cross-check the algebra.
 * :func:`slot_copy` / :func:`slot_zero` - copy-on-write and explicit zeroing
   ("Riesgo de correctitud: estado obsoleto").
+* :func:`commit_index`, :func:`state_pack` / :func:`state_unpack`,
+  :func:`gated_rmsnorm` - the index-update commit, state records for a
+  transfer, and the readout epilogue.
+* :func:`kda_decode_step`, :func:`kda_spec_verify`, :func:`kda_prefill` - the
+  same steps with one decay per key channel (KDA).  :func:`kda_prefill_chunked`
+  evaluates the KDA prefill in windows (the algebra of the GPU's chunked form)
+  and exists only to cross-check that algebra.
 
 Parity pins for each function are in ``tests/test_oracle_pins.py``.  The
 numeric conventions the pages leave open (state orientation, the dk^-1/2 query
