@@ -289,9 +289,11 @@ def chunk_prefill(dims: Dims, pool: StatePool, ckpt: StatePool, params: LayerPar
 def kda_prefill(dims: Dims, pool: StatePool, ckpt: StatePool, params: LayerParams, slot_ids, cu_seqlens,
                 start_pos, total_tokens: int, ckpt_ids, ckpt_block: int, qkv, a, b, out, dev_err=None,
                 stream=None):
-    """KDA prefill in the recurrent form: chunk_prefill's contract with
-    per-key-channel gate logits a [total][hv][dk] and dt_bias [hv][dk]; it
-    needs no workspace."""
+    """KDA prefill: chunk_prefill's contract with per-key-channel gate logits
+    a [total][hv][dk] and dt_bias [hv][dk]; it needs no workspace.  dk 128
+    with dv <= 128 (dv % 4 == 0) runs the 16-token window form on the tensor
+    cores, other shapes (or GDN_KDA_PREFILL_PATH=recurrent) the token
+    recurrence; both keep fp32 accuracy."""
     L = load()
     n_seq = int(slot_ids.shape[0])
     max_ckpt = int(ckpt_ids.shape[1]) if ckpt_ids is not None and ckpt_ids.dim() == 2 else 0

@@ -155,6 +155,14 @@ __device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf
 __device__ __forceinline__ float softplus_f(float x) {
   return x > 20.0f ? x : log1pf(expf(x));
 }
+// The chunked forms take the decay between tokens j and t as
+// exp(b_t - b_j), with b the cumulative log decay.  A token whose decay is 0
+// (log decay -inf: a = +inf, or exp(A_log) * softplus overflowing) would make
+// that -inf - (-inf).  They floor each token's log decay here instead: its
+// exponential is exactly 0 in fp32, so the decay stays 0 and every difference
+// stays finite.  No finite gate of a trained layer comes near it.
+constexpr float kLogDecayFloor = -1000.0f;
+__device__ __forceinline__ float floor_log_decay(float g) { return fmaxf(g, kLogDecayFloor); }
 // alpha = exp(-exp(A_log) * softplus(a + dt_bias))
 __device__ __forceinline__ float gate_alpha(float A_log, float dt_bias, float a) {
   return expf(-expf(A_log) * softplus_f(a + dt_bias));

@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(kCkThreads, 1) kda_chunk_kernel(const KdaChunk
     for (int e = tid; e < kCk * kD; e += kCkThreads) {
       const int t = e / kD, c = e % kD;
       const float x = to_f32(S.ga[cur][t][c]) + dtb;
-      S.al[t][c] = t < nt ? -eA * (x > 20.f ? x : __logf(1.f + __expf(x))) : 0.f;  // softplus
+      S.al[t][c] = t < nt ? floor_log_decay(-eA * (x > 20.f ? x : __logf(1.f + __expf(x)))) : 0.f;  // softplus
     }
     __syncthreads();
     // 2. per token (a warp per token): q, k normalised in place, beta

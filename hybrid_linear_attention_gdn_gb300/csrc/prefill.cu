@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(kThreads) features_kernel(const PrefillArgs a)
     const int h = hq * a.G + tid;
     const float av = to_f32(reinterpret_cast<const Tact*>(a.a)[(size_t)t * a.hv + h]);
     const float bv = to_f32(reinterpret_cast<const Tact*>(a.b)[(size_t)t * a.hv + h]);
-    a.ws_g[(size_t)t * a.hv + h] = -expf(a.A_log[h]) * softplus_f(av + a.dt_bias[h]);
+    a.ws_g[(size_t)t * a.hv + h] = floor_log_decay(-expf(a.A_log[h]) * softplus_f(av + a.dt_bias[h]));
     a.ws_beta[(size_t)t * a.hv + h] = sigmoid_f(bv);
   }
 }

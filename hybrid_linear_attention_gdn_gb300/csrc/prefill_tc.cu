@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(kTh, 3) tc_features_kernel(const TcArgs a, con
       const size_t tok = (size_t)(t0 + pos - p0);
       const float av = to_f32(reinterpret_cast<const Tact*>(a.a)[tok * a.hv + h]);
       const float bb = to_f32(reinterpret_cast<const Tact*>(a.b)[tok * a.hv + h]);
-      gv = -expf(a.A_log[h]) * softplus_f(av + a.dt_bias[h]);
+      gv = floor_log_decay(-expf(a.A_log[h]) * softplus_f(av + a.dt_bias[h]));
       bv = sigmoid_f(bb);
     }
     float* gt = a.ws_gate + ((size_t)gc * a.hv + h) * (2 * kC);

@@ -1,0 +1,123 @@
+"""Tokens whose decay is exactly 0 (gate logit a = +inf, so g = -inf and
+alpha = 0) inside the chunked prefills, against the oracle's token-by-token
+recurrence.
+
+At such a token the state is wiped before the delta-rule update, so every
+output and state after it depends on the tokens from it on only.  The chunked
+forms build decays from differences of cumulative log decays; these tests
+place zero-decay tokens at a sequence's first token, inside a chunk, on both
+sides of a chunk boundary, in runs of two, and (KDA) on single key channels,
+on the tensor-core GDN prefill, the fp32 GDN prefill and the KDA window
+prefill.  The decode kernels' zero-decay closed forms are in test_gpu_decode."""
+import numpy as np
+import pytest
+import torch
+
+import hybrid_linear_attention_gdn_gb300 as gdn
+import oracle
+from hybrid_linear_attention_gdn_gb300 import LayerParams, StatePool, synth
+from helpers import (PREFILL_TOL, Setup, assert_out_close, conv_bits_equal, max_rel_l2, prefill_row_tol,
+                     prefill_state_tol, prefill_tol, to_np)
+
+pytestmark = pytest.mark.gpu
+
+# sequence-relative tokens given a = +inf: the first token, inside the first
+# 64-token chunk, both sides of the chunk boundary at 64 (start 0), a run of two
+ZERO_TOKENS = [0, 17, 63, 64, 100, 101, 190]
+
+
+def _ck_pool(st, n):
+    p = StatePool.empty(st.dims, n, "cuda")
+    p.ssm.fill_(-5.0)
+    p.conv.fill_(9.0)
+    return p
+
+
+def _ock_pool(shape, n):
+    return oracle.Pool(np.full((n, shape.hv, shape.dv, shape.dk), -5.0),
+                       np.full((n, shape.w - 1, shape.channels), 9.0))
+
+
+def _layout(lens, starts, blk, gen, n_slots):
+    n = len(lens)
+    ids = synth.slot_ids(n_slots, n, gen)
+    max_ck = max(1, max((s + L) // blk - s // blk for s, L in zip(starts, lens)))
+    n_ck = n * max_ck + 2
+    ck_ids = synth.slot_ids(n_ck, n * max_ck, gen).reshape(n, max_ck)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32)
+    sp = torch.tensor(starts, dtype=torch.int64)
+    return ids, ck_ids, n_ck, cu, sp
+
+
+def _zero_rows(lens, cu):
+    rows = []
+    for i, L in enumerate(lens):
+        rows += [int(cu[i]) + t for t in ZERO_TOKENS if t < L]
+    return rows
+
+
+def _check(st, shape, ids, ck, ock, n_ck, out, o_ref, tol, row_tol, stol):
+    torch.cuda.synchronize()
+    assert torch.isfinite(out.float()).all()
+    assert_out_close(out, o_ref, shape.dv, tol, row_floor_rms=True, row_tol=row_tol)
+    used = ids.tolist()
+    assert torch.isfinite(st.pool.ssm[used]).all()
+    assert max_rel_l2(to_np(st.pool.ssm[used]), st.opool.ssm[used], shape.dv * shape.dk) <= stol
+    assert conv_bits_equal(st.pool.conv[used], st.opool.conv[used])
+    written = [i for i in range(n_ck) if not np.all(ock.ssm[i] == -5.0)]
+    assert written
+    assert max_rel_l2(to_np(ck.ssm[written]), ock.ssm[written], shape.dv * shape.dk) <= stol
+
+
+@pytest.mark.parametrize("path", ["tc", "cuda"])
+def test_gdn_prefill_zero_decay_tokens(cuda, monkeypatch, path):
+    """Half of the V heads see a = +inf at the chosen tokens; path "cuda"
+    forces the fp32 prefill."""
+    if path == "cuda":
+        monkeypatch.setenv("GDN_PREFILL_PATH", "cuda")
+    shape = synth.QWEN
+    lens, starts, blk = [200, 130], [0, 37], 64
+    st = Setup(shape, seed=150, num_slots=6)
+    ids, ck_ids, n_ck, cu, sp = _layout(lens, starts, blk, st.gen, 6)
+    total = int(cu[-1])
+    qkv, a, b = st.tokens((total,))
+    a[_zero_rows(lens, cu), ::2] = float("inf")
+    ck = _ck_pool(st, n_ck)
+    out = torch.full((total, shape.hv, shape.dv), 3.0, dtype=shape.act_dtype, device="cuda")
+    nbytes = gdn.chunk_prefill_workspace_size(st.dims, len(lens), total)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device="cuda")
+    gdn.chunk_prefill(st.dims, st.pool, ck, st.params, ids.cuda(), cu.cuda(), sp.cuda(), total, ck_ids.cuda(),
+                      blk, qkv.cuda(), a.cuda(), b.cuda(), out, ws)
+    ock = _ock_pool(shape, n_ck)
+    o_ref, err = oracle.prefill(st.od, st.opool, ock, st.oparams, ids.numpy(), cu.numpy(), sp.numpy(),
+                                ck_ids.numpy(), blk, to_np(qkv), to_np(a), to_np(b))
+    assert err == 0
+    _check(st, shape, ids, ck, ock, n_ck, out, o_ref, prefill_tol(shape, path), prefill_row_tol(shape, path),
+           prefill_state_tol(shape, path))
+
+
+def test_kda_prefill_zero_decay_channels(cuda):
+    """KDA: every third key channel of every V head sees a = +inf at the
+    chosen tokens (the chunked form's 16-token windows; the second sequence
+    starts off a window boundary)."""
+    shape = synth.QWEN
+    lens, starts, blk = [200, 130], [0, 37], 64
+    st = Setup(shape, seed=151, num_slots=6)
+    g = synth.generator(152)
+    dt = synth.normal((shape.hv, shape.dk), 0.5, g)
+    params = LayerParams(st.params.conv_w, st.params.A_log, dt.cuda())
+    oparams = oracle.Params(st.oparams.conv_w, st.oparams.A_log, dt.double().numpy())
+    ids, ck_ids, n_ck, cu, sp = _layout(lens, starts, blk, st.gen, 6)
+    total = int(cu[-1])
+    qkv, _, b = st.tokens((total,))
+    a = synth.normal((total, shape.hv, shape.dk), 1.0, st.gen, shape.act_dtype)
+    a[_zero_rows(lens, cu), :, ::3] = float("inf")
+    ck = _ck_pool(st, n_ck)
+    out = torch.full((total, shape.hv, shape.dv), 3.0, dtype=shape.act_dtype, device="cuda")
+    gdn.kda_prefill(st.dims, st.pool, ck, params, ids.cuda(), cu.cuda(), sp.cuda(), total, ck_ids.cuda(), blk,
+                    qkv.cuda(), a.cuda(), b.cuda(), out)
+    ock = _ock_pool(shape, n_ck)
+    o_ref, err = oracle.kda_prefill(st.od, st.opool, ock, oparams, ids.numpy(), cu.numpy(), sp.numpy(),
+                                    ck_ids.numpy(), blk, to_np(qkv), to_np(a), to_np(b))
+    assert err == 0
+    _check(st, shape, ids, ck, ock, n_ck, out, o_ref, PREFILL_TOL, None, PREFILL_TOL)

@@ -513,6 +513,41 @@ def test_prefill_padding_and_oob():
     assert np.all(ck.ssm == 0)
 
 
+@pytest.mark.parametrize("kda", [False, True])
+def test_prefill_zero_decay_first_token_forgets_the_initial_state(kda):
+    """a = +inf at each sequence's first token (every key channel, for KDA) of
+    the even V heads: g = -inf, alpha = 0, so the state is wiped before the
+    first update and those heads' outputs, final states and checkpoints do not
+    depend on the initial SSM state; the odd heads' outputs (finite gates) do."""
+    shape = synth.TINY
+    d = _dims(shape)
+    lens, starts, blk = [70, 33], [0, 50], 32
+    pool, params, cu, sp, qkv, a, b = _prefill_inputs(shape, 16, lens, starts)
+    if kda:
+        g = synth.generator(17)
+        params = oracle.Params(params.conv_w, params.A_log, synth.normal((d.hv, d.dk), 0.5, g).double().numpy())
+        a = synth.normal((int(cu[-1]), d.hv, d.dk), 1.0, g).double().numpy()
+    a[cu[:-1], ::2] = np.inf
+    ids = np.array([3, 6], np.int32)
+    ck_ids = np.array([[0, 1, 2], [3, 4, 5]], np.int32)
+    run = oracle.kda_prefill if kda else oracle.prefill
+    res = []
+    for ssm_seed in (0, 1):
+        p = pool.copy()
+        p.ssm[ids] = np.random.default_rng(ssm_seed).standard_normal(p.ssm[ids].shape)
+        ck = oracle.Pool(np.zeros((6, d.hv, d.dv, d.dk)), np.zeros((6, d.w - 1, d.channels)))
+        out, err = run(d, p, ck, params, ids, cu, sp, ck_ids, blk, qkv, a, b)
+        assert err == 0 and np.isfinite(out).all()
+        res.append((out, p.ssm[ids], ck.ssm))
+    (o1, s1, c1), (o2, s2, c2) = res
+    np.testing.assert_array_equal(o2[:, ::2], o1[:, ::2])
+    np.testing.assert_array_equal(s2[:, ::2], s1[:, ::2])
+    np.testing.assert_array_equal(c2[:, ::2], c1[:, ::2])
+    # (the odd heads' early outputs; their strong decays leave no trace of the
+    # initial state in the final fp64 state)
+    assert np.abs(o2[:, 1::2] - o1[:, 1::2]).max() > 1e-3
+
+
 # ---- readout epilogue: gated RMS norm ------------------------------------
 
 def test_gated_rmsnorm_hand_worked():
