@@ -654,7 +654,7 @@ def measure_rows(gdn, synth, dev, stream, hbm_peak, bf16_peak, which="all", pref
         rkv["draft_tokens_per_s"] = Bk * Tk / (rkv["ms"] * 1e-3)
         rows["kda_verify_b32_t8"] = rkv
         del kspec
-        # KDA prefill (recurrent form), 4 sequences x 8192 tokens, checkpoints
+        # KDA prefill (the 16-token window form), 4 sequences x 8192 tokens, checkpoints
         # every 256: per token qkv, the per-channel gate logits, beta and out
         nK, SK = 4, 8192
         kt = nK * SK

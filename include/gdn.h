@@ -145,7 +145,8 @@ gdn_status gdn_kda_spec_verify(const gdn_dims* dims, gdn_pool work, gdn_pool spe
  * gdn_kda_decode_step; a [total_tokens][hv][dk], params->dt_bias [hv][dk].
  * fp32 accuracy: dk = 128 with dv <= 128 runs a 16-token chunked form (its
  * products on the tensor cores in split tf32), other shapes the token
- * recurrence.  Needs no workspace; ckpt_block a positive multiple of 64.
+ * recurrence.  A zero decay on a key channel (a = +inf) is exact on both.
+ * Needs no workspace; ckpt_block a positive multiple of 64.
  */
 gdn_status gdn_kda_prefill(const gdn_dims* dims, gdn_pool pool, gdn_pool ckpt,
                            const gdn_params* params, const int32_t* slot_ids,
@@ -194,7 +195,9 @@ gdn_status gdn_spec_commit(const gdn_dims* dims, gdn_pool spec, gdn_pool work,
  * the last W-1 raw inputs) is written to checkpoint slot
  * ckpt_ids[n][P/ckpt_block - floor(start_pos[n]/ckpt_block) - 1] of `ckpt`
  * (-1 or an index >= max_ckpt: skipped).  The intra-chunk work uses chunks
- * of 64 tokens aligned to absolute positions.
+ * of 64 tokens aligned to absolute positions.  A token whose decay is 0
+ * (a = +inf) wipes the state before its update, as in gdn_decode_step; the
+ * chunk form floors each token's log decay at -1000 to keep it exact.
  *   cu_seqlens [n_seq+1] int32 (device): absolute row offsets, non-decreasing,
  *     0 <= cu_seqlens[0], cu_seqlens[n_seq] <= total_tokens (usually 0 and
  *     total_tokens; rows outside them are not written and do not affect the
