@@ -160,7 +160,8 @@ __device__ __forceinline__ float softplus_f(float x) {
 // (log decay -inf: a = +inf, or exp(A_log) * softplus overflowing) would make
 // that -inf - (-inf).  They floor each token's log decay here instead: its
 // exponential is exactly 0 in fp32, so the decay stays 0 and every difference
-// stays finite.  No finite gate of a trained layer comes near it.
+// stays finite.  Any log decay below about -104 already has an fp32
+// exponential of 0, so the floor changes no decay, finite or not.
 constexpr float kLogDecayFloor = -1000.0f;
 __device__ __forceinline__ float floor_log_decay(float g) { return fmaxf(g, kLogDecayFloor); }
 // alpha = exp(-exp(A_log) * softplus(a + dt_bias))
