@@ -445,9 +445,14 @@ def _graph_time(f, n_steps, n_replays, dev):
         return None
 
 
+ROW_GROUPS = ("all", "sweep", "slots", "verify", "prefill", "kda_decode", "kda_verify", "kda_prefill",
+              "mixed", "epilogue")
+
+
 def measure_rows(gdn, synth, dev, stream, hbm_peak, bf16_peak, which="all", prefill_len=8192):
     """Every other row of the hot path, timed with CUDA events (not headline).
-    which = "prefill" times only the chunked prefill (for profiling)."""
+    which: "all", or one group of ROW_GROUPS alone (for profiling one kernel;
+    prefill_len sets the tokens per sequence of both 4-sequence prefills)."""
     import torch
     shape = synth.QWEN
     dims = gdn.Dims.of(shape)
@@ -464,10 +469,12 @@ def measure_rows(gdn, synth, dev, stream, hbm_peak, bf16_peak, which="all", pref
         gbs = nbytes / (ms * 1e-3) / 1e9
         return {"ms": ms, "algorithmic_GBps": gbs, "frac_hbm": gbs / hbm_peak}
 
+    def want(group):
+        return which in ("all", group)
+
     # batch sweep (state rotates over POOL // B disjoint sets where possible)
-    full = which == "all"
     sweep = {}
-    for B in ([1, 2, 4, 8, 16, 32, 64, 128, 256] if full else []):
+    for B in ([1, 2, 4, 8, 16, 32, 64, 128, 256] if want("sweep") else []):
         nsets = max(1, min(8, POOL // B))
         perm = torch.randperm(POOL, generator=g).to(torch.int32)
         sets = [perm[k * B:(k + 1) * B].to(dev) for k in range(nsets)]
@@ -486,14 +493,15 @@ def measure_rows(gdn, synth, dev, stream, hbm_peak, bf16_peak, which="all", pref
         # without the per-call host cost (what a graph-captured serving loop sees)
         r["ms_graph"] = _graph_time(f, 20, 10, dev)
         sweep[str(B)] = r
-    rows["decode_sweep"] = sweep
+    if sweep:
+        rows["decode_sweep"] = sweep
 
     slot_bytes = 2097152 + 49152
     perm = torch.randperm(POOL, generator=g).to(torch.int32)
     pair_sets = [(perm[k * 128:k * 128 + 64].to(dev), perm[k * 128 + 64:(k + 1) * 128].to(dev))
                  for k in range(4)]
 
-    def slot_and_spec_rows():
+    def slot_rows():
         def fc(i):
             s, d = pair_sets[i % 4]
             gdn.slot_copy(dims, pool, pool, s, d)
@@ -505,6 +513,22 @@ def measure_rows(gdn, synth, dev, stream, hbm_peak, bf16_peak, which="all", pref
         fz(0)
         rows["slot_zero_64"] = frac(64 * slot_bytes, _events_time(fz, reps, stream))
 
+        # state pack / unpack of 64 slots through one contiguous staging buffer
+        rec = gdn.state_record_bytes(dims)
+        staging = torch.empty(64 * rec, dtype=torch.uint8, device=dev)
+
+        def fpk(i):
+            gdn.state_pack(dims, pool, pair_sets[i % 4][0], staging)
+        fpk(0)
+        rows["state_pack_64"] = frac(64 * 2 * rec, _events_time(fpk, reps, stream))
+
+        def fup(i):
+            gdn.state_unpack(dims, staging, pool, pair_sets[i % 4][1])
+        fup(0)
+        rows["state_unpack_64"] = frac(64 * 2 * rec, _events_time(fup, reps, stream))
+        del staging
+
+    def spec_rows():
         # speculative verify, batch 16, T = 8, spec cache of 16 x 8 slots, then commit
         B, T = 16, 8
         spec = gdn.StatePool.empty(dims, 4 * B * T, dev)
@@ -542,21 +566,6 @@ def measure_rows(gdn, synth, dev, stream, hbm_peak, bf16_peak, which="all", pref
         rows["spec_commit_index_b16"] = {"ms": ms_i, "ms_graph": _graph_time(fi, 20, 10, dev),
                                          "bytes_moved": B * (T + 1 + 2 * T + 2) * 4}
 
-        # state pack / unpack of 64 slots through one contiguous staging buffer
-        rec = gdn.state_record_bytes(dims)
-        staging = torch.empty(64 * rec, dtype=torch.uint8, device=dev)
-
-        def fpk(i):
-            gdn.state_pack(dims, pool, pair_sets[i % 4][0], staging)
-        fpk(0)
-        rows["state_pack_64"] = frac(64 * 2 * rec, _events_time(fpk, reps, stream))
-
-        def fup(i):
-            gdn.state_unpack(dims, staging, pool, pair_sets[i % 4][1])
-        fup(0)
-        rows["state_unpack_64"] = frac(64 * 2 * rec, _events_time(fup, reps, stream))
-        del staging
-
         # verify at larger batches (T = 8), two alternating request / spec-cache sets
         vsweep = {}
         for Bv in (32, 64, 128):
@@ -579,42 +588,41 @@ def measure_rows(gdn, synth, dev, stream, hbm_peak, bf16_peak, which="all", pref
             torch.cuda.empty_cache()
         rows["spec_verify_sweep_t8"] = vsweep
 
-    if full:
-        slot_and_spec_rows()
+    def prefill_row():
+        # chunked prefill: 4 sequences x prefill_len tokens, checkpoints every 256
+        n_seq, S = 4, prefill_len
+        total = n_seq * S
+        qkv, a, b = (t.to(dev) for t in synth.tokens(shape, g, (total,)))
+        cu = torch.arange(0, total + 1, S, dtype=torch.int32, device=dev)
+        sp = torch.zeros(n_seq, dtype=torch.int64, device=dev)
+        n_ck = S // 256
+        ck = gdn.StatePool.empty(dims, 4 * n_ck, dev)
+        ck_ids = torch.arange(4 * n_ck, dtype=torch.int32, device=dev).reshape(4, n_ck)
+        pout = torch.empty((total, 32, 128), dtype=torch.bfloat16, device=dev)
+        wsb = gdn.chunk_prefill_workspace_size(dims, n_seq, total)
+        wsp = torch.empty(wsb, dtype=torch.uint8, device=dev)
+        pids = [perm[k * 4:(k + 1) * 4].to(dev) for k in range(4)]
 
-    # chunked prefill: 4 sequences x prefill_len tokens, checkpoints every 256
-    n_seq, S = 4, prefill_len
-    total = n_seq * S
-    qkv, a, b = (t.to(dev) for t in synth.tokens(shape, g, (total,)))
-    cu = torch.arange(0, total + 1, S, dtype=torch.int32, device=dev)
-    sp = torch.zeros(n_seq, dtype=torch.int64, device=dev)
-    n_ck = S // 256
-    ck = gdn.StatePool.empty(dims, 4 * n_ck, dev)
-    ck_ids = torch.arange(4 * n_ck, dtype=torch.int32, device=dev).reshape(4, n_ck)
-    pout = torch.empty((total, 32, 128), dtype=torch.bfloat16, device=dev)
-    wsb = gdn.chunk_prefill_workspace_size(dims, n_seq, total)
-    wsp = torch.empty(wsb, dtype=torch.uint8, device=dev)
-    pids = [perm[k * 4:(k + 1) * 4].to(dev) for k in range(4)]
+        def fp(i):
+            gdn.chunk_prefill(dims, pool, ck, params, pids[i % 4], cu, sp, total, ck_ids, 256, qkv, a,
+                              b, pout, wsp)
+        fp(0)
+        pms = _events_time(fp, 5, stream)
+        # qkv, a, b and out per token; checkpoints plus each sequence's state read and written
+        pbytes = total * (16384 + 128 + 8192) + (4 * n_ck + 8) * slot_bytes
+        # ~11.7 MFLOP per (64-token chunk, V head) for the chunk form
+        pflop = total / 64 * 32 * 11.7e6
+        rows[f"chunk_prefill_4x{S}"] = {
+            "ms": pms, "tokens_per_s": total / (pms * 1e-3),
+            "algorithmic_GBps": pbytes / (pms * 1e-3) / 1e9,
+            "frac_hbm": pbytes / (pms * 1e-3) / 1e9 / hbm_peak,
+            "TFLOPs": pflop / (pms * 1e-3) / 1e12,
+            "frac_bf16_peak": pflop / (pms * 1e-3) / 1e12 / bf16_peak,
+            "workspace_bytes": wsb}
+        del qkv, a, b, pout, wsp
+        torch.cuda.synchronize()
 
-    def fp(i):
-        gdn.chunk_prefill(dims, pool, ck, params, pids[i % 4], cu, sp, total, ck_ids, 256, qkv, a,
-                          b, pout, wsp)
-    fp(0)
-    pms = _events_time(fp, 5, stream)
-    # qkv, a, b and out per token; checkpoints plus each sequence's state read and written
-    pbytes = total * (16384 + 128 + 8192) + (4 * n_ck + 8) * slot_bytes
-    # ~11.7 MFLOP per (64-token chunk, V head) for the chunk form
-    pflop = total / 64 * 32 * 11.7e6
-    rows[f"chunk_prefill_4x{S}"] = {
-        "ms": pms, "tokens_per_s": total / (pms * 1e-3),
-        "algorithmic_GBps": pbytes / (pms * 1e-3) / 1e9,
-        "frac_hbm": pbytes / (pms * 1e-3) / 1e9 / hbm_peak,
-        "TFLOPs": pflop / (pms * 1e-3) / 1e12,
-        "frac_bf16_peak": pflop / (pms * 1e-3) / 1e12 / bf16_peak,
-        "workspace_bytes": wsb}
-    del qkv, a, b, pout, wsp
-    torch.cuda.synchronize()
-    if full:
+    def kda_rows():
         # KDA decode, batch 64: the per-channel gate logits replace the per-head
         # ones (+ 32 x 128 x 2 bytes per token) and dt_bias is per channel
         kp = gdn.LayerParams(params.conv_w, params.A_log,
@@ -628,12 +636,19 @@ def measure_rows(gdn, synth, dev, stream, hbm_peak, bf16_peak, which="all", pref
         def fk(i):
             q, ka, kb = kin[i % 8]
             gdn.kda_decode_step(dims, pool, kp, ksets[i % 8], q, ka, kb, kout)
-        fk(0)
-        kbytes = 64 * (DECODE_TOKEN_BYTES - 2 * 32 * 2 + 32 * 128 * 2 + 32 * 2) + DECODE_STEP_PARAM_BYTES \
-            + 32 * 128 * 4
-        rk = frac(kbytes, _events_time(fk, reps, stream))
-        rk["tokens_per_s"] = 64 / (rk["ms"] * 1e-3)
-        rows["kda_decode_b64"] = rk
+        if want("kda_decode"):
+            fk(0)
+            kbytes = 64 * (DECODE_TOKEN_BYTES - 2 * 32 * 2 + 32 * 128 * 2 + 32 * 2) \
+                + DECODE_STEP_PARAM_BYTES + 32 * 128 * 4
+            rk = frac(kbytes, _events_time(fk, reps, stream))
+            rk["tokens_per_s"] = 64 / (rk["ms"] * 1e-3)
+            rows["kda_decode_b64"] = rk
+        if want("kda_verify"):
+            kda_verify_row(kp)
+        if want("kda_prefill"):
+            kda_prefill_row(kp)
+
+    def kda_verify_row(kp):
         # KDA verify, batch 32, T = 8, snapshots into a separate spec pool
         Bk, Tk = 32, 8
         kspec = gdn.StatePool.empty(dims, 2 * Bk * Tk, dev)
@@ -654,9 +669,11 @@ def measure_rows(gdn, synth, dev, stream, hbm_peak, bf16_peak, which="all", pref
         rkv["draft_tokens_per_s"] = Bk * Tk / (rkv["ms"] * 1e-3)
         rows["kda_verify_b32_t8"] = rkv
         del kspec
-        # KDA prefill (the 16-token window form), 4 sequences x 8192 tokens, checkpoints
-        # every 256: per token qkv, the per-channel gate logits, beta and out
-        nK, SK = 4, 8192
+
+    def kda_prefill_row(kp):
+        # KDA prefill (the 16-token window form), 4 sequences x prefill_len tokens,
+        # checkpoints every 256: per token qkv, the per-channel gate logits, beta and out
+        nK, SK = 4, prefill_len
         kt = nK * SK
         kpq = synth.tokens(shape, g, (kt,))
         kpin = (kpq[0].to(dev), synth.normal((kt, shape.hv, shape.dk), 1.0, g, shape.act_dtype).to(dev),
@@ -677,7 +694,8 @@ def measure_rows(gdn, synth, dev, stream, hbm_peak, bf16_peak, which="all", pref
         rkp["tokens_per_s"] = kt / (rkp["ms"] * 1e-3)
         rows[f"kda_prefill_{nK}x{SK}"] = rkp
         del kpin, kck, kpo
-        rows["mixed_b64_plus_4x256"] = _mixed_row(gdn, synth, dims, pool, params, perm, g, dev, stream)
+
+    def epilogue_row():
         # readout epilogue over a 4 x 8192-token prefill output: o and z read,
         # y written in place (3 x 256 bytes per (token, V head) row)
         n_tok = 32768
@@ -691,6 +709,19 @@ def measure_rows(gdn, synth, dev, stream, hbm_peak, bf16_peak, which="all", pref
         rows["gated_rmsnorm_32768_tokens"] = frac(3 * n_tok * shape.hv * shape.dv * 2,
                                                   _events_time(fe, 20, stream))
         del eo, ez
+
+    if want("slots"):
+        slot_rows()
+    if want("verify"):
+        spec_rows()
+    if want("prefill"):
+        prefill_row()
+    if want("kda_decode") or want("kda_verify") or want("kda_prefill"):
+        kda_rows()
+    if want("mixed"):
+        rows["mixed_b64_plus_4x256"] = _mixed_row(gdn, synth, dims, pool, params, perm, g, dev, stream)
+    if want("epilogue"):
+        epilogue_row()
     return rows
 
 
@@ -736,10 +767,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-rows", action="store_true", help="headline only")
-    ap.add_argument("--rows", default="all", choices=["all", "prefill"],
-                    help="which secondary rows to time (prefill: the chunked prefill alone)")
+    ap.add_argument("--rows", default="all", choices=list(ROW_GROUPS),
+                    help="which secondary rows to time: all, or one group alone (for profiling)")
     ap.add_argument("--prefill-len", type=int, default=8192,
-                    help="tokens per sequence of the 4-sequence prefill row (multiple of 256)")
+                    help="tokens per sequence of the 4-sequence GDN and KDA prefill rows (multiple of 256)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-soak", action="store_true",
                     help="skip the untimed 1 s warm loop that gives the clock sampler a window")

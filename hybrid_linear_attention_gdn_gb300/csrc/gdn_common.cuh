@@ -158,12 +158,17 @@ __device__ __forceinline__ float softplus_f(float x) {
 // The chunked forms take the decay between tokens j and t as
 // exp(b_t - b_j), with b the cumulative log decay.  A token whose decay is 0
 // (log decay -inf: a = +inf, or exp(A_log) * softplus overflowing) would make
-// that -inf - (-inf).  They floor each token's log decay here instead: its
-// exponential is exactly 0 in fp32, so the decay stays 0 and every difference
-// stays finite.  Any log decay below about -104 already has an fp32
-// exponential of 0, so the floor changes no decay, finite or not.
-constexpr float kLogDecayFloor = -1000.0f;
-__device__ __forceinline__ float floor_log_decay(float g) { return fmaxf(g, kLogDecayFloor); }
+// that -inf - (-inf).  They floor each token's log decay here instead.  At
+// -128 the exponential is exactly 0 in fp32 (expf underflows below about
+// -104, and 2^x on ex2.approx.ftz flushes below about -87), so the decay
+// stays 0 and every difference stays finite; any log decay below -104
+// already has an exponential of 0, so the floor changes no finite decay.  A
+// floor this close to the underflow keeps the cumulative sums after a floored
+// token small, where fp32 still resolves their differences finely.  The
+// comparison lets NaN through (fmaxf would turn it into the floor), so a NaN
+// gate poisons the state exactly as the token recurrence does.
+constexpr float kLogDecayFloor = -128.0f;
+__device__ __forceinline__ float floor_log_decay(float g) { return g < kLogDecayFloor ? kLogDecayFloor : g; }
 // alpha = exp(-exp(A_log) * softplus(a + dt_bias))
 __device__ __forceinline__ float gate_alpha(float A_log, float dt_bias, float a) {
   return expf(-expf(A_log) * softplus_f(a + dt_bias));

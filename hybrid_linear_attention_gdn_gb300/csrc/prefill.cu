@@ -28,7 +28,6 @@
 
 #include <cstdlib>
 #include <cstring>
-#include <mutex>
 
 namespace gdn {
 namespace {
@@ -685,24 +684,14 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[GDN_NOALLOC_SCR
 namespace gdn {
 namespace {
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device.  In host code
-// the array's name only stands for the symbol; the address is looked up once
-// per device, with that device current.
+// Device address of the scratch array in the current device's context.  In
+// host code the array's name only stands for the symbol; its address is
+// looked up on every call (a cheap query next to a prefill), so it stays
+// right after a device reset or in another context.
 gdn_status noalloc_scratch(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return GDN_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return GDN_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return GDN_ERR_CUDA;
+  *out = p;
   return GDN_OK;
 }
 

@@ -239,9 +239,11 @@ gdn_status gdn_chunk_prefill(const gdn_dims* dims, gdn_pool pool, gdn_pool ckpt,
  * longer prefill into several calls - the state carries over in the slot.
  *  - A call whose gdn_chunk_prefill_workspace_size(...) exceeds the scratch
  *    returns GDN_ERR_SCRATCH_LIMIT and launches nothing.
- *  - The first call on a device looks up the scratch's device address
- *    (cudaGetSymbolAddress, with that device current); make that first call
- *    before any stream capture.
+ *  - Every call looks up the scratch's device address in the current
+ *    device's context (cudaGetSymbolAddress), so a device reset or another
+ *    context needs nothing from the caller.  The first call on a device also
+ *    loads the library's device code there; make that first call before any
+ *    stream capture.
  *  - Every call on a device shares the one buffer and finds the previous
  *    call's contents in it.  Nothing in it needs to start at zero: each call
  *    writes what it later reads.  Calls that can overlap on the GPU (streams

@@ -9,7 +9,7 @@ import torch
 import hybrid_linear_attention_gdn_gb300 as gdn
 import oracle
 from hybrid_linear_attention_gdn_gb300 import LayerParams, synth
-from helpers import (STATE_TOL_1, STATE_TOL_64, Setup, assert_out_close, conv_bits_equal, max_rel_l2,
+from helpers import (STATE_TOL_1, STATE_TOL_64, Setup, state_tol, assert_out_close, conv_bits_equal, max_rel_l2,
                      out_tol, to_np)
 
 pytestmark = pytest.mark.gpu
@@ -154,7 +154,9 @@ def test_kda_verify_vs_oracle(cuda, monkeypatch, shape, B, T, path):
     assert torch.equal(st.pool.ssm, before[0]) and torch.equal(st.pool.conv, before[1])
     assert_out_close(out, o_ref, shape.dv, out_tol(shape))
     sids = spec_ids.flatten().tolist()
-    assert max_rel_l2(to_np(spec.ssm[sids]), ospec.ssm[sids], shape.dv * shape.dk) <= STATE_TOL_1 * 5
+    for t in range(T):  # snapshot t: the state after t + 1 steps
+        st_ids = spec_ids[:, t].tolist()
+        assert max_rel_l2(to_np(spec.ssm[st_ids]), ospec.ssm[st_ids], shape.dv * shape.dk) <= state_tol(t + 1), t
     assert conv_bits_equal(spec.conv[sids], ospec.conv[sids])
     unused = [s for s in range(n_spec) if s not in sids]
     assert torch.all(spec.ssm[unused] == 12345.5)
@@ -188,5 +190,7 @@ def test_kda_verify_in_place_then_commit_index(cuda):
                                    to_np(a[r:r + 1, t]), to_np(b[r:r + 1, t]))
     torch.cuda.synchronize()
     new = d_slots.cpu().tolist()
-    assert max_rel_l2(to_np(st.pool.ssm[new]), ref.ssm[ids.tolist()], shape.dv * shape.dk) <= STATE_TOL_1 * 5
+    for r in range(B):
+        assert max_rel_l2(to_np(st.pool.ssm[new[r]]), ref.ssm[int(ids[r])],
+                          shape.dv * shape.dk) <= state_tol(int(L[r]))
     assert conv_bits_equal(st.pool.conv[new], ref.conv[ids.tolist()])

@@ -8,7 +8,7 @@ import torch
 import hybrid_linear_attention_gdn_gb300 as gdn
 import oracle
 from hybrid_linear_attention_gdn_gb300 import synth
-from helpers import STATE_TOL_1, Setup, assert_pool_bits_equal, conv_bits_equal, max_rel_l2, to_np
+from helpers import Setup, assert_pool_bits_equal, conv_bits_equal, max_rel_l2, state_tol, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -99,8 +99,9 @@ def test_verify_in_place_then_commit_index(cuda, monkeypatch, B, T, path):
             oracle.decode_step(st.od, ref, st.oparams, ids[r:r + 1].numpy(),
                                to_np(qkv[r:r + 1, t]), to_np(a[r:r + 1, t]), to_np(b[r:r + 1, t]))
     new = ref_slots.tolist()
-    assert max_rel_l2(to_np(st.pool.ssm[new]), ref.ssm[ids.tolist()],
-                      shape.dv * shape.dk) <= STATE_TOL_1 * 5
+    for r in range(B):
+        assert max_rel_l2(to_np(st.pool.ssm[new[r]]), ref.ssm[int(ids[r])],
+                          shape.dv * shape.dk) <= state_tol(int(L[r]))
     assert conv_bits_equal(st.pool.conv[new], ref.conv[ids.tolist()])
     # every slot the request held is either its new working slot or freed
     held = torch.cat([ids[:, None], spec_ids], 1)

@@ -7,8 +7,8 @@ import torch
 import hybrid_linear_attention_gdn_gb300 as gdn
 import oracle
 from hybrid_linear_attention_gdn_gb300 import StatePool, synth
-from helpers import (assert_out_close, STATE_TOL_1, Setup, assert_pool_bits_equal, conv_bits_equal, max_rel_l2,
-                     out_tol, to_np)
+from helpers import (assert_out_close, Setup, assert_pool_bits_equal, conv_bits_equal, max_rel_l2, out_tol,
+                     state_tol, to_np)
 
 pytestmark = pytest.mark.gpu
 
@@ -62,7 +62,11 @@ def test_verify_then_commit(cuda, monkeypatch, shape, B, T, path):
     assert torch.equal(st.pool.ssm, work_before[0]) and torch.equal(st.pool.conv, work_before[1])
     assert_out_close(out, o_ref, shape.dv, out_tol(shape))
     sids = spec_ids.flatten().tolist()
-    assert max_rel_l2(to_np(spec.ssm[sids]), ospec.ssm[sids], shape.dv * shape.dk) <= STATE_TOL_1 * 5
+    # snapshot t holds the state after t + 1 steps: snapshot 0 is one step
+    # from the working state (the one-step bound), the others at most T <= 64
+    for t in range(T):
+        st_ids = spec_ids[:, t].tolist()
+        assert max_rel_l2(to_np(spec.ssm[st_ids]), ospec.ssm[st_ids], shape.dv * shape.dk) <= state_tol(t + 1), t
     assert conv_bits_equal(spec.conv[sids], ospec.conv[sids])
     # unused spec slots keep their sentinel bytes
     unused = [s for s in range(B * T + 3) if s not in sids]
@@ -85,8 +89,10 @@ def test_verify_then_commit(cuda, monkeypatch, shape, B, T, path):
         for t in range(int(L[r])):
             oracle.decode_step(st.od, ref, st.oparams, ids[r:r + 1].numpy(), to_np(qkv[r:r + 1, t]),
                                to_np(a[r:r + 1, t]), to_np(b[r:r + 1, t]))
+    for r in range(B):
+        s_ = int(ids[r])
+        assert max_rel_l2(to_np(st.pool.ssm[s_]), ref.ssm[s_], shape.dv * shape.dk) <= state_tol(int(L[r]))
     used = ids.tolist()
-    assert max_rel_l2(to_np(st.pool.ssm[used]), ref.ssm[used], shape.dv * shape.dk) <= STATE_TOL_1 * 5
     assert conv_bits_equal(st.pool.conv[used], ref.conv[used])
 
 

@@ -16,7 +16,7 @@ import torch
 
 import hybrid_linear_attention_gdn_gb300 as gdn
 from hybrid_linear_attention_gdn_gb300 import StatePool, binding, synth
-from helpers import PREFILL_TOL, Setup, assert_out_close, max_rel_l2, to_np
+from helpers import Setup
 
 pytestmark = pytest.mark.gpu
 
@@ -60,12 +60,12 @@ def test_noalloc_matches_workspace_prefill_on_two_calls(cuda):
                                   256, qkv, a, b, out_noa, err)
         torch.cuda.synchronize()
         assert int(err.item()) == 0
-        assert_out_close(out_noa, to_np(out_ref), 128, PREFILL_TOL)
-        used = ids.tolist()
-        assert max_rel_l2(to_np(noa.pool.ssm[used]), to_np(ref.pool.ssm[used]), 128) <= PREFILL_TOL
-        assert torch.equal(noa.pool.conv, ref.pool.conv)
-        assert max_rel_l2(to_np(ck_noa.ssm), to_np(ck_ref.ssm), 128) <= PREFILL_TOL
-        assert torch.equal(ck_noa.conv, ck_ref.conv)
+        # the same deterministic kernels on the same inputs: bit for bit
+        assert torch.equal(out_noa.view(torch.int16), out_ref.view(torch.int16))
+        assert torch.equal(noa.pool.ssm.view(torch.int32), ref.pool.ssm.view(torch.int32))
+        assert torch.equal(noa.pool.conv.view(torch.int16), ref.pool.conv.view(torch.int16))
+        assert torch.equal(ck_noa.ssm.view(torch.int32), ck_ref.ssm.view(torch.int32))
+        assert torch.equal(ck_noa.conv.view(torch.int16), ck_ref.conv.view(torch.int16))
     assert binding.launch_count(binding.K_PREFILL) == n0 + 4
 
 
