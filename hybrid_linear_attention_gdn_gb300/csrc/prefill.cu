@@ -485,13 +485,19 @@ cudaError_t launch_history(const PrefillArgs& a, int act, int cv, cudaStream_t s
   return launch_plain(history_kernel<__nv_bfloat16, float>, grid, dim3(kThreads), 0, s, dim3(1), a);
 }
 
-// The tensor-core path takes dk = dv = 128, width 4; GDN_PREFILL_PATH=cuda
-// forces the fp32 CUDA-core path (read on every call, so a process can time
-// or test both).
-bool use_tc_prefill(const gdn_dims& d, const void* qkv, const void* out, const gdn_params& p) {
+// Prefill paths.  The tf32 tensor-core path takes dk = dv = 128, width 4,
+// bf16 activations and conv history; every other shape runs the fp32
+// CUDA-core path.  GDN_PREFILL_PATH (read on every call, so a process can
+// time or test each) forces one: "cuda" the CUDA-core path, "bf16" the
+// tensor-core path with bf16 operands (dk = dv = 128, width 4), whose operand
+// roundings put its outputs above the 2e-3 the tf32 path meets.
+enum class PrefillPath { kCuda, kTf32, kBf16 };
+PrefillPath prefill_path(const gdn_dims& d, const void* qkv, const void* out, const gdn_params& p) {
   const char* e = std::getenv("GDN_PREFILL_PATH");
-  const bool forced_cuda = e && !std::strcmp(e, "cuda");
-  return !forced_cuda && prefill_tc_supported(d, qkv, out, p);
+  if (e && !std::strcmp(e, "cuda")) return PrefillPath::kCuda;
+  if (e && !std::strcmp(e, "bf16"))
+    return prefill_tc_supported(d, qkv, out, p) ? PrefillPath::kBf16 : PrefillPath::kCuda;
+  return prefill_tc32_supported(d, qkv, out, p) ? PrefillPath::kTf32 : PrefillPath::kCuda;
 }
 
 }  // namespace
@@ -563,9 +569,11 @@ static gdn_status chunk_prefill_impl(bool launch, const gdn_dims* dims, gdn_pool
     return GDN_ERR_INVALID_ARG;
   if (total_tokens > 0 && (!qkv || !a || !b || !out)) return GDN_ERR_INVALID_ARG;
   const WsLayout wl = ws_layout(*dims, total_tokens);
-  const bool tc = use_tc_prefill(*dims, qkv, out, *params);
-  const size_t need = tc ? prefill_tc_workspace(*dims, n_seq, total_tokens) : wl.total;
-  if (total_tokens > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
+  const PrefillPath path = prefill_path(*dims, qkv, out, *params);
+  const size_t need = path == PrefillPath::kTf32   ? 0
+                      : path == PrefillPath::kBf16 ? prefill_tc_workspace(*dims, n_seq, total_tokens)
+                                                   : wl.total;
+  if (total_tokens > 0 && need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
     return GDN_ERR_INVALID_ARG;
   if (dims->hv / dims->hk * dims->dv + 2 * dims->dk > 4096) return GDN_ERR_UNSUPPORTED;
   if (!launch) return GDN_OK;
@@ -592,12 +600,13 @@ static gdn_status chunk_prefill_impl(bool launch, const gdn_dims* dims, gdn_pool
   p.b = b;
   p.out = out;
   p.err = dev_err;
-  char* ws = reinterpret_cast<char*>(workspace);
-  p.ws_q = reinterpret_cast<float*>(ws + wl.q);
-  p.ws_k = reinterpret_cast<float*>(ws + wl.k);
-  p.ws_v = reinterpret_cast<float*>(ws + wl.v);
-  p.ws_g = reinterpret_cast<float*>(ws + wl.g);
-  p.ws_beta = reinterpret_cast<float*>(ws + wl.beta);
+  if (char* ws = reinterpret_cast<char*>(workspace)) {  // the tf32 path needs none (may be null)
+    p.ws_q = reinterpret_cast<float*>(ws + wl.q);
+    p.ws_k = reinterpret_cast<float*>(ws + wl.k);
+    p.ws_v = reinterpret_cast<float*>(ws + wl.v);
+    p.ws_g = reinterpret_cast<float*>(ws + wl.g);
+    p.ws_beta = reinterpret_cast<float*>(ws + wl.beta);
+  }
   p.hk = dims->hk;
   p.hv = dims->hv;
   p.dk = dims->dk;
@@ -608,7 +617,11 @@ static gdn_status chunk_prefill_impl(bool launch, const gdn_dims* dims, gdn_pool
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaErrorInvalidValue;
   const int act = dims->act_dtype, cv = dims->conv_dtype;
-  if (tc) {
+  if (path == PrefillPath::kTf32) {
+    e = prefill_tc32_launch(*dims, pool, ckpt, *params, slot_ids, cu_seqlens, start_pos, n_seq, total_tokens,
+                            ckpt_ids, max_ckpt, ckpt_block, qkv, a, b, out, dev_err, s);
+    if (e == cudaSuccess) e = launch_history(p, act, cv, s);
+  } else if (path == PrefillPath::kBf16) {
     e = prefill_tc_launch(*dims, pool, ckpt, *params, slot_ids, cu_seqlens, start_pos, n_seq,
                           total_tokens, ckpt_ids, max_ckpt, ckpt_block, qkv, a, b, out, workspace,
                           dev_err, s);

@@ -1,4 +1,5 @@
-// Tensor-core (tcgen05) chunked prefill for dk = dv = 128; see prefill_tc.cu.
+// Tensor-core (tcgen05) chunked prefills for dk = dv = 128: bf16 operands
+// (prefill_tc.cu) and tf32 operands (prefill_tc32.cu).
 #pragma once
 #include "gdn_common.cuh"
 
@@ -11,6 +12,15 @@ cudaError_t prefill_tc_launch(const gdn_dims& d, const gdn_pool& pool, const gdn
                               const int32_t* ckpt_ids, int32_t max_ckpt, int32_t ckpt_block,
                               const void* qkv, const void* a, const void* b, void* out,
                               void* workspace, uint32_t* dev_err, cudaStream_t s);
+// The same chunk form with every product in tf32 and the features computed in
+// the chain (prefill_tc32.cu): dk = dv = 128, width 4, bf16 activations and
+// conv history.  Needs no workspace.
+bool prefill_tc32_supported(const gdn_dims& d, const void* qkv, const void* out, const gdn_params& p);
+cudaError_t prefill_tc32_launch(const gdn_dims& d, const gdn_pool& pool, const gdn_pool& ckpt, const gdn_params& p,
+                                const int32_t* slot_ids, const int32_t* cu_seqlens, const int64_t* start_pos,
+                                int32_t n_seq, int64_t total, const int32_t* ckpt_ids, int32_t max_ckpt,
+                                int32_t ckpt_block, const void* qkv, const void* a, const void* b, void* out,
+                                uint32_t* dev_err, cudaStream_t s);
 // conv histories of a prefill's checkpoints and final state (prefill.cu)
 cudaError_t conv_history_launch(const gdn_dims& d, const gdn_pool& pool, const gdn_pool& ckpt,
                                 const int32_t* slot_ids, const int32_t* cu_seqlens, const int64_t* start_pos,

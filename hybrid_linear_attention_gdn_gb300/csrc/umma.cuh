@@ -1,6 +1,7 @@
 // tcgen05 (5th-generation tensor core) helpers: shared-memory matrix
-// descriptors, the kind::f16 instruction descriptor, MMA issue/commit, TMEM
-// allocation and loads.  Inline PTX only.
+// descriptors, the kind::f16 and kind::tf32 instruction descriptors, MMA
+// issue/commit (operand A from shared memory or from TMEM), TMEM allocation,
+// loads and stores.  Inline PTX only.
 //
 // Shared-memory operand layouts used here (bf16, 128-byte swizzle):
 //  * K-major tile, R rows x 64 K: row r at (r/8)*1024 + (r%8)*128 bytes, its
@@ -11,6 +12,8 @@
 //    elements of one k; wider MN uses further 64-wide atoms at the descriptor's
 //    leading byte offset.  One MMA k-step (16 rows) advances the start by 2048.
 // Both forms (and M = 128, N = 64..256) were checked against a CPU GEMM.
+// An fp32 (tf32) tile uses the same bytes: a 128-byte row holds 32 elements,
+// and one tf32 k-step (8 elements) is the same 32 bytes.
 #pragma once
 #include <stdint.h>
 
@@ -49,6 +52,41 @@ __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
       "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)accumulate)
       : "memory");
+}
+
+// kind::tf32 instruction descriptor: tf32 A and B (fp32 containers; the
+// tensor core reads their top 19 bits), fp32 D.
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D (TMEM) (+)= A B, A and B from shared-memory descriptors, kind::tf32 (K = 8)
+__device__ __forceinline__ void mma_tf32(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
+                                         bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+// D (TMEM) (+)= A B with A in TMEM (M rows = lanes, K = 8 consecutive fp32
+// columns from tmem_a) and B from a shared-memory descriptor, kind::tf32
+__device__ __forceinline__ void mma_tf32_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc,
+                                            bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(b), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+
+// fp32 rounded to tf32 (10 explicit mantissa bits, nearest, ties away from
+// zero), as an fp32 bit pattern whose low 13 bits are zero
+__device__ __forceinline__ float tf32_round(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;\n" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
 }
 
 // Arrive on `bar` once every MMA issued so far by this thread has completed.
@@ -98,6 +136,28 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane, written; returns
+// once the writes are done (the caller still fences before other threads or
+// the tensor core read them)
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
 }
 
 // byte offset of element (row, col) in a K-major / MN-major 128B-swizzled tile

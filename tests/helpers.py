@@ -6,10 +6,15 @@ Tolerances (stated by the workload definition): bf16 outputs relative-L2
 
 Outputs: the stated relative-L2 bound applies to the output tensor of a call
 (against the exact result) and to every row (one token and V head).  A row is
-compared with the exact result rounded to the output format (RNE), the value
-a correct kernel returns: rounding alone moves a bf16 row by up to 2^-8 of
-relative L2, more than the bound, so the exact row itself is not a target any
-output format can meet.
+held to the bound beyond the error of its correctly rounded value: rounding
+the exact row to the output format (RNE) already moves a bf16 row by up to
+2^-8 of relative L2, and a kernel whose arithmetic is off by far less than a
+unit in the last place still rounds a value that lies near a rounding
+midpoint to the other neighbour (measured: up to 3e-3 on one row of a
+batch-64 decode step whose fp32 arithmetic is exact to ~1e-6), so neither the
+exact row nor its rounded value is a target any output format can meet.
+What the check bounds is ||x - ref|| - ||round(ref) - ref||, the error the
+kernel adds to the unavoidable rounding.
 State: relative L2 per (slot, head) matrix, maximum over them.
 """
 import numpy as np
@@ -23,42 +28,46 @@ OUT_TOL_F32 = 1e-4
 STATE_TOL_1 = 1e-4
 STATE_TOL_64 = 5e-4
 PREFILL_TOL = 2e-3
-# Tensor-core prefill (dk = dv = 128): the workload fixes its intra-chunk
-# WY/UT contractions as bf16 products with fp32 accumulation, which puts the
-# error of exact bf16-operand arithmetic above the 2e-3 stated for bf16
-# outputs.  The bounds come from a float64 model of the chunk form with the
-# same operand roundings (tests/test_prefill_tolerance_model.py; 12 V heads x
-# 4096 tokens on the workload's distributions):
-#   output tensor relative L2: model 4.0e-3 -> 5e-3.  Five roundings of ~1.6e-3
-#     each (q^/k^, v, T, the masked Q K^T, Delta) plus the output's own.
-#   worst output row (RMS-floored): model 1.1e-2 -> 1.5e-2.  The rounding of q^
-#     moves a whole row coherently (the row is S q^, its error S dq^), so rows
-#     have a heavier tail than the output rounding alone gives.
-#   worst state / checkpoint matrix: model 5.8e-3 over 192 matrices -> 1e-2.
-#     The state is dominated by the last few tokens' rank-one terms, so it
-#     averages the roundings over few terms.
-PREFILL_TC_TOL = 5e-3
-PREFILL_TC_ROW_TOL = 1.5e-2
-PREFILL_TC_STATE_TOL = 1e-2
+# The tensor-core prefill with bf16 operands (GDN_PREFILL_PATH=bf16), the
+# literal reading of "intra-chunk WY/UT transform as dense bf16 contractions":
+# every bf16 operand rounding adds about 1.5e-3 of relative L2 to the output,
+# on top of the output's own 1.7e-3, so it cannot meet the 2e-3 stated for
+# bf16 outputs.  Its bounds come from a float64 model of the chunk form with
+# the same operand roundings (tests/test_prefill_tolerance_model.py):
+#   output tensor: model 4.0e-3 -> 5e-3
+#   worst row excess over its rounding (RMS-floored): model 7.2e-3 -> 1.5e-2
+#   worst state / checkpoint matrix: model up to 5.8e-3 -> 1e-2
+# The default tensor-core prefill (tf32 operands) is held to the stated 2e-3
+# on all of these (model: 1.7e-3, 9.1e-4, 5.5e-4).
+PREFILL_BF16_TOL = 5e-3
+PREFILL_BF16_ROW_TOL = 1.5e-2
+PREFILL_BF16_STATE_TOL = 1e-2
 
 
-def uses_tc_prefill(shape, path="tc") -> bool:
-    """The tensor-core path runs dk = dv = 128, width 4 unless the fp32
-    CUDA-core path is forced; other shapes always run the CUDA-core path."""
-    return path == "tc" and shape.dk == 128 and shape.dv == 128 and shape.w == 4
+def prefill_kind(shape, path="tc") -> str:
+    """Which prefill runs: "tf32" (tensor cores; dk = dv = 128, width 4, bf16
+    activations and conv history), "bf16" (tensor cores with bf16 operands,
+    forced by path "bf16" where dk = dv = 128, width 4) or "cuda" (fp32 CUDA
+    cores: every other shape, or path "cuda")."""
+    tc_shape = shape.dk == 128 and shape.dv == 128 and shape.w == 4
+    if path == "cuda":
+        return "cuda"
+    if path == "bf16":
+        return "bf16" if tc_shape else "cuda"
+    return "tf32" if tc_shape and shape.act == "bf16" and shape.conv == "bf16" else "cuda"
 
 
 def prefill_tol(shape, path="tc") -> float:
-    return PREFILL_TC_TOL if uses_tc_prefill(shape, path) else PREFILL_TOL
+    return PREFILL_BF16_TOL if prefill_kind(shape, path) == "bf16" else PREFILL_TOL
 
 
 def prefill_state_tol(shape, path="tc") -> float:
-    return PREFILL_TC_STATE_TOL if uses_tc_prefill(shape, path) else PREFILL_TOL
+    return PREFILL_BF16_STATE_TOL if prefill_kind(shape, path) == "bf16" else PREFILL_TOL
 
 
 def prefill_row_tol(shape, path="tc"):
-    """Per-row bound for assert_out_close (None: the default reading)."""
-    return PREFILL_TC_ROW_TOL if uses_tc_prefill(shape, path) else None
+    """Per-row bound for assert_out_close (None: the stated bound)."""
+    return PREFILL_BF16_ROW_TOL if prefill_kind(shape, path) == "bf16" else None
 
 
 def out_tol(shape) -> float:
@@ -97,13 +106,13 @@ def round_like(ref, dtype: torch.dtype) -> np.ndarray:
 def assert_out_close(out: torch.Tensor, ref, row: int, tol: float, row_floor_rms: bool = False,
                      row_tol: float | None = None):
     """Output check described in the module docstring: the tensor against the
-    exact result, each row against the exact row rounded to the output format.
-    row_floor_rms (the chunked prefills, whose tensor-core operands are
-    rounded, so their error is absolute in scale): a row's error beyond its own
-    rounding, ||x - ref|| - ||round(ref) - ref||, is measured against
-    max(its norm, the RMS row norm of the tensor) - a row whose exact value is
-    thousands of times below the typical row gets the typical absolute error,
-    not a proportionally smaller one.  row_tol replaces tol for the rows."""
+    exact result; each row's error beyond its own rounding,
+    ||x - ref|| - ||round(ref) - ref||, against its norm.  row_floor_rms (the
+    chunked prefills, whose tensor-core operands are rounded, so their error is
+    absolute in scale): that excess is measured against max(its norm, the RMS
+    row norm of the tensor) - a row whose exact value is thousands of times
+    below the typical row gets the typical absolute error, not a
+    proportionally smaller one.  row_tol replaces tol for the rows."""
     x = to_np(out)
     ref = np.asarray(ref, np.float64)
     den = np.linalg.norm(ref)
@@ -114,15 +123,14 @@ def assert_out_close(out: torch.Tensor, ref, row: int, tol: float, row_floor_rms
     xr, rr = x.reshape(-1, row), ref.reshape(-1, row)
     rnd = round_like(ref, out.dtype).reshape(-1, row)
     nrm = np.linalg.norm(rr, axis=1)
+    excess = np.linalg.norm(xr - rr, axis=1) - np.linalg.norm(rnd - rr, axis=1)
     if row_floor_rms:
         floor = np.sqrt(np.mean(nrm ** 2))
-        excess = np.linalg.norm(xr - rr, axis=1) - np.linalg.norm(rnd - rr, axis=1)
         worst = float((excess / np.maximum(nrm, floor)).max()) if floor > 0 else float(excess.max())
     else:
-        num = np.linalg.norm(xr - rnd, axis=1)
         zero = nrm == 0
-        assert np.all(num[zero] == 0), "rows that must be zero are not"
-        worst = float((num[~zero] / nrm[~zero]).max()) if np.any(~zero) else 0.0
+        assert np.all(xr[zero] == 0), "rows that must be zero are not"
+        worst = float((excess[~zero] / nrm[~zero]).max()) if np.any(~zero) else 0.0
     assert worst <= row_tol, f"worst row relative L2 {worst:.3e} > {row_tol:.2e}"
 
 

@@ -40,15 +40,20 @@ def _ck_pool(st, n):
     (synth.TINY, [1, 37, 130, 300, 0], [0, 64, 100, 256, 5], 64, "tc"),
     (synth.QWEN, [70, 200, 513], [0, 128, 0], 256, "tc"),
     (synth.QWEN, [70, 200, 513], [0, 128, 0], 256, "cuda"),
+    (synth.QWEN, [70, 200, 513], [0, 128, 0], 256, "bf16"),
     (synth.QWEN.replace(hk=2, hv=8, dk=64, dv=64), [129, 64, 3], [0, 192, 61], 64, "tc"),
     (synth.TINY, [700, 65, 260], [3, 0, 130], 64, "tc"),
     (synth.QWEN, [200, 1, 70, 129], [200, 77, 4101, 63], 256, "tc"),
-], ids=["tiny", "qwen", "qwen_fp32_path", "dk64_g4", "tiny_ten_checkpoints", "qwen_unaligned_continuations"])
+], ids=["tiny", "qwen", "qwen_fp32_path", "qwen_bf16_operands", "dk64_g4", "tiny_ten_checkpoints",
+        "qwen_unaligned_continuations"])
 def test_prefill_vs_token_recurrence(cuda, monkeypatch, shape, lens, starts, blk, path):
-    """path "cuda" forces the fp32 CUDA-core prefill (the library reads
-    GDN_PREFILL_PATH on every call); it meets the stated 2e-3."""
-    if path == "cuda":
-        monkeypatch.setenv("GDN_PREFILL_PATH", "cuda")
+    """path "tc": the library's choice (the tf32 tensor-core prefill for the
+    Qwen3.5 shape); "cuda" forces the fp32 CUDA-core prefill and "bf16" the
+    bf16-operand tensor-core prefill (the library reads GDN_PREFILL_PATH on
+    every call).  The first two meet the stated 2e-3; the bf16-operand form is
+    held to its modelled bounds."""
+    if path != "tc":
+        monkeypatch.setenv("GDN_PREFILL_PATH", path)
     n = len(lens)
     n_slots = 8 if shape.dk == 16 else 12
     st = Setup(shape, seed=40, num_slots=n_slots)

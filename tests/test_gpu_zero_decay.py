@@ -69,12 +69,12 @@ def _check(st, shape, ids, ck, ock, n_ck, out, o_ref, tol, row_tol, stol):
     assert max_rel_l2(to_np(ck.ssm[written]), ock.ssm[written], shape.dv * shape.dk) <= stol
 
 
-@pytest.mark.parametrize("path", ["tc", "cuda"])
+@pytest.mark.parametrize("path", ["tc", "bf16", "cuda"])
 def test_gdn_prefill_zero_decay_tokens(cuda, monkeypatch, path):
     """Half of the V heads see a = +inf at the chosen tokens; path "cuda"
-    forces the fp32 prefill."""
-    if path == "cuda":
-        monkeypatch.setenv("GDN_PREFILL_PATH", "cuda")
+    forces the fp32 prefill, "bf16" the bf16-operand tensor-core prefill."""
+    if path != "tc":
+        monkeypatch.setenv("GDN_PREFILL_PATH", path)
     shape = synth.QWEN
     lens, starts, blk = [200, 130], [0, 37], 64
     st = Setup(shape, seed=150, num_slots=6)
@@ -173,10 +173,10 @@ def _check_nan(st, shape, lens, cu, ids, ck, ock, ck_ids, out, o_ref, first_clea
             assert np.isnan(ock.ssm[cid, NAN_HEAD]).all()
 
 
-@pytest.mark.parametrize("path", ["tc", "cuda"])
+@pytest.mark.parametrize("path", ["tc", "bf16", "cuda"])
 def test_gdn_prefill_nan_gate_poisons_like_the_recurrence(cuda, monkeypatch, path):
-    if path == "cuda":
-        monkeypatch.setenv("GDN_PREFILL_PATH", "cuda")
+    if path != "tc":
+        monkeypatch.setenv("GDN_PREFILL_PATH", path)
     shape = synth.QWEN
     lens, starts, blk = [200, 130], [0, 37], 64
     st = Setup(shape, seed=153, num_slots=6)
