@@ -13,25 +13,32 @@
 // tensor core are dv rows, or the chunk's 64 k^ rows and 64 q^ rows):
 //   features   the 67 raw input rows (3 of history) of the head's q, k and v
 //              channels arrive by three TMA tensor copies; one thread per
-//              channel runs conv1d + SiLU down the chunk; the q/k rows' L2
-//              norms come from a warp reduce-scatter of the squares.  Written
-//              as tf32 operands: [K^ ; Q^] (shared memory, K-major),
-//              K~^T = (diag(e^{b_last - b}) K^)^T (shared memory, K-major over
-//              tokens) and V^T (tensor memory).
-//   P          [K^;Q^] K^T                                (tcgen05, TMEM)
-//   A, M       A = strict_lower(beta (.) K K^T (.) Gamma) (fp32, for the
-//              solve), M = Q K^T (.) Gamma (.) lower-incl (tf32 operand)
-//   T          (I + A)^-1 diag(beta): 8 x 8 substitutions, then merges on
-//              warp-level mma in split tf32 (hi/lo: fp32 accuracy); written
-//              as T and T'' = -T diag(e^b) (tf32 operands)
-//   Delta^T    = V^T T^T + (S^T K^T) T''^T: the WY form's U - W S with
-//              W = T diag(e^b) K, regrouped so that the state meets only the
-//              T-free K^ (E = S^T K^T comes with O1 = S^T Q^T in one product
-//              whose A operand is the state itself, in TMEM)
-//   state      S^T <- e^{b_last} S^T (in TMEM, by the threads) + Delta^T K~
-//              (one product accumulating into the state; A = Delta^T in TMEM)
-//   output     O = O1 diag(e^b) + Delta^T M^T, staged as a bf16 tile and
-//              written by one TMA tensor store
+//              channel runs conv1d + SiLU down the chunk.  The q and k rows
+//              are kept unnormalised (Y_K, Y_Q): their L2 norms come out of
+//              the next product and are folded into the small operands below.
+//              Written as tf32 operands: [Y_K ; Y_Q] (shared memory, K-major),
+//              K~^T = (diag(e^{b_last - b}) Y_K)^T (shared memory, K-major
+//              over tokens) and V^T (tensor memory).
+//   P          [Y_K;Y_Q] [Y_K;Y_Q]^T (tcgen05, TMEM): its diagonal gives the
+//              norms, rk_i = 1/|y_k,i|, rq_i = dk^-1/2 / |y_q,i| (with the eps)
+//   A, M'      A = strict_lower(beta_i rk_i rk_j (Y_K Y_K^T)_ij Gamma_ij)
+//              (fp32, for the solve), M'_ij = rq_i (Y_Q Y_K^T)_ij Gamma_ij on
+//              and below the diagonal (tf32 operand)
+//   T          X = (I + A)^-1 by 8 x 8 substitutions and three merge levels,
+//              fp32 on the CUDA cores; written as T1 = diag(rk) X diag(beta)
+//              and T2 = -diag(rk) X diag(beta e^b rk) (tf32 operands)
+//   Delta'^T   = V^T T1^T + (S^T Y_K^T) T2^T = (diag(rk) Delta)^T: the WY
+//              form's U - W S with W = T diag(e^b) K^, regrouped so that the
+//              state meets only the T-free Y_K (S^T Y_K^T comes with
+//              S^T Y_Q^T in one product whose A operand is the state itself,
+//              in TMEM)
+//   state      S^T <- e^{b_last} S^T (in TMEM, by the threads) + Delta'^T K~
+//              (one product accumulating into the state; A = Delta'^T in TMEM)
+//   output     O = (S^T Y_Q^T) diag(rq e^b) + Delta'^T M'^T, staged as a bf16
+//              tile and written by one TMA tensor store
+// With k^ = diag(rk) Y_K and q^ = diag(rq) Y_Q these are the chunk form's
+// products exactly: the rk factors of Delta and of the state update meet in
+// Delta', and M' = M diag(1/rk).
 // The fp32 state S^T (dv x dk) lives in TMEM for the whole sequence: it is
 // the accumulator of its own update and the A operand of the products that
 // read it.  Checkpoints are staged from TMEM into the dead [K;Q] tile and
@@ -47,19 +54,19 @@ namespace {
 
 constexpr int kC = 64;                 // chunk
 constexpr int kD = 128;                // dk = dv
-constexpr int kThreads = 256;          // 8 warps
+constexpr int kThreads = 512;          // 16 warps
 constexpr int kRawRows = kC + 3;       // chunk rows plus 3 rows of conv history
 constexpr int kAX = 68;                // row stride (floats) of the solve's A and X
 
 // TMEM columns (fp32, one per column).  Lanes are dv rows, except P, whose
-// lanes are the [K^;Q^] rows.
-constexpr uint32_t TM_S = 0;    // S^T [dv][dk], 128 columns
-constexpr uint32_t TM_P = 128;  // [K;Q] K^T [128 rows][64 tokens]
-constexpr uint32_t TM_E = 192;  // S^T K^T [dv][64], then O1 = S^T Q^T at TM_E + 64
-constexpr uint32_t TM_O1 = 256;
-constexpr uint32_t TM_DL = 320;  // Delta^T [dv][64]
-constexpr uint32_t TM_O2 = 384;  // Delta^T M^T [dv][64]
-constexpr uint32_t TM_V = 448;   // V^T [dv][64] (operand)
+// lanes are the [Y_K;Y_Q] rows.
+constexpr uint32_t TM_S = 0;     // S^T [dv][dk], 128 columns
+constexpr uint32_t TM_P = 128;   // P [128 rows][128]; after the extraction, E and O1:
+constexpr uint32_t TM_E = 128;   //   S^T Y_K^T [dv][64]
+constexpr uint32_t TM_O1 = 192;  //   S^T Y_Q^T [dv][64]
+constexpr uint32_t TM_DL = 256;  // Delta'^T [dv][64]
+constexpr uint32_t TM_O2 = 320;  // Delta'^T M'^T [dv][64]
+constexpr uint32_t TM_V = 384;   // V^T [dv][64] (operand)
 constexpr uint32_t TM_COLS = 512;
 
 struct Tc32Args {
@@ -90,11 +97,11 @@ struct Tc32Args {
 // swizzled K-major layout: a 128-byte row holds 32 elements, 8-row groups
 // are 1024 bytes apart, and wider rows continue in further 32-column blocks.
 struct __align__(1024) Smem32 {
-  uint8_t kq[4 * 128 * 128];  // [K^ ; Q^]: rows 0..63 k^, 64..127 q^ (x dk): 4 blocks of 16 KB
+  uint8_t kq[4 * 128 * 128];  // [Y_K ; Y_Q]: rows 0..63 k, 64..127 q (x dk): 4 blocks of 16 KB
   uint8_t kt[2 * 128 * 128];  // K~^T [dk][64 tokens]: 2 blocks of 16 KB
-  uint8_t tm[2 * 64 * 128];   // T [i][j]: 2 blocks of 8 KB
-  uint8_t t2[2 * 64 * 128];   // T'' = -T diag(e^b); after its product, the output staging tile
-  uint8_t mq[2 * 64 * 128];   // M [i][j]
+  uint8_t tm[2 * 64 * 128];   // T1 [i][j]: 2 blocks of 8 KB
+  uint8_t t2[2 * 64 * 128];   // T2; after its product, the output staging tile
+  uint8_t mq[2 * 64 * 128];   // M' [i][j]
   union {
     __nv_bfloat16 raw[3][kRawRows][kD];  // staged inputs: q, k, v parts
     struct {
@@ -104,8 +111,8 @@ struct __align__(1024) Smem32 {
     } sv;  // the solve's scratch (after the features have read the inputs)
   };
   float g[kC], beta[kC], b[kC], eb[kC], ebl[kC];
-  float part[2][4][kC];  // per-warp partial sums of squares: [k, q][warp][token]
-  float rn[2][kC];       // 1 / ||k^||, dk^-1/2 / ||q^|| per token
+  float rk[kC];  // 1 / sqrt(|y_k|^2 + eps) per token
+  float rq[kC];  // dk^-1/2 / sqrt(|y_q|^2 + eps) per token
   uint64_t ld_bar, mma_bar;
   uint32_t tmem_base;
 };
@@ -126,206 +133,135 @@ __device__ __forceinline__ uint32_t f32_off(int r, int c, uint32_t blk) {
 
 __device__ __forceinline__ float silu_fast(float y) { return __fdividef(y, 1.f + exp_ftz(-y)); }
 
-// ---- the 64 x 64 solve: T = (I + A)^-1 diag(beta) ---------------------------
-// Warp-level tf32 MMA (m16n8k8, fp32 accumulate).  Fragment layout: lane =
-// 4 * g + t; A holds (g, t), (g + 8, t), (g, t + 4), (g + 8, t + 4); B holds
-// (t, g), (t + 4, g); D holds (g, 2t), (g, 2t + 1), (g + 8, 2t), (g + 8, 2t + 1).
-// Operands are split x = hi + lo (both tf32) and each product is taken as
-// lo*hi + hi*lo + hi*hi, which carries fp32 accuracy.
-__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
-  const float h = umma::tf32_round(x);
-  hi = __float_as_uint(h);
-  lo = __float_as_uint(umma::tf32_round(x - h));
-}
-struct FragA {
-  uint32_t h[4], l[4];
-};
-struct FragB {
-  uint32_t h[2], l[2];
-};
-template <class LF>
-__device__ __forceinline__ void frag_a(FragA& a, int k, LF L) {
-  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  split_tf32(L(g, k + t), a.h[0], a.l[0]);
-  split_tf32(L(g + 8, k + t), a.h[1], a.l[1]);
-  split_tf32(L(g, k + t + 4), a.h[2], a.l[2]);
-  split_tf32(L(g + 8, k + t + 4), a.h[3], a.l[3]);
-}
-template <class RF>
-__device__ __forceinline__ void frag_b(FragB& b, int k, RF R) {
-  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  split_tf32(R(k + t, g), b.h[0], b.l[0]);
-  split_tf32(R(k + t + 4, g), b.h[1], b.l[1]);
-}
-__device__ __forceinline__ void mma_m16n8k8(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
-// a 16 x 8 tile product over NK k-steps of 8 from preloaded split fragments
-template <int NK>
-__device__ __forceinline__ void tile_mm(float (&d)[4], const FragA (&a)[NK], const FragB (&b)[NK]) {
-  d[0] = d[1] = d[2] = d[3] = 0.f;
-#pragma unroll
-  for (int s = 0; s < NK; ++s) {
-    mma_m16n8k8(d, a[s].l, b[s].h);
-    mma_m16n8k8(d, a[s].h, b[s].l);
-    mma_m16n8k8(d, a[s].h, b[s].h);
-  }
-}
+// element (r, c) of the solve's 64 x 64 fp32 matrices A and X
 __device__ __forceinline__ int ix(int r, int c) { return r * kAX + c; }
 
+// ---- the 64 x 64 solve ---------------------------------------------------------
+// X = (I + A)^-1 for the strictly lower 64 x 64 A (fp32, rows kAX apart),
+// blockwise: the eight 8 x 8 diagonal blocks by substitution, then merged
+// 8 -> 16 -> 32 -> 64 with X_ba = -X_b (A_ba X_a).  fp32 on the CUDA cores;
+// every entry of X above the diagonal is zero (X is cleared first), so the
+// sums run over whole rows and columns.  Each entry of X is written out as
+// T1 = rk_i X_ij beta_j and T2 = -rk_i X_ij beta_j e^{b_j} rk_j (tf32).
+// Y: 1024 floats of scratch.  512 threads; the caller synchronises before (A
+// complete, X cleared) and after.
 struct TOut {
-  uint8_t* tm;        // T
-  uint8_t* t2;        // T'' = -T diag(e^b)
-  const float* beta;  // [64]
-  const float* eb;    // [64]
+  uint8_t* t1;
+  uint8_t* t2;
+  const float* beta;
+  const float* eb;
+  const float* rk;
 };
-// T entries (r, c), (r, c + 1) (c even) and their T'' counterparts, from X
-// entries x0, x1 (bc: beta of the two columns, ec: their e^b)
-__device__ __forceinline__ void put_t(const TOut& o, int r, int c, float x0, float x1, const float2& bc,
-                                      const float2& ec) {
+__device__ __forceinline__ void put_t(const TOut& o, int r, int c, float x) {
   const uint32_t off = f32_off(r, c, 64 * 128);
-  const float t0 = x0 * bc.x, t1 = x1 * bc.y;
-  *reinterpret_cast<float2*>(o.tm + off) = make_float2(umma::tf32_round(t0), umma::tf32_round(t1));
-  *reinterpret_cast<float2*>(o.t2 + off) = make_float2(umma::tf32_round(-t0 * ec.x), umma::tf32_round(-t1 * ec.y));
+  const float t = o.rk[r] * x * o.beta[c];
+  *reinterpret_cast<float*>(o.t1 + off) = umma::tf32_round(t);
+  *reinterpret_cast<float*>(o.t2 + off) = umma::tf32_round(-t * o.eb[c] * o.rk[c]);
 }
 
-// X = (I + A)^-1 for the 64 x 64 strictly lower A (fp32), written out as the
-// lower triangles of T and T'' (their upper triangles are zero already).
-// 8 x 8 diagonal blocks by substitution, then merged 8 -> 16 -> 32 -> 64 with
-// X_ba = -X_b (A_ba X_a).  Each output column tile j of X_ba needs only column
-// tile j of A_ba X_a, so a warp carries its tile through both products.
-// Entries above the diagonal of X are never stored; reads mask them to zero.
-// Y: 2048 floats of scratch.  256 threads; the caller synchronises before (A
-// complete) and after.
 __device__ __forceinline__ void solve_T(const float* A, float* X, float* Y, const TOut& to) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = lane >> 2, t = lane & 3;
-  auto bc_of = [&](int c) { return make_float2(to.beta[c], to.beta[c + 1]); };
-  auto ec_of = [&](int c) { return make_float2(to.eb[c], to.eb[c + 1]); };
-  // 8 x 8 diagonal blocks: warp w, lane l < 4 = columns 2l and 2l+1 of block w
-  if (lane < 4) {
-    const int o = 8 * warp, c0 = 2 * lane;
+  // 8 x 8 diagonal blocks: thread t < 64 = block t / 8, column t % 8
+  if (tid < kC) {
+    const int o = 8 * (tid >> 3), c = tid & 7;
     float a[28];
 #pragma unroll
     for (int r = 1, i = 0; r < 8; ++r)
 #pragma unroll
       for (int m = 0; m < r; ++m, ++i) a[i] = A[ix(o + r, o + m)];
-    float x0[8], x1[8];
+    float x[8];
 #pragma unroll
     for (int r = 0, i = 0; r < 8; ++r) {
-      float s0 = (r == c0) ? 1.f : 0.f, s1 = (r == c0 + 1) ? 1.f : 0.f;
+      float s = (r == c) ? 1.f : 0.f;
 #pragma unroll
-      for (int m = 0; m < r; ++m, ++i) {
-        s0 = fmaf(-a[i], x0[m], s0);
-        s1 = fmaf(-a[i], x1[m], s1);
-      }
-      x0[r] = s0;
-      x1[r] = s1;
+      for (int m = 0; m < r; ++m, ++i) s = fmaf(-a[i], x[m], s);
+      x[r] = (r < c) ? 0.f : s;
     }
-    const float2 bc = bc_of(o + c0), ec = ec_of(o + c0);
+#pragma unroll
+    for (int r = 0; r < 8; ++r) X[ix(o + r, o + c)] = x[r];
 #pragma unroll
     for (int r = 0; r < 8; ++r)
-      if (r >= c0) {
-        *reinterpret_cast<float2*>(X + ix(o + r, o + c0)) = make_float2(x0[r], x1[r]);
-        put_t(to, o + r, o + c0, x0[r], x1[r], bc, ec);
-      }
+      if (r >= c) put_t(to, o + r, o + c, x[r]);
   }
   __syncthreads();
-  // 8 -> 16: warps 0..3, block pair p (rows/cols 16p ..); M padded to 16
-  if (warp < 4) {
-    const int o = 16 * warp;
-    float* Ys = Y + warp * 128;
-    FragA fa[1], fx[1];
-    FragB fb[1], fy[1];
-    frag_a(fa[0], 0, [&](int r, int k) { return r < 8 ? A[ix(o + 8 + r, o + k)] : 0.f; });
-    frag_b(fb[0], 0, [&](int k, int c) { return k >= c ? X[ix(o + k, o + c)] : 0.f; });
-    frag_a(fx[0], 0, [&](int r, int k) { return (r < 8 && k <= r) ? X[ix(o + 8 + r, o + 8 + k)] : 0.f; });
-    float d[4];
-    tile_mm<1>(d, fa, fb);
-    Ys[g * 8 + 2 * t] = d[0];
-    Ys[g * 8 + 2 * t + 1] = d[1];
-    __syncwarp();
-    frag_b(fy[0], 0, [&](int k, int c) { return Ys[k * 8 + c]; });
-    tile_mm<1>(d, fx, fy);
-    X[ix(o + 8 + g, o + 2 * t)] = -d[0];
-    X[ix(o + 8 + g, o + 2 * t + 1)] = -d[1];
-    put_t(to, o + 8 + g, o + 2 * t, -d[0], -d[1], bc_of(o + 2 * t), ec_of(o + 2 * t));
-  }
-  __syncthreads();
-  // 16 -> 32: warps 0..3 = (pair q, column tile j)
-  if (warp < 4) {
-    const int o = 32 * (warp >> 1), j = warp & 1;
-    float* Ys = Y + 512 + warp * 128;
-    FragA fa[2], fx[2];
-    FragB fb[2], fy[2];
-#pragma unroll
-    for (int s = 0; s < 2; ++s) {
-      frag_a(fa[s], 8 * s, [&](int r, int k) { return A[ix(o + 16 + r, o + k)]; });
-      frag_b(fb[s], 8 * s, [&](int k, int c) { return k >= 8 * j + c ? X[ix(o + k, o + 8 * j + c)] : 0.f; });
-      frag_a(fx[s], 8 * s, [&](int r, int k) { return k <= r ? X[ix(o + 16 + r, o + 16 + k)] : 0.f; });
-    }
-    const int cc = o + 8 * j + 2 * t;
-    float d[4];
-    tile_mm<2>(d, fa, fb);
-    Ys[g * 8 + 2 * t] = d[0];
-    Ys[g * 8 + 2 * t + 1] = d[1];
-    Ys[(g + 8) * 8 + 2 * t] = d[2];
-    Ys[(g + 8) * 8 + 2 * t + 1] = d[3];
-    __syncwarp();
-#pragma unroll
-    for (int s = 0; s < 2; ++s) frag_b(fy[s], 8 * s, [&](int k, int c) { return Ys[k * 8 + c]; });
-    tile_mm<2>(d, fx, fy);
-    X[ix(o + 16 + g, cc)] = -d[0];
-    X[ix(o + 16 + g, cc + 1)] = -d[1];
-    X[ix(o + 24 + g, cc)] = -d[2];
-    X[ix(o + 24 + g, cc + 1)] = -d[3];
-    put_t(to, o + 16 + g, cc, -d[0], -d[1], bc_of(cc), ec_of(cc));
-    put_t(to, o + 24 + g, cc, -d[2], -d[3], bc_of(cc), ec_of(cc));
-  }
-  __syncthreads();
-  // 32 -> 64: warps = (column tile j, row half mh); the two warps of a column
-  // tile exchange their halves of Y_j = A_ba X_a[:, j] through a named
-  // barrier.  Rows of X_a above 8j of column tile j are zero (k-steps skipped).
+  // 8 -> 16: pair p (rows 16p + 8 .., columns 16p ..), entry (i, j) per thread
   {
-    const int j = warp & 3, mh = warp >> 2;
-    float* Ys = Y + 1024 + j * 256;  // 32 x 8
-    FragA fa[4], fx[4];
-    FragB fb[4], fy[4];
+    const int p = (tid >> 6) & 3, i = (tid >> 3) & 7, j = tid & 7, o = 16 * p;
+    if (tid < 256) {
+      float y = 0.f;
 #pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      if (s >= j) {
-        frag_a(fa[s], 8 * s, [&](int r, int k) { return A[ix(32 + 16 * mh + r, k)]; });
-        frag_b(fb[s], 8 * s, [&](int k, int c) { return k >= 8 * j + c ? X[ix(k, 8 * j + c)] : 0.f; });
-      } else {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) fa[s].h[e] = fa[s].l[e] = 0u;
-        fb[s].h[0] = fb[s].h[1] = fb[s].l[0] = fb[s].l[1] = 0u;
-      }
-      frag_a(fx[s], 8 * s, [&](int r, int k) { return k <= 16 * mh + r ? X[ix(32 + 16 * mh + r, 32 + k)] : 0.f; });
+      for (int k = 0; k < 8; ++k) y = fmaf(A[ix(o + 8 + i, o + k)], X[ix(o + k, o + j)], y);
+      Y[tid] = y;  // Y_p[i][j] at 64 p + 8 i + j
     }
-    const int cc = 8 * j + 2 * t;
-    float d[4];
-    tile_mm<4>(d, fa, fb);
-    const int yr = 16 * mh + g;
-    Ys[yr * 8 + 2 * t] = d[0];
-    Ys[yr * 8 + 2 * t + 1] = d[1];
-    Ys[(yr + 8) * 8 + 2 * t] = d[2];
-    Ys[(yr + 8) * 8 + 2 * t + 1] = d[3];
-    named_sync(1 + j, 64);
+    __syncthreads();
+    if (tid < 256) {
+      float x = 0.f;
 #pragma unroll
-    for (int s = 0; s < 4; ++s) frag_b(fy[s], 8 * s, [&](int k, int c) { return Ys[k * 8 + c]; });
-    tile_mm<4>(d, fx, fy);
-    put_t(to, 32 + yr, cc, -d[0], -d[1], bc_of(cc), ec_of(cc));
-    put_t(to, 40 + yr, cc, -d[2], -d[3], bc_of(cc), ec_of(cc));
+      for (int k = 0; k < 8; ++k) x = fmaf(X[ix(o + 8 + i, o + 8 + k)], Y[64 * p + 8 * k + j], x);
+      X[ix(o + 8 + i, o + j)] = -x;
+      put_t(to, o + 8 + i, o + j, -x);
+    }
+  }
+  __syncthreads();
+  // 16 -> 32: pair q (rows 32q + 16 .., columns 32q ..), entry (i, j) per thread
+  {
+    const int q = tid >> 8, i = (tid >> 4) & 15, j = tid & 15, o = 32 * q;
+    float y = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) y = fmaf(A[ix(o + 16 + i, o + k)], X[ix(o + k, o + j)], y);
+    Y[256 * q + 16 * i + j] = y;
+    __syncthreads();
+    float x = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) x = fmaf(X[ix(o + 16 + i, o + 16 + k)], Y[256 * q + 16 * k + j], x);
+    X[ix(o + 16 + i, o + j)] = -x;
+    put_t(to, o + 16 + i, o + j, -x);
+  }
+  __syncthreads();
+  // 32 -> 64: rows 32 + 2w, 32 + 2w + 1, column `lane`
+  {
+    float y[2] = {0.f, 0.f};
+#pragma unroll
+    for (int k4 = 0; k4 < 8; ++k4) {
+      float4 a[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) a[r] = *reinterpret_cast<const float4*>(A + ix(32 + 2 * warp + r, 4 * k4));
+      const float x0 = X[ix(4 * k4, lane)], x1 = X[ix(4 * k4 + 1, lane)], x2 = X[ix(4 * k4 + 2, lane)],
+                  x3 = X[ix(4 * k4 + 3, lane)];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        y[r] = fmaf(a[r].x, x0, y[r]);
+        y[r] = fmaf(a[r].y, x1, y[r]);
+        y[r] = fmaf(a[r].z, x2, y[r]);
+        y[r] = fmaf(a[r].w, x3, y[r]);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) Y[32 * (2 * warp + r) + lane] = y[r];
+    __syncthreads();
+    float x[2] = {0.f, 0.f};
+#pragma unroll
+    for (int k4 = 0; k4 < 8; ++k4) {
+      float4 xb[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) xb[r] = *reinterpret_cast<const float4*>(X + ix(32 + 2 * warp + r, 32 + 4 * k4));
+      const float y0 = Y[32 * (4 * k4) + lane], y1 = Y[32 * (4 * k4 + 1) + lane], y2 = Y[32 * (4 * k4 + 2) + lane],
+                  y3 = Y[32 * (4 * k4 + 3) + lane];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        x[r] = fmaf(xb[r].x, y0, x[r]);
+        x[r] = fmaf(xb[r].y, y1, x[r]);
+        x[r] = fmaf(xb[r].z, y2, x[r]);
+        x[r] = fmaf(xb[r].w, y3, x[r]);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) put_t(to, 32 + 2 * warp + r, lane, -x[r]);
   }
 }
 
 // ---- the kernel -------------------------------------------------------------
-// grid (hv, n_seq), 256 threads, one CTA per SM.  Thread 0 issues the TMA
+// grid (hv, n_seq), 512 threads, one CTA per SM.  Thread 0 issues the TMA
 // copies and the tensor-core products; every wait is bounded (1 s).
 template <typename Tconv>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -364,20 +300,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   umma::fence_after();
   const uint32_t tmem = S.tmem_base;
-  const int lrow = 32 * (warp & 3) + lane;  // TMEM lane of this thread (dv row, or [K;Q] row)
-  const int half = warp >> 2;               // which column half this warp handles
+  const int lrow = 32 * (warp & 3) + lane;  // TMEM lane of this thread (dv row, or [Y_K;Y_Q] row)
+  const int qq = warp >> 2;                 // which column quarter this warp handles
   const uint32_t tlane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
 
-  constexpr uint32_t ID_P = umma::idesc_tf32(128, 64, false, false);
   constexpr uint32_t ID_N64 = umma::idesc_tf32(128, 64, false, false);
   constexpr uint32_t ID_N128 = umma::idesc_tf32(128, 128, false, false);
 
-  // feature channels of this thread: q/k channel (tid < 128: k, else q) and
-  // v channel tid % 128 for token half tid / 128
-  const bool isq = tid >= 128;
+  // feature channels of this thread: q/k channel cqk (k for tid % 256 < 128,
+  // else q) for tokens 32 th .., and v channel lrow for tokens 16 qq ..
+  const bool isq = (tid & 255) >= 128;
   const int cqk = tid & 127;
+  const int th = tid >> 8;
   const int gch_qk = (isq ? hq : a.hk + hq) * kD + cqk;
-  const int gch_v = 2 * a.hk * kD + h * kD + cqk;
+  const int gch_v = 2 * a.hk * kD + h * kD + lrow;
   float wqk[4], wv[4];
   {
     const float4 w4 = *reinterpret_cast<const float4*>(a.conv_w + (size_t)gch_qk * 4);
@@ -411,20 +347,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int q = 0; q < 3; ++q) tma_load_2d(&S.raw[q][0][0], &qmap, part_x[q], row0, &S.ld_bar);
   };
+  // gate inputs of chunk c's token tid (threads 0..63), loaded one chunk ahead
+  auto load_gates = [&](int c, float& av, float& bv) {
+    const int64_t pos = (p0 / kC + c) * kC + tid;
+    av = bv = 0.f;
+    if (c < nch && pos >= p0 && pos < p1) {
+      const size_t tok = (size_t)(t0 + pos - p0);
+      av = __bfloat162float(a.a[tok * a.hv + h]);
+      bv = __bfloat162float(a.b[tok * a.hv + h]);
+    }
+  };
 
-  // initial state S^T rows into TMEM; the upper triangle of T stays zero
-  float* gS = a.ssm + (((size_t)slot * a.hv + h) * kD + lrow) * kD + 64 * half;
+  // initial state S^T rows into TMEM; the upper triangle of T1 stays zero
+  float* gS = a.ssm + (((size_t)slot * a.hv + h) * kD + lrow) * kD + 32 * qq;
   {
     float v[32];
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float4 x = *reinterpret_cast<const float4*>(gS + 32 * k + 4 * i);
-        v[4 * i] = x.x; v[4 * i + 1] = x.y; v[4 * i + 2] = x.z; v[4 * i + 3] = x.w;
-      }
-      umma::tmem_st32(tlane + TM_S + 64 * half + 32 * k, v);
+    for (int i = 0; i < 8; ++i) {
+      const float4 x = *reinterpret_cast<const float4*>(gS + 4 * i);
+      v[4 * i] = x.x; v[4 * i + 1] = x.y; v[4 * i + 2] = x.z; v[4 * i + 3] = x.w;
     }
+    umma::tmem_st32(tlane + TM_S + 32 * qq, v);
   }
   for (int e = tid; e < (int)(sizeof(S.tm) / 16); e += kThreads)
     reinterpret_cast<uint4*>(S.tm)[e] = make_uint4(0u, 0u, 0u, 0u);
@@ -433,6 +376,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     issue_raw(0);
     ld_issued = 1;
   }
+  float ga = 0.f, gb = 0.f;
+  if (tid < kC) load_gates(0, ga, gb);
 
   bool bad = false;
   uint32_t mph = 0;
@@ -456,16 +401,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // gates of the chunk's tokens (outside the sequence: g = beta = 0)
     if (tid < kC) {
       const int64_t pos = P + tid;
-      float gv = 0.f, bv = 0.f;
-      if (pos >= p0 && pos < p1) {
-        const size_t tok = (size_t)(t0 + pos - p0);
-        const float av = __bfloat162float(a.a[tok * a.hv + h]);
-        const float bb = __bfloat162float(a.b[tok * a.hv + h]);
-        gv = floor_log_decay(-eA * softplus_f(av + dtb));
-        bv = sigmoid_f(bb);
-      }
-      S.g[tid] = gv;
-      S.beta[tid] = bv;
+      const bool in = pos >= p0 && pos < p1;
+      S.g[tid] = in ? floor_log_decay(-eA * softplus_f(ga + dtb)) : 0.f;
+      S.beta[tid] = in ? sigmoid_f(gb) : 0.f;
+      load_gates(c + 1, ga, gb);
     }
     // the previous chunk's tensor stores have read the kq tile (checkpoint
     // staging) and the t2 tile (output staging)
@@ -509,100 +448,62 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncthreads();
     }
 
-    // ---- features: q/k (one channel per thread, down the chunk) ------------
+    // ---- features: conv1d + SiLU, one channel per thread down the chunk ----
+    // (each channel's raw rows are loaded into registers first, so that no
+    // shared-memory store of the results has to wait for, or hold up, them)
     {
-      const __nv_bfloat16* xs = &S.raw[isq ? 0 : 1][0][cqk];
-      float y[kC];
-      float x0 = __bfloat162float(xs[0]), x1 = __bfloat162float(xs[kD]), x2 = __bfloat162float(xs[2 * kD]);
+      // q or k, tokens 32 th ..: the [Y_K ; Y_Q] column of this channel, and
+      // for k the K~^T row
+      const int tk = 32 * th;
+      float y[32];
+      {
+        const __nv_bfloat16* xs = &S.raw[isq ? 0 : 1][tk][cqk];
+        float x[35];
 #pragma unroll
-      for (int t = 0; t < kC; ++t) {
-        const float x3 = __bfloat162float(xs[(t + 3) * kD]);
-        float acc = wqk[0] * x0;
-        acc = fmaf(wqk[1], x1, acc);
-        acc = fmaf(wqk[2], x2, acc);
-        acc = fmaf(wqk[3], x3, acc);
-        const bool valid = full || (P + t >= p0 && P + t < p1);
-        y[t] = valid ? silu_fast(acc) : 0.f;
-        x0 = x1;
-        x1 = x2;
-        x2 = x3;
-      }
-      // sums of squares over the warp's 32 channels: a reduce-scatter that
-      // leaves lane l with tokens 2l and 2l + 1
-      float s[32];
+        for (int r = 0; r < 35; ++r) x[r] = __bfloat162float(xs[r * kD]);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float lo = y[i] * y[i], hi = y[32 + i] * y[32 + i];
-        const bool up = lane & 16;
-        s[i] = (up ? hi : lo) + __shfl_xor_sync(0xffffffffu, up ? lo : hi, 16);
+        for (int t = 0; t < 32; ++t) {
+          float acc = wqk[0] * x[t];
+          acc = fmaf(wqk[1], x[t + 1], acc);
+          acc = fmaf(wqk[2], x[t + 2], acc);
+          acc = fmaf(wqk[3], x[t + 3], acc);
+          const bool valid = full || (P + tk + t >= p0 && P + tk + t < p1);
+          y[t] = valid ? umma::tf32_round(silu_fast(acc)) : 0.f;
+        }
       }
+      const int R0 = (isq ? kC : 0) + tk;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const bool up = lane & 8;
-        s[i] = (up ? s[16 + i] : s[i]) + __shfl_xor_sync(0xffffffffu, up ? s[i] : s[16 + i], 8);
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const bool up = lane & 4;
-        s[i] = (up ? s[8 + i] : s[i]) + __shfl_xor_sync(0xffffffffu, up ? s[i] : s[8 + i], 4);
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const bool up = lane & 2;
-        s[i] = (up ? s[4 + i] : s[i]) + __shfl_xor_sync(0xffffffffu, up ? s[i] : s[4 + i], 2);
-      }
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const bool up = lane & 1;
-        s[i] = (up ? s[2 + i] : s[i]) + __shfl_xor_sync(0xffffffffu, up ? s[i] : s[2 + i], 1);
-      }
-      *reinterpret_cast<float2*>(&S.part[isq][warp & 3][2 * lane]) = make_float2(s[0], s[1]);
-      __syncthreads();
-      if (tid < 2 * kC) {
-        const int pq = tid >> 6, t = tid & 63;
-        const float ss = S.part[pq][0][t] + S.part[pq][1][t] + S.part[pq][2][t] + S.part[pq][3][t];
-        S.rn[pq][t] = rsqrtf(ss + kNormEps) * (pq ? rsqrtf((float)kD) : 1.f);
-      }
-      __syncthreads();
-      // [K^;Q^] rows (this channel's column), and for k the scaled K~^T row
-      const int R0 = isq ? kC : 0;
-#pragma unroll
-      for (int t = 0; t < kC; ++t) {
-        y[t] *= S.rn[isq][t];
-        *reinterpret_cast<float*>(S.kq + f32_off(R0 + t, cqk, 128 * 128)) = umma::tf32_round(y[t]);
-      }
+      for (int t = 0; t < 32; ++t) *reinterpret_cast<float*>(S.kq + f32_off(R0 + t, cqk, 128 * 128)) = y[t];
       if (!isq) {
 #pragma unroll
-        for (int t4 = 0; t4 < kC / 4; ++t4) {
-          const float4 e4 = *reinterpret_cast<const float4*>(&S.ebl[4 * t4]);
-          *reinterpret_cast<float4*>(S.kt + f32_off(cqk, 4 * t4, 128 * 128)) =
+        for (int t4 = 0; t4 < 8; ++t4) {
+          const float4 e4 = *reinterpret_cast<const float4*>(&S.ebl[tk + 4 * t4]);
+          *reinterpret_cast<float4*>(S.kt + f32_off(cqk, tk + 4 * t4, 128 * 128)) =
               make_float4(umma::tf32_round(y[4 * t4] * e4.x), umma::tf32_round(y[4 * t4 + 1] * e4.y),
                           umma::tf32_round(y[4 * t4 + 2] * e4.z), umma::tf32_round(y[4 * t4 + 3] * e4.w));
         }
       }
-    }
-    // ---- features: v (channel tid % 128, tokens 32 * (tid / 128) ..), into TMEM
-    {
-      const int t0v = 32 * half;
-      const __nv_bfloat16* xs = &S.raw[2][t0v][cqk];
-      float vv[32];
-      float x0 = __bfloat162float(xs[0]), x1 = __bfloat162float(xs[kD]), x2 = __bfloat162float(xs[2 * kD]);
+      // v: channel lrow, tokens 16 qq .., into TMEM
+      const int tv = 16 * qq;
+      float vv[16];
+      {
+        const __nv_bfloat16* xv = &S.raw[2][tv][lrow];
+        float x[19];
 #pragma unroll
-      for (int t = 0; t < 32; ++t) {
-        const float x3 = __bfloat162float(xs[(t + 3) * kD]);
-        float acc = wv[0] * x0;
-        acc = fmaf(wv[1], x1, acc);
-        acc = fmaf(wv[2], x2, acc);
-        acc = fmaf(wv[3], x3, acc);
-        const bool valid = full || (P + t0v + t >= p0 && P + t0v + t < p1);
-        vv[t] = valid ? umma::tf32_round(silu_fast(acc)) : 0.f;
-        x0 = x1;
-        x1 = x2;
-        x2 = x3;
+        for (int r = 0; r < 19; ++r) x[r] = __bfloat162float(xv[r * kD]);
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          float acc = wv[0] * x[t];
+          acc = fmaf(wv[1], x[t + 1], acc);
+          acc = fmaf(wv[2], x[t + 2], acc);
+          acc = fmaf(wv[3], x[t + 3], acc);
+          const bool valid = full || (P + tv + t >= p0 && P + tv + t < p1);
+          vv[t] = valid ? umma::tf32_round(silu_fast(acc)) : 0.f;
+        }
       }
-      umma::tmem_st32(tlane + TM_V + t0v, vv);
+      umma::tmem_st16(tlane + TM_V + tv, vv);
     }
-    // operands visible to the tensor core, then P = [K;Q] K^T
+    // operands visible to the tensor core, then P = [Y_K;Y_Q] [Y_K;Y_Q]^T
     umma::fence_proxy_async();
     umma::fence_before();
     __syncthreads();
@@ -612,49 +513,70 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int s = 0; s < 16; ++s) {
         const uint32_t ko = (s >> 2) * 16384 + (s & 3) * 32;
-        umma::mma_tf32(tmem + TM_P, umma::adv(dkq, ko), umma::adv(dkq, ko), ID_P, s > 0);
+        umma::mma_tf32(tmem + TM_P, umma::adv(dkq, ko), umma::adv(dkq, ko), ID_N128, s > 0);
       }
       umma::commit(&S.mma_bar);
     }
+    // X is cleared for the solve meanwhile (the raw rows are read)
+    for (int e = tid; e < kC * kAX / 4; e += kThreads)
+      reinterpret_cast<float4*>(S.sv.X)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (!mma_wait()) break;
-    // ---- A (fp32, for the solve) and M (tf32 operand) from P ----------------
-    {
+    // ---- norms from P's diagonal: rk_i (K block), rq_i (Q block) ------------
+    // warps 0..3: lane quarter w holds the diagonal entries (lrow, lrow) in
+    // the 32 x 32 block at columns 32 w ..
+    if (qq == 0) {
       float v[32];
-      umma::tmem_ld32(tlane + TM_P + 32 * half, v);
-      const int c0 = 32 * half;
-      float bc[32];
+      umma::tmem_ld32(tlane + TM_P + 32 * warp, v);
+      float d = v[0];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 1; i < 32; ++i) d = (lane == i) ? v[i] : d;
+      if (lrow < kC)
+        S.rk[lrow] = rsqrtf(d + kNormEps);
+      else
+        S.rq[lrow - kC] = rsqrtf(d + kNormEps) * rsqrtf((float)kD);
+    }
+    __syncthreads();
+    // ---- A (fp32, for the solve) and M' (tf32 operand) from P ---------------
+    // thread: row lrow, columns 16 qq .. 16 qq + 15
+    {
+      float v[16];
+      umma::tmem_ld16(tlane + TM_P + 16 * qq, v);
+      const int c0 = 16 * qq;
+      float bc[16], rkc[16];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
         const float4 b4 = *reinterpret_cast<const float4*>(&S.b[c0 + 4 * i]);
         bc[4 * i] = b4.x; bc[4 * i + 1] = b4.y; bc[4 * i + 2] = b4.z; bc[4 * i + 3] = b4.w;
+        const float4 r4 = *reinterpret_cast<const float4*>(&S.rk[c0 + 4 * i]);
+        rkc[4 * i] = r4.x; rkc[4 * i + 1] = r4.y; rkc[4 * i + 2] = r4.z; rkc[4 * i + 3] = r4.w;
       }
       if (lrow < kC) {
         const int r = lrow;
-        const float br = S.b[r], betar = S.beta[r];
-        float av[32];
+        const float br = S.b[r], fr = S.beta[r] * S.rk[r];
+        float av[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) av[i] = (c0 + i < r) ? betar * v[i] * exp_ftz(br - bc[i]) : 0.f;
+        for (int i = 0; i < 16; ++i) av[i] = (c0 + i < r) ? fr * rkc[i] * v[i] * exp_ftz(br - bc[i]) : 0.f;
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
+        for (int q = 0; q < 4; ++q)
           *reinterpret_cast<float4*>(S.sv.A + ix(r, c0 + 4 * q)) = make_float4(av[4 * q], av[4 * q + 1], av[4 * q + 2], av[4 * q + 3]);
       } else {
         const int r = lrow - kC;
-        const float br = S.b[r];
-        float m[32];
+        const float br = S.b[r], fr = S.rq[r];
+        float m[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) m[i] = (c0 + i <= r) ? umma::tf32_round(v[i] * exp_ftz(br - bc[i])) : 0.f;
+        for (int i = 0; i < 16; ++i) m[i] = (c0 + i <= r) ? umma::tf32_round(fr * v[i] * exp_ftz(br - bc[i])) : 0.f;
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
+        for (int q = 0; q < 4; ++q)
           *reinterpret_cast<float4*>(S.mq + f32_off(r, c0 + 4 * q, 64 * 128)) =
               make_float4(m[4 * q], m[4 * q + 1], m[4 * q + 2], m[4 * q + 3]);
       }
     }
-    // T'' is rewritten (its tile held the previous chunk's output staging)
+    // T2 is rewritten (its tile held the previous chunk's output staging)
     for (int e = tid; e < (int)(sizeof(S.t2) / 16); e += kThreads)
       reinterpret_cast<uint4*>(S.t2)[e] = make_uint4(0u, 0u, 0u, 0u);
     umma::fence_before();
     __syncthreads();
-    solve_T(S.sv.A, S.sv.X, S.sv.Y, TOut{S.tm, S.t2, S.beta, S.eb});
+    solve_T(S.sv.A, S.sv.X, S.sv.Y, TOut{S.tm, S.t2, S.beta, S.eb, S.rk});
     umma::fence_proxy_async();
     __syncthreads();
     // the next chunk's raw rows (the solve's scratch is dead)
@@ -662,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       issue_raw(c + 1);
       ld_issued = c + 2;
     }
-    // ---- Delta^T = V^T T^T, and [E | O1] = S^T [K;Q]^T -----------------------
+    // ---- Delta'^T = V^T T1^T, and [E | O1] = S^T [Y_K;Y_Q]^T -----------------
     if (tid == 0) {
       umma::fence_after();
       const uint64_t dtm = umma::desc(smem_addr(S.tm), 16, 1024);
@@ -678,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma::commit(&S.mma_bar);
     }
     if (!mma_wait()) break;
-    // ---- Delta^T += E T''^T (tensor core), S^T <- e^{b_last} S^T (threads) ----
+    // ---- Delta'^T += E T2^T (tensor core), S^T <- e^{b_last} S^T (threads) ---
     if (tid == 0) {
       const uint64_t dt2 = umma::desc(smem_addr(S.t2), 16, 1024);
 #pragma unroll
@@ -690,17 +612,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
       const float dec = S.eb[kC - 1];
       float v[32];
+      umma::tmem_ld32(tlane + TM_S + 32 * qq, v);
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        umma::tmem_ld32(tlane + TM_S + 64 * half + 32 * k, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= dec;
-        umma::tmem_st32(tlane + TM_S + 64 * half + 32 * k, v);
-      }
+      for (int i = 0; i < 32; ++i) v[i] *= dec;
+      umma::tmem_st32(tlane + TM_S + 32 * qq, v);
     }
     umma::fence_before();
     if (!mma_wait()) break;
-    // ---- S^T += Delta^T K~ ; O2 = Delta^T M^T --------------------------------
+    // ---- S^T += Delta'^T K~ ; O2 = Delta'^T M'^T ------------------------------
     if (tid == 0) {
       const uint64_t dkt = umma::desc(smem_addr(S.kt), 16, 1024);
       const uint64_t dmq = umma::desc(smem_addr(S.mq), 16, 1024);
@@ -715,30 +634,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma::commit(&S.mma_bar);
     }
     if (!mma_wait()) break;
-    // ---- output O = O1 diag(e^b) + O2, staged [token][dv] bf16 in t2 ---------
+    // ---- output O = O1 diag(rq e^b) + O2, staged [token][dv] bf16 in t2 ------
     {
-      float o1[32], o2[32];
-      umma::tmem_ld32(tlane + TM_O1 + 32 * half, o1);
-      umma::tmem_ld32(tlane + TM_O2 + 32 * half, o2);
+      float o1[16], o2[16];
+      umma::tmem_ld16(tlane + TM_O1 + 16 * qq, o1);
+      umma::tmem_ld16(tlane + TM_O2 + 16 * qq, o2);
       __nv_bfloat16* ot = reinterpret_cast<__nv_bfloat16*>(S.t2);
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        ot[(32 * half + i) * kD + lrow] = __float2bfloat16_rn(fmaf(o1[i], S.eb[32 * half + i], o2[i]));
+      for (int i = 0; i < 16; ++i)
+        ot[(16 * qq + i) * kD + lrow] = __float2bfloat16_rn(fmaf(o1[i], S.rq[16 * qq + i] * S.eb[16 * qq + i], o2[i]));
     }
     // checkpoint: the state rows, 128B-swizzled, into four 16 KB boxes (32
-    // columns x 128 rows) in the dead [K;Q] tile, for four tensor stores
+    // columns x 128 rows) in the dead kq tile, for four tensor stores
     const int32_t cid = ckpt_slot(c);
     if (cid >= 0) {
       float v[32];
+      umma::tmem_ld32(tlane + TM_S + 32 * qq, v);
+      uint8_t* box = S.kq + qq * 16384;
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        umma::tmem_ld32(tlane + TM_S + 64 * half + 32 * k, v);
-        uint8_t* box = S.kq + (2 * half + k) * 16384;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          *reinterpret_cast<float4*>(box + lrow * 128 + ((j ^ (lrow & 7)) << 4)) =
-              make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-      }
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<float4*>(box + lrow * 128 + ((j ^ (lrow & 7)) << 4)) =
+            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
     }
     umma::fence_proxy_async();
     umma::fence_before();
@@ -774,13 +690,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // the final state
     float v[32];
+    umma::tmem_ld32(tlane + TM_S + 32 * qq, v);
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      umma::tmem_ld32(tlane + TM_S + 64 * half + 32 * k, v);
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        *reinterpret_cast<float4*>(gS + 32 * k + 4 * i) = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-    }
+    for (int i = 0; i < 8; ++i)
+      *reinterpret_cast<float4*>(gS + 4 * i) = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
   }
   if (tid == 0) bulk_wait_all();
   umma::fence_before();
