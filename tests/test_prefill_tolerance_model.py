@@ -15,7 +15,9 @@ What it shows:
     bf16 operands anywhere on the output's path miss 2e-3 (the bf16-operand
     path, GDN_PREFILL_PATH=bf16, is held to bounds from this model);
   * with every operand in tf32 (the default path) the model sits at ~1.7e-3
-    (tensor), ~9e-4 (rows) and ~6e-4 (states), under the stated 2e-3.
+    (tensor), ~9e-4 (rows) and ~6e-4 (states), under the stated 2e-3; with
+    the operands the tensor core reads from TMEM truncated, as the kernel runs
+    them, at ~1.8e-3, ~1.4e-3 and ~9e-4.
 """
 import numpy as np
 import torch
@@ -41,7 +43,17 @@ def _tf32(x):
     return (((f + 0x1000) & 0xFFFFE000).astype(np.uint32)).view(np.float32).astype(np.float64)
 
 
-ROUND = {"x": lambda m: m, "bf16": _bf16, "tf32": _tf32}
+def _tf32_trunc(x):
+    """tf32 by truncation: what the tensor core reads from an fp32 operand."""
+    f = np.ascontiguousarray(x, np.float32).view(np.uint32) & np.uint32(0xFFFFE000)
+    return f.view(np.float32).astype(np.float64)
+
+
+ROUND = {"x": lambda m: m, "bf16": _bf16, "tf32": _tf32, "tf32t": _tf32_trunc}
+# The tf32 prefill: operands written to shared memory are rounded to nearest;
+# operands the tensor core reads from TMEM as fp32 accumulators or state (the
+# state, S^T K^T, Delta) are truncated by the tensor core itself.
+TF32_KERNEL = dict({o: "tf32" for o in OPERANDS}, S="tf32t", E="tf32t", Do="tf32t", Dt="tf32t")
 
 
 def _features(shape, seed, n_tok):
@@ -148,6 +160,18 @@ def test_tf32_operands_sit_under_the_stated_bound():
     assert whole < 0.95 * PREFILL_TOL, whole
     assert row < 0.6 * PREFILL_TOL, row
     assert state < 0.5 * PREFILL_TOL, state
+    # as the kernel runs them (TMEM operands truncated): ~1.8e-3, ~1.4e-3, ~9e-4
+    whole, row, state = _measure(TF32_KERNEL)
+    assert whole < 0.95 * PREFILL_TOL, whole
+    assert row < 0.8 * PREFILL_TOL, row
+    assert state < 0.6 * PREFILL_TOL, state
+
+
+def test_truncating_every_operand_would_miss():
+    """Rounding the shared-memory operands to nearest is needed: truncation is
+    biased, and with every operand truncated the output misses 2e-3."""
+    whole, _, _ = _measure({o: "tf32t" for o in OPERANDS})
+    assert whole > PREFILL_TOL, whole
 
 
 def test_model_without_rounding_is_the_exact_form():
