@@ -108,9 +108,10 @@ struct __align__(1024) Smem32 {
       float A[kC * kAX];
       float X[kC * kAX];
       float Y[2048];
+      float L0[8][3][64];  // per 8 x 8 diagonal block: L^2, L^4, (I - L)(I + L^2)
     } sv;  // the solve's scratch (after the features have read the inputs)
   };
-  float g[kC], beta[kC], b[kC], eb[kC], ebl[kC];
+  float g[2][kC], beta[2][kC], b[2][kC], eb[2][kC], ebl[2][kC];  // by chunk parity
   float rk[kC];  // 1 / sqrt(|y_k|^2 + eps) per token
   float rq[kC];  // dk^-1/2 / sqrt(|y_q|^2 + eps) per token
   uint64_t ld_bar, mma_bar;
@@ -143,8 +144,9 @@ __device__ __forceinline__ int ix(int r, int c) { return r * kAX + c; }
 // every entry of X above the diagonal is zero (X is cleared first), so the
 // sums run over whole rows and columns.  Each entry of X is written out as
 // T1 = rk_i X_ij beta_j and T2 = -rk_i X_ij beta_j e^{b_j} rk_j (tf32).
-// Y: 1024 floats of scratch.  512 threads; the caller synchronises before (A
-// complete, X cleared) and after.
+// Y: 1024 floats of scratch, L0: 8 x 3 x 64.  512 threads (warps 8..15 wait
+// at the first barrier while warps 0..7 invert the diagonal blocks); the
+// caller synchronises before (A complete, X cleared) and after.
 struct TOut {
   uint8_t* t1;
   uint8_t* t2;
@@ -159,29 +161,53 @@ __device__ __forceinline__ void put_t(const TOut& o, int r, int c, float x) {
   *reinterpret_cast<float*>(o.t2 + off) = umma::tf32_round(-t * o.eb[c] * o.rk[c]);
 }
 
-__device__ __forceinline__ void solve_T(const float* A, float* X, float* Y, const TOut& to) {
+__device__ __forceinline__ void solve_T(const float* A, float* X, float* Y, float (*L0)[3][64], const TOut& to) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // 8 x 8 diagonal blocks: thread t < 64 = block t / 8, column t % 8
-  if (tid < kC) {
-    const int o = 8 * (tid >> 3), c = tid & 7;
-    float a[28];
+  // 8 x 8 diagonal blocks: warp w < 8 inverts block w, L = A_ww (strictly
+  // lower, so L^8 = 0), as (I + L)^-1 = (I - L)(I + L^2)(I + L^4); lane l
+  // holds entries (l / 4, 2 (l % 4)) and (l / 4, 2 (l % 4) + 1)
+  if (warp < 8) {
+    const int o = 8 * warp, i = lane >> 2, j = 2 * (lane & 3);
+    float* L2 = L0[warp][0];
+    float* L4 = L0[warp][1];
+    float* B = L0[warp][2];
+    auto Lw = [&](int r, int c) { return A[ix(o + r, o + c)]; };
+    float s0 = 0.f, s1 = 0.f;  // L^2
 #pragma unroll
-    for (int r = 1, i = 0; r < 8; ++r)
-#pragma unroll
-      for (int m = 0; m < r; ++m, ++i) a[i] = A[ix(o + r, o + m)];
-    float x[8];
-#pragma unroll
-    for (int r = 0, i = 0; r < 8; ++r) {
-      float s = (r == c) ? 1.f : 0.f;
-#pragma unroll
-      for (int m = 0; m < r; ++m, ++i) s = fmaf(-a[i], x[m], s);
-      x[r] = (r < c) ? 0.f : s;
+    for (int k = 0; k < 8; ++k) {
+      const float lik = Lw(i, k);
+      s0 = fmaf(lik, Lw(k, j), s0);
+      s1 = fmaf(lik, Lw(k, j + 1), s1);
     }
+    L2[8 * i + j] = s0;
+    L2[8 * i + j + 1] = s1;
+    __syncwarp();
+    float q0 = 0.f, q1 = 0.f, c0 = 0.f, c1 = 0.f;  // L^4 and L^3 = L L^2
 #pragma unroll
-    for (int r = 0; r < 8; ++r) X[ix(o + r, o + c)] = x[r];
+    for (int k = 0; k < 8; ++k) {
+      const float l2 = L2[8 * i + k], l1 = Lw(i, k);
+      q0 = fmaf(l2, L2[8 * k + j], q0);
+      q1 = fmaf(l2, L2[8 * k + j + 1], q1);
+      c0 = fmaf(l1, L2[8 * k + j], c0);
+      c1 = fmaf(l1, L2[8 * k + j + 1], c1);
+    }
+    L4[8 * i + j] = q0;
+    L4[8 * i + j + 1] = q1;
+    // B = (I - L)(I + L^2) = I - L + L^2 - L^3
+    B[8 * i + j] = (i == j ? 1.f : 0.f) - Lw(i, j) + s0 - c0;
+    B[8 * i + j + 1] = (i == j + 1 ? 1.f : 0.f) - Lw(i, j + 1) + s1 - c1;
+    __syncwarp();
+    float x0 = B[8 * i + j], x1 = B[8 * i + j + 1];  // X = B + B L^4
 #pragma unroll
-    for (int r = 0; r < 8; ++r)
-      if (r >= c) put_t(to, o + r, o + c, x[r]);
+    for (int k = 0; k < 8; ++k) {
+      const float bk = B[8 * i + k];
+      x0 = fmaf(bk, L4[8 * k + j], x0);
+      x1 = fmaf(bk, L4[8 * k + j + 1], x1);
+    }
+    X[ix(o + i, o + j)] = x0;
+    X[ix(o + i, o + j + 1)] = x1;
+    if (j <= i) put_t(to, o + i, o + j, x0);
+    if (j + 1 <= i) put_t(to, o + i, o + j + 1, x1);
   }
   __syncthreads();
   // 8 -> 16: pair p (rows 16p + 8 .., columns 16p ..), entry (i, j) per thread
@@ -307,17 +333,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t ID_N64 = umma::idesc_tf32(128, 64, false, false);
   constexpr uint32_t ID_N128 = umma::idesc_tf32(128, 128, false, false);
 
-  // feature channels of this thread: q/k channel cqk (k for tid % 256 < 128,
-  // else q) for tokens 32 th .., and v channel lrow for tokens 16 qq ..
-  const bool isq = (tid & 255) >= 128;
-  const int cqk = tid & 127;
-  const int th = tid >> 8;
-  const int gch_qk = (isq ? hq : a.hk + hq) * kD + cqk;
+  // feature channels of this thread: the q/k channel pair (2 cp, 2 cp + 1)
+  // (k for tid % 128 < 64, else q) for tokens 16 qq .., and v channel lrow
+  // for the same tokens
+  const bool isq = (tid & 127) >= 64;
+  const int cp = tid & 63;
+  const int gch_qk = (isq ? hq : a.hk + hq) * kD + 2 * cp;
   const int gch_v = 2 * a.hk * kD + h * kD + lrow;
-  float wqk[4], wv[4];
+  float2 wqk[4];
+  float wv[4];
   {
     const float4 w4 = *reinterpret_cast<const float4*>(a.conv_w + (size_t)gch_qk * 4);
-    wqk[0] = w4.x; wqk[1] = w4.y; wqk[2] = w4.z; wqk[3] = w4.w;
+    const float4 u4 = *reinterpret_cast<const float4*>(a.conv_w + (size_t)(gch_qk + 1) * 4);
+    wqk[0] = make_float2(w4.x, u4.x); wqk[1] = make_float2(w4.y, u4.y);
+    wqk[2] = make_float2(w4.z, u4.z); wqk[3] = make_float2(w4.w, u4.w);
     const float4 v4 = *reinterpret_cast<const float4*>(a.conv_w + (size_t)gch_v * 4);
     wv[0] = v4.x; wv[1] = v4.y; wv[2] = v4.z; wv[3] = v4.w;
   }
@@ -347,14 +376,53 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int q = 0; q < 3; ++q) tma_load_2d(&S.raw[q][0][0], &qmap, part_x[q], row0, &S.ld_bar);
   };
-  // gate inputs of chunk c's token tid (threads 0..63), loaded one chunk ahead
+  // gate inputs of chunk c's token tid - 256 (threads 256..319), loaded one
+  // chunk ahead
   auto load_gates = [&](int c, float& av, float& bv) {
-    const int64_t pos = (p0 / kC + c) * kC + tid;
+    const int64_t pos = (p0 / kC + c) * kC + (tid - 8 * 32);
     av = bv = 0.f;
     if (c < nch && pos >= p0 && pos < p1) {
       const size_t tok = (size_t)(t0 + pos - p0);
       av = __bfloat162float(a.a[tok * a.hv + h]);
       bv = __bfloat162float(a.b[tok * a.hv + h]);
+    }
+  };
+
+  // gates of chunk cc into buffer buf (warps 8 and 9: thread 256 + t for
+  // token t, with the inputs loaded one chunk ahead in ga, gb; outside the
+  // sequence g = beta = 0), then the cumulative log decay b, e^b and
+  // e^{b_last - b} (warp 8)
+  const int gt = tid - 8 * 32;  // token of a gate thread
+  const bool gate_thread = gt >= 0 && gt < kC;
+  float ga = 0.f, gb = 0.f;
+  auto gates_into = [&](int cc, int buf) {
+    if (gate_thread) {
+      const int64_t pos = (p0 / kC + cc) * kC + gt;
+      const bool in = pos >= p0 && pos < p1;
+      S.g[buf][gt] = in ? floor_log_decay(-eA * softplus_f(ga + dtb)) : 0.f;
+      S.beta[buf][gt] = in ? sigmoid_f(gb) : 0.f;
+      load_gates(cc + 1, ga, gb);
+      named_sync(1, kC);
+    }
+    if (warp == 8) {
+      float bv[2], carry = 0.f;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float v = S.g[buf][32 * hh + lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float u = __shfl_up_sync(0xffffffffu, v, o);
+          if (lane >= o) v += u;
+        }
+        bv[hh] = v + carry;
+        carry = __shfl_sync(0xffffffffu, bv[hh], 31);
+      }
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        S.b[buf][32 * hh + lane] = bv[hh];
+        S.eb[buf][32 * hh + lane] = expf(bv[hh]);
+        S.ebl[buf][32 * hh + lane] = expf(carry - bv[hh]);
+      }
     }
   };
 
@@ -376,8 +444,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     issue_raw(0);
     ld_issued = 1;
   }
-  float ga = 0.f, gb = 0.f;
-  if (tid < kC) load_gates(0, ga, gb);
+  if (gate_thread) load_gates(0, ga, gb);
+  gates_into(0, 0);
 
   bool bad = false;
   uint32_t mph = 0;
@@ -398,38 +466,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (; c < nch; ++c) {
     const int64_t P = (p0 / kC + c) * kC;
     const bool full = P >= p0 && P + kC <= p1;
-    // gates of the chunk's tokens (outside the sequence: g = beta = 0)
-    if (tid < kC) {
-      const int64_t pos = P + tid;
-      const bool in = pos >= p0 && pos < p1;
-      S.g[tid] = in ? floor_log_decay(-eA * softplus_f(ga + dtb)) : 0.f;
-      S.beta[tid] = in ? sigmoid_f(gb) : 0.f;
-      load_gates(c + 1, ga, gb);
-    }
+    const int gbuf = c & 1;
+    // tokens tlo .. thi - 1 of the chunk lie inside the sequence
+    const int tlo = (int)(p0 > P ? (p0 - P < kC ? p0 - P : kC) : 0);
+    const int thi = (int)(p1 > P ? (p1 - P < kC ? p1 - P : kC) : 0);
+    const float* gb_ = S.b[gbuf];
+    const float* geb = S.eb[gbuf];
+    const float* gebl = S.ebl[gbuf];
+    const float* gbeta = S.beta[gbuf];
     // the previous chunk's tensor stores have read the kq tile (checkpoint
-    // staging) and the t2 tile (output staging)
+    // staging) and the t2 tile (output staging); the gates of this chunk are
+    // in buffer gbuf
     if (tid == 0) bulk_wait_read();
-    __syncthreads();
-    if (warp == 0) {  // cumulative log decay b, e^b, e^{b_last - b}
-      float bv[2], carry = 0.f;
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        float v = S.g[32 * hh + lane];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float u = __shfl_up_sync(0xffffffffu, v, o);
-          if (lane >= o) v += u;
-        }
-        bv[hh] = v + carry;
-        carry = __shfl_sync(0xffffffffu, bv[hh], 31);
-      }
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        S.b[32 * hh + lane] = bv[hh];
-        S.eb[32 * hh + lane] = expf(bv[hh]);
-        S.ebl[32 * hh + lane] = expf(carry - bv[hh]);
-      }
-    }
     // the chunk's raw rows landed
     if (!wait_all(&S.ld_bar, c & 1)) break;
     ld_done = c + 1;
@@ -448,46 +496,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncthreads();
     }
 
-    // ---- features: conv1d + SiLU, one channel per thread down the chunk ----
-    // (each channel's raw rows are loaded into registers first, so that no
+    // ---- features: conv1d + SiLU, down the chunk ---------------------------
+    // (each thread's raw rows are loaded into registers first, so that no
     // shared-memory store of the results has to wait for, or hold up, them)
     {
-      // q or k, tokens 32 th ..: the [Y_K ; Y_Q] column of this channel, and
-      // for k the K~^T row
-      const int tk = 32 * th;
-      float y[32];
+      const int tk = 16 * qq;
+      // q or k: a channel pair, as packed fp32 pairs; its [Y_K ; Y_Q]
+      // columns and, for k, its two K~^T rows
+      float2 y[16];
       {
-        const __nv_bfloat16* xs = &S.raw[isq ? 0 : 1][tk][cqk];
-        float x[35];
+        const __nv_bfloat162* xs = reinterpret_cast<const __nv_bfloat162*>(&S.raw[isq ? 0 : 1][tk][2 * cp]);
+        float2 x[19];
 #pragma unroll
-        for (int r = 0; r < 35; ++r) x[r] = __bfloat162float(xs[r * kD]);
+        for (int r = 0; r < 19; ++r) x[r] = __bfloat1622float2(xs[r * (kD / 2)]);
 #pragma unroll
-        for (int t = 0; t < 32; ++t) {
-          float acc = wqk[0] * x[t];
-          acc = fmaf(wqk[1], x[t + 1], acc);
-          acc = fmaf(wqk[2], x[t + 2], acc);
-          acc = fmaf(wqk[3], x[t + 3], acc);
-          const bool valid = full || (P + tk + t >= p0 && P + tk + t < p1);
-          y[t] = valid ? umma::tf32_round(silu_fast(acc)) : 0.f;
+        for (int t = 0; t < 16; ++t) {
+          float2 acc = mul2(wqk[0], x[t]);
+          acc = fma2(wqk[1], x[t + 1], acc);
+          acc = fma2(wqk[2], x[t + 2], acc);
+          acc = fma2(wqk[3], x[t + 3], acc);
+          const bool valid = (unsigned)(tk + t - tlo) < (unsigned)(thi - tlo);
+          y[t] = valid ? make_float2(umma::tf32_round(silu_fast(acc.x)), umma::tf32_round(silu_fast(acc.y)))
+                       : make_float2(0.f, 0.f);
         }
       }
       const int R0 = (isq ? kC : 0) + tk;
 #pragma unroll
-      for (int t = 0; t < 32; ++t) *reinterpret_cast<float*>(S.kq + f32_off(R0 + t, cqk, 128 * 128)) = y[t];
+      for (int t = 0; t < 16; ++t) *reinterpret_cast<float2*>(S.kq + f32_off(R0 + t, 2 * cp, 128 * 128)) = y[t];
       if (!isq) {
 #pragma unroll
-        for (int t4 = 0; t4 < 8; ++t4) {
-          const float4 e4 = *reinterpret_cast<const float4*>(&S.ebl[tk + 4 * t4]);
-          *reinterpret_cast<float4*>(S.kt + f32_off(cqk, tk + 4 * t4, 128 * 128)) =
-              make_float4(umma::tf32_round(y[4 * t4] * e4.x), umma::tf32_round(y[4 * t4 + 1] * e4.y),
-                          umma::tf32_round(y[4 * t4 + 2] * e4.z), umma::tf32_round(y[4 * t4 + 3] * e4.w));
+        for (int t4 = 0; t4 < 4; ++t4) {
+          const float4 e4 = *reinterpret_cast<const float4*>(&gebl[tk + 4 * t4]);
+          *reinterpret_cast<float4*>(S.kt + f32_off(2 * cp, tk + 4 * t4, 128 * 128)) =
+              make_float4(umma::tf32_round(y[4 * t4].x * e4.x), umma::tf32_round(y[4 * t4 + 1].x * e4.y),
+                          umma::tf32_round(y[4 * t4 + 2].x * e4.z), umma::tf32_round(y[4 * t4 + 3].x * e4.w));
+          *reinterpret_cast<float4*>(S.kt + f32_off(2 * cp + 1, tk + 4 * t4, 128 * 128)) =
+              make_float4(umma::tf32_round(y[4 * t4].y * e4.x), umma::tf32_round(y[4 * t4 + 1].y * e4.y),
+                          umma::tf32_round(y[4 * t4 + 2].y * e4.z), umma::tf32_round(y[4 * t4 + 3].y * e4.w));
         }
       }
-      // v: channel lrow, tokens 16 qq .., into TMEM
-      const int tv = 16 * qq;
+      // v: channel lrow, into TMEM
       float vv[16];
       {
-        const __nv_bfloat16* xv = &S.raw[2][tv][lrow];
+        const __nv_bfloat16* xv = &S.raw[2][tk][lrow];
         float x[19];
 #pragma unroll
         for (int r = 0; r < 19; ++r) x[r] = __bfloat162float(xv[r * kD]);
@@ -497,11 +548,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc = fmaf(wv[1], x[t + 1], acc);
           acc = fmaf(wv[2], x[t + 2], acc);
           acc = fmaf(wv[3], x[t + 3], acc);
-          const bool valid = full || (P + tv + t >= p0 && P + tv + t < p1);
+          const bool valid = (unsigned)(tk + t - tlo) < (unsigned)(thi - tlo);
           vv[t] = valid ? umma::tf32_round(silu_fast(acc)) : 0.f;
         }
       }
-      umma::tmem_st16(tlane + TM_V + tv, vv);
+      umma::tmem_st16(tlane + TM_V + tk, vv);
     }
     // operands visible to the tensor core, then P = [Y_K;Y_Q] [Y_K;Y_Q]^T
     umma::fence_proxy_async();
@@ -517,9 +568,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       umma::commit(&S.mma_bar);
     }
-    // X is cleared for the solve meanwhile (the raw rows are read)
+    // meanwhile X is cleared for the solve (the raw rows are read) and T2 for
+    // its lower triangle (its tile held the previous chunk's output staging)
     for (int e = tid; e < kC * kAX / 4; e += kThreads)
       reinterpret_cast<float4*>(S.sv.X)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int e = tid; e < (int)(sizeof(S.t2) / 16); e += kThreads)
+      reinterpret_cast<uint4*>(S.t2)[e] = make_uint4(0u, 0u, 0u, 0u);
     if (!mma_wait()) break;
     // ---- norms from P's diagonal: rk_i (K block), rq_i (Q block) ------------
     // warps 0..3: lane quarter w holds the diagonal entries (lrow, lrow) in
@@ -545,14 +599,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       float bc[16], rkc[16];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float4 b4 = *reinterpret_cast<const float4*>(&S.b[c0 + 4 * i]);
+        const float4 b4 = *reinterpret_cast<const float4*>(&gb_[c0 + 4 * i]);
         bc[4 * i] = b4.x; bc[4 * i + 1] = b4.y; bc[4 * i + 2] = b4.z; bc[4 * i + 3] = b4.w;
         const float4 r4 = *reinterpret_cast<const float4*>(&S.rk[c0 + 4 * i]);
         rkc[4 * i] = r4.x; rkc[4 * i + 1] = r4.y; rkc[4 * i + 2] = r4.z; rkc[4 * i + 3] = r4.w;
       }
       if (lrow < kC) {
         const int r = lrow;
-        const float br = S.b[r], fr = S.beta[r] * S.rk[r];
+        const float br = gb_[r], fr = gbeta[r] * S.rk[r];
         float av[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) av[i] = (c0 + i < r) ? fr * rkc[i] * v[i] * exp_ftz(br - bc[i]) : 0.f;
@@ -561,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<float4*>(S.sv.A + ix(r, c0 + 4 * q)) = make_float4(av[4 * q], av[4 * q + 1], av[4 * q + 2], av[4 * q + 3]);
       } else {
         const int r = lrow - kC;
-        const float br = S.b[r], fr = S.rq[r];
+        const float br = gb_[r], fr = S.rq[r];
         float m[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) m[i] = (c0 + i <= r) ? umma::tf32_round(fr * v[i] * exp_ftz(br - bc[i])) : 0.f;
@@ -571,12 +625,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               make_float4(m[4 * q], m[4 * q + 1], m[4 * q + 2], m[4 * q + 3]);
       }
     }
-    // T2 is rewritten (its tile held the previous chunk's output staging)
-    for (int e = tid; e < (int)(sizeof(S.t2) / 16); e += kThreads)
-      reinterpret_cast<uint4*>(S.t2)[e] = make_uint4(0u, 0u, 0u, 0u);
     umma::fence_before();
     __syncthreads();
-    solve_T(S.sv.A, S.sv.X, S.sv.Y, TOut{S.tm, S.t2, S.beta, S.eb, S.rk});
+    // the next chunk's gates (warps 8, 9) beside the solve's diagonal blocks
+    if (c + 1 < nch && (warp == 8 || warp == 9)) gates_into(c + 1, gbuf ^ 1);
+    solve_T(S.sv.A, S.sv.X, S.sv.Y, S.sv.L0, TOut{S.tm, S.t2, gbeta, geb, S.rk});
     umma::fence_proxy_async();
     __syncthreads();
     // the next chunk's raw rows (the solve's scratch is dead)
@@ -610,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma::commit(&S.mma_bar);
     }
     {
-      const float dec = S.eb[kC - 1];
+      const float dec = geb[kC - 1];
       float v[32];
       umma::tmem_ld32(tlane + TM_S + 32 * qq, v);
 #pragma unroll
@@ -642,7 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __nv_bfloat16* ot = reinterpret_cast<__nv_bfloat16*>(S.t2);
 #pragma unroll
       for (int i = 0; i < 16; ++i)
-        ot[(16 * qq + i) * kD + lrow] = __float2bfloat16_rn(fmaf(o1[i], S.rq[16 * qq + i] * S.eb[16 * qq + i], o2[i]));
+        ot[(16 * qq + i) * kD + lrow] = __float2bfloat16_rn(fmaf(o1[i], S.rq[16 * qq + i] * geb[16 * qq + i], o2[i]));
     }
     // checkpoint: the state rows, 128B-swizzled, into four 16 KB boxes (32
     // columns x 128 rows) in the dead kq tile, for four tensor stores
