@@ -509,8 +509,6 @@ __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const StepArgs a) {
 // ---------------------------------------------------------------------------
 constexpr int kTW = 16;
 
-__device__ __forceinline__ float2 lo2(float4 v) { return make_float2(v.x, v.y); }
-__device__ __forceinline__ float2 hi2(float4 v) { return make_float2(v.z, v.w); }
 
 struct KdaPrefillArgs {
   float* ssm;
@@ -920,17 +918,17 @@ bool use_tma_decode(const gdn_dims& d, int32_t B, const void* qkv, const gdn_par
   return 4L * B * d.hk > sm_count();
 }
 
-// Verify: the persistent TMA-fed kernel from 6 (request, V head) items per
-// SM up (Qwen3.5-shaped layer, T = 8: 0.74 / 0.83 / 0.89 of HBM at batch
-// 32 / 64 / 128 against 0.70 / 0.73 / 0.74 for the per-head kernel); below
-// that its per-item prologue (the q/k conv of every row block) is not hidden
-// and the per-head kernel is faster (batch 16: 0.72 against 0.57).
+// Verify: the persistent TMA-fed kernel from 3 (request, V head) heads per
+// SM up (Qwen3.5-shaped layer, T = 8, its work split evenly by 32-row stages:
+// 0.71 / 0.78 / 0.85 / 0.88 of HBM at batch 16 / 32 / 64 / 128 against 0.68
+// for the per-head kernel at batch 16); below that its per-segment prologue
+// (the q/k conv) is not hidden and the per-head kernel is faster.
 // GDN_DECODE_PATH=tma / rows forces either, for measurement.
 bool use_tma_verify(const gdn_dims& d, int32_t B, int32_t T, const void* qkv, const gdn_params& p) {
   if (!verify_tma_supported(d, T, qkv, p)) return false;
   const int f = forced_path();
   if (f) return f == 1;
-  return (long)B * d.hv >= 6L * sm_count();
+  return (long)B * d.hv >= 3L * sm_count();
 }
 
 gdn_status run_step(bool verify, bool kda, const gdn_dims* dims, const gdn_pool& work, const gdn_pool* spec,

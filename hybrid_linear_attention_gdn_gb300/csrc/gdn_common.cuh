@@ -159,6 +159,10 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
   return d;
 }
 
+__device__ __forceinline__ float2 lo2(float4 v) { return make_float2(v.x, v.y); }
+__device__ __forceinline__ float2 hi2(float4 v) { return make_float2(v.z, v.w); }
+__device__ __forceinline__ float4 join4(float2 lo, float2 hi) { return make_float4(lo.x, lo.y, hi.x, hi.y); }
+
 // ---- math (CUDA library functions; fp32) -----------------------------------
 // e^x as 2^(x log2 e) on the PTX ex2.approx.ftz instruction (relative error
 // ~2^-22 plus |x| 2^-24 from rounding the product; subnormal results flush to

@@ -6,13 +6,15 @@
 // working slot and writes the state after every draft into a spec slot; the
 // working slot is only read.
 //
-// Because nothing here is written in place, work splits freely: an item is one
-// request, one V head h and one block of R = dv/P rows (P chosen so that there
-// are several items per SM).  One CTA per SM walks a static item list:
-//   warp 8 (producer, one lane): per item, a bundle of bulk copies (the conv
-//     history rows and the T draft activations of the q/k channels of h's QK
-//     head and of the item's v channels, plus their conv weights), then the
-//     item's state rows in 16 KiB chunks through a ring of mbarrier-tracked
+// Because nothing here is written in place, work splits freely.  The unit of
+// work is one stage: 32 state rows of one request and V head.  Each CTA takes
+// an equal, contiguous share of the B * hv * dv/32 stages (so the last wave
+// ends evenly however B compares with the SM count) and walks it as segments
+// (the stages of one request and V head it holds):
+//   warp 8 (producer, one lane): per segment, a bundle of bulk copies (the
+//     conv history rows and the T draft activations of the q/k channels of h's
+//     QK head and of the segment's v channels, plus their conv weights), then
+//     its state rows in 16 KiB chunks through a ring of mbarrier-tracked
 //     shared-memory stages;
 //   warps 0-7: conv + SiLU over the draft sequence (and the snapshot conv
 //     histories, written straight to the spec slots), per-draft L2 norms and
@@ -96,8 +98,29 @@ struct VArgs {
   const void* b;
   void* out;
   uint32_t* err;
-  int32_t hk, hv, dv, C, G, P, T, n_items;
+  int32_t hk, hv, dv, C, G, T;
+  int32_t sph;      // stages (32 rows) per V head: dv / 32
+  int64_t n_units;  // B * hv * sph
 };
+
+// The segment that starts at stage unit u of a CTA's share [.., u1): request
+// r, V head h, stages s0 .. s0 + ns - 1 of the head (rows 32 s0 ..), at most
+// kMaxR / 32 stages (the rows one bundle holds).
+struct Seg {
+  int r, h, s0, ns;
+};
+__device__ __forceinline__ Seg segment_at(const VArgs& a, int64_t u, int64_t u1) {
+  const int64_t hu = u / a.sph;
+  Seg g;
+  g.r = (int)(hu / a.hv);
+  g.h = (int)(hu % a.hv);
+  g.s0 = (int)(u % a.sph);
+  int64_t ns = a.sph - g.s0;
+  if (ns > u1 - u) ns = u1 - u;
+  if (ns > kMaxR / kRows) ns = kMaxR / kRows;
+  g.ns = (int)ns;
+  return g;
+}
 
 template <typename Tact, typename Tconv, int STAGES, int MT, int MINB, bool KDA>
 __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
@@ -108,11 +131,10 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   SM& S = *reinterpret_cast<SM*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int R = a.dv / a.P;
-  const int nchunks = R / kRows;
-  const int nch = 2 * kDK + R;
   const int T = a.T;
-  const int per_req = a.hv * a.P;  // items per request
+  // this CTA's share of the stage units
+  const int64_t u0 = (int64_t)blockIdx.x * a.n_units / gridDim.x;
+  const int64_t u1 = (int64_t)(blockIdx.x + 1) * a.n_units / gridDim.x;
   volatile int* abort_flag = &S.abort;
 
   if (tid == 0) {
@@ -133,12 +155,14 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
     // ------------------------------------------------------------ producer
     if (lane != 0) return;
     const uint32_t ec = sizeof(Tconv), ea = sizeof(Tact);
-    const uint32_t bundle_bytes =
-        (kW - 1) * nch * ec + T * nch * ea + nch * kW * 4 + (KDA ? T * kDK * ea + kDK * 4 : 0u);
     uint32_t n = 0, vk = 0;
     bool ok = true;
-    for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
-      const int r = item / per_req, h = (item % per_req) / a.P, p = item % a.P;
+    for (int64_t u = u0; u < u1 && ok;) {
+      const Seg g = segment_at(a, u, u1);
+      u += g.ns;
+      const int r = g.r, h = g.h, R = g.ns * kRows, nchunks = g.ns, nch = 2 * kDK + R;
+      const uint32_t bundle_bytes =
+          (kW - 1) * nch * ec + T * nch * ea + nch * kW * 4 + (KDA ? T * kDK * ea + kDK * 4 : 0u);
       const int32_t slot = a.slot_ids[r];
       if (slot_class(slot, a.num_slots)) continue;
       if (*abort_flag) break;
@@ -148,7 +172,7 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
       mbar_arrive_expect_tx(&S.bfull[bb], bundle_bytes);
       typename SM::Bundle& Bd = S.bundle[bb];
       const size_t cq = (size_t)hq * kDK, ck = (size_t)a.hk * kDK + cq,
-                   cv = 2 * (size_t)a.hk * kDK + (size_t)h * a.dv + (size_t)p * R;
+                   cv = 2 * (size_t)a.hk * kDK + (size_t)h * a.dv + (size_t)g.s0 * kRows;
       const Tconv* hist = reinterpret_cast<const Tconv*>(a.conv) + (size_t)slot * (kW - 1) * a.C;
       for (int j = 0; j < kW - 1; ++j) {
         bulk_g2s(&Bd.hist[j][0], hist + (size_t)j * a.C + cq, kDK * ec, &S.bfull[bb]);
@@ -171,7 +195,7 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
         bulk_g2s(&Bd.gdt[0], a.dt_bias + (size_t)h * kDK, kDK * 4, &S.bfull[bb]);
       }
       ++vk;
-      const float* src = a.ssm + (((size_t)slot * a.hv + h) * a.dv + (size_t)p * R) * kDK;
+      const float* src = a.ssm + (((size_t)slot * a.hv + h) * a.dv + (size_t)g.s0 * kRows) * kDK;
       for (int c = 0; c < nchunks; ++c, ++n) {
         const int st = n % STAGES;
         if (*abort_flag || !mbar_wait(&S.empty[st], ((n / STAGES) & 1) ^ 1)) { ok = false; break; }
@@ -193,22 +217,25 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
   const int seg = lane % kLPR;
   const int rloc = warp * (32 / kLPR) + lane / kLPR;
   uint32_t n = 0, vk = 0;
-  for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
-    const int r = item / per_req, h = (item % per_req) / a.P, p = item % a.P;
+  for (int64_t u = u0; u < u1;) {
+    const Seg g = segment_at(a, u, u1);
+    u += g.ns;
+    const int r = g.r, h = g.h, R = g.ns * kRows, nchunks = g.ns, nch = 2 * kDK + R;
+    const int row0 = g.s0 * kRows;  // first row of the segment within the head
     const int hq = h / a.G;
     const int32_t slot = a.slot_ids[r];
     const int32_t* sids = a.spec_ids + (size_t)r * T;
     const int cls = slot_class(slot, a.num_slots);
     if (cls) {
-      if (cls == 2 && h == 0 && p == 0 && tid == 0) report(a.err, GDN_DEV_ERR_SLOT_OOB);
+      if (cls == 2 && h == 0 && g.s0 == 0 && tid == 0) report(a.err, GDN_DEV_ERR_SLOT_OOB);
       for (int e = tid; e < T * R; e += kCons) {
         const int t = e / R, i = e % R;
-        reinterpret_cast<Tact*>(a.out)[(((size_t)r * T + t) * a.hv + h) * a.dv + p * R + i] =
+        reinterpret_cast<Tact*>(a.out)[(((size_t)r * T + t) * a.hv + h) * a.dv + row0 + i] =
             from_f32<Tact>(0.f);
       }
       continue;
     }
-    if (h == 0 && p == 0 && tid < T && slot_class(sids[tid], a.spec_num_slots) == 2)
+    if (h == 0 && g.s0 == 0 && tid < T && slot_class(sids[tid], a.spec_num_slots) == 2)
       report(a.err, GDN_DEV_ERR_SLOT_OOB);
     const int bb = vk & 1;
     if (!*abort_flag && !mbar_wait(&S.bfull[bb], (vk >> 1) & 1)) *abort_flag = 1;
@@ -216,15 +243,15 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
     if (*abort_flag) break;
     const typename SM::Bundle& Bd = S.bundle[bb];
     // conv over the drafts; the snapshot history after draft t is
-    // [win1, win2, x_t].  q/k channels are written by the (p = 0) item of the
-    // first V head of the QK group, v channels by their own item.
-    const bool qk_writer = (h % a.G) == 0 && p == 0;
+    // [win1, win2, x_t].  q/k channels are written by the segment holding row
+    // 0 of the first V head of the QK group, v channels by their own segment.
+    const bool qk_writer = (h % a.G) == 0 && g.s0 == 0;
     for (int i = tid; i < nch; i += kCons) {
       const float4 w = *reinterpret_cast<const float4*>(&Bd.w[i * kW]);
       float w0 = to_f32(Bd.hist[0][i]), w1 = to_f32(Bd.hist[1][i]), w2 = to_f32(Bd.hist[2][i]);
       const size_t c = i < kDK ? (size_t)hq * kDK + i
                      : i < 2 * kDK ? (size_t)a.hk * kDK + (size_t)hq * kDK + (i - kDK)
-                                   : 2 * (size_t)a.hk * kDK + (size_t)h * a.dv + (size_t)p * R + (i - 2 * kDK);
+                                   : 2 * (size_t)a.hk * kDK + (size_t)h * a.dv + (size_t)row0 + (i - 2 * kDK);
       const bool writes = i >= 2 * kDK || qk_writer;
       for (int t = 0; t < T; ++t) {
         const float xv = to_f32(Bd.x[t][i]);
@@ -286,40 +313,46 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
       }
     }
     named_sync(kBarCons, kCons);
+    // q^ and k^ normalised in place, once per segment rather than per row
+    for (int e = tid; e < T * 2 * kDK; e += kCons) {
+      const int t = e / (2 * kDK), i = e % (2 * kDK);
+      S.sy[t][i] *= S.snorm[t][i < kDK ? 0 : 1];
+    }
+    named_sync(kBarCons, kCons);
 
     for (int c = 0; c < nchunks; ++c, ++n) {
       const int st = n % STAGES;
       if (!*abort_flag && !mbar_wait(&S.full[st], (n / STAGES) & 1)) *abort_flag = 1;
       if (*abort_flag) continue;
-      const int row = c * kRows + rloc;  // row within the item
+      const int row = c * kRows + rloc;  // row within the segment
       float4 s4[4];
       const float* srow = S.ring[st] + rloc * kDK;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc)
         s4[cc] = *reinterpret_cast<const float4*>(srow + cc * 4 * kLPR + seg * 4);
       for (int t = 0; t < T; ++t) {
-        const float rq = S.snorm[t][0], rk = S.snorm[t][1], kq = S.snorm[t][2];
+        const float kq = S.snorm[t][2];
         const float alpha = S.sgate[t][0], beta = S.sgate[t][1];
         float4 kk[4], qq[4];
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           const int col = cc * 4 * kLPR + seg * 4;
-          const float4 k4 = *reinterpret_cast<const float4*>(&S.sy[t][kDK + col]);
-          const float4 q4 = *reinterpret_cast<const float4*>(&S.sy[t][col]);
-          kk[cc] = make_float4(k4.x * rk, k4.y * rk, k4.z * rk, k4.w * rk);
-          qq[cc] = make_float4(q4.x * rq, q4.y * rq, q4.z * rq, q4.w * rq);
+          kk[cc] = *reinterpret_cast<const float4*>(&S.sy[t][kDK + col]);
+          qq[cc] = *reinterpret_cast<const float4*>(&S.sy[t][col]);
           if constexpr (KDA) {
             // the row becomes St diag(alpha) before its products
             const float4 al = *reinterpret_cast<const float4*>(&S.sal[t][col]);
-            s4[cc] = make_float4(s4[cc].x * al.x, s4[cc].y * al.y, s4[cc].z * al.z, s4[cc].w * al.w);
+            s4[cc] = join4(mul2(lo2(s4[cc]), lo2(al)), mul2(hi2(s4[cc]), hi2(al)));
           }
         }
-        float dk_ = 0.f, dq_ = 0.f;
+        // the row's dot products with k^ and q^, on packed fp32 pairs
+        float2 dk2 = make_float2(0.f, 0.f), dq2 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
-          dk_ += s4[cc].x * kk[cc].x + s4[cc].y * kk[cc].y + s4[cc].z * kk[cc].z + s4[cc].w * kk[cc].w;
-          dq_ += s4[cc].x * qq[cc].x + s4[cc].y * qq[cc].y + s4[cc].z * qq[cc].z + s4[cc].w * qq[cc].w;
+          dk2 = fma2(hi2(s4[cc]), hi2(kk[cc]), fma2(lo2(s4[cc]), lo2(kk[cc]), dk2));
+          dq2 = fma2(hi2(s4[cc]), hi2(qq[cc]), fma2(lo2(s4[cc]), lo2(qq[cc]), dq2));
         }
+        float dk_ = dk2.x + dk2.y, dq_ = dq2.x + dq2.y;
 #pragma unroll
         for (int o = kLPR / 2; o; o >>= 1) {
           dk_ += __shfl_xor_sync(0xffffffffu, dk_, o);
@@ -327,17 +360,17 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
         }
         // KDA: alpha is 1 here (the rows carry the per-channel decay already)
         const float bu = beta * (S.sy[t][2 * kDK + row] - alpha * dk_);
+        const float2 bu2 = make_float2(bu, bu), al2 = make_float2(alpha, alpha);
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
-          s4[cc].x = fmaf(bu, kk[cc].x, KDA ? s4[cc].x : alpha * s4[cc].x);
-          s4[cc].y = fmaf(bu, kk[cc].y, KDA ? s4[cc].y : alpha * s4[cc].y);
-          s4[cc].z = fmaf(bu, kk[cc].z, KDA ? s4[cc].z : alpha * s4[cc].z);
-          s4[cc].w = fmaf(bu, kk[cc].w, KDA ? s4[cc].w : alpha * s4[cc].w);
+          const float2 lo = KDA ? lo2(s4[cc]) : mul2(al2, lo2(s4[cc]));
+          const float2 hi = KDA ? hi2(s4[cc]) : mul2(al2, hi2(s4[cc]));
+          s4[cc] = join4(fma2(bu2, lo2(kk[cc]), lo), fma2(bu2, hi2(kk[cc]), hi));
         }
         const int32_t sid = sids[t];
         if (slot_class(sid, a.spec_num_slots) == 0) {
           float4* drow = reinterpret_cast<float4*>(
-              a.spec_ssm + (((size_t)sid * a.hv + h) * a.dv + (size_t)p * R + row) * kDK);
+              a.spec_ssm + (((size_t)sid * a.hv + h) * a.dv + (size_t)row0 + row) * kDK);
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) st_stream(drow + (cc * 4 * kLPR + seg * 4) / 4, s4[cc]);
         }
@@ -350,7 +383,7 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
     if (*abort_flag) break;
     for (int e = tid; e < T * R; e += kCons) {
       const int t = e / R, i = e % R;
-      reinterpret_cast<Tact*>(a.out)[(((size_t)r * T + t) * a.hv + h) * a.dv + p * R + i] =
+      reinterpret_cast<Tact*>(a.out)[(((size_t)r * T + t) * a.hv + h) * a.dv + row0 + i] =
           from_f32<Tact>(S.so[t][i]);
     }
   }
@@ -370,7 +403,7 @@ cudaError_t launch_v(const VArgs& a, cudaStream_t s) {
     attr_set[dev] = true;
   }
   const int slots = sm_count() * MINB;
-  const int grid = a.n_items < slots ? a.n_items : slots;
+  const int grid = a.n_units < slots ? (int)a.n_units : slots;
   return launch_plain(k, dim3((unsigned)grid), dim3(kThr), sizeof(SM), s, dim3(1), a);
 }
 
@@ -429,19 +462,9 @@ cudaError_t verify_tma_launch(const gdn_dims& d, const gdn_pool& work, const gdn
   a.C = (int32_t)channels(d);
   a.G = d.hv / d.hk;
   a.T = T;
-  // row blocks per head: the fewest that fit (R = dv/P <= 128).  Each item
-  // repeats the q/k conv prologue, which costs more than the load imbalance
-  // of fewer, larger items (Qwen3.5-shaped layer, T = 8, one head per item vs
-  // two row blocks: batch 32: 0.76 vs 0.74 of HBM; batch 64: 0.84 vs 0.79).
-  int P = 1;
-  while (d.dv / P > kMaxR) P *= 2;
-  if (const char* e = std::getenv("GDN_VERIFY_P")) {  // row blocks per head, for measurement
-    const int f = std::atoi(e);
-    if (f == 1 || f == 2 || f == 4) P = f;
-  }
-  if (d.dv % P || (d.dv / P) % kRows || d.dv / P > kMaxR) return cudaErrorInvalidValue;
-  a.P = P;
-  a.n_items = B * d.hv * P;
+  if (d.dv % kRows) return cudaErrorInvalidValue;
+  a.sph = d.dv / kRows;
+  a.n_units = (int64_t)B * d.hv * a.sph;
   return kda ? launch_v_kda<true>(d, a, s) : launch_v_kda<false>(d, a, s);
 }
 
