@@ -44,15 +44,17 @@ POOL = 512
 DECODE_TOKEN_BYTES = 2 * 2097152 + 2 * 49152 + 16384 + 128 + 8192 + 4
 DECODE_STEP_PARAM_BYTES = 8192 * 4 * 4 + 2 * 32 * 4
 
-# ncu DRAM traffic (read + write bytes per launch) of the decode kernel, with
-# the sha256 of the kernel source it was captured on; reported only while the
-# source is unchanged.
+# ncu DRAM traffic (read + write bytes per launch) of the decode kernel on the
+# headline workload itself (profiles/decode_tma_kernel_b64_pool512_dram.md),
+# with the sha256 of the kernel source it was captured on; reported only while
+# the source is unchanged.
 DECODE_TRAFFIC = {
-    "bytes_per_launch": 138589440 + 78073856,
+    "bytes_per_launch": 138593024 + 76964864,
     "source_sha256": "5e61f0355ea21948c588c68cc2ad99a9a58d4a2e91d69b0250e34bab30c41f43",
-    "case": "batch 64 over a 128-slot pool (same requests per launch as the headline), one launch after "
-            "5 warm-up launches; written bytes fall short of the 138 MB of state written because part "
-            "of it is still dirty in L2 when the kernel ends",
+    "case": "batch 64 over the 512-slot pool with the headline's 8-set rotation, the sixth launch "
+            "(ncu dram__bytes_read.sum + dram__bytes_write.sum, one pass): reads are exactly the algorithmic "
+            "138.6 MB; part of the 134 MB of state written is still in L2 when the launch ends and leaves it "
+            "during the next launches, so the launch's own DRAM writes are 77 MB",
 }
 
 
