@@ -621,7 +621,23 @@ def measure_rows(gdn, synth, dev, stream, hbm_peak, bf16_peak, which="all", pref
             "TFLOPs": pflop / (pms * 1e-3) / 1e12,
             "frac_bf16_peak": pflop / (pms * 1e-3) / 1e12 / bf16_peak,
             "workspace_bytes": wsb}
-        del qkv, a, b, pout, wsp
+        # the same prefill with the readout epilogue (gated RMS norm): fused
+        # into the prefill's output, against the prefill then the epilogue
+        z = synth.normal((total, 32, 128), 1.5, g, shape.act_dtype).to(dev)
+        nw = torch.ones(128, dtype=torch.float32, device=dev)
+
+        def fg(i):
+            gdn.chunk_prefill_gated(dims, pool, ck, params, pids[i % 4], cu, sp, total, ck_ids, 256, qkv, a,
+                                    b, z, nw, 1e-6, pout, wsp)
+
+        def fs(i):
+            fp(i)
+            gdn.gated_rmsnorm(dims, pout, z, nw, 1e-6)
+        fg(0)
+        fs(0)
+        rows[f"chunk_prefill_gated_4x{S}"] = {"ms_fused": _events_time(fg, 5, stream),
+                                              "ms_prefill_then_epilogue": _events_time(fs, 5, stream)}
+        del qkv, a, b, pout, wsp, z
         torch.cuda.synchronize()
 
     def kda_rows():

@@ -69,6 +69,8 @@ EXPORTS = {
     "gdn_chunk_prefill_workspace_size": ([_PD, _I32, _I64], ctypes.c_size_t),
     "gdn_chunk_prefill": ([_PD, CPool, CPool, _PP, _P, _P, _P, _I32, _I64, _P, _I32, _I32,
                            _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P], _I32),
+    "gdn_chunk_prefill_gated": ([_PD, CPool, CPool, _PP, _P, _P, _P, _I32, _I64, _P, _I32, _I32,
+                                 _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, ctypes.c_size_t, _P, _P], _I32),
     "gdn_chunk_prefill_noalloc": ([_PD, CPool, CPool, _PP, _P, _P, _P, _I32, _I64, _P, _I32,
                                    _I32, _P, _P, _P, _P, _P, _P], _I32),
     "gdn_mixed_step": ([_PD, CPool, CPool, _PP, _P, _P, _P, _I32, _I32, _I64, _P, _I32, _I32, _P, _P,
@@ -284,6 +286,23 @@ def chunk_prefill(dims: Dims, pool: StatePool, ckpt: StatePool, params: LayerPar
                              _ptr(qkv), _ptr(a), _ptr(b), _ptr(out), _ptr(workspace), ws_bytes,
                              _ptr(dev_err), _stream(stream))
     _check("gdn_chunk_prefill", st)
+
+
+def chunk_prefill_gated(dims: Dims, pool: StatePool, ckpt: StatePool, params: LayerParams, slot_ids,
+                        cu_seqlens, start_pos, total_tokens: int, ckpt_ids, ckpt_block: int, qkv, a, b,
+                        z, weight, eps: float, y, workspace, dev_err=None, stream=None):
+    """chunk_prefill whose output is the gated RMS norm of the readout."""
+    L = load()
+    n_seq = int(slot_ids.shape[0])
+    max_ckpt = int(ckpt_ids.shape[1]) if ckpt_ids is not None and ckpt_ids.dim() == 2 else 0
+    cd, cp = dims.c(), params.c()
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = L.gdn_chunk_prefill_gated(ctypes.byref(cd), pool.c(), ckpt.c(), ctypes.byref(cp),
+                                   _ptr(slot_ids), _ptr(cu_seqlens), _ptr(start_pos), n_seq,
+                                   int(total_tokens), _ptr(ckpt_ids), max_ckpt, int(ckpt_block),
+                                   _ptr(qkv), _ptr(a), _ptr(b), _ptr(z), _ptr(weight), float(eps), _ptr(y),
+                                   _ptr(workspace), ws_bytes, _ptr(dev_err), _stream(stream))
+    _check("gdn_chunk_prefill_gated", st)
 
 
 def kda_prefill(dims: Dims, pool: StatePool, ckpt: StatePool, params: LayerParams, slot_ids, cu_seqlens,

@@ -10,7 +10,9 @@
 // reduction; lane l holds the EPL consecutive elements from l * EPL of a row
 // (one vector access when the row is full-width and aligned), the sum of
 // squares by a warp shuffle.  y may be o (each element is read before the
-// row's reduction and written after it, by the same lane).
+// row's reduction and written after it, by the same lane).  A variant with
+// 16-byte accesses (two rows per warp-wide access, eight rows per warp)
+// measured slower: 0.63 against 0.76 of the copy bandwidth.
 #include "gdn_common.cuh"
 
 namespace gdn {

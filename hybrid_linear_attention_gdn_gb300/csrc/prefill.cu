@@ -553,7 +553,7 @@ static gdn_status chunk_prefill_impl(bool launch, const gdn_dims* dims, gdn_pool
                                      int64_t total_tokens, const int32_t* ckpt_ids, int32_t max_ckpt,
                                      int32_t ckpt_block, const void* qkv, const void* a, const void* b,
                                      void* out, void* workspace, size_t workspace_bytes, uint32_t* dev_err,
-                                     void* stream) {
+                                     void* stream, const gdn::Tc32Epilogue* epi = nullptr) {
   using namespace gdn;
   gdn_status st = check_dims(dims);
   if (st != GDN_OK) return st;
@@ -618,8 +618,12 @@ static gdn_status chunk_prefill_impl(bool launch, const gdn_dims* dims, gdn_pool
   cudaError_t e = cudaErrorInvalidValue;
   const int act = dims->act_dtype, cv = dims->conv_dtype;
   if (path == PrefillPath::kTf32) {
+    // the readout epilogue fuses into the output when its operands allow the
+    // tile copies; otherwise it runs after the prefill, in place
+    const bool fuse = epi && aligned(epi->z, 16) && aligned(epi->weight, 16);
     e = prefill_tc32_launch(*dims, pool, ckpt, *params, slot_ids, cu_seqlens, start_pos, n_seq, total_tokens,
-                            ckpt_ids, max_ckpt, ckpt_block, qkv, a, b, out, dev_err, s);
+                            ckpt_ids, max_ckpt, ckpt_block, qkv, a, b, out, dev_err, s, fuse ? epi : nullptr);
+    if (fuse) epi = nullptr;
     if (e == cudaSuccess) e = launch_history(p, act, cv, s);
   } else if (path == PrefillPath::kBf16) {
     e = prefill_tc_launch(*dims, pool, ckpt, *params, slot_ids, cu_seqlens, start_pos, n_seq,
@@ -634,7 +638,9 @@ static gdn_status chunk_prefill_impl(bool launch, const gdn_dims* dims, gdn_pool
     }
   }
   if (e == cudaSuccess) count_launch(GDN_K_PREFILL);
-  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+  if (e != cudaSuccess) return GDN_ERR_CUDA;
+  if (epi) return gdn_gated_rmsnorm(dims, out, epi->z, epi->weight, epi->eps, total_tokens, out, stream);
+  return GDN_OK;
 }
 
 extern "C" gdn_status gdn_chunk_prefill(const gdn_dims* dims, gdn_pool pool, gdn_pool ckpt,
@@ -648,6 +654,31 @@ extern "C" gdn_status gdn_chunk_prefill(const gdn_dims* dims, gdn_pool pool, gdn
   return chunk_prefill_impl(true, dims, pool, ckpt, params, slot_ids, cu_seqlens, start_pos, n_seq,
                             total_tokens, ckpt_ids, max_ckpt, ckpt_block, qkv, a, b, out, workspace,
                             workspace_bytes, dev_err, stream);
+}
+
+// The prefill with the readout epilogue (gated RMS norm): `y` receives
+// o / sqrt(mean(o^2) + eps) * weight * silu(z) instead of the readout o.
+extern "C" gdn_status gdn_chunk_prefill_gated(const gdn_dims* dims, gdn_pool pool, gdn_pool ckpt,
+                                              const gdn_params* params, const int32_t* slot_ids,
+                                              const int32_t* cu_seqlens, const int64_t* start_pos,
+                                              int32_t n_seq, int64_t total_tokens, const int32_t* ckpt_ids,
+                                              int32_t max_ckpt, int32_t ckpt_block, const void* qkv,
+                                              const void* a, const void* b, const void* z,
+                                              const float* weight, float eps, void* y, void* workspace,
+                                              size_t workspace_bytes, uint32_t* dev_err, void* stream) {
+  using namespace gdn;
+  gdn_status st = check_dims(dims);
+  if (st != GDN_OK) return st;
+  if (!(eps >= 0.f) || (total_tokens > 0 && (!z || !weight))) return GDN_ERR_INVALID_ARG;
+  if (dims->dv > 256) return GDN_ERR_UNSUPPORTED;
+  if ((st = chunk_prefill_impl(false, dims, pool, ckpt, params, slot_ids, cu_seqlens, start_pos, n_seq,
+                               total_tokens, ckpt_ids, max_ckpt, ckpt_block, qkv, a, b, y, workspace,
+                               workspace_bytes, dev_err, stream)) != GDN_OK)
+    return st;
+  const Tc32Epilogue epi{z, weight, eps};
+  return chunk_prefill_impl(true, dims, pool, ckpt, params, slot_ids, cu_seqlens, start_pos, n_seq, total_tokens,
+                            ckpt_ids, max_ckpt, ckpt_block, qkv, a, b, y, workspace, workspace_bytes, dev_err,
+                            stream, total_tokens > 0 ? &epi : nullptr);
 }
 
 // Mixed batch, decode-first: the decode rows through the decode kernel, the

@@ -16,11 +16,18 @@ cudaError_t prefill_tc_launch(const gdn_dims& d, const gdn_pool& pool, const gdn
 // the chain (prefill_tc32.cu): dk = dv = 128, width 4, bf16 activations and
 // conv history.  Needs no workspace.
 bool prefill_tc32_supported(const gdn_dims& d, const void* qkv, const void* out, const gdn_params& p);
+// the readout epilogue fused into the output (gdn_chunk_prefill_gated): out
+// receives y = o / sqrt(mean(o^2) + eps) * weight * silu(z)
+struct Tc32Epilogue {
+  const void* z;         // [total][hv][dv] bf16, 16-byte aligned
+  const float* weight;   // [dv] fp32, 16-byte aligned
+  float eps;
+};
 cudaError_t prefill_tc32_launch(const gdn_dims& d, const gdn_pool& pool, const gdn_pool& ckpt, const gdn_params& p,
                                 const int32_t* slot_ids, const int32_t* cu_seqlens, const int64_t* start_pos,
                                 int32_t n_seq, int64_t total, const int32_t* ckpt_ids, int32_t max_ckpt,
                                 int32_t ckpt_block, const void* qkv, const void* a, const void* b, void* out,
-                                uint32_t* dev_err, cudaStream_t s);
+                                uint32_t* dev_err, cudaStream_t s, const Tc32Epilogue* epi = nullptr);
 // conv histories of a prefill's checkpoints and final state (prefill.cu)
 cudaError_t conv_history_launch(const gdn_dims& d, const gdn_pool& pool, const gdn_pool& ckpt,
                                 const int32_t* slot_ids, const int32_t* cu_seqlens, const int64_t* start_pos,

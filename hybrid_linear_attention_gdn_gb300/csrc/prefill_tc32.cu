@@ -35,7 +35,10 @@
 //   state      S^T <- e^{b_last} S^T (in TMEM, by the threads) + Delta'^T K~
 //              (one product accumulating into the state; A = Delta'^T in TMEM)
 //   output     O = (S^T Y_Q^T) diag(rq e^b) + Delta'^T M'^T, staged as a bf16
-//              tile and written by one TMA tensor store
+//              tile and written by one TMA tensor store; or, with the readout
+//              epilogue fused (EPI), staged in fp32 and written as
+//              y = O / sqrt(mean(O^2) + eps) * w * silu(z) per token, z
+//              arriving by its own TMA tile
 // With k^ = diag(rk) Y_K and q^ = diag(rq) Y_Q these are the chunk form's
 // products exactly: the rk factors of Delta and of the state update meet in
 // Delta', and M' = M diag(1/rk).
@@ -91,6 +94,8 @@ struct Tc32Args {
   __nv_bfloat16* out;
   uint32_t* err;
   int32_t hk, hv, C, G;
+  const float* norm_w;  // the fused epilogue's weight [dv] (EPI)
+  float eps;
 };
 
 // Shared memory.  Operand tiles are fp32 in the tensor core's 128-byte
@@ -114,7 +119,8 @@ struct __align__(1024) Smem32 {
   float g[2][kC], beta[2][kC], b[2][kC], eb[2][kC], ebl[2][kC];  // by chunk parity
   float rk[kC];  // 1 / sqrt(|y_k|^2 + eps) per token
   float rq[kC];  // dk^-1/2 / sqrt(|y_q|^2 + eps) per token
-  uint64_t ld_bar, mma_bar;
+  __nv_bfloat16 zt[kC][kD];  // the fused epilogue's z rows of the chunk (EPI)
+  uint64_t ld_bar, mma_bar, z_bar;
   uint32_t tmem_base;
 };
 
@@ -289,10 +295,11 @@ __device__ __forceinline__ void solve_T(const float* A, float* X, float* Y, floa
 // ---- the kernel -------------------------------------------------------------
 // grid (hv, n_seq), 512 threads, one CTA per SM.  Thread 0 issues the TMA
 // copies and the tensor-core products; every wait is bounded (1 s).
-template <typename Tconv>
+template <typename Tconv, bool EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     tc32_prefill_kernel(const Tc32Args a, const __grid_constant__ CUtensorMap qmap,
-                        const __grid_constant__ CUtensorMap omap, const __grid_constant__ CUtensorMap cmap) {
+                        const __grid_constant__ CUtensorMap omap, const __grid_constant__ CUtensorMap cmap,
+                        const __grid_constant__ CUtensorMap zmap) {
   pdl_wait();
   pdl_trigger();
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -319,6 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     mbar_init(&S.ld_bar, 1);
     mbar_init(&S.mma_bar, 1);
+    mbar_init(&S.z_bar, 1);
     fence_mbar_init();
   }
   if (warp == 0) umma::tmem_alloc(&S.tmem_base, TM_COLS);
@@ -478,6 +486,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // staging) and the t2 tile (output staging); the gates of this chunk are
     // in buffer gbuf
     if (tid == 0) bulk_wait_read();
+    // the fused epilogue's z rows of this chunk (the previous chunk's output
+    // step has read the tile: it ended with a CTA barrier)
+    if (EPI && tid == 0) {
+      mbar_arrive_expect_tx(&S.z_bar, (uint32_t)sizeof(S.zt));
+      tma_load_2d(&S.zt[0][0], &zmap, h * kD, (int32_t)(t0 + (P - p0)), &S.z_bar);
+    }
     // the chunk's raw rows landed
     if (!wait_all(&S.ld_bar, c & 1)) break;
     ld_done = c + 1;
@@ -688,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!mma_wait()) break;
     // ---- output O = O1 diag(rq e^b) + O2, staged [token][dv] bf16 in t2 ------
-    {
+    if constexpr (!EPI) {
       float o1[16], o2[16];
       umma::tmem_ld16(tlane + TM_O1 + 16 * qq, o1);
       umma::tmem_ld16(tlane + TM_O2 + 16 * qq, o2);
@@ -696,6 +710,41 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < 16; ++i)
         ot[(16 * qq + i) * kD + lrow] = __float2bfloat16_rn(fmaf(o1[i], S.rq[16 * qq + i] * geb[16 * qq + i], o2[i]));
+    } else {
+      // fp32 O staged [token][dv] in the kt tile (dead since the state update),
+      // then per token y = O / sqrt(mean(O^2) + eps) * w * silu(z) into t2
+      {
+        float o1[16], o2[16];
+        umma::tmem_ld16(tlane + TM_O1 + 16 * qq, o1);
+        umma::tmem_ld16(tlane + TM_O2 + 16 * qq, o2);
+        float* of = reinterpret_cast<float*>(S.kt);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) of[(16 * qq + i) * kD + lrow] = fmaf(o1[i], S.rq[16 * qq + i] * geb[16 * qq + i], o2[i]);
+      }
+      if (!wait_all(&S.z_bar, c & 1)) break;
+      const float4 w4 = *reinterpret_cast<const float4*>(a.norm_w + 4 * lane);
+      const float* of = reinterpret_cast<const float*>(S.kt);
+      __nv_bfloat16* ot = reinterpret_cast<__nv_bfloat16*>(S.t2);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {  // tokens 4 warp + k: lane holds dv 4 lane .. 4 lane + 3
+        const int t = 4 * warp + k;
+        const float4 o4 = *reinterpret_cast<const float4*>(of + t * kD + 4 * lane);
+        float ss = o4.x * o4.x + o4.y * o4.y + o4.z * o4.z + o4.w * o4.w;
+#pragma unroll
+        for (int m = 16; m; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+        const float inv = rsqrtf(ss / (float)kD + a.eps);
+        const uint2 zu = *reinterpret_cast<const uint2*>(&S.zt[t][4 * lane]);
+        const float2 z01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&zu.x));
+        const float2 z23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&zu.y));
+        const __nv_bfloat162 y01 = __floats2bfloat162_rn(o4.x * inv * w4.x * silu_fast(z01.x),
+                                                         o4.y * inv * w4.y * silu_fast(z01.y));
+        const __nv_bfloat162 y23 = __floats2bfloat162_rn(o4.z * inv * w4.z * silu_fast(z23.x),
+                                                         o4.w * inv * w4.w * silu_fast(z23.y));
+        uint2 yu;
+        yu.x = *reinterpret_cast<const uint32_t*>(&y01);
+        yu.y = *reinterpret_cast<const uint32_t*>(&y23);
+        *reinterpret_cast<uint2*>(ot + t * kD + 4 * lane) = yu;
+      }
     }
     // checkpoint: the state rows, 128B-swizzled, into four 16 KB boxes (32
     // columns x 128 rows) in the dead kq tile, for four tensor stores
@@ -739,6 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma::commit(&S.mma_bar);
       mbar_wait(&S.mma_bar, mph);
       for (int k = ld_done; k < ld_issued; ++k) mbar_wait(&S.ld_bar, k & 1);
+      if (EPI) mbar_wait(&S.z_bar, c & 1);
     }
   } else {
     // the final state
@@ -770,7 +820,7 @@ cudaError_t prefill_tc32_launch(const gdn_dims& d, const gdn_pool& pool, const g
                                 const int32_t* slot_ids, const int32_t* cu_seqlens, const int64_t* start_pos,
                                 int32_t n_seq, int64_t total, const int32_t* ckpt_ids, int32_t max_ckpt,
                                 int32_t ckpt_block, const void* qkv, const void* av, const void* bv, void* out,
-                                uint32_t* dev_err, cudaStream_t s) {
+                                uint32_t* dev_err, cudaStream_t s, const Tc32Epilogue* epi) {
   Tc32Args a;
   a.ssm = pool.ssm;
   a.num_slots = pool.num_slots;
@@ -796,26 +846,31 @@ cudaError_t prefill_tc32_launch(const gdn_dims& d, const gdn_pool& pool, const g
   a.hv = d.hv;
   a.C = (int32_t)channels(d);
   a.G = d.hv / d.hk;
-  auto k = tc32_prefill_kernel<__nv_bfloat16>;
+  a.norm_w = epi ? epi->weight : nullptr;
+  a.eps = epi ? epi->eps : 0.f;
+  auto k = epi ? tc32_prefill_kernel<__nv_bfloat16, true> : tc32_prefill_kernel<__nv_bfloat16, false>;
   const size_t smem = sizeof(Smem32) + 1024;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  // qkv [total][C] in boxes of 128 channels x 67 rows; out [total][hv * 128]
-  // in boxes of one V head x 64 tokens; checkpoint states [slots * hv * 128
-  // rows][128] fp32 in 128B-swizzled boxes of 32 x 128 (over the working pool
-  // when there is no checkpoint pool: never written then)
-  CUtensorMap qmap, omap, cmap;
+  // qkv [total][C] in boxes of 128 channels x 67 rows; out (and z) [total][hv
+  // * 128] in boxes of one V head x 64 tokens; checkpoint states [slots * hv *
+  // 128 rows][128] fp32 in 128B-swizzled boxes of 32 x 128 (over the working
+  // pool when there is no checkpoint pool: never written then)
+  CUtensorMap qmap, omap, cmap, zmap;
   if ((e = tensor_map_2d(&qmap, qkv, total, a.C, 2, kD, kRawRows, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
     return e;
   if ((e = tensor_map_2d(&omap, out, total, (int64_t)a.hv * kD, 2, kD, kC, CU_TENSOR_MAP_SWIZZLE_NONE)) !=
       cudaSuccess)
+    return e;
+  if ((e = tensor_map_2d(&zmap, epi ? epi->z : out, total, (int64_t)a.hv * kD, 2, kD, kC,
+                         CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
     return e;
   const bool has_ck = a.ck_ssm != nullptr && a.ck_num_slots > 0;
   if ((e = tensor_map_2d(&cmap, has_ck ? a.ck_ssm : a.ssm, (int64_t)(has_ck ? a.ck_num_slots : a.num_slots) * a.hv * kD,
                          kD, 4, 32, kD, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
     return e;
   return launch_plain(k, dim3((unsigned)a.hv, (unsigned)n_seq), dim3(kThreads), smem, s, dim3(1), a, qmap, omap,
-                      cmap);
+                      cmap, zmap);
 }
 
 }  // namespace gdn

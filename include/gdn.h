@@ -222,6 +222,30 @@ gdn_status gdn_chunk_prefill(const gdn_dims* dims, gdn_pool pool, gdn_pool ckpt,
                              void* stream);
 
 /*
+ * Chunked prefill with the readout epilogue fused: the call of
+ * gdn_chunk_prefill, except that `y` ([total_tokens][hv][dv], activation
+ * dtype, device) receives the gated RMS norm of the readout (see
+ * gdn_gated_rmsnorm: y = o / sqrt(mean(o^2) + eps) * weight * silu(z), the
+ * Gated DeltaNet block's output normalisation and gate; z [total_tokens][hv][dv]
+ * in the activation dtype, weight [dv] fp32) instead of the readout itself.
+ * State, checkpoints and conv histories are those of gdn_chunk_prefill.
+ * The tf32 tensor-core prefill (dk = dv = 128, width 4, bf16 activations and
+ * history) normalises each chunk's fp32 readout before it leaves the chip (z
+ * and weight 16-byte aligned); every other case runs gdn_chunk_prefill into y
+ * and then gdn_gated_rmsnorm on y in place.  Statuses as gdn_chunk_prefill,
+ * plus GDN_ERR_INVALID_ARG for a null z or weight or eps < 0.
+ */
+gdn_status gdn_chunk_prefill_gated(const gdn_dims* dims, gdn_pool pool, gdn_pool ckpt,
+                                   const gdn_params* params, const int32_t* slot_ids,
+                                   const int32_t* cu_seqlens, const int64_t* start_pos,
+                                   int32_t n_seq, int64_t total_tokens,
+                                   const int32_t* ckpt_ids, int32_t max_ckpt,
+                                   int32_t ckpt_block, const void* qkv, const void* a,
+                                   const void* b, const void* z, const float* weight,
+                                   float eps, void* y, void* workspace,
+                                   size_t workspace_bytes, uint32_t* dev_err, void* stream);
+
+/*
  * Chunked prefill that allocates nothing.  The pages have no counterpart to
  * this call; it is a convenience of this library.
  *

@@ -104,7 +104,7 @@ def round_like(ref, dtype: torch.dtype) -> np.ndarray:
 
 
 def assert_out_close(out: torch.Tensor, ref, row: int, tol: float, row_floor_rms: bool = False,
-                     row_tol: float | None = None):
+                     row_tol: float | None = None, row_weight=None):
     """Output check described in the module docstring: the tensor against the
     exact result; each row's error beyond its own rounding,
     ||x - ref|| - ||round(ref) - ref||, against its norm.  row_floor_rms (the
@@ -112,7 +112,10 @@ def assert_out_close(out: torch.Tensor, ref, row: int, tol: float, row_floor_rms
     absolute in scale): that excess is measured against max(its norm, the RMS
     row norm of the tensor) - a row whose exact value is thousands of times
     below the typical row gets the typical absolute error, not a
-    proportionally smaller one.  row_tol replaces tol for the rows."""
+    proportionally smaller one.  row_tol replaces tol for the rows.
+    row_weight (per row, <= 1) scales each row's excess: for an output that a
+    scale-free map (a norm) took from rows of another tensor, the floor of
+    those rows carried through the map."""
     x = to_np(out)
     ref = np.asarray(ref, np.float64)
     den = np.linalg.norm(ref)
@@ -124,6 +127,8 @@ def assert_out_close(out: torch.Tensor, ref, row: int, tol: float, row_floor_rms
     rnd = round_like(ref, out.dtype).reshape(-1, row)
     nrm = np.linalg.norm(rr, axis=1)
     excess = np.linalg.norm(xr - rr, axis=1) - np.linalg.norm(rnd - rr, axis=1)
+    if row_weight is not None:
+        excess = excess * np.asarray(row_weight, np.float64).reshape(-1)
     if row_floor_rms:
         floor = np.sqrt(np.mean(nrm ** 2))
         worst = float((excess / np.maximum(nrm, floor)).max()) if floor > 0 else float(excess.max())
