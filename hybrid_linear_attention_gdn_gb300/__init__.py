@@ -6,6 +6,6 @@ from .binding import (  # noqa: F401
     K_SLOT_COPY, K_SLOT_ZERO, K_SPEC_COMMIT, K_SPEC_VERIFY, K_STATE_PACK, Dims, GdnError,
     LayerParams, StatePool, chunk_prefill, chunk_prefill_gated, chunk_prefill_noalloc, chunk_prefill_workspace_size,
     decode_step, gated_rmsnorm, kda_decode_step, kda_prefill, kda_spec_verify, selftest_wait_timeout, launch_count, launch_count_reset, launch_counts, load, mixed_step, slot_copy,
-    slot_zero,
+    slot_zero, BoundsError, debug_bounds, debug_bounds_take, selftest_bounds,
     spec_commit, spec_commit_index, spec_verify, state_pack, state_record_bytes, state_unpack,
 )

@@ -86,11 +86,19 @@ EXPORTS = {
     "gdn_status_string": ([_I32], ctypes.c_char_p),
     "gdn_launch_count": ([_I32], ctypes.c_uint64),
     "gdn_launch_count_reset": ([], None),
+    "gdn_selftest_bounds": ([_P], _I32),
+    "gdn_debug_bounds_take": ([ctypes.POINTER(ctypes.c_uint32), ctypes.c_char_p, ctypes.c_size_t,
+                               ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)], _I32),
 }
 
 
+def debug_bounds() -> bool:
+    """GDN_DEBUG_BOUNDS=1 selects the bounds-checked library, libgdn_debug.so."""
+    return os.environ.get("GDN_DEBUG_BOUNDS") == "1"
+
+
 def library_path() -> str:
-    return _build.LIB
+    return _build.LIB_DEBUG if debug_bounds() else _build.LIB
 
 
 def load(build_if_missing: bool = False) -> ctypes.CDLL:
@@ -100,7 +108,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         if _lib is None:
             path = library_path()
             if build_if_missing:
-                _build.build()
+                _build.build(debug_bounds=debug_bounds())
             if not os.path.exists(path):
                 raise RuntimeError(
                     f"libgdn.so not found at {path}: build it with "
@@ -114,10 +122,35 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     return _lib
 
 
+class BoundsError(RuntimeError):
+    """A kernel of the bounds-checked library indexed outside a buffer."""
+
+
+def debug_bounds_take():
+    """Bounds-checked library only: wait for the device, read and clear the
+    kernels' bounds words.  None when no check failed since the last call,
+    else (count, "file:line kind", index, limit)."""
+    count, idx, lim = ctypes.c_uint32(0), ctypes.c_int64(0), ctypes.c_int64(0)
+    where = ctypes.create_string_buffer(256)
+    st = load().gdn_debug_bounds_take(ctypes.byref(count), where, 256, ctypes.byref(idx), ctypes.byref(lim))
+    if st != OK:
+        raise GdnError("gdn_debug_bounds_take", st, load().gdn_status_string(st).decode())
+    if count.value == 0:
+        return None
+    return count.value, where.value.decode(), idx.value, lim.value
+
+
 def _check(fn: str, status: int):
     if status != OK:
         msg = load().gdn_status_string(status).decode()
         raise GdnError(fn, status, msg)
+    # the checked library: every call is followed by a read of the bounds
+    # words (not while a CUDA graph is being captured)
+    if debug_bounds() and not torch.cuda.is_current_stream_capturing():
+        bad = debug_bounds_take()
+        if bad is not None:
+            raise BoundsError(f"{fn}: {bad[0]} index check(s) failed, first at {bad[1]}: "
+                              f"index {bad[2]} of {bad[3]}")
 
 
 def _ptr(t) -> int | None:
@@ -329,6 +362,15 @@ def selftest_wait_timeout(dev_err, stream=None):
     satisfies expires after the library's wait limit and sets DEV_ERR_TIMEOUT
     in dev_err (an int32 device tensor)."""
     _check("gdn_selftest_wait_timeout", load().gdn_selftest_wait_timeout(_ptr(dev_err), _stream(stream)))
+
+
+def selftest_bounds(stream=None):
+    """Bounds-checked library only: launch the checks' positive control (three
+    requests that must fail their checks, none of which can leave real
+    memory).  The bounds words are left for debug_bounds_take()."""
+    st = load().gdn_selftest_bounds(_stream(stream))
+    if st != OK:
+        raise GdnError("gdn_selftest_bounds", st, load().gdn_status_string(st).decode())
 
 
 NOALLOC_SCRATCH_BYTES = 64 << 20

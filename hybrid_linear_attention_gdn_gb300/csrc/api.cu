@@ -2,9 +2,26 @@
 // strings and launch counters.
 #include "gdn_common.cuh"
 
+#include <cstdio>
+
 namespace gdn {
 
 std::atomic<uint64_t> g_launches[GDN_K_COUNT];
+
+namespace {
+struct BoundsUnit {
+  const char* unit;
+  BoundsReader read;
+};
+// filled by static initialisers of the checked build's units (no locking:
+// they run before the library is usable)
+BoundsUnit g_bounds_units[32];
+int g_n_bounds_units = 0;
+}  // namespace
+
+void register_bounds_reader(const char* unit, BoundsReader r) {
+  if (g_n_bounds_units < 32) g_bounds_units[g_n_bounds_units++] = BoundsUnit{unit, r};
+}
 
 gdn_status check_dims(const gdn_dims* d) {
   if (!d) return GDN_ERR_INVALID_ARG;
@@ -48,4 +65,34 @@ extern "C" uint64_t gdn_launch_count(int32_t k) {
 
 extern "C" void gdn_launch_count_reset(void) {
   for (int k = 0; k < GDN_K_COUNT; ++k) gdn::g_launches[k].store(0);
+}
+
+extern "C" gdn_status gdn_debug_bounds_take(uint32_t* count, char* where, size_t where_len, int64_t* index,
+                                           int64_t* limit) {
+#ifndef GDN_DEBUG_BOUNDS
+  (void)count, (void)where, (void)where_len, (void)index, (void)limit;
+  return GDN_ERR_UNSUPPORTED;
+#else
+  if (!count) return GDN_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return GDN_ERR_CUDA;
+  *count = 0;
+  if (where && where_len) where[0] = 0;
+  bool first = true;
+  for (int u = 0; u < gdn::g_n_bounds_units; ++u) {
+    gdn::BoundsWord w;
+    if (!gdn::g_bounds_units[u].read(&w)) return GDN_ERR_CUDA;
+    if (!w.count) continue;
+    *count += w.count;
+    if (first) {
+      first = false;
+      static const char* kinds[3] = {"global", "shared", "TMEM"};
+      if (where && where_len)
+        snprintf(where, where_len, "%s:%d %s", gdn::g_bounds_units[u].unit, w.line,
+                 (w.kind >= 0 && w.kind < 3) ? kinds[w.kind] : "?");
+      if (index) *index = w.index;
+      if (limit) *limit = w.limit;
+    }
+  }
+  return GDN_OK;
+#endif
 }

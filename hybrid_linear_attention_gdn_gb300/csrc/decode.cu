@@ -81,20 +81,46 @@ __device__ __forceinline__ int channel_of(int i, int hq, int h, int hk, int dv, 
   return 2 * hk * DK + h * dv + row0 + (i - 2 * DK);
 }
 
-template <int DK, int NIT>
-__device__ __forceinline__ void load_rows(float4 (&s)[NIT][4], const float* base, int nrows,
-                                          int rloc, int seg) {
+template <int DK, int NIT, typename V>
+__device__ __forceinline__ void load_rows(float4 (&s)[NIT][4], const V& base, int nrows, int rloc, int seg) {
   using M = RowMap<DK>;
 #pragma unroll
   for (int it = 0; it < NIT; ++it) {
     const int row = it * M::RI + rloc;
 #pragma unroll
     for (int c = 0; c < 4; ++c)
-      s[it][c] = row < nrows
-                     ? ld_stream(reinterpret_cast<const float4*>(base + (size_t)row * DK + M::col(c, seg)))
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
+      s[it][c] = row < nrows ? ld_stream(&vec_at<const float4>(base, (size_t)row * DK + M::col(c, seg)))
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
+
+// The caller's tensors of a decode or verify step as checked views (extents
+// in elements; T tokens per request).
+template <int DK, typename Tact, typename Tconv, bool KDA>
+struct StepViews {
+  View<float, 0> ssm, spec_ssm;
+  View<Tconv, 0> conv, spec_conv;
+  View<const float, 0> conv_w, A_log, dt_bias;
+  View<const int32_t, 0> slot_ids, spec_ids;
+  View<const Tact, 0> qkv, a, b;
+  View<Tact, 0> out;
+  __device__ __forceinline__ explicit StepViews(const StepArgs& g, int T) {
+    const long long BT = (long long)g.B * T, gate = BT * g.hv;
+    ssm = GDN_GV(g.ssm, (long long)g.num_slots * g.hv * g.dv * DK);
+    spec_ssm = GDN_GV(g.spec_ssm, (long long)g.spec_num_slots * g.hv * g.dv * DK);
+    conv = GDN_GV(reinterpret_cast<Tconv*>(g.conv), (long long)g.num_slots * (g.W - 1) * g.C);
+    spec_conv = GDN_GV(reinterpret_cast<Tconv*>(g.spec_conv), (long long)g.spec_num_slots * (g.W - 1) * g.C);
+    conv_w = GDN_GV(g.conv_w, (long long)g.C * g.W);
+    A_log = GDN_GV(g.A_log, g.hv);
+    dt_bias = GDN_GV(g.dt_bias, (long long)g.hv * (KDA ? DK : 1));
+    slot_ids = GDN_GV(g.slot_ids, g.B);
+    spec_ids = GDN_GV(g.spec_ids, BT);
+    qkv = GDN_GV(reinterpret_cast<const Tact*>(g.qkv), BT * g.C);
+    a = GDN_GV(reinterpret_cast<const Tact*>(g.a), gate * (KDA ? DK : 1));
+    b = GDN_GV(reinterpret_cast<const Tact*>(g.b), gate);
+    out = GDN_GV(reinterpret_cast<Tact*>(g.out), gate * g.dv);
+  }
+};
 
 // Reduce (q.q, k.k, q.k) over the dk channels of one QK head held in smem,
 // with all warps; result in red_out[0..2] (shared).
@@ -115,9 +141,10 @@ __device__ __forceinline__ void block_norms(const float* sq, const float* sk, fl
     pqk += __shfl_xor_sync(0xffffffffu, pqk, o);
   }
   if (lane == 0) {
-    sred[0][warp] = pq;
-    sred[1][warp] = pk;
-    sred[2][warp] = pqk;
+    const int w = GDN_S(warp, kWarps);
+    sred[0][w] = pq;
+    sred[1][w] = pk;
+    sred[2][w] = pqk;
   }
   __syncthreads();
   if (tid == 0) {
@@ -146,11 +173,15 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const StepArgs a) {
   pdl_trigger();
   using M = RowMap<DK>;
   constexpr int R = NIT * M::RI;
-  __shared__ float sq[DK], sk[DK], sv[R], so[R];
-  __shared__ float sal[KDA ? DK : 1];
-  __shared__ float sraw[kMaxW][2 * DK];
+  __shared__ float sq_[DK], sk_[DK], sv_[R], so_[R];
+  __shared__ float sal_[KDA ? DK : 1];
+  __shared__ float sraw_[kMaxW][2 * DK];
   __shared__ float sred[3][kWarps];
   __shared__ float sscal[8];
+  const auto sq = GDN_SV(sq_, DK), sk = GDN_SV(sk_, DK), sv = GDN_SV(sv_, R), so = GDN_SV(so_, R);
+  const auto sal = GDN_SV(sal_, KDA ? DK : 1);
+  const auto sraw = GDN_SV(&sraw_[0][0], kMaxW * 2 * DK);  // [kMaxW][2 DK]
+  const StepViews<DK, Tact, Tconv, KDA> g(a, 1);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int r = blockIdx.y;
@@ -159,9 +190,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const StepArgs a) {
   const int row0 = p * R;
   const int nrows = min(R, a.dv - row0);
   const int csize = a.G * a.P;
-  const int32_t slot = a.slot_ids[r];
+  const int32_t slot = g.slot_ids[r];
   const int cls = slot_class(slot, a.num_slots);
-  Tact* out = reinterpret_cast<Tact*>(a.out) + ((size_t)r * a.hv + h) * a.dv + row0;
+  const auto out = g.out + (((size_t)r * a.hv + h) * a.dv + row0);
   if (cls) {  // the whole cluster shares r, so it skips together
     if (cls == 2 && blockIdx.x == 0 && tid == 0) report(a.err, GDN_DEV_ERR_SLOT_OOB);
     for (int i = tid; i < nrows; i += kThreads) out[i] = from_f32<Tact>(0.f);
@@ -171,17 +202,17 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const StepArgs a) {
   // 1. state rows in flight first
   const int seg = lane % M::LPR;
   const int rloc = warp * M::RW + lane / M::LPR;
-  float* St = a.ssm + (((size_t)slot * a.hv + h) * a.dv + row0) * DK;
+  const auto St = g.ssm + (((size_t)slot * a.hv + h) * a.dv + row0) * DK;
   float4 s[NIT][4];
   load_rows<DK, NIT>(s, St, nrows, rloc, seg);
 
   // 2. conv1d + SiLU on the q/k channels of hq and the v channels of our rows
   const bool qk_writer = csize == 1 || cluster_ctarank() == 0;
-  Tconv* conv = reinterpret_cast<Tconv*>(a.conv) + (size_t)slot * (a.W - 1) * a.C;
-  const Tact* x = reinterpret_cast<const Tact*>(a.qkv) + (size_t)r * a.C;
+  const auto conv = g.conv + (size_t)slot * (a.W - 1) * a.C;
+  const auto x = g.qkv + (size_t)r * a.C;
   for (int i = tid; i < 2 * DK + nrows; i += kThreads) {
     const int c = channel_of<DK>(i, hq, h, a.hk, a.dv, row0);
-    const float* w = a.conv_w + (size_t)c * a.W;
+    const auto w = g.conv_w + (size_t)c * a.W;
     float hist[kMaxW];
     float acc = 0.f;
 #pragma unroll
@@ -208,30 +239,28 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const StepArgs a) {
     if (i < 2 * DK && qk_writer) {
 #pragma unroll
       for (int j = 0; j < kMaxW - 1; ++j)
-        if (j < a.W - 1) sraw[j][i] = hist[j];
-      sraw[a.W - 1][i] = xv;
+        if (j < a.W - 1) sraw[j * 2 * DK + i] = hist[j];
+      sraw[(a.W - 1) * 2 * DK + i] = xv;
     }
   }
   if (csize > 1) cluster_arrive_release();  // our reads of the shared history are done
   __syncthreads();
 
   // 3. L2 norms and gates
-  block_norms<DK>(sq, sk, sred, sscal);
+  block_norms<DK>(sq_, sk_, sred, sscal);
   if (tid == 0) {
-    const Tact* av = reinterpret_cast<const Tact*>(a.a) + (size_t)r * a.hv;
-    const Tact* bv = reinterpret_cast<const Tact*>(a.b) + (size_t)r * a.hv;
     const float rq = rsqrtf(sscal[0] + kNormEps) * rsqrtf((float)DK);
     const float rk = rsqrtf(sscal[1] + kNormEps);
     sscal[3] = rq;
     sscal[4] = rk;
     sscal[5] = sscal[2] * rq * rk;  // k^ . q^
-    if (!KDA) sscal[6] = gate_alpha(a.A_log[h], a.dt_bias[h], to_f32(av[h]));
-    sscal[7] = sigmoid_f(to_f32(bv[h]));
+    if (!KDA) sscal[6] = gate_alpha(g.A_log[h], g.dt_bias[h], to_f32(g.a[(size_t)r * a.hv + h]));
+    sscal[7] = sigmoid_f(to_f32(g.b[(size_t)r * a.hv + h]));
   }
   if (KDA) {
-    const Tact* av = reinterpret_cast<const Tact*>(a.a) + ((size_t)r * a.hv + h) * DK;
+    const auto av = g.a + ((size_t)r * a.hv + h) * DK;
     for (int i = tid; i < DK; i += kThreads)
-      sal[i] = gate_alpha(a.A_log[h], a.dt_bias[(size_t)h * DK + i], to_f32(av[i]));
+      sal[i] = gate_alpha(g.A_log[h], g.dt_bias[(size_t)h * DK + i], to_f32(av[i]));
   }
   __syncthreads();
   const float rq = sscal[3], rk = sscal[4], kq = sscal[5], alpha = KDA ? 1.f : sscal[6], beta = sscal[7];
@@ -273,7 +302,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const StepArgs a) {
     }
     if (row < nrows) {
       const float bu = beta * (sv[row] - alpha * dk_);
-      float4* dst = reinterpret_cast<float4*>(St + (size_t)row * DK);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         float4 v = s[it][c];
@@ -281,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const StepArgs a) {
         v.y = fmaf(bu, kk[c].y, al[c].y * v.y);
         v.z = fmaf(bu, kk[c].z, al[c].z * v.z);
         v.w = fmaf(bu, kk[c].w, al[c].w * v.w);
-        st_stream(dst + M::col(c, seg) / 4, v);
+        st_stream(&vec_at<float4>(St, (size_t)row * DK + M::col(c, seg)), v);
       }
       if (seg == 0) so[row] = fmaf(bu, kq, alpha * dq_);
     }
@@ -296,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const StepArgs a) {
       const int c = channel_of<DK>(i, hq, h, a.hk, a.dv, row0);
 #pragma unroll
       for (int j = 0; j < kMaxW - 1; ++j)
-        if (j < a.W - 1) conv[(size_t)j * a.C + c] = from_f32<Tconv>(sraw[j + 1][i]);
+        if (j < a.W - 1) conv[(size_t)j * a.C + c] = from_f32<Tconv>(sraw[(j + 1) * 2 * DK + i]);
     }
   }
 }
@@ -320,10 +348,14 @@ __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const StepArgs a) {
   constexpr int R = NIT * M::RI;
   constexpr int NCH = 2 * DK + R;  // channels handled: q, k, our v rows
   extern __shared__ __align__(16) float smem[];
-  float* sy = smem;                     // [T][NCH]  conv+SiLU outputs
-  float* so = sy + (size_t)a.T * NCH;   // [T][R]    outputs
-  float* sscal = so + (size_t)a.T * R;  // [T][5]    rq, rk, kq, alpha, beta
-  float* salk = smem + verify_alpha_off(a.T, NCH, R);  // KDA: [T][DK] alpha
+  const size_t smem_floats = KDA ? verify_alpha_off(a.T, NCH, R) + (size_t)a.T * DK
+                                 : (size_t)a.T * NCH + (size_t)a.T * R + (size_t)a.T * 5;
+  const auto sm = GDN_SV(smem, smem_floats);
+  const auto sy = sm;                                // [T][NCH]  conv+SiLU outputs
+  const auto so = sm + (size_t)a.T * NCH;            // [T][R]    outputs
+  const auto sscal = sm + (size_t)a.T * (NCH + R);   // [T][5]    rq, rk, kq, alpha, beta
+  const auto salk = sm + (KDA ? verify_alpha_off(a.T, NCH, R) : 0);  // KDA: [T][DK] alpha
+  const StepViews<DK, Tact, Tconv, KDA> g(a, a.T);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int r = blockIdx.y;
@@ -332,12 +364,12 @@ __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const StepArgs a) {
   const int row0 = p * R;
   const int nrows = min(R, a.dv - row0);
   const int T = a.T;
-  const int32_t slot = a.slot_ids[r];
+  const int32_t slot = g.slot_ids[r];
   const int cls = slot_class(slot, a.num_slots);
   if (cls) {
     if (cls == 2 && blockIdx.x == 0 && tid == 0) report(a.err, GDN_DEV_ERR_SLOT_OOB);
     for (int t = 0; t < T; ++t) {
-      Tact* out = reinterpret_cast<Tact*>(a.out) + ((((size_t)r * T + t) * a.hv) + h) * a.dv + row0;
+      const auto out = g.out + (((((size_t)r * T + t) * a.hv) + h) * a.dv + row0);
       for (int i = tid; i < nrows; i += kThreads) out[i] = from_f32<Tact>(0.f);
     }
     return;
@@ -345,26 +377,26 @@ __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const StepArgs a) {
 
   const int seg = lane % M::LPR;
   const int rloc = warp * M::RW + lane / M::LPR;
-  const float* St = a.ssm + (((size_t)slot * a.hv + h) * a.dv + row0) * DK;
+  const auto St = g.ssm + (((size_t)slot * a.hv + h) * a.dv + row0) * DK;
   float4 s[NIT][4];
   load_rows<DK, NIT>(s, St, nrows, rloc, seg);
 
   // conv over the draft sequence; snapshot histories go straight to the spec
   // slots (v rows: this CTA; q/k channels: the first V head of the group)
   const bool qk_writer = (h % a.G) == 0 && p == 0;
-  const Tconv* conv = reinterpret_cast<const Tconv*>(a.conv) + (size_t)slot * (a.W - 1) * a.C;
-  const int32_t* sids = a.spec_ids + (size_t)r * T;
+  const auto conv = g.conv + (size_t)slot * (a.W - 1) * a.C;
+  const auto sids = g.spec_ids + (size_t)r * T;
   for (int i = tid; i < NCH; i += kThreads) {
     if (i >= 2 * DK + nrows) continue;
     const int c = channel_of<DK>(i, hq, h, a.hk, a.dv, row0);
-    const float* w = a.conv_w + (size_t)c * a.W;
+    const auto w = g.conv_w + (size_t)c * a.W;
     float win[kMaxW];  // win[0..W-2] = history, oldest first
 #pragma unroll
     for (int j = 0; j < kMaxW - 1; ++j)
       if (j < a.W - 1) win[j] = to_f32(conv[(size_t)j * a.C + c]);
     const bool writes = i >= 2 * DK || qk_writer;
     for (int t = 0; t < T; ++t) {
-      const float xv = to_f32(reinterpret_cast<const Tact*>(a.qkv)[((size_t)r * T + t) * a.C + c]);
+      const float xv = to_f32(g.qkv[((size_t)r * T + t) * a.C + c]);
       float acc = 0.f;
 #pragma unroll
       for (int j = 0; j < kMaxW - 1; ++j)
@@ -379,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const StepArgs a) {
       if (writes) {
         const int32_t sid = sids[t];
         if (slot_class(sid, a.spec_num_slots) == 0) {
-          Tconv* sc = reinterpret_cast<Tconv*>(a.spec_conv) + (size_t)sid * (a.W - 1) * a.C;
+          const auto sc = g.spec_conv + (size_t)sid * (a.W - 1) * a.C;
 #pragma unroll
           for (int j = 0; j < kMaxW - 1; ++j)
             if (j < a.W - 1) sc[(size_t)j * a.C + c] = from_f32<Tconv>(win[j]);
@@ -393,8 +425,8 @@ __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const StepArgs a) {
 
   // per-token norms and gates: warp w handles tokens w, w+8, ...
   for (int t = warp; t < T; t += kWarps) {
-    const float* yq = sy + (size_t)t * NCH;
-    const float* yk = yq + DK;
+    const auto yq = sy + (size_t)t * NCH;
+    const auto yk = yq + DK;
     float pq = 0.f, pk = 0.f, pqk = 0.f;
     for (int i = lane; i < DK; i += 32) {
       pq = fmaf(yq[i], yq[i], pq);
@@ -414,42 +446,37 @@ __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const StepArgs a) {
       sscal[t * 5 + 0] = rq;
       sscal[t * 5 + 1] = rk;
       sscal[t * 5 + 2] = pqk * rq * rk;
-      if (!KDA)
-        sscal[t * 5 + 3] = gate_alpha(a.A_log[h], a.dt_bias[h],
-                                      to_f32(reinterpret_cast<const Tact*>(a.a)[rt * a.hv + h]));
-      sscal[t * 5 + 4] = sigmoid_f(to_f32(reinterpret_cast<const Tact*>(a.b)[rt * a.hv + h]));
+      if (!KDA) sscal[t * 5 + 3] = gate_alpha(g.A_log[h], g.dt_bias[h], to_f32(g.a[rt * a.hv + h]));
+      sscal[t * 5 + 4] = sigmoid_f(to_f32(g.b[rt * a.hv + h]));
     }
   }
   if (KDA) {
     for (int e = tid; e < T * DK; e += kThreads) {
       const int t = e / DK, i = e % DK;
       const size_t rt = (size_t)r * T + t;
-      salk[e] = gate_alpha(a.A_log[h], a.dt_bias[(size_t)h * DK + i],
-                           to_f32(reinterpret_cast<const Tact*>(a.a)[(rt * a.hv + h) * DK + i]));
+      salk[e] = gate_alpha(g.A_log[h], g.dt_bias[(size_t)h * DK + i], to_f32(g.a[(rt * a.hv + h) * DK + i]));
     }
   }
   __syncthreads();
 
   for (int t = 0; t < T; ++t) {
-    const float* yq = sy + (size_t)t * NCH;
-    const float* yk = yq + DK;
-    const float* yv = yk + DK;
+    const auto yq = sy + (size_t)t * NCH;
+    const auto yk = yq + DK;
+    const auto yv = yk + DK;
     const float rq = sscal[t * 5 + 0], rk = sscal[t * 5 + 1], kq = sscal[t * 5 + 2];
     const float alpha = KDA ? 1.f : sscal[t * 5 + 3], beta = sscal[t * 5 + 4];
     float4 kk[4], qq[4], al[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      const float4 k4 = *reinterpret_cast<const float4*>(yk + M::col(c, seg));
-      const float4 q4 = *reinterpret_cast<const float4*>(yq + M::col(c, seg));
+      const float4 k4 = vec_at<float4>(yk, M::col(c, seg));
+      const float4 q4 = vec_at<float4>(yq, M::col(c, seg));
       kk[c] = make_float4(k4.x * rk, k4.y * rk, k4.z * rk, k4.w * rk);
       qq[c] = make_float4(q4.x * rq, q4.y * rq, q4.z * rq, q4.w * rq);
-      al[c] = KDA ? *reinterpret_cast<const float4*>(salk + (size_t)t * DK + M::col(c, seg))
-                  : make_float4(alpha, alpha, alpha, alpha);
+      al[c] = KDA ? vec_at<float4>(salk, (size_t)t * DK + M::col(c, seg)) : make_float4(alpha, alpha, alpha, alpha);
     }
     const int32_t sid = sids[t];
-    float* Sp = slot_class(sid, a.spec_num_slots) == 0
-                    ? a.spec_ssm + (((size_t)sid * a.hv + h) * a.dv + row0) * DK
-                    : nullptr;
+    const bool keep = slot_class(sid, a.spec_num_slots) == 0;
+    const auto Sp = g.spec_ssm + (keep ? (((size_t)sid * a.hv + h) * a.dv + row0) * DK : 0);
 #pragma unroll
     for (int it = 0; it < NIT; ++it) {
       const int row = it * M::RI + rloc;
@@ -478,10 +505,9 @@ __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const StepArgs a) {
         v.w = fmaf(bu, kk[c].w, al[c].w * v.w);
       }
       if (row < nrows) {
-        if (Sp) {
-          float4* dst = reinterpret_cast<float4*>(Sp + (size_t)row * DK);
+        if (keep) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) st_stream(dst + M::col(c, seg) / 4, s[it][c]);
+          for (int c = 0; c < 4; ++c) st_stream(&vec_at<float4>(Sp, (size_t)row * DK + M::col(c, seg)), s[it][c]);
         }
         if (seg == 0) so[(size_t)t * R + row] = fmaf(bu, kq, alpha * dq_);
       }
@@ -489,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const StepArgs a) {
   }
   __syncthreads();
   for (int t = 0; t < T; ++t) {
-    Tact* out = reinterpret_cast<Tact*>(a.out) + ((((size_t)r * T + t) * a.hv) + h) * a.dv + row0;
+    const auto out = g.out + (((((size_t)r * T + t) * a.hv) + h) * a.dv + row0);
     for (int i = tid; i < nrows; i += kThreads) out[i] = from_f32<Tact>(so[(size_t)t * R + i]);
   }
 }
@@ -557,23 +583,26 @@ struct KdaPrefillSmem {
 // channels of qkv (q, k, then its v rows) and the head's gate logits.  ASYNC:
 // 16-byte cp.async pieces (every segment start and length a multiple of 16
 // bytes, checked on the host); otherwise element copies.
-template <int DK, int NIT, typename Tact, bool ASYNC>
-__device__ __forceinline__ void kda_stage(const KdaPrefillArgs& a, Tact* xr, Tact* gs, int64_t tok, int nt,
+// xr, gs: views of one staging buffer each ([kTW][NCH] and [kTW][DK])
+template <int DK, int NIT, typename Tact, bool ASYNC, typename VS>
+__device__ __forceinline__ void kda_stage(const KdaPrefillArgs& a, const VS& xr, const VS& gs, int64_t tok, int nt,
                                           int nrows, int hq, int h, int row0) {
   using L = KdaPrefillSmem<DK, NIT, Tact>;
-  const Tact* qkv = reinterpret_cast<const Tact*>(a.qkv);
-  const Tact* ga = reinterpret_cast<const Tact*>(a.a);
+  const auto qkv = GDN_GV(reinterpret_cast<const Tact*>(a.qkv), a.total * a.C);
+  const auto ga = GDN_GV(reinterpret_cast<const Tact*>(a.a), a.total * a.hv * DK);
   const int nch = 2 * DK + nrows;
   if constexpr (ASYNC) {
     constexpr int E = 16 / sizeof(Tact);  // elements per piece
     const int per_row = nch / E;
     for (int p = threadIdx.x; p < nt * per_row; p += kThreads) {
       const int t = p / per_row, e = (p % per_row) * E;
-      cp_async16(xr + t * L::NCH + e, qkv + (size_t)(tok + t) * a.C + channel_of<DK>(e, hq, h, a.hk, a.dv, row0));
+      const size_t src = (size_t)(tok + t) * a.C + channel_of<DK>(e, hq, h, a.hk, a.dv, row0);
+      if (xr.has(t * L::NCH + e, E) && qkv.has(src, E)) cp_async16(xr.p + t * L::NCH + e, qkv.p + src);
     }
     for (int p = threadIdx.x; p < nt * (DK / E); p += kThreads) {
       const int t = p / (DK / E), e = (p % (DK / E)) * E;
-      cp_async16(gs + t * DK + e, ga + ((size_t)(tok + t) * a.hv + h) * DK + e);
+      const size_t src = ((size_t)(tok + t) * a.hv + h) * DK + e;
+      if (gs.has(t * DK + e, E) && ga.has(src, E)) cp_async16(gs.p + t * DK + e, ga.p + src);
     }
   } else {
     for (int p = threadIdx.x; p < nt * nch; p += kThreads) {
@@ -597,15 +626,23 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const KdaPrefi
   constexpr int kCPT = (NCH + kThreads - 1) / kThreads;  // channels per thread
   static_assert(kThreads % DK == 0, "a thread's gate channel must be fixed");
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  Tact* xr = reinterpret_cast<Tact*>(smem_raw + L::xr);
-  Tact* gs = reinterpret_cast<Tact*>(smem_raw + L::ga);
-  float* xh = reinterpret_cast<float*>(smem_raw + L::xh);
-  float* cwt = reinterpret_cast<float*>(smem_raw + L::cw);
-  float* sy = reinterpret_cast<float*>(smem_raw + L::sy);
-  float* so = reinterpret_cast<float*>(smem_raw + L::so);
-  float* sscal = reinterpret_cast<float*>(smem_raw + L::sc);
-  float* salk = reinterpret_cast<float*>(smem_raw + L::al);
-  float* sb = reinterpret_cast<float*>(smem_raw + L::sb);
+  const auto xr = GDN_SV(reinterpret_cast<Tact*>(smem_raw + L::xr), 2 * kTW * NCH);
+  const auto gs = GDN_SV(reinterpret_cast<Tact*>(smem_raw + L::ga), 2 * kTW * DK);
+  const auto xh = GDN_SV(reinterpret_cast<float*>(smem_raw + L::xh), (kMaxW - 1) * NCH);
+  const auto cwt = GDN_SV(reinterpret_cast<float*>(smem_raw + L::cw), kMaxW * NCH);
+  const auto sy = GDN_SV(reinterpret_cast<float*>(smem_raw + L::sy), kTW * NCH);
+  const auto so = GDN_SV(reinterpret_cast<float*>(smem_raw + L::so), kTW * R);
+  const auto sscal = GDN_SV(reinterpret_cast<float*>(smem_raw + L::sc), kTW * 4);
+  const auto salk = GDN_SV(reinterpret_cast<float*>(smem_raw + L::al), kTW * DK);
+  const auto sb = GDN_SV(reinterpret_cast<float*>(smem_raw + L::sb), 2 * kTW);
+  const int n_seq = gridDim.y;
+  const auto ssm = GDN_GV(a.ssm, (long long)a.num_slots * a.hv * a.dv * DK);
+  const auto ck_ssm = GDN_GV(a.ck_ssm, (long long)a.ck_num_slots * a.hv * a.dv * DK);
+  const auto conv_w = GDN_GV(a.conv_w, (long long)a.C * a.W);
+  const auto cu_seqlens = GDN_GV(a.cu_seqlens, n_seq + 1);
+  const auto start_pos = GDN_GV(a.start_pos, n_seq);
+  const auto slot_ids = GDN_GV(a.slot_ids, n_seq);
+  const auto ckpt_ids = GDN_GV(a.ckpt_ids, (long long)n_seq * a.max_ckpt);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n = blockIdx.y;
@@ -613,13 +650,13 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const KdaPrefi
   const int hq = h / a.G;
   const int row0 = p * R;
   const int nrows = min(R, a.dv - row0);
-  const int64_t t0 = a.cu_seqlens[n], t1 = a.cu_seqlens[n + 1], len = t1 - t0, p0 = a.start_pos[n];
+  const int64_t t0 = cu_seqlens[n], t1 = cu_seqlens[n + 1], len = t1 - t0, p0 = start_pos[n];
   if (t0 < 0 || len < 0 || t1 > a.total || p0 < 0) {
     if (blockIdx.x == 0 && tid == 0) report(a.err, GDN_DEV_ERR_SEQLENS);
     return;
   }
-  Tact* out = reinterpret_cast<Tact*>(a.out);
-  const int32_t slot = a.slot_ids[n];
+  const auto out = GDN_GV(reinterpret_cast<Tact*>(a.out), a.total * a.hv * a.dv);
+  const int32_t slot = slot_ids[n];
   const int cls = slot_class(slot, a.num_slots);
   if (cls) {
     if (cls == 2 && blockIdx.x == 0 && tid == 0) report(a.err, GDN_DEV_ERR_SLOT_OOB);
@@ -629,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const KdaPrefi
   }
   if (len == 0) return;
 
-  const Tact* gb = reinterpret_cast<const Tact*>(a.b);
+  const auto gb = GDN_GV(reinterpret_cast<const Tact*>(a.b), a.total * a.hv);
   // the first window's inputs in flight before anything else
   kda_stage<DK, NIT, Tact, ASYNC>(a, xr, gs, t0, len < kTW ? (int)len : kTW, nrows, hq, h, row0);
   if constexpr (ASYNC) cp_async_commit();
@@ -637,23 +674,25 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const KdaPrefi
 
   const int seg = lane % M::LPR;
   const int rloc = warp * M::RW + lane / M::LPR;
-  float* St = a.ssm + (((size_t)slot * a.hv + h) * a.dv + row0) * DK;
+  const auto St = ssm + (((size_t)slot * a.hv + h) * a.dv + row0) * DK;
   float4 s[NIT][4];
   load_rows<DK, NIT>(s, St, nrows, rloc, seg);
 
   // conv weights and history, right-aligned in kMaxW taps (the newest input
   // last; the taps before the width are zero), one column per channel
-  const Tconv* hist = reinterpret_cast<const Tconv*>(a.conv) + (size_t)slot * (a.W - 1) * a.C;
+  const auto hist = GDN_GV(reinterpret_cast<const Tconv*>(a.conv), (long long)a.num_slots * (a.W - 1) * a.C) +
+                    (size_t)slot * (a.W - 1) * a.C;
   const int lead = kMaxW - a.W;
   for (int i = tid; i < 2 * DK + nrows; i += kThreads) {
     const int ch = channel_of<DK>(i, hq, h, a.hk, a.dv, row0);
 #pragma unroll
-    for (int j = 0; j < kMaxW; ++j) cwt[j * NCH + i] = j >= lead ? a.conv_w[(size_t)ch * a.W + (j - lead)] : 0.f;
+    for (int j = 0; j < kMaxW; ++j) cwt[j * NCH + i] = j >= lead ? conv_w[(size_t)ch * a.W + (j - lead)] : 0.f;
 #pragma unroll
     for (int j = 0; j < kMaxW - 1; ++j) xh[j * NCH + i] = j >= lead ? to_f32(hist[(size_t)(j - lead) * a.C + ch]) : 0.f;
   }
-  const float eA = expf(a.A_log[h]);
-  const float dtb = a.dt_bias[(size_t)h * DK + tid % DK];  // the alphas this thread computes are of channel tid % DK
+  const float eA = expf(GDN_GV(a.A_log, a.hv)[h]);
+  // the alphas this thread computes are of channel tid % DK
+  const float dtb = GDN_GV(a.dt_bias, (long long)a.hv * DK)[(size_t)h * DK + tid % DK];
   const int64_t blk0 = p0 / a.ckpt_block;
   // the next block boundary (absolute position) and its checkpoint index
   int64_t next_bd = (blk0 + 1) * a.ckpt_block;
@@ -669,12 +708,13 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const KdaPrefi
     // 0. the next window's inputs
     float bnext = 0.f;
     if (ntn > 0) {
-      kda_stage<DK, NIT, Tact, ASYNC>(a, xr + nxt * kTW * NCH, gs + nxt * kTW * DK, t0 + wn, ntn, nrows, hq, h, row0);
+      kda_stage<DK, NIT, Tact, ASYNC>(a, xr + nxt * kTW * NCH, gs + nxt * kTW * DK, t0 + wn, ntn, nrows, hq, h,
+                                      row0);
       if constexpr (ASYNC) cp_async_commit();
       if (tid < ntn) bnext = to_f32(gb[(size_t)(t0 + wn + tid) * a.hv + h]);
     }
-    const Tact* x = xr + cur * kTW * NCH;
-    const Tact* gw = gs + cur * kTW * DK;
+    const auto x = xr + cur * kTW * NCH;
+    const auto gw = gs + cur * kTW * DK;
     // 1. conv1d + SiLU of the window's tokens (oldest tap first)
 #pragma unroll
     for (int ci = 0; ci < kCPT; ++ci) {
@@ -707,8 +747,8 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const KdaPrefi
     __syncthreads();
     // 2. per token: q/k norms, k^.q^, beta (a warp per token) and the alphas
     for (int t = warp; t < nt; t += kWarps) {
-      const float* yq = sy + t * NCH;
-      const float* yk = yq + DK;
+      const auto yq = sy + t * NCH;
+      const auto yk = yq + DK;
       float pq = 0.f, pk = 0.f, pqk = 0.f;
       for (int i = lane; i < DK; i += 32) {
         pq = fmaf(yq[i], yq[i], pq);
@@ -735,28 +775,33 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const KdaPrefi
     __syncthreads();
     // 3. the recurrence over the window's tokens
     for (int t = 0; t < nt; ++t) {
-      const float* yq = sy + t * NCH;
-      const float* yk = yq + DK;
-      const float* yv = yk + DK;
+      const auto yq = sy + t * NCH;
+      const auto yk = yq + DK;
+      const auto yv = yk + DK;
       const float rq = sscal[t * 4 + 0], rk = sscal[t * 4 + 1], kq = sscal[t * 4 + 2], beta = sscal[t * 4 + 3];
       // unnormalised q and k: the norms scale the dot products and the update
       float4 kr[4], qr[4], al[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        kr[c] = *reinterpret_cast<const float4*>(yk + M::col(c, seg));
-        qr[c] = *reinterpret_cast<const float4*>(yq + M::col(c, seg));
-        al[c] = *reinterpret_cast<const float4*>(salk + t * DK + M::col(c, seg));
+        kr[c] = vec_at<float4>(yk, M::col(c, seg));
+        qr[c] = vec_at<float4>(yq, M::col(c, seg));
+        al[c] = vec_at<float4>(salk, t * DK + M::col(c, seg));
       }
       // a block boundary after this token: its checkpoint slot
-      float* ck = nullptr;
+      bool to_ck = false;
+      auto ck = ck_ssm;
       if (p0 + w0 + t + 1 == next_bd) {
         const int64_t idx = ck_idx++;
         next_bd += a.ckpt_block;
         if (idx < a.max_ckpt) {
-          const int32_t cid = a.ckpt_ids[(size_t)n * a.max_ckpt + idx];
+          const int32_t cid = ckpt_ids[(size_t)n * a.max_ckpt + idx];
           const int cc = slot_class(cid, a.ck_num_slots);
-          if (cc == 0) ck = a.ck_ssm + (((size_t)cid * a.hv + h) * a.dv + row0) * DK;
-          else if (cc == 2 && tid == 0) report(a.err, GDN_DEV_ERR_SLOT_OOB);
+          if (cc == 0) {
+            to_ck = true;
+            ck = ck_ssm + (((size_t)cid * a.hv + h) * a.dv + row0) * DK;
+          } else if (cc == 2 && tid == 0) {
+            report(a.err, GDN_DEV_ERR_SLOT_OOB);
+          }
         }
       }
 #pragma unroll
@@ -788,10 +833,9 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const KdaPrefi
           v = make_float4(lo.x, lo.y, hi.x, hi.y);
         }
         if (row < nrows) {
-          if (ck) {
-            float4* dst = reinterpret_cast<float4*>(ck + (size_t)row * DK);
+          if (to_ck) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) st_stream(dst + M::col(c, seg) / 4, s[it][c]);
+            for (int c = 0; c < 4; ++c) st_stream(&vec_at<float4>(ck, (size_t)row * DK + M::col(c, seg)), s[it][c]);
           }
           if (seg == 0) so[t * R + row] = fmaf(bu, kq, dq_);
         }
@@ -812,9 +856,8 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const KdaPrefi
   for (int it = 0; it < NIT; ++it) {
     const int row = it * M::RI + rloc;
     if (row < nrows) {
-      float4* dst = reinterpret_cast<float4*>(St + (size_t)row * DK);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) st_stream(dst + M::col(c, seg) / 4, s[it][c]);
+      for (int c = 0; c < 4; ++c) st_stream(&vec_at<float4>(St, (size_t)row * DK + M::col(c, seg)), s[it][c]);
     }
   }
 }

@@ -106,6 +106,11 @@ __global__ void __launch_bounds__(kThr, MINB) decode_tma_kernel(const TmaArgs a)
   const int nchunks = GR / kRows;
   const int nch = 2 * kDK + GR;        // conv channels per item
   volatile int* abort_flag = &S.abort;
+  // extents of the caller's tensors (elements), for the checked build
+  const int nreq = a.n_items / a.hk;
+  [[maybe_unused]] const long long ssm_n = (long long)a.num_slots * a.hv * a.dv * kDK,
+                                   conv_n = (long long)a.num_slots * (kW - 1) * a.C,
+                                   out_n = (long long)nreq * a.hv * a.dv, gate_n = (long long)nreq * a.hv;
 
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -135,7 +140,7 @@ __global__ void __launch_bounds__(kThr, MINB) decode_tma_kernel(const TmaArgs a)
     bool ok = true;
     for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
       const int r = item / a.hk, hq = item % a.hk;
-      const int32_t slot = a.slot_ids[r];
+      const int32_t slot = a.slot_ids[GDN_G(r, nreq)];
       if (slot_class(slot, a.num_slots)) continue;
       if (*abort_flag) break;
       const int bb = vk & 1;
@@ -144,24 +149,32 @@ __global__ void __launch_bounds__(kThr, MINB) decode_tma_kernel(const TmaArgs a)
       typename SM::Bundle& B = S.bundle[bb];
       const size_t cq = (size_t)hq * kDK, ck = (size_t)a.hk * kDK + cq,
                    cv = 2 * (size_t)a.hk * kDK + (size_t)hq * GR;
+      // one bundle copy: `bytes` from global src (inside [base, base + extent))
+      // into the shared bundle
+      auto g2s = [&](void* dst, const void* src, uint32_t bytes, [[maybe_unused]] const void* base,
+                     [[maybe_unused]] long long extent) {
+        if (GDN_GBYTES(src, bytes, base, extent) && GDN_SBYTES(dst, bytes, S))
+          bulk_g2s(dst, src, bytes, &S.bfull[bb]);
+      };
       const Tconv* hist = reinterpret_cast<const Tconv*>(a.conv) + (size_t)slot * (kW - 1) * a.C;
       for (int j = 0; j < kW - 1; ++j) {
-        bulk_g2s(&B.hist[j][0], hist + (size_t)j * a.C + cq, kDK * esz_c, &S.bfull[bb]);
-        bulk_g2s(&B.hist[j][kDK], hist + (size_t)j * a.C + ck, kDK * esz_c, &S.bfull[bb]);
-        bulk_g2s(&B.hist[j][2 * kDK], hist + (size_t)j * a.C + cv, GR * esz_c, &S.bfull[bb]);
+        g2s(&B.hist[j][0], hist + (size_t)j * a.C + cq, kDK * esz_c, a.conv, conv_n * esz_c);
+        g2s(&B.hist[j][kDK], hist + (size_t)j * a.C + ck, kDK * esz_c, a.conv, conv_n * esz_c);
+        g2s(&B.hist[j][2 * kDK], hist + (size_t)j * a.C + cv, GR * esz_c, a.conv, conv_n * esz_c);
       }
       const Tact* x = reinterpret_cast<const Tact*>(a.qkv) + (size_t)r * a.C;
-      bulk_g2s(&B.x[0], x + cq, kDK * esz_a, &S.bfull[bb]);
-      bulk_g2s(&B.x[kDK], x + ck, kDK * esz_a, &S.bfull[bb]);
-      bulk_g2s(&B.x[2 * kDK], x + cv, GR * esz_a, &S.bfull[bb]);
-      bulk_g2s(&B.w[0], a.conv_w + cq * kW, kDK * kW * 4, &S.bfull[bb]);
-      bulk_g2s(&B.w[kDK * kW], a.conv_w + ck * kW, kDK * kW * 4, &S.bfull[bb]);
-      bulk_g2s(&B.w[2 * kDK * kW], a.conv_w + cv * kW, GR * kW * 4, &S.bfull[bb]);
+      const long long x_bytes = (long long)nreq * a.C * esz_a, w_bytes = (long long)a.C * kW * 4;
+      g2s(&B.x[0], x + cq, kDK * esz_a, a.qkv, x_bytes);
+      g2s(&B.x[kDK], x + ck, kDK * esz_a, a.qkv, x_bytes);
+      g2s(&B.x[2 * kDK], x + cv, GR * esz_a, a.qkv, x_bytes);
+      g2s(&B.w[0], a.conv_w + cq * kW, kDK * kW * 4, a.conv_w, w_bytes);
+      g2s(&B.w[kDK * kW], a.conv_w + ck * kW, kDK * kW * 4, a.conv_w, w_bytes);
+      g2s(&B.w[2 * kDK * kW], a.conv_w + cv * kW, GR * kW * 4, a.conv_w, w_bytes);
       if (KDA) {
         const size_t h0 = (size_t)hq * a.G;
-        bulk_g2s(&B.ga[0], reinterpret_cast<const Tact*>(a.a) + ((size_t)r * a.hv + h0) * kDK,
-                 a.G * kDK * esz_a, &S.bfull[bb]);
-        bulk_g2s(&B.gdt[0], a.dt_bias + h0 * kDK, a.G * kDK * 4, &S.bfull[bb]);
+        g2s(&B.ga[0], reinterpret_cast<const Tact*>(a.a) + ((size_t)r * a.hv + h0) * kDK, a.G * kDK * esz_a, a.a,
+            gate_n * kDK * esz_a);
+        g2s(&B.gdt[0], a.dt_bias + h0 * kDK, a.G * kDK * 4, a.dt_bias, (long long)a.hv * kDK * 4);
       }
       ++vk;
       const float* src = a.ssm + ((size_t)slot * a.hv + (size_t)hq * a.G) * a.dv * kDK;
@@ -169,7 +182,9 @@ __global__ void __launch_bounds__(kThr, MINB) decode_tma_kernel(const TmaArgs a)
         const int st = n % STAGES;
         if (*abort_flag || !mbar_wait(&S.empty[st], ((n / STAGES) & 1) ^ 1)) { ok = false; break; }
         mbar_arrive_expect_tx(&S.full[st], kStageBytes);
-        bulk_g2s(S.ring[st], src + (size_t)c * kStageFloats, kStageBytes, &S.full[st]);
+        if (GDN_GBYTES(src + (size_t)c * kStageFloats, kStageBytes, a.ssm, ssm_n * 4) &&
+            GDN_SBYTES(S.ring[GDN_S(st, STAGES)], kStageBytes, S))
+          bulk_g2s(S.ring[st], src + (size_t)c * kStageFloats, kStageBytes, &S.full[st]);
       }
     }
     if (!ok || *abort_flag) {
@@ -188,17 +203,18 @@ __global__ void __launch_bounds__(kThr, MINB) decode_tma_kernel(const TmaArgs a)
   const int rloc = warp * (32 / kLPR) + lane / kLPR;  // row within a chunk
   uint32_t n = 0, vk = 0;
   int item = blockIdx.x;
-  int32_t slot_next = item < a.n_items ? a.slot_ids[item / a.hk] : -1;
+  int32_t slot_next = item < a.n_items ? a.slot_ids[GDN_G(item / a.hk, nreq)] : -1;
   for (; item < a.n_items; item += gridDim.x) {
     const int r = item / a.hk, hq = item % a.hk;
     const int32_t slot = slot_next;
     const int nitem = item + gridDim.x;
-    if (nitem < a.n_items) slot_next = a.slot_ids[nitem / a.hk];
-    Tact* out = reinterpret_cast<Tact*>(a.out) + ((size_t)r * a.hv + (size_t)hq * a.G) * a.dv;
+    if (nitem < a.n_items) slot_next = a.slot_ids[GDN_G(nitem / a.hk, nreq)];
+    Tact* const out_all = reinterpret_cast<Tact*>(a.out);
+    const size_t out0 = ((size_t)r * a.hv + (size_t)hq * a.G) * a.dv;
     const int cls = slot_class(slot, a.num_slots);
     if (cls) {
       if (cls == 2 && hq == 0 && tid == 0) report(a.err, GDN_DEV_ERR_SLOT_OOB);
-      for (int i = tid; i < GR; i += kCons) out[i] = from_f32<Tact>(0.f);
+      for (int i = tid; i < GR; i += kCons) out_all[GDN_G(out0 + i, out_n)] = from_f32<Tact>(0.f);
       continue;
     }
     const int bb = vk & 1;
@@ -208,11 +224,13 @@ __global__ void __launch_bounds__(kThr, MINB) decode_tma_kernel(const TmaArgs a)
     const typename SM::Bundle& B = S.bundle[bb];
     // conv1d + SiLU; the old history is in the bundle, so the new one can be
     // written at once (this CTA is the only one touching these channels)
-    Tconv* hist = reinterpret_cast<Tconv*>(a.conv) + (size_t)slot * (kW - 1) * a.C;
-    for (int i = tid; i < nch; i += kCons) {
+    Tconv* const hist_all = reinterpret_cast<Tconv*>(a.conv);
+    const size_t hist0 = (size_t)slot * (kW - 1) * a.C;
+    for (int i0 = tid; i0 < nch; i0 += kCons) {
+      const int i = GDN_S(i0, kMaxCh);
       const float h0 = to_f32(B.hist[0][i]), h1 = to_f32(B.hist[1][i]), h2 = to_f32(B.hist[2][i]);
       const float xv = to_f32(B.x[i]);
-      const float4 w = *reinterpret_cast<const float4*>(&B.w[i * kW]);
+      const float4 w = reinterpret_cast<const float4*>(B.w)[i];  // kW = 4 weights of channel i
       float acc = w.x * h0;
       acc = fmaf(w.y, h1, acc);
       acc = fmaf(w.z, h2, acc);
@@ -221,24 +239,25 @@ __global__ void __launch_bounds__(kThr, MINB) decode_tma_kernel(const TmaArgs a)
       const size_t c = i < kDK ? (size_t)hq * kDK + i
                      : i < 2 * kDK ? (size_t)a.hk * kDK + (size_t)hq * kDK + (i - kDK)
                                    : 2 * (size_t)a.hk * kDK + (size_t)hq * GR + (i - 2 * kDK);
-      hist[c] = B.hist[1][i];
-      hist[a.C + c] = B.hist[2][i];
-      hist[2 * (size_t)a.C + c] = from_f32<Tconv>(xv);
+      hist_all[GDN_G(hist0 + c, conv_n)] = B.hist[1][i];
+      hist_all[GDN_G(hist0 + a.C + c, conv_n)] = B.hist[2][i];
+      hist_all[GDN_G(hist0 + 2 * (size_t)a.C + c, conv_n)] = from_f32<Tconv>(xv);
     }
     if (KDA) {
-      for (int e = tid; e < a.G * kDK; e += kCons) {
+      for (int e0 = tid; e0 < a.G * kDK; e0 += kCons) {
+        const int e = GDN_S(e0, (KDA ? kMaxGR / kRows : 1) * kDK);
         const int gi = e / kDK, h = hq * a.G + gi;
-        S.sal[gi][e % kDK] = gate_alpha(a.A_log[h], B.gdt[e], to_f32(B.ga[e]));
+        S.sal[KDA ? gi : 0][e % kDK] = gate_alpha(a.A_log[GDN_G(h, a.hv)], B.gdt[e], to_f32(B.ga[e]));
       }
     }
     if (tid < a.G) {
-      const int h = hq * a.G + tid;
-      const float bv = to_f32(reinterpret_cast<const Tact*>(a.b)[(size_t)r * a.hv + h]);
+      const int h = GDN_G(hq * a.G + tid, a.hv), tg = GDN_S(tid, 8);
+      const float bv = to_f32(reinterpret_cast<const Tact*>(a.b)[GDN_G((size_t)r * a.hv + h, gate_n)]);
       if (!KDA) {
-        const float av = to_f32(reinterpret_cast<const Tact*>(a.a)[(size_t)r * a.hv + h]);
-        S.sgate[0][tid] = gate_alpha(a.A_log[h], a.dt_bias[h], av);
+        const float av = to_f32(reinterpret_cast<const Tact*>(a.a)[GDN_G((size_t)r * a.hv + h, gate_n)]);
+        S.sgate[0][tg] = gate_alpha(a.A_log[h], a.dt_bias[h], av);
       }
-      S.sgate[1][tid] = sigmoid_f(bv);
+      S.sgate[1][tg] = sigmoid_f(bv);
     }
     named_sync(kBarCons, kCons);
     mbar_arrive(&S.bempty[bb]);
@@ -259,9 +278,10 @@ __global__ void __launch_bounds__(kThr, MINB) decode_tma_kernel(const TmaArgs a)
         pqk += __shfl_xor_sync(0xffffffffu, pqk, o);
       }
       if (lane == 0) {
-        S.sred[0][warp] = pq;
-        S.sred[1][warp] = pk;
-        S.sred[2][warp] = pqk;
+        const int w = GDN_S(warp, kCW);
+        S.sred[0][w] = pq;
+        S.sred[1][w] = pk;
+        S.sred[2][w] = pqk;
       }
       named_sync(kBarCons, kCons);
       if (tid == 0) {
@@ -283,13 +303,13 @@ __global__ void __launch_bounds__(kThr, MINB) decode_tma_kernel(const TmaArgs a)
     float4 kk[4], qq[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      const int col = c * 4 * kLPR + seg * 4;
+      const int col = GDN_S(c * 4 * kLPR + seg * 4, kDK - 3);
       const float4 k4 = *reinterpret_cast<const float4*>(&S.sy[kDK + col]);
       const float4 q4 = *reinterpret_cast<const float4*>(&S.sy[col]);
       kk[c] = make_float4(k4.x * rk, k4.y * rk, k4.z * rk, k4.w * rk);
       qq[c] = make_float4(q4.x * rq, q4.y * rq, q4.z * rq, q4.w * rq);
     }
-    float* dst_base = a.ssm + ((size_t)slot * a.hv + (size_t)hq * a.G) * a.dv * kDK;
+    const size_t dst0 = ((size_t)slot * a.hv + (size_t)hq * a.G) * a.dv * kDK;
     // KDA: this lane's alphas of the current V head (a chunk's 32 rows belong
     // to one head; reloaded only when the head changes)
     float4 al[4];
@@ -298,20 +318,21 @@ __global__ void __launch_bounds__(kThr, MINB) decode_tma_kernel(const TmaArgs a)
       const int st = n % STAGES;
       if (!*abort_flag && !mbar_wait(&S.full[st], (n / STAGES) & 1)) *abort_flag = 1;
       if (*abort_flag) continue;
-      const int grow = c * kRows + rloc;  // row within the group
-      const int g = grow / a.dv;
+      const int grow = GDN_S(c * kRows + rloc, kMaxGR);  // row within the group
+      const int g = GDN_S(grow / a.dv, 8);
       const float alpha = KDA ? 1.f : S.sgate[0][g], beta = S.sgate[1][g];
-      const float* srow = S.ring[st] + rloc * kDK;
+      const float* srow = S.ring[GDN_S(st, STAGES)] + GDN_S(rloc, kRows) * kDK;
       float4 s4[4];
       if (g != g_al) {
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc)
-          al[cc] = KDA ? *reinterpret_cast<const float4*>(&S.sal[KDA ? g : 0][cc * 4 * kLPR + seg * 4])
+          al[cc] = KDA ? *reinterpret_cast<const float4*>(&S.sal[KDA ? g : 0][GDN_S(cc * 4 * kLPR + seg * 4, kDK - 3)])
                        : make_float4(alpha, alpha, alpha, alpha);
         g_al = g;
       }
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) s4[cc] = *reinterpret_cast<const float4*>(srow + cc * 4 * kLPR + seg * 4);
+      for (int cc = 0; cc < 4; ++cc)
+        s4[cc] = *reinterpret_cast<const float4*>(srow + GDN_S(cc * 4 * kLPR + seg * 4, kDK - 3));
       float dk_ = 0.f, dq_ = 0.f;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
@@ -329,8 +350,9 @@ __global__ void __launch_bounds__(kThr, MINB) decode_tma_kernel(const TmaArgs a)
         dk_ += __shfl_xor_sync(0xffffffffu, dk_, o);
         dq_ += __shfl_xor_sync(0xffffffffu, dq_, o);
       }
-      const float bu = beta * (S.sy[2 * kDK + grow] - alpha * dk_);
-      float4* drow = reinterpret_cast<float4*>(dst_base + (size_t)grow * kDK);
+      const float bu = beta * (S.sy[GDN_S(2 * kDK + grow, kMaxCh)] - alpha * dk_);
+      float4* const ssm4 = reinterpret_cast<float4*>(a.ssm);
+      const size_t drow4 = (dst0 + (size_t)grow * kDK) / 4;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         float4 v = s4[cc];
@@ -338,13 +360,13 @@ __global__ void __launch_bounds__(kThr, MINB) decode_tma_kernel(const TmaArgs a)
         v.y = fmaf(bu, kk[cc].y, al[cc].y * v.y);
         v.z = fmaf(bu, kk[cc].z, al[cc].z * v.z);
         v.w = fmaf(bu, kk[cc].w, al[cc].w * v.w);
-        st_stream(drow + (cc * 4 * kLPR + seg * 4) / 4, v);
+        st_stream(ssm4 + GDN_G(drow4 + (cc * 4 * kLPR + seg * 4) / 4, ssm_n / 4), v);
       }
       if (seg == 0) S.so[grow] = fmaf(bu, kq, alpha * dq_);
     }
     named_sync(kBarCons, kCons);
     if (*abort_flag) break;
-    for (int i = tid; i < GR; i += kCons) out[i] = from_f32<Tact>(S.so[i]);
+    for (int i = tid; i < GR; i += kCons) out_all[GDN_G(out0 + i, out_n)] = from_f32<Tact>(S.so[GDN_S(i, kMaxGR)]);
   }
   if (*abort_flag && tid == 0) report(a.err, GDN_DEV_ERR_TIMEOUT);
 }

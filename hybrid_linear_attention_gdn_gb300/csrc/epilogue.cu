@@ -34,11 +34,12 @@ template <> struct VecOf<float, 2> { using t = float2; };
 template <> struct VecOf<float, 4> { using t = float4; };
 template <> struct VecOf<float, 8> { using t = float4; };  // unused: 32 bytes are never one access
 
-template <typename T, int EPL, bool VEC>
-__device__ __forceinline__ void load_part(const T* row, int j0, int dv, float (&v)[EPL]) {
+// row: a view of one row's dv elements
+template <typename T, int EPL, bool VEC, typename R>
+__device__ __forceinline__ void load_part(const R& row, int j0, int dv, float (&v)[EPL]) {
   if constexpr (VEC) {
     T tmp[EPL];
-    const typename VecOf<T, EPL>::t u = *reinterpret_cast<const typename VecOf<T, EPL>::t*>(row + j0);
+    const typename VecOf<T, EPL>::t u = vec_at<const typename VecOf<T, EPL>::t>(row, j0);
     memcpy(tmp, &u, sizeof(tmp));
 #pragma unroll
     for (int e = 0; e < EPL; ++e) v[e] = to_f32(tmp[e]);
@@ -48,15 +49,15 @@ __device__ __forceinline__ void load_part(const T* row, int j0, int dv, float (&
   }
 }
 
-template <typename T, int EPL, bool VEC>
-__device__ __forceinline__ void store_part(T* row, int j0, int dv, const float (&v)[EPL]) {
+template <typename T, int EPL, bool VEC, typename R>
+__device__ __forceinline__ void store_part(const R& row, int j0, int dv, const float (&v)[EPL]) {
   if constexpr (VEC) {
     T tmp[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) tmp[e] = from_f32<T>(v[e]);
     typename VecOf<T, EPL>::t u;
     memcpy(&u, tmp, sizeof(tmp));
-    *reinterpret_cast<typename VecOf<T, EPL>::t*>(row + j0) = u;
+    vec_at<typename VecOf<T, EPL>::t>(row, j0) = u;
   } else {
 #pragma unroll
     for (int e = 0; e < EPL; ++e)
@@ -74,20 +75,23 @@ __global__ void __launch_bounds__(32 * kWarps)
   const int64_t r0 = ((int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5)) * kRowsPerWarp;
   if (r0 >= rows) return;
   const int j0 = lane * EPL;
+  const auto ov_ = GDN_GV(o, rows * dv), zv_ = GDN_GV(z, rows * dv);
+  const auto yv_ = GDN_GV(y, rows * dv);
+  const auto wv_ = GDN_GV(w, dv);
   float ov[kRowsPerWarp][EPL], zv[kRowsPerWarp][EPL], wv[EPL];
   // every load of the warp's rows in flight before the first reduction
 #pragma unroll
   for (int i = 0; i < kRowsPerWarp; ++i) {
     if (r0 + i < rows) {
-      load_part<T, EPL, VEC>(o + (r0 + i) * dv, j0, dv, ov[i]);
-      load_part<T, EPL, VEC>(z + (r0 + i) * dv, j0, dv, zv[i]);
+      load_part<T, EPL, VEC>(ov_ + (r0 + i) * dv, j0, dv, ov[i]);
+      load_part<T, EPL, VEC>(zv_ + (r0 + i) * dv, j0, dv, zv[i]);
     } else {
 #pragma unroll
       for (int e = 0; e < EPL; ++e) ov[i][e] = zv[i][e] = 0.f;
     }
   }
 #pragma unroll
-  for (int e = 0; e < EPL; ++e) wv[e] = j0 + e < dv ? w[j0 + e] : 0.f;
+  for (int e = 0; e < EPL; ++e) wv[e] = j0 + e < dv ? wv_[j0 + e] : 0.f;
   float ss[kRowsPerWarp];
 #pragma unroll
   for (int i = 0; i < kRowsPerWarp; ++i) {
@@ -109,7 +113,7 @@ __global__ void __launch_bounds__(32 * kWarps)
       const float gate = zv[i][e] / (1.f + exp_ftz(-zv[i][e]));  // silu(z)
       yv[e] = ov[i][e] * inv * wv[e] * gate;
     }
-    store_part<T, EPL, VEC>(y + (r0 + i) * dv, j0, dv, yv);
+    store_part<T, EPL, VEC>(yv_ + (r0 + i) * dv, j0, dv, yv);
   }
 }
 

@@ -32,6 +32,163 @@ __device__ __forceinline__ void report(uint32_t* err, uint32_t bits) {
   if (err) atomicOr(err, bits);
 }
 
+// ---- bounds-checked build ----------------------------------------------------
+// Compiled with -DGDN_DEBUG_BOUNDS (the separate libgdn_debug.so), every
+// computed index of the kernels goes through one of the checks below: global
+// (GDN_G), shared (GDN_S) and TMEM (GDN_T) element indices, and spans of bulk
+// copies (GDN_SPAN_G / GDN_SPAN_S).  An index outside its buffer is recorded
+// in this translation unit's bounds word (how many, and the first one's line,
+// kind, index and limit); the access is then redirected to element 0 (an
+// index) or skipped (a span), so a failing check neither faults nor traps.
+// The host reads and clears the words with gdn_debug_bounds_take().  In the
+// normal build every check is the identity and compiles away.
+struct BoundsWord {
+  unsigned int count;
+  int line, kind;  // kind: 0 global, 1 shared, 2 TMEM
+  long long index, limit;
+};
+#ifdef GDN_DEBUG_BOUNDS
+#ifndef GDN_TU
+#define GDN_TU "?"
+#endif
+namespace {
+__device__ BoundsWord g_bounds_word;
+__device__ __noinline__ void bounds_fail(int line, int kind, long long i, long long n) {
+  if (atomicAdd(&g_bounds_word.count, 1u) == 0) {
+    g_bounds_word.line = line;
+    g_bounds_word.kind = kind;
+    g_bounds_word.index = i;
+    g_bounds_word.limit = n;
+  }
+}
+template <typename I>
+__device__ __forceinline__ I bounds_ix(I i, long long n, int line, int kind) {
+  if ((unsigned long long)(long long)i < (unsigned long long)n) return i;
+  bounds_fail(line, kind, (long long)i, n);
+  return I(0);
+}
+// [off, off + len) inside [0, n)
+__device__ __forceinline__ bool bounds_span(long long off, long long len, long long n, int line, int kind) {
+  if (off >= 0 && len >= 0 && off + len <= n) return true;
+  bounds_fail(line, kind, off + len, n);
+  return false;
+}
+}  // namespace
+#define GDN_G(i, n) ::gdn::bounds_ix((i), (long long)(n), __LINE__, 0)
+#define GDN_S(i, n) ::gdn::bounds_ix((i), (long long)(n), __LINE__, 1)
+#define GDN_T(i, n) ::gdn::bounds_ix((i), (long long)(n), __LINE__, 2)
+#define GDN_SPAN_G(off, len, n) ::gdn::bounds_span((long long)(off), (long long)(len), (long long)(n), __LINE__, 0)
+#define GDN_SPAN_S(off, len, n) ::gdn::bounds_span((long long)(off), (long long)(len), (long long)(n), __LINE__, 1)
+#else
+#define GDN_G(i, n) (i)
+#define GDN_S(i, n) (i)
+#define GDN_T(i, n) (i)
+#define GDN_SPAN_G(off, len, n) true
+#define GDN_SPAN_S(off, len, n) true
+#endif
+// A buffer seen by a kernel: a pointer and, in the checked build, the
+// buffer's extent (elements) and the line that made the view.  Indexing,
+// at() and sub-views are checked there; a failed check is recorded and the
+// access goes to a small per-unit scratch buffer instead.  In the normal
+// build a View is its pointer.
+#ifdef GDN_DEBUG_BOUNDS
+namespace {
+__device__ __align__(16) unsigned char g_bounds_sink[256];
+}  // namespace
+#endif
+template <typename T, int KIND>
+struct View {
+  T* p;
+#ifdef GDN_DEBUG_BOUNDS
+  long long n;
+  int line;
+#endif
+  // element i (checked: i inside the view)
+  __device__ __forceinline__ T& operator[](long long i) const { return *at(i, 1); }
+  // pointer to element i, where w elements from i on are inside the view
+  __device__ __forceinline__ T* at(long long i, long long w = 1) const {
+#ifdef GDN_DEBUG_BOUNDS
+    if (i < 0 || i + w > n || w * (long long)sizeof(T) > (long long)sizeof(g_bounds_sink)) {
+      bounds_fail(line, KIND, i + w - 1, n);
+      return reinterpret_cast<T*>(g_bounds_sink);
+    }
+#endif
+    return p + i;
+  }
+  // whether elements [i, i + w) are inside the view (a failure is recorded);
+  // for asynchronous copies, which are skipped rather than redirected
+  __device__ __forceinline__ bool has([[maybe_unused]] long long i, [[maybe_unused]] long long w) const {
+#ifdef GDN_DEBUG_BOUNDS
+    if (i < 0 || i + w > n) {
+      bounds_fail(line, KIND, i + w - 1, n);
+      return false;
+    }
+#endif
+    return true;
+  }
+  // the view from element off on
+  __device__ __forceinline__ View operator+(long long off) const {
+    View v = *this;
+#ifdef GDN_DEBUG_BOUNDS
+    if (off < 0 || off > n) {
+      bounds_fail(line, KIND, off, n);
+      v.n = 0;
+      return v;
+    }
+    v.n = n - off;
+#endif
+    v.p = p + off;
+    return v;
+  }
+};
+// a view of the buffer p[0 .. n) (n ignored in the normal build)
+template <int KIND, typename T>
+__device__ __forceinline__ View<T, KIND> make_view(T* p, [[maybe_unused]] long long n,
+                                                   [[maybe_unused]] int line) {
+  View<T, KIND> v;
+  v.p = p;
+#ifdef GDN_DEBUG_BOUNDS
+  v.n = n;
+  v.line = line;
+#endif
+  return v;
+}
+template <typename V, typename T, int KIND>
+__device__ __forceinline__ V& vec_at(const View<T, KIND>& v, long long i) {
+  static_assert(sizeof(V) % sizeof(T) == 0, "a vector of whole elements");
+  return *reinterpret_cast<V*>(v.at(i, (long long)(sizeof(V) / sizeof(T))));
+}
+// the same on a plain pointer (unchecked)
+template <typename V, typename T>
+__device__ __forceinline__ V& vec_at(T* p, long long i) {
+  return *reinterpret_cast<V*>(p + i);
+}
+// The V at byte offset `off` of a shared-memory tile of `bytes` bytes
+// (checked: the V lies inside the tile; a failure is recorded against the
+// caller's line and the access goes to the tile's start).
+template <typename V>
+__device__ __forceinline__ V& tile_at(unsigned char* tile, [[maybe_unused]] unsigned bytes, unsigned off,
+                                      [[maybe_unused]] int line = __builtin_LINE()) {
+#ifdef GDN_DEBUG_BOUNDS
+  if ((unsigned long long)off + sizeof(V) > bytes) {
+    bounds_fail(line, 1, (long long)off + (long long)sizeof(V) - 1, bytes);
+    off = 0;
+  }
+#endif
+  return *reinterpret_cast<V*>(tile + off);
+}
+#define GDN_GV(p, n) ::gdn::make_view<0>((p), (long long)(n), __LINE__)
+#define GDN_SV(p, n) ::gdn::make_view<1>((p), (long long)(n), __LINE__)
+
+// byte distance from `base` to `p`
+__host__ __device__ __forceinline__ long long byte_off(const void* base, const void* p) {
+  return (long long)(reinterpret_cast<const unsigned char*>(p) - reinterpret_cast<const unsigned char*>(base));
+}
+// `bytes` at global `p` inside the buffer [base, base + extent bytes)
+#define GDN_GBYTES(p, bytes, base, extent) GDN_SPAN_G(::gdn::byte_off((base), (p)), (bytes), (extent))
+// `bytes` at shared `p` inside the CTA's shared-memory struct `S`
+#define GDN_SBYTES(p, bytes, S) GDN_SPAN_S(::gdn::byte_off(&(S), (p)), (bytes), sizeof(S))
+
 // 0 = usable, 1 = padding (-1), 2 = out of range
 __device__ __forceinline__ int slot_class(int32_t id, int32_t n) {
   if (id == -1) return 1;
@@ -262,6 +419,21 @@ inline size_t ssm_slot_bytes(const gdn_dims& d) {
 inline size_t conv_slot_bytes(const gdn_dims& d) {
   return (size_t)(d.conv_width - 1) * channels(d) * dtype_size(d.conv_dtype);
 }
+
+// Bounds words of the checked build: each translation unit registers a
+// reader that copies its word out and clears it.
+using BoundsReader = bool (*)(BoundsWord*);
+void register_bounds_reader(const char* unit, BoundsReader r);
+#ifdef GDN_DEBUG_BOUNDS
+namespace {
+bool read_bounds_word(BoundsWord* w) {
+  if (cudaMemcpyFromSymbol(w, g_bounds_word, sizeof *w) != cudaSuccess) return false;
+  const BoundsWord zero = {};
+  return cudaMemcpyToSymbol(g_bounds_word, &zero, sizeof zero) == cudaSuccess;
+}
+const int g_bounds_registered = (register_bounds_reader(GDN_TU, read_bounds_word), 0);
+}  // namespace
+#endif
 
 // Host-side validation shared by every entry point.
 gdn_status check_dims(const gdn_dims* d);

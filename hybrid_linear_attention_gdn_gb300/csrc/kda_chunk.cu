@@ -151,28 +151,31 @@ __device__ __forceinline__ int ck_channel(int i, int hq, int h, int hk, int dv) 
 template <typename Tact, bool ASYNC>
 __device__ __forceinline__ void ck_stage(const KdaChunkArgs& a, Tact (*xr)[kCh], Tact (*gs)[kD], int64_t tok, int nt,
                                          int hq, int h) {
-  const Tact* qkv = reinterpret_cast<const Tact*>(a.qkv);
-  const Tact* ga = reinterpret_cast<const Tact*>(a.a);
+  const auto qkv = GDN_GV(reinterpret_cast<const Tact*>(a.qkv), a.total * a.C);
+  const auto ga = GDN_GV(reinterpret_cast<const Tact*>(a.a), a.total * a.hv * kD);
+  const auto xv = GDN_SV(&xr[0][0], kCk * kCh), gv = GDN_SV(&gs[0][0], kCk * kD);  // one staging buffer each
   const int nch = 2 * kD + a.dv;
   if constexpr (ASYNC) {
     constexpr int E = 16 / sizeof(Tact);
     const int per_row = nch / E;
     for (int p = threadIdx.x; p < nt * per_row; p += kCkThreads) {
       const int t = p / per_row, e = (p % per_row) * E;
-      cp_async16(&xr[t][e], qkv + (size_t)(tok + t) * a.C + ck_channel(e, hq, h, a.hk, a.dv));
+      const size_t src = (size_t)(tok + t) * a.C + ck_channel(e, hq, h, a.hk, a.dv);
+      if (xv.has(t * kCh + e, E) && qkv.has(src, E)) cp_async16(&xr[t][e], qkv.p + src);
     }
     for (int p = threadIdx.x; p < nt * (kD / E); p += kCkThreads) {
       const int t = p / (kD / E), e = (p % (kD / E)) * E;
-      cp_async16(&gs[t][e], ga + ((size_t)(tok + t) * a.hv + h) * kD + e);
+      const size_t src = ((size_t)(tok + t) * a.hv + h) * kD + e;
+      if (gv.has(t * kD + e, E) && ga.has(src, E)) cp_async16(&gs[t][e], ga.p + src);
     }
   } else {
     for (int p = threadIdx.x; p < nt * nch; p += kCkThreads) {
       const int t = p / nch, e = p % nch;
-      xr[t][e] = qkv[(size_t)(tok + t) * a.C + ck_channel(e, hq, h, a.hk, a.dv)];
+      xv[t * kCh + e] = qkv[(size_t)(tok + t) * a.C + ck_channel(e, hq, h, a.hk, a.dv)];
     }
     for (int p = threadIdx.x; p < nt * kD; p += kCkThreads) {
       const int t = p / kD, e = p % kD;
-      gs[t][e] = ga[((size_t)(tok + t) * a.hv + h) * kD + e];
+      gv[t * kD + e] = ga[((size_t)(tok + t) * a.hv + h) * kD + e];
     }
   }
 }
@@ -190,13 +193,21 @@ __global__ void __launch_bounds__(kCkThreads, 1) kda_chunk_kernel(const KdaChunk
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int h = blockIdx.x, n = blockIdx.y, hq = h / a.G;
   const int dv = a.dv, nch = 2 * kD + dv;
-  const int64_t t0 = a.cu_seqlens[n], t1 = a.cu_seqlens[n + 1], len = t1 - t0, p0 = a.start_pos[n];
+  // the caller's tensors (extents in elements)
+  const int n_seq = gridDim.y;
+  const auto cu_seqlens = GDN_GV(a.cu_seqlens, n_seq + 1);
+  const auto start_pos = GDN_GV(a.start_pos, n_seq);
+  const auto slot_ids = GDN_GV(a.slot_ids, n_seq);
+  const auto ckpt_ids = GDN_GV(a.ckpt_ids, (long long)n_seq * a.max_ckpt);
+  const auto ssm = GDN_GV(a.ssm, (long long)a.num_slots * a.hv * dv * kD);
+  const auto ck_ssm = GDN_GV(a.ck_ssm, (long long)a.ck_num_slots * a.hv * dv * kD);
+  const int64_t t0 = cu_seqlens[n], t1 = cu_seqlens[n + 1], len = t1 - t0, p0 = start_pos[n];
   if (t0 < 0 || len < 0 || t1 > a.total || p0 < 0) {
     if (h == 0 && tid == 0) report(a.err, GDN_DEV_ERR_SEQLENS);
     return;
   }
-  Tact* out = reinterpret_cast<Tact*>(a.out);
-  const int32_t slot = a.slot_ids[n];
+  const auto out = GDN_GV(reinterpret_cast<Tact*>(a.out), a.total * a.hv * dv);
+  const int32_t slot = slot_ids[n];
   const int cls = slot_class(slot, a.num_slots);
   if (cls) {
     if (cls == 2 && h == 0 && tid == 0) report(a.err, GDN_DEV_ERR_SLOT_OOB);
@@ -208,42 +219,46 @@ __global__ void __launch_bounds__(kCkThreads, 1) kda_chunk_kernel(const KdaChunk
 
   // windows aligned to absolute multiples of 16: the first ends at the next one
   const int first = len < kCk - (int)(p0 % kCk) ? (int)len : kCk - (int)(p0 % kCk);
-  const Tact* gb = reinterpret_cast<const Tact*>(a.b);
+  const auto gb = GDN_GV(reinterpret_cast<const Tact*>(a.b), a.total * a.hv);
   ck_stage<Tact, ASYNC>(a, S.xr[0], S.ga[0], t0, first, hq, h);
   if constexpr (ASYNC) cp_async_commit();
-  if (tid < first) S.bl[0][tid] = to_f32(gb[(size_t)(t0 + tid) * a.hv + h]);
+  if (tid < first) S.bl[0][GDN_S(tid, kCk)] = to_f32(gb[(size_t)(t0 + tid) * a.hv + h]);
 
   // this thread's state: rows rA = 16 warp + g and rB = rA + 8, in the
   // tensor core's C layout: sc[j] = (rA, 8j + 2tq), (rA, 8j + 2tq + 1),
   // (rB, 8j + 2tq), (rB, 8j + 2tq + 1)
   const int g = lane >> 2, tq = lane & 3;
-  const int rA = 16 * warp + g, rB = rA + 8;
+  const int rA = GDN_S(16 * warp + g, kMaxV - 8), rB = rA + 8;
   const bool vA = rA < dv, vB = rB < dv;
-  float* StA = a.ssm + (((size_t)slot * a.hv + h) * dv + rA) * kD;
-  float* StB = StA + 8 * kD;
+  const auto StA = ssm + (((size_t)slot * a.hv + h) * dv + (vA ? rA : 0)) * kD;
+  const auto StB = ssm + (((size_t)slot * a.hv + h) * dv + (vB ? rB : 0)) * kD;
   float sc[16][4];
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
-    const float2 x = vA ? *reinterpret_cast<const float2*>(StA + 8 * j + 2 * tq) : make_float2(0.f, 0.f);
-    const float2 y = vB ? *reinterpret_cast<const float2*>(StB + 8 * j + 2 * tq) : make_float2(0.f, 0.f);
+    const float2 x = vA ? vec_at<float2>(StA, 8 * j + 2 * tq) : make_float2(0.f, 0.f);
+    const float2 y = vB ? vec_at<float2>(StB, 8 * j + 2 * tq) : make_float2(0.f, 0.f);
     sc[j][0] = x.x;
     sc[j][1] = x.y;
     sc[j][2] = y.x;
     sc[j][3] = y.y;
   }
   // conv weights and history, right-aligned in kCkMaxW taps
-  const Tconv* hist = reinterpret_cast<const Tconv*>(a.conv) + (size_t)slot * (a.W - 1) * a.C;
+  const auto hist = GDN_GV(reinterpret_cast<const Tconv*>(a.conv), (long long)a.num_slots * (a.W - 1) * a.C) +
+                    (size_t)slot * (a.W - 1) * a.C;
+  const auto conv_w = GDN_GV(a.conv_w, (long long)a.C * a.W);
   const int lead = kCkMaxW - a.W;
-  for (int i = tid; i < nch; i += kCkThreads) {
+  for (int i0 = tid; i0 < nch; i0 += kCkThreads) {
+    const int i = GDN_S(i0, kCh);
     const int ch = ck_channel(i, hq, h, a.hk, dv);
 #pragma unroll
-    for (int j = 0; j < kCkMaxW; ++j) S.cw[j][i] = j >= lead ? a.conv_w[(size_t)ch * a.W + (j - lead)] : 0.f;
+    for (int j = 0; j < kCkMaxW; ++j) S.cw[j][i] = j >= lead ? conv_w[(size_t)ch * a.W + (j - lead)] : 0.f;
 #pragma unroll
     for (int j = 0; j < kCkMaxW - 1; ++j)
       S.xh[j][i] = j >= lead ? to_f32(hist[(size_t)(j - lead) * a.C + ch]) : 0.f;
   }
-  const float eA = expf(a.A_log[h]);
-  const float dtb = a.dt_bias[(size_t)h * kD + (tid & (kD - 1))];  // alpha channel of this thread
+  const float eA = expf(GDN_GV(a.A_log, a.hv)[h]);
+  // alpha channel of this thread
+  const float dtb = GDN_GV(a.dt_bias, (long long)a.hv * kD)[(size_t)h * kD + (tid & (kD - 1))];
   const int64_t blk0 = p0 / a.ckpt_block;
   int64_t next_bd = (blk0 + 1) * a.ckpt_block;
   int64_t ck_idx = 0;
@@ -261,13 +276,13 @@ __global__ void __launch_bounds__(kCkThreads, 1) kda_chunk_kernel(const KdaChunk
     if (ntn > 0) {
       ck_stage<Tact, ASYNC>(a, S.xr[nxt], S.ga[nxt], t0 + wn, ntn, hq, h);
       if constexpr (ASYNC) cp_async_commit();
-      if (tid < ntn) bnext = to_f32(gb[(size_t)(t0 + wn + tid) * a.hv + h]);
+      if (tid < ntn) bnext = to_f32(gb[(size_t)(t0 + wn + tid) * a.hv + h]);  // (tid < kCk)
     }
     // 1. conv1d + SiLU (tokens past the window's end: zero)
 #pragma unroll
     for (int ci = 0; ci < 2; ++ci) {
       const int i = tid + ci * kCkThreads;
-      if (i < nch) {
+      if (i < nch && GDN_S(i, kCh) == i) {
         float w[kCkMaxW], win[kCkMaxW - 1];
 #pragma unroll
         for (int j = 0; j < kCkMaxW; ++j) w[j] = S.cw[j][i];
@@ -425,6 +440,7 @@ __global__ void __launch_bounds__(kCkThreads, 1) kda_chunk_kernel(const KdaChunk
 #pragma unroll
       for (int nt2 = 0; nt2 < 2; ++nt2) {
         const int tok = 8 * nt2 + 2 * tq;
+        // rA, rB < kMaxV (checked where they are set): inside sy's kCh = 2 kD + kMaxV
         xk[nt2][0] = (vA ? S.sy[tok][2 * kD + rA] : 0.f) - xk[nt2][0];
         xk[nt2][1] = (vA ? S.sy[tok + 1][2 * kD + rA] : 0.f) - xk[nt2][1];
         xk[nt2][2] = (vB ? S.sy[tok][2 * kD + rB] : 0.f) - xk[nt2][2];
@@ -484,14 +500,15 @@ __global__ void __launch_bounds__(kCkThreads, 1) kda_chunk_kernel(const KdaChunk
       const int64_t idx = ck_idx++;
       next_bd += a.ckpt_block;
       if (idx < a.max_ckpt) {
-        const int32_t cid = a.ckpt_ids[(size_t)n * a.max_ckpt + idx];
+        const int32_t cid = ckpt_ids[(size_t)n * a.max_ckpt + idx];
         const int cc = slot_class(cid, a.ck_num_slots);
         if (cc == 0) {
-          float* dA = a.ck_ssm + (((size_t)cid * a.hv + h) * dv + rA) * kD;
+          const auto dA = ck_ssm + (((size_t)cid * a.hv + h) * dv + (vA ? rA : 0)) * kD;
+          const auto dB = ck_ssm + (((size_t)cid * a.hv + h) * dv + (vB ? rB : 0)) * kD;
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            if (vA) *reinterpret_cast<float2*>(dA + 8 * j + 2 * tq) = make_float2(sc[j][0], sc[j][1]);
-            if (vB) *reinterpret_cast<float2*>(dA + 8 * kD + 8 * j + 2 * tq) = make_float2(sc[j][2], sc[j][3]);
+            if (vA) vec_at<float2>(dA, 8 * j + 2 * tq) = make_float2(sc[j][0], sc[j][1]);
+            if (vB) vec_at<float2>(dB, 8 * j + 2 * tq) = make_float2(sc[j][2], sc[j][3]);
           }
         } else if (cc == 2 && tid == 0) {
           report(a.err, GDN_DEV_ERR_SLOT_OOB);
@@ -502,17 +519,17 @@ __global__ void __launch_bounds__(kCkThreads, 1) kda_chunk_kernel(const KdaChunk
     // 6. the window's outputs; the next window's beta logits and inputs land
     for (int e = tid; e < nt * dv; e += kCkThreads) {
       const int t = e / dv, i = e % dv;
-      out[((size_t)(t0 + w0 + t) * a.hv + h) * dv + i] = from_f32<Tact>(S.so[t][i]);
+      out[((size_t)(t0 + w0 + t) * a.hv + h) * dv + i] = from_f32<Tact>(S.so[GDN_S(t, kCk)][GDN_S(i, kMaxV)]);
     }
-    if (tid < ntn) S.bl[nxt][tid] = bnext;
+    if (tid < ntn) S.bl[nxt][GDN_S(tid, kCk)] = bnext;
     if constexpr (ASYNC) cp_async_wait_all();
     __syncthreads();
     w0 = wn;
   }
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
-    if (vA) *reinterpret_cast<float2*>(StA + 8 * j + 2 * tq) = make_float2(sc[j][0], sc[j][1]);
-    if (vB) *reinterpret_cast<float2*>(StB + 8 * j + 2 * tq) = make_float2(sc[j][2], sc[j][3]);
+    if (vA) vec_at<float2>(StA, 8 * j + 2 * tq) = make_float2(sc[j][0], sc[j][1]);
+    if (vB) vec_at<float2>(StB, 8 * j + 2 * tq) = make_float2(sc[j][2], sc[j][3]);
   }
 }
 

@@ -70,7 +70,44 @@ struct PrefillArgs {
   int32_t hk, hv, dk, dv, W, C, G;
 };
 
-__device__ __forceinline__ int seq_of_token(const int32_t* cu, int n_seq, int64_t t) {
+// The caller's tensors and the workspace of a prefill as checked views
+// (extents in elements).
+template <typename Tact, typename Tconv>
+struct PrefillViews {
+  View<float, 0> ssm, ck_ssm, ws_q, ws_k, ws_v, ws_g, ws_beta;
+  View<Tconv, 0> conv, ck_conv;
+  View<const float, 0> conv_w, A_log, dt_bias;
+  View<const int32_t, 0> slot_ids, cu_seqlens, ckpt_ids;
+  View<const int64_t, 0> start_pos;
+  View<const Tact, 0> qkv, a, b;
+  View<Tact, 0> out;
+  __device__ __forceinline__ explicit PrefillViews(const PrefillArgs& g) {
+    const long long slot_n = (long long)g.hv * g.dv * g.dk, hist_n = (long long)(g.W - 1) * g.C;
+    ssm = GDN_GV(g.ssm, g.num_slots * slot_n);
+    ck_ssm = GDN_GV(g.ck_ssm, g.ck_num_slots * slot_n);
+    conv = GDN_GV(reinterpret_cast<Tconv*>(g.conv), g.num_slots * hist_n);
+    ck_conv = GDN_GV(reinterpret_cast<Tconv*>(g.ck_conv), g.ck_num_slots * hist_n);
+    ws_q = GDN_GV(g.ws_q, g.total * g.hk * g.dk);
+    ws_k = GDN_GV(g.ws_k, g.total * g.hk * g.dk);
+    ws_v = GDN_GV(g.ws_v, g.total * g.hv * g.dv);
+    ws_g = GDN_GV(g.ws_g, g.total * g.hv);
+    ws_beta = GDN_GV(g.ws_beta, g.total * g.hv);
+    conv_w = GDN_GV(g.conv_w, (long long)g.C * g.W);
+    A_log = GDN_GV(g.A_log, g.hv);
+    dt_bias = GDN_GV(g.dt_bias, g.hv);
+    slot_ids = GDN_GV(g.slot_ids, g.n_seq);
+    cu_seqlens = GDN_GV(g.cu_seqlens, g.n_seq + 1);
+    ckpt_ids = GDN_GV(g.ckpt_ids, (long long)g.n_seq * g.max_ckpt);
+    start_pos = GDN_GV(g.start_pos, g.n_seq);
+    qkv = GDN_GV(reinterpret_cast<const Tact*>(g.qkv), g.total * g.C);
+    a = GDN_GV(reinterpret_cast<const Tact*>(g.a), g.total * g.hv);
+    b = GDN_GV(reinterpret_cast<const Tact*>(g.b), g.total * g.hv);
+    out = GDN_GV(reinterpret_cast<Tact*>(g.out), g.total * g.hv * g.dv);
+  }
+};
+
+template <typename V>
+__device__ __forceinline__ int seq_of_token(const V& cu, int n_seq, int64_t t) {
   int lo = 0, hi = n_seq - 1;  // last n with cu[n] <= t
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -86,27 +123,29 @@ template <int DK, typename Tact, typename Tconv>
 __global__ void __launch_bounds__(kThreads) features_kernel(const PrefillArgs a) {
   pdl_wait();
   pdl_trigger();
-  __shared__ float sq[DK], sk[DK];
+  __shared__ float sq_[DK], sk_[DK];
   __shared__ float sred[2][kWarps];
   __shared__ float sr[2];
+  const auto sq = GDN_SV(sq_, DK), sk = GDN_SV(sk_, DK);
+  const PrefillViews<Tact, Tconv> g(a);
   const int64_t t = blockIdx.x;
   const int hq = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n = seq_of_token(a.cu_seqlens, a.n_seq, t);
-  const int32_t slot = a.slot_ids[n];
+  const int n = seq_of_token(g.cu_seqlens, a.n_seq, t);
+  const int32_t slot = g.slot_ids[n];
   if (slot_class(slot, a.num_slots)) return;  // the chunk kernel zeroes its outputs
-  const int64_t t0 = a.cu_seqlens[n];
+  const int64_t t0 = g.cu_seqlens[n];
   const int64_t i = t - t0;  // index within the sequence
   if (i < 0) return;         // inconsistent cu_seqlens: reported by the chunk kernel
-  const Tact* qkv = reinterpret_cast<const Tact*>(a.qkv);
-  const Tconv* hist = reinterpret_cast<const Tconv*>(a.conv) + (size_t)slot * (a.W - 1) * a.C;
+  const auto qkv = g.qkv;
+  const auto hist = g.conv + (size_t)slot * (a.W - 1) * a.C;
   const int nch = 2 * DK + a.G * a.dv;
   for (int idx = tid; idx < nch; idx += kThreads) {
     int c;
     if (idx < DK) c = hq * DK + idx;
     else if (idx < 2 * DK) c = a.hk * DK + hq * DK + (idx - DK);
     else c = 2 * a.hk * DK + hq * a.G * a.dv + (idx - 2 * DK);
-    const float* w = a.conv_w + (size_t)c * a.W;
+    const auto w = g.conv_w + (size_t)c * a.W;
     float acc = 0.f;
 #pragma unroll
     for (int j = 0; j < kMaxW; ++j) {
@@ -120,7 +159,7 @@ __global__ void __launch_bounds__(kThreads) features_kernel(const PrefillArgs a)
     const float y = silu_f(acc);
     if (idx < DK) sq[idx] = y;
     else if (idx < 2 * DK) sk[idx - DK] = y;
-    else a.ws_v[(size_t)t * a.hv * a.dv + (size_t)hq * a.G * a.dv + (idx - 2 * DK)] = y;
+    else g.ws_v[(size_t)t * a.hv * a.dv + (size_t)hq * a.G * a.dv + (idx - 2 * DK)] = y;
   }
   __syncthreads();
   float pq = 0.f, pk = 0.f;
@@ -134,8 +173,9 @@ __global__ void __launch_bounds__(kThreads) features_kernel(const PrefillArgs a)
     pk += __shfl_xor_sync(0xffffffffu, pk, o);
   }
   if (lane == 0) {
-    sred[0][warp] = pq;
-    sred[1][warp] = pk;
+    const int w = GDN_S(warp, kWarps);
+    sred[0][w] = pq;
+    sred[1][w] = pk;
   }
   __syncthreads();
   if (tid == 0) {
@@ -148,18 +188,18 @@ __global__ void __launch_bounds__(kThreads) features_kernel(const PrefillArgs a)
     sr[1] = rsqrtf(y + kNormEps);
   }
   __syncthreads();
-  float* oq = a.ws_q + ((size_t)t * a.hk + hq) * DK;
-  float* ok = a.ws_k + ((size_t)t * a.hk + hq) * DK;
+  const auto oq = g.ws_q + ((size_t)t * a.hk + hq) * DK;
+  const auto ok = g.ws_k + ((size_t)t * a.hk + hq) * DK;
   for (int m = tid; m < DK; m += kThreads) {
     oq[m] = sq[m] * sr[0];
     ok[m] = sk[m] * sr[1];
   }
   if (tid < a.G) {
     const int h = hq * a.G + tid;
-    const float av = to_f32(reinterpret_cast<const Tact*>(a.a)[(size_t)t * a.hv + h]);
-    const float bv = to_f32(reinterpret_cast<const Tact*>(a.b)[(size_t)t * a.hv + h]);
-    a.ws_g[(size_t)t * a.hv + h] = floor_log_decay(-expf(a.A_log[h]) * softplus_f(av + a.dt_bias[h]));
-    a.ws_beta[(size_t)t * a.hv + h] = sigmoid_f(bv);
+    const float av = to_f32(g.a[(size_t)t * a.hv + h]);
+    const float bv = to_f32(g.b[(size_t)t * a.hv + h]);
+    g.ws_g[(size_t)t * a.hv + h] = floor_log_decay(-expf(g.A_log[h]) * softplus_f(av + g.dt_bias[h]));
+    g.ws_beta[(size_t)t * a.hv + h] = sigmoid_f(bv);
   }
 }
 
@@ -185,18 +225,20 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const PrefillArgs a)
   pdl_wait();
   pdl_trigger();
   using L = ChunkSmem<DK, DVT>;
-  extern __shared__ float sm[];
-  float* St = sm;
-  float* K = St + DVT * L::LK;
-  float* Q = K + kChunk * L::LK;
-  float* Wm = Q + kChunk * L::LK;
-  float* V = Wm + kChunk * L::LK;
-  float* U = V + kChunk * L::LV;
-  float* A = U + kChunk * L::LV;
-  float* Tm = A + kChunk * L::LC;
-  float* sb = Tm + kChunk * L::LC;
-  float* sbeta = sb + kChunk;
-  float* seb = sbeta + kChunk;
+  extern __shared__ float sm_[];
+  const auto sm = GDN_SV(sm_, L::floats);
+  const auto St = sm;
+  const auto K = St + DVT * L::LK;
+  const auto Q = K + kChunk * L::LK;
+  const auto Wm = Q + kChunk * L::LK;
+  const auto V = Wm + kChunk * L::LK;
+  const auto U = V + kChunk * L::LV;
+  const auto A = U + kChunk * L::LV;
+  const auto Tm = A + kChunk * L::LC;
+  const auto sb = Tm + kChunk * L::LC;
+  const auto sbeta = sb + kChunk;
+  const auto seb = sbeta + kChunk;
+  const PrefillViews<Tact, float> g(a);  // (the conv history is not touched here)
 
   const int tid = threadIdx.x;
   const int n_tiles = (a.dv + DVT - 1) / DVT;
@@ -205,10 +247,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const PrefillArgs a)
   const int j0 = (blockIdx.x % n_tiles) * DVT;
   const int ncols = min(DVT, a.dv - j0);
   const int hq = h / a.G;
-  const int64_t t0 = a.cu_seqlens[n], len = (int64_t)a.cu_seqlens[n + 1] - t0;
-  const int64_t p0 = a.start_pos[n];
-  const int32_t slot = a.slot_ids[n];
-  Tact* out = reinterpret_cast<Tact*>(a.out);
+  const int64_t t0 = g.cu_seqlens[n], len = (int64_t)g.cu_seqlens[n + 1] - t0;
+  const int64_t p0 = g.start_pos[n];
+  const int32_t slot = g.slot_ids[n];
+  const auto out = g.out;
   if (t0 < 0 || len < 0 || t0 + len > a.total || p0 < 0) {
     if (blockIdx.x == 0 && tid == 0) report(a.err, GDN_DEV_ERR_SEQLENS);
     return;
@@ -222,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const PrefillArgs a)
     }
     return;
   }
-  float* gS = a.ssm + (((size_t)slot * a.hv + h) * a.dv + j0) * DK;
+  const auto gS = g.ssm + (((size_t)slot * a.hv + h) * a.dv + j0) * DK;
   for (int e = tid; e < DVT * DK; e += kThreads) {
     const int j = e / DK, m = e % DK;
     St[j * L::LK + m] = j < ncols ? gS[(size_t)j * DK + m] : 0.f;
@@ -238,18 +280,18 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const PrefillArgs a)
     for (int e = tid; e < kChunk * DK; e += kThreads) {
       const int r = e / DK, m = e % DK;
       const bool ok = r < nr;
-      K[r * L::LK + m] = ok ? a.ws_k[((tb + r) * a.hk + hq) * DK + m] : 0.f;
-      Q[r * L::LK + m] = ok ? a.ws_q[((tb + r) * a.hk + hq) * DK + m] : 0.f;
+      K[r * L::LK + m] = ok ? g.ws_k[((tb + r) * a.hk + hq) * DK + m] : 0.f;
+      Q[r * L::LK + m] = ok ? g.ws_q[((tb + r) * a.hk + hq) * DK + m] : 0.f;
     }
     for (int e = tid; e < kChunk * DVT; e += kThreads) {
       const int r = e / DVT, j = e % DVT;
-      V[r * L::LV + j] = (r < nr && j < ncols) ? a.ws_v[((tb + r) * a.hv + h) * a.dv + j0 + j] : 0.f;
+      V[r * L::LV + j] = (r < nr && j < ncols) ? g.ws_v[((tb + r) * a.hv + h) * a.dv + j0 + j] : 0.f;
     }
     if (tid < 32) {  // inclusive prefix sum of g (warp 0, two 32-wide halves)
       float carry = 0.f;
       for (int half = 0; half < 2; ++half) {
         const int r = half * 32 + tid;
-        float v = r < nr ? a.ws_g[(tb + r) * a.hv + h] : 0.f;
+        float v = r < nr ? g.ws_g[(tb + r) * a.hv + h] : 0.f;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const float u = __shfl_up_sync(0xffffffffu, v, o);
@@ -262,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const PrefillArgs a)
     }
     if (tid >= 64 && tid < 128) {
       const int r = tid - 64;
-      sbeta[r] = r < nr ? a.ws_beta[(tb + r) * a.hv + h] : 0.f;
+      sbeta[r] = r < nr ? g.ws_beta[(tb + r) * a.hv + h] : 0.f;
     }
     __syncthreads();
     if (tid < kChunk) seb[tid] = expf(sb[tid]);
@@ -352,10 +394,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const PrefillArgs a)
     if (pos % a.ckpt_block == 0) {
       const int64_t idx = pos / a.ckpt_block - p0 / a.ckpt_block - 1;
       if (idx >= 0 && idx < a.max_ckpt) {
-        const int32_t cid = a.ckpt_ids[(size_t)n * a.max_ckpt + idx];
+        const int32_t cid = g.ckpt_ids[(size_t)n * a.max_ckpt + idx];
         if (slot_class(cid, a.ck_num_slots) == 0) {
           __syncthreads();
-          float* cS = a.ck_ssm + (((size_t)cid * a.hv + h) * a.dv + j0) * DK;
+          const auto cS = g.ck_ssm + (((size_t)cid * a.hv + h) * a.dv + j0) * DK;
           for (int e = tid; e < ncols * DK; e += kThreads)
             cS[(size_t)(e / DK) * DK + (e % DK)] = St[(e / DK) * L::LK + (e % DK)];
         }
@@ -377,13 +419,14 @@ __global__ void __launch_bounds__(kThreads) history_kernel(const PrefillArgs a) 
   const int n = blockIdx.y, grp = blockIdx.z;
   const int c = blockIdx.x * kThreads + threadIdx.x;
   if (c >= a.C) return;
-  const int32_t slot = a.slot_ids[n];
+  const PrefillViews<Tact, Tconv> g(a);
+  const int32_t slot = g.slot_ids[n];
   if (slot_class(slot, a.num_slots)) return;
-  const int64_t t0 = a.cu_seqlens[n], len = (int64_t)a.cu_seqlens[n + 1] - t0;
-  const int64_t p0 = a.start_pos[n], p1 = p0 + len;
+  const int64_t t0 = g.cu_seqlens[n], len = (int64_t)g.cu_seqlens[n + 1] - t0;
+  const int64_t p0 = g.start_pos[n], p1 = p0 + len;
   if (t0 < 0 || len < 0 || t0 + len > a.total || p0 < 0) return;
-  Tconv* hist = reinterpret_cast<Tconv*>(a.conv) + (size_t)slot * (a.W - 1) * a.C;
-  const Tact* qkv = reinterpret_cast<const Tact*>(a.qkv);
+  const auto hist = g.conv + (size_t)slot * (a.W - 1) * a.C;
+  const auto qkv = g.qkv;
   // Group 0 owns the working slot's history: it reads the old rows before
   // writing the new ones, and only its first checkpoint can reach back into
   // them (later checkpoints lie at least one 64-token block further on).
@@ -406,11 +449,11 @@ __global__ void __launch_bounds__(kThreads) history_kernel(const PrefillArgs a) 
     const int idx = grp * kCkGroup + k;
     const int64_t P = (p0 / blk + 1 + idx) * blk;
     if (idx >= a.max_ckpt || P > p1) break;
-    const int32_t cid = a.ckpt_ids[(size_t)n * a.max_ckpt + idx];
+    const int32_t cid = g.ckpt_ids[(size_t)n * a.max_ckpt + idx];
     const int cc = slot_class(cid, a.ck_num_slots);
     if (cc == 2 && c == 0) report(a.err, GDN_DEV_ERR_SLOT_OOB);
     if (cc) continue;
-    Tconv* ch = reinterpret_cast<Tconv*>(a.ck_conv) + (size_t)cid * (a.W - 1) * a.C;
+    const auto ch = g.ck_conv + (size_t)cid * (a.W - 1) * a.C;
     for (int j = 0; j < a.W - 1; ++j)
       ch[(size_t)j * a.C + c] = from_f32<Tconv>(raw(P - p0 - (a.W - 1) + j));
   }

@@ -84,9 +84,10 @@ struct TcArgs {
 };
 
 __device__ __forceinline__ bool seq_ok(const TcArgs& a, int n, int64_t& t0, int64_t& len, int64_t& p0) {
-  t0 = a.cu_seqlens[n];
-  len = (int64_t)a.cu_seqlens[n + 1] - t0;
-  p0 = a.start_pos[n];
+  const auto cu = GDN_GV(a.cu_seqlens, a.n_seq + 1);
+  t0 = cu[n];
+  len = (int64_t)cu[n + 1] - t0;
+  p0 = GDN_GV(a.start_pos, a.n_seq)[n];
   return !(t0 < 0 || len < 0 || t0 + len > a.total || p0 < 0);
 }
 
@@ -129,15 +130,17 @@ __global__ void __launch_bounds__(1024) plan_kernel(const TcArgs a) {
   }
   __syncthreads();
   int run = (warp ? warp_sums[warp - 1] : 0) + incl - sum;  // exclusive prefix of this thread
+  const auto chunk_base = GDN_GV(a.chunk_base, a.n_seq + 1);
   for (int n = lo; n < hi; ++n) {
-    a.chunk_base[n] = run;
+    chunk_base[n] = run;
     int64_t t0, len, p0;
     if (seq_ok(a, n, t0, len, p0)) run += n_chunks_of(p0, len);
   }
-  if (tid == 1023) a.chunk_base[a.n_seq] = warp_sums[31];
+  if (tid == 1023) chunk_base[a.n_seq] = warp_sums[31];
 }
 
-__device__ __forceinline__ int seq_of_chunk(const int32_t* base, int n_seq, int gc) {
+template <typename V>
+__device__ __forceinline__ int seq_of_chunk(const V& base, int n_seq, int gc) {
   int lo = 0, hi = n_seq - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -161,8 +164,9 @@ __device__ __forceinline__ int seq_of_chunk(const int32_t* base, int n_seq, int 
 // swizzled operand image.
 // ---------------------------------------------------------------------------
 constexpr int kTileRows = kC + 3;
-__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8]) {
-  const uint4 u = *reinterpret_cast<const uint4*>(p);
+template <typename V>  // a view of bf16 elements, 8 from i on
+__device__ __forceinline__ void load8(const V& xs, size_t i, const __nv_bfloat16*, float (&v)[8]) {
+  const uint4 u = vec_at<const uint4>(xs, i);
   const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -171,8 +175,9 @@ __device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8]) {
     v[2 * i + 1] = f.y;
   }
 }
-__device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
-  const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+template <typename V>  // a view of fp32 elements, 8 from i on
+__device__ __forceinline__ void load8(const V& xs, size_t i, const float*, float (&v)[8]) {
+  const float4 a = vec_at<const float4>(xs, i), b = vec_at<const float4>(xs, i + 4);
   v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
   v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
@@ -181,16 +186,17 @@ __device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
 // r .. r+3 = positions P+r-3 .. P+r); zero outside the sequence.  The fast
 // exponential and division are far finer than the bf16 operands they feed.
 // emit(r, y) receives each row's 8 results.
-template <bool kFull, typename Tact, class Emit>
-__device__ __forceinline__ void conv_walk8(const Tact* xs, int nch, int r0, int lc, const float (&w)[8][4],
+template <bool kFull, typename Tact, class Emit, typename V>
+__device__ __forceinline__ void conv_walk8(const V& xs, int nch, int r0, int lc, const float (&w)[8][4],
                                            int64_t P, int64_t p0, int64_t p1, Emit emit) {
   float x[4][8];
+  const Tact* tag = nullptr;  // selects the element type's load8
 #pragma unroll
-  for (int j = 0; j < 3; ++j) load8(xs + (size_t)(r0 + j) * nch + lc, x[j]);
+  for (int j = 0; j < 3; ++j) load8(xs, (size_t)(r0 + j) * nch + lc, tag, x[j]);
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     const int r = r0 + k;
-    load8(xs + (size_t)(r + 3) * nch + lc, x[(k + 3) & 3]);
+    load8(xs, (size_t)(r + 3) * nch + lc, tag, x[(k + 3) & 3]);
     const bool valid = kFull || (P + r >= p0 && P + r < p1);  // kFull: the chunk is inside
     float y[8];
 #pragma unroll
@@ -212,23 +218,27 @@ __global__ void __launch_bounds__(kTh, 3) tc_features_kernel(const TcArgs a, con
   extern __shared__ __align__(16) unsigned char fsm_raw[];
   const int gc = blockIdx.x, hq = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (gc >= a.chunk_base[a.n_seq]) return;
-  const int n = seq_of_chunk(a.chunk_base, a.n_seq, gc);
+  const auto chunk_base = GDN_GV(a.chunk_base, a.n_seq + 1);
+  if (gc >= chunk_base[a.n_seq]) return;
+  const int n = seq_of_chunk(chunk_base, a.n_seq, gc);
   int64_t t0, len, p0;
   if (!seq_ok(a, n, t0, len, p0)) return;
-  const int32_t slot = a.slot_ids[n];
+  const int32_t slot = GDN_GV(a.slot_ids, a.n_seq)[n];
   if (slot_class(slot, a.num_slots)) return;
-  const int64_t P = (p0 / kC + (gc - a.chunk_base[n])) * kC;  // absolute position of row 0
+  const int64_t P = (p0 / kC + (gc - chunk_base[n])) * kC;  // absolute position of row 0
   const int64_t p1 = p0 + len;
   const int nparts = 2 + a.G;
   // part p: [67 rows][128 channels]; 128-byte aligned for the tensor copies
   Tact* xs = reinterpret_cast<Tact*>(fsm_raw + ((128u - (smem_addr(fsm_raw) & 127u)) & 127u));
+  const auto xsv = GDN_SV(xs, (size_t)nparts * kTileRows * kD);
   uint64_t* bar = reinterpret_cast<uint64_t*>(xs + (size_t)nparts * kTileRows * kD);
-  auto part = [&](int q) { return xs + (size_t)q * kTileRows * kD; };
+  auto part = [&](int q) { return xsv + (size_t)q * kTileRows * kD; };
   auto part_chan = [&](int q) -> int {  // first global channel of part q
     return q < 2 ? (q * a.hk + hq) * kD : (2 * a.hk + hq * a.G + (q - 2)) * kD;
   };
-  const Tconv* hist = reinterpret_cast<const Tconv*>(a.conv) + (size_t)slot * 3 * a.C;
+  const auto hist = GDN_GV(reinterpret_cast<const Tconv*>(a.conv), (long long)a.num_slots * 3 * a.C) +
+                    (size_t)slot * 3 * a.C;
+  const auto conv_w = GDN_GV(a.conv_w, (long long)a.C * 4);
   if (tid == 0) {
     mbar_init(bar, 1);
     fence_mbar_init();
@@ -237,7 +247,9 @@ __global__ void __launch_bounds__(kTh, 3) tc_features_kernel(const TcArgs a, con
   if (tid == 0) {
     mbar_arrive_expect_tx(bar, (uint32_t)(nparts * kTileRows * kD * sizeof(Tact)));
     const int32_t row0 = (int32_t)(t0 + (P - 3 - p0));  // packed row of tile row 0 (may be < 0)
-    for (int q = 0; q < nparts; ++q) tma_load_2d(part(q), &qmap, part_chan(q), row0, bar);
+    for (int q = 0; q < nparts; ++q)  // a box of 128 channels x 67 rows
+      if (xsv.has((size_t)q * kTileRows * kD, kTileRows * kD) && GDN_SPAN_G(part_chan(q), kD, a.C))
+        tma_load_2d(xs + (size_t)q * kTileRows * kD, &qmap, part_chan(q), row0, bar);
   }
   // this lane's q/k conv weights (lane l < 16: q channels 8l .. 8l+7, lane
   // 16 + l the same k channels) and the gates, while the tile lands
@@ -246,7 +258,7 @@ __global__ void __launch_bounds__(kTh, 3) tc_features_kernel(const TcArgs a, con
   float w[8][4];
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
-    const float4 w4 = *reinterpret_cast<const float4*>(a.conv_w + (size_t)(part_chan(isq ? 0 : 1) + lc + c) * 4);
+    const float4 w4 = vec_at<const float4>(conv_w, (size_t)(part_chan(isq ? 0 : 1) + lc + c) * 4);
     w[c][0] = w4.x; w[c][1] = w4.y; w[c][2] = w4.z; w[c][3] = w4.w;
   }
   // gates (rows outside the sequence: g = beta = 0)
@@ -257,12 +269,12 @@ __global__ void __launch_bounds__(kTh, 3) tc_features_kernel(const TcArgs a, con
     float gv = 0.f, bv = 0.f;
     if (pos >= p0 && pos < p1) {
       const size_t tok = (size_t)(t0 + pos - p0);
-      const float av = to_f32(reinterpret_cast<const Tact*>(a.a)[tok * a.hv + h]);
-      const float bb = to_f32(reinterpret_cast<const Tact*>(a.b)[tok * a.hv + h]);
-      gv = floor_log_decay(-expf(a.A_log[h]) * softplus_f(av + a.dt_bias[h]));
+      const float av = to_f32(GDN_GV(reinterpret_cast<const Tact*>(a.a), a.total * a.hv)[tok * a.hv + h]);
+      const float bb = to_f32(GDN_GV(reinterpret_cast<const Tact*>(a.b), a.total * a.hv)[tok * a.hv + h]);
+      gv = floor_log_decay(-expf(GDN_GV(a.A_log, a.hv)[h]) * softplus_f(av + GDN_GV(a.dt_bias, a.hv)[h]));
       bv = sigmoid_f(bb);
     }
-    float* gt = a.ws_gate + ((size_t)gc * a.hv + h) * (2 * kC);
+    const auto gt = GDN_GV(a.ws_gate, (long long)a.n_chunks_max * a.hv * 2 * kC) + ((size_t)gc * a.hv + h) * (2 * kC);
     gt[r] = gv;
     gt[kC + r] = bv;
   }
@@ -285,8 +297,8 @@ __global__ void __launch_bounds__(kTh, 3) tc_features_kernel(const TcArgs a, con
       for (int e = tid; e < nh * per_row; e += kTh) {
         const int64_t pos = lo + e / per_row;
         const int q = (e % per_row) / (kD / 8), c = 8 * (e % (kD / 8));
-        const Tconv* src = hist + (size_t)(3 - (p0 - pos)) * a.C + part_chan(q) + c;
-        Tact* dst = part(q) + (size_t)(pos - (P - 3)) * kD + c;
+        const auto src = hist + ((size_t)(3 - (p0 - pos)) * a.C + part_chan(q) + c);
+        const auto dst = part(q) + (size_t)(pos - (P - 3)) * kD + c;
 #pragma unroll
         for (int k = 0; k < 8; ++k) dst[k] = from_f32<Tact>(to_f32(src[k]));
       }
@@ -297,9 +309,9 @@ __global__ void __launch_bounds__(kTh, 3) tc_features_kernel(const TcArgs a, con
 
   // q and k: warp w walks rows 8w .. 8w+7
   {
-    const Tact* xp = part(isq ? 0 : 1);
+    const auto xp = part(isq ? 0 : 1);
     const float qscale = isq ? rsqrtf((float)kD) : 1.f;
-    uint8_t* kq = a.ws_kq + ((size_t)gc * a.hk + hq) * kKQBytes;
+    const auto kq = GDN_GV(a.ws_kq, (long long)a.n_chunks_max * a.hk * kKQBytes) + ((size_t)gc * a.hk + hq) * kKQBytes;
     auto emit = [&](int r, float (&y)[8]) {
       float ss = 0.f;
 #pragma unroll
@@ -310,12 +322,12 @@ __global__ void __launch_bounds__(kTh, 3) tc_features_kernel(const TcArgs a, con
 #pragma unroll
       for (int c = 0; c < 8; ++c) y[c] *= sc;
       const int R = isq ? kC + r : r;  // image rows: k^ 0..63, q^ 64..127
-      *reinterpret_cast<uint4*>(kq + umma::sw128_off(R, lc, 128 * 128)) = umma::pack8_bf16(y);
+      vec_at<uint4>(kq, umma::sw128_off(R, lc, 128 * 128)) = umma::pack8_bf16(y);
     };
     if (full)
-      conv_walk8<true>(xp, kD, 8 * warp, lc, w, P, p0, p1, emit);
+      conv_walk8<true, Tact>(xp, kD, 8 * warp, lc, w, P, p0, p1, emit);
     else
-      conv_walk8<false>(xp, kD, 8 * warp, lc, w, P, p0, p1, emit);
+      conv_walk8<false, Tact>(xp, kD, 8 * warp, lc, w, P, p0, p1, emit);
   }
   // v: (8-channel group, 8-row block) items, G*16 groups per row
   {
@@ -326,17 +338,18 @@ __global__ void __launch_bounds__(kTh, 3) tc_features_kernel(const TcArgs a, con
       float wv[8][4];
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        const float4 w4 = *reinterpret_cast<const float4*>(a.conv_w + (size_t)(part_chan(2 + gi) + d + c) * 4);
+        const float4 w4 = vec_at<const float4>(conv_w, (size_t)(part_chan(2 + gi) + d + c) * 4);
         wv[c][0] = w4.x; wv[c][1] = w4.y; wv[c][2] = w4.z; wv[c][3] = w4.w;
       }
-      uint8_t* vimg = a.ws_v + ((size_t)gc * a.hv + hq * a.G + gi) * kVBytes;
+      const auto vimg = GDN_GV(a.ws_v, (long long)a.n_chunks_max * a.hv * kVBytes) +
+                        ((size_t)gc * a.hv + hq * a.G + gi) * kVBytes;
       auto emit = [&](int r, float (&y)[8]) {
-        *reinterpret_cast<uint4*>(vimg + umma::sw128_off(r, d, 64 * 128)) = umma::pack8_bf16(y);
+        vec_at<uint4>(vimg, umma::sw128_off(r, d, 64 * 128)) = umma::pack8_bf16(y);
       };
       if (full)
-        conv_walk8<true>(part(2 + gi), kD, 8 * rb, d, wv, P, p0, p1, emit);
+        conv_walk8<true, Tact>(part(2 + gi), kD, 8 * rb, d, wv, P, p0, p1, emit);
       else
-        conv_walk8<false>(part(2 + gi), kD, 8 * rb, d, wv, P, p0, p1, emit);
+        conv_walk8<false, Tact>(part(2 + gi), kD, 8 * rb, d, wv, P, p0, p1, emit);
     }
   }
 }
@@ -438,8 +451,9 @@ struct TOut {
 
 // T entries (r, c), (r, c + 1) (c even) as a bf16 pair; bc is beta of the
 // two columns (loaded once per lane by the caller)
-__device__ __forceinline__ void put_t_pair(const TOut& o, int r, int c, float x0, float x1, const float2& bc) {
-  *reinterpret_cast<__nv_bfloat162*>(o.tm + t_off(r, c)) = __floats2bfloat162_rn(x0 * bc.x, x1 * bc.y);
+__device__ __forceinline__ void put_t_pair(const TOut& o, int r, int c, float x0, float x1, const float2& bc,
+                                           int line = __builtin_LINE()) {
+  tile_at<__nv_bfloat162>(o.tm, 64 * 128, t_off(r, c), line) = __floats2bfloat162_rn(x0 * bc.x, x1 * bc.y);
 }
 
 // X = (I + A)^-1 for the 64 x 64 strictly lower A (fp32), written out as the
@@ -452,9 +466,12 @@ __device__ __forceinline__ void put_t_pair(const TOut& o, int r, int c, float x0
 // Entries above the diagonal of X are never stored; reads mask them to zero.
 // Y: 2048 floats of scratch.  256 threads; the caller synchronises before (A
 // complete) and after.
-__device__ __forceinline__ void solve_T(const float* A, float* X, float* Y, const TOut& to) {
+__device__ __forceinline__ void solve_T(const float* A_, float* X_, float* Y_, const TOut& to) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
+  const auto A = GDN_SV(A_, 64 * kAXStride);
+  const auto X = GDN_SV(X_, 64 * kAXStride);
+  const auto Y = GDN_SV(Y_, 2048);
   // 8 x 8 diagonal blocks: warp w, lane l < 4 = columns 2l and 2l+1 of block
   // w (two independent substitutions), written as fp32 pairs to X and bf16
   // pairs to T
@@ -481,7 +498,7 @@ __device__ __forceinline__ void solve_T(const float* A, float* X, float* Y, cons
 #pragma unroll
     for (int r = 0; r < 8; ++r)
       if (r >= c0) {
-        *reinterpret_cast<float2*>(X + ix(o + r, o + c0)) = make_float2(x0[r], x1[r]);
+        vec_at<float2>(X, ix(o + r, o + c0)) = make_float2(x0[r], x1[r]);
         put_t_pair(to, o + r, o + c0, x0[r], x1[r], bc);
       }
   }
@@ -489,7 +506,7 @@ __device__ __forceinline__ void solve_T(const float* A, float* X, float* Y, cons
   // 8 -> 16: warps 0..3, block pair p (rows/cols 16p ..); M padded to 16
   if (warp < 4) {
     const int o = 16 * warp;
-    float* Ys = Y + warp * 128;
+    const auto Ys = Y + warp * 128;
     uint32_t fa[1][4], fb[1][2], fx[1][4], fy[1][2];
     frag_a(fa[0], 0, [&](int r, int k) { return r < 8 ? A[ix(o + 8 + r, o + k)] : 0.f; });
     frag_b(fb[0], 0, [&](int k, int c) { return k >= c ? X[ix(o + k, o + c)] : 0.f; });
@@ -510,7 +527,7 @@ __device__ __forceinline__ void solve_T(const float* A, float* X, float* Y, cons
   // 16 -> 32: warps 0..3 = (pair q, column tile j)
   if (warp < 4) {
     const int o = 32 * (warp >> 1), j = warp & 1;
-    float* Ys = Y + 512 + warp * 128;
+    const auto Ys = Y + (512 + warp * 128);
     uint32_t fa[2][4], fb[2][2], fx[2][4], fy[2][2];
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
@@ -543,7 +560,7 @@ __device__ __forceinline__ void solve_T(const float* A, float* X, float* Y, cons
   // barrier.  Rows of X_a above 8j of column tile j are zero (k-steps skipped).
   {
     const int j = warp & 3, mh = warp >> 2;
-    float* Ys = Y + 1024 + j * 256;  // 32 x 8
+    const auto Ys = Y + (1024 + j * 256);  // 32 x 8
     uint32_t fa[4][4], fb[4][2], fx[4][4], fy[4][2];
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
@@ -590,8 +607,9 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     if (h == 0 && tid == 0) report(a.err, GDN_DEV_ERR_SEQLENS);
     return;
   }
-  const int32_t slot = a.slot_ids[n];
-  Tact* out = reinterpret_cast<Tact*>(a.out);
+  const int32_t slot = GDN_GV(a.slot_ids, a.n_seq)[n];
+  const auto out = GDN_GV(reinterpret_cast<Tact*>(a.out), a.total * a.hv * kD);
+  const auto ckpt_ids = GDN_GV(a.ckpt_ids, (long long)a.n_seq * a.max_ckpt);
   const int cls = slot_class(slot, a.num_slots);
   if (cls) {
     if (cls == 2 && h == 0 && tid == 0) report(a.err, GDN_DEV_ERR_SLOT_OOB);
@@ -600,7 +618,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     return;
   }
   const int nch = n_chunks_of(p0, len);
-  const int gc0 = a.chunk_base[n];
+  const int gc0 = GDN_GV(a.chunk_base, a.n_seq + 1)[n];
   const int64_t p1 = p0 + len;
 
   if (tid == 0) {
@@ -626,6 +644,12 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   constexpr uint32_t ID_64_MK = umma::idesc_bf16(128, 64, true, false);
   constexpr uint32_t ID_128_KM = umma::idesc_bf16(128, 128, false, true);
   constexpr uint32_t ID_128_KK = umma::idesc_bf16(128, 128, false, false);
+  // operand extents of the products below: [K;Q] and S^T 2 blocks of 128 rows
+  // x 128 bytes, V 2 atoms of 64 rows, the 64-token tiles 128 or 64 rows
+  static_assert(sizeof(ChainSmem::kq[0]) == kKQBytes && sizeof(ChainSmem::v[0]) == kVBytes, "operand tiles");
+  static_assert(sizeof(ChainSmem::st) == 2 * 16384 && sizeof(ChainSmem::wt) == 16384, "operand tiles");
+  static_assert(sizeof(ChainSmem::tm) == 8192 && sizeof(ChainSmem::qk) == 8192, "operand tiles");
+  static_assert(TM_D2 + 128 <= TM_COLS && TM_O2 + 64 <= TM_D2, "TMEM regions");
   // bf16 outputs: the output tiles and checkpoints leave by TMA tensor stores
   // (fp32 outputs stage 32 KB, which overlaps the checkpoint boxes)
   constexpr bool kTmaStores = sizeof(Tact) == 2;
@@ -646,7 +670,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     if (rem != 0) return -1;
     const int idx = (kpc_pow2 ? (q >> kpc_sh) : q / kpc) - 1;
     if (idx >= a.max_ckpt) return -1;
-    const int32_t id = a.ckpt_ids[(size_t)n * a.max_ckpt + idx];
+    const int32_t id = ckpt_ids[(size_t)n * a.max_ckpt + idx];
     return slot_class(id, a.ck_num_slots) == 0 ? id : -1;
   };
   // the four tensor stores of a checkpoint staged by the compute warps (state
@@ -654,6 +678,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   // two bulk groups, the Delta tiles' first
   auto store_ckpt = [&](int32_t cid, int buf) {
     const int32_t y = (int32_t)(((int64_t)cid * a.hv + h) * kD);
+    if (!GDN_SPAN_G(y, kD, (long long)a.ck_num_slots * a.hv * kD)) return;
     tma_store_2d(&cmap, S.dt, 0, y);
     tma_store_2d(&cmap, S.dtt, 32, y);
     bulk_commit();
@@ -673,9 +698,14 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       auto issue_load = [&](int c) {
         const int gc = gc0 + c, buf = c & 1;
         mbar_arrive_expect_tx(&S.ld_full[buf], kKQBytes + kVBytes + kGateBytes);
-        bulk_g2s(S.kq[buf], a.ws_kq + ((size_t)gc * a.hk + hq) * kKQBytes, kKQBytes, &S.ld_full[buf]);
-        bulk_g2s(S.v[buf], a.ws_v + ((size_t)gc * a.hv + h) * kVBytes, kVBytes, &S.ld_full[buf]);
-        bulk_g2s(S.gates[buf], a.ws_gate + ((size_t)gc * a.hv + h) * (2 * kC), kGateBytes, &S.ld_full[buf]);
+        const size_t okq = ((size_t)gc * a.hk + hq) * kKQBytes, ov = ((size_t)gc * a.hv + h) * kVBytes,
+                     og = ((size_t)gc * a.hv + h) * (2 * kC);
+        if (GDN_SPAN_G(okq, kKQBytes, (long long)a.n_chunks_max * a.hk * kKQBytes))
+          bulk_g2s(S.kq[buf], a.ws_kq + okq, kKQBytes, &S.ld_full[buf]);
+        if (GDN_SPAN_G(ov, kVBytes, (long long)a.n_chunks_max * a.hv * kVBytes))
+          bulk_g2s(S.v[buf], a.ws_v + ov, kVBytes, &S.ld_full[buf]);
+        if (GDN_SPAN_G(og, 2 * kC, (long long)a.n_chunks_max * a.hv * 2 * kC))
+          bulk_g2s(S.gates[buf], a.ws_gate + og, kGateBytes, &S.ld_full[buf]);
       };
       auto issue_kq = [&](int c) {
         const uint64_t dkq = umma::desc(smem_addr(S.kq[c & 1]), 16, 1024);
@@ -750,17 +780,18 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     __syncwarp();
   } else {
     // state rows: S^T[lrow][64*half .. +64) in registers, bf16 copy as operand
-    float* gS = a.ssm + (((size_t)slot * a.hv + h) * kD + lrow) * kD + 64 * half;
+    const auto gS = GDN_GV(a.ssm, (long long)a.num_slots * a.hv * kD * kD) +
+                    ((((size_t)slot * a.hv + h) * kD + lrow) * kD + 64 * half);
     float sreg[64];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const float4 v = *reinterpret_cast<const float4*>(gS + 4 * i);
+      const float4 v = vec_at<const float4>(gS, 4 * i);
       sreg[4 * i] = v.x;
       sreg[4 * i + 1] = v.y;
       sreg[4 * i + 2] = v.z;
       sreg[4 * i + 3] = v.w;
     }
-    umma::store_row64(S.st + half * (128 * 128), lrow, sreg);
+    umma::store_row64(S.st + half * (128 * 128), 128 * 128, lrow, sreg);
     // T is lower triangular: its upper triangle is written only here
     for (int e = tid; e < 64 * 128 / 16; e += kTh) reinterpret_cast<uint4*>(S.tm)[e] = make_uint4(0u, 0u, 0u, 0u);
 
@@ -774,6 +805,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     bool bad = false;  // this thread saw a bounded wait expire
     float* Af = S.ax[0];
     float* Xf = S.ax[1];
+    const auto Av = GDN_SV(Af, 64 * kAXStride);
     float* Yf = reinterpret_cast<float*>(S.wt);
 
     // one warp, gates of chunk c resident: cumulative log-decay b, e^b, e^{b_last - b}
@@ -846,8 +878,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
           }
 #pragma unroll
           for (int q = 0; q < 8; ++q)
-            *reinterpret_cast<float4*>(Af + ix(r, c0 + 4 * q)) =
-                make_float4(av[4 * q], av[4 * q + 1], av[4 * q + 2], av[4 * q + 3]);
+            vec_at<float4>(Av, ix(r, c0 + 4 * q)) = make_float4(av[4 * q], av[4 * q + 1], av[4 * q + 2], av[4 * q + 3]);
         } else {
           const int t = lrow - kC;
           const float bt = b[t];
@@ -860,7 +891,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
             const int cch = 4 * half + ch;
-            *reinterpret_cast<uint4*>(S.qk + (t >> 3) * 1024 + (t & 7) * 128 + ((cch ^ (t & 7)) << 4)) =
+            tile_at<uint4>(S.qk, sizeof(S.qk), (t >> 3) * 1024 + (t & 7) * 128 + ((cch ^ (t & 7)) << 4)) =
                 umma::pack8_bf16(m + 8 * ch);
           }
         }
@@ -902,7 +933,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
           const int cch = 4 * half + ch;
-          *reinterpret_cast<uint4*>(S.wt + (lrow >> 3) * 1024 + (lrow & 7) * 128 + ((cch ^ (lrow & 7)) << 4)) =
+          tile_at<uint4>(S.wt, sizeof(S.wt), (lrow >> 3) * 1024 + (lrow & 7) * 128 + ((cch ^ (lrow & 7)) << 4)) =
               umma::pack8_bf16(v + 8 * ch);
         }
       }
@@ -932,8 +963,8 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         for (int ch = 0; ch < 4; ++ch) {
           const int cch = 4 * half + ch;
           const uint32_t off = (lrow >> 3) * 1024 + (lrow & 7) * 128 + ((cch ^ (lrow & 7)) << 4);
-          *reinterpret_cast<uint4*>(S.dt + off) = umma::pack8_bf16(d + 8 * ch);
-          *reinterpret_cast<uint4*>(S.dtt + off) = umma::pack8_bf16(dd + 8 * ch);
+          tile_at<uint4>(S.dt, sizeof(S.dt), off) = umma::pack8_bf16(d + 8 * ch);
+          tile_at<uint4>(S.dtt, sizeof(S.dtt), off) = umma::pack8_bf16(dd + 8 * ch);
         }
       }
       umma::fence_proxy_async();
@@ -977,7 +1008,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         for (int i = 0; i < 32; ++i) sreg[32 + i] = fmaf(dec, sreg[32 + i], d2[i]);
         umma::tmem_ld32(tlane + TM_O1 + 32 * half, o1);
       }
-      umma::store_row64(S.st + half * (128 * 128), lrow, sreg);
+      umma::store_row64(S.st + half * (128 * 128), 128 * 128, lrow, sreg);
       // checkpoint slot of a block boundary at this chunk's end (-1: none)
       const int32_t cid = ckpt_slot(c);
       prev_ck = cid >= 0;
@@ -988,20 +1019,22 @@ __global__ void __launch_bounds__(kChainThreads, 1)
           // [K;Q] tile, both dead now; the issue warp writes them out with
           // four tensor stores after st_bar (instead of 512-byte-strided row
           // stores) and holds both tiles until the stores have read them
+          // (the dt and dtt tiles are adjacent: two 16 KB boxes from dt)
+          static_assert(offsetof(ChainSmem, dtt) == offsetof(ChainSmem, dt) + 16384, "adjacent Delta tiles");
           uint8_t* box = half ? S.kq[buf] : S.dt;
 #pragma unroll
           for (int bl = 0; bl < 2; ++bl)
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-              *reinterpret_cast<float4*>(box + bl * 16384 + lrow * 128 + ((j ^ (lrow & 7)) << 4)) =
+              tile_at<float4>(box, 2 * 16384, bl * 16384 + lrow * 128 + ((j ^ (lrow & 7)) << 4)) =
                   make_float4(sreg[32 * bl + 4 * j], sreg[32 * bl + 4 * j + 1], sreg[32 * bl + 4 * j + 2],
                               sreg[32 * bl + 4 * j + 3]);
         } else {
-          float* cS = a.ck_ssm + (((size_t)cid * a.hv + h) * kD + lrow) * kD + 64 * half;
+          const auto cS = GDN_GV(a.ck_ssm, (long long)a.ck_num_slots * a.hv * kD * kD) +
+                          ((((size_t)cid * a.hv + h) * kD + lrow) * kD + 64 * half);
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            *reinterpret_cast<float4*>(cS + 4 * i) =
-                make_float4(sreg[4 * i], sreg[4 * i + 1], sreg[4 * i + 2], sreg[4 * i + 3]);
+            vec_at<float4>(cS, 4 * i) = make_float4(sreg[4 * i], sreg[4 * i + 1], sreg[4 * i + 2], sreg[4 * i + 3]);
         }
       }
       // state image (and checkpoint) written, O1 read: the issue warp may
@@ -1022,8 +1055,9 @@ __global__ void __launch_bounds__(kChainThreads, 1)
           ebr[4 * i + 2] = e4.z;
           ebr[4 * i + 3] = e4.w;
         }
-        // stage O as [token][dv] in the (now free) scratch tile
-        Tact* ot = reinterpret_cast<Tact*>(S.wt);
+        // stage O as [token][dv] in the (now free) scratch tile; fp32 outputs
+        // run on into the Delta tiles after it
+        const auto ot = GDN_SV(reinterpret_cast<Tact*>(S.wt), (offsetof(ChainSmem, tm) - offsetof(ChainSmem, wt)) / sizeof(Tact));
 #pragma unroll
         for (int i = 0; i < 32; ++i) ot[(32 * half + i) * kD + lrow] = from_f32<Tact>(fmaf(o1[i], ebr[i], o2[i]));
       }
@@ -1034,7 +1068,8 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       // 64 x 128 output tile
       const bool full = P >= p0 && P + kC <= p1;
       if (kTmaStores && full && tid == 0) {
-        tma_store_2d(&omap, S.wt, h * kD, (int32_t)(t0 + (P - p0)));
+        if (GDN_SPAN_G(t0 + (P - p0), kC, a.total) && GDN_SPAN_G(h * kD, kD, (long long)a.hv * kD))
+          tma_store_2d(&omap, S.wt, h * kD, (int32_t)(t0 + (P - p0)));
         bulk_commit();
       }
       // otherwise output rows of the chunk's tokens: 16-byte stores of whole
@@ -1042,13 +1077,13 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       // first barrier)
       if (!(kTmaStores && full)) {
         constexpr int EPC = 16 / sizeof(Tact), CPR = kD / EPC;
-        const Tact* ot = reinterpret_cast<const Tact*>(S.wt);
+        const auto ot = GDN_SV(reinterpret_cast<const Tact*>(S.wt),
+                               (offsetof(ChainSmem, tm) - offsetof(ChainSmem, wt)) / sizeof(Tact));
         for (int e = tid; e < kC * CPR; e += kTh) {
           const int r = e / CPR, ch = e % CPR;
           const int64_t pos = P + r;
           if (pos >= p0 && pos < p1)
-            *reinterpret_cast<uint4*>(out + ((t0 + pos - p0) * a.hv + h) * kD + ch * EPC) =
-                *reinterpret_cast<const uint4*>(ot + r * kD + ch * EPC);
+            vec_at<uint4>(out, ((t0 + pos - p0) * a.hv + h) * kD + ch * EPC) = vec_at<const uint4>(ot, r * kD + ch * EPC);
         }
       }
     }
@@ -1057,8 +1092,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     } else {
 #pragma unroll
       for (int i = 0; i < 16; ++i)
-        *reinterpret_cast<float4*>(gS + 4 * i) =
-            make_float4(sreg[4 * i], sreg[4 * i + 1], sreg[4 * i + 2], sreg[4 * i + 3]);
+        vec_at<float4>(gS, 4 * i) = make_float4(sreg[4 * i], sreg[4 * i + 1], sreg[4 * i + 2], sreg[4 * i + 3]);
     }
   }
   // the tensor stores have landed before the CTA's shared memory goes away

@@ -125,9 +125,10 @@ struct __align__(1024) Smem32 {
 };
 
 __device__ __forceinline__ bool seq_ok(const Tc32Args& a, int n, int64_t& t0, int64_t& len, int64_t& p0) {
-  t0 = a.cu_seqlens[n];
-  len = (int64_t)a.cu_seqlens[n + 1] - t0;
-  p0 = a.start_pos[n];
+  const auto cu = GDN_GV(a.cu_seqlens, a.n_seq + 1);
+  t0 = cu[n];
+  len = (int64_t)cu[n + 1] - t0;
+  p0 = GDN_GV(a.start_pos, a.n_seq)[n];
   return !(t0 < 0 || len < 0 || t0 + len > a.total || p0 < 0);
 }
 
@@ -160,23 +161,27 @@ struct TOut {
   const float* eb;
   const float* rk;
 };
-__device__ __forceinline__ void put_t(const TOut& o, int r, int c, float x) {
+constexpr unsigned kTileT = 2 * 64 * 128;  // bytes of a 64 x 64 fp32 operand tile (T1, T2, M')
+__device__ __forceinline__ void put_t(const TOut& o, int r, int c, float x, int line = __builtin_LINE()) {
   const uint32_t off = f32_off(r, c, 64 * 128);
-  const float t = o.rk[r] * x * o.beta[c];
-  *reinterpret_cast<float*>(o.t1 + off) = umma::tf32_round(t);
-  *reinterpret_cast<float*>(o.t2 + off) = umma::tf32_round(-t * o.eb[c] * o.rk[c]);
+  const float t = o.rk[GDN_S(r, kC)] * x * o.beta[GDN_S(c, kC)];
+  tile_at<float>(o.t1, kTileT, off, line) = umma::tf32_round(t);
+  tile_at<float>(o.t2, kTileT, off, line) = umma::tf32_round(-t * o.eb[c] * o.rk[c]);
 }
 
-__device__ __forceinline__ void solve_T(const float* A, float* X, float* Y, float (*L0)[3][64], const TOut& to) {
+__device__ __forceinline__ void solve_T(const float* A_, float* X_, float* Y_, float (*L0)[3][64], const TOut& to) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const auto A = GDN_SV(A_, kC * kAX);
+  const auto X = GDN_SV(X_, kC * kAX);
+  const auto Y = GDN_SV(Y_, 2048);
   // 8 x 8 diagonal blocks: warp w < 8 inverts block w, L = A_ww (strictly
   // lower, so L^8 = 0), as (I + L)^-1 = (I - L)(I + L^2)(I + L^4); lane l
   // holds entries (l / 4, 2 (l % 4)) and (l / 4, 2 (l % 4) + 1)
   if (warp < 8) {
     const int o = 8 * warp, i = lane >> 2, j = 2 * (lane & 3);
-    float* L2 = L0[warp][0];
-    float* L4 = L0[warp][1];
-    float* B = L0[warp][2];
+    const auto L2 = GDN_SV(L0[warp][0], 64);
+    const auto L4 = GDN_SV(L0[warp][1], 64);
+    const auto B = GDN_SV(L0[warp][2], 64);
     auto Lw = [&](int r, int c) { return A[ix(o + r, o + c)]; };
     float s0 = 0.f, s1 = 0.f;  // L^2
 #pragma unroll
@@ -257,7 +262,7 @@ __device__ __forceinline__ void solve_T(const float* A, float* X, float* Y, floa
     for (int k4 = 0; k4 < 8; ++k4) {
       float4 a[2];
 #pragma unroll
-      for (int r = 0; r < 2; ++r) a[r] = *reinterpret_cast<const float4*>(A + ix(32 + 2 * warp + r, 4 * k4));
+      for (int r = 0; r < 2; ++r) a[r] = vec_at<const float4>(A, ix(32 + 2 * warp + r, 4 * k4));
       const float x0 = X[ix(4 * k4, lane)], x1 = X[ix(4 * k4 + 1, lane)], x2 = X[ix(4 * k4 + 2, lane)],
                   x3 = X[ix(4 * k4 + 3, lane)];
 #pragma unroll
@@ -276,7 +281,7 @@ __device__ __forceinline__ void solve_T(const float* A, float* X, float* Y, floa
     for (int k4 = 0; k4 < 8; ++k4) {
       float4 xb[2];
 #pragma unroll
-      for (int r = 0; r < 2; ++r) xb[r] = *reinterpret_cast<const float4*>(X + ix(32 + 2 * warp + r, 32 + 4 * k4));
+      for (int r = 0; r < 2; ++r) xb[r] = vec_at<const float4>(X, ix(32 + 2 * warp + r, 32 + 4 * k4));
       const float y0 = Y[32 * (4 * k4) + lane], y1 = Y[32 * (4 * k4 + 1) + lane], y2 = Y[32 * (4 * k4 + 2) + lane],
                   y3 = Y[32 * (4 * k4 + 3) + lane];
 #pragma unroll
@@ -311,12 +316,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (h == 0 && tid == 0) report(a.err, GDN_DEV_ERR_SEQLENS);
     return;
   }
-  const int32_t slot = a.slot_ids[n];
+  // the caller's tensors (extents in elements)
+  const auto out = GDN_GV(a.out, a.total * a.hv * kD);
+  const auto gate_a = GDN_GV(a.a, a.total * a.hv), gate_b = GDN_GV(a.b, a.total * a.hv);
+  const auto ckpt_ids = GDN_GV(a.ckpt_ids, (long long)a.n_seq * a.max_ckpt);
+  const int32_t slot = GDN_GV(a.slot_ids, a.n_seq)[n];
   const int cls = slot_class(slot, a.num_slots);
   if (cls) {
     if (cls == 2 && h == 0 && tid == 0) report(a.err, GDN_DEV_ERR_SLOT_OOB);
     for (int64_t e = tid; e < len * kD; e += kThreads)
-      a.out[((t0 + e / kD) * a.hv + h) * kD + (e % kD)] = __float2bfloat16_rn(0.f);
+      out[((t0 + e / kD) * a.hv + h) * kD + (e % kD)] = __float2bfloat16_rn(0.f);
     return;
   }
   if (len == 0) return;
@@ -340,6 +349,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   constexpr uint32_t ID_N64 = umma::idesc_tf32(128, 64, false, false);
   constexpr uint32_t ID_N128 = umma::idesc_tf32(128, 128, false, false);
+  // operand extents of the products below (their k-steps walk 32-column
+  // blocks: 128 rows x 128 bytes per block of kq and kt, 64 rows of tm, t2, mq)
+  static_assert(4 * 16384 <= sizeof(Smem32::kq) && 2 * 16384 <= sizeof(Smem32::kt), "operand tiles");
+  static_assert(2 * 8192 <= sizeof(Smem32::tm) && 2 * 8192 <= sizeof(Smem32::t2) && 2 * 8192 <= sizeof(Smem32::mq),
+                "operand tiles");
+  static_assert(TM_V + 64 <= TM_COLS && TM_O2 + 64 <= TM_V && TM_DL + 64 <= TM_O2 && TM_O1 + 64 <= TM_DL,
+                "TMEM regions");
 
   // feature channels of this thread: the q/k channel pair (2 cp, 2 cp + 1)
   // (k for tid % 128 < 64, else q) for tokens 16 qq .., and v channel lrow
@@ -351,14 +367,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   float2 wqk[4];
   float wv[4];
   {
-    const float4 w4 = *reinterpret_cast<const float4*>(a.conv_w + (size_t)gch_qk * 4);
-    const float4 u4 = *reinterpret_cast<const float4*>(a.conv_w + (size_t)(gch_qk + 1) * 4);
+    const auto cw = GDN_GV(a.conv_w, (long long)a.C * 4);
+    const float4 w4 = vec_at<const float4>(cw, (size_t)gch_qk * 4);
+    const float4 u4 = vec_at<const float4>(cw, (size_t)(gch_qk + 1) * 4);
     wqk[0] = make_float2(w4.x, u4.x); wqk[1] = make_float2(w4.y, u4.y);
     wqk[2] = make_float2(w4.z, u4.z); wqk[3] = make_float2(w4.w, u4.w);
-    const float4 v4 = *reinterpret_cast<const float4*>(a.conv_w + (size_t)gch_v * 4);
+    const float4 v4 = vec_at<const float4>(cw, (size_t)gch_v * 4);
     wv[0] = v4.x; wv[1] = v4.y; wv[2] = v4.z; wv[3] = v4.w;
   }
-  const float eA = expf(a.A_log[h]), dtb = a.dt_bias[h];
+  const float eA = expf(GDN_GV(a.A_log, a.hv)[h]), dtb = GDN_GV(a.dt_bias, a.hv)[h];
   const int part_x[3] = {hq * kD, (a.hk + hq) * kD, 2 * a.hk * kD + h * kD};
 
   // checkpoint slot at the end of chunk c (-1: none): chunk c ends at the
@@ -374,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (q % kpc != 0) return -1;
     const int idx = q / kpc - 1;
     if (idx >= a.max_ckpt) return -1;
-    const int32_t id = a.ckpt_ids[(size_t)n * a.max_ckpt + idx];
+    const int32_t id = ckpt_ids[(size_t)n * a.max_ckpt + idx];
     return slot_class(id, a.ck_num_slots) == 0 ? id : -1;
   };
   auto issue_raw = [&](int c) {  // thread 0: chunk c's raw rows into S.raw
@@ -382,7 +399,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t row0 = (int32_t)(t0 + (P - 3 - p0));  // packed row of raw row 0 (may be < 0)
     mbar_arrive_expect_tx(&S.ld_bar, 3u * kRawRows * kD * 2u);
 #pragma unroll
-    for (int q = 0; q < 3; ++q) tma_load_2d(&S.raw[q][0][0], &qmap, part_x[q], row0, &S.ld_bar);
+    for (int q = 0; q < 3; ++q)  // a box of 128 channels from part_x[q], 67 rows (rows outside: zeros)
+      if (GDN_SPAN_G(part_x[q], kD, a.C) && GDN_SBYTES(&S.raw[q][0][0], kRawRows * kD * 2, S))
+        tma_load_2d(&S.raw[q][0][0], &qmap, part_x[q], row0, &S.ld_bar);
   };
   // gate inputs of chunk c's token tid - 256 (threads 256..319), loaded one
   // chunk ahead
@@ -391,8 +410,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     av = bv = 0.f;
     if (c < nch && pos >= p0 && pos < p1) {
       const size_t tok = (size_t)(t0 + pos - p0);
-      av = __bfloat162float(a.a[tok * a.hv + h]);
-      bv = __bfloat162float(a.b[tok * a.hv + h]);
+      av = __bfloat162float(gate_a[tok * a.hv + h]);
+      bv = __bfloat162float(gate_b[tok * a.hv + h]);
     }
   };
 
@@ -407,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (gate_thread) {
       const int64_t pos = (p0 / kC + cc) * kC + gt;
       const bool in = pos >= p0 && pos < p1;
-      S.g[buf][gt] = in ? floor_log_decay(-eA * softplus_f(ga + dtb)) : 0.f;
+      S.g[buf][GDN_S(gt, kC)] = in ? floor_log_decay(-eA * softplus_f(ga + dtb)) : 0.f;
       S.beta[buf][gt] = in ? sigmoid_f(gb) : 0.f;
       load_gates(cc + 1, ga, gb);
       named_sync(1, kC);
@@ -435,12 +454,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   // initial state S^T rows into TMEM; the upper triangle of T1 stays zero
-  float* gS = a.ssm + (((size_t)slot * a.hv + h) * kD + lrow) * kD + 32 * qq;
+  const auto gS = GDN_GV(a.ssm, (long long)a.num_slots * a.hv * kD * kD) +
+                  ((((size_t)slot * a.hv + h) * kD + lrow) * kD + 32 * qq);
   {
     float v[32];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const float4 x = *reinterpret_cast<const float4*>(gS + 4 * i);
+      const float4 x = vec_at<const float4>(gS, 4 * i);
       v[4 * i] = x.x; v[4 * i + 1] = x.y; v[4 * i + 2] = x.z; v[4 * i + 3] = x.w;
     }
     umma::tmem_st32(tlane + TM_S + 32 * qq, v);
@@ -490,7 +510,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // step has read the tile: it ended with a CTA barrier)
     if (EPI && tid == 0) {
       mbar_arrive_expect_tx(&S.z_bar, (uint32_t)sizeof(S.zt));
-      tma_load_2d(&S.zt[0][0], &zmap, h * kD, (int32_t)(t0 + (P - p0)), &S.z_bar);
+      if (GDN_SPAN_G(h * kD, kD, (long long)a.hv * kD))
+        tma_load_2d(&S.zt[0][0], &zmap, h * kD, (int32_t)(t0 + (P - p0)), &S.z_bar);
     }
     // the chunk's raw rows landed
     if (!wait_all(&S.ld_bar, c & 1)) break;
@@ -499,9 +520,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (P - 3 < p0) {
       const int64_t lo = (P - 3 > p0 - 3) ? P - 3 : p0 - 3;
       const int64_t hi = (P + kC < p0) ? P + kC : p0;
-      const Tconv* hist = reinterpret_cast<const Tconv*>(a.conv) + (size_t)slot * 3 * a.C;
+      const auto hist = GDN_GV(reinterpret_cast<const Tconv*>(a.conv), (long long)a.num_slots * 3 * a.C) +
+                        (size_t)slot * 3 * a.C;
       for (int64_t pos = lo; pos < hi; ++pos) {
-        const int r = (int)(pos - (P - 3));
+        const int r = GDN_S((int)(pos - (P - 3)), kRawRows);
         for (int e = tid; e < 3 * kD; e += kThreads) {
           const int q = e / kD, ch = e % kD;
           S.raw[q][r][ch] = __float2bfloat16_rn(to_f32(hist[(size_t)(3 - (p0 - pos)) * a.C + part_x[q] + ch]));
@@ -519,7 +541,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // columns and, for k, its two K~^T rows
       float2 y[16];
       {
-        const __nv_bfloat162* xs = reinterpret_cast<const __nv_bfloat162*>(&S.raw[isq ? 0 : 1][tk][2 * cp]);
+        // channel pair 2 cp of rows tk .. tk + 18 of the q or k part
+        const auto xs = GDN_SV(reinterpret_cast<const __nv_bfloat162*>(&S.raw[isq ? 0 : 1][0][0]), kRawRows * kD / 2) +
+                        (tk * (kD / 2) + cp);
         float2 x[19];
 #pragma unroll
         for (int r = 0; r < 19; ++r) x[r] = __bfloat1622float2(xs[r * (kD / 2)]);
@@ -536,15 +560,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int R0 = (isq ? kC : 0) + tk;
 #pragma unroll
-      for (int t = 0; t < 16; ++t) *reinterpret_cast<float2*>(S.kq + f32_off(R0 + t, 2 * cp, 128 * 128)) = y[t];
+      for (int t = 0; t < 16; ++t) tile_at<float2>(S.kq, sizeof(S.kq), f32_off(R0 + t, 2 * cp, 128 * 128)) = y[t];
       if (!isq) {
 #pragma unroll
         for (int t4 = 0; t4 < 4; ++t4) {
-          const float4 e4 = *reinterpret_cast<const float4*>(&gebl[tk + 4 * t4]);
-          *reinterpret_cast<float4*>(S.kt + f32_off(2 * cp, tk + 4 * t4, 128 * 128)) =
+          const float4 e4 = *reinterpret_cast<const float4*>(&gebl[GDN_S(tk + 4 * t4, kC - 3)]);
+          tile_at<float4>(S.kt, sizeof(S.kt), f32_off(2 * cp, tk + 4 * t4, 128 * 128)) =
               make_float4(umma::tf32_round(y[4 * t4].x * e4.x), umma::tf32_round(y[4 * t4 + 1].x * e4.y),
                           umma::tf32_round(y[4 * t4 + 2].x * e4.z), umma::tf32_round(y[4 * t4 + 3].x * e4.w));
-          *reinterpret_cast<float4*>(S.kt + f32_off(2 * cp + 1, tk + 4 * t4, 128 * 128)) =
+          tile_at<float4>(S.kt, sizeof(S.kt), f32_off(2 * cp + 1, tk + 4 * t4, 128 * 128)) =
               make_float4(umma::tf32_round(y[4 * t4].y * e4.x), umma::tf32_round(y[4 * t4 + 1].y * e4.y),
                           umma::tf32_round(y[4 * t4 + 2].y * e4.z), umma::tf32_round(y[4 * t4 + 3].y * e4.w));
         }
@@ -552,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // v: channel lrow, into TMEM
       float vv[16];
       {
-        const __nv_bfloat16* xv = &S.raw[2][tk][lrow];
+        const auto xv = GDN_SV(&S.raw[2][0][0], kRawRows * kD) + (tk * kD + lrow);
         float x[19];
 #pragma unroll
         for (int r = 0; r < 19; ++r) x[r] = __bfloat162float(xv[r * kD]);
@@ -599,9 +623,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 1; i < 32; ++i) d = (lane == i) ? v[i] : d;
       if (lrow < kC)
-        S.rk[lrow] = rsqrtf(d + kNormEps);
+        S.rk[GDN_S(lrow, kC)] = rsqrtf(d + kNormEps);
       else
-        S.rq[lrow - kC] = rsqrtf(d + kNormEps) * rsqrtf((float)kD);
+        S.rq[GDN_S(lrow - kC, kC)] = rsqrtf(d + kNormEps) * rsqrtf((float)kD);
     }
     __syncthreads();
     // ---- A (fp32, for the solve) and M' (tf32 operand) from P ---------------
@@ -613,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float bc[16], rkc[16];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float4 b4 = *reinterpret_cast<const float4*>(&gb_[c0 + 4 * i]);
+        const float4 b4 = *reinterpret_cast<const float4*>(&gb_[GDN_S(c0 + 4 * i, kC - 3)]);
         bc[4 * i] = b4.x; bc[4 * i + 1] = b4.y; bc[4 * i + 2] = b4.z; bc[4 * i + 3] = b4.w;
         const float4 r4 = *reinterpret_cast<const float4*>(&S.rk[c0 + 4 * i]);
         rkc[4 * i] = r4.x; rkc[4 * i + 1] = r4.y; rkc[4 * i + 2] = r4.z; rkc[4 * i + 3] = r4.w;
@@ -626,7 +650,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 16; ++i) av[i] = (c0 + i < r) ? fr * rkc[i] * v[i] * exp_ftz(br - bc[i]) : 0.f;
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-          *reinterpret_cast<float4*>(S.sv.A + ix(r, c0 + 4 * q)) = make_float4(av[4 * q], av[4 * q + 1], av[4 * q + 2], av[4 * q + 3]);
+          vec_at<float4>(GDN_SV(S.sv.A, kC * kAX), ix(r, c0 + 4 * q)) =
+              make_float4(av[4 * q], av[4 * q + 1], av[4 * q + 2], av[4 * q + 3]);
       } else {
         const int r = lrow - kC;
         const float br = gb_[r], fr = S.rq[r];
@@ -635,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 16; ++i) m[i] = (c0 + i <= r) ? umma::tf32_round(fr * v[i] * exp_ftz(br - bc[i])) : 0.f;
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-          *reinterpret_cast<float4*>(S.mq + f32_off(r, c0 + 4 * q, 64 * 128)) =
+          tile_at<float4>(S.mq, sizeof(S.mq), f32_off(r, c0 + 4 * q, 64 * 128)) =
               make_float4(m[4 * q], m[4 * q + 1], m[4 * q + 2], m[4 * q + 3]);
       }
     }
@@ -706,7 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float o1[16], o2[16];
       umma::tmem_ld16(tlane + TM_O1 + 16 * qq, o1);
       umma::tmem_ld16(tlane + TM_O2 + 16 * qq, o2);
-      __nv_bfloat16* ot = reinterpret_cast<__nv_bfloat16*>(S.t2);
+      const auto ot = GDN_SV(reinterpret_cast<__nv_bfloat16*>(S.t2), kC * kD);
 #pragma unroll
       for (int i = 0; i < 16; ++i)
         ot[(16 * qq + i) * kD + lrow] = __float2bfloat16_rn(fmaf(o1[i], S.rq[16 * qq + i] * geb[16 * qq + i], o2[i]));
@@ -717,18 +742,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         float o1[16], o2[16];
         umma::tmem_ld16(tlane + TM_O1 + 16 * qq, o1);
         umma::tmem_ld16(tlane + TM_O2 + 16 * qq, o2);
-        float* of = reinterpret_cast<float*>(S.kt);
+        const auto of = GDN_SV(reinterpret_cast<float*>(S.kt), kC * kD);
 #pragma unroll
         for (int i = 0; i < 16; ++i) of[(16 * qq + i) * kD + lrow] = fmaf(o1[i], S.rq[16 * qq + i] * geb[16 * qq + i], o2[i]);
       }
       if (!wait_all(&S.z_bar, c & 1)) break;
-      const float4 w4 = *reinterpret_cast<const float4*>(a.norm_w + 4 * lane);
-      const float* of = reinterpret_cast<const float*>(S.kt);
-      __nv_bfloat16* ot = reinterpret_cast<__nv_bfloat16*>(S.t2);
+      const float4 w4 = vec_at<const float4>(GDN_GV(a.norm_w, kD), 4 * lane);
+      const auto of = GDN_SV(reinterpret_cast<const float*>(S.kt), kC * kD);
+      const auto ot = GDN_SV(reinterpret_cast<__nv_bfloat16*>(S.t2), kC * kD);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {  // tokens 4 warp + k: lane holds dv 4 lane .. 4 lane + 3
-        const int t = 4 * warp + k;
-        const float4 o4 = *reinterpret_cast<const float4*>(of + t * kD + 4 * lane);
+        const int t = GDN_S(4 * warp + k, kC);
+        const float4 o4 = vec_at<const float4>(of, t * kD + 4 * lane);
         float ss = o4.x * o4.x + o4.y * o4.y + o4.z * o4.z + o4.w * o4.w;
 #pragma unroll
         for (int m = 16; m; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
@@ -743,7 +768,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint2 yu;
         yu.x = *reinterpret_cast<const uint32_t*>(&y01);
         yu.y = *reinterpret_cast<const uint32_t*>(&y23);
-        *reinterpret_cast<uint2*>(ot + t * kD + 4 * lane) = yu;
+        vec_at<uint2>(ot, t * kD + 4 * lane) = yu;
       }
     }
     // checkpoint: the state rows, 128B-swizzled, into four 16 KB boxes (32
@@ -752,32 +777,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (cid >= 0) {
       float v[32];
       umma::tmem_ld32(tlane + TM_S + 32 * qq, v);
-      uint8_t* box = S.kq + qq * 16384;
 #pragma unroll
       for (int j = 0; j < 8; ++j)
-        *reinterpret_cast<float4*>(box + lrow * 128 + ((j ^ (lrow & 7)) << 4)) =
+        tile_at<float4>(S.kq, sizeof(S.kq), qq * 16384 + lrow * 128 + ((j ^ (lrow & 7)) << 4)) =
             make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
     }
     umma::fence_proxy_async();
     umma::fence_before();
     __syncthreads();
     if (tid == 0) {
-      if (full) tma_store_2d(&omap, S.t2, h * kD, (int32_t)(t0 + (P - p0)));
+      // boxes: 128 channels x 64 tokens of the output; 32 x 128 rows of a checkpoint
+      if (full && GDN_SPAN_G(t0 + (P - p0), kC, a.total) && GDN_SPAN_G(h * kD, kD, (long long)a.hv * kD))
+        tma_store_2d(&omap, S.t2, h * kD, (int32_t)(t0 + (P - p0)));
       if (cid >= 0) {
         const int32_t y = (int32_t)(((int64_t)cid * a.hv + h) * kD);
+        if (GDN_SPAN_G(y, kD, (long long)a.ck_num_slots * a.hv * kD)) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) tma_store_2d(&cmap, S.kq + k * 16384, 32 * k, y);
+          for (int k = 0; k < 4; ++k) tma_store_2d(&cmap, S.kq + k * 16384, 32 * k, y);
+        }
       }
       bulk_commit();
     }
     if (!full) {  // rows of the chunk's tokens inside the sequence: 16-byte stores
-      const __nv_bfloat16* ot = reinterpret_cast<const __nv_bfloat16*>(S.t2);
+      const auto ot = GDN_SV(reinterpret_cast<const __nv_bfloat16*>(S.t2), kC * kD);
       for (int e = tid; e < kC * (kD / 8); e += kThreads) {
         const int r = e / (kD / 8), ch = e % (kD / 8);
         const int64_t pos = P + r;
         if (pos >= p0 && pos < p1)
-          *reinterpret_cast<uint4*>(a.out + ((t0 + pos - p0) * a.hv + h) * kD + ch * 8) =
-              *reinterpret_cast<const uint4*>(ot + r * kD + ch * 8);
+          vec_at<uint4>(out, ((t0 + pos - p0) * a.hv + h) * kD + ch * 8) = vec_at<const uint4>(ot, r * kD + ch * 8);
       }
     }
   }
@@ -796,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     umma::tmem_ld32(tlane + TM_S + 32 * qq, v);
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-      *reinterpret_cast<float4*>(gS + 4 * i) = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+      vec_at<float4>(gS, 4 * i) = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
   }
   if (tid == 0) bulk_wait_all();
   umma::fence_before();

@@ -44,28 +44,45 @@ struct SlotOpArgs {
   uint32_t* err;
 };
 
+// bytes from the first to the end of the last of `n` slots (or records) of
+// `part` bytes each, `stride` bytes apart
+__device__ __forceinline__ long long slots_extent(int32_t n, size_t stride, size_t part) {
+  return n > 0 ? (long long)((size_t)(n - 1) * stride + part) : 0;
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kThreads) slot_op_kernel(SlotOpArgs a) {
   pdl_wait();
   pdl_trigger();
   const bool leader = blockIdx.x == 0 && threadIdx.x == 0;
   const size_t total = a.ssm_bytes + a.conv_bytes;
+  // the two sides in 16-byte units, and the id arrays
+  const auto src_ssm = GDN_GV(reinterpret_cast<const uint4*>(a.src_ssm),
+                              slots_extent(a.src_n, a.src_sstride, a.ssm_bytes) / 16);
+  const auto src_conv = GDN_GV(reinterpret_cast<const uint4*>(a.src_conv),
+                               slots_extent(a.src_n, a.src_cstride, a.conv_bytes) / 16);
+  const auto dst_ssm = GDN_GV(reinterpret_cast<uint4*>(a.dst_ssm), slots_extent(a.dst_n, a.dst_sstride, a.ssm_bytes) / 16);
+  const auto dst_conv =
+      GDN_GV(reinterpret_cast<uint4*>(a.dst_conv), slots_extent(a.dst_n, a.dst_cstride, a.conv_bytes) / 16);
+  const auto src_ids = GDN_GV(a.src_ids, (long long)a.n * (MODE == MODE_COMMIT ? a.T : 1));
+  const auto dst_ids = GDN_GV(a.dst_ids, a.n);
+  const auto accept_len = GDN_GV(a.accept_len, a.n);
   for (int32_t r = blockIdx.y; r < a.n; r += gridDim.y) {
     int32_t src = 0, dst;
     if (MODE == MODE_COMMIT) {
-      const int32_t L = a.accept_len[r];
+      const int32_t L = accept_len[r];
       if (L < 0 || L > a.T) {
         if (leader) report(a.err, GDN_DEV_ERR_SLOT_OOB);
         continue;
       }
       if (L == 0) continue;
-      src = a.src_ids[(size_t)r * a.T + (L - 1)];
+      src = src_ids[(size_t)r * a.T + (L - 1)];
     } else if (MODE == MODE_COPY || MODE == MODE_PACK) {
-      src = a.src_ids[r];
+      src = src_ids[r];
     } else if (MODE == MODE_UNPACK) {
       src = r;
     }
-    dst = MODE == MODE_PACK ? r : a.dst_ids[r];
+    dst = MODE == MODE_PACK ? r : dst_ids[r];
     const int cd = slot_class(dst, a.dst_n);
     const int cs = MODE == MODE_ZERO ? 0 : slot_class(src, a.src_n);
     // pack writes a zero record for a padding or out-of-range id
@@ -77,27 +94,22 @@ __global__ void __launch_bounds__(kThreads) slot_op_kernel(SlotOpArgs a) {
     if (MODE == MODE_PACK && cs == 2 && leader) report(a.err, GDN_DEV_ERR_SLOT_OOB);
     const size_t begin = (size_t)blockIdx.x * kPiece;
     if (begin >= total) continue;
-    char* dssm = a.dst_ssm + (size_t)dst * a.dst_sstride;
-    char* dconv = a.dst_conv + (size_t)dst * a.dst_cstride;
-    const char* sssm = a.src_ssm + (size_t)src * a.src_sstride;
-    const char* sconv = a.src_conv + (size_t)src * a.src_cstride;
+    // byte offsets of this slot's (record's) two parts
+    const size_t dss = (size_t)dst * a.dst_sstride, dcs = (size_t)dst * a.dst_cstride;
+    const size_t sss = (size_t)src * a.src_sstride, scs = (size_t)src * a.src_cstride;
     uint4 v[kVec];
 #pragma unroll
     for (int i = 0; i < kVec; ++i) {
       const size_t off = begin + ((size_t)i * kThreads + threadIdx.x) * 16;
       v[i] = make_uint4(0, 0, 0, 0);
-      if (!zero_fill && off < total) {
-        const char* p = off < a.ssm_bytes ? sssm + off : sconv + (off - a.ssm_bytes);
-        v[i] = *reinterpret_cast<const uint4*>(p);
-      }
+      if (!zero_fill && off < total)
+        v[i] = off < a.ssm_bytes ? src_ssm[(sss + off) / 16] : src_conv[(scs + off - a.ssm_bytes) / 16];
     }
 #pragma unroll
     for (int i = 0; i < kVec; ++i) {
       const size_t off = begin + ((size_t)i * kThreads + threadIdx.x) * 16;
-      if (off < total) {
-        char* p = off < a.ssm_bytes ? dssm + off : dconv + (off - a.ssm_bytes);
-        __stcs(reinterpret_cast<uint4*>(p), v[i]);
-      }
+      if (off < total)
+        __stcs(off < a.ssm_bytes ? dst_ssm.at((dss + off) / 16) : dst_conv.at((dcs + off - a.ssm_bytes) / 16), v[i]);
     }
   }
 }
@@ -220,9 +232,11 @@ __global__ void __launch_bounds__(kIdxThreads)
   pdl_trigger();
   const int32_t r = blockIdx.x * kIdxThreads + threadIdx.x;
   if (r >= B) return;
-  const int32_t* sp = spec_ids + (size_t)r * T;
-  int32_t* fr = freed + (size_t)r * T;
-  const int32_t L = accept_len[r];
+  const long long BT = (long long)B * T;
+  const auto sp = GDN_GV(spec_ids, BT) + (size_t)r * T;
+  const auto fr = GDN_GV(freed, BT) + (size_t)r * T;
+  const auto slots = GDN_GV(slot_ids, B);
+  const int32_t L = GDN_GV(accept_len, B)[r];
   if (L == 0) {
     for (int32_t t = 0; t < T; ++t) fr[t] = sp[t];
     return;
@@ -233,11 +247,11 @@ __global__ void __launch_bounds__(kIdxThreads)
     for (int32_t t = 0; t < T; ++t) fr[t] = -1;
     return;
   }
-  fr[0] = slot_ids[r];
+  fr[0] = slots[r];
   int32_t k = 1;
   for (int32_t t = 0; t < T; ++t)
     if (t != L - 1) fr[k++] = sp[t];
-  slot_ids[r] = acc;
+  slots[r] = acc;
 }
 
 }  // namespace
@@ -314,6 +328,25 @@ __global__ void wait_selftest_kernel(uint32_t* err) {
   __syncthreads();
   if (threadIdx.x == 0 && !mbar_wait(&bar, 0)) report(err, GDN_DEV_ERR_TIMEOUT);
 }
+
+#ifdef GDN_DEBUG_BOUNDS
+// Positive control of the checked build: one thread indexes a global and a
+// shared view one element past their declared extents and asks for a span
+// that ends past its view.  Each view covers only the first half of its
+// buffer, so even an index that escaped its check would stay inside real
+// memory; with the checks working, the two indices go to the scratch buffer
+// and the span is refused.
+__device__ int g_bounds_probe[8];
+__global__ void bounds_selftest_kernel() {
+  __shared__ int probe[8];
+  if (threadIdx.x != 0) return;
+  const auto gv = GDN_GV(g_bounds_probe, 4);
+  gv[4] = 1;
+  const auto sv = GDN_SV(probe, 4);
+  sv[4] = 1;
+  if (gv.has(2, 4)) g_bounds_probe[0] = probe[4];
+}
+#endif
 }  // namespace
 }  // namespace gdn
 
@@ -323,4 +356,15 @@ extern "C" gdn_status gdn_selftest_wait_timeout(uint32_t* dev_err, void* stream)
   const cudaError_t e = launch_plain(wait_selftest_kernel, dim3(1), dim3(32), 0,
                                      reinterpret_cast<cudaStream_t>(stream), dim3(1), dev_err);
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+extern "C" gdn_status gdn_selftest_bounds(void* stream) {
+#ifdef GDN_DEBUG_BOUNDS
+  const cudaError_t e = gdn::launch_plain(gdn::bounds_selftest_kernel, dim3(1), dim3(32), 0,
+                                          reinterpret_cast<cudaStream_t>(stream), dim3(1));
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+#else
+  (void)stream;
+  return GDN_ERR_UNSUPPORTED;
+#endif
 }

@@ -23,6 +23,30 @@ namespace gdn {
 namespace umma {
 
 constexpr uint32_t kSwizzle128 = 2;
+constexpr uint32_t kTmemCols = 512;  // TMEM columns of an SM
+
+// Checked build: a TMEM access of `ncols` columns from taddr stays inside the
+// SM's 512 columns, and (warp-level loads and stores, 32x32b shape) touches
+// the lanes of its warp's quarter.  A failure is recorded against the
+// caller's line and the access is skipped.  Always true in the normal build.
+__device__ __forceinline__ bool tmem_ok([[maybe_unused]] uint32_t taddr, [[maybe_unused]] uint32_t ncols,
+                                        [[maybe_unused]] bool warp_lanes, [[maybe_unused]] int line) {
+#ifdef GDN_DEBUG_BOUNDS
+  const uint32_t col = taddr & 0xFFFFu, lane = taddr >> 16;
+  if (col + ncols > kTmemCols) {
+    bounds_fail(line, 2, (long long)col + ncols - 1, kTmemCols);
+    return false;
+  }
+  const uint32_t quarter = 32u * ((threadIdx.x >> 5) & 3u);
+  if (warp_lanes ? lane != quarter : lane >= 128u) {
+    bounds_fail(line, 2, lane, warp_lanes ? quarter : 128);
+    return false;
+  }
+#endif
+  return true;
+}
+// columns an MMA of instruction descriptor `idesc` writes (N)
+__host__ __device__ constexpr uint32_t idesc_n(uint32_t idesc) { return ((idesc >> 17) & 0x3Fu) << 3; }
 
 __device__ __forceinline__ uint64_t desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   uint64_t d = 0;
@@ -46,7 +70,8 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
 }
 
 __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
-                                         bool accumulate) {
+                                         bool accumulate, int line = __builtin_LINE()) {
+  if (!tmem_ok(tmem_d, idesc_n(idesc), false, line)) return;
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
@@ -63,7 +88,8 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N, bool a_mn, bool 
 
 // D (TMEM) (+)= A B, A and B from shared-memory descriptors, kind::tf32 (K = 8)
 __device__ __forceinline__ void mma_tf32(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
-                                         bool accumulate) {
+                                         bool accumulate, int line = __builtin_LINE()) {
+  if (!tmem_ok(tmem_d, idesc_n(idesc), false, line)) return;
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
@@ -73,7 +99,8 @@ __device__ __forceinline__ void mma_tf32(uint32_t tmem_d, uint64_t a, uint64_t b
 // D (TMEM) (+)= A B with A in TMEM (M rows = lanes, K = 8 consecutive fp32
 // columns from tmem_a) and B from a shared-memory descriptor, kind::tf32
 __device__ __forceinline__ void mma_tf32_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc,
-                                            bool accumulate) {
+                                            bool accumulate, int line = __builtin_LINE()) {
+  if (!tmem_ok(tmem_d, idesc_n(idesc), false, line) || !tmem_ok(tmem_a, 8, false, line)) return;
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n}\n" ::"r"(tmem_d),
@@ -122,7 +149,12 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 
 // 32 consecutive fp32 columns of this thread's TMEM lane (warp w reads lanes
 // 32*(w%4) .. +31; taddr already carries the lane base in bits 16..31).
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32], int line = __builtin_LINE()) {
+  if (!tmem_ok(taddr, 32, true, line)) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = 0.f;
+    return;
+  }
   uint32_t r[32];
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
@@ -141,7 +173,8 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 // 32 consecutive fp32 columns of this thread's TMEM lane, written; returns
 // once the writes are done (the caller still fences before other threads or
 // the tensor core read them)
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32], int line = __builtin_LINE()) {
+  if (!tmem_ok(taddr, 32, true, line)) return;
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
       "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
@@ -161,7 +194,12 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
 }
 
 // 16 consecutive fp32 columns of this thread's TMEM lane (as tmem_ld32)
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16], int line = __builtin_LINE()) {
+  if (!tmem_ok(taddr, 16, true, line)) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = 0.f;
+    return;
+  }
   uint32_t r[16];
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
@@ -173,7 +211,8 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 // 16 consecutive fp32 columns of this thread's TMEM lane, written (as tmem_st32)
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16], int line = __builtin_LINE()) {
+  if (!tmem_ok(taddr, 16, true, line)) return;
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(
           taddr),
@@ -208,13 +247,15 @@ __device__ __forceinline__ uint4 pack8_bf16(const float* f) {
   return u;
 }
 
-// store one 64-element row (8 x 16-byte chunks) of a swizzled tile
-__device__ __forceinline__ void store_row64(uint8_t* tile, int row, const float* v64) {
+// store one 64-element row (8 x 16-byte chunks) of a swizzled tile of
+// tile_bytes bytes
+__device__ __forceinline__ void store_row64(uint8_t* tile, unsigned tile_bytes, int row, const float* v64,
+                                            int line = __builtin_LINE()) {
 #pragma unroll
   for (int ch = 0; ch < 8; ++ch) {
     const uint32_t off = (uint32_t)(row >> 3) * 1024u + (uint32_t)(row & 7) * 128u +
                          (uint32_t)((ch ^ (row & 7)) << 4);
-    *reinterpret_cast<uint4*>(tile + off) = pack8_bf16(v64 + ch * 8);
+    tile_at<uint4>(tile, tile_bytes, off, line) = pack8_bf16(v64 + ch * 8);
   }
 }
 

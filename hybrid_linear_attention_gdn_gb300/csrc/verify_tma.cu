@@ -136,6 +136,13 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
   const int64_t u0 = (int64_t)blockIdx.x * a.n_units / gridDim.x;
   const int64_t u1 = (int64_t)(blockIdx.x + 1) * a.n_units / gridDim.x;
   volatile int* abort_flag = &S.abort;
+  // extents of the caller's tensors (elements), for the checked build
+  const int nreq = (int)(a.n_units / ((int64_t)a.hv * a.sph));
+  [[maybe_unused]] const long long ssm_n = (long long)a.num_slots * a.hv * a.dv * kDK,
+                                   conv_n = (long long)a.num_slots * (kW - 1) * a.C,
+                                   spec_ssm_n = (long long)a.spec_num_slots * a.hv * a.dv * kDK,
+                                   spec_conv_n = (long long)a.spec_num_slots * (kW - 1) * a.C,
+                                   gate_n = (long long)nreq * T * a.hv, out_n = (long long)nreq * T * a.hv * a.dv;
 
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -163,7 +170,7 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
       const int r = g.r, h = g.h, R = g.ns * kRows, nchunks = g.ns, nch = 2 * kDK + R;
       const uint32_t bundle_bytes =
           (kW - 1) * nch * ec + T * nch * ea + nch * kW * 4 + (KDA ? T * kDK * ea + kDK * 4 : 0u);
-      const int32_t slot = a.slot_ids[r];
+      const int32_t slot = a.slot_ids[GDN_G(r, nreq)];
       if (slot_class(slot, a.num_slots)) continue;
       if (*abort_flag) break;
       const int hq = h / a.G;
@@ -173,26 +180,35 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
       typename SM::Bundle& Bd = S.bundle[bb];
       const size_t cq = (size_t)hq * kDK, ck = (size_t)a.hk * kDK + cq,
                    cv = 2 * (size_t)a.hk * kDK + (size_t)h * a.dv + (size_t)g.s0 * kRows;
+      // one bundle copy: `bytes` from global src (inside [base, base + extent))
+      // into the shared bundle
+      auto g2s = [&](void* dst, const void* src, uint32_t bytes, [[maybe_unused]] const void* base,
+                     [[maybe_unused]] long long extent) {
+        if (GDN_GBYTES(src, bytes, base, extent) && GDN_SBYTES(dst, bytes, S))
+          bulk_g2s(dst, src, bytes, &S.bfull[bb]);
+      };
       const Tconv* hist = reinterpret_cast<const Tconv*>(a.conv) + (size_t)slot * (kW - 1) * a.C;
       for (int j = 0; j < kW - 1; ++j) {
-        bulk_g2s(&Bd.hist[j][0], hist + (size_t)j * a.C + cq, kDK * ec, &S.bfull[bb]);
-        bulk_g2s(&Bd.hist[j][kDK], hist + (size_t)j * a.C + ck, kDK * ec, &S.bfull[bb]);
-        bulk_g2s(&Bd.hist[j][2 * kDK], hist + (size_t)j * a.C + cv, R * ec, &S.bfull[bb]);
+        g2s(&Bd.hist[j][0], hist + (size_t)j * a.C + cq, kDK * ec, a.conv, conv_n * ec);
+        g2s(&Bd.hist[j][kDK], hist + (size_t)j * a.C + ck, kDK * ec, a.conv, conv_n * ec);
+        g2s(&Bd.hist[j][2 * kDK], hist + (size_t)j * a.C + cv, R * ec, a.conv, conv_n * ec);
       }
+      const long long x_bytes = (long long)nreq * T * a.C * ea, w_bytes = (long long)a.C * kW * 4;
       for (int t = 0; t < T; ++t) {
         const Tact* x = reinterpret_cast<const Tact*>(a.qkv) + ((size_t)r * T + t) * a.C;
-        bulk_g2s(&Bd.x[t][0], x + cq, kDK * ea, &S.bfull[bb]);
-        bulk_g2s(&Bd.x[t][kDK], x + ck, kDK * ea, &S.bfull[bb]);
-        bulk_g2s(&Bd.x[t][2 * kDK], x + cv, R * ea, &S.bfull[bb]);
+        const int tt = GDN_S(t, MT);
+        g2s(&Bd.x[tt][0], x + cq, kDK * ea, a.qkv, x_bytes);
+        g2s(&Bd.x[tt][kDK], x + ck, kDK * ea, a.qkv, x_bytes);
+        g2s(&Bd.x[tt][2 * kDK], x + cv, R * ea, a.qkv, x_bytes);
       }
-      bulk_g2s(&Bd.w[0], a.conv_w + cq * kW, kDK * kW * 4, &S.bfull[bb]);
-      bulk_g2s(&Bd.w[kDK * kW], a.conv_w + ck * kW, kDK * kW * 4, &S.bfull[bb]);
-      bulk_g2s(&Bd.w[2 * kDK * kW], a.conv_w + cv * kW, R * kW * 4, &S.bfull[bb]);
+      g2s(&Bd.w[0], a.conv_w + cq * kW, kDK * kW * 4, a.conv_w, w_bytes);
+      g2s(&Bd.w[kDK * kW], a.conv_w + ck * kW, kDK * kW * 4, a.conv_w, w_bytes);
+      g2s(&Bd.w[2 * kDK * kW], a.conv_w + cv * kW, R * kW * 4, a.conv_w, w_bytes);
       if constexpr (KDA) {
         for (int t = 0; t < T; ++t)
-          bulk_g2s(&Bd.ga[t][0], reinterpret_cast<const Tact*>(a.a) + (((size_t)r * T + t) * a.hv + h) * kDK,
-                   kDK * ea, &S.bfull[bb]);
-        bulk_g2s(&Bd.gdt[0], a.dt_bias + (size_t)h * kDK, kDK * 4, &S.bfull[bb]);
+          g2s(&Bd.ga[GDN_S(t, MT)][0], reinterpret_cast<const Tact*>(a.a) + (((size_t)r * T + t) * a.hv + h) * kDK,
+              kDK * ea, a.a, gate_n * kDK * ea);
+        g2s(&Bd.gdt[0], a.dt_bias + (size_t)h * kDK, kDK * 4, a.dt_bias, (long long)a.hv * kDK * 4);
       }
       ++vk;
       const float* src = a.ssm + (((size_t)slot * a.hv + h) * a.dv + (size_t)g.s0 * kRows) * kDK;
@@ -200,7 +216,9 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
         const int st = n % STAGES;
         if (*abort_flag || !mbar_wait(&S.empty[st], ((n / STAGES) & 1) ^ 1)) { ok = false; break; }
         mbar_arrive_expect_tx(&S.full[st], kStageBytes);
-        bulk_g2s(S.ring[st], src + (size_t)c * kStageFloats, kStageBytes, &S.full[st]);
+        if (GDN_GBYTES(src + (size_t)c * kStageFloats, kStageBytes, a.ssm, ssm_n * 4) &&
+            GDN_SBYTES(S.ring[GDN_S(st, STAGES)], kStageBytes, S))
+          bulk_g2s(S.ring[st], src + (size_t)c * kStageFloats, kStageBytes, &S.full[st]);
       }
     }
     if (!ok || *abort_flag) {
@@ -223,19 +241,20 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
     const int r = g.r, h = g.h, R = g.ns * kRows, nchunks = g.ns, nch = 2 * kDK + R;
     const int row0 = g.s0 * kRows;  // first row of the segment within the head
     const int hq = h / a.G;
-    const int32_t slot = a.slot_ids[r];
-    const int32_t* sids = a.spec_ids + (size_t)r * T;
+    const int32_t slot = a.slot_ids[GDN_G(r, nreq)];
+    // spec slot of draft t of this request
+    auto sid_of = [&](int t) { return a.spec_ids[GDN_G((size_t)r * T + t, (long long)nreq * T)]; };
     const int cls = slot_class(slot, a.num_slots);
     if (cls) {
       if (cls == 2 && h == 0 && g.s0 == 0 && tid == 0) report(a.err, GDN_DEV_ERR_SLOT_OOB);
       for (int e = tid; e < T * R; e += kCons) {
         const int t = e / R, i = e % R;
-        reinterpret_cast<Tact*>(a.out)[(((size_t)r * T + t) * a.hv + h) * a.dv + row0 + i] =
+        reinterpret_cast<Tact*>(a.out)[GDN_G((((size_t)r * T + t) * a.hv + h) * a.dv + row0 + i, out_n)] =
             from_f32<Tact>(0.f);
       }
       continue;
     }
-    if (h == 0 && g.s0 == 0 && tid < T && slot_class(sids[tid], a.spec_num_slots) == 2)
+    if (h == 0 && g.s0 == 0 && tid < T && slot_class(sid_of(tid), a.spec_num_slots) == 2)
       report(a.err, GDN_DEV_ERR_SLOT_OOB);
     const int bb = vk & 1;
     if (!*abort_flag && !mbar_wait(&S.bfull[bb], (vk >> 1) & 1)) *abort_flag = 1;
@@ -246,14 +265,16 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
     // [win1, win2, x_t].  q/k channels are written by the segment holding row
     // 0 of the first V head of the QK group, v channels by their own segment.
     const bool qk_writer = (h % a.G) == 0 && g.s0 == 0;
-    for (int i = tid; i < nch; i += kCons) {
-      const float4 w = *reinterpret_cast<const float4*>(&Bd.w[i * kW]);
+    for (int i0 = tid; i0 < nch; i0 += kCons) {
+      const int i = GDN_S(i0, kMaxCh);
+      const float4 w = reinterpret_cast<const float4*>(Bd.w)[i];  // kW = 4 weights of channel i
       float w0 = to_f32(Bd.hist[0][i]), w1 = to_f32(Bd.hist[1][i]), w2 = to_f32(Bd.hist[2][i]);
       const size_t c = i < kDK ? (size_t)hq * kDK + i
                      : i < 2 * kDK ? (size_t)a.hk * kDK + (size_t)hq * kDK + (i - kDK)
                                    : 2 * (size_t)a.hk * kDK + (size_t)h * a.dv + (size_t)row0 + (i - 2 * kDK);
       const bool writes = i >= 2 * kDK || qk_writer;
-      for (int t = 0; t < T; ++t) {
+      for (int t0 = 0; t0 < T; ++t0) {
+        const int t = GDN_S(t0, MT);
         const float xv = to_f32(Bd.x[t][i]);
         float acc = w.x * w0;
         acc = fmaf(w.y, w1, acc);
@@ -263,34 +284,37 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
         w0 = w1;
         w1 = w2;
         w2 = xv;
-        const int32_t sid = sids[t];
+        const int32_t sid = sid_of(t);
         if (writes && slot_class(sid, a.spec_num_slots) == 0) {
-          Tconv* sc = reinterpret_cast<Tconv*>(a.spec_conv) + (size_t)sid * (kW - 1) * a.C + c;
-          sc[0] = from_f32<Tconv>(w0);
-          sc[a.C] = from_f32<Tconv>(w1);
-          sc[2 * (size_t)a.C] = from_f32<Tconv>(w2);
+          Tconv* const sc = reinterpret_cast<Tconv*>(a.spec_conv);
+          const size_t c0 = (size_t)sid * (kW - 1) * a.C + c;
+          sc[GDN_G(c0, spec_conv_n)] = from_f32<Tconv>(w0);
+          sc[GDN_G(c0 + a.C, spec_conv_n)] = from_f32<Tconv>(w1);
+          sc[GDN_G(c0 + 2 * (size_t)a.C, spec_conv_n)] = from_f32<Tconv>(w2);
         }
       }
     }
     if (tid < T) {
       const size_t rt = (size_t)r * T + tid;
-      S.sgate[tid][0] = KDA ? 1.f
-                            : gate_alpha(a.A_log[h], a.dt_bias[h],
-                                         to_f32(reinterpret_cast<const Tact*>(a.a)[rt * a.hv + h]));
-      S.sgate[tid][1] = sigmoid_f(to_f32(reinterpret_cast<const Tact*>(a.b)[rt * a.hv + h]));
+      const int tt = GDN_S(tid, MT);
+      S.sgate[tt][0] = KDA ? 1.f
+                           : gate_alpha(a.A_log[GDN_G(h, a.hv)], a.dt_bias[GDN_G(h, a.hv)],
+                                        to_f32(reinterpret_cast<const Tact*>(a.a)[GDN_G(rt * a.hv + h, gate_n)]));
+      S.sgate[tt][1] = sigmoid_f(to_f32(reinterpret_cast<const Tact*>(a.b)[GDN_G(rt * a.hv + h, gate_n)]));
     }
     if constexpr (KDA) {
       // alpha[t][c] = exp(-exp(A_log) softplus(a[t][c] + dt_bias[c])), from the bundle
-      const float A_log = a.A_log[h];
+      const float A_log = a.A_log[GDN_G(h, a.hv)];
       for (int e = tid; e < T * kDK; e += kCons) {
-        const int t = e / kDK, c = e % kDK;
+        const int t = GDN_S(e / kDK, MT), c = e % kDK;
         S.sal[t][c] = gate_alpha(A_log, Bd.gdt[c], to_f32(Bd.ga[t][c]));
       }
     }
     named_sync(kBarCons, kCons);
     mbar_arrive(&S.bempty[bb]);
     ++vk;
-    for (int t = warp; t < T; t += kCW) {
+    for (int t0 = warp; t0 < T; t0 += kCW) {
+      const int t = GDN_S(t0, MT);
       float pq = 0.f, pk = 0.f, pqk = 0.f;
       for (int i = lane; i < kDK; i += 32) {
         const float q = S.sy[t][i], k = S.sy[t][kDK + i];
@@ -315,7 +339,7 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
     named_sync(kBarCons, kCons);
     // q^ and k^ normalised in place, once per segment rather than per row
     for (int e = tid; e < T * 2 * kDK; e += kCons) {
-      const int t = e / (2 * kDK), i = e % (2 * kDK);
+      const int t = GDN_S(e / (2 * kDK), MT), i = e % (2 * kDK);
       S.sy[t][i] *= S.snorm[t][i < kDK ? 0 : 1];
     }
     named_sync(kBarCons, kCons);
@@ -324,19 +348,20 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
       const int st = n % STAGES;
       if (!*abort_flag && !mbar_wait(&S.full[st], (n / STAGES) & 1)) *abort_flag = 1;
       if (*abort_flag) continue;
-      const int row = c * kRows + rloc;  // row within the segment
+      const int row = GDN_S(c * kRows + rloc, kMaxR);  // row within the segment
       float4 s4[4];
-      const float* srow = S.ring[st] + rloc * kDK;
+      const float* srow = S.ring[GDN_S(st, STAGES)] + GDN_S(rloc, kRows) * kDK;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc)
-        s4[cc] = *reinterpret_cast<const float4*>(srow + cc * 4 * kLPR + seg * 4);
-      for (int t = 0; t < T; ++t) {
+        s4[cc] = *reinterpret_cast<const float4*>(srow + GDN_S(cc * 4 * kLPR + seg * 4, kDK - 3));
+      for (int t0 = 0; t0 < T; ++t0) {
+        const int t = GDN_S(t0, MT);
         const float kq = S.snorm[t][2];
         const float alpha = S.sgate[t][0], beta = S.sgate[t][1];
         float4 kk[4], qq[4];
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
-          const int col = cc * 4 * kLPR + seg * 4;
+          const int col = GDN_S(cc * 4 * kLPR + seg * 4, kDK - 3);
           kk[cc] = *reinterpret_cast<const float4*>(&S.sy[t][kDK + col]);
           qq[cc] = *reinterpret_cast<const float4*>(&S.sy[t][col]);
           if constexpr (KDA) {
@@ -359,7 +384,7 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
           dq_ += __shfl_xor_sync(0xffffffffu, dq_, o);
         }
         // KDA: alpha is 1 here (the rows carry the per-channel decay already)
-        const float bu = beta * (S.sy[t][2 * kDK + row] - alpha * dk_);
+        const float bu = beta * (S.sy[t][GDN_S(2 * kDK + row, kMaxCh)] - alpha * dk_);
         const float2 bu2 = make_float2(bu, bu), al2 = make_float2(alpha, alpha);
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
@@ -367,12 +392,13 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
           const float2 hi = KDA ? hi2(s4[cc]) : mul2(al2, hi2(s4[cc]));
           s4[cc] = join4(fma2(bu2, lo2(kk[cc]), lo), fma2(bu2, hi2(kk[cc]), hi));
         }
-        const int32_t sid = sids[t];
+        const int32_t sid = sid_of(t);
         if (slot_class(sid, a.spec_num_slots) == 0) {
-          float4* drow = reinterpret_cast<float4*>(
-              a.spec_ssm + (((size_t)sid * a.hv + h) * a.dv + (size_t)row0 + row) * kDK);
+          float4* const spec4 = reinterpret_cast<float4*>(a.spec_ssm);
+          const size_t drow4 = (((size_t)sid * a.hv + h) * a.dv + (size_t)row0 + row) * kDK / 4;
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) st_stream(drow + (cc * 4 * kLPR + seg * 4) / 4, s4[cc]);
+          for (int cc = 0; cc < 4; ++cc)
+            st_stream(spec4 + GDN_G(drow4 + (cc * 4 * kLPR + seg * 4) / 4, spec_ssm_n / 4), s4[cc]);
         }
         if (seg == 0) S.so[t][row] = fmaf(bu, kq, alpha * dq_);
       }
@@ -383,8 +409,8 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
     if (*abort_flag) break;
     for (int e = tid; e < T * R; e += kCons) {
       const int t = e / R, i = e % R;
-      reinterpret_cast<Tact*>(a.out)[(((size_t)r * T + t) * a.hv + h) * a.dv + row0 + i] =
-          from_f32<Tact>(S.so[t][i]);
+      reinterpret_cast<Tact*>(a.out)[GDN_G((((size_t)r * T + t) * a.hv + h) * a.dv + row0 + i, out_n)] =
+          from_f32<Tact>(S.so[GDN_S(t, MT)][GDN_S(i, kMaxR)]);
     }
   }
   if (*abort_flag && tid == 0) report(a.err, GDN_DEV_ERR_TIMEOUT);

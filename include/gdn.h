@@ -417,6 +417,37 @@ const char* gdn_status_string(int32_t status);
 uint64_t gdn_launch_count(int32_t kernel);
 void gdn_launch_count_reset(void);
 
+/*
+ * Bounds words of the checked build (libgdn_debug.so, compiled with
+ * GDN_DEBUG_BOUNDS): every computed global, shared-memory and TMEM index of
+ * the kernels is checked against the extent of its buffer (the tensor shapes
+ * this header states, the CTA's shared-memory layout, the TMEM columns); an
+ * index outside is counted, the first one's place recorded, and the access
+ * redirected to element 0 or skipped, without a trap.  This call waits for
+ * the device (cudaDeviceSynchronize), then copies the words out and clears
+ * them:
+ *   *count  number of failed checks since the last call (host, required);
+ *   where   if count > 0, "<source file>:<line> <global|shared|TMEM>" of the
+ *           first failure in the first unit that had one, NUL-terminated,
+ *           truncated to where_len bytes (host; may be NULL);
+ *   *index, *limit  that failure's index (for a span: its end) and the
+ *           extent it was checked against (host; may be NULL).
+ * GDN_ERR_UNSUPPORTED from the normal library (nothing is checked there),
+ * GDN_ERR_INVALID_ARG for a null count, GDN_ERR_CUDA if a copy fails.
+ */
+gdn_status gdn_debug_bounds_take(uint32_t* count, char* where, size_t where_len, int64_t* index,
+                                 int64_t* limit);
+
+/*
+ * Positive control of the checked build: one kernel makes three out-of-range
+ * requests that the checks must catch (an index one past a global view, one
+ * past a shared view, a span ending past its view), each view covering only
+ * half of its buffer so that nothing outside real memory is ever touched.  A
+ * following gdn_debug_bounds_take() reports count 3, the first "global".
+ * GDN_ERR_UNSUPPORTED from the normal library (launches nothing).
+ */
+gdn_status gdn_selftest_bounds(void* stream);
+
 #ifdef __cplusplus
 }
 #endif

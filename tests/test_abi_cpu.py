@@ -211,3 +211,19 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(binding, "library_path", lambda: str(tmp_path / "absent.so"))
     with pytest.raises(RuntimeError, match="libgdn.so not found"):
         binding.load()
+
+
+def test_normal_library_has_no_bounds_checks(lib):
+    """The bounds words and their positive control belong to the checked build
+    (libgdn_debug.so); the normal library answers GDN_ERR_UNSUPPORTED from the
+    host, launching nothing."""
+    count = ctypes.c_uint32(7)
+    assert lib.gdn_debug_bounds_take(ctypes.byref(count), None, 0, None, None) == binding.ERR_UNSUPPORTED
+    assert lib.gdn_selftest_bounds(None) == binding.ERR_UNSUPPORTED
+
+
+def test_checked_library_is_selected_by_the_environment(monkeypatch):
+    monkeypatch.setenv("GDN_DEBUG_BOUNDS", "1")
+    assert binding.library_path() == _build.LIB_DEBUG
+    monkeypatch.setenv("GDN_DEBUG_BOUNDS", "0")
+    assert binding.library_path() == _build.LIB
