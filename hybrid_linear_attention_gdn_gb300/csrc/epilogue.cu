@@ -6,14 +6,26 @@
 //   y = o / sqrt(mean(o^2) + eps) * w * silu(z),   w [dv] shared by the heads.
 //
 // HBM bound (o and z read once, y written once: 3 x 256 bytes per bf16 row of
-// 128): each warp takes four rows and issues all their loads before the first
-// reduction; lane l holds the EPL consecutive elements from l * EPL of a row
-// (one vector access when the row is full-width and aligned), the sum of
-// squares by a warp shuffle.  y may be o (each element is read before the
-// row's reduction and written after it, by the same lane).  A variant with
-// 16-byte accesses (two rows per warp-wide access, eight rows per warp)
-// measured slower: 0.63 against 0.76 of the copy bandwidth.
+// 128).  Two forms:
+//  * streamed (rows of 64 to 512 bytes, 16-byte aligned tensors): each warp
+//    copies 2 KB of consecutive rows of o and of z into shared memory by
+//    16-byte cp.async copies, all in flight at once without holding
+//    registers, then normalises them.  A row is LPR = row bytes / 16 lanes;
+//    lane l copies, and later reads back, the 16-byte pieces l % LPR of its
+//    rows, so no lane reads another's copies and no barrier is needed; the
+//    sum of squares reduces over the row's lanes by shuffles, and y leaves by
+//    16-byte stores.  (The same layout with the loads straight into
+//    registers measured 0.63 of the copy bandwidth: too few bytes in flight.)
+//  * general: each warp takes four rows and issues all their loads before the
+//    first reduction; lane l holds the EPL consecutive elements from l * EPL
+//    of a row (one vector access when the row is full-width and aligned).
+// In both, y may be o: every element is read before its row's reduction and
+// written after it, by the same lane.
 #include "gdn_common.cuh"
+#include "decode_tma.cuh"  // sm_count
+
+#include <cstdlib>
+#include <cstring>
 
 namespace gdn {
 namespace {
@@ -21,6 +33,12 @@ namespace {
 constexpr int kWarps = 8;        // warps per CTA
 constexpr int kRowsPerWarp = 4;  // rows a warp loads before its first reduction
 constexpr int kRowsPerCta = kWarps * kRowsPerWarp;
+
+// silu(z) = z / (1 + e^-z) with the approximate exponential and division
+// (ex2.approx and rcp.approx, a few ulp of fp32: far below the bf16 rounding
+// of the outputs).  An IEEE division here cost several times the two
+// special-function operations per element that the norm needs.
+__device__ __forceinline__ float silu_approx(float z) { return __fdividef(z, 1.f + exp_ftz(-z)); }
 
 // EPL consecutive elements of one row, by one vector access when VEC (the row
 // is full-width and 16-byte aligned; the vector is EPL * sizeof(T) <= 16 bytes)
@@ -110,11 +128,99 @@ __global__ void __launch_bounds__(32 * kWarps)
     float yv[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) {
-      const float gate = zv[i][e] / (1.f + exp_ftz(-zv[i][e]));  // silu(z)
+      const float gate = silu_approx(zv[i][e]);
       yv[e] = ov[i][e] * inv * wv[e] * gate;
     }
     store_part<T, EPL, VEC>(yv_ + (r0 + i) * dv, j0, dv, yv);
   }
+}
+
+// ---- streamed form -----------------------------------------------------------
+constexpr int kSWarps = 8;          // warps per CTA
+constexpr int kSGroupBytes = 2048;  // bytes of o (and of z) per warp: 8 rows of 256 bytes
+
+// LPR lanes per row (row bytes / 16); a warp's group is kSGroupBytes of
+// consecutive rows (RPG rows).  One group per warp, many CTAs: every load of
+// the group is in flight before the first is waited for, and the CTAs that
+// follow keep each SM's copies going while earlier ones compute and store.
+// (Measured on the Qwen3.5-shaped readout, 32768 tokens x 32 heads: 1.04 of
+// the measured copy bandwidth; the same copies walked by a persistent grid,
+// several groups per warp through a ring of stages, reached 0.80 - 0.85.)
+template <typename T, int LPR>
+__global__ void __launch_bounds__(32 * kSWarps)
+    gated_rmsnorm_stream_kernel(const T* o, const T* z, const float* __restrict__ w, float eps, int64_t rows,
+                                int dv, T* y) {
+  constexpr int E = 16 / sizeof(T);              // elements per 16-byte piece
+  constexpr int RPG = kSGroupBytes / (16 * LPR);  // rows per group
+  constexpr int RPI = 32 / LPR;                   // rows per warp-wide access
+  constexpr int NI = RPG / RPI;                   // accesses per group (per lane)
+  static_assert(RPG % RPI == 0 && NI >= 1, "whole accesses per group");
+  __shared__ __align__(16) uint4 stage[kSWarps][2][kSGroupBytes / 16];  // [warp][o | z]
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int piece = lane % LPR, sub = lane / LPR;  // 16-byte piece of the row, row within an access
+  const int64_t g = (int64_t)blockIdx.x * kSWarps + warp;
+  if (g * RPG >= rows) return;
+  const auto ov = GDN_GV(reinterpret_cast<const uint4*>(o), rows * LPR);
+  const auto zv = GDN_GV(reinterpret_cast<const uint4*>(z), rows * LPR);
+  const auto yv = GDN_GV(reinterpret_cast<uint4*>(y), rows * LPR);
+  const auto sv = GDN_SV(&stage[0][0][0], kSWarps * 2 * (kSGroupBytes / 16));
+  const int so = warp * 2 * (kSGroupBytes / 16), sz = so + kSGroupBytes / 16;  // this warp's o and z parts
+  // every piece of the group this lane reads: into shared memory, all in flight
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    const int64_t row = g * RPG + i * RPI + sub;
+    if (row < rows) {
+      const int64_t src = row * LPR + piece;
+      const int dst = i * 32 + lane;
+      if (sv.has(so + dst, 1) && ov.has(src, 1)) cp_async16(sv.p + so + dst, ov.p + src);
+      if (sv.has(sz + dst, 1) && zv.has(src, 1)) cp_async16(sv.p + sz + dst, zv.p + src);
+    }
+  }
+  cp_async_commit();
+  // the lane's weights meanwhile: elements piece * E .. piece * E + E - 1
+  float wv[E];
+  {
+    const auto wg = GDN_GV(w, dv);
+#pragma unroll
+    for (int e = 0; e < E; ++e) wv[e] = wg[piece * E + e];
+  }
+  cp_async_wait_all();  // this lane's copies have landed (it reads only those)
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    const int64_t row = g * RPG + i * RPI + sub;
+    const uint4 ou = sv[so + i * 32 + lane], zu = sv[sz + i * 32 + lane];
+    T ot[E], zt[E];
+    memcpy(ot, &ou, 16);
+    memcpy(zt, &zu, 16);
+    float of[E], ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      of[e] = to_f32(ot[e]);
+      ss = fmaf(of[e], of[e], ss);
+    }
+#pragma unroll
+    for (int m = LPR / 2; m; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+    const float inv = rsqrtf(ss / (float)dv + eps);
+    T yt[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) yt[e] = from_f32<T>(of[e] * inv * wv[e] * silu_approx(to_f32(zt[e])));
+    uint4 yu;
+    memcpy(&yu, yt, 16);
+    if (row < rows) yv[row * LPR + piece] = yu;
+  }
+}
+
+template <typename T, int LPR>
+cudaError_t launch_stream(const T* o, const T* z, const float* w, float eps, int64_t rows, int dv, T* y,
+                          cudaStream_t s) {
+  constexpr int RPG = kSGroupBytes / (16 * LPR);
+  const int64_t groups = (rows + RPG - 1) / RPG;
+  const int64_t ctas = (groups + kSWarps - 1) / kSWarps;
+  if (ctas > 2147483647LL) return cudaErrorInvalidValue;
+  return launch_pdl(gated_rmsnorm_stream_kernel<T, LPR>, dim3((unsigned)ctas), dim3(32 * kSWarps), 0, s, dim3(1),
+                    o, z, w, eps, rows, dv, y);
 }
 
 template <typename T, int EPL>
@@ -130,12 +236,28 @@ cudaError_t launch_epl(const T* o, const T* z, const float* w, float eps, int64_
                     y);
 }
 
+// GDN_EPILOGUE=rows selects the general form at every shape (read on every
+// call, so one process can time both)
+bool stream_epilogue() {
+  const char* e = std::getenv("GDN_EPILOGUE");
+  return !(e && e[0] == 'r');
+}
+
 template <typename T>
 cudaError_t launch_rmsnorm_t(const void* o, const void* z, const float* w, float eps, int64_t rows, int dv,
                              void* y, cudaStream_t s) {
   const T* ot = static_cast<const T*>(o);
   const T* zt = static_cast<const T*>(z);
   T* yt = static_cast<T*>(y);
+  // streamed: rows of 64, 128, 256 or 512 bytes, every tensor 16-byte aligned
+  const size_t row_bytes = (size_t)dv * sizeof(T);
+  const bool al16 = aligned(o, 16) && aligned(z, 16) && aligned(y, 16);
+  if (al16 && stream_epilogue()) {
+    if (row_bytes == 64) return launch_stream<T, 4>(ot, zt, w, eps, rows, dv, yt, s);
+    if (row_bytes == 128) return launch_stream<T, 8>(ot, zt, w, eps, rows, dv, yt, s);
+    if (row_bytes == 256) return launch_stream<T, 16>(ot, zt, w, eps, rows, dv, yt, s);
+    if (row_bytes == 512) return launch_stream<T, 32>(ot, zt, w, eps, rows, dv, yt, s);
+  }
   // vector accesses when every lane holds EPL elements of a full-width row and
   // every row starts 16-byte aligned
   const int epl = dv <= 32 ? 1 : dv <= 64 ? 2 : dv <= 128 ? 4 : 8;

@@ -21,12 +21,18 @@ def _rows(shape, n_tok, seed):
     return o, z, w
 
 
+@pytest.mark.parametrize("form", ["stream", "rows"])
 @pytest.mark.parametrize("shape,n_tok", [
     (synth.QWEN, 64), (synth.QWEN, 3), (synth.TINY, 37),
     (synth.QWEN.replace(hk=2, hv=8, dk=64, dv=64), 11),
+    (synth.QWEN.replace(act="f32", conv="f32", hk=1, hv=5), 7),
     (synth.QWEN.replace(act="f32", conv="f32", hk=4, hv=8, dv=200), 5),
-], ids=["qwen_b64", "qwen_3", "tiny_f32_dv16", "dv64", "f32_dv200_ragged"])
-def test_gated_rmsnorm_vs_oracle(cuda, shape, n_tok):
+], ids=["qwen_b64", "qwen_3", "tiny_f32_dv16", "dv64", "f32_dv128_ragged", "f32_dv200_ragged"])
+def test_gated_rmsnorm_vs_oracle(cuda, monkeypatch, form, shape, n_tok):
+    """Both forms (the streamed one takes rows of 64 to 512 bytes; dv 200 in
+    fp32 goes to the general one either way), rows not a whole number of the
+    streamed form's groups included."""
+    monkeypatch.setenv("GDN_EPILOGUE", form)
     o, z, w = _rows(shape, n_tok, 60 + n_tok)
     od = odims(shape)
     ref = oracle.gated_rmsnorm(od, to_np(o), to_np(z), w.double().numpy(), eps=1e-6)
