@@ -774,8 +774,16 @@ def _mixed_row(gdn, synth, dims, pool, params, perm, g, dev, stream):
     fp(0)
     ms_m = _events_time(fm, 20, stream)
     ms_p = _events_time(fp, 20, stream)
-    return {"ms": ms_m, "tokens_per_s": total / (ms_m * 1e-3), "ms_all_through_prefill": ms_p,
-            "batch": f"{n_dec} decode + 4 x {L} continuation tokens"}
+    # the same call as separate launches (decode kernel, chains, histories)
+    import os
+    os.environ["GDN_MIXED"] = "split"
+    try:
+        fm(0)
+        ms_s = _events_time(fm, 20, stream)
+    finally:
+        del os.environ["GDN_MIXED"]
+    return {"ms": ms_m, "tokens_per_s": total / (ms_m * 1e-3), "ms_split_launches": ms_s,
+            "ms_all_through_prefill": ms_p, "batch": f"{n_dec} decode + 4 x {L} continuation tokens"}
 
 
 def main():

@@ -21,8 +21,8 @@ F32, BF16 = 0, 1
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_SCRATCH_LIMIT = 0, 1, 2, 3, 4
 DEV_ERR_SLOT_OOB, DEV_ERR_TIMEOUT, DEV_ERR_SEQLENS = 1, 2, 4
 (K_DECODE, K_SPEC_VERIFY, K_SLOT_COPY, K_SLOT_ZERO, K_SPEC_COMMIT, K_PREFILL, K_COMMIT_INDEX,
- K_STATE_PACK, K_GATED_RMSNORM, K_KDA_DECODE, K_KDA_VERIFY, K_KDA_PREFILL) = range(12)
-K_COUNT = 12
+ K_STATE_PACK, K_GATED_RMSNORM, K_KDA_DECODE, K_KDA_VERIFY, K_KDA_PREFILL, K_MIXED) = range(13)
+K_COUNT = 13
 
 _DT_CODE = {torch.float32: F32, torch.bfloat16: BF16}
 

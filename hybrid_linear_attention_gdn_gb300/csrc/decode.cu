@@ -1056,6 +1056,11 @@ gdn_status run_step(bool verify, bool kda, const gdn_dims* dims, const gdn_pool&
 }
 
 }  // namespace
+
+// the decode step's kernel choice for batch B, for the mixed step
+bool decode_takes_tma(const gdn_dims& d, int32_t B, const void* qkv, const gdn_params& p) {
+  return use_tma_decode(d, B, qkv, p);
+}
 }  // namespace gdn
 
 extern "C" gdn_status gdn_decode_step(const gdn_dims* dims, gdn_pool pool, const gdn_params* params,

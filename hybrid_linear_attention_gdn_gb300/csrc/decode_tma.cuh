@@ -9,6 +9,8 @@ bool decode_tma_supported(const gdn_dims& d, const void* qkv, const gdn_params& 
 cudaError_t decode_tma_launch(const gdn_dims& d, const gdn_pool& pool, const gdn_params& p,
                               const int32_t* slot_ids, int32_t B, const void* qkv, const void* a,
                               const void* b, void* out, uint32_t* dev_err, bool kda, cudaStream_t s);
+// whether gdn_decode_step takes the TMA-fed kernel for batch B
+bool decode_takes_tma(const gdn_dims& d, int32_t B, const void* qkv, const gdn_params& p);
 int sm_count();
 // CTAs per SM for the persistent kernels: 0 = the default choice of each
 // kernel, 1 or 2 forced by GDN_TMA_CTAS (for measurement).

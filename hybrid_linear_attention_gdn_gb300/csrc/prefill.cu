@@ -24,6 +24,8 @@
 //             every checkpoint and the final one (it reads the old history
 //             before overwriting it, and runs after `features` read it)
 #include "gdn_common.cuh"
+#include "decode_tma.cuh"
+#include "prefill_history.cuh"
 #include "prefill_tc.cuh"
 
 #include <cstdlib>
@@ -32,80 +34,11 @@
 namespace gdn {
 namespace {
 
+using namespace pfx;
+
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kChunk = 64;
-constexpr int kMaxW = 8;
-constexpr int kCkGroup = 4;  // checkpoints per history-kernel thread
-
-struct PrefillArgs {
-  float* ssm;
-  void* conv;
-  int32_t num_slots;
-  float* ck_ssm;
-  void* ck_conv;
-  int32_t ck_num_slots;
-  const float* conv_w;
-  const float* A_log;
-  const float* dt_bias;
-  const int32_t* slot_ids;
-  const int32_t* cu_seqlens;
-  const int64_t* start_pos;
-  int32_t n_seq;
-  int64_t total;
-  const int32_t* ckpt_ids;
-  int32_t max_ckpt;
-  int32_t ckpt_block;
-  const void* qkv;
-  const void* a;
-  const void* b;
-  void* out;
-  uint32_t* err;
-  // workspace (fp32)
-  float* ws_q;     // [total][hk][dk]  q^ (scaled by dk^-1/2)
-  float* ws_k;     // [total][hk][dk]  k^
-  float* ws_v;     // [total][hv][dv]
-  float* ws_g;     // [total][hv]      log decay g
-  float* ws_beta;  // [total][hv]
-  int32_t hk, hv, dk, dv, W, C, G;
-};
-
-// The caller's tensors and the workspace of a prefill as checked views
-// (extents in elements).
-template <typename Tact, typename Tconv>
-struct PrefillViews {
-  View<float, 0> ssm, ck_ssm, ws_q, ws_k, ws_v, ws_g, ws_beta;
-  View<Tconv, 0> conv, ck_conv;
-  View<const float, 0> conv_w, A_log, dt_bias;
-  View<const int32_t, 0> slot_ids, cu_seqlens, ckpt_ids;
-  View<const int64_t, 0> start_pos;
-  View<const Tact, 0> qkv, a, b;
-  View<Tact, 0> out;
-  __device__ __forceinline__ explicit PrefillViews(const PrefillArgs& g) {
-    const long long slot_n = (long long)g.hv * g.dv * g.dk, hist_n = (long long)(g.W - 1) * g.C;
-    ssm = GDN_GV(g.ssm, g.num_slots * slot_n);
-    ck_ssm = GDN_GV(g.ck_ssm, g.ck_num_slots * slot_n);
-    conv = GDN_GV(reinterpret_cast<Tconv*>(g.conv), g.num_slots * hist_n);
-    ck_conv = GDN_GV(reinterpret_cast<Tconv*>(g.ck_conv), g.ck_num_slots * hist_n);
-    ws_q = GDN_GV(g.ws_q, g.total * g.hk * g.dk);
-    ws_k = GDN_GV(g.ws_k, g.total * g.hk * g.dk);
-    ws_v = GDN_GV(g.ws_v, g.total * g.hv * g.dv);
-    ws_g = GDN_GV(g.ws_g, g.total * g.hv);
-    ws_beta = GDN_GV(g.ws_beta, g.total * g.hv);
-    conv_w = GDN_GV(g.conv_w, (long long)g.C * g.W);
-    A_log = GDN_GV(g.A_log, g.hv);
-    dt_bias = GDN_GV(g.dt_bias, g.hv);
-    slot_ids = GDN_GV(g.slot_ids, g.n_seq);
-    cu_seqlens = GDN_GV(g.cu_seqlens, g.n_seq + 1);
-    ckpt_ids = GDN_GV(g.ckpt_ids, (long long)g.n_seq * g.max_ckpt);
-    start_pos = GDN_GV(g.start_pos, g.n_seq);
-    qkv = GDN_GV(reinterpret_cast<const Tact*>(g.qkv), g.total * g.C);
-    a = GDN_GV(reinterpret_cast<const Tact*>(g.a), g.total * g.hv);
-    b = GDN_GV(reinterpret_cast<const Tact*>(g.b), g.total * g.hv);
-    out = GDN_GV(reinterpret_cast<Tact*>(g.out), g.total * g.hv * g.dv);
-  }
-};
-
 template <typename V>
 __device__ __forceinline__ int seq_of_token(const V& cu, int n_seq, int64_t t) {
   int lo = 0, hi = n_seq - 1;  // last n with cu[n] <= t
@@ -410,61 +343,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const PrefillArgs a)
 }
 
 // ---------------------------------------------------------------------------
-// history: grid (ceil(C / 256), n_seq); one thread per channel
+// history: grid (ceil(C / 256), n_seq, groups); one thread per channel
+// (history_channel, prefill_history.cuh)
 // ---------------------------------------------------------------------------
 template <typename Tact, typename Tconv>
 __global__ void __launch_bounds__(kThreads) history_kernel(const PrefillArgs a) {
   pdl_wait();
   pdl_trigger();
-  const int n = blockIdx.y, grp = blockIdx.z;
-  const int c = blockIdx.x * kThreads + threadIdx.x;
-  if (c >= a.C) return;
-  const PrefillViews<Tact, Tconv> g(a);
-  const int32_t slot = g.slot_ids[n];
-  if (slot_class(slot, a.num_slots)) return;
-  const int64_t t0 = g.cu_seqlens[n], len = (int64_t)g.cu_seqlens[n + 1] - t0;
-  const int64_t p0 = g.start_pos[n], p1 = p0 + len;
-  if (t0 < 0 || len < 0 || t0 + len > a.total || p0 < 0) return;
-  const auto hist = g.conv + (size_t)slot * (a.W - 1) * a.C;
-  const auto qkv = g.qkv;
-  // Group 0 owns the working slot's history: it reads the old rows before
-  // writing the new ones, and only its first checkpoint can reach back into
-  // them (later checkpoints lie at least one 64-token block further on).
-  float old[kMaxW];
-#pragma unroll
-  for (int j = 0; j < kMaxW - 1; ++j)
-    if (j < a.W - 1) old[j] = grp == 0 ? to_f32(hist[(size_t)j * a.C + c]) : 0.f;
-  // raw input at sequence-relative index m (negative: the old history)
-  auto raw = [&](int64_t m) -> float {
-    if (m >= 0) return to_f32(qkv[(t0 + m) * a.C + c]);
-    float v = 0.f;
-#pragma unroll
-    for (int j = 0; j < kMaxW - 1; ++j)
-      if (j == a.W - 1 + m) v = old[j];
-    return v;
-  };
-  const int64_t blk = a.ckpt_block;
-#pragma unroll
-  for (int k = 0; k < kCkGroup; ++k) {
-    const int idx = grp * kCkGroup + k;
-    const int64_t P = (p0 / blk + 1 + idx) * blk;
-    if (idx >= a.max_ckpt || P > p1) break;
-    const int32_t cid = g.ckpt_ids[(size_t)n * a.max_ckpt + idx];
-    const int cc = slot_class(cid, a.ck_num_slots);
-    if (cc == 2 && c == 0) report(a.err, GDN_DEV_ERR_SLOT_OOB);
-    if (cc) continue;
-    const auto ch = g.ck_conv + (size_t)cid * (a.W - 1) * a.C;
-    for (int j = 0; j < a.W - 1; ++j)
-      ch[(size_t)j * a.C + c] = from_f32<Tconv>(raw(P - p0 - (a.W - 1) + j));
-  }
-  if (grp != 0) return;
-  float nw[kMaxW];
-#pragma unroll
-  for (int j = 0; j < kMaxW - 1; ++j)
-    if (j < a.W - 1) nw[j] = raw(len - (a.W - 1) + j);
-#pragma unroll
-  for (int j = 0; j < kMaxW - 1; ++j)
-    if (j < a.W - 1) hist[(size_t)j * a.C + c] = from_f32<Tconv>(nw[j]);
+  history_channel<Tact, Tconv>(a, blockIdx.y, blockIdx.z, (int)(blockIdx.x * kThreads + threadIdx.x));
 }
 
 // channels x sequences x groups of kCkGroup checkpoints
@@ -748,6 +634,24 @@ extern "C" gdn_status gdn_mixed_step(const gdn_dims* dims, gdn_pool pool, gdn_po
   const int32_t* pre_cu = n_pre > 0 ? cu_seqlens + n_decode : nullptr;
   const int64_t* pre_sp = n_pre > 0 ? start_pos + n_decode : nullptr;
   const int32_t* pre_ck = (n_pre > 0 && max_ckpt > 0) ? ckpt_ids + (size_t)n_decode * max_ckpt : nullptr;
+  // one launch when both halves take their fast paths and the workspace
+  // holds the work queue (after the same host checks as the separate calls)
+  if (n_pre > 0 && n_decode > 0 && mixed_fused_supported(*dims, qkv, out, *params) &&
+      prefill_path(*dims, qkv, out, *params) == PrefillPath::kTf32 &&
+      decode_takes_tma(*dims, n_decode, qkv, *params) && workspace &&
+      workspace_bytes >= mixed_fused_queue_bytes(n_pre) && aligned(workspace, 8)) {
+    if (!qkv || !a || !b || !out) return GDN_ERR_INVALID_ARG;
+    if ((st = check_pool(*dims, pool)) != GDN_OK) return st;
+    if ((st = chunk_prefill_impl(false, dims, pool, ckpt, params, pre_ids, pre_cu, pre_sp, n_pre, total_tokens,
+                                 pre_ck, max_ckpt, ckpt_block, qkv, a, b, out, nullptr, 0, dev_err, stream)) !=
+        GDN_OK)
+      return st;
+    const cudaError_t e = mixed_fused_launch(*dims, pool, ckpt, *params, slot_ids, cu_seqlens, start_pos, n_seq,
+                                             n_decode, total_tokens, ckpt_ids, max_ckpt, ckpt_block, qkv, a, b,
+                                             out, workspace, dev_err, reinterpret_cast<cudaStream_t>(stream));
+    count_launch(GDN_K_MIXED);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+  }
   if (n_pre > 0 &&
       (st = chunk_prefill_impl(false, dims, pool, ckpt, params, pre_ids, pre_cu, pre_sp, n_pre, total_tokens,
                                pre_ck, max_ckpt, ckpt_block, qkv, a, b, out, workspace, workspace_bytes,

@@ -28,6 +28,17 @@ cudaError_t prefill_tc32_launch(const gdn_dims& d, const gdn_pool& pool, const g
                                 int32_t n_seq, int64_t total, const int32_t* ckpt_ids, int32_t max_ckpt,
                                 int32_t ckpt_block, const void* qkv, const void* a, const void* b, void* out,
                                 uint32_t* dev_err, cudaStream_t s, const Tc32Epilogue* epi = nullptr);
+// The single-launch mixed step (prefill_tc32.cu): decode requests as the
+// TMA-fed decode items and continuations as tf32 chains plus their conv
+// histories, in one persistent launch.  queue: mixed_fused_queue_bytes(n_pre)
+// bytes of device memory, 8-byte aligned.
+bool mixed_fused_supported(const gdn_dims& d, const void* qkv, const void* out, const gdn_params& p);
+size_t mixed_fused_queue_bytes(int32_t n_pre);
+cudaError_t mixed_fused_launch(const gdn_dims& d, const gdn_pool& pool, const gdn_pool& ckpt, const gdn_params& p,
+                               const int32_t* slot_ids, const int32_t* cu_seqlens, const int64_t* start_pos,
+                               int32_t n_seq, int32_t n_decode, int64_t total, const int32_t* ckpt_ids,
+                               int32_t max_ckpt, int32_t ckpt_block, const void* qkv, const void* av,
+                               const void* bv, void* out, void* queue, uint32_t* dev_err, cudaStream_t s);
 // conv histories of a prefill's checkpoints and final state (prefill.cu)
 cudaError_t conv_history_launch(const gdn_dims& d, const gdn_pool& pool, const gdn_pool& ckpt,
                                 const int32_t* slot_ids, const int32_t* cu_seqlens, const int64_t* start_pos,

@@ -48,9 +48,15 @@
 // leave by TMA tensor stores.  The conv histories of checkpoints and of the
 // final state come from the history kernel of prefill.cu.
 #include "gdn_common.cuh"
+#include "decode_tma.cuh"
+#include "decode_tma_item.cuh"
+#include "prefill_history.cuh"
 #include "prefill_tc.cuh"
 #include "tma.cuh"
 #include "umma.cuh"
+
+#include <atomic>
+#include <cstdlib>
 
 namespace gdn {
 namespace {
@@ -297,20 +303,18 @@ __device__ __forceinline__ void solve_T(const float* A_, float* X_, float* Y_, f
   }
 }
 
-// ---- the kernel -------------------------------------------------------------
-// grid (hv, n_seq), 512 threads, one CTA per SM.  Thread 0 issues the TMA
-// copies and the tensor-core products; every wait is bounded (1 s).
+// ---- one chain ---------------------------------------------------------------
+// V head h of sequence n, by all kThreads threads of the CTA, which holds the
+// 512 TMEM columns from `tmem` on.  Thread 0 issues the TMA copies and the
+// tensor-core products; every wait is bounded (1 s).  The chain's barriers
+// are set up here and invalidated at its end, after its last tensor store
+// has completed, so the shared memory can serve the next work item.
 template <typename Tconv, bool EPI>
-__global__ void __launch_bounds__(kThreads, 1)
-    tc32_prefill_kernel(const Tc32Args a, const __grid_constant__ CUtensorMap qmap,
-                        const __grid_constant__ CUtensorMap omap, const __grid_constant__ CUtensorMap cmap,
-                        const __grid_constant__ CUtensorMap zmap) {
-  pdl_wait();
-  pdl_trigger();
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
-  Smem32& S = *reinterpret_cast<Smem32*>(smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023));
+__device__ __forceinline__ void tc32_chain(const Tc32Args& a, const CUtensorMap& qmap, const CUtensorMap& omap,
+                                           const CUtensorMap& cmap, const CUtensorMap& zmap, Smem32& S,
+                                           const uint32_t tmem, const int h, const int n) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int h = blockIdx.x, n = blockIdx.y, hq = h / a.G;
+  const int hq = h / a.G;
   int64_t t0, len, p0;
   if (!seq_ok(a, n, t0, len, p0)) {
     if (h == 0 && tid == 0) report(a.err, GDN_DEV_ERR_SEQLENS);
@@ -338,11 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&S.z_bar, 1);
     fence_mbar_init();
   }
-  if (warp == 0) umma::tmem_alloc(&S.tmem_base, TM_COLS);
-  umma::fence_before();
   __syncthreads();
-  umma::fence_after();
-  const uint32_t tmem = S.tmem_base;
   const int lrow = 32 * (warp & 3) + lane;  // TMEM lane of this thread (dv row, or [Y_K;Y_Q] row)
   const int qq = warp >> 2;                 // which column quarter this warp handles
   const uint32_t tlane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
@@ -828,7 +828,286 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) bulk_wait_all();
   umma::fence_before();
   __syncthreads();
+  if (tid == 0) {
+    mbar_inval(&S.ld_bar);
+    mbar_inval(&S.mma_bar);
+    mbar_inval(&S.z_bar);
+  }
+}
+
+// grid (hv, n_seq), 512 threads, one CTA per SM: one chain each.
+template <typename Tconv, bool EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc32_prefill_kernel(const Tc32Args a, const __grid_constant__ CUtensorMap qmap,
+                        const __grid_constant__ CUtensorMap omap, const __grid_constant__ CUtensorMap cmap,
+                        const __grid_constant__ CUtensorMap zmap) {
+  pdl_wait();
+  pdl_trigger();
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  Smem32& S = *reinterpret_cast<Smem32*>(smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023));
+  const int warp = threadIdx.x >> 5;
+  if (warp == 0) umma::tmem_alloc(&S.tmem_base, TM_COLS);
+  umma::fence_before();
+  __syncthreads();
+  umma::fence_after();
+  const uint32_t tmem = S.tmem_base;
+  tc32_chain<Tconv, EPI>(a, qmap, omap, cmap, zmap, S, tmem, blockIdx.x, blockIdx.y);
+  umma::fence_before();
+  __syncthreads();
   if (warp == 0) umma::tmem_dealloc(tmem, TM_COLS);
+}
+
+// ---- the single-launch mixed step ---------------------------------------------
+// TokenSpeed talk, "Kernel: 让 MLA 真正跑满 GPU": a decode-first batch of
+// decode requests and prefill continuations, variable length, no padding.
+// One persistent launch (one CTA per SM) takes work items from a queue in
+// global memory, in this order:
+//   chains     (V head, continuation): tc32_chain above;
+//   decode     (request, QK head): the TMA-fed decode items of
+//              decode_tma_item.cuh.  A CTA that takes one enters a decode
+//              walk: its producer lane takes the following items itself and
+//              hands each to the consumers with its bundle, until it takes a
+//              non-decode item, which ends the walk for the whole CTA;
+//   histories  (continuation, checkpoint group, 512 channels): the conv
+//              histories of pfx::history_channel, each once every chain of
+//              its continuation has finished (and so read the old history).
+// Every item computes exactly what the separate launches compute, so the
+// results are bit-identical to the decode step and chunked prefill called
+// one after the other.  The chains come first so that the decode items fill
+// the SMs the chains leave free and then the ones they release.
+//
+// The queue words live in the caller's workspace, each tagged with a
+// per-call epoch in its upper half, so no word needs clearing before a call;
+// the last CTA to finish returns them to zero (so a replayed CUDA graph, with
+// its epoch baked in, starts afresh too).
+constexpr int kDecStages = 10;  // the decode walk's ring: as the one-CTA-per-SM decode kernel
+using DecSmem = dtma::TmaSmem<__nv_bfloat16, __nv_bfloat16, kDecStages, false>;
+static_assert(dtma::bundle_aligned<__nv_bfloat16, __nv_bfloat16, kDecStages, false>(), "bulk-copy destinations");
+static_assert(dtma::vectors_aligned<__nv_bfloat16, __nv_bfloat16, kDecStages, false>(), "float4 reads");
+static_assert(dtma::kThr <= kThreads, "the decode walk's warps are a subset of the CTA");
+
+struct MixedArgs {
+  dtma::TmaArgs dec;      // the decode requests (rows 0 .. n_decode - 1)
+  Tc32Args pf;            // the continuations
+  pfx::PrefillArgs hist;  // the same continuations, for their conv histories
+  unsigned long long* queue;     // [0]: next item, [1]: CTAs done, [2 ..]: chains done per continuation
+  uint32_t epoch;
+  int32_t n_chain, n_dec, n_hist, hist_blocks, hist_groups;
+};
+
+struct __align__(1024) MixedSmem {
+  union {
+    Smem32 pf;
+    DecSmem dec;
+  };
+  int item;   // the CTA's next work item (broadcast)
+  int ready;  // a history item's continuation is ready
+};
+
+// (epoch, count) words: count under this call's epoch, 0 under another
+__device__ __forceinline__ uint32_t epoch_count(unsigned long long w, uint32_t epoch) {
+  return (uint32_t)(w >> 32) == epoch ? (uint32_t)w : 0u;
+}
+// Word q carries this call's epoch from now on: a word of another call (or
+// zero) becomes (epoch, 0) by one compare-and-swap, which at most one caller
+// wins; false if the word stayed contended for the retry limit.  Counting is
+// then a plain atomic add (no compare-and-swap on the hot word: contended
+// swaps made the walk several times slower).
+__device__ __forceinline__ bool epoch_install(unsigned long long* q, uint32_t epoch) {
+  for (int it = 0; it < (1 << 20); ++it) {
+    const unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(q);
+    if ((uint32_t)(old >> 32) == epoch) return true;
+    if (atomicCAS(q, old, (unsigned long long)epoch << 32) == old) return true;
+  }
+  return false;
+}
+// add 1 to word q's count (its epoch installed first); the count before, or
+// -1 if the epoch could not be installed
+__device__ __forceinline__ long long epoch_add(unsigned long long* q, uint32_t epoch) {
+  if (!epoch_install(q, epoch)) return -1;
+  const unsigned long long old = atomicAdd(q, 1ull);
+  return (uint32_t)(old >> 32) == epoch ? (long long)(uint32_t)old : -1;
+}
+
+// thread 0: the next work item (>= total, or -1 on a failure, ends the CTA's
+// walk).  One atomic add; only when it lands on a word of another call (the
+// first takes of this one) is the epoch installed and the add repeated: the
+// install wipes such stray adds, and an add after it counts for this call.
+__device__ __forceinline__ int take_item(const MixedArgs& m) {
+  for (int tries = 0; tries < 4; ++tries) {
+    const unsigned long long old = atomicAdd(m.queue, 1ull);
+    if ((uint32_t)(old >> 32) == m.epoch) return (uint32_t)old > 0x7fffffffu ? 0x7fffffff : (int)(uint32_t)old;
+    if (!epoch_install(m.queue, m.epoch)) break;
+  }
+  report(m.pf.err, GDN_DEV_ERR_TIMEOUT);
+  return -1;
+}
+
+// The decode walk from item `first`: warps 0-8 as in the decode kernel (the
+// producer lane taking the items), the other warps idle.  Returns, to every
+// thread, the first item taken that is not a decode item.
+__device__ __forceinline__ int mixed_decode(const MixedArgs& m, MixedSmem& M, const int first) {
+  using namespace dtma;
+  DecSmem& S = M.dec;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const TmaArgs& a = m.dec;
+  [[maybe_unused]] const int nreq = a.n_items / a.hk;
+  auto is_dec = [&](int item) { return item >= m.n_chain && item < m.n_chain + m.n_dec; };
+  if (tid == 0) init_barriers<DecSmem, kDecStages>(S);
+  __syncthreads();
+  volatile int* abort_flag = &S.abort;
+  if (warp == kCW) {
+    if (lane == 0) {
+      // producer: every item goes through a bundle buffer, so that the
+      // consumers follow the same sequence; an unusable slot's item and the
+      // final non-decode item travel without copies
+      uint32_t n = 0, vk = 0;
+      bool ok = true;
+      int item = first;
+      for (;;) {
+        const bool dec = is_dec(item);
+        int r = 0, hq = 0;
+        int32_t slot = -1;
+        if (dec) {
+          const int d = item - m.n_chain;
+          r = d / a.hk;
+          hq = d % a.hk;
+          slot = a.slot_ids[GDN_G(r, nreq)];
+        }
+        if (*abort_flag) break;
+        if (!dec || slot_class(slot, a.num_slots)) {
+          const int bb = vk & 1;
+          if (!mbar_wait(&S.bempty[bb], ((vk >> 1) & 1) ^ 1)) {
+            ok = false;
+            break;
+          }
+          S.bitem[bb] = item;
+          mbar_arrive(&S.bfull[bb]);
+          ++vk;
+          if (!dec) break;
+        } else {
+          if (!(ok = produce_item<__nv_bfloat16, __nv_bfloat16, kDecStages, false>(a, S, r, hq, slot, vk, n, item)))
+            break;
+        }
+        item = take_item(m);
+      }
+      if (!ok || *abort_flag) producer_drain<DecSmem, kDecStages>(a, S, vk, n);
+    }
+  } else if (warp < kCW) {
+    uint32_t n = 0, vk = 0;
+    for (;;) {
+      const int bb = vk & 1;
+      if (!*abort_flag && !mbar_wait(&S.bfull[bb], (vk >> 1) & 1)) *abort_flag = 1;
+      named_sync(kBarCons, kCons);
+      if (*abort_flag) break;
+      const int item = S.bitem[bb];
+      ++vk;
+      if (!is_dec(item)) {
+        if (tid == 0) M.item = item;
+        break;
+      }
+      const int d = item - m.n_chain, r = d / a.hk, hq = d % a.hk;
+      const int32_t slot = a.slot_ids[GDN_G(r, nreq)];
+      const int cls = slot_class(slot, a.num_slots);
+      if (cls) {
+        consume_skipped<__nv_bfloat16>(a, r, hq, cls);
+        named_sync(kBarCons, kCons);  // every consumer has read the item
+        mbar_arrive(&S.bempty[bb]);
+        continue;
+      }
+      if (!consume_bundle<__nv_bfloat16, __nv_bfloat16, kDecStages, false>(a, S, r, hq, slot, bb, n)) break;
+    }
+    if (*abort_flag && tid == 0) {
+      report(a.err, GDN_DEV_ERR_TIMEOUT);
+      M.item = -1;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    for (int s = 0; s < kDecStages; ++s) {
+      mbar_inval(&S.full[s]);
+      mbar_inval(&S.empty[s]);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_inval(&S.bfull[s]);
+      mbar_inval(&S.bempty[s]);
+    }
+  }
+  const int next = M.item;
+  __syncthreads();
+  return next;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    mixed_kernel(const MixedArgs m, const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
+                 const __grid_constant__ CUtensorMap cmap) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  MixedSmem& M = *reinterpret_cast<MixedSmem*>(smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023));
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int total = m.n_chain + m.n_dec + m.n_hist;
+  const int hv = m.pf.hv;
+  unsigned long long* const chains_done = m.queue + 2;
+  if (warp == 0) umma::tmem_alloc(&M.pf.tmem_base, TM_COLS);
+  if (tid == 0) M.item = take_item(m);
+  umma::fence_before();
+  __syncthreads();
+  umma::fence_after();
+  const uint32_t tmem = M.pf.tmem_base;
+  int item = M.item;
+  __syncthreads();
+  while (item >= 0 && item < total) {
+    if (item < m.n_chain) {
+      const int n = item / hv, h = item % hv;
+      tc32_chain<__nv_bfloat16, false>(m.pf, qmap, omap, cmap, omap, M.pf, tmem, h, n);
+      if (tid == 0) {
+        __threadfence();  // this chain's reads of the old conv history are done
+        epoch_add(chains_done + n, m.epoch);
+        M.item = take_item(m);
+      }
+      __syncthreads();
+      item = M.item;
+    } else if (item < m.n_chain + m.n_dec) {
+      item = mixed_decode(m, M, item);
+    } else {
+      const int k = item - m.n_chain - m.n_dec;
+      const int n = k / (m.hist_groups * m.hist_blocks);
+      const int grp = (k / m.hist_blocks) % m.hist_groups, blk = k % m.hist_blocks;
+      if (tid == 0) {
+        // every chain of continuation n has finished (bounded wait)
+        bool ok = true;
+        const uint64_t t0 = globaltimer_ns();
+        while (epoch_count(*reinterpret_cast<volatile unsigned long long*>(chains_done + n), m.epoch) <
+               (uint32_t)hv) {
+          if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            ok = false;
+            report(m.pf.err, GDN_DEV_ERR_TIMEOUT);
+            break;
+          }
+        }
+        __threadfence();
+        M.ready = ok;
+      }
+      __syncthreads();
+      const int c = blk * kThreads + tid;
+      if (M.ready && c < m.hist.C) pfx::history_channel<__nv_bfloat16, __nv_bfloat16>(m.hist, n, grp, c);
+      __syncthreads();
+      if (tid == 0) M.item = take_item(m);
+      __syncthreads();
+      item = M.item;
+    }
+  }
+  umma::fence_before();
+  __syncthreads();
+  if (warp == 0) umma::tmem_dealloc(tmem, TM_COLS);
+  // the last CTA out returns the queue words to zero
+  if (tid == 0) {
+    __threadfence();
+    const long long done = epoch_add(m.queue + 1, m.epoch);
+    if (done == (long long)gridDim.x - 1) {
+      __threadfence();
+      for (int i = 0; i < 2 + m.pf.n_seq; ++i) m.queue[i] = 0ull;
+    }
+  }
 }
 
 }  // namespace
@@ -898,6 +1177,131 @@ cudaError_t prefill_tc32_launch(const gdn_dims& d, const gdn_pool& pool, const g
     return e;
   return launch_plain(k, dim3((unsigned)a.hv, (unsigned)n_seq), dim3(kThreads), smem, s, dim3(1), a, qmap, omap,
                       cmap, zmap);
+}
+
+// ---------------------------------------------------------------------------
+bool mixed_fused_supported(const gdn_dims& d, const void* qkv, const void* out, const gdn_params& p) {
+  if (!prefill_tc32_supported(d, qkv, out, p) || !decode_tma_supported(d, qkv, p)) return false;
+  const char* e = std::getenv("GDN_MIXED");  // read on every call: "split" for the separate launches
+  return !(e && e[0] == 's');
+}
+
+size_t mixed_fused_queue_bytes(int32_t n_pre) { return sizeof(unsigned long long) * (2 + (size_t)n_pre); }
+
+cudaError_t mixed_fused_launch(const gdn_dims& d, const gdn_pool& pool, const gdn_pool& ckpt, const gdn_params& p,
+                               const int32_t* slot_ids, const int32_t* cu_seqlens, const int64_t* start_pos,
+                               int32_t n_seq, int32_t n_decode, int64_t total, const int32_t* ckpt_ids,
+                               int32_t max_ckpt, int32_t ckpt_block, const void* qkv, const void* av,
+                               const void* bv, void* out, void* queue, uint32_t* dev_err, cudaStream_t s) {
+  static std::atomic<uint32_t> epochs{0};
+  uint32_t epoch = epochs.fetch_add(1) + 1;
+  if (epoch == 0) epoch = epochs.fetch_add(1) + 1;
+  const int32_t n_pre = n_seq - n_decode;
+  MixedArgs m = {};
+  // decode rows: the first n_decode rows of every per-token tensor
+  m.dec.ssm = pool.ssm;
+  m.dec.conv = pool.conv;
+  m.dec.num_slots = pool.num_slots;
+  m.dec.conv_w = p.conv_w;
+  m.dec.A_log = p.A_log;
+  m.dec.dt_bias = p.dt_bias;
+  m.dec.slot_ids = slot_ids;
+  m.dec.qkv = qkv;
+  m.dec.a = av;
+  m.dec.b = bv;
+  m.dec.out = out;
+  m.dec.err = dev_err;
+  m.dec.hk = d.hk;
+  m.dec.hv = d.hv;
+  m.dec.dv = d.dv;
+  m.dec.C = (int32_t)channels(d);
+  m.dec.G = d.hv / d.hk;
+  m.dec.n_items = n_decode * d.hk;
+  // continuations: sequences n_decode .., rows at their absolute offsets
+  const int32_t* pre_ids = slot_ids + n_decode;
+  const int32_t* pre_cu = cu_seqlens + n_decode;
+  const int64_t* pre_sp = start_pos + n_decode;
+  const int32_t* pre_ck = max_ckpt > 0 ? ckpt_ids + (size_t)n_decode * max_ckpt : nullptr;
+  Tc32Args& a = m.pf;
+  a.ssm = pool.ssm;
+  a.num_slots = pool.num_slots;
+  a.ck_ssm = ckpt.ssm;
+  a.ck_num_slots = max_ckpt > 0 ? ckpt.num_slots : 0;
+  a.conv = reinterpret_cast<const __nv_bfloat16*>(pool.conv);
+  a.conv_w = p.conv_w;
+  a.A_log = p.A_log;
+  a.dt_bias = p.dt_bias;
+  a.slot_ids = pre_ids;
+  a.cu_seqlens = pre_cu;
+  a.start_pos = pre_sp;
+  a.n_seq = n_pre;
+  a.total = total;
+  a.ckpt_ids = pre_ck;
+  a.max_ckpt = max_ckpt;
+  a.ckpt_block = ckpt_block;
+  a.a = reinterpret_cast<const __nv_bfloat16*>(av);
+  a.b = reinterpret_cast<const __nv_bfloat16*>(bv);
+  a.out = reinterpret_cast<__nv_bfloat16*>(out);
+  a.err = dev_err;
+  a.hk = d.hk;
+  a.hv = d.hv;
+  a.C = (int32_t)channels(d);
+  a.G = d.hv / d.hk;
+  a.norm_w = nullptr;
+  a.eps = 0.f;
+  pfx::PrefillArgs& hq = m.hist;
+  hq.ssm = pool.ssm;
+  hq.conv = pool.conv;
+  hq.num_slots = pool.num_slots;
+  hq.ck_ssm = ckpt.ssm;
+  hq.ck_conv = ckpt.conv;
+  hq.ck_num_slots = a.ck_num_slots;
+  hq.conv_w = p.conv_w;
+  hq.A_log = p.A_log;
+  hq.dt_bias = p.dt_bias;
+  hq.slot_ids = pre_ids;
+  hq.cu_seqlens = pre_cu;
+  hq.start_pos = pre_sp;
+  hq.n_seq = n_pre;
+  hq.total = total;
+  hq.ckpt_ids = pre_ck;
+  hq.max_ckpt = max_ckpt;
+  hq.ckpt_block = ckpt_block;
+  hq.qkv = qkv;
+  hq.a = av;
+  hq.b = bv;
+  hq.out = out;
+  hq.err = dev_err;
+  hq.hk = d.hk;
+  hq.hv = d.hv;
+  hq.dk = d.dk;
+  hq.dv = d.dv;
+  hq.W = d.conv_width;
+  hq.C = (int32_t)channels(d);
+  hq.G = d.hv / d.hk;
+  m.queue = reinterpret_cast<unsigned long long*>(queue);
+  m.epoch = epoch;
+  m.n_chain = n_pre * d.hv;
+  m.n_dec = n_decode * d.hk;
+  m.hist_blocks = (hq.C + kThreads - 1) / kThreads;
+  m.hist_groups = max_ckpt > pfx::kCkGroup ? (max_ckpt + pfx::kCkGroup - 1) / pfx::kCkGroup : 1;
+  m.n_hist = n_pre * m.hist_groups * m.hist_blocks;
+  const size_t smem = sizeof(MixedSmem) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(mixed_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  CUtensorMap qmap, omap, cmap;
+  if ((e = tensor_map_2d(&qmap, qkv, total, a.C, 2, kD, kRawRows, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
+    return e;
+  if ((e = tensor_map_2d(&omap, out, total, (int64_t)a.hv * kD, 2, kD, kC, CU_TENSOR_MAP_SWIZZLE_NONE)) !=
+      cudaSuccess)
+    return e;
+  const bool has_ck = a.ck_ssm != nullptr && a.ck_num_slots > 0;
+  if ((e = tensor_map_2d(&cmap, has_ck ? a.ck_ssm : a.ssm, (int64_t)(has_ck ? a.ck_num_slots : a.num_slots) * a.hv * kD,
+                         kD, 4, 32, kD, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+    return e;
+  const int64_t items = (int64_t)m.n_chain + m.n_dec + m.n_hist;
+  const int grid = (int)(items < sm_count() ? items : sm_count());
+  return launch_plain(mixed_kernel, dim3((unsigned)grid), dim3(kThreads), smem, s, dim3(1), m, qmap, omap, cmap);
 }
 
 }  // namespace gdn

@@ -30,6 +30,7 @@
 
 #include <cstddef>
 #include <cstdlib>
+#include <type_traits>
 #include "decode_tma.cuh"
 
 namespace gdn {
@@ -344,16 +345,21 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
     }
     named_sync(kBarCons, kCons);
 
-    for (int c = 0; c < nchunks; ++c, ++n) {
-      const int st = n % STAGES;
-      if (!*abort_flag && !mbar_wait(&S.full[st], (n / STAGES) & 1)) *abort_flag = 1;
-      if (*abort_flag) continue;
-      const int row = GDN_S(c * kRows + rloc, kMaxR);  // row within the segment
-      float4 s4[4];
-      const float* srow = S.ring[GDN_S(st, STAGES)] + GDN_S(rloc, kRows) * kDK;
+    // NR = 1 or 2 stages at once: with two, each lane carries a row of each
+    // through the drafts, so every draft's k^, q^ (and KDA alpha) slices are
+    // loaded once for both rows and the two rows' reductions overlap
+    auto rows_step = [&](auto nr_c, int c, const int (&st)[2]) {
+      constexpr int NR = decltype(nr_c)::value;
+      int row[NR];
+      float4 s4[NR][4];
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc)
-        s4[cc] = *reinterpret_cast<const float4*>(srow + GDN_S(cc * 4 * kLPR + seg * 4, kDK - 3));
+      for (int j = 0; j < NR; ++j) {
+        row[j] = GDN_S((c + j) * kRows + rloc, kMaxR);  // row within the segment
+        const float* srow = S.ring[GDN_S(st[j], STAGES)] + GDN_S(rloc, kRows) * kDK;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+          s4[j][cc] = *reinterpret_cast<const float4*>(srow + GDN_S(cc * 4 * kLPR + seg * 4, kDK - 3));
+      }
       for (int t0 = 0; t0 < T; ++t0) {
         const int t = GDN_S(t0, MT);
         const float kq = S.snorm[t][2];
@@ -365,45 +371,73 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
           kk[cc] = *reinterpret_cast<const float4*>(&S.sy[t][kDK + col]);
           qq[cc] = *reinterpret_cast<const float4*>(&S.sy[t][col]);
           if constexpr (KDA) {
-            // the row becomes St diag(alpha) before its products
+            // the rows become St diag(alpha) before their products
             const float4 al = *reinterpret_cast<const float4*>(&S.sal[t][col]);
-            s4[cc] = join4(mul2(lo2(s4[cc]), lo2(al)), mul2(hi2(s4[cc]), hi2(al)));
+#pragma unroll
+            for (int j = 0; j < NR; ++j)
+              s4[j][cc] = join4(mul2(lo2(s4[j][cc]), lo2(al)), mul2(hi2(s4[j][cc]), hi2(al)));
           }
         }
-        // the row's dot products with k^ and q^, on packed fp32 pairs
-        float2 dk2 = make_float2(0.f, 0.f), dq2 = make_float2(0.f, 0.f);
+        // each row's dot products with k^ and q^, on packed fp32 pairs
+        float dk_[NR], dq_[NR];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          dk2 = fma2(hi2(s4[cc]), hi2(kk[cc]), fma2(lo2(s4[cc]), lo2(kk[cc]), dk2));
-          dq2 = fma2(hi2(s4[cc]), hi2(qq[cc]), fma2(lo2(s4[cc]), lo2(qq[cc]), dq2));
-        }
-        float dk_ = dk2.x + dk2.y, dq_ = dq2.x + dq2.y;
+        for (int j = 0; j < NR; ++j) {
+          float2 dk2 = make_float2(0.f, 0.f), dq2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int o = kLPR / 2; o; o >>= 1) {
-          dk_ += __shfl_xor_sync(0xffffffffu, dk_, o);
-          dq_ += __shfl_xor_sync(0xffffffffu, dq_, o);
+          for (int cc = 0; cc < 4; ++cc) {
+            dk2 = fma2(hi2(s4[j][cc]), hi2(kk[cc]), fma2(lo2(s4[j][cc]), lo2(kk[cc]), dk2));
+            dq2 = fma2(hi2(s4[j][cc]), hi2(qq[cc]), fma2(lo2(s4[j][cc]), lo2(qq[cc]), dq2));
+          }
+          dk_[j] = dk2.x + dk2.y;
+          dq_[j] = dq2.x + dq2.y;
         }
-        // KDA: alpha is 1 here (the rows carry the per-channel decay already)
-        const float bu = beta * (S.sy[t][GDN_S(2 * kDK + row, kMaxCh)] - alpha * dk_);
-        const float2 bu2 = make_float2(bu, bu), al2 = make_float2(alpha, alpha);
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          const float2 lo = KDA ? lo2(s4[cc]) : mul2(al2, lo2(s4[cc]));
-          const float2 hi = KDA ? hi2(s4[cc]) : mul2(al2, hi2(s4[cc]));
-          s4[cc] = join4(fma2(bu2, lo2(kk[cc]), lo), fma2(bu2, hi2(kk[cc]), hi));
-        }
+        for (int o = kLPR / 2; o; o >>= 1)
+#pragma unroll
+          for (int j = 0; j < NR; ++j) {
+            dk_[j] += __shfl_xor_sync(0xffffffffu, dk_[j], o);
+            dq_[j] += __shfl_xor_sync(0xffffffffu, dq_[j], o);
+          }
         const int32_t sid = sid_of(t);
-        if (slot_class(sid, a.spec_num_slots) == 0) {
-          float4* const spec4 = reinterpret_cast<float4*>(a.spec_ssm);
-          const size_t drow4 = (((size_t)sid * a.hv + h) * a.dv + (size_t)row0 + row) * kDK / 4;
+        const bool keep = slot_class(sid, a.spec_num_slots) == 0;
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc)
-            st_stream(spec4 + GDN_G(drow4 + (cc * 4 * kLPR + seg * 4) / 4, spec_ssm_n / 4), s4[cc]);
+        for (int j = 0; j < NR; ++j) {
+          // KDA: alpha is 1 here (the rows carry the per-channel decay already)
+          const float bu = beta * (S.sy[t][GDN_S(2 * kDK + row[j], kMaxCh)] - alpha * dk_[j]);
+          const float2 bu2 = make_float2(bu, bu), al2 = make_float2(alpha, alpha);
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            const float2 lo = KDA ? lo2(s4[j][cc]) : mul2(al2, lo2(s4[j][cc]));
+            const float2 hi = KDA ? hi2(s4[j][cc]) : mul2(al2, hi2(s4[j][cc]));
+            s4[j][cc] = join4(fma2(bu2, lo2(kk[cc]), lo), fma2(bu2, hi2(kk[cc]), hi));
+          }
+          if (keep) {
+            float4* const spec4 = reinterpret_cast<float4*>(a.spec_ssm);
+            const size_t drow4 = (((size_t)sid * a.hv + h) * a.dv + (size_t)row0 + row[j]) * kDK / 4;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)
+              st_stream(spec4 + GDN_G(drow4 + (cc * 4 * kLPR + seg * 4) / 4, spec_ssm_n / 4), s4[j][cc]);
+          }
+          if (seg == 0) S.so[t][row[j]] = fmaf(bu, kq, alpha * dq_[j]);
         }
-        if (seg == 0) S.so[t][row] = fmaf(bu, kq, alpha * dq_);
       }
-      __syncwarp();  // the whole warp is done with its rows of the stage
-      if (lane == 0) mbar_arrive(&S.empty[st]);
+    };
+    for (int c = 0; c < nchunks;) {
+      const int nr = c + 1 < nchunks ? 2 : 1;
+      const int st[2] = {(int)(n % STAGES), (int)((n + 1) % STAGES)};
+      for (int j = 0; j < nr; ++j)
+        if (!*abort_flag && !mbar_wait(&S.full[st[j]], ((n + j) / STAGES) & 1)) *abort_flag = 1;
+      if (!*abort_flag) {
+        if (nr == 2)
+          rows_step(std::integral_constant<int, 2>{}, c, st);
+        else
+          rows_step(std::integral_constant<int, 1>{}, c, st);
+        __syncwarp();  // the whole warp is done with its rows of the stages
+        if (lane == 0)
+          for (int j = 0; j < nr; ++j) mbar_arrive(&S.empty[st[j]]);
+      }
+      c += nr;
+      n += nr;
     }
     named_sync(kBarCons, kCons);
     if (*abort_flag) break;
@@ -435,9 +469,14 @@ cudaError_t launch_v(const VArgs& a, cudaStream_t s) {
 
 template <typename Tact, typename Tconv, bool KDA>
 cudaError_t launch_v_dt(const VArgs& a, cudaStream_t s) {
-  // the two-CTA layout only where two fit on an SM (not KDA with fp32 activations)
-  constexpr bool kTwoFit = 2 * (sizeof(VSmem<Tact, Tconv, 3, 8, KDA>) + 1024) <= 228 * 1024;
-  if (kTwoFit && a.T <= 8 && tma_ctas_per_sm() != 1) return launch_v<Tact, Tconv, 3, 8, 2, KDA>(a, s);
+  // the two-CTA layout only where two fit on an SM, with a 4-stage ring (two
+  // stages consumed at once, two filling) where that fits, else 3 stages
+  constexpr bool kFit4 = 2 * (sizeof(VSmem<Tact, Tconv, 4, 8, KDA>) + 1024) <= 228 * 1024;
+  constexpr bool kFit3 = 2 * (sizeof(VSmem<Tact, Tconv, 3, 8, KDA>) + 1024) <= 228 * 1024;
+  if (a.T <= 8 && tma_ctas_per_sm() != 1) {
+    if (kFit4) return launch_v<Tact, Tconv, 4, 8, 2, KDA>(a, s);
+    if (kFit3) return launch_v<Tact, Tconv, 3, 8, 2, KDA>(a, s);
+  }
   return launch_v<Tact, Tconv, 4, kMaxT, 1, KDA>(a, s);
 }
 

@@ -301,9 +301,20 @@ gdn_status gdn_chunk_prefill_noalloc(const gdn_dims* dims, gdn_pool pool,
  * size gdn_chunk_prefill_workspace_size(dims, n_seq, total_tokens) suffices.
  * 0 <= n_decode <= min(n_seq, total_tokens), else GDN_ERR_INVALID_ARG.  Slot
  * ids must be distinct across the whole batch (precondition).  One call, on
- * one stream, with no host synchronisation: the decode rows go to the decode
- * kernel and the continuations to the chunked prefill, each at its own
- * roofline.
+ * one stream, with no host synchronisation.  Where both halves take their
+ * fast paths (dk = dv = 128, conv width 4, bf16 activations and history,
+ * 16-byte aligned qkv, out and conv weights, G * dv <= 256) and there are
+ * both decode requests and continuations, the whole batch is ONE launch: a
+ * persistent kernel whose work queue holds the continuations' chains, the
+ * decode requests and the continuations' conv histories; it keeps that queue
+ * in the first 8 * (2 + n_seq - n_decode) bytes of the workspace (8-byte
+ * aligned; left zero after the call, and nothing in it needs to be zero
+ * before), so workspace may be smaller than the prefill's size there but not
+ * smaller than that.  Otherwise the decode rows go to the decode kernel and
+ * the continuations to the chunked prefill (up to three launches).  Both give
+ * the same bits as gdn_decode_step and gdn_chunk_prefill called one after
+ * the other.  GDN_MIXED=split (read on every call) forces the separate
+ * launches.
  */
 gdn_status gdn_mixed_step(const gdn_dims* dims, gdn_pool pool, gdn_pool ckpt,
                           const gdn_params* params, const int32_t* slot_ids,
@@ -413,7 +424,8 @@ const char* gdn_status_string(int32_t status);
 #define GDN_K_KDA_DECODE 9
 #define GDN_K_KDA_VERIFY 10
 #define GDN_K_KDA_PREFILL 11 /* the recurrence and its conv-history kernel */
-#define GDN_K_COUNT 12
+#define GDN_K_MIXED 12       /* the single-launch mixed step */
+#define GDN_K_COUNT 13
 uint64_t gdn_launch_count(int32_t kernel);
 void gdn_launch_count_reset(void);
 

@@ -109,10 +109,22 @@ def test_mixed_step_vs_oracle(cuda, shape, n_dec, lens, starts):
     assert torch.equal(st.pool.ssm[rest].cpu(), torch.from_numpy(st.opool.ssm[rest]).float())
 
 
+def _one_launch(shape, n_dec, lens):
+    """Whether the mixed step is one launch for this batch (both halves on
+    their fast paths: the Qwen3.5 shape, the decode step's TMA-fed kernel from
+    3 requests up, continuations present)."""
+    return shape is synth.QWEN and n_dec >= 3 and len(lens) > 0
+
+
+@pytest.mark.parametrize("form", ["one_launch", "split"])
 @pytest.mark.parametrize("shape,n_dec,lens,starts", CASES, ids=IDS)
-def test_mixed_step_equals_separate_calls(cuda, shape, n_dec, lens, starts):
+def test_mixed_step_equals_separate_calls(cuda, monkeypatch, form, shape, n_dec, lens, starts):
     """Bit for bit the decode step on the decode rows and the chunked prefill on
-    the rest, called one after the other."""
+    the rest, called one after the other: as one launch where the batch allows
+    it, and as separate launches (GDN_MIXED=split)."""
+    if form == "split":
+        monkeypatch.setenv("GDN_MIXED", "split")
+    fused = form == "one_launch" and _one_launch(shape, n_dec, lens)
     n_slots = 16 if shape is synth.TINY else max(24, n_dec + len(lens) + 4)
     st = Setup(shape, seed=51, num_slots=n_slots)
     ids, cu, sp, ck_ids, n_ck, qkv, a, b = _batch(st, n_dec, lens, starts, n_slots)
@@ -123,10 +135,13 @@ def test_mixed_step_equals_separate_calls(cuda, shape, n_dec, lens, starts):
     out1 = torch.zeros((total, shape.hv, shape.dv), dtype=shape.act_dtype, device="cuda")
     out2 = torch.zeros_like(out1)
     ws = _workspace(st.dims, n, total)
-    n_dec0 = gdn.launch_count(gdn.K_DECODE)
+    n_dec0, n_mix0 = gdn.launch_count(gdn.K_DECODE), gdn.launch_count(gdn.K_MIXED)
     gdn.mixed_step(st.dims, st.pool, ck1, st.params, ids.cuda(), cu.cuda(), sp.cuda(), total, n_dec,
                    ck_ids.cuda(), BLK, q, av, bv, out1, ws)
-    assert gdn.launch_count(gdn.K_DECODE) == n_dec0 + (1 if n_dec else 0)
+    assert gdn.launch_count(gdn.K_MIXED) == n_mix0 + (1 if fused else 0)
+    assert gdn.launch_count(gdn.K_DECODE) == n_dec0 + (1 if n_dec and not fused else 0)
+    if fused:  # the work queue is left zero in the workspace
+        assert not torch.any(ws[:8 * (2 + len(lens))])
     if n_dec:
         gdn.decode_step(st.dims, pool2, st.params, ids[:n_dec].cuda(), q[:n_dec], av[:n_dec], bv[:n_dec],
                         out2[:n_dec])
@@ -152,3 +167,74 @@ def test_mixed_step_bad_arguments(cuda):
     with pytest.raises(gdn.GdnError) as e:
         gdn.mixed_step(st.dims, st.pool, ck, st.params, ids, cu, sp, 5, 4, None, BLK, qkv, a, b, out, ws)
     assert e.value.status == gdn.binding.ERR_INVALID_ARG
+
+
+def test_mixed_one_launch_with_padding_and_bad_ids_matches_split(cuda, monkeypatch):
+    """Padding (-1) and out-of-range ids among the decode requests and the
+    continuations: the one-launch step writes the same bits (zero rows for the
+    skipped requests, untouched slots) and the same error bits as the
+    separate launches."""
+    shape = synth.QWEN
+    n_slots = 24
+    st = Setup(shape, seed=53, num_slots=n_slots)
+    n_dec, lens, starts = 8, [70, 129, 40], [63, 4100, 7]
+    ids, cu, sp, ck_ids, n_ck, qkv, a, b = _batch(st, n_dec, lens, starts, n_slots)
+    ids[2], ids[5], ids[n_dec + 1] = -1, n_slots + 3, -1
+    n, total = ids.shape[0], int(cu[-1])
+    q, av, bv = qkv.cuda(), a.cuda(), b.cuda()
+    res = []
+    for form in ("one_launch", "split"):
+        if form == "split":
+            monkeypatch.setenv("GDN_MIXED", "split")
+        pool = StatePool(st.pool.ssm.clone(), st.pool.conv.clone())
+        ck = _ck_pool(st, n_ck)
+        out = torch.full((total, shape.hv, shape.dv), 3.0, dtype=shape.act_dtype, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        n_mix0 = gdn.launch_count(gdn.K_MIXED)
+        gdn.mixed_step(st.dims, pool, ck, st.params, ids.cuda(), cu.cuda(), sp.cuda(), total, n_dec,
+                       ck_ids.cuda(), BLK, q, av, bv, out, _workspace(st.dims, n, total), err)
+        torch.cuda.synchronize()
+        assert gdn.launch_count(gdn.K_MIXED) == n_mix0 + (1 if form == "one_launch" else 0)
+        res.append((out, pool, ck, err))
+    (o1, p1, c1, e1), (o2, p2, c2, e2) = res
+    assert int(e1.item()) == int(e2.item()) == gdn.DEV_ERR_SLOT_OOB
+    assert torch.equal(o1, o2)
+    assert torch.equal(p1.ssm, p2.ssm) and torch.equal(p1.conv, p2.conv)
+    assert torch.equal(c1.ssm, c2.ssm) and torch.equal(c1.conv, c2.conv)
+    assert torch.all(o1[2] == 0) and torch.all(o1[5] == 0)
+
+
+def test_mixed_one_launch_replayed_from_a_cuda_graph(cuda):
+    """The one-launch step captured in a CUDA graph and replayed twice gives the
+    bits of two eager calls: its work queue starts afresh on every replay
+    (the launch leaves it zero)."""
+    shape = synth.QWEN
+    n_slots = 24
+    st = Setup(shape, seed=54, num_slots=n_slots)
+    n_dec, lens, starts = 6, [100, 64], [30, 512]
+    ids, cu, sp, ck_ids, n_ck, qkv, a, b = _batch(st, n_dec, lens, starts, n_slots)
+    n, total = ids.shape[0], int(cu[-1])
+    args = (ids.cuda(), cu.cuda(), sp.cuda(), total, n_dec, ck_ids.cuda(), BLK, qkv.cuda(), a.cuda(), b.cuda())
+    ws = _workspace(st.dims, n, total)
+    eager = StatePool(st.pool.ssm.clone(), st.pool.conv.clone())
+    ck_e = _ck_pool(st, n_ck)
+    out_e = torch.zeros((total, shape.hv, shape.dv), dtype=shape.act_dtype, device="cuda")
+    for _ in range(2):
+        gdn.mixed_step(st.dims, eager, ck_e, st.params, *args, out_e, ws)
+    graph = StatePool(st.pool.ssm.clone(), st.pool.conv.clone())
+    ck_g = _ck_pool(st, n_ck)
+    out_g = torch.zeros_like(out_e)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            gdn.mixed_step(st.dims, graph, ck_g, st.params, *args, out_g, ws)
+    torch.cuda.current_stream().wait_stream(s)
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out_g, out_e)
+    assert torch.equal(graph.ssm, eager.ssm) and torch.equal(graph.conv, eager.conv)
+    assert torch.equal(ck_g.ssm, ck_e.ssm) and torch.equal(ck_g.conv, ck_e.conv)
+    assert not torch.any(ws[:8 * (2 + len(lens))])
