@@ -70,12 +70,12 @@ constexpr int kAX = 68;                // row stride (floats) of the solve's A a
 // TMEM columns (fp32, one per column).  Lanes are dv rows, except P, whose
 // lanes are the [Y_K;Y_Q] rows.
 constexpr uint32_t TM_S = 0;     // S^T [dv][dk], 128 columns
-constexpr uint32_t TM_P = 128;   // P [128 rows][128]; after the extraction, E and O1:
-constexpr uint32_t TM_E = 128;   //   S^T Y_K^T [dv][64]
-constexpr uint32_t TM_O1 = 192;  //   S^T Y_Q^T [dv][64]
-constexpr uint32_t TM_DL = 256;  // Delta'^T [dv][64]
-constexpr uint32_t TM_O2 = 320;  // Delta'^T M'^T [dv][64]
-constexpr uint32_t TM_V = 384;   // V^T [dv][64] (operand)
+constexpr uint32_t TM_P = 128;   // P [128 rows][128]
+constexpr uint32_t TM_E = 256;   // S^T Y_K^T [dv][64]
+constexpr uint32_t TM_O1 = 320;  // S^T Y_Q^T [dv][64]
+constexpr uint32_t TM_DL = 384;  // Delta'^T [dv][64]
+constexpr uint32_t TM_V = 448;   // V^T [dv][64] (operand); then O2:
+constexpr uint32_t TM_O2 = 448;  //   Delta'^T M'^T [dv][64] (V read by then)
 constexpr uint32_t TM_COLS = 512;
 
 struct Tc32Args {
@@ -126,7 +126,7 @@ struct __align__(1024) Smem32 {
   float rk[kC];  // 1 / sqrt(|y_k|^2 + eps) per token
   float rq[kC];  // dk^-1/2 / sqrt(|y_q|^2 + eps) per token
   __nv_bfloat16 zt[kC][kD];  // the fused epilogue's z rows of the chunk (EPI)
-  uint64_t ld_bar, mma_bar, z_bar;
+  uint64_t ld_bar, mma_bar, z_bar, eo_bar;
   uint32_t tmem_base;
 };
 
@@ -150,16 +150,52 @@ __device__ __forceinline__ float silu_fast(float y) { return __fdividef(y, 1.f +
 // element (r, c) of the solve's 64 x 64 fp32 matrices A and X
 __device__ __forceinline__ int ix(int r, int c) { return r * kAX + c; }
 
+// ---- warp-level tf32 products with fp32 accuracy -------------------------------
+// mma m16n8k8 (row.col, fp32 accumulate).  Lane = 4 g + q: A holds (g, q),
+// (g + 8, q), (g, q + 4), (g + 8, q + 4); B holds (q, g), (q + 4, g); C and D
+// hold (g, 2q), (g, 2q + 1), (g + 8, 2q), (g + 8, 2q + 1).  Each operand is
+// split x = hi + lo, both tf32 rounded to nearest, and a product is the three
+// products hi hi + hi lo + lo hi: the lo lo term lies below fp32's rounding,
+// so the sum carries an fp32 product.
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+  hi = __float_as_uint(umma::tf32_round(x));
+  lo = __float_as_uint(umma::tf32_round(x - __uint_as_float(hi)));
+}
+__device__ __forceinline__ void mma_m16n8k8(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// one k-step D += L R: L (16 x 8) element (r, k) from la(r, k0 + k), R (8 x 8)
+// element (k, c) from lb(k0 + k, c)
+template <class LA, class LB>
+__device__ __forceinline__ void step3(float (&d)[4], int k0, LA la, LB lb) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+  const float a[4] = {la(g, k0 + q), la(g + 8, k0 + q), la(g, k0 + q + 4), la(g + 8, k0 + q + 4)};
+  const float b[2] = {lb(k0 + q, g), lb(k0 + q + 4, g)};
+  uint32_t ah[4], al[4], bh[2], bl[2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) split_tf32(a[i], ah[i], al[i]);
+  split_tf32(b[0], bh[0], bl[0]);
+  split_tf32(b[1], bh[1], bl[1]);
+  mma_m16n8k8(d, al, bh[0], bh[1]);
+  mma_m16n8k8(d, ah, bl[0], bl[1]);
+  mma_m16n8k8(d, ah, bh[0], bh[1]);
+}
+
 // ---- the 64 x 64 solve ---------------------------------------------------------
 // X = (I + A)^-1 for the strictly lower 64 x 64 A (fp32, rows kAX apart),
-// blockwise: the eight 8 x 8 diagonal blocks by substitution, then merged
-// 8 -> 16 -> 32 -> 64 with X_ba = -X_b (A_ba X_a).  fp32 on the CUDA cores;
-// every entry of X above the diagonal is zero (X is cleared first), so the
-// sums run over whole rows and columns.  Each entry of X is written out as
-// T1 = rk_i X_ij beta_j and T2 = -rk_i X_ij beta_j e^{b_j} rk_j (tf32).
-// Y: 1024 floats of scratch, L0: 8 x 3 x 64.  512 threads (warps 8..15 wait
-// at the first barrier while warps 0..7 invert the diagonal blocks); the
-// caller synchronises before (A complete, X cleared) and after.
+// blockwise: the eight 8 x 8 diagonal blocks by substitution on the CUDA
+// cores, then merged 8 -> 16 -> 32 -> 64 with X_ba = -X_b (A_ba X_a) on
+// fp32-accurate warp-level tensor-core products; every entry of X above the
+// diagonal is zero (X is cleared first), so the sums run over whole rows and
+// columns.  Each entry of X is written out as T1 = rk_i X_ij beta_j and
+// T2 = -rk_i X_ij beta_j e^{b_j} rk_j (tf32).  Y: 2048 floats of scratch,
+// L0: 8 x 3 x 64.  512 threads (warps 8..15 wait at the first barrier while
+// warps 0..7 invert the diagonal blocks; named barriers 2..5 in the last
+// merge); the caller synchronises before (A complete, X cleared) and after.
 struct TOut {
   uint8_t* t1;
   uint8_t* t2;
@@ -227,6 +263,8 @@ __device__ __forceinline__ void solve_T(const float* A_, float* X_, float* Y_, f
     if (j + 1 <= i) put_t(to, o + i, o + j + 1, x1);
   }
   __syncthreads();
+  // 8 -> 16 and 16 -> 32 on the CUDA cores (the tensor-core form measured
+  // slower at these sizes: each product is a short chain of dependent steps)
   // 8 -> 16: pair p (rows 16p + 8 .., columns 16p ..), entry (i, j) per thread
   {
     const int p = (tid >> 6) & 3, i = (tid >> 3) & 7, j = tid & 7, o = 16 * p;
@@ -261,45 +299,40 @@ __device__ __forceinline__ void solve_T(const float* A_, float* X_, float* Y_, f
     put_t(to, o + 16 + i, o + j, -x);
   }
   __syncthreads();
-  // 32 -> 64: rows 32 + 2w, 32 + 2w + 1, column `lane`
-  {
-    float y[2] = {0.f, 0.f};
+  // 32 -> 64 on fp32-accurate warp-level tensor-core products (step3): a
+  // warp carries one column tile j of X_ba through both products, since column
+  // tile j of X_ba needs only column tile j of Y = A_ba X_a.
+  const int g = lane >> 2, q = lane & 3;
+  // 32 -> 64: warps 0..7 = (column tile j = warp % 4, row half mh = warp / 4);
+  // the two warps of a column tile share Y[:, 8j ..] through a named barrier.
+  // k-steps whose X_a rows lie above the tile's columns (s < j), or whose
+  // X_b columns lie right of the warp's rows (s > 2 mh + 1), are zero.
+  if (warp < 8) {
+    const int j = warp & 3, mh = warp >> 2;
+    const auto Ys = Y + (1024 + j * 256);  // Y[:, 8j ..] [32][8]
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int k4 = 0; k4 < 8; ++k4) {
-      float4 a[2];
+    for (int s = 0; s < 4; ++s)
+      if (s >= j)
+        step3(d, 8 * s, [&](int r, int k) { return A[ix(32 + 16 * mh + r, k)]; },
+              [&](int k, int c) { return X[ix(k, 8 * j + c)]; });
+    const int yr = 16 * mh + g;
+    Ys[yr * 8 + 2 * q] = d[0];
+    Ys[yr * 8 + 2 * q + 1] = d[1];
+    Ys[(yr + 8) * 8 + 2 * q] = d[2];
+    Ys[(yr + 8) * 8 + 2 * q + 1] = d[3];
+    named_sync(2 + j, 64);
+    float e[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int r = 0; r < 2; ++r) a[r] = vec_at<const float4>(A, ix(32 + 2 * warp + r, 4 * k4));
-      const float x0 = X[ix(4 * k4, lane)], x1 = X[ix(4 * k4 + 1, lane)], x2 = X[ix(4 * k4 + 2, lane)],
-                  x3 = X[ix(4 * k4 + 3, lane)];
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        y[r] = fmaf(a[r].x, x0, y[r]);
-        y[r] = fmaf(a[r].y, x1, y[r]);
-        y[r] = fmaf(a[r].z, x2, y[r]);
-        y[r] = fmaf(a[r].w, x3, y[r]);
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < 2; ++r) Y[32 * (2 * warp + r) + lane] = y[r];
-    __syncthreads();
-    float x[2] = {0.f, 0.f};
-#pragma unroll
-    for (int k4 = 0; k4 < 8; ++k4) {
-      float4 xb[2];
-#pragma unroll
-      for (int r = 0; r < 2; ++r) xb[r] = vec_at<const float4>(X, ix(32 + 2 * warp + r, 32 + 4 * k4));
-      const float y0 = Y[32 * (4 * k4) + lane], y1 = Y[32 * (4 * k4 + 1) + lane], y2 = Y[32 * (4 * k4 + 2) + lane],
-                  y3 = Y[32 * (4 * k4 + 3) + lane];
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        x[r] = fmaf(xb[r].x, y0, x[r]);
-        x[r] = fmaf(xb[r].y, y1, x[r]);
-        x[r] = fmaf(xb[r].z, y2, x[r]);
-        x[r] = fmaf(xb[r].w, y3, x[r]);
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < 2; ++r) put_t(to, 32 + 2 * warp + r, lane, -x[r]);
+    for (int s = 0; s < 4; ++s)
+      if (s <= 2 * mh + 1)
+        step3(e, 8 * s, [&](int r, int k) { return X[ix(32 + 16 * mh + r, 32 + k)]; },
+              [&](int k, int c) { return Ys[k * 8 + c]; });
+    const int cc = 8 * j + 2 * q;
+    put_t(to, 32 + yr, cc, -e[0]);
+    put_t(to, 32 + yr, cc + 1, -e[1]);
+    put_t(to, 40 + yr, cc, -e[2]);
+    put_t(to, 40 + yr, cc + 1, -e[3]);
   }
 }
 
@@ -340,6 +373,7 @@ __device__ __forceinline__ void tc32_chain(const Tc32Args& a, const CUtensorMap&
     mbar_init(&S.ld_bar, 1);
     mbar_init(&S.mma_bar, 1);
     mbar_init(&S.z_bar, 1);
+    mbar_init(&S.eo_bar, 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -354,7 +388,8 @@ __device__ __forceinline__ void tc32_chain(const Tc32Args& a, const CUtensorMap&
   static_assert(4 * 16384 <= sizeof(Smem32::kq) && 2 * 16384 <= sizeof(Smem32::kt), "operand tiles");
   static_assert(2 * 8192 <= sizeof(Smem32::tm) && 2 * 8192 <= sizeof(Smem32::t2) && 2 * 8192 <= sizeof(Smem32::mq),
                 "operand tiles");
-  static_assert(TM_V + 64 <= TM_COLS && TM_O2 + 64 <= TM_V && TM_DL + 64 <= TM_O2 && TM_O1 + 64 <= TM_DL,
+  static_assert(TM_P == TM_S + 128 && TM_E == TM_P + 128 && TM_O1 == TM_E + 64 && TM_DL == TM_O1 + 64 &&
+                    TM_V == TM_DL + 64 && TM_V + 64 <= TM_COLS && TM_O2 == TM_V,
                 "TMEM regions");
 
   // feature channels of this thread: the q/k channel pair (2 cp, 2 cp + 1)
@@ -490,6 +525,7 @@ __device__ __forceinline__ void tc32_chain(const Tc32Args& a, const CUtensorMap&
     return ok;
   };
 
+  bool eo_pending = false;  // [E | O1] of chunk c issued and not yet waited for
   int c = 0;
   for (; c < nch; ++c) {
     const int64_t P = (p0 / kC + c) * kC;
@@ -668,6 +704,21 @@ __device__ __forceinline__ void tc32_chain(const Tc32Args& a, const CUtensorMap&
     __syncthreads();
     // the next chunk's gates (warps 8, 9) beside the solve's diagonal blocks
     if (c + 1 < nch && (warp == 8 || warp == 9)) gates_into(c + 1, gbuf ^ 1);
+    // [E | O1] = S^T [Y_K;Y_Q]^T: the state entering the chunk (final since
+    // the previous chunk's update completed) meets the chunk's keys and
+    // queries on the tensor core during the solve.  Issued by a lane of warp
+    // 10, idle in the solve's first phase: a thread issuing products waits
+    // for the tensor core to take them, about as long as they run.
+    eo_pending = true;
+    if (warp == 10 && lane == 0) {
+      umma::fence_after();
+      const uint64_t dkq = umma::desc(smem_addr(S.kq), 16, 1024);
+#pragma unroll
+      for (int s = 0; s < 16; ++s)
+        umma::mma_tf32_ta(tmem + TM_E, tmem + TM_S + 8 * s, umma::adv(dkq, (s >> 2) * 16384 + (s & 3) * 32),
+                          ID_N128, s > 0);
+      umma::commit(&S.eo_bar);
+    }
     solve_T(S.sv.A, S.sv.X, S.sv.Y, S.sv.L0, TOut{S.tm, S.t2, gbeta, geb, S.rk});
     umma::fence_proxy_async();
     __syncthreads();
@@ -676,25 +727,19 @@ __device__ __forceinline__ void tc32_chain(const Tc32Args& a, const CUtensorMap&
       issue_raw(c + 1);
       ld_issued = c + 2;
     }
-    // ---- Delta'^T = V^T T1^T, and [E | O1] = S^T [Y_K;Y_Q]^T -----------------
+    // E and O1 have long completed (every thread sees it before the state,
+    // which they read, is scaled below)
+    if (!wait_all(&S.eo_bar, c & 1)) break;
+    eo_pending = false;
+    umma::fence_after();
+    // ---- Delta'^T = V^T T1^T + E T2^T (tensor core), S^T <- e^{b_last} S^T --
     if (tid == 0) {
-      umma::fence_after();
       const uint64_t dtm = umma::desc(smem_addr(S.tm), 16, 1024);
-      const uint64_t dkq = umma::desc(smem_addr(S.kq), 16, 1024);
+      const uint64_t dt2 = umma::desc(smem_addr(S.t2), 16, 1024);
 #pragma unroll
       for (int s = 0; s < 8; ++s)
         umma::mma_tf32_ta(tmem + TM_DL, tmem + TM_V + 8 * s, umma::adv(dtm, (s >> 2) * 8192 + (s & 3) * 32), ID_N64,
                           s > 0);
-#pragma unroll
-      for (int s = 0; s < 16; ++s)
-        umma::mma_tf32_ta(tmem + TM_E, tmem + TM_S + 8 * s, umma::adv(dkq, (s >> 2) * 16384 + (s & 3) * 32),
-                          ID_N128, s > 0);
-      umma::commit(&S.mma_bar);
-    }
-    if (!mma_wait()) break;
-    // ---- Delta'^T += E T2^T (tensor core), S^T <- e^{b_last} S^T (threads) ---
-    if (tid == 0) {
-      const uint64_t dt2 = umma::desc(smem_addr(S.t2), 16, 1024);
 #pragma unroll
       for (int s = 0; s < 8; ++s)
         umma::mma_tf32_ta(tmem + TM_DL, tmem + TM_E + 8 * s, umma::adv(dt2, (s >> 2) * 8192 + (s & 3) * 32), ID_N64,
@@ -814,6 +859,7 @@ __device__ __forceinline__ void tc32_chain(const Tc32Args& a, const CUtensorMap&
       report(a.err, GDN_DEV_ERR_TIMEOUT);
       umma::commit(&S.mma_bar);
       mbar_wait(&S.mma_bar, mph);
+      if (eo_pending) mbar_wait(&S.eo_bar, c & 1);
       for (int k = ld_done; k < ld_issued; ++k) mbar_wait(&S.ld_bar, k & 1);
       if (EPI) mbar_wait(&S.z_bar, c & 1);
     }
@@ -832,6 +878,7 @@ __device__ __forceinline__ void tc32_chain(const Tc32Args& a, const CUtensorMap&
     mbar_inval(&S.ld_bar);
     mbar_inval(&S.mma_bar);
     mbar_inval(&S.z_bar);
+    mbar_inval(&S.eo_bar);
   }
 }
 
