@@ -336,6 +336,9 @@ __device__ __forceinline__ float exp_ftz(float x) {
   return y;
 }
 __device__ __forceinline__ float silu_f(float y) { return y / (1.0f + expf(-y)); }
+// the same with the approximate exponential and division (ex2.approx,
+// rcp.approx: a few ulp of fp32), for prologues that run it on every draft
+__device__ __forceinline__ float silu_fast_f(float y) { return __fdividef(y, 1.f + exp_ftz(-y)); }
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
 __device__ __forceinline__ float softplus_f(float x) {
   return x > 20.0f ? x : log1pf(expf(x));

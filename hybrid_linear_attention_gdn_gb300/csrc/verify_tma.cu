@@ -281,7 +281,7 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
         acc = fmaf(w.y, w1, acc);
         acc = fmaf(w.z, w2, acc);
         acc = fmaf(w.w, xv, acc);
-        S.sy[t][i] = silu_f(acc);
+        S.sy[t][i] = silu_fast_f(acc);
         w0 = w1;
         w1 = w2;
         w2 = xv;
