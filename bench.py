@@ -46,11 +46,11 @@ DECODE_STEP_PARAM_BYTES = 8192 * 4 * 4 + 2 * 32 * 4
 
 # ncu DRAM traffic (read + write bytes per launch) of the decode kernel on the
 # headline workload itself (profiles/decode_tma_kernel_b64_pool512_dram.md),
-# with the sha256 of the kernel source it was captured on; reported only while
-# the source is unchanged.
+# with the sha256 of the kernel's sources (DECODE_SOURCES) it was captured on;
+# reported only while they are unchanged.
 DECODE_TRAFFIC = {
-    "bytes_per_launch": 138593024 + 76964864,
-    "source_sha256": "5e61f0355ea21948c588c68cc2ad99a9a58d4a2e91d69b0250e34bab30c41f43",
+    "bytes_per_launch": 138596096 + 76754432,
+    "source_sha256": "42d6dd52e9e6106fe1c06ee851ae482d4de2862e4f71eb27aef542749b838bd3",
     "case": "batch 64 over the 512-slot pool with the headline's 8-set rotation, the sixth launch "
             "(ncu dram__bytes_read.sum + dram__bytes_write.sum, one pass): reads are exactly the algorithmic "
             "138.6 MB; part of the 134 MB of state written is still in L2 when the launch ends and leaves it "
@@ -58,9 +58,18 @@ DECODE_TRAFFIC = {
 }
 
 
-def _sha(path):
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+def _sha(*paths):
+    """sha256 of the files' contents, in order."""
+    h = hashlib.sha256()
+    for path in paths:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+# the sources of the headline decode kernel
+DECODE_SOURCES = [os.path.join("hybrid_linear_attention_gdn_gb300", "csrc", f)
+                  for f in ("decode_tma.cu", "decode_tma_item.cuh", "gdn_common.cuh")]
 
 
 def _peaks():
@@ -326,8 +335,8 @@ def run_ours(args):
         return per_step[min(len(per_step) - 1, int(q * (len(per_step) - 1) + 0.5))]
     step_stats = {"median": statistics.median(per_step), "p10": pct(0.10), "p90": pct(0.90),
                   "how": "separate pass, CUDA events around each step"}
-    src = os.path.join(ROOT, "hybrid_linear_attention_gdn_gb300", "csrc", "decode_tma.cu")
-    traffic = DECODE_TRAFFIC["bytes_per_launch"] if DECODE_TRAFFIC["source_sha256"] == _sha(src) else None
+    srcs = [os.path.join(ROOT, f) for f in DECODE_SOURCES]
+    traffic = DECODE_TRAFFIC["bytes_per_launch"] if DECODE_TRAFFIC["source_sha256"] == _sha(*srcs) else None
 
     # ---- end to end through the public API with host buffers: every step's
     # inputs are copied in from pinned host memory and its output read back,
