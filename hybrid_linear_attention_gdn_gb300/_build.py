@@ -21,7 +21,7 @@ OBJ_DIR_DEBUG = os.path.join(PKG, "_build_debug")
 LIB_DEBUG = os.path.join(PKG, "libgdn_debug.so")
 
 SOURCES = ["api.cu", "slot_ops.cu", "decode.cu", "decode_tma.cu", "verify_tma.cu", "prefill.cu", "prefill_tc.cu",
-           "prefill_tc32.cu", "epilogue.cu", "kda_chunk.cu"]
+           "prefill_tc32.cu", "epilogue.cu", "kda_chunk.cu", "kda_tc32.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
          "--expt-relaxed-constexpr"]

@@ -27,6 +27,7 @@
 #include "decode_tma.cuh"
 #include "prefill_tc.cuh"
 #include "kda_chunk.cuh"
+#include "kda_tc32.cuh"
 
 #include <cstdlib>
 #include <cstring>
@@ -1155,12 +1156,18 @@ extern "C" gdn_status gdn_kda_prefill(const gdn_dims* dims, gdn_pool pool, gdn_p
   const bool async = aligned(qkv, 16) && aligned(a, 16) && ((size_t)dims->dk * es) % 16 == 0 &&
                      ((size_t)dims->dv * es) % 16 == 0 && ((size_t)k.C * es) % 16 == 0;
   cudaError_t e = cudaErrorInvalidValue;
-  // the chunked form where it applies (dk 128, dv <= 128: 8.3 against 9.2 ms
-  // for the token recurrence at 4 x 8192); GDN_KDA_PREFILL_PATH=recurrent
-  // forces the recurrence, read on every call
+  // the 64-token chunk form on the tensor cores where it applies (dk = dv =
+  // 128, bf16, width 4), else the 16-token window form (dk 128, dv <= 128),
+  // else the token recurrence; GDN_KDA_PREFILL_PATH=window or recurrent
+  // forces one of the latter (read on every call)
   const char* kp = std::getenv("GDN_KDA_PREFILL_PATH");
-  const bool chunked = kda_chunk_supported(*dims) && !(kp && !std::strcmp(kp, "recurrent"));
-  if (chunked)
+  const bool force_rec = kp && !std::strcmp(kp, "recurrent"), force_win = kp && !std::strcmp(kp, "window");
+  const bool tc = !force_rec && !force_win && kda_tc32_supported(*dims, qkv, a, out, *params);
+  const bool window = !tc && !force_rec && kda_chunk_supported(*dims);
+  if (tc)
+    e = kda_tc32_launch(*dims, pool, ckpt, *params, slot_ids, cu_seqlens, start_pos, n_seq, total_tokens, ckpt_ids,
+                        max_ckpt, ckpt_block, qkv, a, b, out, dev_err, cs);
+  else if (window)
     e = kda_chunk_launch(*dims, pool, ckpt, *params, slot_ids, cu_seqlens, start_pos, n_seq, total_tokens, ckpt_ids,
                          max_ckpt, ckpt_block, qkv, a, b, out, dev_err, cs);
   else switch (dims->dk) {

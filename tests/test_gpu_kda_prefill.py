@@ -66,15 +66,22 @@ def _n_ck(starts, lens, blk):
     (synth.QWEN.replace(conv="f32", dv=96), [33, 300], [5, 64], 64, "chunked"),
     # v rows of 200 bytes: the staging falls back to element copies
     (synth.QWEN.replace(dv=100), [45, 130], [9, 0], 64, "chunked"),
+    (synth.QWEN, [70, 200, 513], [0, 128, 0], 256, "window"),
+    (synth.QWEN, [200, 1, 70, 129], [200, 77, 4101, 63], 256, "window"),
+    # one sequence of 24 chunks, with checkpoints every 64 tokens
+    (synth.QWEN, [1500], [7], 64, "chunked"),
 ], ids=["tiny", "qwen_recurrent", "dk64_g4", "f32_recurrent", "qwen_unaligned_continuations_recurrent", "qwen",
-        "f32", "qwen_unaligned_continuations", "dv96_f32conv", "dv100_element_staging"])
+        "f32", "qwen_unaligned_continuations", "dv96_f32conv", "dv100_element_staging", "qwen_window",
+        "qwen_unaligned_continuations_window", "qwen_1500_every_chunk_checkpointed"])
 def test_kda_prefill_vs_oracle(cuda, monkeypatch, shape, lens, starts, blk, path):
-    """path "recurrent" forces the token recurrence (the library reads
-    GDN_KDA_PREFILL_PATH on every call); "chunked" is the default, which
-    takes the chunked form where it applies (dk 128, dv <= 128) and the
+    """path "recurrent" forces the token recurrence and "window" the 16-token
+    window form (the library reads GDN_KDA_PREFILL_PATH on every call);
+    "chunked" is the default, which takes the 64-token chunk form on the
+    tensor cores where it applies (dk = dv = 128, bf16: the qwen cases), the
+    window form for the other shapes with dk 128 and dv <= 128, and the
     recurrence elsewhere (the tiny and dk 64 cases)."""
-    if path == "recurrent":
-        monkeypatch.setenv("GDN_KDA_PREFILL_PATH", "recurrent")
+    if path in ("recurrent", "window"):
+        monkeypatch.setenv("GDN_KDA_PREFILL_PATH", path)
     n = len(lens)
     n_slots = 8 if shape.dk == 16 else 12
     st = Setup(shape, seed=140, num_slots=n_slots)

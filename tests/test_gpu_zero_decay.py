@@ -96,10 +96,14 @@ def test_gdn_prefill_zero_decay_tokens(cuda, monkeypatch, path):
            prefill_state_tol(shape, path))
 
 
-def test_kda_prefill_zero_decay_channels(cuda):
+@pytest.mark.parametrize("path", ["tc", "window"])
+def test_kda_prefill_zero_decay_channels(cuda, monkeypatch, path):
     """KDA: every third key channel of every V head sees a = +inf at the
-    chosen tokens (the chunked form's 16-token windows; the second sequence
-    starts off a window boundary)."""
+    chosen tokens (the 64-token chunk form on the tensor cores, and the
+    16-token window form; the second sequence starts off a chunk and a
+    window boundary)."""
+    if path == "window":
+        monkeypatch.setenv("GDN_KDA_PREFILL_PATH", "window")
     shape = synth.QWEN
     lens, starts, blk = [200, 130], [0, 37], 64
     st = Setup(shape, seed=151, num_slots=6)
@@ -198,7 +202,10 @@ def test_gdn_prefill_nan_gate_poisons_like_the_recurrence(cuda, monkeypatch, pat
                prefill_state_tol(shape, path))
 
 
-def test_kda_prefill_nan_gate_poisons_like_the_recurrence(cuda):
+@pytest.mark.parametrize("path", ["tc", "window"])
+def test_kda_prefill_nan_gate_poisons_like_the_recurrence(cuda, monkeypatch, path):
+    if path == "window":
+        monkeypatch.setenv("GDN_KDA_PREFILL_PATH", "window")
     shape = synth.QWEN
     lens, starts, blk = [200, 130], [0, 37], 64
     st = Setup(shape, seed=154, num_slots=6)
@@ -219,5 +226,6 @@ def test_kda_prefill_nan_gate_poisons_like_the_recurrence(cuda):
     o_ref, err = oracle.kda_prefill(st.od, st.opool, ock, oparams, ids.numpy(), cu.numpy(), sp.numpy(),
                                     ck_ids.numpy(), blk, to_np(qkv), to_np(a), to_np(b))
     assert err == 0
-    # the NaN token's 16-token window starts at 80
-    _check_nan(st, shape, lens, cu, ids, ck, ock, ck_ids, out, o_ref, 80, PREFILL_TOL, PREFILL_TOL)
+    # the NaN token's 64-token chunk starts at 64, its 16-token window at 80
+    _check_nan(st, shape, lens, cu, ids, ck, ock, ck_ids, out, o_ref, 64 if path == "tc" else 80, PREFILL_TOL,
+               PREFILL_TOL)
