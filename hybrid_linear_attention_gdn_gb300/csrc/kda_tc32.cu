@@ -20,15 +20,21 @@
 //
 // A' and M cannot be one product of decayed operands: e^{lb_t - lb_j} split
 // as e^{lb_t} e^{-lb_j} overflows.  They are taken in 8-token blocks with a
-// reference token per block pair, so that every factor is a product of
-// alphas over a token range (at most 1):
-//   off the diagonal (t in block I > J, j in block J):
-//     e^{lb_t - lb_j} = fl8_t  D8_IJ  fr8_j, fl8_t = e^{lb_t - lb_b(I)} (from the
-//     block's first token), fr8_j = e^{lb_e(J) - lb_j} (to the block's last),
-//     D8_IJ = e^{lb_b(I) - lb_e(J)}: one fp16 warp-level tensor-core product
-//     per block pair, of Lk8 = k^ (.) fl8 and Lq8 = q^ (.) fl8 rows against
-//     Rk8 = k^ (.) fr8 rows scaled by D8 (fp16 keeps the 10-bit mantissa the
-//     tf32 products keep; every operand lies in [-1, 1]);
+// reference token R between the two blocks of a pair, so that every factor
+// is a product of alphas over a token range (at most 1):
+//   off the diagonal (t in block I, j in block J < I, a reference block R
+//     with J < R <= I): e^{lb_t - lb_j} is the row factor e^{lb_t - lb_b(R)}
+//     = fl8_t e^{lb_b(I) - lb_b(R)} (fl8 from the block's first token) times
+//     the column factor e^{lb_b(R) - lb_j} = e^{lb_b(R) - lb_e(J)} fr8_j (fr8
+//     to the block's last token; b(), e() a block's first and last token).
+//     The 28 block pairs fall into
+//     three levels of a binary split, each one product for all its pairs:
+//     R = block 4 (rows of blocks 4..7 against columns of 0..3), R = 2 and 6
+//     (rows 2, 3 x columns 0, 1 and rows 6, 7 x columns 4, 5), R = the row
+//     block itself (1 x 0, 3 x 2, 5 x 4, 7 x 6).  Levels 3 and 2 make one
+//     tcgen05 product (M = 128: their k and q rows; N = 64), level 1 another
+//     (N = 32), in fp16 (the 10-bit mantissa the tf32 products keep; every
+//     operand lies in [-1, 1]);
 //   on the eight 8 x 8 diagonal blocks: fp32 running products of alpha down
 //     each row, on the CUDA cores.
 // Every within-block factor is a running product of alphas (no differences
@@ -45,9 +51,10 @@
 //              V^T (tf32) into TMEM
 //   norms      rk_t = 1/|y_k,t|, rq_t = dk^-1/2 / |y_q,t| (with the eps)
 //   diagonal   the 8 x 8 diagonal blocks of A' and M
-//   transform  thread (c, quarter): fl8, fr8 by running products; the tf32
-//              operand tiles [K~;Q~] and K-^T, the fp16 Lk8, Lq8, Rk8 and D8
-//   off-diag   A' and M below the diagonal blocks (mma m16n8k16 f16)
+//   transform  thread (channel pair, 8-token block): fl8, fr8 by running
+//              products; the tf32 operand tiles [K~;Q~] and K-^T, the fp16
+//              operands of the off-diagonal products
+//   off-diag   A' and M below the diagonal blocks (two tcgen05 products)
 //   S [K~;Q~]^T  (tcgen05, A operand the state in TMEM) issued before the
 //              solve, runs under it
 //   solve      X = (I + diag(beta) A')^-1 as in the GDN chain; T1 = X
@@ -69,11 +76,11 @@ namespace {
 #include "tc32_common.cuh"
 
 constexpr int kYS = kD + 4;   // row stride (floats) of the fp32 feature and alpha rows
-constexpr int kHS = kD + 8;   // row stride (halves) of the fp16 operand rows: 272 bytes
-constexpr int kPairs = 28;    // 8-token block pairs I > J of a chunk
 
 // TMEM columns (fp32; lanes are dv rows)
 constexpr uint32_t TM_S = 0;     // S [dv][dk]
+constexpr uint32_t TM_DX = 128;  // off-diagonal levels 3 and 2 [their 128 rows][64]
+constexpr uint32_t TM_DY = 192;  // off-diagonal level 1 [its 64 rows (+ 64 unused)][32]
 constexpr uint32_t TM_E = 256;   // S K~^T [dv][64]
 constexpr uint32_t TM_O1 = 320;  // S Q~^T [dv][64]
 constexpr uint32_t TM_DL = 384;  // Delta [dv][64]
@@ -118,9 +125,8 @@ struct __align__(1024) KSmem {
     } t;
     struct {
       float al[kC][kYS];         // alpha per token and channel
-      __half d8[kPairs][kD];     // D8 per block pair and channel
     } g;
-    __half rk8[kC][kHS];         // Rk8 (written over al)
+    uint8_t by[2 * 32 * 128];    // level-1 columns (fp16 operand, over al)
   } rt;
   union {                     // region U
     struct {
@@ -132,9 +138,10 @@ struct __align__(1024) KSmem {
       float yq[kC][kYS];
     } y;
     struct {
-      __half lk[kC][kHS];  // Lk8, Lq8
-      __half lq[kC][kHS];
-    } h;
+      uint8_t ax[2 * 128 * 128];  // levels 3 and 2: rows (fp16 operand)
+      uint8_t bx[2 * 64 * 128];   //   and their columns
+      uint8_t ay[2 * 64 * 128];   // level 1: rows (64 of the product's 128; it reads 8 KB past)
+    } ops;
     struct {
       float A[kC * kAX];
       float X[kC * kAX];
@@ -148,6 +155,7 @@ struct __align__(1024) KSmem {
   float alast[kD];    // e^{lb_63} per channel
   float rk[kC];       // 1 / sqrt(|y_k|^2 + eps)
   float rq[kC];       // dk^-1/2 / sqrt(|y_q|^2 + eps)
+  float nrm[2][2][kC];  // sums of squares over half the channels: [k, q][half][token]
   float dgA[kC][8];   // diagonal blocks: beta_t A'[t][j] (j < t, local j), and
   float dgM[kC][8];   //   M[t][j] (j <= t)
   float ones[kC];
@@ -156,6 +164,10 @@ struct __align__(1024) KSmem {
 };
 
 static_assert(sizeof(KSmem) + 1024 <= 232448, "one CTA's shared memory (with the alignment slack)");
+// the level-1 product reads rows 64..127 of its second column block, 8 KB
+// past the end of ay: still inside the CTA's shared memory
+static_assert(offsetof(KSmem, ru) + 32768 + 16384 + 8192 + 16384 <= sizeof(KSmem),
+              "level-1 rows read past ay (its second column block starts 8 KB in and spans 16 KB)");
 
 __device__ __forceinline__ bool seq_ok(const KdaTcArgs& a, int n, int64_t& t0, int64_t& len, int64_t& p0) {
   const auto cu = GDN_GV(a.cu_seqlens, a.n_seq + 1);
@@ -163,51 +175,6 @@ __device__ __forceinline__ bool seq_ok(const KdaTcArgs& a, int n, int64_t& t0, i
   len = (int64_t)cu[n + 1] - t0;
   p0 = GDN_GV(a.start_pos, a.n_seq)[n];
   return !(t0 < 0 || len < 0 || t0 + len > a.total || p0 < 0);
-}
-
-// ---- warp-level fp16 products ---------------------------------------------------
-// ldmatrix: four (two) 8 x 8 matrices of 16-bit elements; lane i supplies the
-// address of row i % 8 of matrix i / 8 and receives row i / 4, elements
-// 2 (i % 4) and 2 (i % 4) + 1 of each matrix
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_addr(p)));
-}
-__device__ __forceinline__ void ldsm_x2(uint32_t (&r)[2], const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];\n"
-               : "=r"(r[0]), "=r"(r[1])
-               : "r"(smem_addr(p)));
-}
-// D += A B (m16n8k16, fp16 operands, fp32 accumulate).  Lane = 4 g + q: A
-// holds rows g and g + 8, columns 2q, 2q + 1 and 2q + 8, 2q + 9; B columns g,
-// rows 2q, 2q + 1 and 2q + 8, 2q + 9; D (g, 2q), (g, 2q + 1), (g + 8, 2q),
-// (g + 8, 2q + 1).
-__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ uint32_t hmul2_bits(uint32_t x, uint32_t y) {
-  const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&x), *reinterpret_cast<const __half2*>(&y));
-  return *reinterpret_cast<const uint32_t*>(&r);
-}
-
-// Block pairs (I > J) in order p = I (I - 1) / 2 + J
-__host__ __device__ constexpr int pair_index(int I, int J) { return I * (I - 1) / 2 + J; }
-
-// The off-diagonal block pairs of warps 0..14: up to two pairs, as 8 I + J
-// (-1: none)
-__device__ __forceinline__ void warp_pairs(int w, int& p0, int& p1) {
-  constexpr int8_t tbl[15][2] = {{8 * 1 + 0, 8 * 7 + 6}, {8 * 2 + 0, 8 * 2 + 1}, {8 * 3 + 0, 8 * 3 + 1},
-                                 {8 * 3 + 2, -1},        {8 * 4 + 0, 8 * 4 + 1}, {8 * 4 + 2, 8 * 4 + 3},
-                                 {8 * 5 + 0, 8 * 5 + 1}, {8 * 5 + 2, 8 * 5 + 3}, {8 * 5 + 4, -1},
-                                 {8 * 6 + 0, 8 * 6 + 1}, {8 * 6 + 2, 8 * 6 + 3}, {8 * 6 + 4, 8 * 6 + 5},
-                                 {8 * 7 + 0, 8 * 7 + 1}, {8 * 7 + 2, 8 * 7 + 3}, {8 * 7 + 4, 8 * 7 + 5}};
-  p0 = tbl[w][0];
-  p1 = tbl[w][1];
 }
 
 // ---- diagonal 8 x 8 blocks --------------------------------------------------------
@@ -340,12 +307,13 @@ __device__ __forceinline__ void kda_chain(const KdaTcArgs& a, const CUtensorMap&
   constexpr uint32_t ID_N64 = umma::idesc_tf32(128, 64, false, false);
   constexpr uint32_t ID_N128 = umma::idesc_tf32(128, 128, false, false);
   static_assert(4 * 16384 <= sizeof(KSmem::kq) && 2 * 16384 <= sizeof(KSmem::kt), "operand tiles");
-  static_assert(sizeof(KSmem::rt) == 3 * 16384 && kC * kYS * 4 + kPairs * kD * 2 <= 3 * 16384,
-                "region T holds T1, T2, M or alpha and D8");
-  static_assert(2 * kC * kYS * 4 <= sizeof(KSmem::ru) && 2 * kC * kAX * 4 + (2048 + 8 * 3 * 64) * 4 <= sizeof(KSmem::ru),
-                "region U holds the feature rows or the solve's scratch");
-  static_assert(TM_E == TM_S + 256 && TM_O1 == TM_E + 64 && TM_DL == TM_O1 + 64 && TM_V == TM_DL + 64 &&
-                    TM_V + 64 <= TM_COLS && TM_O2 == TM_V,
+  static_assert(sizeof(KSmem::rt) == 3 * 16384 && kC * kYS * 4 <= 3 * 16384,
+                "region T holds T1, T2, M or alpha (then the level-1 columns)");
+  static_assert(2 * kC * kYS * 4 <= sizeof(KSmem::ru) && 2 * kC * kAX * 4 + (2048 + 8 * 3 * 64) * 4 <= sizeof(KSmem::ru) &&
+                    4 * 16384 <= sizeof(KSmem::ru),
+                "region U holds the feature rows, the off-diagonal operands or the solve's scratch");
+  static_assert(TM_DX == TM_S + 128 && TM_DY == TM_DX + 64 && TM_E >= TM_DY + 32 && TM_O1 == TM_E + 64 &&
+                    TM_DL == TM_O1 + 64 && TM_V == TM_DL + 64 && TM_V + 64 <= TM_COLS && TM_O2 == TM_V,
                 "TMEM regions");
 
   // feature channels of this thread: the q/k channel pair (2 cp, 2 cp + 1)
@@ -365,10 +333,11 @@ __device__ __forceinline__ void kda_chain(const KdaTcArgs& a, const CUtensorMap&
     const float4 v4 = vec_at<const float4>(cw, (size_t)gch_v * 4);
     wv[0] = v4.x; wv[1] = v4.y; wv[2] = v4.z; wv[3] = v4.w;
   }
-  // gate channel of this thread (gates and transform: channel gc, tokens 16 gq ..)
-  const int gc = tid & 127, gq = tid >> 7;
+  // gate channels of this thread (gates and transform: channels 2 gp, 2 gp + 1
+  // of the 8-token block gb)
+  const int gp = tid & 63, gb = tid >> 6;
   const float eA = expf(GDN_GV(a.A_log, a.hv)[h]);
-  const float dtb = GDN_GV(a.dt_bias, (long long)a.hv * kD)[(size_t)h * kD + gc];
+  const float2 dtb = vec_at<const float2>(GDN_GV(a.dt_bias, (long long)a.hv * kD), (size_t)h * kD + 2 * gp);
   const int part_x[3] = {hq * kD, (a.hk + hq) * kD, 2 * a.hk * kD + h * kD};
 
   // checkpoint slot at the end of chunk c (-1: none), as in the GDN chain
@@ -451,6 +420,16 @@ __device__ __forceinline__ void kda_chain(const KdaTcArgs& a, const CUtensorMap&
     bl = load_beta(c + 1);
     if (!wait_all(&S.ld_bar, c & 1)) break;
     ld_done = c + 1;
+    // the next chunk's boxes into L2 now; their copies into shared memory
+    // start after the solve (where they lie wholly inside the tensors)
+    if (tid == 0 && c + 1 < nch) {
+      const int32_t row1 = (int32_t)(t0 + (P + kC - 3 - p0));
+      if (row1 >= 0 && (int64_t)row1 + kRawRows <= a.total) {
+#pragma unroll
+        for (int q = 0; q < 3; ++q) tma_prefetch_2d(&qmap, part_x[q], row1);
+        tma_prefetch_2d(&amap, h * kD, row1 + 3);
+      }
+    }
     // the up to 3 rows just before the sequence start come from the conv history
     if (P - 3 < p0) {
       const int64_t lo = (P - 3 > p0 - 3) ? P - 3 : p0 - 3;
@@ -466,27 +445,27 @@ __device__ __forceinline__ void kda_chain(const KdaTcArgs& a, const CUtensorMap&
       __syncthreads();
     }
 
-    // ---- gates: log alpha, alpha, 8-block totals (thread: channel gc, tokens 16 gq ..)
+    // ---- gates: log alpha, alpha, 8-block totals (thread: channels 2 gp, 2 gp + 1
+    //      of the 8-token block gb) ---------------------------------------------
     {
-      const auto ga = GDN_SV(&S.ru.in.ga[0][0], kC * kD);
+      const auto ga = GDN_SV(reinterpret_cast<const __nv_bfloat162*>(&S.ru.in.ga[0][0]), kC * kD / 2);
       const auto al = GDN_SV(&S.rt.g.al[0][0], kC * kYS);
-      float G0 = 0.f, G1 = 0.f, f0 = 0.f, f1 = 0.f;
+      float2 G = make_float2(0.f, 0.f), f = G;
 #pragma unroll
-      for (int t = 0; t < 16; ++t) {
-        const int tt = 16 * gq + t;
+      for (int t = 0; t < 8; ++t) {
+        const int tt = 8 * gb + t;
         const bool valid = (unsigned)(tt - tlo) < (unsigned)(thi - tlo);
-        const float x = __bfloat162float(ga[tt * kD + gc]) + dtb;
-        const float sp = x > 20.f ? x : __logf(1.f + __expf(x));
-        const float g = valid ? floor_log_decay(-eA * sp) : 0.f;
-        al[tt * kYS + gc] = __expf(g);
-        if (t < 8) G0 += g; else G1 += g;
-        if (t == 0) f0 = g;
-        if (t == 8) f1 = g;
+        const float2 x = __bfloat1622float2(ga[tt * (kD / 2) + gp]);
+        const float x0 = x.x + dtb.x, x1 = x.y + dtb.y;
+        const float s0 = x0 > 20.f ? x0 : __logf(1.f + __expf(x0)), s1 = x1 > 20.f ? x1 : __logf(1.f + __expf(x1));
+        const float g0 = valid ? floor_log_decay(-eA * s0) : 0.f, g1 = valid ? floor_log_decay(-eA * s1) : 0.f;
+        vec_at<float2>(al, tt * kYS + 2 * gp) = make_float2(__expf(g0), __expf(g1));
+        G.x += g0;
+        G.y += g1;
+        if (t == 0) f = make_float2(g0, g1);
       }
-      S.G8[2 * gq][gc] = G0;
-      S.G8[2 * gq + 1][gc] = G1;
-      S.g8f[2 * gq][gc] = f0;
-      S.g8f[2 * gq + 1][gc] = f1;
+      vec_at<float2>(&S.G8[GDN_S(gb, 8)][0], 2 * gp) = G;
+      vec_at<float2>(&S.g8f[GDN_S(gb, 8)][0], 2 * gp) = f;
     }
 
     // ---- features: conv1d + SiLU, down the chunk ---------------------------
@@ -510,6 +489,25 @@ __device__ __forceinline__ void kda_chain(const KdaTcArgs& a, const CUtensorMap&
           const bool valid = (unsigned)(tk + t - tlo) < (unsigned)(thi - tlo);
           y[t] = valid ? make_float2(silu_tanh(acc.x), silu_tanh(acc.y)) : make_float2(0.f, 0.f);
         }
+      }
+      // the tokens' sums of squares over the warp's 64 channels: a
+      // reduce-scatter leaves lanes 2 t and 2 t + 1 with token t's
+      {
+        float ss[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) ss[t] = fmaf(y[t].x, y[t].x, y[t].y * y[t].y);
+#pragma unroll
+        for (int s2 = 16; s2 >= 2; s2 >>= 1) {
+          const bool up = lane & s2;
+#pragma unroll
+          for (int i = 0; i < s2 / 2; ++i) {
+            const float send = up ? ss[i] : ss[i + s2 / 2];
+            const float keep = up ? ss[i + s2 / 2] : ss[i];
+            ss[i] = keep + __shfl_xor_sync(0xffffffffu, send, s2);
+          }
+        }
+        ss[0] += __shfl_xor_sync(0xffffffffu, ss[0], 1);
+        if (!(lane & 1)) S.nrm[isq][warp & 1][GDN_S(tk + (lane >> 1), kC)] = ss[0];
       }
       {
         const auto xv = GDN_SV(&S.ru.in.raw[2][0][0], kRawRows * kD) + (tk * kD + lrow);
@@ -535,36 +533,11 @@ __device__ __forceinline__ void kda_chain(const KdaTcArgs& a, const CUtensorMap&
 #pragma unroll
       for (int t = 0; t < 16; ++t) vec_at<float2>(yd, (tk + t) * kYS + 2 * cp) = y[t];
       umma::tmem_st16(tlane + TM_V + tk, vv);
-    }
-    __syncthreads();
-    // ---- norms: warp w, tokens 4 w .. 4 w + 3 ---------------------------------
-    {
-      float sk[4], sq[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int t = 4 * warp + i;
-        const float4 k4 = vec_at<const float4>(GDN_SV(&S.ru.y.yk[0][0], kC * kYS), t * kYS + 4 * lane);
-        const float4 q4 = vec_at<const float4>(GDN_SV(&S.ru.y.yq[0][0], kC * kYS), t * kYS + 4 * lane);
-        sk[i] = dot4(k4, k4);
-        sq[i] = dot4(q4, q4);
-      }
-#pragma unroll
-      for (int o = 16; o; o >>= 1)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          sk[i] += __shfl_xor_sync(0xffffffffu, sk[i], o);
-          sq[i] += __shfl_xor_sync(0xffffffffu, sq[i], o);
-        }
-      if (lane < 4) {
-        float k = sk[0], q = sq[0];
-#pragma unroll
-        for (int i = 1; i < 4; ++i)
-          if (lane == i) {
-            k = sk[i];
-            q = sq[i];
-          }
-        S.rk[4 * warp + lane] = rsqrtf(k + kNormEps);
-        S.rq[4 * warp + lane] = rsqrtf(q + kNormEps) * rsqrtf((float)kD);
+      // the norms: rk_t = 1 / sqrt(|y_k,t|^2 + eps), rq_t = dk^-1/2 / sqrt(|y_q,t|^2 + eps)
+      if (tid < 2 * kC) {
+        const int t = tid & (kC - 1), iq = tid >> 6;
+        const float r = rsqrtf(S.nrm[iq][0][t] + S.nrm[iq][1][t] + kNormEps);
+        if (iq) S.rq[t] = r * rsqrtf((float)kD); else S.rk[t] = r;
       }
     }
     __syncthreads();
@@ -574,143 +547,193 @@ __device__ __forceinline__ void kda_chain(const KdaTcArgs& a, const CUtensorMap&
     else
       diag_block<0>(S, warp >> 1);
 
-    // ---- transform (thread: channel gc, tokens 16 gq ..) -----------------------
+    // ---- transform (thread: channels 2 gp, 2 gp + 1 of the 8-token block gb) --
     {
       const auto al = GDN_SV(&S.rt.g.al[0][0], kC * kYS);
       const auto yk = GDN_SV(&S.ru.y.yk[0][0], kC * kYS), yq = GDN_SV(&S.ru.y.yq[0][0], kC * kYS);
-      float a16[16], k16[16], q16[16];
+      float2 a8[8], k8[8], q8[8];
 #pragma unroll
-      for (int t = 0; t < 16; ++t) {
-        const int tt = 16 * gq + t;
-        a16[t] = al[tt * kYS + gc];
-        k16[t] = yk[tt * kYS + gc];
-        q16[t] = yq[tt * kYS + gc];
+      for (int t = 0; t < 8; ++t) {
+        const int tt = 8 * gb + t;
+        a8[t] = vec_at<const float2>(al, tt * kYS + 2 * gp);
+        k8[t] = vec_at<const float2>(yk, tt * kYS + 2 * gp);
+        q8[t] = vec_at<const float2>(yq, tt * kYS + 2 * gp);
       }
-      // block factors of the thread's 8-blocks I0 = 2 gq, I1 = 2 gq + 1:
-      // e^{lb} at their first tokens and e^{lb_63 - lb} at their last
-      float pre = 0.f, post = 0.f, tot = 0.f;
+      // block factors (per channel, from the 8-block totals G and first-token
+      // log decays f): e^{lb} at this block's first token (Eb) and e^{lb_63 -
+      // lb} at its last (Ee); the off-diagonal row factors e^{lb_b(gb) -
+      // lb_b(R)} (F2 for R = 2, 6; F1 for R = 4) and column factors e^{lb_b(R)
+      // - lb_e(gb)} (E3 for R = gb + 1; E2 for R = 2, 6; EY for R = 4)
+      float2 G[8], F[8];
 #pragma unroll
       for (int K = 0; K < 8; ++K) {
-        const float gk = S.G8[K][gc];
-        tot += gk;
-        if (K < 2 * gq) pre += gk;
-        if (K > 2 * gq + 1) post += gk;
+        G[K] = vec_at<const float2>(&S.G8[K][0], 2 * gp);
+        F[K] = vec_at<const float2>(&S.g8f[K][0], 2 * gp);
       }
-      const float G0 = S.G8[2 * gq][gc], G1 = S.G8[2 * gq + 1][gc];
-      const float Eb0 = expf(pre + S.g8f[2 * gq][gc]), Eb1 = expf(pre + G0 + S.g8f[2 * gq + 1][gc]);
-      const float Ee1 = expf(post), Ee0 = expf(post + G1);
-      if (gq == 0) S.alast[gc] = expf(tot);
-      // D8 for every block pair: thread tid takes entries tid + 512 m
+      float2 pre = make_float2(0.f, 0.f), post = pre, tot = pre, fb = F[0], f1 = pre, e2 = pre, ey = pre;
+      float2 f2 = pre, e3 = F[1];
 #pragma unroll
-      for (int m = 0; m < kPairs * kD / kThreads; ++m) {
-        const int e = tid + kThreads * m, p = e >> 7, cc = e & 127;
-        int I = 1;
-#pragma unroll
-        for (int i = 2; i < 8; ++i)
-          if (p >= pair_index(i, 0)) I = i;
-        const int J = p - pair_index(I, 0);
-        float s = S.g8f[I][cc];
-        for (int K = J + 1; K < I; ++K) s += S.G8[K][cc];
-        S.rt.g.d8[GDN_S(p, kPairs)][cc] = __float2half_rn(expf(s));
+      for (int K = 0; K < 8; ++K) {
+        tot = make_float2(tot.x + G[K].x, tot.y + G[K].y);
+        if (K < gb) pre = make_float2(pre.x + G[K].x, pre.y + G[K].y);
+        if (K > gb) post = make_float2(post.x + G[K].x, post.y + G[K].y);
+        if (K == gb) fb = F[K];
+        if (K >= 4 && K < gb) f1 = make_float2(f1.x + G[K].x, f1.y + G[K].y);
+        if (K > gb && K < (gb < 4 ? 2 : 6)) e2 = make_float2(e2.x + G[K].x, e2.y + G[K].y);
+        if (K > gb && K < 4) ey = make_float2(ey.x + G[K].x, ey.y + G[K].y);
+        if (K + 1 == gb) f2 = make_float2(G[K].x - F[K].x, G[K].y - F[K].y);
+        if (K == gb + 1) e3 = F[K];
       }
-      float4 rk4[4], rq4[4];
+      const float2 Eb = make_float2(__expf(pre.x + fb.x), __expf(pre.y + fb.y));
+      const float2 Ee = make_float2(__expf(post.x), __expf(post.y));
+      if (gb == 0) vec_at<float2>(S.alast, 2 * gp) = make_float2(__expf(tot.x), __expf(tot.y));
+      const float2 F1 = make_float2(__expf(f1.x - F[4].x + fb.x), __expf(f1.y - F[4].y + fb.y));
+      const float2 F2 = (gb & 1) ? make_float2(__expf(f2.x + fb.x), __expf(f2.y + fb.y)) : make_float2(1.f, 1.f);
+      const float2 E3 = make_float2(__expf(e3.x), __expf(e3.y));
+      const float2 R2 = gb < 4 ? F[2] : F[6];
+      const float2 E2 = make_float2(__expf(e2.x + R2.x), __expf(e2.y + R2.y));
+      const float2 EY = make_float2(__expf(ey.x + F[4].x), __expf(ey.y + F[4].y));
+      float rk8v[8], rq8v[8];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        rk4[i] = *reinterpret_cast<const float4*>(&S.rk[16 * gq + 4 * i]);
-        rq4[i] = *reinterpret_cast<const float4*>(&S.rq[16 * gq + 4 * i]);
+      for (int i = 0; i < 2; ++i) {
+        const float4 r4 = *reinterpret_cast<const float4*>(&S.rk[8 * gb + 4 * i]);
+        const float4 s4 = *reinterpret_cast<const float4*>(&S.rq[8 * gb + 4 * i]);
+        rk8v[4 * i] = r4.x; rk8v[4 * i + 1] = r4.y; rk8v[4 * i + 2] = r4.z; rk8v[4 * i + 3] = r4.w;
+        rq8v[4 * i] = s4.x; rq8v[4 * i + 1] = s4.y; rq8v[4 * i + 2] = s4.z; rq8v[4 * i + 3] = s4.w;
       }
       // alpha, the feature rows and the diagonal blocks are read: the
       // operands take regions T and U
       __syncthreads();
-      float fl[16], fr[16];
+      // fl8_t = prod of alpha from the block's first token to t, fr8_t from t
+      // to its last (exclusive of the first and of t)
+      float2 fl[8], fr[8];
+      fl[0] = make_float2(1.f, 1.f);
 #pragma unroll
-      for (int hb = 0; hb < 2; ++hb) {
-        float f = 1.f;
-        fl[8 * hb] = 1.f;
+      for (int t = 1; t < 8; ++t) fl[t] = make_float2(fl[t - 1].x * a8[t].x, fl[t - 1].y * a8[t].y);
+      fr[7] = make_float2(1.f, 1.f);
 #pragma unroll
-        for (int t = 1; t < 8; ++t) {
-          f *= a16[8 * hb + t];
-          fl[8 * hb + t] = f;
+      for (int t = 6; t >= 0; --t) fr[t] = make_float2(fr[t + 1].x * a8[t + 1].x, fr[t + 1].y * a8[t + 1].y);
+      // an fp16 channel pair of row `row` of a 128B-swizzled K-major operand
+      // whose 64-channel blocks are kb bytes apart
+      auto put_h = [&](uint8_t* tile, unsigned bytes, uint32_t kb, int row, float x, float y) {
+        tile_at<__half2>(tile, bytes, umma::sw128_off(row, 2 * gp, kb)) = __floats2half2_rn(x, y);
+      };
+      const int m3 = gb >> 1;                                  // level-3 row / column block
+      const int m2 = (gb & 1) + ((gb >> 2) << 1);              // level-2 row / column block
+      float km0[8], km1[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const int tt = 8 * gb + t;
+        const float2 kh = make_float2(k8[t].x * rk8v[t], k8[t].y * rk8v[t]);
+        const float2 qh = make_float2(q8[t].x * rq8v[t], q8[t].y * rq8v[t]);
+        const float2 kl = make_float2(kh.x * fl[t].x, kh.y * fl[t].y), ql = make_float2(qh.x * fl[t].x, qh.y * fl[t].y);
+        const float2 kr = make_float2(kh.x * fr[t].x, kh.y * fr[t].y);
+        tile_at<float2>(S.kq, sizeof(S.kq), f32_off(tt, 2 * gp, 128 * 128)) =
+            make_float2(umma::tf32_round(kl.x * Eb.x), umma::tf32_round(kl.y * Eb.y));
+        tile_at<float2>(S.kq, sizeof(S.kq), f32_off(kC + tt, 2 * gp, 128 * 128)) =
+            make_float2(umma::tf32_round(ql.x * Eb.x), umma::tf32_round(ql.y * Eb.y));
+        km0[t] = umma::tf32_round(kr.x * Ee.x);
+        km1[t] = umma::tf32_round(kr.y * Ee.y);
+        if (gb & 1) {  // level-3 rows (blocks 1, 3, 5, 7)
+          put_h(S.ru.ops.ax, sizeof(S.ru.ops.ax), 16384, 8 * m3 + t, kl.x, kl.y);
+          put_h(S.ru.ops.ax, sizeof(S.ru.ops.ax), 16384, 32 + 8 * m3 + t, ql.x, ql.y);
+        } else {       // level-3 columns (blocks 0, 2, 4, 6)
+          put_h(S.ru.ops.bx, sizeof(S.ru.ops.bx), 8192, 8 * m3 + t, kr.x * E3.x, kr.y * E3.y);
         }
-        f = 1.f;
-#pragma unroll
-        for (int t = 7; t >= 0; --t) {
-          fr[8 * hb + t] = f;
-          f *= a16[8 * hb + t];
+        if (gb & 2) {  // level-2 rows (blocks 2, 3, 6, 7)
+          put_h(S.ru.ops.ax, sizeof(S.ru.ops.ax), 16384, 64 + 8 * m2 + t, kl.x * F2.x, kl.y * F2.y);
+          put_h(S.ru.ops.ax, sizeof(S.ru.ops.ax), 16384, 96 + 8 * m2 + t, ql.x * F2.x, ql.y * F2.y);
+        } else {       // level-2 columns (blocks 0, 1, 4, 5)
+          put_h(S.ru.ops.bx, sizeof(S.ru.ops.bx), 8192, 32 + 8 * m2 + t, kr.x * E2.x, kr.y * E2.y);
+        }
+        if (gb >= 4) {  // level-1 rows (blocks 4..7)
+          put_h(S.ru.ops.ay, sizeof(S.ru.ops.ay), 8192, 8 * (gb - 4) + t, kl.x * F1.x, kl.y * F1.y);
+          put_h(S.ru.ops.ay, sizeof(S.ru.ops.ay), 8192, 32 + 8 * (gb - 4) + t, ql.x * F1.x, ql.y * F1.y);
+        } else {        // level-1 columns (blocks 0..3)
+          put_h(S.rt.by, sizeof(S.rt.by), 4096, 8 * gb + t, kr.x * EY.x, kr.y * EY.y);
         }
       }
-      const auto lk = GDN_SV(&S.ru.h.lk[0][0], kC * kHS), lq = GDN_SV(&S.ru.h.lq[0][0], kC * kHS);
-      const auto rk8 = GDN_SV(&S.rt.rk8[0][0], kC * kHS);
-      float km[16];
 #pragma unroll
-      for (int t = 0; t < 16; ++t) {
-        const int tt = 16 * gq + t;
-        const float rkt = reinterpret_cast<const float*>(rk4)[t], rqt = reinterpret_cast<const float*>(rq4)[t];
-        const float kh = k16[t] * rkt, qh = q16[t] * rqt;
-        const float Eb = t < 8 ? Eb0 : Eb1, Ee = t < 8 ? Ee0 : Ee1;
-        tile_at<float>(S.kq, sizeof(S.kq), f32_off(tt, gc, 128 * 128)) = umma::tf32_round(kh * fl[t] * Eb);
-        tile_at<float>(S.kq, sizeof(S.kq), f32_off(kC + tt, gc, 128 * 128)) = umma::tf32_round(qh * fl[t] * Eb);
-        km[t] = umma::tf32_round(kh * fr[t] * Ee);
-        lk[tt * kHS + gc] = __float2half_rn(kh * fl[t]);
-        lq[tt * kHS + gc] = __float2half_rn(qh * fl[t]);
-        rk8[tt * kHS + gc] = __float2half_rn(kh * fr[t]);
+      for (int h4 = 0; h4 < 2; ++h4) {
+        tile_at<float4>(S.kt, sizeof(S.kt), f32_off(2 * gp, 8 * gb + 4 * h4, 128 * 128)) =
+            make_float4(km0[4 * h4], km0[4 * h4 + 1], km0[4 * h4 + 2], km0[4 * h4 + 3]);
+        tile_at<float4>(S.kt, sizeof(S.kt), f32_off(2 * gp + 1, 8 * gb + 4 * h4, 128 * 128)) =
+            make_float4(km1[4 * h4], km1[4 * h4 + 1], km1[4 * h4 + 2], km1[4 * h4 + 3]);
       }
-#pragma unroll
-      for (int t4 = 0; t4 < 4; ++t4)
-        tile_at<float4>(S.kt, sizeof(S.kt), f32_off(gc, 16 * gq + 4 * t4, 128 * 128)) =
-            make_float4(km[4 * t4], km[4 * t4 + 1], km[4 * t4 + 2], km[4 * t4 + 3]);
     }
     umma::fence_proxy_async();
     umma::fence_before();
     __syncthreads();
-    // ---- A' and M below the diagonal blocks (warps 0..14) ----------------------
-    float cacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    int pr[2] = {-1, -1};
-    if (warp < 15) {
-      warp_pairs(warp, pr[0], pr[1]);
-      const auto lk = GDN_SV(&S.ru.h.lk[0][0], kC * kHS), lq = GDN_SV(&S.ru.h.lq[0][0], kC * kHS);
-      const auto rk8 = GDN_SV(&S.rt.rk8[0][0], kC * kHS);
-      const auto d8 = GDN_SV(reinterpret_cast<const uint32_t*>(&S.rt.g.d8[0][0]), kPairs * kD / 2);
-      const int q = lane & 3;
-      const int mi = lane >> 3, ri = lane & 7;  // ldmatrix: matrix and row this lane addresses
-      const int Ia = pr[0] >> 3, Ib = pr[1] >= 0 ? pr[1] >> 3 : Ia;
-#pragma unroll 2
-      for (int ks = 0; ks < kD / 16; ++ks) {
-        const int k0 = 16 * ks;
-        uint32_t fa[2][4];
-        // A: rows 0..7 Lk8, rows 8..15 Lq8 of block I; columns k0 .. k0 + 15
-        ldsm_x4(fa[0], (mi & 1 ? lq : lk).at((8 * Ia + ri) * kHS + k0 + 8 * (mi >> 1), 8));
-        if (Ib != Ia) ldsm_x4(fa[1], (mi & 1 ? lq : lk).at((8 * Ib + ri) * kHS + k0 + 8 * (mi >> 1), 8));
+    // ---- A' and M below the diagonal blocks: levels 3 and 2 (rows: ax, columns:
+    //      bx; N = 64) and level 1 (ay, by; N = 32) on the tensor core -------
+    if (tid == 0) {
+      umma::fence_after();
+      constexpr uint32_t ID_X = umma::idesc_f16(128, 64, false, false);
+      constexpr uint32_t ID_Y = umma::idesc_f16(128, 32, false, false);
+      const uint64_t dax = umma::desc(smem_addr(S.ru.ops.ax), 16, 1024);
+      const uint64_t dbx = umma::desc(smem_addr(S.ru.ops.bx), 16, 1024);
+      const uint64_t day = umma::desc(smem_addr(S.ru.ops.ay), 16, 1024);
+      const uint64_t dby = umma::desc(smem_addr(S.rt.by), 16, 1024);
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          if (pr[i] < 0) continue;
-          const int I = pr[i] >> 3, J = pr[i] & 7, p = pair_index(I, J);
-          uint32_t fb[2];
-          ldsm_x2(fb, rk8.at((8 * J + ri) * kHS + k0 + 8 * (mi & 1), 8));
-          fb[0] = hmul2_bits(fb[0], d8[(p * kD + k0 + 2 * q) / 2]);
-          fb[1] = hmul2_bits(fb[1], d8[(p * kD + k0 + 8 + 2 * q) / 2]);
-          mma_f16(cacc[i], (i == 1 && Ib != Ia) ? fa[1] : fa[0], fb[0], fb[1]);
-        }
-      }
+      for (int s = 0; s < 8; ++s)  // K = 16 channels a step, 64-channel blocks
+        umma::mma_bf16(tmem + TM_DX, umma::adv(dax, (s >> 2) * 16384 + (s & 3) * 32),
+                       umma::adv(dbx, (s >> 2) * 8192 + (s & 3) * 32), ID_X, s > 0);
+#pragma unroll
+      for (int s = 0; s < 8; ++s)
+        umma::mma_bf16(tmem + TM_DY, umma::adv(day, (s >> 2) * 8192 + (s & 3) * 32),
+                       umma::adv(dby, (s >> 2) * 4096 + (s & 3) * 32), ID_Y, s > 0);
+      umma::commit(&S.mma_bar);
     }
-    // every operand read: A (fp32, for the solve), M (tf32 operand), X and T1,
-    // T2 (cleared: the solve writes their lower triangles)
-    __syncthreads();
+    if (!mma_wait()) break;
+    // A (fp32, for the solve: beta_t A'), M (tf32 operand), X and T1, T2
+    // (cleared: the solve writes their lower triangles)
     {
       const auto A = GDN_SV(S.ru.sv.A, kC * kAX);
-      if (warp < 15) {
-        const int g = lane >> 2, q = lane & 3;
+      const int q4 = warp & 3, k4 = warp >> 2;
+      // 8 entries of row t in block column J: k rows (even lane quarter) to A,
+      // q rows (odd) to M
+      auto put4 = [&](int t, int j, float x0, float x1, float x2, float x3) {
+        if (!(q4 & 1)) {
+          const float bt = S.beta[GDN_S(t, kC)];
+          vec_at<float4>(A, t * kAX + j) = make_float4(x0 * bt, x1 * bt, x2 * bt, x3 * bt);
+        } else {
+          tile_at<float4>(S.rt.t.mq, sizeof(S.rt.t.mq), f32_off(t, j, 64 * 128)) =
+              make_float4(umma::tf32_round(x0), umma::tf32_round(x1), umma::tf32_round(x2), umma::tf32_round(x3));
+        }
+      };
+#define GDN_PUT8(t, J, v, o)                                                \
+  do {                                                                      \
+    put4((t), 8 * (J), v[(o)], v[(o) + 1], v[(o) + 2], v[(o) + 3]);         \
+    put4((t), 8 * (J) + 4, v[(o) + 4], v[(o) + 5], v[(o) + 6], v[(o) + 7]); \
+  } while (0)
+      const int m = lane >> 3, r = lane & 7;
+      if (q4 < 2) {
+        // lanes 0..63: level-3 rows (block 2m + 1; its columns: block 2m, at
+        // columns 8m of the first product) and level-1 rows (block 4 + m)
+        if (k4 == 0) {
+          float v[32], w[8];
+          umma::tmem_ld32(tlane + TM_DX, v);
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          if (pr[i] < 0) continue;
-          const int I = pr[i] >> 3, J = pr[i] & 7;
-          const int t = 8 * I + g, j = 8 * J + 2 * q;
-          const float bt = S.beta[t];
-          vec_at<float2>(A, t * kAX + j) = make_float2(cacc[i][0] * bt, cacc[i][1] * bt);
-          tile_at<float2>(S.rt.t.mq, sizeof(S.rt.t.mq), f32_off(t, j, 64 * 128)) =
-              make_float2(umma::tf32_round(cacc[i][2]), umma::tf32_round(cacc[i][3]));
+          for (int i = 0; i < 8; ++i) w[i] = m == 0 ? v[i] : m == 1 ? v[8 + i] : m == 2 ? v[16 + i] : v[24 + i];
+          GDN_PUT8(8 * (2 * m + 1) + r, 2 * m, w, 0);
+        } else if (k4 < 3) {
+          float v[16];
+          umma::tmem_ld16(tlane + TM_DY + 16 * (k4 - 1), v);
+          GDN_PUT8(8 * (4 + m) + r, 2 * (k4 - 1), v, 0);
+          GDN_PUT8(8 * (4 + m) + r, 2 * (k4 - 1) + 1, v, 8);
+        }
+      } else if (k4 < 2) {
+        // lanes 64..127: level-2 rows (blocks 2, 3, 6, 7); columns 32..47 hold
+        // blocks 0, 1 (for rows of 2, 3), 48..63 blocks 4, 5 (rows of 6, 7)
+        float v[16];
+        umma::tmem_ld16(tlane + TM_DX + 32 + 16 * k4, v);
+        if ((m >> 1) == k4) {
+          const int I = m + 2 + 2 * (m >> 1);
+          GDN_PUT8(8 * I + r, 4 * k4, v, 0);
+          GDN_PUT8(8 * I + r, 4 * k4 + 1, v, 8);
         }
       }
+#undef GDN_PUT8
       // row t, columns 8 J .. 8 J + 7: the diagonal block (J = t / 8) from
       // dgA / dgM, zeros right of it
       {
@@ -904,7 +927,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 bool kda_tc32_supported(const gdn_dims& d, const void* qkv, const void* av, const void* out, const gdn_params& p) {
   if (d.dk != kD || d.dv != kD || d.conv_width != 4) return false;
   if (d.act_dtype != GDN_BF16 || d.conv_dtype != GDN_BF16) return false;
-  if (!aligned(qkv, 16) || !aligned(av, 16) || !aligned(out, 16) || !aligned(p.conv_w, 16)) return false;
+  if (!aligned(qkv, 16) || !aligned(av, 16) || !aligned(out, 16) || !aligned(p.conv_w, 16) || !aligned(p.dt_bias, 8))
+    return false;
   return true;
 }
 

@@ -79,6 +79,13 @@ __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b
       : "memory");
 }
 
+// kind::f16 instruction descriptor: fp16 A and B, fp32 D (issued by mma_bf16,
+// the same instruction).
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
 // kind::tf32 instruction descriptor: tf32 A and B (fp32 containers; the
 // tensor core reads their top 19 bits), fp32 D.
 __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N, bool a_mn, bool b_mn) {
