@@ -698,7 +698,7 @@ def measure_rows(gdn, synth, dev, stream, hbm_peak, bf16_peak, which="all", pref
         del kspec
 
     def kda_prefill_row(kp):
-        # KDA prefill (the 16-token window form), 4 sequences x prefill_len tokens,
+        # KDA prefill (the 64-token chunk form on the tensor cores), 4 sequences x prefill_len tokens,
         # checkpoints every 256: per token qkv, the per-channel gate logits, beta and out
         nK, SK = 4, prefill_len
         kt = nK * SK

@@ -159,7 +159,7 @@ struct __align__(1024) KSmem {
   float dgA[kC][8];   // diagonal blocks: beta_t A'[t][j] (j < t, local j), and
   float dgM[kC][8];   //   M[t][j] (j <= t)
   float ones[kC];
-  uint64_t ld_bar, mma_bar, eo_bar;
+  uint64_t ld_bar, mma_bar, eo_bar, od_bar;  // od_bar: the two off-diagonal products (two issuers)
   uint32_t tmem_base;
 };
 
@@ -195,11 +195,13 @@ __host__ __device__ constexpr int diag_off(int rg, int r) {
 }
 static_assert(diag_off(0, 4) == 32 && diag_off(1, 4) == 32, "32 values per lane");
 
-__device__ __forceinline__ float dot4(float4 a, float4 b) {
-  return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
-}
+// a (.) b on packed fp32 pairs
 __device__ __forceinline__ float4 mul4(float4 a, float4 b) {
-  return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w);
+  return join4(mul2(lo2(a), lo2(b)), mul2(hi2(a), hi2(b)));
+}
+// acc + a . b
+__device__ __forceinline__ float dot4acc(float4 a, float4 b, float acc) {
+  return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, acc))));
 }
 
 template <int RG>
@@ -227,9 +229,9 @@ __device__ __forceinline__ void diag_block(KSmem& S, const int B) {
         p[r] = mul4(p[r], aj);
       }
       if (t >= j) {
-        const float4 kp = mul4(kj, p[r]);
-        acc[o + j] += dot4(qr[r], kp);
-        if (t > j) acc[o + t + 1 + j] += dot4(kr[r], kp);
+        const float4 kp = t == j ? kj : mul4(kj, p[r]);
+        acc[o + j] = dot4acc(qr[r], kp, acc[o + j]);
+        if (t > j) acc[o + t + 1 + j] = dot4acc(kr[r], kp, acc[o + t + 1 + j]);
       }
     }
   }
@@ -295,6 +297,7 @@ __device__ __forceinline__ void kda_chain(const KdaTcArgs& a, const CUtensorMap&
   if (tid == 0) {
     mbar_init(&S.ld_bar, 1);
     mbar_init(&S.mma_bar, 1);
+    mbar_init(&S.od_bar, 2);
     mbar_init(&S.eo_bar, 1);
     fence_mbar_init();
   }
@@ -354,18 +357,31 @@ __device__ __forceinline__ void kda_chain(const KdaTcArgs& a, const CUtensorMap&
     return slot_class(id, a.ck_num_slots) == 0 ? id : -1;
   };
   constexpr uint32_t kLoadBytes = 3u * kRawRows * kD * 2u + (uint32_t)kC * kD * 2u;
-  auto issue_loads = [&](int c) {  // thread 0: chunk c's raw rows and gate logits into region U
+  // warp 0: chunk c's gate logits (lane 3, with the phase's byte count) and
+  // raw rows (lanes 0..2: the q, k and v boxes at once) into region U.  The
+  // gate-logit box lies past the solve's scratch, so it goes first, as soon
+  // as the previous chunk's off-diagonal products have read their operands.
+  auto issue_ga = [&](int c) {
+    const int64_t P = (p0 / kC + c) * kC;
+    const int32_t row = (int32_t)(t0 + (P - p0));  // packed row of the chunk's first token (may be < 0)
+    if (lane == 3) {
+      mbar_arrive_expect_tx(&S.ld_bar, kLoadBytes);
+      // 128 channels of V head h, 64 rows (rows outside: zeros)
+      if (GDN_SPAN_G(h * kD, kD, (long long)a.hv * kD) && GDN_SBYTES(&S.ru.in.ga[0][0], kC * kD * 2, S))
+        tma_load_2d(&S.ru.in.ga[0][0], &amap, h * kD, row, &S.ld_bar);
+    }
+  };
+  auto issue_raw = [&](int c) {
     const int64_t P = (p0 / kC + c) * kC;
     const int32_t row0 = (int32_t)(t0 + (P - 3 - p0));  // packed row of raw row 0 (may be < 0)
-    mbar_arrive_expect_tx(&S.ld_bar, kLoadBytes);
-#pragma unroll
-    for (int q = 0; q < 3; ++q)  // a box of 128 channels from part_x[q], 67 rows (rows outside: zeros)
-      if (GDN_SPAN_G(part_x[q], kD, a.C) && GDN_SBYTES(&S.ru.in.raw[q][0][0], kRawRows * kD * 2, S))
-        tma_load_2d(&S.ru.in.raw[q][0][0], &qmap, part_x[q], row0, &S.ld_bar);
-    // gate logits: 128 channels of V head h, 64 rows from the chunk's first token
-    if (GDN_SPAN_G(h * kD, kD, (long long)a.hv * kD) && GDN_SBYTES(&S.ru.in.ga[0][0], kC * kD * 2, S))
-      tma_load_2d(&S.ru.in.ga[0][0], &amap, h * kD, row0 + 3, &S.ld_bar);
+    if (lane < 3) {  // a box of 128 channels of the q, k or v part, 67 rows (rows outside: zeros)
+      const int x = lane == 0 ? hq * kD : lane == 1 ? (a.hk + hq) * kD : 2 * a.hk * kD + h * kD;
+      if (GDN_SPAN_G(x, kD, a.C) && GDN_SBYTES(&S.ru.in.raw[lane][0][0], kRawRows * kD * 2, S))
+        tma_load_2d(&S.ru.in.raw[lane][0][0], &qmap, x, row0, &S.ld_bar);
+    }
   };
+  static_assert(offsetof(decltype(KSmem::ru), in.ga) >= offsetof(decltype(KSmem::ru), sv.L0) + sizeof(KSmem::ru.sv.L0),
+                "the gate-logit box lies past the solve's scratch");
   // beta logit of chunk c's token tid (threads 0..63), loaded one chunk ahead
   auto load_beta = [&](int c) -> float {
     const int64_t pos = (p0 / kC + c) * kC + tid;
@@ -387,10 +403,12 @@ __device__ __forceinline__ void kda_chain(const KdaTcArgs& a, const CUtensorMap&
     umma::tmem_st32(tlane + TM_S + 32 * qq, v);
   }
   int ld_issued = 0, ld_done = 0;
-  if (tid == 0) {
-    issue_loads(0);
-    ld_issued = 1;
+  if (warp == 0) {
+    issue_ga(0);
+    __syncwarp();  // the phase's byte count before any of its copies
+    issue_raw(0);
   }
+  ld_issued = 1;
   float bl = load_beta(0);
 
   bool bad = false;
@@ -406,7 +424,7 @@ __device__ __forceinline__ void kda_chain(const KdaTcArgs& a, const CUtensorMap&
     return ok;
   };
 
-  bool eo_pending = false;
+  bool eo_pending = false, od_pending = false;
   int c = 0;
   for (; c < nch; ++c) {
     const int64_t P = (p0 / kC + c) * kC;
@@ -564,35 +582,31 @@ __device__ __forceinline__ void kda_chain(const KdaTcArgs& a, const CUtensorMap&
       // lb} at its last (Ee); the off-diagonal row factors e^{lb_b(gb) -
       // lb_b(R)} (F2 for R = 2, 6; F1 for R = 4) and column factors e^{lb_b(R)
       // - lb_e(gb)} (E3 for R = gb + 1; E2 for R = 2, 6; EY for R = 4)
-      float2 G[8], F[8];
+      float2 G[8];
 #pragma unroll
-      for (int K = 0; K < 8; ++K) {
-        G[K] = vec_at<const float2>(&S.G8[K][0], 2 * gp);
-        F[K] = vec_at<const float2>(&S.g8f[K][0], 2 * gp);
-      }
-      float2 pre = make_float2(0.f, 0.f), post = pre, tot = pre, fb = F[0], f1 = pre, e2 = pre, ey = pre;
-      float2 f2 = pre, e3 = F[1];
+      for (int K = 0; K < 8; ++K) G[K] = vec_at<const float2>(&S.G8[K][0], 2 * gp);
+      auto gf = [&](int K) { return vec_at<const float2>(&S.g8f[GDN_S(K, 8)][0], 2 * gp); };
+      const float2 fb = gf(gb), f4 = gf(4), fR = gf(gb < 4 ? 2 : 6);
+      const float2 fn = gf(gb < 7 ? gb + 1 : 7), fp = gf(gb > 0 ? gb - 1 : 0);
+      float2 pre = make_float2(0.f, 0.f), post = pre, tot = pre, f1 = pre, e2 = pre, ey = pre, f2 = pre;
 #pragma unroll
       for (int K = 0; K < 8; ++K) {
         tot = make_float2(tot.x + G[K].x, tot.y + G[K].y);
         if (K < gb) pre = make_float2(pre.x + G[K].x, pre.y + G[K].y);
         if (K > gb) post = make_float2(post.x + G[K].x, post.y + G[K].y);
-        if (K == gb) fb = F[K];
         if (K >= 4 && K < gb) f1 = make_float2(f1.x + G[K].x, f1.y + G[K].y);
         if (K > gb && K < (gb < 4 ? 2 : 6)) e2 = make_float2(e2.x + G[K].x, e2.y + G[K].y);
         if (K > gb && K < 4) ey = make_float2(ey.x + G[K].x, ey.y + G[K].y);
-        if (K + 1 == gb) f2 = make_float2(G[K].x - F[K].x, G[K].y - F[K].y);
-        if (K == gb + 1) e3 = F[K];
+        if (K + 1 == gb) f2 = make_float2(G[K].x - fp.x, G[K].y - fp.y);
       }
       const float2 Eb = make_float2(__expf(pre.x + fb.x), __expf(pre.y + fb.y));
       const float2 Ee = make_float2(__expf(post.x), __expf(post.y));
       if (gb == 0) vec_at<float2>(S.alast, 2 * gp) = make_float2(__expf(tot.x), __expf(tot.y));
-      const float2 F1 = make_float2(__expf(f1.x - F[4].x + fb.x), __expf(f1.y - F[4].y + fb.y));
+      const float2 F1 = make_float2(__expf(f1.x - f4.x + fb.x), __expf(f1.y - f4.y + fb.y));
       const float2 F2 = (gb & 1) ? make_float2(__expf(f2.x + fb.x), __expf(f2.y + fb.y)) : make_float2(1.f, 1.f);
-      const float2 E3 = make_float2(__expf(e3.x), __expf(e3.y));
-      const float2 R2 = gb < 4 ? F[2] : F[6];
-      const float2 E2 = make_float2(__expf(e2.x + R2.x), __expf(e2.y + R2.y));
-      const float2 EY = make_float2(__expf(ey.x + F[4].x), __expf(ey.y + F[4].y));
+      const float2 E3 = make_float2(__expf(fn.x), __expf(fn.y));
+      const float2 E2 = make_float2(__expf(e2.x + fR.x), __expf(e2.y + fR.y));
+      const float2 EY = make_float2(__expf(ey.x + f4.x), __expf(ey.y + f4.y));
       float rk8v[8], rq8v[8];
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
@@ -613,52 +627,66 @@ __device__ __forceinline__ void kda_chain(const KdaTcArgs& a, const CUtensorMap&
       fr[7] = make_float2(1.f, 1.f);
 #pragma unroll
       for (int t = 6; t >= 0; --t) fr[t] = make_float2(fr[t + 1].x * a8[t + 1].x, fr[t + 1].y * a8[t + 1].y);
-      // an fp16 channel pair of row `row` of a 128B-swizzled K-major operand
-      // whose 64-channel blocks are kb bytes apart
-      auto put_h = [&](uint8_t* tile, unsigned bytes, uint32_t kb, int row, float x, float y) {
-        tile_at<__half2>(tile, bytes, umma::sw128_off(row, 2 * gp, kb)) = __floats2half2_rn(x, y);
+      // Rows 8 m + t of the 128B-swizzled K-major operands (row r at (r / 8)
+      // 1024 + (r % 8) 128 bytes, its 16-byte chunks permuted by XOR with r %
+      // 8): the thread's channel pair sits at a fixed byte of a chunk, and
+      // for token t of its block at row offset t 128 + (chunk ^ t) 16.
+      // fp16 operands: 64-channel blocks kb bytes apart, 8 channels a chunk.
+      const uint32_t ch16 = (uint32_t)(((2 * gp) & 63) >> 3) << 4, cb16 = (uint32_t)((2 * gp) & 7) * 2;
+      auto rowh = [&](uint32_t kb, int m) { return (uint32_t)(gp >> 5) * kb + (uint32_t)m * 1024u + cb16; };
+      auto put_h = [&](uint8_t* tile, unsigned bytes, uint32_t ob, int t, float x, float y) {
+        tile_at<__half2>(tile, bytes, ob + (uint32_t)t * 128u + (ch16 ^ ((uint32_t)t << 4))) = __floats2half2_rn(x, y);
       };
       const int m3 = gb >> 1;                                  // level-3 row / column block
       const int m2 = (gb & 1) + ((gb >> 2) << 1);              // level-2 row / column block
+      const uint32_t oax3 = rowh(16384, m3), oaq3 = rowh(16384, 4 + m3), obx3 = rowh(8192, m3);
+      const uint32_t oax2 = rowh(16384, 8 + m2), oaq2 = rowh(16384, 12 + m2), obx2 = rowh(8192, 4 + m2);
+      const uint32_t oay = rowh(8192, gb - 4), oayq = rowh(8192, gb), oby = rowh(4096, gb);
+      // fp32 (tf32) operand [K~;Q~]: 32-channel blocks 16 KB apart, 4 channels a chunk
+      const uint32_t ch32 = (uint32_t)(((2 * gp) & 31) >> 2) << 4;
+      const uint32_t okq = (uint32_t)(gp >> 4) * 16384u + (uint32_t)gb * 1024u + (uint32_t)((2 * gp) & 3) * 4u;
       float km0[8], km1[8];
 #pragma unroll
       for (int t = 0; t < 8; ++t) {
-        const int tt = 8 * gb + t;
         const float2 kh = make_float2(k8[t].x * rk8v[t], k8[t].y * rk8v[t]);
         const float2 qh = make_float2(q8[t].x * rq8v[t], q8[t].y * rq8v[t]);
         const float2 kl = make_float2(kh.x * fl[t].x, kh.y * fl[t].y), ql = make_float2(qh.x * fl[t].x, qh.y * fl[t].y);
         const float2 kr = make_float2(kh.x * fr[t].x, kh.y * fr[t].y);
-        tile_at<float2>(S.kq, sizeof(S.kq), f32_off(tt, 2 * gp, 128 * 128)) =
+        const uint32_t rt32 = okq + (uint32_t)t * 128u + (ch32 ^ ((uint32_t)t << 4));
+        tile_at<float2>(S.kq, sizeof(S.kq), rt32) =
             make_float2(umma::tf32_round(kl.x * Eb.x), umma::tf32_round(kl.y * Eb.y));
-        tile_at<float2>(S.kq, sizeof(S.kq), f32_off(kC + tt, 2 * gp, 128 * 128)) =
+        tile_at<float2>(S.kq, sizeof(S.kq), rt32 + 8u * 1024u) =  // Q~ rows: 64 rows on
             make_float2(umma::tf32_round(ql.x * Eb.x), umma::tf32_round(ql.y * Eb.y));
         km0[t] = umma::tf32_round(kr.x * Ee.x);
         km1[t] = umma::tf32_round(kr.y * Ee.y);
         if (gb & 1) {  // level-3 rows (blocks 1, 3, 5, 7)
-          put_h(S.ru.ops.ax, sizeof(S.ru.ops.ax), 16384, 8 * m3 + t, kl.x, kl.y);
-          put_h(S.ru.ops.ax, sizeof(S.ru.ops.ax), 16384, 32 + 8 * m3 + t, ql.x, ql.y);
+          put_h(S.ru.ops.ax, sizeof(S.ru.ops.ax), oax3, t, kl.x, kl.y);
+          put_h(S.ru.ops.ax, sizeof(S.ru.ops.ax), oaq3, t, ql.x, ql.y);
         } else {       // level-3 columns (blocks 0, 2, 4, 6)
-          put_h(S.ru.ops.bx, sizeof(S.ru.ops.bx), 8192, 8 * m3 + t, kr.x * E3.x, kr.y * E3.y);
+          put_h(S.ru.ops.bx, sizeof(S.ru.ops.bx), obx3, t, kr.x * E3.x, kr.y * E3.y);
         }
         if (gb & 2) {  // level-2 rows (blocks 2, 3, 6, 7)
-          put_h(S.ru.ops.ax, sizeof(S.ru.ops.ax), 16384, 64 + 8 * m2 + t, kl.x * F2.x, kl.y * F2.y);
-          put_h(S.ru.ops.ax, sizeof(S.ru.ops.ax), 16384, 96 + 8 * m2 + t, ql.x * F2.x, ql.y * F2.y);
+          put_h(S.ru.ops.ax, sizeof(S.ru.ops.ax), oax2, t, kl.x * F2.x, kl.y * F2.y);
+          put_h(S.ru.ops.ax, sizeof(S.ru.ops.ax), oaq2, t, ql.x * F2.x, ql.y * F2.y);
         } else {       // level-2 columns (blocks 0, 1, 4, 5)
-          put_h(S.ru.ops.bx, sizeof(S.ru.ops.bx), 8192, 32 + 8 * m2 + t, kr.x * E2.x, kr.y * E2.y);
+          put_h(S.ru.ops.bx, sizeof(S.ru.ops.bx), obx2, t, kr.x * E2.x, kr.y * E2.y);
         }
         if (gb >= 4) {  // level-1 rows (blocks 4..7)
-          put_h(S.ru.ops.ay, sizeof(S.ru.ops.ay), 8192, 8 * (gb - 4) + t, kl.x * F1.x, kl.y * F1.y);
-          put_h(S.ru.ops.ay, sizeof(S.ru.ops.ay), 8192, 32 + 8 * (gb - 4) + t, ql.x * F1.x, ql.y * F1.y);
+          put_h(S.ru.ops.ay, sizeof(S.ru.ops.ay), oay, t, kl.x * F1.x, kl.y * F1.y);
+          put_h(S.ru.ops.ay, sizeof(S.ru.ops.ay), oayq, t, ql.x * F1.x, ql.y * F1.y);
         } else {        // level-1 columns (blocks 0..3)
-          put_h(S.rt.by, sizeof(S.rt.by), 4096, 8 * gb + t, kr.x * EY.x, kr.y * EY.y);
+          put_h(S.rt.by, sizeof(S.rt.by), oby, t, kr.x * EY.x, kr.y * EY.y);
         }
       }
 #pragma unroll
       for (int h4 = 0; h4 < 2; ++h4) {
-        tile_at<float4>(S.kt, sizeof(S.kt), f32_off(2 * gp, 8 * gb + 4 * h4, 128 * 128)) =
-            make_float4(km0[4 * h4], km0[4 * h4 + 1], km0[4 * h4 + 2], km0[4 * h4 + 3]);
-        tile_at<float4>(S.kt, sizeof(S.kt), f32_off(2 * gp + 1, 8 * gb + 4 * h4, 128 * 128)) =
-            make_float4(km1[4 * h4], km1[4 * h4 + 1], km1[4 * h4 + 2], km1[4 * h4 + 3]);
+        // rows 2 gp and 2 gp + 1, in an order that puts the 8 lanes of each
+        // quarter-warp store on 8 distinct 16-byte chunks (row % 8 distinct)
+        const bool sw = (gp >> 2) & 1;
+        const float4 v0 = make_float4(km0[4 * h4], km0[4 * h4 + 1], km0[4 * h4 + 2], km0[4 * h4 + 3]);
+        const float4 v1 = make_float4(km1[4 * h4], km1[4 * h4 + 1], km1[4 * h4 + 2], km1[4 * h4 + 3]);
+        tile_at<float4>(S.kt, sizeof(S.kt), f32_off(2 * gp + sw, 8 * gb + 4 * h4, 128 * 128)) = sw ? v1 : v0;
+        tile_at<float4>(S.kt, sizeof(S.kt), f32_off(2 * gp + !sw, 8 * gb + 4 * h4, 128 * 128)) = sw ? v0 : v1;
       }
     }
     umma::fence_proxy_async();
@@ -666,27 +694,56 @@ __device__ __forceinline__ void kda_chain(const KdaTcArgs& a, const CUtensorMap&
     __syncthreads();
     // ---- A' and M below the diagonal blocks: levels 3 and 2 (rows: ax, columns:
     //      bx; N = 64) and level 1 (ay, by; N = 32) on the tensor core -------
+    od_pending = true;
+    // (issued by two threads, one product each: a thread issuing products
+    // waits for the tensor core to take each one)
     if (tid == 0) {
       umma::fence_after();
       constexpr uint32_t ID_X = umma::idesc_f16(128, 64, false, false);
-      constexpr uint32_t ID_Y = umma::idesc_f16(128, 32, false, false);
       const uint64_t dax = umma::desc(smem_addr(S.ru.ops.ax), 16, 1024);
       const uint64_t dbx = umma::desc(smem_addr(S.ru.ops.bx), 16, 1024);
-      const uint64_t day = umma::desc(smem_addr(S.ru.ops.ay), 16, 1024);
-      const uint64_t dby = umma::desc(smem_addr(S.rt.by), 16, 1024);
 #pragma unroll
       for (int s = 0; s < 8; ++s)  // K = 16 channels a step, 64-channel blocks
         umma::mma_bf16(tmem + TM_DX, umma::adv(dax, (s >> 2) * 16384 + (s & 3) * 32),
                        umma::adv(dbx, (s >> 2) * 8192 + (s & 3) * 32), ID_X, s > 0);
+      umma::commit(&S.od_bar);
+    } else if (tid == 32) {
+      umma::fence_after();
+      constexpr uint32_t ID_Y = umma::idesc_f16(128, 32, false, false);
+      const uint64_t day = umma::desc(smem_addr(S.ru.ops.ay), 16, 1024);
+      const uint64_t dby = umma::desc(smem_addr(S.rt.by), 16, 1024);
 #pragma unroll
       for (int s = 0; s < 8; ++s)
         umma::mma_bf16(tmem + TM_DY, umma::adv(day, (s >> 2) * 8192 + (s & 3) * 32),
                        umma::adv(dby, (s >> 2) * 4096 + (s & 3) * 32), ID_Y, s > 0);
-      umma::commit(&S.mma_bar);
+      umma::commit(&S.od_bar);
     }
-    if (!mma_wait()) break;
-    // A (fp32, for the solve: beta_t A'), M (tf32 operand), X and T1, T2
-    // (cleared: the solve writes their lower triangles)
+    // meanwhile (neither is an operand of the products): M's diagonal blocks
+    // from dgM, zeros right of them, and T2 cleared
+    {
+      const int t = tid >> 3, J = tid & 7, I = t >> 3, tl = t & 7;
+      if (J >= I) {
+        float mv[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) mv[jj] = (J == I && jj <= tl) ? umma::tf32_round(S.dgM[t][jj]) : 0.f;
+#pragma unroll
+        for (int h4 = 0; h4 < 2; ++h4)
+          tile_at<float4>(S.rt.t.mq, sizeof(S.rt.t.mq), f32_off(t, 8 * J + 4 * h4, 64 * 128)) =
+              make_float4(mv[4 * h4], mv[4 * h4 + 1], mv[4 * h4 + 2], mv[4 * h4 + 3]);
+      }
+      for (int e = tid; e < (int)(sizeof(S.rt.t.t2) / 16); e += kThreads)
+        reinterpret_cast<uint4*>(S.rt.t.t2)[e] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (!wait_all(&S.od_bar, c & 1)) break;
+    od_pending = false;
+    umma::fence_after();
+    // the next chunk's gate logits (their part of region U is free from here)
+    if (c + 1 < nch) {
+      if (warp == 0) issue_ga(c + 1);
+      ld_issued = c + 2;
+    }
+    // A (fp32, for the solve: beta_t A'), M below the diagonal blocks (tf32
+    // operand), X and T1 (cleared: the solve writes their lower triangles)
     {
       const auto A = GDN_SV(S.ru.sv.A, kC * kAX);
       const int q4 = warp & 3, k4 = warp >> 2;
@@ -734,30 +791,24 @@ __device__ __forceinline__ void kda_chain(const KdaTcArgs& a, const CUtensorMap&
         }
       }
 #undef GDN_PUT8
-      // row t, columns 8 J .. 8 J + 7: the diagonal block (J = t / 8) from
-      // dgA / dgM, zeros right of it
+      // row t, columns 8 J .. 8 J + 7: A's diagonal block (J = t / 8) from
+      // dgA, zeros right of it
       {
         const int t = tid >> 3, J = tid & 7, I = t >> 3, tl = t & 7;
         if (J >= I) {
-          float av[8], mv[8];
+          float av[8];
 #pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            av[jj] = (J == I && jj < tl) ? S.dgA[t][jj] : 0.f;
-            mv[jj] = (J == I && jj <= tl) ? umma::tf32_round(S.dgM[t][jj]) : 0.f;
-          }
+          for (int jj = 0; jj < 8; ++jj) av[jj] = (J == I && jj < tl) ? S.dgA[t][jj] : 0.f;
 #pragma unroll
-          for (int h4 = 0; h4 < 2; ++h4) {
+          for (int h4 = 0; h4 < 2; ++h4)
             vec_at<float4>(A, t * kAX + 8 * J + 4 * h4) =
                 make_float4(av[4 * h4], av[4 * h4 + 1], av[4 * h4 + 2], av[4 * h4 + 3]);
-            tile_at<float4>(S.rt.t.mq, sizeof(S.rt.t.mq), f32_off(t, 8 * J + 4 * h4, 64 * 128)) =
-                make_float4(mv[4 * h4], mv[4 * h4 + 1], mv[4 * h4 + 2], mv[4 * h4 + 3]);
-          }
         }
       }
       for (int e = tid; e < kC * kAX / 4; e += kThreads)
         reinterpret_cast<float4*>(S.ru.sv.X)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int e = tid; e < (int)(2 * sizeof(S.rt.t.tm) / 16); e += kThreads)
-        reinterpret_cast<uint4*>(S.rt.t.tm)[e] = make_uint4(0u, 0u, 0u, 0u);  // tm and t2
+      for (int e = tid; e < (int)(sizeof(S.rt.t.tm) / 16); e += kThreads)
+        reinterpret_cast<uint4*>(S.rt.t.tm)[e] = make_uint4(0u, 0u, 0u, 0u);
     }
     __syncthreads();
     // ---- E | O1 = S [K~;Q~]^T on the tensor core, issued by a lane of warp 10,
@@ -778,10 +829,7 @@ __device__ __forceinline__ void kda_chain(const KdaTcArgs& a, const CUtensorMap&
     umma::fence_proxy_async();
     __syncthreads();
     // the next chunk's raw rows and gate logits (region U is dead)
-    if (tid == 0 && c + 1 < nch) {
-      issue_loads(c + 1);
-      ld_issued = c + 2;
-    }
+    if (c + 1 < nch && warp == 0) issue_raw(c + 1);
     if (!wait_all(&S.eo_bar, c & 1)) break;
     eo_pending = false;
     umma::fence_after();
@@ -878,6 +926,7 @@ __device__ __forceinline__ void kda_chain(const KdaTcArgs& a, const CUtensorMap&
       umma::commit(&S.mma_bar);
       mbar_wait(&S.mma_bar, mph);
       if (eo_pending) mbar_wait(&S.eo_bar, c & 1);
+      if (od_pending) mbar_wait(&S.od_bar, c & 1);
       for (int k = ld_done; k < ld_issued; ++k) mbar_wait(&S.ld_bar, k & 1);
     }
   } else {
@@ -894,6 +943,7 @@ __device__ __forceinline__ void kda_chain(const KdaTcArgs& a, const CUtensorMap&
   if (tid == 0) {
     mbar_inval(&S.ld_bar);
     mbar_inval(&S.mma_bar);
+    mbar_inval(&S.od_bar);
     mbar_inval(&S.eo_bar);
   }
 }
