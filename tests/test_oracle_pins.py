@@ -763,7 +763,7 @@ def test_kda_prefill_equals_kda_decode_steps_and_checkpoints():
     assert np.all(ck.ssm[[2, 4, 5]] == -9.0)
 
 
-@pytest.mark.parametrize("chunk", [1, 4, 16, 32])
+@pytest.mark.parametrize("chunk", [1, 4, 16, 32, 64])
 @pytest.mark.parametrize("strong_decay", [False, True])
 def test_kda_window_form_equals_token_recurrence(chunk, strong_decay):
     """The KDA prefill in windows of `chunk` tokens (A', M, T from per-channel
@@ -776,7 +776,9 @@ def test_kda_window_form_equals_token_recurrence(chunk, strong_decay):
     g, pool, params = _tiny_setup(90 + chunk)
     A_log = np.full(d.hv, math.log(16.0)) if strong_decay else params.A_log
     pk = oracle.Params(params.conv_w, A_log, synth.normal((d.hv, d.dk), 0.5, g).double().numpy())
-    lens, starts, blk = [70, 45, 9], [0, 50, 3], 32
+    # checkpoint blocks of 32 tokens (64 for the 64-token chunks: a block
+    # boundary is always a chunk boundary)
+    lens, starts, blk = [70, 45, 9], [0, 50, 3], max(32, chunk)
     cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
     ids = np.array([3, 6, 1], np.int32)
     qkv, _, b = (t.double().numpy() for t in synth.tokens(shape, g, (int(cu[-1]),)))
@@ -793,4 +795,5 @@ def test_kda_window_form_equals_token_recurrence(chunk, strong_decay):
     np.testing.assert_array_equal(pool2.conv, pool.conv)
     np.testing.assert_allclose(ck2.ssm, ck1.ssm, rtol=1e-10, atol=1e-12)
     np.testing.assert_array_equal(ck2.conv, ck1.conv)
-    assert not np.all(ck1.ssm[[0, 1, 3]] == -9.0)  # the boundaries 32, 64 (seq 0) and 64 (seq 1) were written
+    written = [0, 1, 3] if blk == 32 else [0, 3]  # the boundaries 32, 64 (seq 0) and 64 (seq 1)
+    assert not np.any([np.all(ck1.ssm[i] == -9.0) for i in written])
