@@ -165,18 +165,26 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
     const uint32_t ec = sizeof(Tconv), ea = sizeof(Tact);
     uint32_t n = 0, vk = 0;
     bool ok = true;
-    for (int64_t u = u0; u < u1 && ok;) {
-      const Seg g = segment_at(a, u, u1);
-      u += g.ns;
-      const int r = g.r, h = g.h, R = g.ns * kRows, nchunks = g.ns, nch = 2 * kDK + R;
+    // the next segment at or after u whose working slot is in range (the
+    // consumers skip the others without a bundle), or false
+    auto next_valid = [&](int64_t& u, Seg& g) -> bool {
+      while (u < u1) {
+        g = segment_at(a, u, u1);
+        u += g.ns;
+        if (!slot_class(a.slot_ids[GDN_G(g.r, nreq)], a.num_slots)) return true;
+      }
+      return false;
+    };
+    // segment g's bundle into buffer vk % 2 (free once the consumers have
+    // finished the prologue of the segment two before); false on a timeout
+    auto issue_bundle = [&](const Seg& g) -> bool {
+      const int r = g.r, h = g.h, R = g.ns * kRows, nch = 2 * kDK + R;
       const uint32_t bundle_bytes =
           (kW - 1) * nch * ec + T * nch * ea + nch * kW * 4 + (KDA ? T * kDK * ea + kDK * 4 : 0u);
       const int32_t slot = a.slot_ids[GDN_G(r, nreq)];
-      if (slot_class(slot, a.num_slots)) continue;
-      if (*abort_flag) break;
       const int hq = h / a.G;
       const int bb = vk & 1;
-      if (!mbar_wait(&S.bempty[bb], ((vk >> 1) & 1) ^ 1)) { ok = false; break; }
+      if (!mbar_wait(&S.bempty[bb], ((vk >> 1) & 1) ^ 1)) return false;
       mbar_arrive_expect_tx(&S.bfull[bb], bundle_bytes);
       typename SM::Bundle& Bd = S.bundle[bb];
       const size_t cq = (size_t)hq * kDK, ck = (size_t)a.hk * kDK + cq,
@@ -212,6 +220,22 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
         g2s(&Bd.gdt[0], a.dt_bias + (size_t)h * kDK, kDK * 4, a.dt_bias, (long long)a.hv * kDK * 4);
       }
       ++vk;
+      return true;
+    };
+    // each segment's bundle goes out one segment ahead of its state chunks,
+    // so it has landed when the consumers reach the segment
+    int64_t u = u0;
+    Seg g, gn;
+    bool have = next_valid(u, g);
+    if (have && !issue_bundle(g)) ok = false;
+    while (have && ok && !*abort_flag) {
+      const bool have_next = next_valid(u, gn);
+      if (have_next && !issue_bundle(gn)) {
+        ok = false;
+        break;
+      }
+      const int h = g.h, nchunks = g.ns;
+      const int32_t slot = a.slot_ids[GDN_G(g.r, nreq)];
       const float* src = a.ssm + (((size_t)slot * a.hv + h) * a.dv + (size_t)g.s0 * kRows) * kDK;
       for (int c = 0; c < nchunks; ++c, ++n) {
         const int st = n % STAGES;
@@ -221,6 +245,8 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
             GDN_SBYTES(S.ring[GDN_S(st, STAGES)], kStageBytes, S))
           bulk_g2s(S.ring[st], src + (size_t)c * kStageFloats, kStageBytes, &S.full[st]);
       }
+      g = gn;
+      have = have_next;
     }
     if (!ok || *abort_flag) {
       *abort_flag = 1;
