@@ -27,8 +27,8 @@
 //     = fl8_t e^{lb_b(I) - lb_b(R)} (fl8 from the block's first token) times
 //     the column factor e^{lb_b(R) - lb_j} = e^{lb_b(R) - lb_e(J)} fr8_j (fr8
 //     to the block's last token; b(), e() a block's first and last token).
-//     The 28 block pairs fall into
-//     three levels of a binary split, each one product for all its pairs:
+//     The 28 block pairs fall into three levels of a binary split, each one
+//     product for all its pairs:
 //     R = block 4 (rows of blocks 4..7 against columns of 0..3), R = 2 and 6
 //     (rows 2, 3 x columns 0, 1 and rows 6, 7 x columns 4, 5), R = the row
 //     block itself (1 x 0, 3 x 2, 5 x 4, 7 x 6).  Levels 3 and 2 make one
@@ -43,13 +43,15 @@
 //
 // One CTA per (V head, sequence), 512 threads, walks the sequence's chunks in
 // order; the fp32 state S lives in TMEM for the whole sequence.  Per chunk:
-//   gates      thread (channel c, 16-token quarter): log alpha, alpha, the
-//              8-block totals
-//   features   the 67 raw rows of the head's q, k and v channels and the
-//              chunk's gate logits arrive by TMA tensor copies; conv1d +
-//              SiLU down the chunk; q and k rows (fp32) into shared memory,
-//              V^T (tf32) into TMEM
-//   norms      rk_t = 1/|y_k,t|, rq_t = dk^-1/2 / |y_q,t| (with the eps)
+//   gates      thread (channel pair, 8-token block): log alpha, alpha, the
+//              8-block totals, from the chunk's gate logits (one TMA box,
+//              loaded under the previous chunk's solve)
+//   features   the 67 raw rows of the head's q, k and v channels arrive by
+//              three TMA boxes; conv1d + SiLU down the chunk; q and k rows
+//              (fp32) into shared memory, V^T (tf32) into TMEM, and each
+//              token's sums of squares over the warp's channels
+//   norms      rk_t = 1/|y_k,t|, rq_t = dk^-1/2 / |y_q,t| (with the eps) from
+//              those sums
 //   diagonal   the 8 x 8 diagonal blocks of A' and M
 //   transform  thread (channel pair, 8-token block): fl8, fr8 by running
 //              products; the tf32 operand tiles [K~;Q~] and K-^T, the fp16
