@@ -70,6 +70,7 @@ struct __align__(128) VSmem {
   float snorm[MT][3];     // rq, rk, k^.q^ per draft
   float sgate[MT][2];     // alpha, beta per draft
   float sal[KDA ? MT : 1][kDK];  // KDA: alpha per draft and key channel
+  int32_t ssid[MT];       // the segment's spec slot per draft
   uint64_t full[STAGES], empty[STAGES], bfull[2], bempty[2];
   int abort;
 };
@@ -122,6 +123,9 @@ __device__ __forceinline__ Seg segment_at(const VArgs& a, int64_t u, int64_t u1)
   g.ns = (int)ns;
   return g;
 }
+
+// a line of global memory into L1 (no value returned, nothing to wait for)
+__device__ __forceinline__ void prefetch_l1(const void* p) { asm volatile("prefetch.L1 [%0];\n" ::"l"(p)); }
 
 template <typename Tact, typename Tconv, int STAGES, int MT, int MINB, bool KDA>
 __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
@@ -283,6 +287,9 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
     }
     if (h == 0 && g.s0 == 0 && tid < T && slot_class(sid_of(tid), a.spec_num_slots) == 2)
       report(a.err, GDN_DEV_ERR_SLOT_OOB);
+    // the drafts' spec slots, read once per segment (the loops below take
+    // them from shared memory rather than reloading them per draft)
+    if (tid < T) S.ssid[GDN_S(tid, MT)] = sid_of(tid);
     const int bb = vk & 1;
     if (!*abort_flag && !mbar_wait(&S.bfull[bb], (vk >> 1) & 1)) *abort_flag = 1;
     named_sync(kBarCons, kCons);
@@ -311,7 +318,7 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
         w0 = w1;
         w1 = w2;
         w2 = xv;
-        const int32_t sid = sid_of(t);
+        const int32_t sid = S.ssid[t];
         if (writes && slot_class(sid, a.spec_num_slots) == 0) {
           Tconv* const sc = reinterpret_cast<Tconv*>(a.spec_conv);
           const size_t c0 = (size_t)sid * (kW - 1) * a.C + c;
@@ -424,7 +431,7 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
             dk_[j] += __shfl_xor_sync(0xffffffffu, dk_[j], o);
             dq_[j] += __shfl_xor_sync(0xffffffffu, dq_[j], o);
           }
-        const int32_t sid = sid_of(t);
+        const int32_t sid = S.ssid[t];
         const bool keep = slot_class(sid, a.spec_num_slots) == 0;
 #pragma unroll
         for (int j = 0; j < NR; ++j) {
@@ -448,6 +455,20 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
         }
       }
     };
+    // the next segment's per-draft scalars (its working slot, the drafts'
+    // spec slots and gate logits) into L1 while this segment's rows run, so
+    // that its prologue does not start on cold global loads
+    if (u < u1 && tid <= T) {
+      const Seg gn = segment_at(a, u, u1);
+      if (tid < T) {
+        const size_t rt = (size_t)gn.r * T + tid;
+        prefetch_l1(&a.spec_ids[GDN_G(rt, (long long)nreq * T)]);
+        prefetch_l1(&reinterpret_cast<const Tact*>(a.b)[GDN_G(rt * a.hv + gn.h, gate_n)]);
+        if (!KDA) prefetch_l1(&reinterpret_cast<const Tact*>(a.a)[GDN_G(rt * a.hv + gn.h, gate_n)]);
+      } else {
+        prefetch_l1(&a.slot_ids[GDN_G(gn.r, nreq)]);
+      }
+    }
     for (int c = 0; c < nchunks;) {
       const int nr = c + 1 < nchunks ? 2 : 1;
       const int st[2] = {(int)(n % STAGES), (int)((n + 1) % STAGES)};
