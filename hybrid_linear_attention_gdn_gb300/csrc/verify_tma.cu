@@ -124,6 +124,16 @@ __device__ __forceinline__ Seg segment_at(const VArgs& a, int64_t u, int64_t u1)
   return g;
 }
 
+// two consecutive elements (8-byte aligned for fp32, 4-byte for bf16) as fp32
+__device__ __forceinline__ float2 load_pair(const float* p) { return *reinterpret_cast<const float2*>(p); }
+__device__ __forceinline__ float2 load_pair(const __nv_bfloat16* p) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+__device__ __forceinline__ void store_pair(float* p, float2 v) { *reinterpret_cast<float2*>(p) = v; }
+__device__ __forceinline__ void store_pair(__nv_bfloat16* p, float2 v) {
+  *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(v.x, v.y);
+}
+
 // a line of global memory into L1 (no value returned, nothing to wait for)
 __device__ __forceinline__ void prefetch_l1(const void* p) { asm volatile("prefetch.L1 [%0];\n" ::"l"(p)); }
 
@@ -299,22 +309,28 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
     // [win1, win2, x_t].  q/k channels are written by the segment holding row
     // 0 of the first V head of the QK group, v channels by their own segment.
     const bool qk_writer = (h % a.G) == 0 && g.s0 == 0;
-    for (int i0 = tid; i0 < nch; i0 += kCons) {
-      const int i = GDN_S(i0, kMaxCh);
-      const float4 w = reinterpret_cast<const float4*>(Bd.w)[i];  // kW = 4 weights of channel i
-      float w0 = to_f32(Bd.hist[0][i]), w1 = to_f32(Bd.hist[1][i]), w2 = to_f32(Bd.hist[2][i]);
+    // a channel pair (2 i, 2 i + 1) per thread: pair loads and stores (every
+    // part's channel count is even, so a pair never straddles two parts).
+    for (int i0 = 2 * tid; i0 < nch; i0 += 2 * kCons) {
+      const int i = GDN_S(i0, kMaxCh - 1);
+      const float4 wa = reinterpret_cast<const float4*>(Bd.w)[i];  // kW = 4 weights of channel i
+      const float4 wb = reinterpret_cast<const float4*>(Bd.w)[i + 1];
+      float2 w0 = load_pair(&Bd.hist[0][i]), w1 = load_pair(&Bd.hist[1][i]), w2 = load_pair(&Bd.hist[2][i]);
       const size_t c = i < kDK ? (size_t)hq * kDK + i
                      : i < 2 * kDK ? (size_t)a.hk * kDK + (size_t)hq * kDK + (i - kDK)
                                    : 2 * (size_t)a.hk * kDK + (size_t)h * a.dv + (size_t)row0 + (i - 2 * kDK);
       const bool writes = i >= 2 * kDK || qk_writer;
       for (int t0 = 0; t0 < T; ++t0) {
         const int t = GDN_S(t0, MT);
-        const float xv = to_f32(Bd.x[t][i]);
-        float acc = w.x * w0;
-        acc = fmaf(w.y, w1, acc);
-        acc = fmaf(w.z, w2, acc);
-        acc = fmaf(w.w, xv, acc);
-        S.sy[t][i] = silu_fast_f(acc);
+        const float2 xv = load_pair(&Bd.x[t][i]);
+        float ax = wa.x * w0.x, ay = wb.x * w0.y;
+        ax = fmaf(wa.y, w1.x, ax);
+        ay = fmaf(wb.y, w1.y, ay);
+        ax = fmaf(wa.z, w2.x, ax);
+        ay = fmaf(wb.z, w2.y, ay);
+        ax = fmaf(wa.w, xv.x, ax);
+        ay = fmaf(wb.w, xv.y, ay);
+        *reinterpret_cast<float2*>(&S.sy[t][i]) = make_float2(silu_fast_f(ax), silu_fast_f(ay));
         w0 = w1;
         w1 = w2;
         w2 = xv;
@@ -322,9 +338,9 @@ __global__ void __launch_bounds__(kThr, MINB) verify_tma_kernel(const VArgs a) {
         if (writes && slot_class(sid, a.spec_num_slots) == 0) {
           Tconv* const sc = reinterpret_cast<Tconv*>(a.spec_conv);
           const size_t c0 = (size_t)sid * (kW - 1) * a.C + c;
-          sc[GDN_G(c0, spec_conv_n)] = from_f32<Tconv>(w0);
-          sc[GDN_G(c0 + a.C, spec_conv_n)] = from_f32<Tconv>(w1);
-          sc[GDN_G(c0 + 2 * (size_t)a.C, spec_conv_n)] = from_f32<Tconv>(w2);
+          store_pair(&sc[GDN_G(c0, spec_conv_n - 1)], w0);
+          store_pair(&sc[GDN_G(c0 + a.C, spec_conv_n - 1)], w1);
+          store_pair(&sc[GDN_G(c0 + 2 * (size_t)a.C, spec_conv_n - 1)], w2);
         }
       }
     }
