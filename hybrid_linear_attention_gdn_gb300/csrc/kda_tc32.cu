@@ -567,6 +567,34 @@ __device__ __forceinline__ void kda_chain(const KdaTcArgs& a, const CUtensorMap&
     else
       diag_block<0>(S, warp >> 1);
 
+    // ---- A' and M below the diagonal blocks: levels 3 and 2 (rows: ax, columns:
+    //      bx; N = 64) and level 1 (ay, by; N = 32) on the tensor core, issued
+    //      by two threads (one product each: a thread issuing products waits
+    //      for the tensor core to take each one) once the transform has
+    //      written their operands -------------------------------------------
+    auto issue_offdiag = [&]() {
+      if (tid == 0) {
+        umma::fence_after();
+        constexpr uint32_t ID_X = umma::idesc_f16(128, 64, false, false);
+        const uint64_t dax = umma::desc(smem_addr(S.ru.ops.ax), 16, 1024);
+        const uint64_t dbx = umma::desc(smem_addr(S.ru.ops.bx), 16, 1024);
+#pragma unroll
+        for (int s = 0; s < 8; ++s)  // K = 16 channels a step, 64-channel blocks
+          umma::mma_bf16(tmem + TM_DX, umma::adv(dax, (s >> 2) * 16384 + (s & 3) * 32),
+                         umma::adv(dbx, (s >> 2) * 8192 + (s & 3) * 32), ID_X, s > 0);
+        umma::commit(&S.od_bar);
+      } else if (tid == 32) {
+        umma::fence_after();
+        constexpr uint32_t ID_Y = umma::idesc_f16(128, 32, false, false);
+        const uint64_t day = umma::desc(smem_addr(S.ru.ops.ay), 16, 1024);
+        const uint64_t dby = umma::desc(smem_addr(S.rt.by), 16, 1024);
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+          umma::mma_bf16(tmem + TM_DY, umma::adv(day, (s >> 2) * 8192 + (s & 3) * 32),
+                         umma::adv(dby, (s >> 2) * 4096 + (s & 3) * 32), ID_Y, s > 0);
+        umma::commit(&S.od_bar);
+      }
+    };
     // ---- transform (thread: channels 2 gp, 2 gp + 1 of the 8-token block gb) --
     {
       const auto al = GDN_SV(&S.rt.g.al[0][0], kC * kYS);
@@ -647,18 +675,18 @@ __device__ __forceinline__ void kda_chain(const KdaTcArgs& a, const CUtensorMap&
       // fp32 (tf32) operand [K~;Q~]: 32-channel blocks 16 KB apart, 4 channels a chunk
       const uint32_t ch32 = (uint32_t)(((2 * gp) & 31) >> 2) << 4;
       const uint32_t okq = (uint32_t)(gp >> 4) * 16384u + (uint32_t)gb * 1024u + (uint32_t)((2 * gp) & 3) * 4u;
+      // the off-diagonal products' operands first; the [K~;Q~] and K-^T
+      // values wait in registers for the products' issue
       float km0[8], km1[8];
+      float2 kqk[8], kqq[8];
 #pragma unroll
       for (int t = 0; t < 8; ++t) {
         const float2 kh = make_float2(k8[t].x * rk8v[t], k8[t].y * rk8v[t]);
         const float2 qh = make_float2(q8[t].x * rq8v[t], q8[t].y * rq8v[t]);
         const float2 kl = make_float2(kh.x * fl[t].x, kh.y * fl[t].y), ql = make_float2(qh.x * fl[t].x, qh.y * fl[t].y);
         const float2 kr = make_float2(kh.x * fr[t].x, kh.y * fr[t].y);
-        const uint32_t rt32 = okq + (uint32_t)t * 128u + (ch32 ^ ((uint32_t)t << 4));
-        tile_at<float2>(S.kq, sizeof(S.kq), rt32) =
-            make_float2(umma::tf32_round(kl.x * Eb.x), umma::tf32_round(kl.y * Eb.y));
-        tile_at<float2>(S.kq, sizeof(S.kq), rt32 + 8u * 1024u) =  // Q~ rows: 64 rows on
-            make_float2(umma::tf32_round(ql.x * Eb.x), umma::tf32_round(ql.y * Eb.y));
+        kqk[t] = make_float2(umma::tf32_round(kl.x * Eb.x), umma::tf32_round(kl.y * Eb.y));
+        kqq[t] = make_float2(umma::tf32_round(ql.x * Eb.x), umma::tf32_round(ql.y * Eb.y));
         km0[t] = umma::tf32_round(kr.x * Ee.x);
         km1[t] = umma::tf32_round(kr.y * Ee.y);
         if (gb & 1) {  // level-3 rows (blocks 1, 3, 5, 7)
@@ -680,6 +708,18 @@ __device__ __forceinline__ void kda_chain(const KdaTcArgs& a, const CUtensorMap&
           put_h(S.rt.by, sizeof(S.rt.by), oby, t, kr.x * EY.x, kr.y * EY.y);
         }
       }
+      umma::fence_proxy_async();
+      umma::fence_before();
+      __syncthreads();
+      od_pending = true;
+      issue_offdiag();
+      // meanwhile [K~;Q~] and K-^T (read by later products only)
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const uint32_t rt32 = okq + (uint32_t)t * 128u + (ch32 ^ ((uint32_t)t << 4));
+        tile_at<float2>(S.kq, sizeof(S.kq), rt32) = kqk[t];
+        tile_at<float2>(S.kq, sizeof(S.kq), rt32 + 8u * 1024u) = kqq[t];  // Q~ rows: 64 rows on
+      }
 #pragma unroll
       for (int h4 = 0; h4 < 2; ++h4) {
         // rows 2 gp and 2 gp + 1, in an order that puts the 8 lanes of each
@@ -690,35 +730,7 @@ __device__ __forceinline__ void kda_chain(const KdaTcArgs& a, const CUtensorMap&
         tile_at<float4>(S.kt, sizeof(S.kt), f32_off(2 * gp + sw, 8 * gb + 4 * h4, 128 * 128)) = sw ? v1 : v0;
         tile_at<float4>(S.kt, sizeof(S.kt), f32_off(2 * gp + !sw, 8 * gb + 4 * h4, 128 * 128)) = sw ? v0 : v1;
       }
-    }
-    umma::fence_proxy_async();
-    umma::fence_before();
-    __syncthreads();
-    // ---- A' and M below the diagonal blocks: levels 3 and 2 (rows: ax, columns:
-    //      bx; N = 64) and level 1 (ay, by; N = 32) on the tensor core -------
-    od_pending = true;
-    // (issued by two threads, one product each: a thread issuing products
-    // waits for the tensor core to take each one)
-    if (tid == 0) {
-      umma::fence_after();
-      constexpr uint32_t ID_X = umma::idesc_f16(128, 64, false, false);
-      const uint64_t dax = umma::desc(smem_addr(S.ru.ops.ax), 16, 1024);
-      const uint64_t dbx = umma::desc(smem_addr(S.ru.ops.bx), 16, 1024);
-#pragma unroll
-      for (int s = 0; s < 8; ++s)  // K = 16 channels a step, 64-channel blocks
-        umma::mma_bf16(tmem + TM_DX, umma::adv(dax, (s >> 2) * 16384 + (s & 3) * 32),
-                       umma::adv(dbx, (s >> 2) * 8192 + (s & 3) * 32), ID_X, s > 0);
-      umma::commit(&S.od_bar);
-    } else if (tid == 32) {
-      umma::fence_after();
-      constexpr uint32_t ID_Y = umma::idesc_f16(128, 32, false, false);
-      const uint64_t day = umma::desc(smem_addr(S.ru.ops.ay), 16, 1024);
-      const uint64_t dby = umma::desc(smem_addr(S.rt.by), 16, 1024);
-#pragma unroll
-      for (int s = 0; s < 8; ++s)
-        umma::mma_bf16(tmem + TM_DY, umma::adv(day, (s >> 2) * 8192 + (s & 3) * 32),
-                       umma::adv(dby, (s >> 2) * 4096 + (s & 3) * 32), ID_Y, s > 0);
-      umma::commit(&S.od_bar);
+      umma::fence_proxy_async();  // (seen by the products that read them after later barriers)
     }
     // meanwhile (neither is an operand of the products): M's diagonal blocks
     // from dgM, zeros right of them, and T2 cleared
