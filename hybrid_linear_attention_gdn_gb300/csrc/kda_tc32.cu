@@ -45,9 +45,11 @@
 // order; the fp32 state S lives in TMEM for the whole sequence.  Per chunk:
 //   gates      thread (channel pair, 8-token block): log alpha, alpha, the
 //              8-block totals, from the chunk's gate logits (one TMA box,
-//              loaded under the previous chunk's solve)
+//              loaded under the previous chunk's assembly and solve, with
+//              its own barrier: the gates do not wait for the raw rows)
 //   features   the 67 raw rows of the head's q, k and v channels arrive by
-//              three TMA boxes; conv1d + SiLU down the chunk; q and k rows
+//              three TMA boxes (issued after the previous chunk's solve,
+//              landing under the gates); conv1d + SiLU down the chunk; q and k rows
 //              (fp32) into shared memory, V^T (tf32) into TMEM, and each
 //              token's sums of squares over the warp's channels
 //   norms      rk_t = 1/|y_k,t|, rq_t = dk^-1/2 / |y_q,t| (with the eps) from
@@ -161,7 +163,8 @@ struct __align__(1024) KSmem {
   float dgA[kC][8];   // diagonal blocks: beta_t A'[t][j] (j < t, local j), and
   float dgM[kC][8];   //   M[t][j] (j <= t)
   float ones[kC];
-  uint64_t ld_bar, mma_bar, eo_bar, od_bar;  // od_bar: the two off-diagonal products (two issuers)
+  uint64_t ld_bar, ga_bar;  // the raw rows; the gate logits (they land first: the gates start on them)
+  uint64_t mma_bar, eo_bar, od_bar;  // od_bar: the two off-diagonal products (two issuers)
   uint32_t tmem_base;
 };
 
@@ -298,6 +301,7 @@ __device__ __forceinline__ void kda_chain(const KdaTcArgs& a, const CUtensorMap&
 
   if (tid == 0) {
     mbar_init(&S.ld_bar, 1);
+    mbar_init(&S.ga_bar, 1);
     mbar_init(&S.mma_bar, 1);
     mbar_init(&S.od_bar, 2);
     mbar_init(&S.eo_bar, 1);
@@ -358,24 +362,27 @@ __device__ __forceinline__ void kda_chain(const KdaTcArgs& a, const CUtensorMap&
     const int32_t id = ckpt_ids[(size_t)n * a.max_ckpt + idx];
     return slot_class(id, a.ck_num_slots) == 0 ? id : -1;
   };
-  constexpr uint32_t kLoadBytes = 3u * kRawRows * kD * 2u + (uint32_t)kC * kD * 2u;
-  // warp 0: chunk c's gate logits (lane 3, with the phase's byte count) and
-  // raw rows (lanes 0..2: the q, k and v boxes at once) into region U.  The
-  // gate-logit box lies past the solve's scratch, so it goes first, as soon
-  // as the previous chunk's off-diagonal products have read their operands.
+  constexpr uint32_t kRawBytes = 3u * kRawRows * kD * 2u, kGaBytes = (uint32_t)kC * kD * 2u;
+  // warp 0: chunk c's gate logits (lane 3, on ga_bar) and raw rows (lanes
+  // 0..2: the q, k and v boxes at once, on ld_bar) into region U, each call
+  // with its barrier's byte count.  The gate-logit box lies past the solve's
+  // scratch, so it goes first, as soon as the previous chunk's off-diagonal
+  // products have read their operands.
   auto issue_ga = [&](int c) {
     const int64_t P = (p0 / kC + c) * kC;
     const int32_t row = (int32_t)(t0 + (P - p0));  // packed row of the chunk's first token (may be < 0)
     if (lane == 3) {
-      mbar_arrive_expect_tx(&S.ld_bar, kLoadBytes);
+      mbar_arrive_expect_tx(&S.ga_bar, kGaBytes);
       // 128 channels of V head h, 64 rows (rows outside: zeros)
       if (GDN_SPAN_G(h * kD, kD, (long long)a.hv * kD) && GDN_SBYTES(&S.ru.in.ga[0][0], kC * kD * 2, S))
-        tma_load_2d(&S.ru.in.ga[0][0], &amap, h * kD, row, &S.ld_bar);
+        tma_load_2d(&S.ru.in.ga[0][0], &amap, h * kD, row, &S.ga_bar);
     }
   };
   auto issue_raw = [&](int c) {
     const int64_t P = (p0 / kC + c) * kC;
     const int32_t row0 = (int32_t)(t0 + (P - 3 - p0));  // packed row of raw row 0 (may be < 0)
+    if (lane == 0) mbar_arrive_expect_tx(&S.ld_bar, kRawBytes);
+    __syncwarp();  // the phase's byte count before any of its copies
     if (lane < 3) {  // a box of 128 channels of the q, k or v part, 67 rows (rows outside: zeros)
       const int x = lane == 0 ? hq * kD : lane == 1 ? (a.hk + hq) * kD : 2 * a.hk * kD + h * kD;
       if (GDN_SPAN_G(x, kD, a.C) && GDN_SBYTES(&S.ru.in.raw[lane][0][0], kRawRows * kD * 2, S))
@@ -384,12 +391,18 @@ __device__ __forceinline__ void kda_chain(const KdaTcArgs& a, const CUtensorMap&
   };
   static_assert(offsetof(decltype(KSmem::ru), in.ga) >= offsetof(decltype(KSmem::ru), sv.L0) + sizeof(KSmem::ru.sv.L0),
                 "the gate-logit box lies past the solve's scratch");
-  // beta logit of chunk c's token tid (threads 0..63), loaded one chunk ahead
-  auto load_beta = [&](int c) -> float {
+  // raw bits of the beta logit of chunk c's token tid (threads 0..63, 0 for
+  // the other threads and outside the sequence).  An asm load, so that it is
+  // issued where it stands (at the chunk start) and its latency runs under
+  // the gates, not where its value is first used.
+  auto load_beta = [&](int c) -> uint16_t {
     const int64_t pos = (p0 / kC + c) * kC + tid;
-    if (tid < kC && c < nch && pos >= p0 && pos < p1)
-      return __bfloat162float(gate_b[(size_t)(t0 + pos - p0) * a.hv + h]);
-    return 0.f;
+    uint16_t v = 0;
+    if (tid < kC && pos >= p0 && pos < p1) {
+      const __nv_bfloat16* src = gate_b.at((long long)(t0 + pos - p0) * a.hv + h);
+      asm volatile("ld.global.nc.b16 %0, [%1];\n" : "=h"(v) : "l"(src));
+    }
+    return v;
   };
 
   // initial state rows into TMEM
@@ -404,14 +417,12 @@ __device__ __forceinline__ void kda_chain(const KdaTcArgs& a, const CUtensorMap&
     }
     umma::tmem_st32(tlane + TM_S + 32 * qq, v);
   }
-  int ld_issued = 0, ld_done = 0;
+  int ld_issued = 0, ld_done = 0, ga_issued = 0, ga_done = 0;
   if (warp == 0) {
     issue_ga(0);
-    __syncwarp();  // the phase's byte count before any of its copies
     issue_raw(0);
   }
-  ld_issued = 1;
-  float bl = load_beta(0);
+  ld_issued = ga_issued = 1;
 
   bool bad = false;
   uint32_t mph = 0;
@@ -433,38 +444,14 @@ __device__ __forceinline__ void kda_chain(const KdaTcArgs& a, const CUtensorMap&
     const bool full = P >= p0 && P + kC <= p1;
     const int tlo = (int)(p0 > P ? (p0 - P < kC ? p0 - P : kC) : 0);
     const int thi = (int)(p1 > P ? (p1 - P < kC ? p1 - P : kC) : 0);
+    const uint16_t bl = load_beta(c);
     // the previous chunk's tensor stores have read kq (checkpoint staging)
     // and t2 (output staging)
     if (tid == 0) bulk_wait_read();
-    if (tid < kC) S.beta[tid] = (unsigned)(tid - tlo) < (unsigned)(thi - tlo) ? sigmoid_f(bl) : 0.f;
-    bl = load_beta(c + 1);
-    if (!wait_all(&S.ld_bar, c & 1)) break;
-    ld_done = c + 1;
-    // the next chunk's boxes into L2 now; their copies into shared memory
-    // start after the solve (where they lie wholly inside the tensors)
-    if (tid == 0 && c + 1 < nch) {
-      const int32_t row1 = (int32_t)(t0 + (P + kC - 3 - p0));
-      if (row1 >= 0 && (int64_t)row1 + kRawRows <= a.total) {
-#pragma unroll
-        for (int q = 0; q < 3; ++q) tma_prefetch_2d(&qmap, part_x[q], row1);
-        tma_prefetch_2d(&amap, h * kD, row1 + 3);
-      }
-    }
-    // the up to 3 rows just before the sequence start come from the conv history
-    if (P - 3 < p0) {
-      const int64_t lo = (P - 3 > p0 - 3) ? P - 3 : p0 - 3;
-      const int64_t hi = (P + kC < p0) ? P + kC : p0;
-      const auto hist = GDN_GV(a.conv, (long long)a.num_slots * 3 * a.C) + (size_t)slot * 3 * a.C;
-      for (int64_t pos = lo; pos < hi; ++pos) {
-        const int r = GDN_S((int)(pos - (P - 3)), kRawRows);
-        for (int e = tid; e < 3 * kD; e += kThreads) {
-          const int q = e / kD, ch = e % kD;
-          S.ru.in.raw[q][r][ch] = hist[(size_t)(3 - (p0 - pos)) * a.C + part_x[q] + ch];
-        }
-      }
-      __syncthreads();
-    }
-
+    // the gate logits (issued under the previous chunk's assembly) have
+    // landed; the raw rows (issued after its solve) are awaited after the gates
+    if (!wait_all(&S.ga_bar, c & 1)) break;
+    ga_done = c + 1;
     // ---- gates: log alpha, alpha, 8-block totals (thread: channels 2 gp, 2 gp + 1
     //      of the 8-token block gb) ---------------------------------------------
     {
@@ -486,6 +473,30 @@ __device__ __forceinline__ void kda_chain(const KdaTcArgs& a, const CUtensorMap&
       }
       vec_at<float2>(&S.G8[GDN_S(gb, 8)][0], 2 * gp) = G;
       vec_at<float2>(&S.g8f[GDN_S(gb, 8)][0], 2 * gp) = f;
+    }
+    if (tid < kC)
+      S.beta[tid] =
+          (unsigned)(tid - tlo) < (unsigned)(thi - tlo) ? sigmoid_f(__bfloat162float(__ushort_as_bfloat16(bl))) : 0.f;
+
+    // each thread's own wait (the copies' writes are visible to it after
+    // it); an expired wait is acted on at the barrier after the features
+    if (mbar_wait(&S.ld_bar, c & 1))
+      ld_done = c + 1;
+    else
+      bad = true;
+    // the up to 3 rows just before the sequence start come from the conv history
+    if (P - 3 < p0) {
+      const int64_t lo = (P - 3 > p0 - 3) ? P - 3 : p0 - 3;
+      const int64_t hi = (P + kC < p0) ? P + kC : p0;
+      const auto hist = GDN_GV(a.conv, (long long)a.num_slots * 3 * a.C) + (size_t)slot * 3 * a.C;
+      for (int64_t pos = lo; pos < hi; ++pos) {
+        const int r = GDN_S((int)(pos - (P - 3)), kRawRows);
+        for (int e = tid; e < 3 * kD; e += kThreads) {
+          const int q = e / kD, ch = e % kD;
+          S.ru.in.raw[q][r][ch] = hist[(size_t)(3 - (p0 - pos)) * a.C + part_x[q] + ch];
+        }
+      }
+      __syncthreads();
     }
 
     // ---- features: conv1d + SiLU, down the chunk ---------------------------
@@ -546,7 +557,7 @@ __device__ __forceinline__ void kda_chain(const KdaTcArgs& a, const CUtensorMap&
       }
     }
     // the raw rows and gate logits are read: the feature rows take region U
-    __syncthreads();
+    if (__syncthreads_or(bad)) break;
     {
       const int tk = 16 * qq;
       const auto yd = GDN_SV(isq ? &S.ru.y.yq[0][0] : &S.ru.y.yk[0][0], kC * kYS);
@@ -751,10 +762,19 @@ __device__ __forceinline__ void kda_chain(const KdaTcArgs& a, const CUtensorMap&
     if (!wait_all(&S.od_bar, c & 1)) break;
     od_pending = false;
     umma::fence_after();
-    // the next chunk's gate logits (their part of region U is free from here)
+    // the next chunk's gate logits (their part of region U is free from
+    // here), and its raw boxes into L2 (their copies into shared memory start
+    // after the solve, where they lie wholly inside the tensor)
     if (c + 1 < nch) {
-      if (warp == 0) issue_ga(c + 1);
-      ld_issued = c + 2;
+      if (warp == 0) {
+        issue_ga(c + 1);
+        const int32_t row1 = (int32_t)(t0 + (P + kC - 3 - p0));
+        if (lane == 4 && row1 >= 0 && (int64_t)row1 + kRawRows <= a.total) {
+#pragma unroll
+          for (int q = 0; q < 3; ++q) tma_prefetch_2d(&qmap, part_x[q], row1);
+        }
+      }
+      ga_issued = c + 2;
     }
     // A (fp32, for the solve: beta_t A'), M below the diagonal blocks (tf32
     // operand), X and T1 (cleared: the solve writes their lower triangles)
@@ -842,8 +862,11 @@ __device__ __forceinline__ void kda_chain(const KdaTcArgs& a, const CUtensorMap&
     solve_T(S.ru.sv.A, S.ru.sv.X, S.ru.sv.Y, S.ru.sv.L0, TOut{S.rt.t.tm, S.rt.t.t2, S.beta, S.ones, S.ones});
     umma::fence_proxy_async();
     __syncthreads();
-    // the next chunk's raw rows and gate logits (region U is dead)
-    if (c + 1 < nch && warp == 0) issue_raw(c + 1);
+    // the next chunk's raw rows (region U is dead)
+    if (c + 1 < nch) {
+      if (warp == 0) issue_raw(c + 1);
+      ld_issued = c + 2;
+    }
     if (!wait_all(&S.eo_bar, c & 1)) break;
     eo_pending = false;
     umma::fence_after();
@@ -942,6 +965,7 @@ __device__ __forceinline__ void kda_chain(const KdaTcArgs& a, const CUtensorMap&
       if (eo_pending) mbar_wait(&S.eo_bar, c & 1);
       if (od_pending) mbar_wait(&S.od_bar, c & 1);
       for (int k = ld_done; k < ld_issued; ++k) mbar_wait(&S.ld_bar, k & 1);
+      for (int k = ga_done; k < ga_issued; ++k) mbar_wait(&S.ga_bar, k & 1);
     }
   } else {
     // the final state
@@ -956,6 +980,7 @@ __device__ __forceinline__ void kda_chain(const KdaTcArgs& a, const CUtensorMap&
   __syncthreads();
   if (tid == 0) {
     mbar_inval(&S.ld_bar);
+    mbar_inval(&S.ga_bar);
     mbar_inval(&S.mma_bar);
     mbar_inval(&S.od_bar);
     mbar_inval(&S.eo_bar);
