@@ -49,16 +49,17 @@
 //              its own barrier: the gates do not wait for the raw rows)
 //   features   the 67 raw rows of the head's q, k and v channels arrive by
 //              three TMA boxes (issued after the previous chunk's solve,
-//              landing under the gates); conv1d + SiLU down the chunk; q and k rows
-//              (fp32) into shared memory, V^T (tf32) into TMEM, and each
-//              token's sums of squares over the warp's channels
+//              landing under the gates); conv1d + SiLU down the chunk; q and
+//              k rows (fp32) into shared memory, V^T (tf32) into TMEM, and
+//              each token's sums of squares over the warp's channels
 //   norms      rk_t = 1/|y_k,t|, rq_t = dk^-1/2 / |y_q,t| (with the eps) from
 //              those sums
 //   diagonal   the 8 x 8 diagonal blocks of A' and M
 //   transform  thread (channel pair, 8-token block): fl8, fr8 by running
-//              products; the tf32 operand tiles [K~;Q~] and K-^T, the fp16
-//              operands of the off-diagonal products
-//   off-diag   A' and M below the diagonal blocks (two tcgen05 products)
+//              products; the fp16 operands of the off-diagonal products
+//   off-diag   A' and M below the diagonal blocks (two tcgen05 products),
+//              issued as soon as their operands are written; the tf32
+//              operand tiles [K~;Q~] and K-^T are written while they run
 //   S [K~;Q~]^T  (tcgen05, A operand the state in TMEM) issued before the
 //              solve, runs under it
 //   solve      X = (I + diag(beta) A')^-1 as in the GDN chain; T1 = X
